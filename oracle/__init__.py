@@ -1,0 +1,196 @@
+"""Plain CPU oracle for the Ulysses 4D sequence/head relayout and its fused QK variant.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The CUDA library never calls it and has no CPU fallback.
+
+The arithmetic lives in ``ulysses_oracle.c`` (six nested loops for the relayout, double precision
+for RMSNorm + RoPE); this module only compiles it with gcc and marshals numpy arrays through
+ctypes. What is computed, and the passages it follows:
+
+* fast-ulysses 0.1.0 (PyPI page), opening paragraph and "Quick start": mode 0 maps
+  ``(b, s_local, n_global, d) -> (b, s_global, n_local, d)``.
+* fast-ulysses 0.2.1 (README), "Quick start": mode 1 returns to x's shape.
+* fast-ulysses 0.1.0, "What it does": uneven per-rank ``seq_splits`` / ``head_splits``.
+* fast-ulysses 0.1.0, "Fusion examples": QK RMSNorm + RoPE inside the scatter.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Sequence
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(HERE, "ulysses_oracle.c")
+LIBRARY = os.path.join(HERE, "liboracle.so")
+
+_i64 = ctypes.c_int64
+_p = ctypes.c_void_p
+_pi64 = ctypes.POINTER(ctypes.c_int64)
+
+
+def build(out: str = LIBRARY, source: str = SOURCE) -> str:
+    """Compile the oracle with gcc into a shared library and return its path."""
+    cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-shared", "-fPIC", "-o", out, source, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _needs_build(lib: str, source: str) -> bool:
+    return not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(source)
+
+
+def _i64_array(values: Sequence[int]):
+    return (ctypes.c_int64 * len(values))(*[int(v) for v in values])
+
+
+def _ptr_array(arrays):
+    return (ctypes.c_void_p * len(arrays))(*[a.ctypes.data for a in arrays])
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library (the real one, or a test's planted variant)."""
+
+    def __init__(self, lib_path: str | None = None):
+        if lib_path is None:
+            lib_path = LIBRARY
+            if _needs_build(lib_path, SOURCE):
+                build(lib_path, SOURCE)
+        self.path = lib_path
+        lib = ctypes.CDLL(lib_path)
+        lib.orc_a2a_4d.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, _i64, ctypes.c_int, _p, _p]
+        lib.orc_a2a_4d.restype = ctypes.c_int
+        lib.orc_a2a_4d_source.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, ctypes.c_int,
+                                           ctypes.c_int, _i64, ctypes.POINTER(ctypes.c_int), _pi64]
+        lib.orc_a2a_4d_source.restype = ctypes.c_int
+        fused_args = [ctypes.c_int, _i64, _pi64, _pi64, _i64, _p, _p, ctypes.c_double,
+                      ctypes.c_double, _p]
+        for name in ("orc_qk_fused_A", "orc_qk_fused_B"):
+            getattr(lib, name).argtypes = fused_args
+            getattr(lib, name).restype = ctypes.c_int
+        lib.orc_qk_fused_row.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, ctypes.c_int, _i64,
+                                         _i64, _i64, _p, _p, ctypes.c_double, ctypes.c_double, _p]
+        lib.orc_qk_fused_row.restype = ctypes.c_int
+        lib.orc_rmsnorm.argtypes = [_p, _i64, _p, ctypes.c_double, _p]
+        lib.orc_rmsnorm.restype = None
+        lib.orc_rope.argtypes = [_p, _i64, ctypes.c_double, ctypes.c_double]
+        lib.orc_rope.restype = None
+        lib.orc_bf16_to_double_array.argtypes = [_p, _i64, _p]
+        lib.orc_bf16_to_double_array.restype = None
+        lib.orc_double_to_bf16_array.argtypes = [_p, _i64, _p]
+        lib.orc_double_to_bf16_array.restype = None
+        self.lib = lib
+
+    # ---- relayout -------------------------------------------------------------------------
+    @staticmethod
+    def out_shapes(b, seq_splits, head_splits, d, mode):
+        """Shapes the definition gives each rank's output (mode 0: (b, S, n_r, d))."""
+        S, N = int(sum(seq_splits)), int(sum(head_splits))
+        if mode == 0:
+            return [(b, S, int(n), d) for n in head_splits]
+        return [(b, int(s), N, d) for s in seq_splits]
+
+    def a2a_4d(self, xs: Sequence[np.ndarray], seq_splits, head_splits, mode: int):
+        """Relayout W host arrays (any dtype; moved as raw bytes). Returns W new arrays."""
+        W = len(xs)
+        b, d = xs[0].shape[0], xs[0].shape[3]
+        e = xs[0].dtype.itemsize
+        xs = [np.ascontiguousarray(x) for x in xs]
+        outs = [np.empty(s, dtype=xs[0].dtype) for s in self.out_shapes(b, seq_splits, head_splits, d, mode)]
+        rc = self.lib.orc_a2a_4d(W, b, _i64_array(seq_splits), _i64_array(head_splits), d, e, mode,
+                                 ctypes.cast(_ptr_array(xs), _p), ctypes.cast(_ptr_array(outs), _p))
+        if rc != 0:
+            raise ValueError("oracle rejected the geometry")
+        return outs
+
+    def a2a_4d_raw(self, W, b, seq_splits, head_splits, d, e, mode, in_ptrs, out_ptrs):
+        """Same as ``a2a_4d`` on raw host addresses (the caller sizes the buffers)."""
+        rc = self.lib.orc_a2a_4d(W, b, _i64_array(seq_splits), _i64_array(head_splits), d, e, mode,
+                                 ctypes.cast((ctypes.c_void_p * W)(*in_ptrs), _p),
+                                 ctypes.cast((ctypes.c_void_p * W)(*out_ptrs), _p))
+        if rc != 0:
+            raise ValueError("oracle rejected the geometry")
+
+    def a2a_4d_source(self, W, b, seq_splits, head_splits, d, mode, out_rank, out_elem):
+        """(source rank, flat source element index) of one output element."""
+        src_rank = ctypes.c_int(-1)
+        src_elem = ctypes.c_int64(-1)
+        rc = self.lib.orc_a2a_4d_source(W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
+                                        mode, out_rank, int(out_elem), ctypes.byref(src_rank),
+                                        ctypes.byref(src_elem))
+        if rc != 0:
+            raise ValueError("oracle rejected the query")
+        return src_rank.value, src_elem.value
+
+    # ---- fused QK RMSNorm + RoPE ----------------------------------------------------------
+    def _fused(self, fn, xs_bf16: Sequence[np.ndarray], seq_splits, head_splits, w, eps, theta):
+        W = len(xs_bf16)
+        b, d = xs_bf16[0].shape[0], xs_bf16[0].shape[3]
+        xs = [np.ascontiguousarray(x).view(np.uint16) for x in xs_bf16]
+        w64 = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
+        outs = [np.empty(s, dtype=np.float64) for s in self.out_shapes(b, seq_splits, head_splits, d, 0)]
+        rc = fn(W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
+                ctypes.cast(_ptr_array(xs), _p), w64.ctypes.data, float(eps), float(theta),
+                ctypes.cast(_ptr_array(outs), _p))
+        if rc != 0:
+            raise ValueError("oracle rejected the geometry")
+        return outs
+
+    def qk_fused_A(self, xs_bf16, seq_splits, head_splits, w, eps, theta):
+        """Transform at the source row, then place (unrounded double outputs)."""
+        return self._fused(self.lib.orc_qk_fused_A, xs_bf16, seq_splits, head_splits, w, eps, theta)
+
+    def qk_fused_B(self, xs_bf16, seq_splits, head_splits, w, eps, theta):
+        """Place the bf16 bytes, then transform at the destination row."""
+        return self._fused(self.lib.orc_qk_fused_B, xs_bf16, seq_splits, head_splits, w, eps, theta)
+
+    def qk_fused_row(self, xs_bf16, seq_splits, head_splits, w, eps, theta, r, bb, s, h):
+        """One output row (rank r, batch bb, global position s, local head h) in double."""
+        W = len(xs_bf16)
+        b, d = xs_bf16[0].shape[0], xs_bf16[0].shape[3]
+        xs = [np.ascontiguousarray(x).view(np.uint16) for x in xs_bf16]
+        w64 = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
+        y = np.empty(d, dtype=np.float64)
+        rc = self.lib.orc_qk_fused_row(W, b, _i64_array(seq_splits), _i64_array(head_splits), d, r,
+                                       bb, s, h, ctypes.cast(_ptr_array(xs), _p), w64.ctypes.data,
+                                       float(eps), float(theta), y.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle rejected the query")
+        return y
+
+    def rmsnorm(self, x, w, eps):
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        w = np.ascontiguousarray(w, dtype=np.float64)
+        y = np.empty_like(x)
+        self.lib.orc_rmsnorm(x.ctypes.data, x.size, w.ctypes.data, float(eps), y.ctypes.data)
+        return y
+
+    def rope(self, y, p, theta):
+        y = np.array(y, dtype=np.float64, copy=True)
+        self.lib.orc_rope(y.ctypes.data, y.size, float(p), float(theta))
+        return y
+
+    def bf16_to_double(self, h):
+        h = np.ascontiguousarray(h, dtype=np.uint16)
+        out = np.empty(h.shape, dtype=np.float64)
+        self.lib.orc_bf16_to_double_array(h.ctypes.data, h.size, out.ctypes.data)
+        return out
+
+    def double_to_bf16(self, x):
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        out = np.empty(x.shape, dtype=np.uint16)
+        self.lib.orc_double_to_bf16_array(x.ctypes.data, x.size, out.ctypes.data)
+        return out
+
+
+_default: Oracle | None = None
+
+
+def get() -> Oracle:
+    """The oracle built from ``ulysses_oracle.c`` (compiled on first use if needed)."""
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default

@@ -1,0 +1,326 @@
+/*
+ * ulysses_oracle.c -- plain CPU oracle for the Ulysses 4D sequence/head relayout.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the CPU baseline leg of the
+ * benchmark may load this file's shared library. The product path never calls it and has no CPU
+ * fallback. It shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes, and where that is stated:
+ *
+ *   fast-ulysses 0.1.0 (PyPI page), opening paragraph and "Quick start":
+ *     one all-to-all trades the sequence shard for a head shard, a second trades it back;
+ *     mode 0 maps (b, s_local, n_global, d) -> (b, s_global, n_local, d).
+ *   fast-ulysses 0.2.1 (README), "Quick start": mode 1 returns to x's shape.
+ *   fast-ulysses 0.1.0, "What it does": per-rank seq_splits / head_splits (uneven shards);
+ *     even splits are a special case of the same mapping.
+ *   fast-ulysses 0.1.0, "Fusion examples": QK RMSNorm + RoPE inside the scatter.
+ *
+ * With W ranks, s_q = seq_splits[q], n_r = head_splits[r], S = sum s_q, N = sum n_r,
+ * seq_off(q) = sum_{p<q} s_p and head_off(r) = sum_{p<r} n_p, mode 0 is
+ *
+ *     out[r][bb][seq_off(q) + i][h][j] = in[q][bb][i][head_off(r) + h][j]
+ *
+ * for every q, r, bb < b, i < s_q, h < n_r, j < d; mode 1 is the same assignment read the
+ * other way (out[q][bb][i][head_off(r)+h][j] = in[r][bb][seq_off(q)+i][h][j]). Elements are
+ * moved as raw bytes, e bytes each, so the element type never matters.
+ *
+ * The fused QK transform follows the plainest reading of "QK RMSNorm + RoPE": per head row of
+ * d values (bf16 in), RMSNorm over d with eps inside the square root and one weight vector of
+ * length d, then rotary embedding on adjacent pairs (2j, 2j+1) with angle p * theta^(-2j/d),
+ * where p is the token's global sequence index. Everything is in double; the result is left
+ * unrounded (a bf16 round-to-nearest-even helper is provided separately).
+ *
+ * All functions return 0 on success and -1 on invalid arguments.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_MAX_W 8
+
+/* Sum of the first k entries of a split vector: the offset of shard k. */
+static int64_t offset_of(const int64_t* splits, int k)
+{
+    int64_t s = 0;
+    for (int p = 0; p < k; ++p) s += splits[p];
+    return s;
+}
+
+static int check_geometry(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                          int64_t d)
+{
+    if (W < 1 || W > ORC_MAX_W || b < 1 || d < 1) return -1;
+    if (!seq_splits || !head_splits) return -1;
+    for (int q = 0; q < W; ++q)
+        if (seq_splits[q] < 0 || head_splits[q] < 0) return -1;
+    if (offset_of(seq_splits, W) < 1 || offset_of(head_splits, W) < 1) return -1;
+    return 0;
+}
+
+/*
+ * The relayout, six nested loops, one element (e bytes) per innermost step.
+ * in[k] and out[k] are the W ranks' buffers. Mode 0: in[q] is (b, s_q, N, d) and out[r] is
+ * (b, S, n_r, d). Mode 1: in[r] is (b, S, n_r, d) and out[q] is (b, s_q, N, d).
+ */
+int orc_a2a_4d(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+               int64_t d, int64_t e, int mode, const uint8_t* const* in, uint8_t* const* out)
+{
+    if (check_geometry(W, b, seq_splits, head_splits, d)) return -1;
+    if (!(e == 1 || e == 2 || e == 4) || !(mode == 0 || mode == 1)) return -1;
+    const int64_t S = offset_of(seq_splits, W);
+    const int64_t N = offset_of(head_splits, W);
+
+    for (int q = 0; q < W; ++q) {
+        const int64_t s_q = seq_splits[q];
+        const int64_t seq_off_q = offset_of(seq_splits, q);
+        for (int r = 0; r < W; ++r) {
+            const int64_t n_r = head_splits[r];
+            const int64_t head_off_r = offset_of(head_splits, r);
+            for (int64_t bb = 0; bb < b; ++bb)
+                for (int64_t i = 0; i < s_q; ++i)
+                    for (int64_t h = 0; h < n_r; ++h)
+                        for (int64_t j = 0; j < d; ++j) {
+                            /* element index inside rank q's (b, s_q, N, d) tensor */
+                            const int64_t seq_side = ((bb * s_q + i) * N + head_off_r + h) * d + j;
+                            /* element index inside rank r's (b, S, n_r, d) tensor */
+                            const int64_t head_side = ((bb * S + seq_off_q + i) * n_r + h) * d + j;
+                            if (mode == 0)
+                                memcpy(out[r] + head_side * e, in[q] + seq_side * e, (size_t)e);
+                            else
+                                memcpy(out[q] + seq_side * e, in[r] + head_side * e, (size_t)e);
+                        }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Where one output element comes from, read off the same definition: given the output rank and
+ * the flat element index inside that rank's output tensor, return the source rank and the flat
+ * element index inside that rank's input tensor. Used to check single sampled outputs of
+ * workloads too large to relayout on the host.
+ */
+int orc_a2a_4d_source(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                      int64_t d, int mode, int out_rank, int64_t out_elem, int* src_rank,
+                      int64_t* src_elem)
+{
+    if (check_geometry(W, b, seq_splits, head_splits, d)) return -1;
+    if (!(mode == 0 || mode == 1) || out_rank < 0 || out_rank >= W || out_elem < 0) return -1;
+    const int64_t S = offset_of(seq_splits, W);
+    const int64_t N = offset_of(head_splits, W);
+
+    if (mode == 0) {
+        const int r = out_rank;
+        const int64_t n_r = head_splits[r];
+        if (out_elem >= b * S * n_r * d) return -1;
+        const int64_t j = out_elem % d;
+        const int64_t h = (out_elem / d) % n_r;
+        const int64_t s = (out_elem / (d * n_r)) % S;
+        const int64_t bb = out_elem / (d * n_r * S);
+        for (int q = 0; q < W; ++q) {
+            const int64_t lo = offset_of(seq_splits, q);
+            if (s >= lo && s < lo + seq_splits[q]) {
+                const int64_t i = s - lo;
+                *src_rank = q;
+                *src_elem = ((bb * seq_splits[q] + i) * N + offset_of(head_splits, r) + h) * d + j;
+                return 0;
+            }
+        }
+        return -1;
+    } else {
+        const int q = out_rank;
+        const int64_t s_q = seq_splits[q];
+        if (out_elem >= b * s_q * N * d) return -1;
+        const int64_t j = out_elem % d;
+        const int64_t g = (out_elem / d) % N;
+        const int64_t i = (out_elem / (d * N)) % s_q;
+        const int64_t bb = out_elem / (d * N * s_q);
+        for (int r = 0; r < W; ++r) {
+            const int64_t lo = offset_of(head_splits, r);
+            if (g >= lo && g < lo + head_splits[r]) {
+                const int64_t h = g - lo;
+                *src_rank = r;
+                *src_elem = ((bb * S + offset_of(seq_splits, q) + i) * head_splits[r] + h) * d + j;
+                return 0;
+            }
+        }
+        return -1;
+    }
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Fused QK RMSNorm + RoPE, in double.                                                         */
+/* ------------------------------------------------------------------------------------------ */
+
+/* bf16 bit pattern -> value: bf16 is the upper half of an IEEE binary32. */
+double orc_bf16_to_double(uint16_t h)
+{
+    uint32_t bits = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/*
+ * double -> bf16 bit pattern with one round-to-nearest-even step (8 significand bits, exponent
+ * range of binary32, gradual underflow, overflow to infinity).
+ */
+uint16_t orc_double_to_bf16(double x)
+{
+    const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x)) return (uint16_t)(sign | 0x7FC0u);
+    const double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80u);
+    if (a == 0.0) return sign;
+    int E;
+    frexp(a, &E);           /* a in [2^(E-1), 2^E) */
+    int ex = E - 1;         /* a in [2^ex, 2^(ex+1)) */
+    if (ex < -126) ex = -126; /* below the normal range the spacing stays 2^-133 */
+    const double quantum = ldexp(1.0, ex - 7);
+    const double k = nearbyint(a / quantum); /* default rounding mode: nearest, ties to even */
+    const double v = k * quantum;
+    if (v >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80u);
+    const float f = (float)v; /* exact: v has at most 8 significant bits */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return (uint16_t)(sign | (uint16_t)(bits >> 16));
+}
+
+/* RMSNorm over one row of d values: y = x / sqrt(mean(x^2) + eps) * w. */
+void orc_rmsnorm(const double* x, int64_t d, const double* w, double eps, double* y)
+{
+    double sum_sq = 0.0;
+    for (int64_t j = 0; j < d; ++j) sum_sq += x[j] * x[j];
+    const double mean_sq = sum_sq / (double)d;
+    const double inv_rms = 1.0 / sqrt(mean_sq + eps);
+    for (int64_t j = 0; j < d; ++j) y[j] = x[j] * inv_rms * w[j];
+}
+
+/*
+ * Rotary embedding of one row in place, adjacent pairs: for j < d/2 the pair (y[2j], y[2j+1])
+ * is rotated by the angle p * theta^(-2j/d).
+ */
+void orc_rope(double* y, int64_t d, double p, double theta)
+{
+    for (int64_t j = 0; j < d / 2; ++j) {
+        const double freq = pow(theta, -2.0 * (double)j / (double)d);
+        const double angle = p * freq;
+        const double c = cos(angle), s = sin(angle);
+        const double a = y[2 * j], bq = y[2 * j + 1];
+        y[2 * j] = a * c - bq * s;
+        y[2 * j + 1] = a * s + bq * c;
+    }
+}
+
+/* One head row: bf16 in -> RMSNorm -> RoPE at position p -> double out. */
+static void transform_row(const uint16_t* x_bf16, int64_t d, const double* w, double eps,
+                          double p, double theta, double* y)
+{
+    double* x = (double*)malloc((size_t)d * sizeof(double));
+    for (int64_t j = 0; j < d; ++j) x[j] = orc_bf16_to_double(x_bf16[j]);
+    orc_rmsnorm(x, d, w, eps, y);
+    orc_rope(y, d, p, theta);
+    free(x);
+}
+
+/*
+ * Formulation A: transform each source row where it sits (position p = seq_off(q) + i), then
+ * place it where mode 0 puts it. x_in[q] holds rank q's (b, s_q, N, d) bf16 tensor; y_out[r]
+ * receives rank r's (b, S, n_r, d) tensor in double.
+ */
+int orc_qk_fused_A(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                   int64_t d, const uint16_t* const* x_in, const double* w, double eps,
+                   double theta, double* const* y_out)
+{
+    if (check_geometry(W, b, seq_splits, head_splits, d) || (d % 2) != 0) return -1;
+    const int64_t S = offset_of(seq_splits, W);
+    const int64_t N = offset_of(head_splits, W);
+    for (int q = 0; q < W; ++q) {
+        const int64_t s_q = seq_splits[q];
+        const int64_t seq_off_q = offset_of(seq_splits, q);
+        for (int64_t bb = 0; bb < b; ++bb)
+            for (int64_t i = 0; i < s_q; ++i)
+                for (int64_t g = 0; g < N; ++g) {
+                    /* the destination rank owns global head g */
+                    int r = 0;
+                    while (!(g >= offset_of(head_splits, r) &&
+                             g < offset_of(head_splits, r) + head_splits[r]))
+                        ++r;
+                    const int64_t n_r = head_splits[r];
+                    const int64_t h = g - offset_of(head_splits, r);
+                    const uint16_t* src = x_in[q] + ((bb * s_q + i) * N + g) * d;
+                    double* dst = y_out[r] + ((bb * S + seq_off_q + i) * n_r + h) * d;
+                    transform_row(src, d, w, eps, (double)(seq_off_q + i), theta, dst);
+                }
+    }
+    return 0;
+}
+
+/*
+ * Formulation B: relayout the bf16 bytes first (mode 0), then transform each destination row
+ * with p = its index along the output's global sequence axis.
+ */
+int orc_qk_fused_B(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                   int64_t d, const uint16_t* const* x_in, const double* w, double eps,
+                   double theta, double* const* y_out)
+{
+    if (check_geometry(W, b, seq_splits, head_splits, d) || (d % 2) != 0) return -1;
+    const int64_t S = offset_of(seq_splits, W);
+    uint8_t* moved[ORC_MAX_W] = {0};
+    for (int r = 0; r < W; ++r)
+        moved[r] = (uint8_t*)malloc((size_t)(b * S * head_splits[r] * d * 2 + 1));
+    int rc = orc_a2a_4d(W, b, seq_splits, head_splits, d, 2, 0, (const uint8_t* const*)x_in,
+                        moved);
+    if (rc == 0) {
+        for (int r = 0; r < W; ++r) {
+            const int64_t n_r = head_splits[r];
+            for (int64_t bb = 0; bb < b; ++bb)
+                for (int64_t s = 0; s < S; ++s)
+                    for (int64_t h = 0; h < n_r; ++h) {
+                        const int64_t row = (bb * S + s) * n_r + h;
+                        transform_row((const uint16_t*)moved[r] + row * d, d, w, eps, (double)s,
+                                      theta, y_out[r] + row * d);
+                    }
+        }
+    }
+    for (int r = 0; r < W; ++r) free(moved[r]);
+    return rc;
+}
+
+/*
+ * One output row of the fused transform, for sampled checks of large workloads: rank r's row
+ * (bb, s, h) of its (b, S, n_r, d) output, computed from the source row the definition names.
+ */
+int orc_qk_fused_row(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                     int64_t d, int r, int64_t bb, int64_t s, int64_t h,
+                     const uint16_t* const* x_in, const double* w, double eps, double theta,
+                     double* y)
+{
+    if (check_geometry(W, b, seq_splits, head_splits, d) || (d % 2) != 0) return -1;
+    if (r < 0 || r >= W || bb < 0 || bb >= b || h < 0 || h >= head_splits[r]) return -1;
+    if (s < 0 || s >= offset_of(seq_splits, W)) return -1;
+    const int64_t N = offset_of(head_splits, W);
+    for (int q = 0; q < W; ++q) {
+        const int64_t lo = offset_of(seq_splits, q);
+        if (s >= lo && s < lo + seq_splits[q]) {
+            const int64_t i = s - lo;
+            const uint16_t* src =
+                x_in[q] + ((bb * seq_splits[q] + i) * N + offset_of(head_splits, r) + h) * d;
+            transform_row(src, d, w, eps, (double)s, theta, y);
+            return 0;
+        }
+    }
+    return -1;
+}
+
+/* Element-wise array forms of the two bf16 conversions above. */
+void orc_bf16_to_double_array(const uint16_t* h, int64_t n, double* out)
+{
+    for (int64_t k = 0; k < n; ++k) out[k] = orc_bf16_to_double(h[k]);
+}
+
+void orc_double_to_bf16_array(const double* x, int64_t n, uint16_t* out)
+{
+    for (int64_t k = 0; k < n; ++k) out[k] = orc_double_to_bf16(x[k]);
+}

@@ -1,0 +1,411 @@
+"""Checks that tie the CPU oracle to something other than itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises ``AssertionError`` when the oracle
+disagrees with an independent fact: a library formulation of the same mapping (torch ``split`` +
+``cat``; the pages' own baseline of permute + all_to_all + permute, emulated in one process), an
+identity or invariant (W=1, round trip, byte conservation), the shapes the pages print, a library
+routine (``torch.nn.functional.rms_norm``, complex multiplication, torch's float32->bf16
+rounding) or a closed form (one-hot rows, unit-weight RMS).
+
+``test_oracle.py`` runs every pin against the oracle; ``test_oracle_mutants.py`` plants plausible
+mistakes in a copy of the oracle's C source and checks that some pin catches each one.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+import os
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+UINT = {1: np.uint8, 2: np.uint16, 4: np.uint32}
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# --------------------------------------------------------------------------------------------
+# independent formulations of the relayout
+# --------------------------------------------------------------------------------------------
+def split_cat_mode0(xs, head_splits):
+    """out[r] = concatenation over ranks q (along the sequence) of rank q's r-th head group."""
+    W = len(xs)
+    pieces = [torch.split(torch.from_numpy(x), list(head_splits), dim=2) for x in xs]
+    return [torch.cat([pieces[q][r] for q in range(W)], dim=1).numpy() for r in range(W)]
+
+
+def split_cat_mode1(ys, seq_splits):
+    """out[q] = concatenation over ranks r (along heads) of rank r's q-th sequence piece."""
+    W = len(ys)
+    pieces = [torch.split(torch.from_numpy(y), list(seq_splits), dim=1) for y in ys]
+    return [torch.cat([pieces[r][q] for r in range(W)], dim=2).numpy() for q in range(W)]
+
+
+def pages_base_mode0(xs):
+    """Even splits only: the baseline the pages measure against, permute + all_to_all_single +
+    permute, with the all-to-all of W ranks emulated as a swap of the (sender, receiver) axes."""
+    W = len(xs)
+    b, s, N, d = xs[0].shape
+    n = N // W
+    send = [torch.from_numpy(x).reshape(b, s, W, n, d).permute(2, 0, 1, 3, 4) for x in xs]
+    recv = [torch.stack([send[q][r] for q in range(W)], dim=0) for r in range(W)]
+    return [t.permute(1, 0, 2, 3, 4).reshape(b, W * s, n, d).numpy() for t in recv]
+
+
+def pages_base_mode1(ys):
+    W = len(ys)
+    b, S, n, d = ys[0].shape
+    s = S // W
+    send = [torch.from_numpy(y).reshape(b, W, s, n, d).permute(1, 0, 2, 3, 4) for y in ys]
+    recv = [torch.stack([send[r][q] for r in range(W)], dim=0) for q in range(W)]
+    return [t.permute(1, 2, 0, 3, 4).reshape(b, s, W * n, d).numpy() for t in recv]
+
+
+# --------------------------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------------------------
+def _rand_inputs(rng, W, b, seq_splits, head_splits, d, e, mode):
+    N, S = sum(head_splits), sum(seq_splits)
+    if mode == 0:
+        shapes = [(b, s, N, d) for s in seq_splits]
+    else:
+        shapes = [(b, S, n, d) for n in head_splits]
+    info = np.iinfo(UINT[e])
+    return [rng.integers(0, info.max, size=sh, dtype=UINT[e], endpoint=True) for sh in shapes]
+
+
+def _same(a_list, b_list, what):
+    assert len(a_list) == len(b_list), what
+    for k, (a, b) in enumerate(zip(a_list, b_list)):
+        assert a.shape == b.shape, f"{what}: rank {k} shape {a.shape} != {b.shape}"
+        assert np.array_equal(a, b), f"{what}: rank {k} differs"
+
+
+def _random_geometries(rng, count, max_W=4, allow_zero=True):
+    out = []
+    while len(out) < count:
+        W = int(rng.integers(1, max_W + 1))
+        lo = 0 if allow_zero else 1
+        seq = [int(v) for v in rng.integers(lo, 5, size=W)]
+        heads = [int(v) for v in rng.integers(lo, 4, size=W)]
+        if sum(seq) == 0 or sum(heads) == 0:
+            continue
+        out.append((W, int(rng.integers(1, 3)), seq, heads, int(rng.choice([2, 4, 8])),
+                    int(rng.choice([1, 2, 4]))))
+    return out
+
+
+# --------------------------------------------------------------------------------------------
+# relayout pins
+# --------------------------------------------------------------------------------------------
+def pin_relayout_vs_split_cat(orc, quick=False):
+    rng = np.random.default_rng(11)
+    for W, b, seq, heads, d, e in _random_geometries(rng, 40 if quick else 200):
+        xs = _rand_inputs(rng, W, b, seq, heads, d, e, 0)
+        _same(orc.a2a_4d(xs, seq, heads, 0), split_cat_mode0(xs, heads), f"mode0 {W,b,seq,heads,d,e}")
+        ys = _rand_inputs(rng, W, b, seq, heads, d, e, 1)
+        _same(orc.a2a_4d(ys, seq, heads, 1), split_cat_mode1(ys, seq), f"mode1 {W,b,seq,heads,d,e}")
+
+
+def pin_relayout_enumeration(orc, quick=False):
+    """Every split combination with shares in {0, 1, 2} for W <= 3 (W <= 2 when quick), b in
+    {1, 2}, against the split/cat formulation."""
+    rng = np.random.default_rng(12)
+    max_W = 2 if quick else 3
+    for W in range(1, max_W + 1):
+        for seq in itertools.product(range(3), repeat=W):
+            if sum(seq) == 0:
+                continue
+            for heads in itertools.product(range(3), repeat=W):
+                if sum(heads) == 0:
+                    continue
+                for b in (1, 2):
+                    xs = _rand_inputs(rng, W, b, seq, heads, 4, 2, 0)
+                    _same(orc.a2a_4d(xs, seq, heads, 0), split_cat_mode0(xs, heads), "enum mode0")
+                    ys = _rand_inputs(rng, W, b, seq, heads, 4, 2, 1)
+                    _same(orc.a2a_4d(ys, seq, heads, 1), split_cat_mode1(ys, seq), "enum mode1")
+
+
+def pin_relayout_vs_pages_base(orc, quick=False):
+    rng = np.random.default_rng(13)
+    for W in (1, 2, 3, 4, 8):
+        for b, s, n, d, e in ((1, 3, 2, 8, 2), (2, 5, 1, 4, 4), (1, 2, 3, 16, 1)):
+            seq, heads = [s] * W, [n] * W
+            xs = _rand_inputs(rng, W, b, seq, heads, d, e, 0)
+            _same(orc.a2a_4d(xs, seq, heads, 0), pages_base_mode0(xs), f"base mode0 W={W}")
+            ys = _rand_inputs(rng, W, b, seq, heads, d, e, 1)
+            _same(orc.a2a_4d(ys, seq, heads, 1), pages_base_mode1(ys), f"base mode1 W={W}")
+
+
+def pin_identity_w1(orc, quick=False):
+    rng = np.random.default_rng(14)
+    for b, s, n, d, e in ((1, 7, 3, 8, 2), (2, 1, 5, 4, 4), (3, 4, 1, 16, 1)):
+        x = _rand_inputs(rng, 1, b, [s], [n], d, e, 0)
+        _same(orc.a2a_4d(x, [s], [n], 0), x, "W=1 mode 0 identity")
+        _same(orc.a2a_4d(x, [s], [n], 1), x, "W=1 mode 1 identity")
+
+
+def pin_round_trip(orc, quick=False):
+    rng = np.random.default_rng(15)
+    for W, b, seq, heads, d, e in _random_geometries(rng, 30 if quick else 120):
+        xs = _rand_inputs(rng, W, b, seq, heads, d, e, 0)
+        _same(orc.a2a_4d(orc.a2a_4d(xs, seq, heads, 0), seq, heads, 1), xs, "mode1(mode0(x))")
+        ys = _rand_inputs(rng, W, b, seq, heads, d, e, 1)
+        _same(orc.a2a_4d(orc.a2a_4d(ys, seq, heads, 1), seq, heads, 0), ys, "mode0(mode1(y))")
+
+
+def pin_conservation_and_coverage(orc, quick=False):
+    """Unique 32-bit tags in, every output slot written exactly once with some input's tag."""
+    rng = np.random.default_rng(16)
+    for W, b, seq, heads, d, _ in _random_geometries(rng, 20 if quick else 80):
+        N, S = sum(heads), sum(seq)
+        for mode in (0, 1):
+            in_shapes = ([(b, s, N, d) for s in seq] if mode == 0 else [(b, S, n, d) for n in heads])
+            out_shapes = orc.out_shapes(b, seq, heads, d, mode)
+            base = 0
+            xs = []
+            for sh in in_shapes:
+                cnt = int(np.prod(sh))
+                xs.append((np.arange(cnt, dtype=np.uint32) + base + 1).reshape(sh))
+                base += cnt
+            outs = [np.zeros(sh, dtype=np.uint32) for sh in out_shapes]  # 0 = never written
+            orc.a2a_4d_raw(W, b, seq, heads, d, 4, mode, [x.ctypes.data for x in xs],
+                           [o.ctypes.data for o in outs])
+            # the sizes the definition implies: sum of splits equals the global extents
+            assert sum(int(np.prod(s)) for s in out_shapes) == base
+            got = np.sort(np.concatenate([o.ravel() for o in outs])) if outs else np.array([])
+            want = np.arange(1, base + 1, dtype=np.uint32)
+            assert np.array_equal(got, want), f"not a permutation of the input (mode {mode})"
+
+
+def pin_source_query(orc, quick=False):
+    """The single-element query names the input element the bulk relayout put there."""
+    rng = np.random.default_rng(17)
+    for W, b, seq, heads, d, e in _random_geometries(rng, 20 if quick else 60):
+        for mode in (0, 1):
+            xs = _rand_inputs(rng, W, b, seq, heads, d, e, mode)
+            outs = orc.a2a_4d(xs, seq, heads, mode)
+            for r, o in enumerate(outs):
+                flat = o.ravel()
+                for k in rng.integers(0, max(flat.size, 1), size=min(8, flat.size)):
+                    q, idx = orc.a2a_4d_source(W, b, seq, heads, d, mode, r, int(k))
+                    assert xs[q].ravel()[idx] == flat[k], "source query disagrees with relayout"
+
+
+def _golden_lines():
+    with open(os.path.join(GOLDEN, "page_examples.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield [p.strip() for p in line.split("|")]
+
+
+def _kv(text):
+    return dict(item.split("=", 1) for item in text.split())
+
+
+def pin_page_shapes(orc, quick=False):
+    """The shapes the two Quick start sections print, computed by actually running the oracle."""
+    rng = np.random.default_rng(18)
+    lines = {name: (_kv(inp), _kv(exp)) for name, inp, exp in _golden_lines()}
+    inp, exp = lines["quickstart_v010"]
+    for ws in ((2,) if quick else (1, 2, 8)):
+        b, s, hpr, d = int(inp["b"]), int(inp["s_local"]), int(inp["heads_per_rank"]), int(inp["d"])
+        xs = _rand_inputs(rng, ws, b, [s] * ws, [hpr] * ws, d, 2, 0)
+        assert xs[0].shape == (b, s, hpr * ws, d)
+        outs = orc.a2a_4d(xs, [s] * ws, [hpr] * ws, 0)
+        want = eval(exp["out_shape"], {"ws": ws})  # noqa: S307  (fixture arithmetic like 16*ws)
+        assert all(o.shape == want for o in outs)
+    inp, exp = lines["quickstart_v021"]
+    for ws in ((2,) if quick else (2, 4)):
+        b, s, hpr, d = int(inp["b"]), int(inp["s_local"]), int(inp["heads_per_rank"]), int(inp["d"])
+        xs = _rand_inputs(rng, ws, b, [s] * ws, [hpr] * ws, d, 2, 0)
+        ys = orc.a2a_4d(xs, [s] * ws, [hpr] * ws, 0)
+        assert all(y.shape == eval(exp["out_shape"], {"ws": ws}) for y in ys)  # noqa: S307
+        zs = orc.a2a_4d(ys, [s] * ws, [hpr] * ws, 1)
+        assert all(z.shape == eval(exp["back"], {"ws": ws}) for z in zs)  # noqa: S307
+        _same(zs, xs, "quick start round trip")
+
+
+# --------------------------------------------------------------------------------------------
+# fused QK RMSNorm + RoPE pins
+# --------------------------------------------------------------------------------------------
+def _freq(theta, j, d):
+    return theta ** (-2.0 * j / d)
+
+
+def pin_rmsnorm_vs_torch(orc, quick=False):
+    rng = np.random.default_rng(21)
+    for d in (2, 8, 64, 128):
+        for eps in (1e-6, 1e-2, 0.0):
+            x = rng.standard_normal(d) * rng.uniform(0.01, 10)
+            w = 1.0 + 0.1 * rng.standard_normal(d)
+            want = F.rms_norm(torch.from_numpy(x)[None], (d,), weight=torch.from_numpy(w),
+                              eps=eps)[0].numpy()
+            np.testing.assert_allclose(orc.rmsnorm(x, w, eps), want, rtol=1e-13, atol=1e-15)
+
+
+def pin_rope_vs_complex(orc, quick=False):
+    """Adjacent pairs as complex numbers, multiplied by exp(i * p * theta^(-2j/d))."""
+    rng = np.random.default_rng(22)
+    for d in (2, 8, 128):
+        for p in (0, 1, 7, 9450, 75599, 249999):
+            y = rng.standard_normal(d)
+            z = torch.view_as_complex(torch.from_numpy(y.copy()).view(d // 2, 2))
+            ang = torch.tensor([p * _freq(1e4, j, d) for j in range(d // 2)], dtype=torch.float64)
+            rot = z * torch.polar(torch.ones_like(ang), ang)
+            want = torch.view_as_real(rot).reshape(d).numpy()
+            np.testing.assert_allclose(orc.rope(y, p, 1e4), want, rtol=1e-12, atol=1e-12)
+
+
+def pin_rope_identities(orc, quick=False):
+    rng = np.random.default_rng(23)
+    d = 128
+    y = rng.standard_normal(d)
+    np.testing.assert_array_equal(orc.rope(y, 0, 1e4), y)           # p = 0 is the identity
+    for p1, p2 in ((3, 5), (9450, -9450), (75599, 1), (12345, 678)):
+        a = orc.rope(y, p1, 1e4)
+        pairs_in = np.hypot(y[0::2], y[1::2])
+        pairs_out = np.hypot(a[0::2], a[1::2])
+        np.testing.assert_allclose(pairs_out, pairs_in, rtol=1e-12)  # rotation keeps pair norms
+        np.testing.assert_allclose(orc.rope(a, p2, 1e4), orc.rope(y, p1 + p2, 1e4),
+                                   rtol=1e-9, atol=1e-9)             # rotations compose
+
+
+def pin_one_hot_rows(orc, quick=False):
+    """x = e_(2j): the normalised row is c * e_(2j) with c = w_(2j) / sqrt(1/d + eps), and RoPE
+    turns it into c * (cos(p theta_j), sin(p theta_j)) in pair j, zero elsewhere."""
+    d, eps, theta = 16, 1e-6, 1e4
+    w = np.linspace(0.5, 1.5, d)
+    for j in range(d // 2):
+        for p in (0, 1, 4, 100):
+            x = np.zeros(d)
+            x[2 * j] = 1.0
+            got = orc.rope(orc.rmsnorm(x, w, eps), p, theta)
+            c = w[2 * j] / math.sqrt(1.0 / d + eps)
+            want = np.zeros(d)
+            want[2 * j] = c * math.cos(p * _freq(theta, j, d))
+            want[2 * j + 1] = c * math.sin(p * _freq(theta, j, d))
+            np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-13)
+
+
+def pin_unit_weight_rms(orc, quick=False):
+    """With unit weights the output's RMS is sqrt(ms / (ms + eps)) at any position."""
+    rng = np.random.default_rng(24)
+    d = 128
+    for eps in (1e-6, 0.5):
+        x = rng.standard_normal(d) * 0.05
+        ms = float(np.mean(x * x))
+        y = orc.rope(orc.rmsnorm(x, np.ones(d), eps), 777, 1e4)
+        assert abs(math.sqrt(float(np.mean(y * y))) - math.sqrt(ms / (ms + eps))) < 1e-12
+
+
+def _bf16_inputs(rng, W, b, seq, heads, d):
+    N = sum(heads)
+    out = []
+    for s in seq:
+        v = torch.from_numpy(rng.standard_normal((b, s, N, d)).astype(np.float32)).to(torch.bfloat16)
+        out.append(v.view(torch.int16).numpy().view(np.uint16))
+    return out
+
+
+def pin_fused_formulations_agree(orc, quick=False):
+    """Transform-then-place equals place-then-transform, exactly (same double operations)."""
+    rng = np.random.default_rng(25)
+    cases = [(2, 1, [3, 2], [2, 1], 8), (3, 2, [2, 0, 3], [1, 2, 1], 16), (1, 1, [5], [2], 4),
+             (4, 1, [1, 2, 1, 3], [1, 1, 1, 1], 8)]
+    for W, b, seq, heads, d in cases:
+        xs = _bf16_inputs(rng, W, b, seq, heads, d)
+        w = 1.0 + 0.1 * rng.standard_normal(d)
+        A = orc.qk_fused_A(xs, seq, heads, w, 1e-6, 1e4)
+        B = orc.qk_fused_B(xs, seq, heads, w, 1e-6, 1e4)
+        _same(A, B, "fused A vs B")
+        for r in range(W):
+            for bb in range(b):
+                for s in range(sum(seq)):
+                    for h in range(heads[r]):
+                        row = orc.qk_fused_row(xs, seq, heads, w, 1e-6, 1e4, r, bb, s, h)
+                        assert np.array_equal(row, A[r][bb, s, h]), "fused row query disagrees"
+
+
+def pin_fused_placement_decode(orc, quick=False):
+    """One-hot source rows whose hot pair index encodes (source rank, global head): each output
+    row's hot pair and rotation angle must decode to the rank/head/position mode 0 names."""
+    theta = 1e4
+    W, seq, heads = 3, [2, 1, 2], [1, 2, 1]
+    N, S = sum(heads), sum(seq)
+    d = 2 * W * N                      # one pair per (q, g)
+    xs = []
+    for q in range(W):
+        x = np.zeros((1, seq[q], N, d), dtype=np.float32)
+        for g in range(N):
+            x[0, :, g, 2 * (q * N + g)] = 1.0
+        xs.append(torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    outs = orc.qk_fused_A(xs, seq, heads, np.ones(d), 0.0, theta)
+    head_owner = [r for r in range(W) for _ in range(heads[r])]
+    seq_owner = [q for q in range(W) for _ in range(seq[q])]
+    for r in range(W):
+        for s in range(S):
+            for h in range(heads[r]):
+                row = outs[r][0, s, h]
+                mags = np.hypot(row[0::2], row[1::2])
+                j = int(np.argmax(mags))
+                q, g = divmod(j, N)
+                assert q == seq_owner[s], "row came from the wrong source rank"
+                assert head_owner[g] == r and g - sum(heads[:r]) == h, "wrong head"
+                ang = math.atan2(row[2 * j + 1], row[2 * j]) % (2 * math.pi)
+                p = ang / _freq(theta, j, d)
+                assert abs(p - s) < 1e-6, f"rotation angle decodes to p={p}, expected {s}"
+
+
+def pin_bf16_rounding(orc, quick=False):
+    """double -> bf16 on float32-representable values equals torch's float32 -> bf16 (one
+    round-to-nearest-even); bf16 -> double equals torch's widening."""
+    rng = np.random.default_rng(26)
+    bits = rng.integers(0, 2 ** 32, size=200000, dtype=np.uint64).astype(np.uint32)
+    ties = (rng.integers(0, 2 ** 16, size=20000, dtype=np.uint64).astype(np.uint32) << 16) | 0x8000
+    near = np.concatenate([ties - 1, ties + 1])
+    special = np.array([0x00000001, 0x00008000, 0x00018000, 0x007F8000, 0x7F7F8000, 0x7F7FFFFF,
+                        0x80008000, 0x3F808000, 0x3F818000], dtype=np.uint32)
+    allbits = np.concatenate([bits, ties, near, special])
+    f = allbits.view(np.float32)
+    f = f[np.isfinite(f)]
+    want = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = orc.double_to_bf16(f.astype(np.float64))
+    assert np.array_equal(got, want), "bf16 rounding differs from torch float32->bf16"
+    h = np.arange(0, 2 ** 16, dtype=np.uint32).astype(np.uint16)
+    wide = torch.from_numpy(h.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    mine = orc.bf16_to_double(h)
+    finite = np.isfinite(wide)
+    assert np.array_equal(mine[finite], wide[finite])
+
+
+PINS = [
+    pin_relayout_vs_split_cat,
+    pin_relayout_enumeration,
+    pin_relayout_vs_pages_base,
+    pin_identity_w1,
+    pin_round_trip,
+    pin_conservation_and_coverage,
+    pin_source_query,
+    pin_page_shapes,
+    pin_rmsnorm_vs_torch,
+    pin_rope_vs_complex,
+    pin_rope_identities,
+    pin_one_hot_rows,
+    pin_unit_weight_rms,
+    pin_fused_formulations_agree,
+    pin_fused_placement_decode,
+    pin_bf16_rounding,
+]
+
+
+def run_all(orc, quick=True):
+    """Run every pin; return the names of those that failed (a crash counts as a failure)."""
+    failed = []
+    for pin in PINS:
+        try:
+            pin(orc, quick=quick)
+        except Exception as exc:  # noqa: BLE001  (any failure is a caught mistake)
+            failed.append(f"{pin.__name__}: {type(exc).__name__}")
+    return failed

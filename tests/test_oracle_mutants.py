@@ -1,0 +1,108 @@
+"""Plant plausible mistakes in a copy of the oracle's C source and check that the pins catch each.
+
+Each planted variant is compiled into a temporary directory and the whole pin set runs against it
+in a child process (a variant that crashes the child also counts as caught). This is what shows
+the pins are strong enough to trust the oracle: a dropped term, a wrong index, a wrong sign or a
+transposed operand anywhere in it makes at least one pin fail.
+"""
+import json
+import os
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+import oracle as oracle_pkg
+
+TESTS = os.path.dirname(os.path.abspath(__file__))
+
+MUTANTS = {
+    "seq_side_drops_head_offset": [
+        ("* N + head_off_r + h) * d + j;", "* N + h) * d + j;")],
+    "head_side_drops_seq_offset": [
+        ("(bb * S + seq_off_q + i) * n_r + h) * d + j;", "(bb * S + i) * n_r + h) * d + j;")],
+    "head_side_wrong_batch_stride": [
+        ("(bb * S + seq_off_q + i) * n_r + h) * d + j;",
+         "(bb * s_q + seq_off_q + i) * n_r + h) * d + j;")],
+    "seq_side_wrong_batch_stride": [
+        ("((bb * s_q + i) * N + head_off_r + h) * d + j;",
+         "((bb * S + i) * N + head_off_r + h) * d + j;")],
+    "offsets_include_own_shard": [
+        ("for (int p = 0; p < k; ++p) s += splits[p];",
+         "for (int p = 0; p <= k && p < 8; ++p) s += splits[p];")],
+    "mode1_reads_wrong_rank": [
+        ("memcpy(out[q] + seq_side * e, in[r] + head_side * e, (size_t)e);",
+         "memcpy(out[q] + seq_side * e, in[q] + head_side * e, (size_t)e);")],
+    "mode1_same_as_mode0": [
+        ("if (mode == 0)\n                                memcpy",
+         "if (mode == 0 || mode == 1)\n                                memcpy")],
+    "source_query_drops_head_offset": [
+        ("N + offset_of(head_splits, r) + h) * d + j;", "N + h) * d + j;")],
+    "rmsnorm_drops_eps": [("sqrt(mean_sq + eps)", "sqrt(mean_sq)")],
+    "rmsnorm_sum_not_mean": [("sum_sq / (double)d", "sum_sq")],
+    "rmsnorm_drops_weight": [("x[j] * inv_rms * w[j]", "x[j] * inv_rms")],
+    "rmsnorm_eps_outside_sqrt": [("1.0 / sqrt(mean_sq + eps)", "1.0 / (sqrt(mean_sq) + eps)")],
+    "rope_sin_sign": [("y[2 * j] = a * c - bq * s;", "y[2 * j] = a * c + bq * s;"),
+                      ("y[2 * j + 1] = a * s + bq * c;", "y[2 * j + 1] = -a * s + bq * c;")],
+    "rope_freq_exponent": [("-2.0 * (double)j / (double)d", "-1.0 * (double)j / (double)d")],
+    "rope_rotate_half_pairs": [
+        ("const double a = y[2 * j], bq = y[2 * j + 1];", "const double a = y[j], bq = y[j + d / 2];"),
+        ("y[2 * j] = a * c - bq * s;", "y[j] = a * c - bq * s;"),
+        ("y[2 * j + 1] = a * s + bq * c;", "y[j + d / 2] = a * s + bq * c;")],
+    "fused_local_position": [
+        ("transform_row(src, d, w, eps, (double)(seq_off_q + i), theta, dst);",
+         "transform_row(src, d, w, eps, (double)i, theta, dst);")],
+    "fused_row_local_position": [
+        ("transform_row(src, d, w, eps, (double)s, theta, y);",
+         "transform_row(src, d, w, eps, (double)i, theta, y);")],
+    "bf16_truncates": [("nearbyint(a / quantum)", "floor(a / quantum)")],
+    "bf16_one_bit_too_many": [("ldexp(1.0, ex - 7)", "ldexp(1.0, ex - 8)")],
+    "bf16_widening_drops_low_bits": [("uint32_t bits = (uint32_t)h << 16;",
+                                      "uint32_t bits = ((uint32_t)h & 0xFFF0u) << 16;")],
+}
+
+CHILD = r"""
+import json, sys
+sys.path.insert(0, {tests!r}); sys.path.insert(0, {root!r})
+import oracle, oracle_pins
+orc = oracle.Oracle({lib!r})
+print(json.dumps(oracle_pins.run_all(orc, quick=True)))
+"""
+
+
+def _check(name, tmpdir):
+    with open(oracle_pkg.SOURCE) as f:
+        src = f.read()
+    for old, new in MUTANTS[name]:
+        assert src.count(old) == 1, f"{name}: pattern not found exactly once: {old!r}"
+        src = src.replace(old, new)
+    c_path = os.path.join(tmpdir, f"{name}.c")
+    with open(c_path, "w") as f:
+        f.write(src)
+    lib = oracle_pkg.build(os.path.join(tmpdir, f"lib{name}.so"), c_path)
+    code = CHILD.format(tests=TESTS, root=os.path.dirname(TESTS), lib=lib)
+    proc = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    if proc.returncode != 0:
+        return name, ["crashed"]
+    return name, json.loads(proc.stdout.strip().splitlines()[-1])
+
+
+def test_every_planted_mistake_is_caught(tmp_path):
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 2)) as pool:
+        results = dict(pool.map(lambda n: _check(n, str(tmp_path)), MUTANTS))
+    missed = [n for n, failed in results.items() if not failed]
+    assert not missed, f"planted mistakes no pin caught: {missed}"
+
+
+def test_unmutated_copy_passes(tmp_path):
+    """The same child-process harness on an unmodified copy reports no failure."""
+    lib = oracle_pkg.build(os.path.join(str(tmp_path), "libclean.so"))
+    code = CHILD.format(tests=TESTS, root=os.path.dirname(TESTS), lib=lib)
+    proc = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    assert proc.returncode == 0, proc.stderr[-2000:]
+    assert json.loads(proc.stdout.strip().splitlines()[-1]) == []
+
+
+if __name__ == "__main__":
+    pytest.main([__file__, "-q"])
