@@ -1,0 +1,463 @@
+"""Benchmark of the Ulysses exchange around one attention block at the Wan-720p shape.
+
+One step is one pass of the whole hot path over one batch of synthetic bf16 input, W=8 virtual
+ranks, b=1, 75,600 tokens (9,450 per rank), 40 heads (5 per rank), d=128:
+  1. q and k: mode 0 with QK RMSNorm + RoPE fused into the scatter (one launch),
+  2. v: plain mode 0 (one launch),
+  3. the attention output: plain mode 1 back to sequence shards (one launch).
+Throughput counts algorithmic bytes (every tensor byte read once and written once) per second.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle on this machine's host cores on the same workload
+geometry (a bounded sequence slice per step); it is a slow plain program, not a tuned baseline.
+Under torchrun (N > 1) every rank runs its own replica of the workload on its own GPU (the path
+does not shard across GPUs); the value is all ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "relayout GB/s (read+write) at Wan-720p shape, W=8; % of HBM roofline"
+EPS, THETA = 1e-6, 1e4
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [(t, l.split(", ")) for t, l in self.lines if l.count(",") >= 8]
+        inside = [r for t, r in rows if self.t0 is not None and self.t0 <= t <= self.t1]
+        use = inside or [r for _, r in rows[-3:]]
+        if not use:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in use if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(use[0][2]), "reasons": sorted(reasons),
+                "samples": len(use), "samples_in_timed_region": len(inside),
+                "power_w_max": max((num(r[3]) or 0.0) for r in use)}
+
+
+# ------------------------------------------------------------------------------------------------
+# the GPU workload
+# ------------------------------------------------------------------------------------------------
+class Workload:
+    def __init__(self, torch, B, wl, device):
+        self.torch, self.B = torch, B
+        cfg = wl.WAN
+        self.cfg = cfg
+        bf16 = torch.bfloat16
+        self.plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
+        self.q = wl.seq_side_inputs(cfg, device, seed=wl.FUSED.seed)
+        self.k = wl.seq_side_inputs(cfg, device, seed=wl.FUSED.extra["k_seed"])
+        self.v = wl.seq_side_inputs(cfg, device, seed=5)
+        self.o = wl.head_side_inputs(cfg, device, seed=6)
+        self.w = wl.rms_weights(cfg.d, seed=wl.FUSED.extra["w_seed"]).to(device)
+        head = [cfg.head_side_shape(r) for r in range(cfg.W)]
+        seq = [cfg.seq_side_shape(q) for q in range(cfg.W)]
+        self.qo = [torch.empty(s, dtype=bf16, device=device) for s in head]
+        self.ko = [torch.empty(s, dtype=bf16, device=device) for s in head]
+        self.vo = [torch.empty(s, dtype=bf16, device=device) for s in head]
+        self.oo = [torch.empty(s, dtype=bf16, device=device) for s in seq]
+        self.side = cfg.plane_bytes()          # one tensor set, all ranks: 774,144,000 bytes
+        self.bytes_fused = 4 * self.side       # q, k in; q, k out
+        self.bytes_plain = 2 * self.side       # in + out
+        self.bytes_step = self.bytes_fused + 2 * self.bytes_plain
+        self.launches_per_step = (B.ulysses_plan_num_chunks(self.plan, 0) * 2 +
+                                  B.ulysses_plan_num_chunks(self.plan, 1))
+
+    def step(self, stream, ev=None):
+        B = self.B
+        if ev:
+            ev[0].record(stream)
+        B.ulysses_a2a_4d_qk_fused(self.plan, self.q, self.k, self.qo, self.ko, self.w, EPS, THETA,
+                                  stream)
+        if ev:
+            ev[1].record(stream)
+        B.ulysses_a2a_4d(self.plan, 0, self.v, self.vo, stream)
+        if ev:
+            ev[2].record(stream)
+        B.ulysses_a2a_4d(self.plan, 1, self.o, self.oo, stream)
+        if ev:
+            ev[3].record(stream)
+
+
+def d2d_gbs(torch, nbytes, reps=20):
+    """Flat device-to-device copy (cudaMemcpyAsync) of nbytes, counted as read + write."""
+    a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    b = torch.empty_like(a)
+    a.fill_(1)
+    for _ in range(3):
+        b.copy_(a)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(reps):
+        b.copy_(a)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / reps
+    del a, b
+    return 2 * nbytes / (ms * 1e-3) / 1e9
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def read_traffic(kernel: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if taken on the current source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(path) as f:
+            lines = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    except OSError:
+        return None
+    for parts in lines:
+        if len(parts) >= 4 and parts[0] == kernel:
+            src = os.path.join(ROOT, "ulysses_sequence_all_gb300", "csrc", parts[1])
+            try:
+                with open(src, "rb") as f:
+                    digest = hashlib.sha256(f.read()).hexdigest()[:16]
+            except OSError:
+                return None
+            return int(parts[3]) if digest == parts[2] else None
+    return None
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and --impl reference)
+# ------------------------------------------------------------------------------------------------
+def oracle_step_sample(tokens_per_rank: int, seed: int = 0):
+    """Inputs for one oracle step on the Wan geometry with `tokens_per_rank` tokens per rank."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    W, N, d = 8, 40, 128
+    seq = [tokens_per_rank] * W
+    heads = [5] * W
+    S = sum(seq)
+
+    def bf16(shape):  # bf16 bit patterns of N(0, 1) values
+        x = rng.standard_normal(shape, dtype=np.float32)
+        return (x.view(np.uint32) >> 16).astype(np.uint16)
+
+    q = [bf16((1, s, N, d)) for s in seq]
+    k = [bf16((1, s, N, d)) for s in seq]
+    v = [bf16((1, s, N, d)) for s in seq]
+    o = [bf16((1, S, n, d)) for n in heads]
+    w = 1.0 + 0.1 * rng.standard_normal((2, d))
+    return seq, heads, q, k, v, o, w
+
+
+def oracle_step(orc, sample):
+    seq, heads, q, k, v, o, w = sample
+    orc.qk_fused_A(q, seq, heads, w[0], EPS, THETA)
+    orc.qk_fused_A(k, seq, heads, w[1], EPS, THETA)
+    orc.a2a_4d(v, seq, heads, 0)
+    orc.a2a_4d(o, seq, heads, 1)
+
+
+def sample_bytes(tokens_per_rank: int) -> int:
+    side = 8 * tokens_per_rank * 40 * 128 * 2
+    return 4 * side + 2 * (2 * side)
+
+
+def cpu_baseline(budget_s: float = 15.0):
+    import oracle
+    orc = oracle.get()
+    t = 64
+    smp = oracle_step_sample(t)
+    t0 = time.perf_counter()
+    oracle_step(orc, smp)
+    per_token = (time.perf_counter() - t0) / t
+    tokens = max(64, min(9450, int(budget_s / max(per_token, 1e-9))))
+    smp = oracle_step_sample(tokens, seed=1)
+    t0 = time.perf_counter()
+    oracle_step(orc, smp)
+    dt = time.perf_counter() - t0
+    return {"value": round(sample_bytes(tokens) / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": (f"one step (fused q,k mode 0 + v mode 0 + o mode 1) on the Wan-720p geometry "
+                       f"with {tokens} of 9,450 tokens per rank (W=8, 40 heads, d=128, bf16), "
+                       f"single-threaded C oracle, {dt:.1f} s")}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    orc = oracle.get()
+    smp = oracle_step_sample(32)
+    t0 = time.perf_counter()
+    oracle_step(orc, smp)
+    per_token = (time.perf_counter() - t0) / 32
+    total_steps = args.steps + args.warmup
+    tokens = max(8, min(2048, int(60.0 / total_steps / max(per_token, 1e-9))))
+    smp = oracle_step_sample(tokens, seed=2)
+    for _ in range(args.warmup):
+        oracle_step(orc, smp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(orc, smp)
+    dt = time.perf_counter() - t0
+    value = sample_bytes(tokens) * args.steps / dt / 1e9
+    sample = (f"each step: fused q,k mode 0 + v mode 0 + o mode 1 on the Wan-720p geometry with "
+              f"{tokens} of 9,450 tokens per rank, single-threaded C oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(), "gpu_launches": 0,
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}))
+
+
+def workload_config():
+    return {"workload": "wan720p_ulysses_attention_exchange", "W": 8, "b": 1, "s_global": 75600,
+            "n_global": 40, "d": 128, "dtype": "bf16",
+            "step": "fused q,k RMSNorm+RoPE mode 0 + v mode 0 + attention-out mode 1",
+            "bytes_per_step": 8 * 774144000,
+            "l2": "inputs larger than L2 (774,144,000 B per tensor set vs 126 MB L2), no flush",
+            "parallelism": "replicas"}
+
+
+# ------------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    from ulysses_sequence_all_gb300 import binding as B
+    from ulysses_sequence_all_gb300 import workloads as wl
+
+    wk = Workload(torch, B, wl, "cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        wk.step(stream)
+    torch.cuda.synchronize()
+    assert B.ulysses_device_status() == 0
+
+    # per-kernel timing pass (events between launches, on the launching stream)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    kt = {"fused_qk": [], "mode0": [], "mode1": []}
+    for _ in range(min(args.steps, 50)):
+        wk.step(stream, ev)
+        torch.cuda.synchronize()
+        kt["fused_qk"].append(ev[0].elapsed_time(ev[1]))
+        kt["mode0"].append(ev[1].elapsed_time(ev[2]))
+        kt["mode1"].append(ev[2].elapsed_time(ev[3]))
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark("t0")
+    start.record(stream)
+    for _ in range(args.steps):
+        wk.step(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    if pg:
+        pg.barrier()
+    clock_info = clocks.stop()
+    ms = start.elapsed_time(end) / args.steps
+    if pg:
+        t = torch.tensor([ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    assert B.ulysses_device_status() == 0, "a kernel recorded a wait timeout"
+    value = wk.bytes_step * world / (ms * 1e-3) / 1e9
+
+    # end to end through the host-buffer entry points: pinned host in, device, pinned host out
+    e2e = run_e2e(torch, B, wk, stream, args)
+    if pg:
+        t = torch.tensor([e2e["ms_per_step"]], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e["ms_per_step"] = float(t.item())
+        e2e["value"] = round(wk.bytes_step * world / (e2e["ms_per_step"] * 1e-3) / 1e9, 3)
+
+    med = {k: statistics.median(v) for k, v in kt.items()}
+    gbs = {"fused_qk": wk.bytes_fused / (med["fused_qk"] * 1e-3) / 1e9,
+           "mode0": wk.bytes_plain / (med["mode0"] * 1e-3) / 1e9,
+           "mode1": wk.bytes_plain / (med["mode1"] * 1e-3) / 1e9}
+    dominant = max(med, key=lambda k: med[k])
+    peak, peak_kind = read_peaks()
+    kernel_name = {"fused_qk": "fused_qk_kernel", "mode0": "relayout_tma_kernel<0>",
+                   "mode1": "relayout_tma_kernel<1>"}[dominant]
+    traffic = read_traffic(kernel_name)
+    d2d = d2d_gbs(torch, wk.side) if rank == 0 else None
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, Wan-720p-shaped; no dataset)",
+        "config": workload_config(),
+        "clocks": clock_info,
+        "e2e": {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
+        "gpu_launches": wk.launches_per_step * args.steps,
+        "roofline": {"bound": "hbm", "kernel": kernel_name,
+                     "achieved": round(gbs[dominant], 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs[dominant] / peak, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": {"fused_qk": wk.bytes_fused,
+                                                      "mode0": wk.bytes_plain,
+                                                      "mode1": wk.bytes_plain}[dominant]},
+        "kernels": {k: {"median_ms": round(med[k], 4), "GB/s": round(gbs[k], 1),
+                        "frac_of_peak": round(gbs[k] / peak, 4),
+                        "frac_of_d2d": round(gbs[k] / d2d, 4) if d2d else None} for k in med},
+        "d2d_copy_GBps": round(d2d, 1) if d2d else None,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def run_e2e(torch, B, wk, stream, args):
+    """The same step with every input copied from pinned host memory and every output read
+    back into pinned host memory inside the timed region (host-buffer C ABI entry points)."""
+    pin = lambda ts: [t.cpu().pin_memory() for t in ts]  # noqa: E731
+    hq, hk, hv, ho = pin(wk.q), pin(wk.k), pin(wk.v), pin(wk.o)
+    hqo = [torch.empty_like(t, device="cpu").pin_memory() for t in wk.qo]
+    hko = [torch.empty_like(t, device="cpu").pin_memory() for t in wk.ko]
+    hvo = [torch.empty_like(t, device="cpu").pin_memory() for t in wk.vo]
+    hoo = [torch.empty_like(t, device="cpu").pin_memory() for t in wk.oo]
+
+    def step():
+        B.ulysses_a2a_4d_qk_fused_host(wk.plan, hq, hk, hqo, hko, wk.q, wk.k, wk.qo, wk.ko, wk.w,
+                                       EPS, THETA, stream)
+        B.ulysses_a2a_4d_host(wk.plan, 0, hv, hvo, wk.v, wk.vo, stream)
+        B.ulysses_a2a_4d_host(wk.plan, 1, ho, hoo, wk.o, wk.oo, stream)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(3, args.e2e_steps)
+    s.record(stream)
+    for _ in range(n):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    h2d = sum(t.numel() * t.element_size() for t in hq + hk + hv + ho)
+    d2h = sum(t.numel() * t.element_size() for t in hqo + hko + hvo + hoo)
+    return {"value": round(wk.bytes_step / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,189 @@
+/*
+ * ulysses.h -- C ABI of the GB300 Ulysses 4D sequence/head relayout library (libulysses.so).
+ *
+ * What the library computes (fast-ulysses 0.1.0, PyPI page, opening paragraph and "Quick start";
+ * fast-ulysses 0.2.1, README, "Quick start" and "API"): the all-to-all of Ulysses sequence
+ * parallelism on W ranks, here W virtual ranks on one GPU, each rank a separate device buffer.
+ * With s_q = seq_splits[q], n_r = head_splits[r], S = sum s_q, N = sum n_r,
+ * seq_off(q) = s_0 + ... + s_(q-1) and head_off(r) = n_0 + ... + n_(r-1):
+ *
+ *   mode 0  rank q's (b, s_q, N, d) tensor  ->  rank r's (b, S, n_r, d) tensor
+ *           out[r][bb][seq_off(q) + i][h][:] = in[q][bb][i][head_off(r) + h][:]
+ *   mode 1  the exact inverse on the same splits ("a second trades it back"):
+ *           out[q][bb][i][head_off(r) + h][:] = in[r][bb][seq_off(q) + i][h][:]
+ *
+ * Uneven shards (fast-ulysses 0.1.0, "What it does") are the general case; even splits are not a
+ * separate path. A split of zero is allowed (that rank contributes or receives nothing); S and N
+ * must be positive.
+ *
+ * Conventions shared by every entry point:
+ *  - Every function returns a status: ULY_OK (0) or a negative ULY_E* code; ulysses_strerror()
+ *    names it. Nothing is printed and nothing aborts.
+ *  - Tensors are dense, row-major (C order), as the shapes above state, with no padding.
+ *  - Device pointers are addresses on the current CUDA device, 16-byte aligned (ULY_EALIGN
+ *    otherwise). A pointer may be NULL only when that rank's tensor has zero bytes.
+ *  - The caller owns every buffer and keeps it alive until the work queued on `stream` has
+ *    finished. Pointer arrays (W entries each) are read during the call only.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Device work is
+ *    queued asynchronously; no call synchronises except ulysses_device_status().
+ *  - Calls allocate no memory. A plan holds only host memory and may be used by several host
+ *    threads at once for launches; ulysses_plan_set_chunk_bytes() must not race with launches.
+ *  - Input and output ranges must not overlap each other, and outputs must not overlap one another
+ *    (ULY_EOVERLAP).
+ *  - Kernels never spin without bound: a wait that exceeds its time limit sets a bit in a device
+ *    status word, read with ulysses_device_status().
+ */
+#ifndef ULYSSES_H
+#define ULYSSES_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum {
+    ULY_OK = 0,
+    ULY_EINVAL = -1,   /* bad argument: W, splits, b, d, dtype, mode, rank, NULL pointer */
+    ULY_EALIGN = -2,   /* a device pointer is not 16-byte aligned, or d * elem_size % 16 != 0 */
+    ULY_EOVERLAP = -3, /* an output range overlaps an input range or another output range */
+    ULY_ECHUNK = -4,   /* the chunk cap is smaller than one sequence row on some rank */
+    ULY_ECUDA = -5,    /* a CUDA runtime call failed; ulysses_last_cuda_error() has the code */
+    ULY_ENOMEM = -6,   /* host memory for a plan could not be allocated */
+    ULY_EDEVICE = -7   /* a kernel recorded a wait timeout in the device status word */
+};
+
+/* Element types (fast-ulysses 0.2.1, README, "Limits": float16 / bfloat16 / float32 /
+ * float8_e4m3fn / float8_e5m2 / int8 / uint8). The relayout moves bytes, so only the size
+ * matters to it; the fused QK call requires ULY_BF16. */
+enum {
+    ULY_U8 = 1,
+    ULY_F8E4M3 = 2,
+    ULY_F8E5M2 = 3,
+    ULY_I8 = 4,
+    ULY_F16 = 5,
+    ULY_BF16 = 6,
+    ULY_F32 = 7
+};
+
+/* Relayout engines: ULY_ENGINE_AUTO picks the fastest measured one. */
+enum { ULY_ENGINE_AUTO = 0, ULY_ENGINE_TMA = 1, ULY_ENGINE_VEC = 2 };
+
+typedef struct ulysses_plan_s* ulysses_plan_t;
+
+/*
+ * Build the host-side addressing plan (fast-ulysses 0.1.0, "What it does": the addressing is a
+ * host-side plan, testable without a GPU, with no launch configuration to tune).
+ *   W            number of ranks, 1..8 (fast-ulysses 0.1.0, "Limits": world_size in [1, 8],
+ *                odd sizes included).
+ *   b            batch, >= 1.
+ *   seq_splits   W entries s_q >= 0 with S = sum > 0 (host array, read during the call).
+ *   head_splits  W entries n_r >= 0 with N = sum > 0 (host array, read during the call).
+ *   d            head dimension; d * elem_size must be a multiple of 16 (fast-ulysses 0.2.1,
+ *                "Limits": d * elem_size 16-byte aligned), else ULY_EALIGN.
+ *   dtype        one of ULY_U8 .. ULY_F32.
+ *   out          receives the plan; release it with ulysses_plan_destroy().
+ * Makes no CUDA call. The default chunk cap is 1 GiB (see ulysses_plan_set_chunk_bytes).
+ */
+int ulysses_plan(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits, int64_t d,
+                 int dtype, ulysses_plan_t* out);
+
+/* Release a plan (NULL is accepted). Work already queued with it is unaffected. */
+int ulysses_plan_destroy(ulysses_plan_t plan);
+
+/*
+ * Cap on the bytes any one rank reads or writes in one kernel launch (FastVideo, "Ulysses
+ * performance on GB200": each rank keeps at most 1 GiB of window storage and long sequences are
+ * exchanged in chunks). A call whose per-rank bytes exceed the cap is split into several launches
+ * along the sequence shards (the source sequence in mode 0, the destination sequence in mode 1);
+ * the result is identical to one launch. max_chunk_bytes >= 1; default 1 << 30.
+ */
+int ulysses_plan_set_chunk_bytes(ulysses_plan_t plan, int64_t max_chunk_bytes);
+
+/* Bytes of rank `rank`'s input and output tensors for `mode` (either pointer may be NULL). */
+int ulysses_plan_bytes(ulysses_plan_t plan, int mode, int rank, int64_t* in_bytes,
+                       int64_t* out_bytes);
+
+/* Number of launches a call in `mode` makes under the current chunk cap (ULY_ECHUNK when no
+ * split along whole sequence rows meets the cap). */
+int ulysses_plan_num_chunks(ulysses_plan_t plan, int mode, int64_t* n_chunks);
+
+/* Rows of each sequence shard that launch `chunk` covers: for q < W, rows
+ * [row_lo[q], row_lo[q] + row_count[q]) of shard q (host arrays of W entries). */
+int ulysses_plan_chunk_rows(ulysses_plan_t plan, int mode, int64_t chunk, int64_t* row_lo,
+                            int64_t* row_count);
+
+/*
+ * The relayout (fast-ulysses 0.2.1, README, "API": all_to_all_4d(x, mode, seq_splits,
+ * head_splits)), for all W ranks in one call.
+ *   mode     0 or 1 (see the top of this file).
+ *   in_ptrs  W device pointers; mode 0: rank q's (b, s_q, N, d), mode 1: rank r's (b, S, n_r, d).
+ *   out_ptrs W device pointers; mode 0: rank r's (b, S, n_r, d), mode 1: rank q's (b, s_q, N, d).
+ * Bit-exact byte move. Queues one kernel launch per chunk on `stream`.
+ */
+int ulysses_a2a_4d(ulysses_plan_t plan, int mode, const void* const* in_ptrs,
+                   void* const* out_ptrs, void* stream);
+
+/* Same as ulysses_a2a_4d with an explicit engine (ULY_ENGINE_*): TMA bulk copies through shared
+ * memory, or 16-byte vector loads and stores. Both give identical bytes. */
+int ulysses_a2a_4d_engine(ulysses_plan_t plan, int mode, int engine, const void* const* in_ptrs,
+                          void* const* out_ptrs, void* stream);
+
+/*
+ * Mode 0 with QK RMSNorm + RoPE applied inside the scatter (fast-ulysses 0.1.0, "Fusion
+ * examples"). For q and k separately, every head row x of d bf16 values at global sequence
+ * position p = seq_off(q) + i becomes
+ *     y = x / sqrt(mean(x^2) + eps) * w                  (w: rms_w[0][:] for q, rms_w[1][:] for k)
+ *     (y[2j], y[2j+1]) rotated by the angle p * rope_theta^(-2j/d), j < d/2
+ * computed in fp32 and rounded once to bf16 (nearest even), then placed where mode 0 puts it.
+ *   plan     must have dtype ULY_BF16 and d in {8, 16, 32, 64, 128, 256}; S < 2^24.
+ *   q_in, k_in     W device pointers, rank q's (b, s_q, N, d) bf16.
+ *   q_out, k_out   W device pointers, rank r's (b, S, n_r, d) bf16.
+ *   rms_w    device pointer to 2 * d fp32 values, q's weight then k's.
+ *   eps      > 0 or 0; rope_theta > 0.
+ * V and the attention output go through ulysses_a2a_4d (mode 0 / mode 1).
+ */
+int ulysses_a2a_4d_qk_fused(ulysses_plan_t plan, const void* const* q_in, const void* const* k_in,
+                            void* const* q_out, void* const* k_out, const float* rms_w, float eps,
+                            float rope_theta, void* stream);
+
+/*
+ * End-to-end form for host-resident data: on `stream`, copy each rank's input from host_in[k] to
+ * dev_in[k], run ulysses_a2a_4d, and copy each dev_out[k] back to host_out[k]. Host buffers should
+ * be page-locked for the copies to be asynchronous. Device buffers are the caller's, as above.
+ */
+int ulysses_a2a_4d_host(ulysses_plan_t plan, int mode, const void* const* host_in,
+                        void* const* host_out, void* const* dev_in, void* const* dev_out,
+                        void* stream);
+
+/*
+ * End-to-end form of ulysses_a2a_4d_qk_fused for host-resident q and k: on `stream`, copy each
+ * rank's q and k from host to the device buffers, run the fused call, and copy q_out and k_out
+ * back to the host. Same arguments and rules as the device form, plus the host buffers.
+ */
+int ulysses_a2a_4d_qk_fused_host(ulysses_plan_t plan, const void* const* q_host_in,
+                                 const void* const* k_host_in, void* const* q_host_out,
+                                 void* const* k_host_out, void* const* q_in, void* const* k_in,
+                                 void* const* q_out, void* const* k_out, const float* rms_w,
+                                 float eps, float rope_theta, void* stream);
+
+/* Synchronise the current device, then return in *status the device status word accumulated by
+ * this library's kernels since the last call (0 = no kernel timed out) and clear it. Returns
+ * ULY_EDEVICE when the word was non-zero. */
+int ulysses_device_status(unsigned* status);
+
+/* The cudaError_t value of the last ULY_ECUDA returned on this host thread (0 if none). */
+int ulysses_last_cuda_error(void);
+
+/* A static, human-readable name for a status code. */
+const char* ulysses_strerror(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int ulysses_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ULYSSES_H */

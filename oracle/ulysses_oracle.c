@@ -47,6 +47,16 @@ static int64_t offset_of(const int64_t* splits, int k)
     return s;
 }
 
+/* Copy one element of e bytes (a constant size per case, so the compiler inlines the copy). */
+static void copy_elem(uint8_t* dst, const uint8_t* src, int64_t e)
+{
+    switch (e) {
+        case 1: memcpy(dst, src, 1); break;
+        case 2: memcpy(dst, src, 2); break;
+        default: memcpy(dst, src, 4); break;
+    }
+}
+
 static int check_geometry(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
                           int64_t d)
 {
@@ -86,9 +96,9 @@ int orc_a2a_4d(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_
                             /* element index inside rank r's (b, S, n_r, d) tensor */
                             const int64_t head_side = ((bb * S + seq_off_q + i) * n_r + h) * d + j;
                             if (mode == 0)
-                                memcpy(out[r] + head_side * e, in[q] + seq_side * e, (size_t)e);
+                                copy_elem(out[r] + head_side * e, in[q] + seq_side * e, e);
                             else
-                                memcpy(out[q] + seq_side * e, in[r] + head_side * e, (size_t)e);
+                                copy_elem(out[q] + seq_side * e, in[r] + head_side * e, e);
                         }
         }
     }

@@ -32,11 +32,12 @@ MUTANTS = {
         ("for (int p = 0; p < k; ++p) s += splits[p];",
          "for (int p = 0; p <= k && p < 8; ++p) s += splits[p];")],
     "mode1_reads_wrong_rank": [
-        ("memcpy(out[q] + seq_side * e, in[r] + head_side * e, (size_t)e);",
-         "memcpy(out[q] + seq_side * e, in[q] + head_side * e, (size_t)e);")],
+        ("copy_elem(out[q] + seq_side * e, in[r] + head_side * e, e);",
+         "copy_elem(out[q] + seq_side * e, in[q] + head_side * e, e);")],
     "mode1_same_as_mode0": [
-        ("if (mode == 0)\n                                memcpy",
-         "if (mode == 0 || mode == 1)\n                                memcpy")],
+        ("if (mode == 0)\n                                copy_elem",
+         "if (mode == 0 || mode == 1)\n                                copy_elem")],
+    "element_copy_truncated": [("case 2: memcpy(dst, src, 2); break;", "case 2: memcpy(dst, src, 1); break;")],
     "source_query_drops_head_offset": [
         ("N + offset_of(head_splits, r) + h) * d + j;", "N + h) * d + j;")],
     "rmsnorm_drops_eps": [("sqrt(mean_sq + eps)", "sqrt(mean_sq)")],

@@ -5,13 +5,6 @@ The compute lives in ``libulysses.so`` (hand-written sm_103a kernels behind a C 
 ``include/ulysses.h``); ``binding`` marshals tensors and pointers into it. Importing this package
 does not load the library; the first call into ``binding`` does, and raises if it is missing.
 """
-from . import workloads  # noqa: F401  (pure-Python input generators)
+from . import binding, workloads  # noqa: F401
 
-__all__ = ["workloads", "binding"]
-
-
-def __getattr__(name):
-    if name == "binding":
-        from . import binding
-        return binding
-    raise AttributeError(name)
+__all__ = ["binding", "workloads"]

@@ -1,0 +1,208 @@
+"""Thin ctypes binding of libulysses.so: the C ABI of include/ulysses.h under the same names.
+
+Only argument marshalling happens here (torch tensors -> device pointers, Python lists -> C
+arrays, status codes -> exceptions); every step of the relayout runs in the library's kernels.
+Loading fails loudly when the library has not been built: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.environ.get("ULYSSES_LIBRARY", os.path.join(PKG, "libulysses.so"))
+
+ULY_OK, ULY_EINVAL, ULY_EALIGN, ULY_EOVERLAP, ULY_ECHUNK, ULY_ECUDA, ULY_ENOMEM, ULY_EDEVICE = (
+    0, -1, -2, -3, -4, -5, -6, -7)
+ULY_U8, ULY_F8E4M3, ULY_F8E5M2, ULY_I8, ULY_F16, ULY_BF16, ULY_F32 = 1, 2, 3, 4, 5, 6, 7
+ULY_ENGINE_AUTO, ULY_ENGINE_TMA, ULY_ENGINE_VEC = 0, 1, 2
+
+DTYPE_CODES = {"uint8": ULY_U8, "float8_e4m3fn": ULY_F8E4M3, "float8_e5m2": ULY_F8E5M2,
+               "int8": ULY_I8, "float16": ULY_F16, "bfloat16": ULY_BF16, "float32": ULY_F32}
+
+# Every symbol include/ulysses.h declares.
+EXPORTS = ["ulysses_plan", "ulysses_plan_destroy", "ulysses_plan_set_chunk_bytes",
+           "ulysses_plan_bytes", "ulysses_plan_num_chunks", "ulysses_plan_chunk_rows",
+           "ulysses_a2a_4d", "ulysses_a2a_4d_engine", "ulysses_a2a_4d_qk_fused",
+           "ulysses_a2a_4d_host", "ulysses_a2a_4d_qk_fused_host", "ulysses_device_status", "ulysses_last_cuda_error",
+           "ulysses_strerror", "ulysses_version"]
+
+
+class UlyssesError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = _lib().ulysses_strerror(status).decode()
+        if status == ULY_ECUDA:
+            msg += f" (cudaError {_lib().ulysses_last_cuda_error()})"
+        super().__init__(f"{what}: {msg} [{status}]" if what else f"{msg} [{status}]")
+
+
+_LIB = None
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_pp = ctypes.POINTER(ctypes.c_void_p)
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIBRARY):
+            raise RuntimeError(f"libulysses.so is not built ({LIBRARY}); run "
+                               "`python -m ulysses_sequence_all_gb300.build` first")
+        lib = ctypes.CDLL(LIBRARY)
+        lib.ulysses_plan.argtypes = [ctypes.c_int, _i64, ctypes.POINTER(_i64), ctypes.POINTER(_i64),
+                                     _i64, ctypes.c_int, ctypes.POINTER(_p)]
+        lib.ulysses_plan_destroy.argtypes = [_p]
+        lib.ulysses_plan_set_chunk_bytes.argtypes = [_p, _i64]
+        lib.ulysses_plan_bytes.argtypes = [_p, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_i64),
+                                           ctypes.POINTER(_i64)]
+        lib.ulysses_plan_num_chunks.argtypes = [_p, ctypes.c_int, ctypes.POINTER(_i64)]
+        lib.ulysses_plan_chunk_rows.argtypes = [_p, ctypes.c_int, _i64, ctypes.POINTER(_i64),
+                                                ctypes.POINTER(_i64)]
+        lib.ulysses_a2a_4d.argtypes = [_p, ctypes.c_int, _pp, _pp, _p]
+        lib.ulysses_a2a_4d_engine.argtypes = [_p, ctypes.c_int, ctypes.c_int, _pp, _pp, _p]
+        lib.ulysses_a2a_4d_qk_fused.argtypes = [_p, _pp, _pp, _pp, _pp, _p, ctypes.c_float,
+                                                ctypes.c_float, _p]
+        lib.ulysses_a2a_4d_host.argtypes = [_p, ctypes.c_int, _pp, _pp, _pp, _pp, _p]
+        lib.ulysses_a2a_4d_qk_fused_host.argtypes = [_p, _pp, _pp, _pp, _pp, _pp, _pp, _pp, _pp, _p,
+                                                     ctypes.c_float, ctypes.c_float, _p]
+        lib.ulysses_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.ulysses_last_cuda_error.argtypes = []
+        lib.ulysses_strerror.argtypes = [ctypes.c_int]
+        lib.ulysses_strerror.restype = ctypes.c_char_p
+        lib.ulysses_version.argtypes = []
+        for name in EXPORTS:
+            if name != "ulysses_strerror":
+                getattr(lib, name).restype = ctypes.c_int
+        _LIB = lib
+    return _LIB
+
+
+def library():
+    """The loaded ctypes library (raises if it has not been built)."""
+    return _lib()
+
+
+def _check(status: int, what: str):
+    if status != ULY_OK:
+        raise UlyssesError(status, what)
+
+
+def _addr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()  # torch.Tensor
+
+
+def _ptrs(xs: Sequence) -> ctypes.Array:
+    return (ctypes.c_void_p * len(xs))(*[_addr(x) for x in xs])
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream  # torch.cuda.Stream
+
+
+class Plan:
+    """Owns one ulysses_plan_t (host memory only)."""
+
+    def __init__(self, handle: int, W: int, b: int, seq_splits, head_splits, d: int, dtype: str):
+        self.handle = handle
+        self.W, self.b, self.d, self.dtype = W, b, d, dtype
+        self.seq_splits, self.head_splits = list(seq_splits), list(head_splits)
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _LIB is not None:
+            _LIB.ulysses_plan_destroy(self.handle)
+            self.handle = None
+
+    @property
+    def _as_parameter_(self):
+        return ctypes.c_void_p(self.handle)
+
+
+def ulysses_plan(W: int, b: int, seq_splits, head_splits, d: int, dtype: str) -> Plan:
+    out = ctypes.c_void_p()
+    code = DTYPE_CODES.get(dtype, dtype if isinstance(dtype, int) else -1)
+    _check(_lib().ulysses_plan(W, b, (_i64 * W)(*seq_splits), (_i64 * W)(*head_splits), d, code,
+                               ctypes.byref(out)), "ulysses_plan")
+    return Plan(out.value, W, b, seq_splits, head_splits, d, dtype)
+
+
+def ulysses_plan_set_chunk_bytes(plan: Plan, max_chunk_bytes: int):
+    _check(_lib().ulysses_plan_set_chunk_bytes(plan, max_chunk_bytes), "ulysses_plan_set_chunk_bytes")
+
+
+def ulysses_plan_bytes(plan: Plan, mode: int, rank: int):
+    i, o = _i64(), _i64()
+    _check(_lib().ulysses_plan_bytes(plan, mode, rank, ctypes.byref(i), ctypes.byref(o)),
+           "ulysses_plan_bytes")
+    return i.value, o.value
+
+
+def ulysses_plan_num_chunks(plan: Plan, mode: int = 0) -> int:
+    n = _i64()
+    _check(_lib().ulysses_plan_num_chunks(plan, mode, ctypes.byref(n)), "ulysses_plan_num_chunks")
+    return n.value
+
+
+def ulysses_plan_chunk_rows(plan: Plan, mode: int, chunk: int):
+    lo, cnt = (_i64 * plan.W)(), (_i64 * plan.W)()
+    _check(_lib().ulysses_plan_chunk_rows(plan, mode, chunk, lo, cnt), "ulysses_plan_chunk_rows")
+    return list(lo), list(cnt)
+
+
+def ulysses_a2a_4d(plan: Plan, mode: int, ins: Sequence, outs: Sequence, stream=None):
+    _check(_lib().ulysses_a2a_4d(plan, mode, _ptrs(ins), _ptrs(outs), _stream(stream)),
+           "ulysses_a2a_4d")
+
+
+def ulysses_a2a_4d_engine(plan: Plan, mode: int, engine: int, ins: Sequence, outs: Sequence,
+                          stream=None):
+    _check(_lib().ulysses_a2a_4d_engine(plan, mode, engine, _ptrs(ins), _ptrs(outs), _stream(stream)),
+           "ulysses_a2a_4d_engine")
+
+
+def ulysses_a2a_4d_qk_fused(plan: Plan, q_in, k_in, q_out, k_out, rms_w, eps: float,
+                            rope_theta: float, stream=None):
+    _check(_lib().ulysses_a2a_4d_qk_fused(plan, _ptrs(q_in), _ptrs(k_in), _ptrs(q_out), _ptrs(k_out),
+                                          _addr(rms_w), eps, rope_theta, _stream(stream)),
+           "ulysses_a2a_4d_qk_fused")
+
+
+def ulysses_a2a_4d_host(plan: Plan, mode: int, host_in, host_out, dev_in, dev_out, stream=None):
+    _check(_lib().ulysses_a2a_4d_host(plan, mode, _ptrs(host_in), _ptrs(host_out), _ptrs(dev_in),
+                                      _ptrs(dev_out), _stream(stream)), "ulysses_a2a_4d_host")
+
+
+def ulysses_a2a_4d_qk_fused_host(plan: Plan, q_host_in, k_host_in, q_host_out, k_host_out, q_in,
+                                 k_in, q_out, k_out, rms_w, eps: float, rope_theta: float,
+                                 stream=None):
+    _check(_lib().ulysses_a2a_4d_qk_fused_host(
+        plan, _ptrs(q_host_in), _ptrs(k_host_in), _ptrs(q_host_out), _ptrs(k_host_out), _ptrs(q_in),
+        _ptrs(k_in), _ptrs(q_out), _ptrs(k_out), _addr(rms_w), eps, rope_theta, _stream(stream)),
+        "ulysses_a2a_4d_qk_fused_host")
+
+
+def ulysses_device_status() -> int:
+    """Synchronise; return and clear the kernels' device status word (0 = no wait timed out)."""
+    st = ctypes.c_uint()
+    rc = _lib().ulysses_device_status(ctypes.byref(st))
+    if rc not in (ULY_OK, ULY_EDEVICE):
+        _check(rc, "ulysses_device_status")
+    return st.value
+
+
+def ulysses_strerror(status: int) -> str:
+    return _lib().ulysses_strerror(status).decode()
+
+
+def ulysses_version() -> int:
+    return _lib().ulysses_version()

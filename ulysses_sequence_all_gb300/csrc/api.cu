@@ -1,0 +1,399 @@
+// api.cu -- the extern "C" entry points declared in include/ulysses.h: argument checks, chunking,
+// argument blocks, launches. All device work goes to the caller's stream; nothing synchronises
+// except ulysses_device_status().
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/ulysses.h"
+#include "plan.h"
+
+namespace uly {
+int64_t relayout_unit_bytes(int engine);
+cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStream_t stream,
+                            int device, int sm_count);
+cudaError_t relayout_status(unsigned* status, bool clear);
+void fused_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages, uint32_t* stage_bytes);
+cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count);
+cudaError_t fused_status(unsigned* status, bool clear);
+}  // namespace uly
+
+using namespace uly;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e)
+{
+    t_last_cuda_error = int(e);
+    return ULY_ECUDA;
+}
+
+struct DeviceInfo {
+    int device;
+    int sm_count;
+};
+
+int current_device(DeviceInfo* info)
+{
+    static int sm_counts[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= 64) return ULY_EINVAL;
+    if (sm_counts[dev] == 0) {
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        sm_counts[dev] = sms;
+    }
+    info->device = dev;
+    info->sm_count = sm_counts[dev];
+    return ULY_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks W pointers against their sizes: present when non-empty, 16-byte aligned.
+int check_ptrs(const void* const* ptrs, const int64_t* bytes, int W)
+{
+    if (!ptrs) return ULY_EINVAL;
+    for (int k = 0; k < W; ++k) {
+        if (bytes[k] == 0) continue;
+        if (!ptrs[k]) return ULY_EINVAL;
+        if (!aligned16(ptrs[k])) return ULY_EALIGN;
+    }
+    return ULY_OK;
+}
+
+bool ranges_overlap(const void* a, int64_t na, const void* b, int64_t nb)
+{
+    if (na == 0 || nb == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + uintptr_t(nb) && b0 < a0 + uintptr_t(na);
+}
+
+// Outputs may overlap neither inputs nor each other (inputs may alias each other: they are read).
+int check_overlap(const void* const* in, const int64_t* in_bytes, int n_in, const void* const* out,
+                  const int64_t* out_bytes, int n_out)
+{
+    for (int o = 0; o < n_out; ++o) {
+        for (int i = 0; i < n_in; ++i)
+            if (ranges_overlap(out[o], out_bytes[o], in[i], in_bytes[i])) return ULY_EOVERLAP;
+        for (int o2 = o + 1; o2 < n_out; ++o2)
+            if (ranges_overlap(out[o], out_bytes[o], out[o2], out_bytes[o2])) return ULY_EOVERLAP;
+    }
+    return ULY_OK;
+}
+
+void side_bytes(const Plan& p, int mode, int64_t* in_b, int64_t* out_b)
+{
+    for (int k = 0; k < p.W; ++k) {
+        const int64_t sq = seq_side_bytes(p, k), hd = head_side_bytes(p, k);
+        in_b[k] = mode == 0 ? sq : hd;
+        out_b[k] = mode == 0 ? hd : sq;
+    }
+}
+
+int relayout_impl(const Plan& p, int mode, int engine, const void* const* in_ptrs,
+                  void* const* out_ptrs, cudaStream_t stream)
+{
+    if (mode != 0 && mode != 1) return ULY_EINVAL;
+    if (engine == ULY_ENGINE_AUTO) engine = ULY_ENGINE_TMA;
+    if (engine != ULY_ENGINE_TMA && engine != ULY_ENGINE_VEC) return ULY_EINVAL;
+    int64_t in_b[kMaxW], out_b[kMaxW];
+    side_bytes(p, mode, in_b, out_b);
+    int rc = check_ptrs(in_ptrs, in_b, p.W);
+    if (rc) return rc;
+    rc = check_ptrs(const_cast<const void* const*>(out_ptrs), out_b, p.W);
+    if (rc) return rc;
+    rc = check_overlap(in_ptrs, in_b, p.W, const_cast<const void* const*>(out_ptrs), out_b, p.W);
+    if (rc) return rc;
+    int64_t C = 0;
+    rc = num_chunks(p, &C);
+    if (rc) return rc;
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc) return rc;
+
+    RelayoutArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int k = 0; k < p.W; ++k) {
+        uint8_t* in = static_cast<uint8_t*>(const_cast<void*>(in_ptrs[k]));
+        uint8_t* out = static_cast<uint8_t*>(out_ptrs[k]);
+        a.seq_ptr[k] = mode == 0 ? in : out;
+        a.head_ptr[k] = mode == 0 ? out : in;
+    }
+    const int64_t unit_bytes = relayout_unit_bytes(engine);
+    for (int64_t c = 0; c < C; ++c) {
+        ChunkRows rows;
+        chunk_rows(p, C, c, &rows);
+        build_relayout_units(p, rows, unit_bytes, &a);
+        cudaError_t e = relayout_launch(a, mode, engine, stream, dev.device, dev.sm_count);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return ULY_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ulysses_plan(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits, int64_t d,
+                 int dtype, ulysses_plan_t* out)
+{
+    if (!out) return ULY_EINVAL;
+    *out = nullptr;
+    Plan p;
+    const int rc = plan_init(&p, W, b, seq_splits, head_splits, d, dtype);
+    if (rc) return rc;
+    ulysses_plan_s* h = new (std::nothrow) ulysses_plan_s;
+    if (!h) return ULY_ENOMEM;
+    h->p = p;
+    *out = h;
+    return ULY_OK;
+}
+
+int ulysses_plan_destroy(ulysses_plan_t plan)
+{
+    delete plan;
+    return ULY_OK;
+}
+
+int ulysses_plan_set_chunk_bytes(ulysses_plan_t plan, int64_t max_chunk_bytes)
+{
+    if (!plan || max_chunk_bytes < 1) return ULY_EINVAL;
+    plan->p.chunk_cap = max_chunk_bytes;
+    return ULY_OK;
+}
+
+int ulysses_plan_bytes(ulysses_plan_t plan, int mode, int rank, int64_t* in_bytes, int64_t* out_bytes)
+{
+    if (!plan || (mode != 0 && mode != 1) || rank < 0 || rank >= plan->p.W) return ULY_EINVAL;
+    const int64_t sq = seq_side_bytes(plan->p, rank), hd = head_side_bytes(plan->p, rank);
+    if (in_bytes) *in_bytes = mode == 0 ? sq : hd;
+    if (out_bytes) *out_bytes = mode == 0 ? hd : sq;
+    return ULY_OK;
+}
+
+int ulysses_plan_num_chunks(ulysses_plan_t plan, int mode, int64_t* n_chunks)
+{
+    if (!plan || !n_chunks || (mode != 0 && mode != 1)) return ULY_EINVAL;
+    return num_chunks(plan->p, n_chunks);
+}
+
+int ulysses_plan_chunk_rows(ulysses_plan_t plan, int mode, int64_t chunk, int64_t* row_lo,
+                            int64_t* row_count)
+{
+    if (!plan || !row_lo || !row_count || (mode != 0 && mode != 1)) return ULY_EINVAL;
+    int64_t C = 0;
+    const int rc = num_chunks(plan->p, &C);
+    if (rc) return rc;
+    if (chunk < 0 || chunk >= C) return ULY_EINVAL;
+    ChunkRows rows;
+    chunk_rows(plan->p, C, chunk, &rows);
+    for (int q = 0; q < plan->p.W; ++q) {
+        row_lo[q] = rows.lo[q];
+        row_count[q] = rows.cnt[q];
+    }
+    return ULY_OK;
+}
+
+int ulysses_a2a_4d(ulysses_plan_t plan, int mode, const void* const* in_ptrs, void* const* out_ptrs,
+                   void* stream)
+{
+    if (!plan) return ULY_EINVAL;
+    return relayout_impl(plan->p, mode, ULY_ENGINE_AUTO, in_ptrs, out_ptrs,
+                         static_cast<cudaStream_t>(stream));
+}
+
+int ulysses_a2a_4d_engine(ulysses_plan_t plan, int mode, int engine, const void* const* in_ptrs,
+                          void* const* out_ptrs, void* stream)
+{
+    if (!plan) return ULY_EINVAL;
+    return relayout_impl(plan->p, mode, engine, in_ptrs, out_ptrs, static_cast<cudaStream_t>(stream));
+}
+
+int ulysses_a2a_4d_qk_fused(ulysses_plan_t plan, const void* const* q_in, const void* const* k_in,
+                            void* const* q_out, void* const* k_out, const float* rms_w, float eps,
+                            float rope_theta, void* stream)
+{
+    if (!plan) return ULY_EINVAL;
+    const Plan& p = plan->p;
+    if (p.dtype != ULY_BF16) return ULY_EINVAL;
+    if (!(p.d == 8 || p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128 || p.d == 256))
+        return ULY_EINVAL;
+    if (p.S >= (int64_t(1) << 24)) return ULY_EINVAL;  // positions must be exact in fp32
+    if (!(eps >= 0.0f) || !(rope_theta > 0.0f)) return ULY_EINVAL;
+    if (!rms_w) return ULY_EINVAL;
+    if (!aligned16(rms_w)) return ULY_EALIGN;
+    int64_t in_b[kMaxW], out_b[kMaxW];
+    side_bytes(p, 0, in_b, out_b);
+    int rc;
+    if ((rc = check_ptrs(q_in, in_b, p.W)) || (rc = check_ptrs(k_in, in_b, p.W)) ||
+        (rc = check_ptrs(const_cast<const void* const*>(q_out), out_b, p.W)) ||
+        (rc = check_ptrs(const_cast<const void* const*>(k_out), out_b, p.W)))
+        return rc;
+    // all four tensor sets at once: 2W inputs (plus the weights) against 2W outputs
+    const void* ins[2 * kMaxW + 1];
+    int64_t ins_b[2 * kMaxW + 1];
+    const void* outs[2 * kMaxW];
+    int64_t outs_b[2 * kMaxW];
+    for (int k = 0; k < p.W; ++k) {
+        ins[k] = q_in[k];
+        ins[p.W + k] = k_in[k];
+        ins_b[k] = ins_b[p.W + k] = in_b[k];
+        outs[k] = q_out[k];
+        outs[p.W + k] = k_out[k];
+        outs_b[k] = outs_b[p.W + k] = out_b[k];
+    }
+    ins[2 * p.W] = rms_w;
+    ins_b[2 * p.W] = 2 * p.d * int64_t(sizeof(float));
+    rc = check_overlap(ins, ins_b, 2 * p.W + 1, outs, outs_b, 2 * p.W);
+    if (rc) return rc;
+    int64_t T = 0;
+    int stages = 0;
+    uint32_t stage_bytes = 0;
+    fused_geometry(p, &T, &stages, &stage_bytes);
+    if (stages == 0) return ULY_EINVAL;  // one token's q and k rows do not fit twice in smem
+    int64_t C = 0;
+    if ((rc = num_chunks(p, &C))) return rc;
+    DeviceInfo dev;
+    if ((rc = current_device(&dev))) return rc;
+
+    FusedArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int k = 0; k < p.W; ++k) {
+        a.q_in[k] = static_cast<const uint8_t*>(q_in[k]);
+        a.k_in[k] = static_cast<const uint8_t*>(k_in[k]);
+        a.q_out[k] = static_cast<uint8_t*>(q_out[k]);
+        a.k_out[k] = static_cast<uint8_t*>(k_out[k]);
+    }
+    a.rms_w = rms_w;
+    a.eps = eps;
+    a.stages = stages;
+    a.stage_bytes = stage_bytes;
+    rope_turns(p.d, double(rope_theta), a.turn_hi, a.turn_lo);
+    for (int64_t c = 0; c < C; ++c) {
+        ChunkRows rows;
+        chunk_rows(p, C, c, &rows);
+        build_fused_units(p, rows, T, &a);
+        cudaError_t e = fused_launch(a, static_cast<cudaStream_t>(stream), dev.device, dev.sm_count);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return ULY_OK;
+}
+
+int ulysses_a2a_4d_host(ulysses_plan_t plan, int mode, const void* const* host_in,
+                        void* const* host_out, void* const* dev_in, void* const* dev_out, void* stream)
+{
+    if (!plan || !host_in || !host_out || !dev_in || !dev_out) return ULY_EINVAL;
+    const Plan& p = plan->p;
+    if (mode != 0 && mode != 1) return ULY_EINVAL;
+    int64_t in_b[kMaxW], out_b[kMaxW];
+    side_bytes(p, mode, in_b, out_b);
+    for (int k = 0; k < p.W; ++k) {
+        if ((in_b[k] && !host_in[k]) || (out_b[k] && !host_out[k])) return ULY_EINVAL;
+    }
+    // validate the device side before queuing any copy
+    int rc = check_ptrs(const_cast<const void* const*>(dev_in), in_b, p.W);
+    if (rc) return rc;
+    rc = check_ptrs(const_cast<const void* const*>(dev_out), out_b, p.W);
+    if (rc) return rc;
+    rc = check_overlap(const_cast<const void* const*>(dev_in), in_b, p.W,
+                       const_cast<const void* const*>(dev_out), out_b, p.W);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int k = 0; k < p.W; ++k) {
+        if (!in_b[k]) continue;
+        cudaError_t e = cudaMemcpyAsync(dev_in[k], host_in[k], size_t(in_b[k]), cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    rc = relayout_impl(p, mode, ULY_ENGINE_AUTO, const_cast<const void* const*>(dev_in), dev_out, st);
+    if (rc) return rc;
+    for (int k = 0; k < p.W; ++k) {
+        if (!out_b[k]) continue;
+        cudaError_t e = cudaMemcpyAsync(host_out[k], dev_out[k], size_t(out_b[k]), cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return ULY_OK;
+}
+
+int ulysses_a2a_4d_qk_fused_host(ulysses_plan_t plan, const void* const* q_host_in,
+                                 const void* const* k_host_in, void* const* q_host_out,
+                                 void* const* k_host_out, void* const* q_in, void* const* k_in,
+                                 void* const* q_out, void* const* k_out, const float* rms_w,
+                                 float eps, float rope_theta, void* stream)
+{
+    if (!plan || !q_host_in || !k_host_in || !q_host_out || !k_host_out || !q_in || !k_in)
+        return ULY_EINVAL;
+    const Plan& p = plan->p;
+    int64_t in_b[kMaxW], out_b[kMaxW];
+    side_bytes(p, 0, in_b, out_b);
+    for (int k = 0; k < p.W; ++k) {
+        if ((in_b[k] && (!q_host_in[k] || !k_host_in[k])) ||
+            (out_b[k] && (!q_host_out[k] || !k_host_out[k])))
+            return ULY_EINVAL;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the device call validates everything device-side; check pointers before the first copy
+    int rc = check_ptrs(const_cast<const void* const*>(q_in), in_b, p.W);
+    if (!rc) rc = check_ptrs(const_cast<const void* const*>(k_in), in_b, p.W);
+    if (rc) return rc;
+    for (int k = 0; k < p.W; ++k) {
+        if (!in_b[k]) continue;
+        cudaError_t e = cudaMemcpyAsync(q_in[k], q_host_in[k], size_t(in_b[k]), cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(k_in[k], k_host_in[k], size_t(in_b[k]), cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    rc = ulysses_a2a_4d_qk_fused(plan, const_cast<const void* const*>(q_in),
+                                 const_cast<const void* const*>(k_in), q_out, k_out, rms_w, eps,
+                                 rope_theta, stream);
+    if (rc) return rc;
+    for (int k = 0; k < p.W; ++k) {
+        if (!out_b[k]) continue;
+        cudaError_t e = cudaMemcpyAsync(q_host_out[k], q_out[k], size_t(out_b[k]), cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(k_host_out[k], k_out[k], size_t(out_b[k]), cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return ULY_OK;
+}
+
+int ulysses_device_status(unsigned* status)
+{
+    if (!status) return ULY_EINVAL;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned a = 0, b = 0;
+    if ((e = relayout_status(&a, true)) != cudaSuccess) return cuda_fail(e);
+    if ((e = fused_status(&b, true)) != cudaSuccess) return cuda_fail(e);
+    *status = a | b;
+    return *status ? ULY_EDEVICE : ULY_OK;
+}
+
+int ulysses_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* ulysses_strerror(int status)
+{
+    switch (status) {
+        case ULY_OK: return "ok";
+        case ULY_EINVAL: return "invalid argument";
+        case ULY_EALIGN: return "misaligned pointer or d * elem_size not a multiple of 16";
+        case ULY_EOVERLAP: return "output range overlaps an input or another output";
+        case ULY_ECHUNK: return "chunk cap smaller than one sequence row";
+        case ULY_ECUDA: return "CUDA runtime error (see ulysses_last_cuda_error)";
+        case ULY_ENOMEM: return "out of host memory";
+        case ULY_EDEVICE: return "a kernel wait timed out (device status word set)";
+        default: return "unknown status";
+    }
+}
+
+int ulysses_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// plan.h -- host plan of the Ulysses 4D relayout and the by-value argument blocks its kernels
+// receive. Shared by plan.cpp (host only, no CUDA calls) and the .cu files.
+#pragma once
+#include <cstdint>
+
+namespace uly {
+
+constexpr int kMaxW = 8;
+constexpr int kMaxSeg = kMaxW * kMaxW;
+constexpr int kMaxFusedD = 256;
+
+struct Plan {
+    int W;
+    int dtype;
+    int64_t b, d, e;  // batch, head dim, element bytes
+    int64_t S, N;     // global sequence length, global head count
+    int64_t s[kMaxW], n[kMaxW];
+    int64_t seq_off[kMaxW + 1], head_off[kMaxW + 1];
+    int64_t chunk_cap;  // max bytes one rank reads or writes per launch
+};
+
+// Rows of each sequence shard covered by one launch.
+struct ChunkRows {
+    int64_t lo[kMaxW];
+    int64_t cnt[kMaxW];
+};
+
+int64_t elem_size_of(int dtype);  // 0 for an unknown dtype
+int plan_init(Plan* p, int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+              int64_t d, int dtype);  // ULY_* status
+int64_t seq_side_bytes(const Plan& p, int q);   // rank q's (b, s_q, N, d) tensor
+int64_t head_side_bytes(const Plan& p, int r);  // rank r's (b, S, n_r, d) tensor
+int num_chunks(const Plan& p, int64_t* n_chunks);  // ULY_OK or ULY_ECHUNK
+void chunk_rows(const Plan& p, int64_t n_chunks, int64_t chunk, ChunkRows* out);
+
+// ---- relayout kernels' argument block (passed by value, lives in the parameter bank) ----------
+// A work unit is a block of up to rows_per_unit[r] consecutive rows of one segment (q, r) and one
+// batch index, or, when one row's run (n_r * d * e bytes) exceeds unit_bytes, a unit_bytes-wide
+// piece of a single row. "Seq side" is rank q's (b, s_q, N, d) tensor (mode 0 reads it, mode 1
+// writes it); "head side" is rank r's (b, S, n_r, d) tensor.
+struct RelayoutArgs {
+    uint8_t* seq_ptr[kMaxW];
+    uint8_t* head_ptr[kMaxW];
+    int64_t s[kMaxW], seq_off[kMaxW], n[kMaxW], head_off[kMaxW];
+    int64_t row_lo[kMaxW], rows[kMaxW];          // this launch's rows of shard q
+    int64_t rows_per_unit[kMaxW], pieces[kMaxW];  // per destination head group r
+    int64_t unit_begin[kMaxSeg + 1];              // prefix of unit counts over g = q * W + r
+    int64_t S, N, b, d_bytes;
+    int64_t total_units;
+    int32_t W, unit_bytes;
+};
+
+// Fills the unit tables of `a` for one launch (pointers are set by the caller).
+void build_relayout_units(const Plan& p, const ChunkRows& rows, int64_t unit_bytes, RelayoutArgs* a);
+
+// ---- fused QK kernel's argument block ---------------------------------------------------------
+// A work unit is `tokens_per_unit` consecutive source rows (tokens) of one shard q and one batch
+// index; it covers all N heads of both q and k for those tokens.
+struct FusedArgs {
+    const uint8_t* q_in[kMaxW];
+    const uint8_t* k_in[kMaxW];
+    uint8_t* q_out[kMaxW];
+    uint8_t* k_out[kMaxW];
+    const float* rms_w;  // [2][d]
+    int64_t s[kMaxW], seq_off[kMaxW], n[kMaxW], head_off[kMaxW];
+    int64_t row_lo[kMaxW], rows[kMaxW];
+    int64_t unit_begin[kMaxW + 1];
+    int64_t S, N, b;
+    int64_t total_units;
+    int32_t W, d, tokens_per_unit, stages;
+    uint32_t stage_bytes;
+    float eps;
+    // theta^(-2j/d) / (2 pi) as an unevaluated sum hi + lo of two floats, j < d/2.
+    float turn_hi[kMaxFusedD / 2];
+    float turn_lo[kMaxFusedD / 2];
+};
+
+void build_fused_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_unit, FusedArgs* a);
+void rope_turns(int64_t d, double theta, float* turn_hi, float* turn_lo);
+
+}  // namespace uly
+
+struct ulysses_plan_s {
+    uly::Plan p;
+};

@@ -1,0 +1,273 @@
+// relayout.cu -- the Ulysses 4D sequence/head relayout kernels (modes 0 and 1).
+//
+// The relayout is a permutation of contiguous runs: for every segment (q, r) -- rank q's sequence
+// shard and rank r's head group -- and every batch index, row i of rank q's (b, s_q, N, d) tensor
+// holds at byte offset head_off(r) * d * e one run of n_r * d * e bytes, and that run is row
+// seq_off(q) + i of rank r's (b, S, n_r, d) tensor. On the head side consecutive rows of a
+// segment are adjacent, so a block of rows is one contiguous span there and a strided gather on
+// the sequence side (fast-ulysses 0.1.0, opening paragraph: the relayout is expressed as copy
+// strides instead of separate permute kernels).
+//
+// Two engines move the same work units:
+//  * TMA: a persistent grid, one warp per CTA, a ring of shared-memory stages. Each unit's rows
+//    come in through cp.async.bulk (one per strided run, or one for the contiguous span) that
+//    complete on the stage's mbarrier, and leave through cp.async.bulk stores. No thread touches
+//    the bytes; the SM only issues copies.
+//  * VEC: a grid-stride loop of warps, 16-byte vector loads (L1 no-allocate) and stores, several
+//    in flight per lane.
+#include <cuda_runtime.h>
+
+#include "../../include/ulysses.h"
+#include "plan.h"
+#include "ptx.cuh"
+
+namespace uly {
+
+static __device__ unsigned g_relayout_status;
+
+#ifndef ULY_TMA_UNIT_BYTES
+#define ULY_TMA_UNIT_BYTES 32768
+#endif
+#ifndef ULY_TMA_STAGES
+#define ULY_TMA_STAGES 6
+#endif
+#ifndef ULY_TMA_CTAS_PER_SM
+#define ULY_TMA_CTAS_PER_SM 1
+#endif
+#ifndef ULY_VEC_UNIT_BYTES
+#define ULY_VEC_UNIT_BYTES 16384
+#endif
+#ifndef ULY_VEC_UNROLL
+#define ULY_VEC_UNROLL 4
+#endif
+constexpr int kTmaBarrierBytes = 128;  // the stage barriers sit before the first stage
+constexpr int kVecThreads = 256;
+
+struct Unit {
+    int q, r;
+    int64_t bb, i0, nrows, col0, cols;
+};
+
+// Largest segment g with unit_begin[g] <= u; segments without units share a prefix value with
+// their successor, so the match always owns unit u.
+__device__ __forceinline__ int find_segment(const RelayoutArgs& a, int64_t u)
+{
+    int lo = 0, hi = a.W * a.W - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.unit_begin[mid] <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ Unit decode(const RelayoutArgs& a, int64_t u)
+{
+    Unit t;
+    const int g = find_segment(a, u);
+    t.q = g / a.W;
+    t.r = g - t.q * a.W;
+    const int64_t local = u - a.unit_begin[g];
+    const int64_t R = a.rows_per_unit[t.r];
+    const int64_t P = a.pieces[t.r];
+    const int64_t rows = a.rows[t.q];
+    const int64_t per_batch = ((rows + R - 1) / R) * P;
+    t.bb = local / per_batch;
+    const int64_t rem = local - t.bb * per_batch;
+    const int64_t blk = rem / P;
+    const int64_t piece = rem - blk * P;
+    const int64_t i0 = blk * R;
+    t.nrows = min(R, rows - i0);
+    t.i0 = a.row_lo[t.q] + i0;
+    const int64_t run = a.n[t.r] * a.d_bytes;
+    t.col0 = piece * a.unit_bytes;
+    t.cols = (P == 1) ? run : min(int64_t(a.unit_bytes), run - t.col0);
+    return t;
+}
+
+// Row k of unit t on rank q's (b, s_q, N, d) tensor.
+__device__ __forceinline__ uint8_t* seq_addr(const RelayoutArgs& a, const Unit& t, int64_t k)
+{
+    return a.seq_ptr[t.q] + ((t.bb * a.s[t.q] + t.i0 + k) * a.N + a.head_off[t.r]) * a.d_bytes + t.col0;
+}
+
+// Row k of unit t on rank r's (b, S, n_r, d) tensor (rows are adjacent: pitch n_r * d * e).
+__device__ __forceinline__ uint8_t* head_addr(const RelayoutArgs& a, const Unit& t, int64_t k)
+{
+    return a.head_ptr[t.r] + ((t.bb * a.S + a.seq_off[t.q] + t.i0 + k) * a.n[t.r]) * a.d_bytes +
+           t.col0;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(32, 1) relayout_tma_kernel(const __grid_constant__ RelayoutArgs a)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int K = ULY_TMA_STAGES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint8_t* stage0 = smem + kTmaBarrierBytes;
+    const int lane = threadIdx.x;
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    const int64_t n = first < a.total_units ? (a.total_units - 1 - first) / step + 1 : 0;
+    if (n == 0) return;
+    if (lane == 0) {
+        for (int s = 0; s < K; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    auto issue_load = [&](int64_t k) {
+        const Unit t = decode(a, first + k * step);
+        const int s = int(k % K);
+        uint8_t* dst = stage0 + size_t(s) * ULY_TMA_UNIT_BYTES;
+        const uint32_t bytes = uint32_t(t.nrows * t.cols);
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
+        __syncwarp();
+        if (MODE == 0) {  // strided runs of the sequence side, packed back to back
+            for (int64_t row = lane; row < t.nrows; row += 32)
+                bulk_g2s(dst + row * t.cols, seq_addr(a, t, row), uint32_t(t.cols), &full[s]);
+        } else {  // one contiguous span of the head side
+            if (lane == 0) bulk_g2s(dst, head_addr(a, t, 0), bytes, &full[s]);
+        }
+    };
+    auto issue_store = [&](int64_t k) {
+        const Unit t = decode(a, first + k * step);
+        const uint8_t* src = stage0 + size_t(k % K) * ULY_TMA_UNIT_BYTES;
+        if (MODE == 0) {
+            if (lane == 0) bulk_s2g(head_addr(a, t, 0), src, uint32_t(t.nrows * t.cols));
+        } else {
+            for (int64_t row = lane; row < t.nrows; row += 32)
+                bulk_s2g(seq_addr(a, t, row), src + row * t.cols, uint32_t(t.cols));
+        }
+        bulk_commit();
+    };
+
+    int64_t loaded = n < K - 1 ? n : K - 1;
+    for (int64_t k = 0; k < loaded; ++k) issue_load(k);
+    int64_t k = 0;
+    bool ok = true;
+    for (; k < n; ++k) {
+        const int s = int(k % K);
+        if (!mbar_wait_bounded(&full[s], uint32_t((k / K) & 1))) {
+            ok = false;
+            break;
+        }
+        issue_store(k);
+        if (loaded < n) {
+            // the next load reuses the stage of unit k - 1: its stores must have read it
+            bulk_wait_read<1>();
+            __syncwarp();
+            issue_load(loaded);
+            ++loaded;
+        }
+    }
+    if (!ok) {
+        if (lane == 0) atomicOr(&g_relayout_status, kStatusWaitTimeout);
+        for (int64_t j = k; j < loaded; ++j) {  // let every load still in flight land
+            if (!mbar_wait_bounded(&full[j % K], uint32_t((j / K) & 1))) {
+                if (lane == 0) atomicOr(&g_relayout_status, kStatusDrainTimeout);
+                break;
+            }
+        }
+    }
+    bulk_wait<0>();
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kVecThreads) relayout_vec_kernel(const __grid_constant__ RelayoutArgs a)
+{
+    constexpr int U = ULY_VEC_UNROLL;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t u = warp; u < a.total_units; u += nwarps) {
+        const Unit t = decode(a, u);
+        const uint8_t* seq0 = seq_addr(a, t, 0);
+        const uint8_t* head0 = head_addr(a, t, 0);
+        const int64_t seq_pitch = a.N * a.d_bytes;
+        const int64_t head_pitch = a.n[t.r] * a.d_bytes;
+        const uint8_t* src = MODE == 0 ? seq0 : head0;
+        uint8_t* dst = const_cast<uint8_t*>(MODE == 0 ? head0 : seq0);
+        const int64_t src_pitch = MODE == 0 ? seq_pitch : head_pitch;
+        const int64_t dst_pitch = MODE == 0 ? head_pitch : seq_pitch;
+        const uint32_t vpr = uint32_t(t.cols >> 4);  // 16-byte vectors per row
+        const uint32_t total = uint32_t(t.nrows) * vpr;
+        // lane's (row, vector) and its advance per 32 vectors, kept without per-step division
+        uint32_t k = lane / vpr, c = lane % vpr;
+        const uint32_t dk = 32 / vpr, dc = 32 % vpr;
+        for (uint32_t v0 = 0; v0 < total; v0 += 32 * U) {
+            uint4 buf[U];
+            uint32_t kk[U], cc[U];
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                kk[j] = k;
+                cc[j] = c;
+                if (v0 + j * 32 + lane < total) buf[j] = ld_stream_v4(src + k * src_pitch + c * 16);
+                k += dk;
+                c += dc;
+                if (c >= vpr) {
+                    c -= vpr;
+                    k += 1;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < U; ++j)
+                if (v0 + j * 32 + lane < total) st_v4(dst + kk[j] * dst_pitch + cc[j] * 16, buf[j]);
+        }
+    }
+}
+
+int64_t relayout_unit_bytes(int engine) { return engine == ULY_ENGINE_VEC ? ULY_VEC_UNIT_BYTES : ULY_TMA_UNIT_BYTES; }
+
+static int g_smem_set[64];
+
+cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStream_t stream,
+                            int device, int sm_count)
+{
+    if (a.total_units == 0) return cudaSuccess;
+    if (engine == ULY_ENGINE_VEC) {
+        static int blocks_per_sm = 0;
+        if (blocks_per_sm == 0) {
+            int nb = 0;
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, relayout_vec_kernel<0>, kVecThreads, 0);
+            blocks_per_sm = nb > 0 ? nb : 1;
+        }
+        const int64_t warps_needed = a.total_units;
+        int64_t grid = int64_t(sm_count) * blocks_per_sm;
+        const int64_t max_grid = (warps_needed * 32 + kVecThreads - 1) / kVecThreads;
+        if (grid > max_grid) grid = max_grid;
+        if (mode == 0)
+            relayout_vec_kernel<0><<<unsigned(grid), kVecThreads, 0, stream>>>(a);
+        else
+            relayout_vec_kernel<1><<<unsigned(grid), kVecThreads, 0, stream>>>(a);
+        return cudaGetLastError();
+    }
+    const int smem = kTmaBarrierBytes + ULY_TMA_STAGES * ULY_TMA_UNIT_BYTES;
+    if (device >= 0 && device < 64 && !g_smem_set[device]) {
+        cudaError_t e0 = cudaFuncSetAttribute(relayout_tma_kernel<0>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e1 = cudaFuncSetAttribute(relayout_tma_kernel<1>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e0 != cudaSuccess) return e0;
+        if (e1 != cudaSuccess) return e1;
+        g_smem_set[device] = 1;
+    }
+    int64_t grid = int64_t(sm_count) * ULY_TMA_CTAS_PER_SM;
+    if (grid > a.total_units) grid = a.total_units;
+    if (mode == 0)
+        relayout_tma_kernel<0><<<unsigned(grid), 32, smem, stream>>>(a);
+    else
+        relayout_tma_kernel<1><<<unsigned(grid), 32, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t relayout_status(unsigned* status, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_relayout_status, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_relayout_status, &zero, sizeof(unsigned));
+}
+
+}  // namespace uly
