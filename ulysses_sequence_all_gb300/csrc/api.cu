@@ -16,6 +16,9 @@ int64_t relayout_unit_bytes(int engine);
 cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStream_t stream,
                             int device, int sm_count);
 cudaError_t relayout_status(unsigned* status, bool clear);
+int64_t relayout_tile_rows(int64_t row_bytes);
+cudaError_t relayout_rows_launch(const RowTileArgs& a, int mode, cudaStream_t stream, int device,
+                                 int sm_count);
 void fused_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages, uint32_t* stage_bytes);
 cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count);
 cudaError_t fused_status(unsigned* status, bool clear);
@@ -120,6 +123,26 @@ int relayout_impl(const Plan& p, int mode, int engine, const void* const* in_ptr
     rc = current_device(&dev);
     if (rc) return rc;
 
+    // TMA engine: whole-row tiles when a row fits a stage, row-run segments otherwise
+    const int64_t tile_rows = engine == ULY_ENGINE_TMA ? relayout_tile_rows(p.N * p.d * p.e) : 0;
+    if (tile_rows > 0) {
+        RowTileArgs t;
+        std::memset(&t, 0, sizeof t);
+        for (int k = 0; k < p.W; ++k) {
+            uint8_t* in = static_cast<uint8_t*>(const_cast<void*>(in_ptrs[k]));
+            uint8_t* out = static_cast<uint8_t*>(out_ptrs[k]);
+            t.seq_ptr[k] = mode == 0 ? in : out;
+            t.head_ptr[k] = mode == 0 ? out : in;
+        }
+        for (int64_t c = 0; c < C; ++c) {
+            ChunkRows rows;
+            chunk_rows(p, C, c, &rows);
+            build_row_tiles(p, rows, tile_rows, &t);
+            cudaError_t e = relayout_rows_launch(t, mode, stream, dev.device, dev.sm_count);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        return ULY_OK;
+    }
     RelayoutArgs a;
     std::memset(&a, 0, sizeof a);
     for (int k = 0; k < p.W; ++k) {

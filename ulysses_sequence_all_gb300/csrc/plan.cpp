@@ -155,6 +155,31 @@ void build_relayout_units(const Plan& p, const ChunkRows& rows, int64_t unit_byt
     a->total_units = total;
 }
 
+void build_row_tiles(const Plan& p, const ChunkRows& rows, int64_t tile_rows, RowTileArgs* a)
+{
+    const int W = p.W;
+    a->W = W;
+    a->S = p.S;
+    a->N = p.N;
+    a->b = p.b;
+    a->d_bytes = p.d * p.e;
+    a->tile_rows = tile_rows;
+    int64_t total = 0;
+    for (int k = 0; k < kMaxW; ++k) {
+        const bool live = k < W;
+        a->s[k] = live ? p.s[k] : 0;
+        a->seq_off[k] = live ? p.seq_off[k] : 0;
+        a->n[k] = live ? p.n[k] : 0;
+        a->head_off[k] = live ? p.head_off[k] : 0;
+        a->row_lo[k] = live ? rows.lo[k] : 0;
+        a->rows[k] = live ? rows.cnt[k] : 0;
+        a->unit_begin[k] = total;
+        if (live) total += p.b * ceil_div(a->rows[k], tile_rows);
+    }
+    a->unit_begin[kMaxW] = total;
+    a->total_units = total;
+}
+
 void build_fused_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_unit, FusedArgs* a)
 {
     const int W = p.W;

@@ -53,6 +53,24 @@ struct RelayoutArgs {
 // Fills the unit tables of `a` for one launch (pointers are set by the caller).
 void build_relayout_units(const Plan& p, const ChunkRows& rows, int64_t unit_bytes, RelayoutArgs* a);
 
+// ---- row-tile relayout argument block ---------------------------------------------------------
+// A work unit is up to tile_rows consecutive rows (tokens) of one sequence shard q and one batch
+// index, with all N heads: on the sequence side one contiguous span of tile_rows * N * d * e bytes,
+// on the head side W contiguous spans (one per rank r, tile_rows * n_r * d * e bytes each). Used
+// when a whole row fits a shared-memory stage.
+struct RowTileArgs {
+    uint8_t* seq_ptr[kMaxW];
+    uint8_t* head_ptr[kMaxW];
+    int64_t s[kMaxW], seq_off[kMaxW], n[kMaxW], head_off[kMaxW];
+    int64_t row_lo[kMaxW], rows[kMaxW];
+    int64_t unit_begin[kMaxW + 1];  // prefix of unit counts over q
+    int64_t S, N, b, d_bytes;
+    int64_t tile_rows, total_units;
+    int32_t W;
+};
+
+void build_row_tiles(const Plan& p, const ChunkRows& rows, int64_t tile_rows, RowTileArgs* a);
+
 // ---- fused QK kernel's argument block ---------------------------------------------------------
 // A work unit is `tokens_per_unit` consecutive source rows (tokens) of one shard q and one batch
 // index; it covers all N heads of both q and k for those tokens.

@@ -174,6 +174,137 @@ __global__ void __launch_bounds__(32, 1) relayout_tma_kernel(const __grid_consta
     bulk_wait<0>();
 }
 
+// ---- row tiles: whole rows through shared memory ------------------------------------------------
+// Unit = up to tile_rows consecutive rows of shard q, batch bb. Shared memory holds the rows in
+// their sequence-side layout (row i, all N heads). Mode 0: one bulk load of the contiguous
+// sequence-side span, then one bulk store per (row, destination rank) run; the runs of one rank
+// are adjacent in its tensor, so each rank receives one contiguous span per unit. Mode 1 mirrors
+// this: one bulk load per (row, source rank) run, one bulk store of the contiguous span. Both
+// sides are therefore streamed in long sequential spans across the grid.
+struct RowTile {
+    int q;
+    int64_t bb, i0, nrows;
+};
+
+__device__ __forceinline__ RowTile decode_rows(const RowTileArgs& a, int64_t u)
+{
+    int lo = 0, hi = a.W - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.unit_begin[mid] <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    RowTile t;
+    t.q = lo;
+    const int64_t T = a.tile_rows;
+    const int64_t rows = a.rows[lo];
+    const int64_t blocks = (rows + T - 1) / T;
+    const int64_t local = u - a.unit_begin[lo];
+    t.bb = local / blocks;
+    const int64_t blk = local - t.bb * blocks;
+    t.i0 = a.row_lo[lo] + blk * T;
+    t.nrows = min(T, rows - blk * T);
+    return t;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(32, 1) relayout_rows_kernel(const __grid_constant__ RowTileArgs a)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int K = ULY_TMA_STAGES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint8_t* stage0 = smem + kTmaBarrierBytes;
+    const int lane = threadIdx.x;
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    const int64_t n = first < a.total_units ? (a.total_units - 1 - first) / step + 1 : 0;
+    if (n == 0) return;
+    if (lane == 0) {
+        for (int s = 0; s < K; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    const int W = a.W;
+    const int64_t row_bytes = a.N * a.d_bytes;
+
+    // sequence side: nrows whole rows, contiguous
+    auto seq_span = [&](const RowTile& t) {
+        return a.seq_ptr[t.q] + (t.bb * a.s[t.q] + t.i0) * row_bytes;
+    };
+    // head side of rank r: nrows runs of n_r * d * e bytes, contiguous
+    auto head_span = [&](const RowTile& t, int r) {
+        return a.head_ptr[r] + (t.bb * a.S + a.seq_off[t.q] + t.i0) * a.n[r] * a.d_bytes;
+    };
+
+    auto issue_load = [&](int64_t k) {
+        const RowTile t = decode_rows(a, first + k * step);
+        const int s = int(k % K);
+        uint8_t* stage = stage0 + size_t(s) * ULY_TMA_UNIT_BYTES;
+        const uint32_t bytes = uint32_t(t.nrows * row_bytes);
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
+        __syncwarp();
+        if (MODE == 0) {
+            if (lane == 0) bulk_g2s(stage, seq_span(t), bytes, &full[s]);
+        } else {
+            const int pairs = int(t.nrows) * W;
+            for (int idx = lane; idx < pairs; idx += 32) {
+                const int i = idx / W, r = idx - (idx / W) * W;
+                const int64_t run = a.n[r] * a.d_bytes;
+                if (run == 0) continue;
+                bulk_g2s(stage + i * row_bytes + a.head_off[r] * a.d_bytes, head_span(t, r) + i * run,
+                         uint32_t(run), &full[s]);
+            }
+        }
+    };
+    auto issue_store = [&](int64_t k) {
+        const RowTile t = decode_rows(a, first + k * step);
+        const uint8_t* stage = stage0 + size_t(k % K) * ULY_TMA_UNIT_BYTES;
+        if (MODE == 0) {
+            const int pairs = int(t.nrows) * W;
+            for (int idx = lane; idx < pairs; idx += 32) {
+                const int i = idx / W, r = idx - (idx / W) * W;
+                const int64_t run = a.n[r] * a.d_bytes;
+                if (run == 0) continue;
+                bulk_s2g(head_span(t, r) + i * run, stage + i * row_bytes + a.head_off[r] * a.d_bytes,
+                         uint32_t(run));
+            }
+        } else {
+            if (lane == 0) bulk_s2g(seq_span(t), stage, uint32_t(t.nrows * row_bytes));
+        }
+        bulk_commit();
+    };
+
+    int64_t loaded = n < K - 1 ? n : K - 1;
+    for (int64_t k = 0; k < loaded; ++k) issue_load(k);
+    int64_t k = 0;
+    bool ok = true;
+    for (; k < n; ++k) {
+        const int s = int(k % K);
+        if (!mbar_wait_bounded(&full[s], uint32_t((k / K) & 1))) {
+            ok = false;
+            break;
+        }
+        issue_store(k);
+        if (loaded < n) {
+            bulk_wait_read<1>();  // stores of unit k - 1 have left the stage about to be refilled
+            __syncwarp();
+            issue_load(loaded);
+            ++loaded;
+        }
+    }
+    if (!ok) {
+        if (lane == 0) atomicOr(&g_relayout_status, kStatusWaitTimeout);
+        for (int64_t j = k; j < loaded; ++j) {
+            if (!mbar_wait_bounded(&full[j % K], uint32_t((j / K) & 1))) {
+                if (lane == 0) atomicOr(&g_relayout_status, kStatusDrainTimeout);
+                break;
+            }
+        }
+    }
+    bulk_wait<0>();
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kVecThreads) relayout_vec_kernel(const __grid_constant__ RelayoutArgs a)
 {
@@ -222,6 +353,23 @@ int64_t relayout_unit_bytes(int engine) { return engine == ULY_ENGINE_VEC ? ULY_
 
 static int g_smem_set[64];
 
+static cudaError_t ensure_tma_smem(int device, int smem)
+{
+    if (device < 0 || device >= 64 || g_smem_set[device]) return cudaSuccess;
+    const void* kernels[] = {reinterpret_cast<const void*>(relayout_tma_kernel<0>),
+                             reinterpret_cast<const void*>(relayout_tma_kernel<1>),
+                             reinterpret_cast<const void*>(relayout_rows_kernel<0>),
+                             reinterpret_cast<const void*>(relayout_rows_kernel<1>)};
+    for (const void* k : kernels) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+    }
+    g_smem_set[device] = 1;
+    return cudaSuccess;
+}
+
+constexpr int kTmaSmem = kTmaBarrierBytes + ULY_TMA_STAGES * ULY_TMA_UNIT_BYTES;
+
 cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStream_t stream,
                             int device, int sm_count)
 {
@@ -243,22 +391,35 @@ cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStr
             relayout_vec_kernel<1><<<unsigned(grid), kVecThreads, 0, stream>>>(a);
         return cudaGetLastError();
     }
-    const int smem = kTmaBarrierBytes + ULY_TMA_STAGES * ULY_TMA_UNIT_BYTES;
-    if (device >= 0 && device < 64 && !g_smem_set[device]) {
-        cudaError_t e0 = cudaFuncSetAttribute(relayout_tma_kernel<0>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        cudaError_t e1 = cudaFuncSetAttribute(relayout_tma_kernel<1>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e0 != cudaSuccess) return e0;
-        if (e1 != cudaSuccess) return e1;
-        g_smem_set[device] = 1;
-    }
+    cudaError_t e = ensure_tma_smem(device, kTmaSmem);
+    if (e != cudaSuccess) return e;
     int64_t grid = int64_t(sm_count) * ULY_TMA_CTAS_PER_SM;
     if (grid > a.total_units) grid = a.total_units;
     if (mode == 0)
-        relayout_tma_kernel<0><<<unsigned(grid), 32, smem, stream>>>(a);
+        relayout_tma_kernel<0><<<unsigned(grid), 32, kTmaSmem, stream>>>(a);
     else
-        relayout_tma_kernel<1><<<unsigned(grid), 32, smem, stream>>>(a);
+        relayout_tma_kernel<1><<<unsigned(grid), 32, kTmaSmem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+// Rows per tile for the row-tile kernel, 0 when one row does not fit a stage.
+int64_t relayout_tile_rows(int64_t row_bytes)
+{
+    return row_bytes <= ULY_TMA_UNIT_BYTES ? ULY_TMA_UNIT_BYTES / row_bytes : 0;
+}
+
+cudaError_t relayout_rows_launch(const RowTileArgs& a, int mode, cudaStream_t stream, int device,
+                                 int sm_count)
+{
+    if (a.total_units == 0) return cudaSuccess;
+    cudaError_t e = ensure_tma_smem(device, kTmaSmem);
+    if (e != cudaSuccess) return e;
+    int64_t grid = int64_t(sm_count) * ULY_TMA_CTAS_PER_SM;
+    if (grid > a.total_units) grid = a.total_units;
+    if (mode == 0)
+        relayout_rows_kernel<0><<<unsigned(grid), 32, kTmaSmem, stream>>>(a);
+    else
+        relayout_rows_kernel<1><<<unsigned(grid), 32, kTmaSmem, stream>>>(a);
     return cudaGetLastError();
 }
 

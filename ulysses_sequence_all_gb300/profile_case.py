@@ -1,0 +1,60 @@
+"""Profiling harness: runs the library's kernels on one workload a few times, for ncu captures.
+
+    python -m ulysses_sequence_all_gb300.profile_case --kernel all --workload wan --iters 2
+
+Allocates only what the chosen kernels need (the Wan-720p shape: 774,144,000 bytes per tensor
+set, about 3.1 GB for the fused call's inputs and outputs), launches each kernel `iters` times,
+synchronises and checks the device status word. It reports no timing.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import binding as B
+from . import workloads as wl
+
+WORKLOADS = {"wan": wl.WAN, "long": wl.LONG_QKV, "tiny": wl.TINY}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--kernel", choices=["fused", "mode0", "mode1", "all"], default="all")
+    ap.add_argument("--engine", choices=["tma", "vec"], default="tma")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="wan")
+    ap.add_argument("--iters", type=int, default=2)
+    args = ap.parse_args()
+    cfg = WORKLOADS[args.workload]
+    engine = B.ULY_ENGINE_TMA if args.engine == "tma" else B.ULY_ENGINE_VEC
+    plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
+    dt = wl.torch_dtype(cfg.dtype)
+    head = [torch.empty(cfg.head_side_shape(r), dtype=dt, device="cuda") for r in range(cfg.W)]
+    if args.kernel in ("mode0", "all"):
+        x = wl.seq_side_inputs(cfg, "cuda")
+        for _ in range(args.iters):
+            B.ulysses_a2a_4d_engine(plan, 0, engine, x, head)
+        torch.cuda.synchronize()
+        del x
+    if args.kernel in ("mode1", "all"):
+        y = wl.head_side_inputs(cfg, "cuda")
+        seq = [torch.empty(cfg.seq_side_shape(q), dtype=dt, device="cuda") for q in range(cfg.W)]
+        for _ in range(args.iters):
+            B.ulysses_a2a_4d_engine(plan, 1, engine, y, seq)
+        torch.cuda.synchronize()
+        del y, seq
+    if args.kernel in ("fused", "all"):
+        q = wl.seq_side_inputs(cfg, "cuda", seed=3)
+        k = wl.seq_side_inputs(cfg, "cuda", seed=4)
+        w = wl.rms_weights(cfg.d).cuda()
+        ko = [torch.empty_like(t) for t in head]
+        for _ in range(args.iters):
+            B.ulysses_a2a_4d_qk_fused(plan, q, k, head, ko, w, 1e-6, 1e4)
+        torch.cuda.synchronize()
+    status = B.ulysses_device_status()
+    if status:
+        raise SystemExit(f"device status word {status:#x}")
+
+
+if __name__ == "__main__":
+    main()
