@@ -5,18 +5,21 @@
 //     y = x / sqrt(mean(x^2) + eps) * w,   (y[2j], y[2j+1]) rotated by p * theta^(-2j/d),
 // in fp32, rounded once to bf16 (nearest even), and written where mode 0 places the row.
 //
-// Structure: a persistent grid with one CTA per SM and a ring of shared-memory stages.
-//  * Warp 0 produces. Per work unit (a few consecutive tokens of one source rank: all N heads of
-//    q and of k, two contiguous spans) its lanes first fill the stage's cos/sin table for those
-//    tokens' positions, then lane 0 starts the two cp.async.bulk loads. All 32 lanes arrive on
+// Structure: a persistent grid with one CTA per SM and a ring of K shared-memory stages.
+//  * Warp 0 moves data. Per work unit (a few consecutive tokens of one source rank: all N heads
+//    of q and of k, two contiguous spans) its lanes fill the stage's cos/sin table for those
+//    tokens' positions, then lane 0 starts the two cp.async.bulk loads; all 32 lanes arrive on
 //    the stage's "full" mbarrier (lane 0 with the expected transaction bytes), so a consumer that
-//    sees the phase complete sees both the table and the data.
+//    sees the phase complete sees both the table and the data. When the consumers report a unit
+//    done on its "computed" mbarrier, the lanes issue one cp.async.bulk store per (token, q|k,
+//    destination rank): n_r heads that are contiguous in the stage and in the destination.
+//    Loads run K - kFusedDrain units ahead; a stage is refilled once the stores that last read it
+//    (kFusedDrain bulk groups back) have finished reading shared memory.
 //  * The consumer warps split a stage's head rows into contiguous ranges. A group of d/8 lanes
 //    holds one head row (8 values per lane) and each group keeps two rows in flight; the sum of
 //    squares is reduced with xor shuffles inside the group, the weight and rotation are applied in
-//    registers, and each lane stores 16 bytes straight to the destination rank (a head row is one
-//    contiguous 2d-byte span there). Each consumer warp then arrives on the stage's "empty"
-//    mbarrier so the producer can refill it.
+//    registers, and the bf16 result overwrites its input in shared memory. Each consumer warp then
+//    fences its writes for the async proxy and arrives on the stage's "computed" mbarrier.
 //
 // RoPE angles: p * theta^(-2j/d) reaches ~75,600 rad at the Wan shape, where an fp32 product
 // alone is off by ~5e-3 rad. The angle is formed in turns (units of 2 pi): the host supplies
@@ -35,21 +38,37 @@ namespace uly {
 
 static __device__ unsigned g_fused_status;
 
+#ifndef ULY_FUSED_CTAS_PER_SM
+#define ULY_FUSED_CTAS_PER_SM 3
+#endif
 #ifndef ULY_FUSED_CONSUMER_WARPS
-#define ULY_FUSED_CONSUMER_WARPS 16
+#define ULY_FUSED_CONSUMER_WARPS 4
 #endif
 #ifndef ULY_FUSED_STAGE_TARGET
-#define ULY_FUSED_STAGE_TARGET 40960
+#define ULY_FUSED_STAGE_TARGET 20480
 #endif
 #ifndef ULY_FUSED_MAX_STAGES
-#define ULY_FUSED_MAX_STAGES 4
+#define ULY_FUSED_MAX_STAGES 3
 #endif
+#ifndef ULY_FUSED_DRAIN
+#define ULY_FUSED_DRAIN 1
+#endif
+constexpr int kFusedCtasPerSm = ULY_FUSED_CTAS_PER_SM;
 constexpr int kFusedMaxStages = ULY_FUSED_MAX_STAGES;
-constexpr int kFusedSmemBudget = 210 * 1024;
-constexpr int kFusedHeader = 128;  // 2 * kFusedMaxStages barriers
-constexpr int kFusedThreads = 32 * (1 + ULY_FUSED_CONSUMER_WARPS);
-constexpr int kFusedMaxHeads = 1024;
-constexpr int kIlp = 2;  // head rows in flight per lane group
+constexpr int kFusedDrain = ULY_FUSED_DRAIN;  // store groups left draining when a stage refills
+// an SM holds 228 KiB of shared memory, 1 KiB of it reserved per resident CTA
+constexpr int kFusedSmemBudget = (227 * 1024) / kFusedCtasPerSm - 1024;
+constexpr int kFusedHeader = 256;  // three barriers per stage
+static_assert(3 * 8 * kFusedMaxStages <= kFusedHeader, "stage barriers must fit the header");
+static_assert(kFusedDrain >= 1 && kFusedDrain < kFusedMaxStages, "need a load in flight");
+static_assert(ULY_FUSED_CONSUMER_WARPS % 2 == 0, "consumer warps split evenly between q and k");
+// warp roles
+constexpr int kLoaderWarp = 0, kTableWarp = 1, kStorerWarp = 2, kFirstConsumerWarp = 3;
+constexpr int kFusedThreads = 32 * (kFirstConsumerWarp + ULY_FUSED_CONSUMER_WARPS);
+#ifndef ULY_FUSED_ILP
+#define ULY_FUSED_ILP 2
+#endif
+constexpr int kIlp = ULY_FUSED_ILP;  // head rows in flight per lane group
 
 struct FusedUnit {
     int q;
@@ -73,7 +92,7 @@ __device__ __forceinline__ FusedUnit fused_decode(const FusedArgs& a, int64_t u)
     const int64_t rows = a.rows[lo];
     const int64_t blocks = (rows + T - 1) / T;
     const int64_t local = u - a.unit_begin[lo];
-    t.bb = local / blocks;
+    t.bb = div_fast(local, blocks);
     const int64_t blk = local - t.bb * blocks;
     t.i0 = a.row_lo[lo] + blk * T;
     t.ntok = int(min(T, rows - blk * T));
@@ -104,21 +123,19 @@ __device__ __forceinline__ float2 rope_cos_sin(float p, float hi, float lo)
 // Shared-memory layout (byte offsets), shared by the kernel and its launcher.
 struct FusedSmem {
     int turns;      // float2 (hi, lo) per pair j < d/2
-    int heads;      // int per global head: destination rank << 16 | local head index
     int tables;     // per stage: float2 (cos, sin) per (token, pair)
     int stages;     // per stage: q span then k span
     int table_bytes;
     int total;
 };
 
-__host__ __device__ inline FusedSmem fused_smem_layout(int d, int64_t N, int tokens, int stages,
+__host__ __device__ inline FusedSmem fused_smem_layout(int d, int tokens, int stages,
                                                        uint32_t stage_bytes)
 {
     auto up = [](int x) { return (x + 127) & ~127; };
     FusedSmem m;
     m.turns = kFusedHeader;
-    m.heads = up(m.turns + (d / 2) * 8);
-    m.tables = up(m.heads + int(N) * 4);
+    m.tables = up(m.turns + (d / 2) * 8);
     m.table_bytes = up(tokens * (d / 2) * 8);
     m.stages = up(m.tables + stages * m.table_bytes);
     m.total = m.stages + stages * int(stage_bytes);
@@ -126,7 +143,8 @@ __host__ __device__ inline FusedSmem fused_smem_layout(int d, int64_t N, int tok
 }
 
 template <int G>  // lanes per head row; d = 8 * G
-__global__ void __launch_bounds__(kFusedThreads, 1) fused_qk_kernel(const __grid_constant__ FusedArgs a)
+__global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
+    fused_qk_kernel(const __grid_constant__ FusedArgs a)
 {
     constexpr int D = 8 * G;
     constexpr int HALF = D / 2;
@@ -136,87 +154,130 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_qk_kernel(const __grid
     extern __shared__ __align__(1024) uint8_t smem[];
     const int K = a.stages;
     const int N = int(a.N);
-    const FusedSmem L = fused_smem_layout(D, a.N, a.tokens_per_unit, K, a.stage_bytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + kFusedMaxStages;
+    const FusedSmem L = fused_smem_layout(D, a.tokens_per_unit, K, a.stage_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);    // data landed + rope table written
+    uint64_t* computed = full + kFusedMaxStages;           // consumers done with the stage
+    uint64_t* empty = computed + kFusedMaxStages;          // stores have read the stage
     float2* turns = reinterpret_cast<float2*>(smem + L.turns);
-    int* head_map = reinterpret_cast<int*>(smem + L.heads);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t first = blockIdx.x, step = gridDim.x;
     const int64_t n = first < a.total_units ? (a.total_units - 1 - first) / step + 1 : 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < K; ++s) {
-            mbar_init(&full[s], 32);
-            mbar_init(&empty[s], NW);
+            mbar_init(&full[s], 1 + 32);  // loader lane + the table warp's lanes
+            mbar_init(&computed[s], NW);
+            mbar_init(&empty[s], 1);
         }
         fence_barrier_init();
     }
     for (int j = threadIdx.x; j < HALF; j += blockDim.x) turns[j] = make_float2(a.turn_hi[j], a.turn_lo[j]);
-    for (int g = threadIdx.x; g < N; g += blockDim.x) {
-        int r = 0;
-        while (r + 1 < a.W && g >= a.head_off[r + 1]) ++r;
-        head_map[g] = (r << 16) | int(g - a.head_off[r]);
-    }
     __syncthreads();
     if (n == 0) return;
     const int row_bytes = N * D * 2;  // one token, all heads, one tensor
 
-    if (warp == 0) {  // producer
+    if (warp == kLoaderWarp) {  // one lane streams units into the stages
+        if (lane != 0) return;
         const uint64_t policy = policy_evict_first();
-        int64_t k = 0;
-        for (; k < n; ++k) {
-            const int s = int(k % K);
-            if (k >= K && !mbar_wait_bounded(&empty[s], uint32_t(((k / K) - 1) & 1))) {
-                if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
+        int64_t j = 0;
+        for (; j < n; ++j) {
+            const int s = int(j % K);
+            if (j >= K && !mbar_wait_bounded(&empty[s], uint32_t(((j / K) - 1) & 1))) {
+                atomicOr(&g_fused_status, kStatusWaitTimeout);
                 break;
             }
-            const FusedUnit t = fused_decode(a, first + k * step);
-            float2* table = reinterpret_cast<float2*>(smem + L.tables + s * L.table_bytes);
-            const float p0 = float(a.seq_off[t.q] + t.i0);
-            for (int e = lane; e < t.ntok * HALF; e += 32) {
-                const float2 tj = turns[e % HALF];
-                table[e] = rope_cos_sin(p0 + float(e / HALF), tj.x, tj.y);
-            }
-            __syncwarp();
-            if (lane == 0) {
-                const uint32_t bytes = uint32_t(t.ntok) * uint32_t(row_bytes);
-                const int64_t off = (t.bb * a.s[t.q] + t.i0) * row_bytes;
-                uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
-                mbar_arrive_expect_tx(&full[s], 2 * bytes);
-                bulk_g2s_hint(dst, a.q_in[t.q] + off, bytes, &full[s], policy);
-                bulk_g2s_hint(dst + bytes, a.k_in[t.q] + off, bytes, &full[s], policy);
-            } else {
-                mbar_arrive(&full[s]);
-            }
+            const FusedUnit t = fused_decode(a, first + j * step);
+            const uint32_t bytes = uint32_t(t.ntok) * uint32_t(row_bytes);
+            const int64_t off = (t.bb * a.s[t.q] + t.i0) * row_bytes;
+            uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
+            mbar_arrive_expect_tx(&full[s], 2 * bytes);
+            bulk_g2s_hint(dst, a.q_in[t.q] + off, bytes, &full[s], policy);
+            bulk_g2s_hint(dst + bytes, a.k_in[t.q] + off, bytes, &full[s], policy);
         }
-        // do not leave while copies into this CTA's shared memory are in flight
-        if (lane == 0) {
-            for (int64_t j = (k > K ? k - K : 0); j < k; ++j) {
-                if (!mbar_wait_bounded(&full[j % K], uint32_t((j / K) & 1))) {
-                    atomicOr(&g_fused_status, kStatusDrainTimeout);
-                    break;
-                }
+        // do not leave while copies into this CTA's shared memory may be in flight
+        for (int64_t jj = (j > K ? j - K : 0); jj < j; ++jj) {
+            if (!mbar_wait_bounded(&full[jj % K], uint32_t((jj / K) & 1))) {
+                atomicOr(&g_fused_status, kStatusDrainTimeout);
+                break;
             }
         }
         return;
     }
 
-    // consumers
-    const int cw = warp - 1;
-    const int sub = lane % G;    // which 8 values of the row this lane holds
-    const int group = lane / G;  // which head row of the warp slot
-    float wq[8], wk[8];
+    if (warp == kTableWarp) {  // cos/sin of each unit's positions, once the stage's table is free
+        for (int64_t j = 0; j < n; ++j) {
+            const int s = int(j % K);
+            if (j >= K && !mbar_wait_bounded(&computed[s], uint32_t(((j / K) - 1) & 1))) {
+                if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
+                break;
+            }
+            const FusedUnit t = fused_decode(a, first + j * step);
+            float2* table = reinterpret_cast<float2*>(smem + L.tables + s * L.table_bytes);
+            const float p0 = float(a.seq_off[t.q] + t.i0);
+            // Per token the pairs are stored so that the lanes of a row group read 16 contiguous
+            // bytes each: first (cos, sin) of pairs 4i, 4i+1 for every lane i, then of pairs
+            // 4i+2, 4i+3.
+            for (int e = lane; e < t.ntok * HALF; e += 32) {
+                const int tok = e / HALF, j = e % HALF;
+                const float2 tj = turns[j];
+                const int at = tok * HALF + ((j >> 1) & 1) * (HALF / 2) + (j >> 2) * 2 + (j & 1);
+                table[at] = rope_cos_sin(p0 + float(tok), tj.x, tj.y);
+            }
+            mbar_arrive(&full[s]);  // release: this lane's table entries
+        }
+        return;
+    }
+
+    if (warp == kStorerWarp) {
+        // The results sit where their inputs were: for each token, q|k and destination rank one
+        // run of n_r heads, contiguous in the stage and in the destination tensor. A stage is
+        // handed back to the loader kFusedDrain units later, once its stores have read it.
+        int64_t j = 0;
+        for (; j < n; ++j) {
+            const int s = int(j % K);
+            if (!mbar_wait_bounded(&computed[s], uint32_t((j / K) & 1))) {
+                if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
+                break;
+            }
+            const FusedUnit t = fused_decode(a, first + j * step);
+            const uint8_t* st = smem + L.stages + size_t(s) * a.stage_bytes;
+            const int64_t row0 = t.bb * a.S + a.seq_off[t.q] + t.i0;
+            const int W = a.W;
+            const int runs = t.ntok * 2 * W;
+            for (int idx = lane; idx < runs; idx += 32) {
+                const int rest = idx / W, r = idx - rest * W;
+                const int which = rest & 1, tok = rest >> 1;
+                const int64_t run = a.n[r] * (D * 2);
+                if (run == 0) continue;
+                const uint8_t* src = st + (which * t.ntok + tok) * row_bytes + a.head_off[r] * (D * 2);
+                uint8_t* dst = (which ? a.k_out[r] : a.q_out[r]) + (row0 + tok) * run;
+                bulk_s2g(dst, src, uint32_t(run));
+            }
+            bulk_commit();
+            if (j >= kFusedDrain) {
+                bulk_wait_read<kFusedDrain>();  // unit j - kFusedDrain has left shared memory
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[(j - kFusedDrain) % K]);
+            }
+        }
+        bulk_wait<0>();
+        return;
+    }
+
+    // consumers: the first half of the warps normalise q rows, the second half k rows
+    constexpr int HALF_NW = NW / 2;
+    const int cw = warp - kFirstConsumerWarp;
+    const int which = cw >= HALF_NW;          // 0: q, 1: k (uniform per warp)
+    const int cwi = cw - which * HALF_NW;     // rank among the warps of this tensor
+    const int sub = lane % G;                 // which 8 values of the row this lane holds
+    const int group = lane / G;               // which head row of the warp slot
+    float w[8];
     {
-        const float4* wp = reinterpret_cast<const float4*>(a.rms_w + sub * 8);
-        const float4* kp = reinterpret_cast<const float4*>(a.rms_w + D + sub * 8);
-        const float4 a0 = wp[0], a1 = wp[1], b0 = kp[0], b1 = kp[1];
-        wq[0] = a0.x; wq[1] = a0.y; wq[2] = a0.z; wq[3] = a0.w;
-        wq[4] = a1.x; wq[5] = a1.y; wq[6] = a1.z; wq[7] = a1.w;
-        wk[0] = b0.x; wk[1] = b0.y; wk[2] = b0.z; wk[3] = b0.w;
-        wk[4] = b1.x; wk[5] = b1.y; wk[6] = b1.z; wk[7] = b1.w;
+        const float4* wp = reinterpret_cast<const float4*>(a.rms_w + which * D + sub * 8);
+        const float4 a0 = wp[0], a1 = wp[1];
+        w[0] = a0.x; w[1] = a0.y; w[2] = a0.z; w[3] = a0.w;
+        w[4] = a1.x; w[5] = a1.y; w[6] = a1.z; w[7] = a1.w;
     }
     const float inv_d = 1.0f / float(D);
-    const int twoN = 2 * N;
     for (int64_t k = 0; k < n; ++k) {
         const int s = int(k % K);
         const FusedUnit t = fused_decode(a, first + k * step);
@@ -224,29 +285,33 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_qk_kernel(const __grid
             if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
             break;
         }
-        const uint8_t* st = smem + L.stages + size_t(s) * a.stage_bytes;
+        // this tensor's rows in the stage: (token, head) row ri at byte ri * 2d
+        uint8_t* rows_base = smem + L.stages + size_t(s) * a.stage_bytes + which * t.ntok * row_bytes;
         const float2* table = reinterpret_cast<const float2*>(smem + L.tables + s * L.table_bytes);
-        const int items = t.ntok * twoN;  // head rows: (token, q|k, head)
-        const int steps = (items + PER_STEP - 1) / PER_STEP;
-        const int m_lo = cw * steps / NW, m_hi = (cw + 1) * steps / NW;
-        const int64_t row0 = t.bb * a.S + a.seq_off[t.q] + t.i0;  // destination row of token 0
+        const int rows = t.ntok * N;
+        const int steps = (rows + PER_STEP - 1) / PER_STEP;
+        const int m_lo = cwi * steps / HALF_NW, m_hi = (cwi + 1) * steps / HALF_NW;
+        int base = m_lo * PER_STEP;   // first row of the current step and its (token, head)
+        int base_tok = base / N;
+        int base_head = base - base_tok * N;
         for (int m = m_lo; m < m_hi; ++m) {
-            int tok[kIlp], which[kIlp], head[kIlp];
+            uint8_t* slot[kIlp];
+            int tok[kIlp];
             bool ok[kIlp];
             float v[kIlp][8], ss[kIlp];
 #pragma unroll
             for (int u = 0; u < kIlp; ++u) {
-                const int item = m * PER_STEP + u * GPW + group;
-                ok[u] = item < items;
-                const int it = ok[u] ? item : 0;
-                tok[u] = it / twoN;
-                const int rem = it - tok[u] * twoN;
-                which[u] = rem >= N;
-                head[u] = rem - which[u] * N;
+                const int o = u * GPW + group;
+                ok[u] = base + o < rows;
+                slot[u] = rows_base + (base + o) * (D * 2) + sub * 16;
+                int hh = base_head + o, tk = base_tok;
+                while (hh >= N) {
+                    hh -= N;
+                    ++tk;
+                }
+                tok[u] = tk;
                 uint4 x = make_uint4(0, 0, 0, 0);
-                if (ok[u])
-                    x = ld_shared_v4(st + (which[u] * t.ntok + tok[u]) * row_bytes + head[u] * (D * 2) +
-                                     sub * 16);
+                if (ok[u]) x = ld_shared_v4(slot[u]);
                 v[u][0] = bf16_lo(x.x); v[u][1] = bf16_hi(x.x);
                 v[u][2] = bf16_lo(x.y); v[u][3] = bf16_hi(x.y);
                 v[u][4] = bf16_lo(x.z); v[u][5] = bf16_hi(x.z);
@@ -265,28 +330,32 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_qk_kernel(const __grid
             for (int u = 0; u < kIlp; ++u) {
                 if (!ok[u]) continue;
                 const float inv = rsqrtf(ss[u] * inv_d + a.eps);
-                const float4 cs01 = *reinterpret_cast<const float4*>(table + tok[u] * HALF + sub * 4);
-                const float4 cs23 = *reinterpret_cast<const float4*>(table + tok[u] * HALF + sub * 4 + 2);
+                // pairs 4*sub .. 4*sub+3 as two 16-byte halves (see the table layout)
+                const float2* tt = table + tok[u] * HALF + sub * 2;
+                const float4 cs01 = *reinterpret_cast<const float4*>(tt);
+                const float4 cs23 = *reinterpret_cast<const float4*>(tt + HALF / 2);
                 const float c[4] = {cs01.x, cs01.z, cs23.x, cs23.z};
                 const float sn[4] = {cs01.y, cs01.w, cs23.y, cs23.w};
-                uint32_t o[4];
+                uint32_t o4[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float w0 = which[u] ? wk[2 * e] : wq[2 * e];
-                    const float w1 = which[u] ? wk[2 * e + 1] : wq[2 * e + 1];
-                    const float y0 = v[u][2 * e] * inv * w0;
-                    const float y1 = v[u][2 * e + 1] * inv * w1;
-                    o[e] = pack_bf16(y0 * c[e] - y1 * sn[e], y0 * sn[e] + y1 * c[e]);
+                    const float y0 = v[u][2 * e] * inv * w[2 * e];
+                    const float y1 = v[u][2 * e + 1] * inv * w[2 * e + 1];
+                    o4[e] = pack_bf16(y0 * c[e] - y1 * sn[e], y0 * sn[e] + y1 * c[e]);
                 }
-                const int hm = head_map[head[u]];
-                const int r = hm >> 16, h = hm & 0xFFFF;
-                uint8_t* out = which[u] ? a.k_out[r] : a.q_out[r];
-                st_v4(out + ((row0 + tok[u]) * a.n[r] + h) * (D * 2) + sub * 16,
-                      make_uint4(o[0], o[1], o[2], o[3]));
+                st_shared_v4(slot[u], make_uint4(o4[0], o4[1], o4[2], o4[3]));  // in place
+            }
+            base += PER_STEP;
+            base_head += PER_STEP;
+            while (base_head >= N) {
+                base_head -= N;
+                ++base_tok;
             }
         }
+        // make this warp's shared-memory results visible to the bulk-copy unit, then report
+        fence_proxy_async_shared();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (lane == 0) mbar_arrive(&computed[s]);
     }
 }
 
@@ -296,13 +365,12 @@ void fused_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages, uint32
     *stages = 0;
     *tokens_per_unit = 1;
     *stage_bytes = 0;
-    if (p.N > kFusedMaxHeads) return;
     const int64_t pair_bytes = 2 * p.N * p.d * 2;  // one token of q and of k
     int64_t T = ULY_FUSED_STAGE_TARGET / pair_bytes;
     if (T < 1) T = 1;
     const int64_t sb = T * pair_bytes;
-    for (int K = kFusedMaxStages; K >= 2; --K) {
-        const FusedSmem m = fused_smem_layout(int(p.d), p.N, int(T), K, uint32_t(sb));
+    for (int K = kFusedMaxStages; K >= kFusedDrain + 1; --K) {
+        const FusedSmem m = fused_smem_layout(int(p.d), int(T), K, uint32_t(sb));
         if (sb <= (1 << 20) && m.total <= kFusedSmemBudget) {
             *tokens_per_unit = T;
             *stages = K;
@@ -325,7 +393,7 @@ static cudaError_t launch_g(const FusedArgs& a, cudaStream_t stream, int device,
         if (e != cudaSuccess) return e;
         g_fused_smem_set[device] |= 1 << bit;
     }
-    const FusedSmem m = fused_smem_layout(a.d, a.N, a.tokens_per_unit, a.stages, a.stage_bytes);
+    const FusedSmem m = fused_smem_layout(a.d, a.tokens_per_unit, a.stages, a.stage_bytes);
     fused_qk_kernel<G><<<grid, kFusedThreads, m.total, stream>>>(a);
     return cudaGetLastError();
 }
@@ -333,7 +401,7 @@ static cudaError_t launch_g(const FusedArgs& a, cudaStream_t stream, int device,
 cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count)
 {
     if (a.total_units == 0) return cudaSuccess;
-    int64_t grid = sm_count;
+    int64_t grid = int64_t(sm_count) * kFusedCtasPerSm;
     if (grid > a.total_units) grid = a.total_units;
     switch (a.d / 8) {
         case 1: return launch_g<1>(a, stream, device, int(grid));

@@ -13,6 +13,13 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr unsigned kStatusWaitTimeout = 1u;
 constexpr unsigned kStatusDrainTimeout = 2u;
 
+// Non-negative a / b (b > 0), in 32-bit arithmetic when both fit, which is the common case.
+__device__ __forceinline__ int64_t div_fast(int64_t a, int64_t b)
+{
+    if (((a | b) >> 32) == 0) return int64_t(uint32_t(a) / uint32_t(b));
+    return a / b;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -144,6 +151,20 @@ __device__ __forceinline__ void st_v4(void* p, const uint4& v)
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
                  : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(void* p, const uint4& v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory writes before later async-proxy
+// (bulk copy) reads of the same memory, once a barrier has passed between them.
+__device__ __forceinline__ void fence_proxy_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ uint4 ld_shared_v4(const void* p)

@@ -26,13 +26,13 @@ namespace uly {
 static __device__ unsigned g_relayout_status;
 
 #ifndef ULY_TMA_UNIT_BYTES
-#define ULY_TMA_UNIT_BYTES 32768
+#define ULY_TMA_UNIT_BYTES 24576
 #endif
 #ifndef ULY_TMA_STAGES
-#define ULY_TMA_STAGES 6
+#define ULY_TMA_STAGES 4
 #endif
 #ifndef ULY_TMA_CTAS_PER_SM
-#define ULY_TMA_CTAS_PER_SM 1
+#define ULY_TMA_CTAS_PER_SM 2
 #endif
 #ifndef ULY_VEC_UNIT_BYTES
 #define ULY_VEC_UNIT_BYTES 16384
@@ -40,8 +40,54 @@ static __device__ unsigned g_relayout_status;
 #ifndef ULY_VEC_UNROLL
 #define ULY_VEC_UNROLL 4
 #endif
+#ifndef ULY_TMA_LOOKAHEAD
+#define ULY_TMA_LOOKAHEAD 3
+#endif
+static_assert(ULY_TMA_LOOKAHEAD >= 1 && ULY_TMA_LOOKAHEAD < ULY_TMA_STAGES, "lookahead < stages");
+static_assert(ULY_TMA_STAGES <= 16, "stage barriers must fit the barrier area");
 constexpr int kTmaBarrierBytes = 128;  // the stage barriers sit before the first stage
 constexpr int kVecThreads = 256;
+
+// The stage ring of the TMA kernels (one warp per CTA). Unit k of this CTA lives in stage
+// k % K. Loads run L units ahead of the unit being stored; a stage is refilled only when the
+// bulk stores that last read it (unit k + L - K, K - L groups back) have finished reading shared
+// memory. So up to L loads and K - L store groups are in flight, and the loop never waits on the
+// stores it has just issued. Every wait is bounded; on a timeout the status word records it,
+// loads still in flight are waited for (bounded again), and the warp returns.
+template <class Load, class Store>
+__device__ __forceinline__ void run_stage_ring(uint64_t* full, int64_t n, int lane, Load load,
+                                               Store store)
+{
+    constexpr int K = ULY_TMA_STAGES, L = ULY_TMA_LOOKAHEAD;
+    int64_t loaded = n < L ? n : L;
+    for (int64_t k = 0; k < loaded; ++k) load(k);
+    int64_t k = 0;
+    bool ok = true;
+    for (; k < n; ++k) {
+        if (!mbar_wait_bounded(&full[k % K], uint32_t((k / K) & 1))) {
+            ok = false;
+            break;
+        }
+        store(k);
+        bulk_commit();
+        if (loaded < n) {
+            bulk_wait_read<K - L>();
+            __syncwarp();
+            load(loaded);
+            ++loaded;
+        }
+    }
+    if (!ok) {
+        if (lane == 0) atomicOr(&g_relayout_status, kStatusWaitTimeout);
+        for (int64_t j = k; j < loaded; ++j) {
+            if (!mbar_wait_bounded(&full[j % K], uint32_t((j / K) & 1))) {
+                if (lane == 0) atomicOr(&g_relayout_status, kStatusDrainTimeout);
+                break;
+            }
+        }
+    }
+    bulk_wait<0>();
+}
 
 struct Unit {
     int q, r;
@@ -74,9 +120,9 @@ __device__ __forceinline__ Unit decode(const RelayoutArgs& a, int64_t u)
     const int64_t P = a.pieces[t.r];
     const int64_t rows = a.rows[t.q];
     const int64_t per_batch = ((rows + R - 1) / R) * P;
-    t.bb = local / per_batch;
+    t.bb = div_fast(local, per_batch);
     const int64_t rem = local - t.bb * per_batch;
-    const int64_t blk = rem / P;
+    const int64_t blk = div_fast(rem, P);
     const int64_t piece = rem - blk * P;
     const int64_t i0 = blk * R;
     t.nrows = min(R, rows - i0);
@@ -140,38 +186,8 @@ __global__ void __launch_bounds__(32, 1) relayout_tma_kernel(const __grid_consta
             for (int64_t row = lane; row < t.nrows; row += 32)
                 bulk_s2g(seq_addr(a, t, row), src + row * t.cols, uint32_t(t.cols));
         }
-        bulk_commit();
     };
-
-    int64_t loaded = n < K - 1 ? n : K - 1;
-    for (int64_t k = 0; k < loaded; ++k) issue_load(k);
-    int64_t k = 0;
-    bool ok = true;
-    for (; k < n; ++k) {
-        const int s = int(k % K);
-        if (!mbar_wait_bounded(&full[s], uint32_t((k / K) & 1))) {
-            ok = false;
-            break;
-        }
-        issue_store(k);
-        if (loaded < n) {
-            // the next load reuses the stage of unit k - 1: its stores must have read it
-            bulk_wait_read<1>();
-            __syncwarp();
-            issue_load(loaded);
-            ++loaded;
-        }
-    }
-    if (!ok) {
-        if (lane == 0) atomicOr(&g_relayout_status, kStatusWaitTimeout);
-        for (int64_t j = k; j < loaded; ++j) {  // let every load still in flight land
-            if (!mbar_wait_bounded(&full[j % K], uint32_t((j / K) & 1))) {
-                if (lane == 0) atomicOr(&g_relayout_status, kStatusDrainTimeout);
-                break;
-            }
-        }
-    }
-    bulk_wait<0>();
+    run_stage_ring(full, n, lane, issue_load, issue_store);
 }
 
 // ---- row tiles: whole rows through shared memory ------------------------------------------------
@@ -202,7 +218,7 @@ __device__ __forceinline__ RowTile decode_rows(const RowTileArgs& a, int64_t u)
     const int64_t rows = a.rows[lo];
     const int64_t blocks = (rows + T - 1) / T;
     const int64_t local = u - a.unit_begin[lo];
-    t.bb = local / blocks;
+    t.bb = div_fast(local, blocks);
     const int64_t blk = local - t.bb * blocks;
     t.i0 = a.row_lo[lo] + blk * T;
     t.nrows = min(T, rows - blk * T);
@@ -272,37 +288,8 @@ __global__ void __launch_bounds__(32, 1) relayout_rows_kernel(const __grid_const
         } else {
             if (lane == 0) bulk_s2g(seq_span(t), stage, uint32_t(t.nrows * row_bytes));
         }
-        bulk_commit();
     };
-
-    int64_t loaded = n < K - 1 ? n : K - 1;
-    for (int64_t k = 0; k < loaded; ++k) issue_load(k);
-    int64_t k = 0;
-    bool ok = true;
-    for (; k < n; ++k) {
-        const int s = int(k % K);
-        if (!mbar_wait_bounded(&full[s], uint32_t((k / K) & 1))) {
-            ok = false;
-            break;
-        }
-        issue_store(k);
-        if (loaded < n) {
-            bulk_wait_read<1>();  // stores of unit k - 1 have left the stage about to be refilled
-            __syncwarp();
-            issue_load(loaded);
-            ++loaded;
-        }
-    }
-    if (!ok) {
-        if (lane == 0) atomicOr(&g_relayout_status, kStatusWaitTimeout);
-        for (int64_t j = k; j < loaded; ++j) {
-            if (!mbar_wait_bounded(&full[j % K], uint32_t((j / K) & 1))) {
-                if (lane == 0) atomicOr(&g_relayout_status, kStatusDrainTimeout);
-                break;
-            }
-        }
-    }
-    bulk_wait<0>();
+    run_stage_ring(full, n, lane, issue_load, issue_store);
 }
 
 template <int MODE>
