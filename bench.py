@@ -192,9 +192,23 @@ def read_peaks():
         return 6800.0, "fallback"
 
 
-def read_traffic(kernel: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if taken on the current source."""
+def source_digest(files) -> str | None:
+    """sha256 (first 16 hex digits) of the named csrc files, concatenated in the given order."""
     import hashlib
+    h = hashlib.sha256()
+    for name in files:
+        try:
+            with open(os.path.join(ROOT, "ulysses_sequence_all_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        except OSError:
+            return None
+    return h.hexdigest()[:16]
+
+
+def read_traffic(kernel: str):
+    """Per-launch DRAM bytes (read + write) from the committed ncu summary, or None when the
+    kernel's sources have changed since the counters were taken. Lines of profiles/traffic.txt:
+    kernel  comma-separated-source-files  digest  bytes-per-launch."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(path) as f:
@@ -203,13 +217,7 @@ def read_traffic(kernel: str):
         return None
     for parts in lines:
         if len(parts) >= 4 and parts[0] == kernel:
-            src = os.path.join(ROOT, "ulysses_sequence_all_gb300", "csrc", parts[1])
-            try:
-                with open(src, "rb") as f:
-                    digest = hashlib.sha256(f.read()).hexdigest()[:16]
-            except OSError:
-                return None
-            return int(parts[3]) if digest == parts[2] else None
+            return int(parts[3]) if source_digest(parts[1].split(",")) == parts[2] else None
     return None
 
 
@@ -383,8 +391,8 @@ def run_ours(args):
            "mode1": wk.bytes_plain / (med["mode1"] * 1e-3) / 1e9}
     dominant = max(med, key=lambda k: med[k])
     peak, peak_kind = read_peaks()
-    kernel_name = {"fused_qk": "fused_qk_kernel", "mode0": "relayout_tma_kernel<0>",
-                   "mode1": "relayout_tma_kernel<1>"}[dominant]
+    kernel_name = {"fused_qk": "fused_qk_kernel", "mode0": "relayout_rows_kernel<0>",
+                   "mode1": "relayout_rows_kernel<1>"}[dominant]
     traffic = read_traffic(kernel_name)
     d2d = d2d_gbs(torch, wk.side) if rank == 0 else None
     line = {

@@ -5,21 +5,23 @@
 //     y = x / sqrt(mean(x^2) + eps) * w,   (y[2j], y[2j+1]) rotated by p * theta^(-2j/d),
 // in fp32, rounded once to bf16 (nearest even), and written where mode 0 places the row.
 //
-// Structure: a persistent grid with one CTA per SM and a ring of K shared-memory stages.
-//  * Warp 0 moves data. Per work unit (a few consecutive tokens of one source rank: all N heads
-//    of q and of k, two contiguous spans) its lanes fill the stage's cos/sin table for those
-//    tokens' positions, then lane 0 starts the two cp.async.bulk loads; all 32 lanes arrive on
-//    the stage's "full" mbarrier (lane 0 with the expected transaction bytes), so a consumer that
-//    sees the phase complete sees both the table and the data. When the consumers report a unit
-//    done on its "computed" mbarrier, the lanes issue one cp.async.bulk store per (token, q|k,
-//    destination rank): n_r heads that are contiguous in the stage and in the destination.
-//    Loads run K - kFusedDrain units ahead; a stage is refilled once the stores that last read it
-//    (kFusedDrain bulk groups back) have finished reading shared memory.
-//  * The consumer warps split a stage's head rows into contiguous ranges. A group of d/8 lanes
-//    holds one head row (8 values per lane) and each group keeps two rows in flight; the sum of
-//    squares is reduced with xor shuffles inside the group, the weight and rotation are applied in
-//    registers, and the bf16 result overwrites its input in shared memory. Each consumer warp then
-//    fences its writes for the async proxy and arrives on the stage's "computed" mbarrier.
+// Structure: a persistent grid of several CTAs per SM, each with a ring of K shared-memory
+// stages. A work unit is a few consecutive tokens of one source rank: all N heads of q and of k,
+// two contiguous spans of the sequence-side tensors. Warp roles per CTA:
+//  * loader: one lane waits for the stage to be free ("empty" mbarrier), then starts the two
+//    cp.async.bulk loads, completing on the stage's "full" mbarrier as transaction bytes;
+//  * table: once the consumers of the stage's previous unit are done ("computed"), the lanes
+//    fill the stage's cos/sin table for the unit's positions and arrive on "full", so a consumer
+//    that sees the phase complete sees both the table and the data;
+//  * storer: when the consumers report a unit done ("computed"), the lanes issue one
+//    cp.async.bulk store per (token, q|k, destination rank): n_r heads that are contiguous in the
+//    stage and in the destination; kFusedDrain units later, once those stores have read shared
+//    memory, the stage is handed back to the loader ("empty");
+//  * consumers: half of them take q rows, half k rows. A group of d/8 lanes holds one head row
+//    (8 values per lane) and each group keeps kIlp rows in flight; the sum of squares is reduced
+//    with xor shuffles inside the group, the weight and rotation are applied in registers, and the
+//    bf16 result overwrites its input in shared memory. Each consumer warp then fences its writes
+//    for the async proxy and arrives on "computed".
 //
 // RoPE angles: p * theta^(-2j/d) reaches ~75,600 rad at the Wan shape, where an fp32 product
 // alone is off by ~5e-3 rad. The angle is formed in turns (units of 2 pi): the host supplies
