@@ -43,6 +43,19 @@ def parse():
     return ap.parse_args()
 
 
+def aggregate_throughput(local_ms: float, bytes_per_rank_step: int, dist=None, device="cpu"):
+    """Whole-job throughput of replicas: every rank's bytes over the slowest rank's time.
+    Returns (max ms per step over ranks, GB/s of all ranks together)."""
+    world, ms = 1, float(local_ms)
+    if dist is not None and dist.is_initialized():
+        import torch
+        world = dist.get_world_size()
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, bytes_per_rank_step * world / (ms * 1e-3) / 1e9
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -369,21 +382,13 @@ def run_ours(args):
     if pg:
         pg.barrier()
     clock_info = clocks.stop()
-    ms = start.elapsed_time(end) / args.steps
-    if pg:
-        t = torch.tensor([ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, value = aggregate_throughput(start.elapsed_time(end) / args.steps, wk.bytes_step, pg, "cuda")
     assert B.ulysses_device_status() == 0, "a kernel recorded a wait timeout"
-    value = wk.bytes_step * world / (ms * 1e-3) / 1e9
 
     # end to end through the host-buffer entry points: pinned host in, device, pinned host out
     e2e = run_e2e(torch, B, wk, stream, args)
-    if pg:
-        t = torch.tensor([e2e["ms_per_step"]], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e["ms_per_step"] = float(t.item())
-        e2e["value"] = round(wk.bytes_step * world / (e2e["ms_per_step"] * 1e-3) / 1e9, 3)
+    e2e["ms_per_step"], e2e_value = aggregate_throughput(e2e["ms_per_step"], wk.bytes_step, pg, "cuda")
+    e2e["value"] = round(e2e_value, 3)
 
     med = {k: statistics.median(v) for k, v in kt.items()}
     gbs = {"fused_qk": wk.bytes_fused / (med["fused_qk"] * 1e-3) / 1e9,

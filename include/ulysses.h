@@ -173,6 +173,15 @@ int ulysses_a2a_4d_qk_fused_host(ulysses_plan_t plan, const void* const* q_host_
  * ULY_EDEVICE when the word was non-zero. */
 int ulysses_device_status(unsigned* status);
 
+/*
+ * Self-test of the failure path (no counterpart on the pages, which describe hangs on misuse but
+ * no detection): queue on `stream` a one-warp kernel that waits on a barrier nothing arrives on,
+ * with a limit of limit_us microseconds (1 .. 1,000,000) instead of the kernels' 2 s. The wait
+ * gives up, sets the timeout bit (1) of the device status word, and the kernel returns normally,
+ * so the context stays usable; ulysses_device_status() then reports ULY_EDEVICE with status 1.
+ */
+int ulysses_selftest_wait_timeout(unsigned limit_us, void* stream);
+
 /* The cudaError_t value of the last ULY_ECUDA returned on this host thread (0 if none). */
 int ulysses_last_cuda_error(void);
 

@@ -25,8 +25,9 @@ DTYPE_CODES = {"uint8": ULY_U8, "float8_e4m3fn": ULY_F8E4M3, "float8_e5m2": ULY_
 EXPORTS = ["ulysses_plan", "ulysses_plan_destroy", "ulysses_plan_set_chunk_bytes",
            "ulysses_plan_bytes", "ulysses_plan_num_chunks", "ulysses_plan_chunk_rows",
            "ulysses_a2a_4d", "ulysses_a2a_4d_engine", "ulysses_a2a_4d_qk_fused",
-           "ulysses_a2a_4d_host", "ulysses_a2a_4d_qk_fused_host", "ulysses_device_status", "ulysses_last_cuda_error",
-           "ulysses_strerror", "ulysses_version"]
+           "ulysses_a2a_4d_host", "ulysses_a2a_4d_qk_fused_host", "ulysses_device_status",
+           "ulysses_selftest_wait_timeout", "ulysses_last_cuda_error", "ulysses_strerror",
+           "ulysses_version"]
 
 
 class UlyssesError(RuntimeError):
@@ -68,6 +69,7 @@ def _lib():
         lib.ulysses_a2a_4d_qk_fused_host.argtypes = [_p, _pp, _pp, _pp, _pp, _pp, _pp, _pp, _pp, _p,
                                                      ctypes.c_float, ctypes.c_float, _p]
         lib.ulysses_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.ulysses_selftest_wait_timeout.argtypes = [ctypes.c_uint, _p]
         lib.ulysses_last_cuda_error.argtypes = []
         lib.ulysses_strerror.argtypes = [ctypes.c_int]
         lib.ulysses_strerror.restype = ctypes.c_char_p
@@ -198,6 +200,12 @@ def ulysses_device_status() -> int:
     if rc not in (ULY_OK, ULY_EDEVICE):
         _check(rc, "ulysses_device_status")
     return st.value
+
+
+def ulysses_selftest_wait_timeout(limit_us: int, stream=None):
+    """Queue the failure-path self-test kernel (a wait that must time out after limit_us)."""
+    _check(_lib().ulysses_selftest_wait_timeout(limit_us, _stream(stream)),
+           "ulysses_selftest_wait_timeout")
 
 
 def ulysses_strerror(status: int) -> str:

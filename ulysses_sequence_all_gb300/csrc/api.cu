@@ -22,6 +22,7 @@ cudaError_t relayout_rows_launch(const RowTileArgs& a, int mode, cudaStream_t st
 void fused_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages, uint32_t* stage_bytes);
 cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count);
 cudaError_t fused_status(unsigned* status, bool clear);
+cudaError_t selftest_timeout_launch(uint64_t limit_ns, cudaStream_t stream);
 }  // namespace uly
 
 using namespace uly;
@@ -398,6 +399,13 @@ int ulysses_device_status(unsigned* status)
     if ((e = fused_status(&b, true)) != cudaSuccess) return cuda_fail(e);
     *status = a | b;
     return *status ? ULY_EDEVICE : ULY_OK;
+}
+
+int ulysses_selftest_wait_timeout(unsigned limit_us, void* stream)
+{
+    if (limit_us < 1 || limit_us > 1000000u) return ULY_EINVAL;
+    cudaError_t e = selftest_timeout_launch(uint64_t(limit_us) * 1000u, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ULY_OK : cuda_fail(e);
 }
 
 int ulysses_last_cuda_error(void) { return t_last_cuda_error; }

@@ -213,16 +213,18 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
                 break;
             }
             const FusedUnit t = fused_decode(a, first + j * step);
-            float2* table = reinterpret_cast<float2*>(smem + L.tables + s * L.table_bytes);
+            float* table = reinterpret_cast<float*>(smem + L.tables + s * L.table_bytes);
             const float p0 = float(a.seq_off[t.q] + t.i0);
-            // Per token the pairs are stored so that the lanes of a row group read 16 contiguous
-            // bytes each: first (cos, sin) of pairs 4i, 4i+1 for every lane i, then of pairs
-            // 4i+2, 4i+3.
+            // Per token, lane i of a row group owns pairs 4i .. 4i+3, read as two 16-byte
+            // entries (c_j, c_j+1, s_j, s_j+1) for j = 4i and j = 4i+2; the entries of all lanes
+            // for j = 4i come first, then those for j = 4i+2, so each read is contiguous.
             for (int e = lane; e < t.ntok * HALF; e += 32) {
                 const int tok = e / HALF, j = e % HALF;
                 const float2 tj = turns[j];
-                const int at = tok * HALF + ((j >> 1) & 1) * (HALF / 2) + (j >> 2) * 2 + (j & 1);
-                table[at] = rope_cos_sin(p0 + float(tok), tj.x, tj.y);
+                const float2 cs = rope_cos_sin(p0 + float(tok), tj.x, tj.y);
+                const int at = ((tok * 2 + ((j >> 1) & 1)) * G + (j >> 2)) * 4 + (j & 1);
+                table[at] = cs.x;
+                table[at + 2] = cs.y;
             }
             mbar_arrive(&full[s]);  // release: this lane's table entries
         }
@@ -272,12 +274,15 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     const int cwi = cw - which * HALF_NW;     // rank among the warps of this tensor
     const int sub = lane % G;                 // which 8 values of the row this lane holds
     const int group = lane / G;               // which head row of the warp slot
-    float w[8];
+    // This lane's 8 weights as packed pairs: even / odd elements of pairs (0,1) and (2,3), plus the
+    // negated odd ones (the rotation subtracts them).
+    float2 wE[2], wO[2], wOn[2];
     {
         const float4* wp = reinterpret_cast<const float4*>(a.rms_w + which * D + sub * 8);
         const float4 a0 = wp[0], a1 = wp[1];
-        w[0] = a0.x; w[1] = a0.y; w[2] = a0.z; w[3] = a0.w;
-        w[4] = a1.x; w[5] = a1.y; w[6] = a1.z; w[7] = a1.w;
+        wE[0] = make_float2(a0.x, a0.z); wO[0] = make_float2(a0.y, a0.w);
+        wE[1] = make_float2(a1.x, a1.z); wO[1] = make_float2(a1.y, a1.w);
+        for (int h = 0; h < 2; ++h) wOn[h] = make_float2(-wO[h].x, -wO[h].y);
     }
     const float inv_d = 1.0f / float(D);
     for (int64_t k = 0; k < n; ++k) {
@@ -289,7 +294,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
         }
         // this tensor's rows in the stage: (token, head) row ri at byte ri * 2d
         uint8_t* rows_base = smem + L.stages + size_t(s) * a.stage_bytes + which * t.ntok * row_bytes;
-        const float2* table = reinterpret_cast<const float2*>(smem + L.tables + s * L.table_bytes);
+        const float4* table = reinterpret_cast<const float4*>(smem + L.tables + s * L.table_bytes);
         const int rows = t.ntok * N;
         const int steps = (rows + PER_STEP - 1) / PER_STEP;
         const int m_lo = cwi * steps / HALF_NW, m_hi = (cwi + 1) * steps / HALF_NW;
@@ -300,7 +305,9 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
             uint8_t* slot[kIlp];
             int tok[kIlp];
             bool ok[kIlp];
-            float v[kIlp][8], ss[kIlp];
+            // even / odd elements of pairs (0,1) and (2,3) of this lane's 8 values, packed
+            float2 vE[kIlp][2], vO[kIlp][2];
+            float ss[kIlp];
 #pragma unroll
             for (int u = 0; u < kIlp; ++u) {
                 const int o = u * GPW + group;
@@ -314,14 +321,15 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
                 tok[u] = tk;
                 uint4 x = make_uint4(0, 0, 0, 0);
                 if (ok[u]) x = ld_shared_v4(slot[u]);
-                v[u][0] = bf16_lo(x.x); v[u][1] = bf16_hi(x.x);
-                v[u][2] = bf16_lo(x.y); v[u][3] = bf16_hi(x.y);
-                v[u][4] = bf16_lo(x.z); v[u][5] = bf16_hi(x.z);
-                v[u][6] = bf16_lo(x.w); v[u][7] = bf16_hi(x.w);
-                float acc = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc = fmaf(v[u][e], v[u][e], acc);
-                ss[u] = acc;
+                vE[u][0] = make_float2(bf16_lo(x.x), bf16_lo(x.y));
+                vO[u][0] = make_float2(bf16_hi(x.x), bf16_hi(x.y));
+                vE[u][1] = make_float2(bf16_lo(x.z), bf16_lo(x.w));
+                vO[u][1] = make_float2(bf16_hi(x.z), bf16_hi(x.w));
+                float2 acc = __fmul2_rn(vE[u][0], vE[u][0]);
+                acc = __ffma2_rn(vO[u][0], vO[u][0], acc);
+                acc = __ffma2_rn(vE[u][1], vE[u][1], acc);
+                acc = __ffma2_rn(vO[u][1], vO[u][1], acc);
+                ss[u] = acc.x + acc.y;
             }
 #pragma unroll
             for (int off = G / 2; off > 0; off >>= 1) {
@@ -332,18 +340,21 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
             for (int u = 0; u < kIlp; ++u) {
                 if (!ok[u]) continue;
                 const float inv = rsqrtf(ss[u] * inv_d + a.eps);
-                // pairs 4*sub .. 4*sub+3 as two 16-byte halves (see the table layout)
-                const float2* tt = table + tok[u] * HALF + sub * 2;
-                const float4 cs01 = *reinterpret_cast<const float4*>(tt);
-                const float4 cs23 = *reinterpret_cast<const float4*>(tt + HALF / 2);
-                const float c[4] = {cs01.x, cs01.z, cs23.x, cs23.z};
-                const float sn[4] = {cs01.y, cs01.w, cs23.y, cs23.w};
+                const float2 inv2 = make_float2(inv, inv);
                 uint32_t o4[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float y0 = v[u][2 * e] * inv * w[2 * e];
-                    const float y1 = v[u][2 * e + 1] * inv * w[2 * e + 1];
-                    o4[e] = pack_bf16(y0 * c[e] - y1 * sn[e], y0 * sn[e] + y1 * c[e]);
+                for (int h = 0; h < 2; ++h) {
+                    // (c_j, c_j+1, s_j, s_j+1) for j = 4 sub + 2 h (see the table layout)
+                    const float4 cs = table[(tok[u] * 2 + h) * G + sub];
+                    const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
+                    const float2 A = __fmul2_rn(vE[u][h], wE[h]);   // weighted even elements
+                    const float2 Bp = __fmul2_rn(vO[u][h], wO[h]);  // weighted odd elements
+                    const float2 Bn = __fmul2_rn(vO[u][h], wOn[h]);
+                    // rotation, then the 1/rms factor (the rotation is linear)
+                    const float2 oE = __fmul2_rn(__ffma2_rn(Bn, s2, __fmul2_rn(A, c2)), inv2);
+                    const float2 oO = __fmul2_rn(__ffma2_rn(A, s2, __fmul2_rn(Bp, c2)), inv2);
+                    o4[2 * h] = pack_bf16(oE.x, oO.x);
+                    o4[2 * h + 1] = pack_bf16(oE.y, oO.y);
                 }
                 st_shared_v4(slot[u], make_uint4(o4[0], o4[1], o4[2], o4[3]));  // in place
             }

@@ -58,9 +58,24 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
                  : "memory");
 }
 
+// Suspend-time hint (ns) for a try_wait that finds the phase incomplete: the warp may sleep up to
+// this long in hardware instead of returning at once (0 = the implementation's default).
+#ifndef ULY_WAIT_HINT_NS
+#define ULY_WAIT_HINT_NS 0
+#endif
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 {
     uint32_t done;
+#if ULY_WAIT_HINT_NS > 0
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "n"(ULY_WAIT_HINT_NS)
+        : "memory");
+#else
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
@@ -68,16 +83,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
         : "=r"(done)
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
+#endif
     return done != 0;
 }
 
-// Waits for the barrier phase with the given parity to complete; false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity)
+// Waits for the barrier phase with the given parity to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
     return true;
 }

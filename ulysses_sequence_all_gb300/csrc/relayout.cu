@@ -410,6 +410,26 @@ cudaError_t relayout_rows_launch(const RowTileArgs& a, int mode, cudaStream_t st
     return cudaGetLastError();
 }
 
+// Failure-path self-test: one warp waits on a barrier nothing ever arrives on, gives up after
+// limit_ns, records the timeout in the status word and returns like any kernel that timed out.
+__global__ void __launch_bounds__(32, 1) selftest_timeout_kernel(uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t never;
+    if (threadIdx.x == 0) {
+        mbar_init(&never, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    if (!mbar_wait_bounded(&never, 0u, limit_ns) && threadIdx.x == 0)
+        atomicOr(&g_relayout_status, kStatusWaitTimeout);
+}
+
+cudaError_t selftest_timeout_launch(uint64_t limit_ns, cudaStream_t stream)
+{
+    selftest_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t relayout_status(unsigned* status, bool clear)
 {
     cudaError_t e = cudaMemcpyFromSymbol(status, g_relayout_status, sizeof(unsigned));
