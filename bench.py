@@ -408,6 +408,8 @@ def run_ours(args):
         "config": workload_config(),
         "clocks": clock_info,
         "e2e": {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
+        "e2e_detail": {"ms_per_step": round(e2e["ms_per_step"], 3),
+                       "per_call_ms": e2e["per_call_ms"]},
         "gpu_launches": wk.launches_per_step * args.steps,
         "roofline": {"bound": "hbm", "kernel": kernel_name,
                      "achieved": round(gbs[dominant], 1), "peak": peak, "unit": "GB/s",
@@ -460,8 +462,28 @@ def run_e2e(torch, B, wk, stream, args):
     ms = s.elapsed_time(e) / n
     h2d = sum(t.numel() * t.element_size() for t in hq + hk + hv + ho)
     d2h = sum(t.numel() * t.element_size() for t in hqo + hko + hvo + hoo)
+
+    # outside the timed region: each host-buffer call on its own (median of 3)
+    calls = {
+        "fused_qk": lambda: B.ulysses_a2a_4d_qk_fused_host(wk.plan, hq, hk, hqo, hko, wk.q, wk.k,
+                                                           wk.qo, wk.ko, wk.w, EPS, THETA, stream),
+        "mode0": lambda: B.ulysses_a2a_4d_host(wk.plan, 0, hv, hvo, wk.v, wk.vo, stream),
+        "mode1": lambda: B.ulysses_a2a_4d_host(wk.plan, 1, ho, hoo, wk.o, wk.oo, stream),
+    }
+    per_call = {}
+    for name, fn in calls.items():
+        ts = []
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        per_call[name] = round(statistics.median(ts), 3)
     return {"value": round(wk.bytes_step / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "per_call_ms": per_call}
 
 
 def main():

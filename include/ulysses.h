@@ -149,18 +149,25 @@ int ulysses_a2a_4d_qk_fused(ulysses_plan_t plan, const void* const* q_in, const 
                             float rope_theta, void* stream);
 
 /*
- * End-to-end form for host-resident data: on `stream`, copy each rank's input from host_in[k] to
- * dev_in[k], run ulysses_a2a_4d, and copy each dev_out[k] back to host_out[k]. Host buffers should
- * be page-locked for the copies to be asynchronous. Device buffers are the caller's, as above.
+ * End-to-end form for host-resident data: copy each rank's input from host_in[k] to dev_in[k],
+ * run the relayout, and copy each dev_out[k] back to host_out[k]. The work is cut into about
+ * eight sequence chunks so that copies in and copies out overlap: chunk c is copied in and
+ * relaid out on `stream`, then copied out on an auxiliary stream while chunk c+1 is copied in;
+ * `stream` finally waits for the auxiliary stream, so the call is ordered on `stream` as a whole
+ * (when `stream` has completed, host_out holds the result). The auxiliary stream and a few events
+ * are created once per device on the first such call (no device memory) and reused; concurrent
+ * calls from several host threads are serialised while they enqueue. Host buffers should be
+ * page-locked for the copies to be asynchronous. Device buffers are the caller's, as above.
  */
 int ulysses_a2a_4d_host(ulysses_plan_t plan, int mode, const void* const* host_in,
                         void* const* host_out, void* const* dev_in, void* const* dev_out,
                         void* stream);
 
 /*
- * End-to-end form of ulysses_a2a_4d_qk_fused for host-resident q and k: on `stream`, copy each
- * rank's q and k from host to the device buffers, run the fused call, and copy q_out and k_out
- * back to the host. Same arguments and rules as the device form, plus the host buffers.
+ * End-to-end form of ulysses_a2a_4d_qk_fused for host-resident q and k: copy each rank's q and k
+ * from host to the device buffers, run the fused call, and copy q_out and k_out back to the
+ * host, chunked and overlapped exactly as ulysses_a2a_4d_host. Same arguments and rules as the
+ * device form, plus the host buffers.
  */
 int ulysses_a2a_4d_qk_fused_host(ulysses_plan_t plan, const void* const* q_host_in,
                                  const void* const* k_host_in, void* const* q_host_out,

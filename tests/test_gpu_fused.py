@@ -121,6 +121,29 @@ def test_fused_chunked_equals_unchunked():
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+@pytest.mark.parametrize("g", [(5, 2, [300, 310, 290, 305, 295], [9, 8, 8, 8, 7], 128),
+                               (3, 1, [4, 0, 3], [2, 1, 1], 64)], ids=["uneven_b2", "zero_split"])
+def test_fused_host_buffers_match_device_path(oracle, g):
+    """The chunked host-buffer fused call gives the device call's bytes exactly (twice in a row)."""
+    W, b, seq, heads, d = g
+    q, k, w = make_inputs(g, seed=11)
+    qa, ka = run_fused(g, q, k, w)
+    plan = B.ulysses_plan(W, b, seq, heads, d, "bfloat16")
+    hq = [x.cpu().pin_memory() for x in q]
+    hk = [x.cpu().pin_memory() for x in k]
+    hqo = [torch.zeros(t.shape, dtype=torch.bfloat16).pin_memory() for t in qa]
+    hko = [torch.zeros(t.shape, dtype=torch.bfloat16).pin_memory() for t in ka]
+    dq = [torch.empty_like(x) for x in q]
+    dk = [torch.empty_like(x) for x in k]
+    dqo = [torch.empty_like(t) for t in qa]
+    dko = [torch.empty_like(t) for t in ka]
+    for _ in range(2):
+        B.ulysses_a2a_4d_qk_fused_host(plan, hq, hk, hqo, hko, dq, dk, dqo, dko, w, EPS, THETA)
+        torch.cuda.synchronize()
+        for h, dev in zip(hqo + hko, qa + ka):
+            assert torch.equal(h.view(torch.int16), dev.cpu().view(torch.int16))
+
+
 def test_fused_zero_rows_stay_zero():
     """All-zero head rows normalise to zero (eps > 0) and stay zero under rotation."""
     g = (2, 1, [5, 3], [2, 2], 128)

@@ -220,6 +220,35 @@ def test_end_to_end_host_buffers(oracle):
             assert np.array_equal(h.view(torch.int16).numpy().view(np.uint16), w)
 
 
+@pytest.mark.parametrize("g", [(4, 2, [3, 0, 5, 1], [2, 3, 0, 1], 64, "bfloat16"),
+                               (3, 1, [7, 2, 9], [1, 1, 2], 16, "float32"),
+                               (8, 1, [1] * 8, [5] * 8, 128, "bfloat16")],
+                         ids=["zero_splits_b2", "fp32", "one_row_per_rank"])
+def test_end_to_end_host_buffers_edges(oracle, g):
+    """The chunked host-buffer path on zero splits, b > 1, shards shorter than the chunk count:
+    identical to the oracle, and twice in a row on the same buffers."""
+    W, b, seq, heads, d, dtype = g
+    plan = B.ulysses_plan(*g)
+    td = wl.torch_dtype(dtype)
+    N, S = sum(heads), sum(seq)
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(zlib.crc32(str(g).encode()))
+    for mode in (0, 1):
+        in_shapes = [(b, s, N, d) for s in seq] if mode == 0 else [(b, S, n, d) for n in heads]
+        out_shapes = [(b, S, n, d) for n in heads] if mode == 0 else [(b, s, N, d) for s in seq]
+        src = [torch.randn(sh, generator=gen).to(td) for sh in in_shapes]
+        host_in = [x.pin_memory() for x in src]
+        host_out = [torch.full(sh, 7, dtype=td).pin_memory() for sh in out_shapes]
+        dev_in = [torch.empty(sh, dtype=td, device="cuda") for sh in in_shapes]
+        dev_out = [torch.empty(sh, dtype=td, device="cuda") for sh in out_shapes]
+        want = oracle.a2a_4d([host_raw(x) for x in src], seq, heads, mode)
+        for _ in range(2):
+            B.ulysses_a2a_4d_host(plan, mode, host_in, host_out, dev_in, dev_out)
+            torch.cuda.synchronize()
+            for h, w in zip(host_out, want):
+                assert np.array_equal(host_raw(h), w)
+
+
 def test_misaligned_and_overlapping_on_device():
     plan = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "bfloat16")
     x = [torch.zeros(1, 4, 4, 64, dtype=torch.bfloat16, device="cuda") for _ in range(2)]

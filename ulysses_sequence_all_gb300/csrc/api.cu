@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "../../include/ulysses.h"
@@ -103,64 +104,234 @@ void side_bytes(const Plan& p, int mode, int64_t* in_b, int64_t* out_b)
     }
 }
 
-int relayout_impl(const Plan& p, int mode, int engine, const void* const* in_ptrs,
-                  void* const* out_ptrs, cudaStream_t stream)
+// Argument checks of a relayout call (no CUDA call).
+int relayout_check(const Plan& p, int mode, int engine, const void* const* in_ptrs,
+                   void* const* out_ptrs)
 {
     if (mode != 0 && mode != 1) return ULY_EINVAL;
-    if (engine == ULY_ENGINE_AUTO) engine = ULY_ENGINE_TMA;
-    if (engine != ULY_ENGINE_TMA && engine != ULY_ENGINE_VEC) return ULY_EINVAL;
+    if (engine != ULY_ENGINE_AUTO && engine != ULY_ENGINE_TMA && engine != ULY_ENGINE_VEC)
+        return ULY_EINVAL;
     int64_t in_b[kMaxW], out_b[kMaxW];
     side_bytes(p, mode, in_b, out_b);
     int rc = check_ptrs(in_ptrs, in_b, p.W);
     if (rc) return rc;
     rc = check_ptrs(const_cast<const void* const*>(out_ptrs), out_b, p.W);
     if (rc) return rc;
-    rc = check_overlap(in_ptrs, in_b, p.W, const_cast<const void* const*>(out_ptrs), out_b, p.W);
-    if (rc) return rc;
-    int64_t C = 0;
-    rc = num_chunks(p, &C);
-    if (rc) return rc;
-    DeviceInfo dev;
-    rc = current_device(&dev);
-    if (rc) return rc;
+    return check_overlap(in_ptrs, in_b, p.W, const_cast<const void* const*>(out_ptrs), out_b, p.W);
+}
 
+// One launch of the relayout over the given rows of every sequence shard.
+int relayout_rows(const Plan& p, int mode, int engine, const void* const* in_ptrs,
+                  void* const* out_ptrs, const ChunkRows& rows, cudaStream_t stream,
+                  const DeviceInfo& dev)
+{
+    if (engine == ULY_ENGINE_AUTO) engine = ULY_ENGINE_TMA;
+    uint8_t* seq[kMaxW];
+    uint8_t* head[kMaxW];
+    for (int k = 0; k < p.W; ++k) {
+        uint8_t* in = static_cast<uint8_t*>(const_cast<void*>(in_ptrs[k]));
+        uint8_t* out = static_cast<uint8_t*>(out_ptrs[k]);
+        seq[k] = mode == 0 ? in : out;
+        head[k] = mode == 0 ? out : in;
+    }
     // TMA engine: whole-row tiles when a row fits a stage, row-run segments otherwise
     const int64_t tile_rows = engine == ULY_ENGINE_TMA ? relayout_tile_rows(p.N * p.d * p.e) : 0;
+    cudaError_t e;
     if (tile_rows > 0) {
         RowTileArgs t;
         std::memset(&t, 0, sizeof t);
         for (int k = 0; k < p.W; ++k) {
-            uint8_t* in = static_cast<uint8_t*>(const_cast<void*>(in_ptrs[k]));
-            uint8_t* out = static_cast<uint8_t*>(out_ptrs[k]);
-            t.seq_ptr[k] = mode == 0 ? in : out;
-            t.head_ptr[k] = mode == 0 ? out : in;
+            t.seq_ptr[k] = seq[k];
+            t.head_ptr[k] = head[k];
         }
-        for (int64_t c = 0; c < C; ++c) {
-            ChunkRows rows;
-            chunk_rows(p, C, c, &rows);
-            build_row_tiles(p, rows, tile_rows, &t);
-            cudaError_t e = relayout_rows_launch(t, mode, stream, dev.device, dev.sm_count);
-            if (e != cudaSuccess) return cuda_fail(e);
+        build_row_tiles(p, rows, tile_rows, &t);
+        e = relayout_rows_launch(t, mode, stream, dev.device, dev.sm_count);
+    } else {
+        RelayoutArgs a;
+        std::memset(&a, 0, sizeof a);
+        for (int k = 0; k < p.W; ++k) {
+            a.seq_ptr[k] = seq[k];
+            a.head_ptr[k] = head[k];
         }
-        return ULY_OK;
+        build_relayout_units(p, rows, relayout_unit_bytes(engine), &a);
+        e = relayout_launch(a, mode, engine, stream, dev.device, dev.sm_count);
     }
-    RelayoutArgs a;
-    std::memset(&a, 0, sizeof a);
-    for (int k = 0; k < p.W; ++k) {
-        uint8_t* in = static_cast<uint8_t*>(const_cast<void*>(in_ptrs[k]));
-        uint8_t* out = static_cast<uint8_t*>(out_ptrs[k]);
-        a.seq_ptr[k] = mode == 0 ? in : out;
-        a.head_ptr[k] = mode == 0 ? out : in;
-    }
-    const int64_t unit_bytes = relayout_unit_bytes(engine);
+    return e == cudaSuccess ? ULY_OK : cuda_fail(e);
+}
+
+int relayout_impl(const Plan& p, int mode, int engine, const void* const* in_ptrs,
+                  void* const* out_ptrs, cudaStream_t stream)
+{
+    int rc = relayout_check(p, mode, engine, in_ptrs, out_ptrs);
+    if (rc) return rc;
+    int64_t C = 0;
+    if ((rc = num_chunks(p, &C))) return rc;
+    DeviceInfo dev;
+    if ((rc = current_device(&dev))) return rc;
     for (int64_t c = 0; c < C; ++c) {
         ChunkRows rows;
         chunk_rows(p, C, c, &rows);
-        build_relayout_units(p, rows, unit_bytes, &a);
-        cudaError_t e = relayout_launch(a, mode, engine, stream, dev.device, dev.sm_count);
-        if (e != cudaSuccess) return cuda_fail(e);
+        if ((rc = relayout_rows(p, mode, engine, in_ptrs, out_ptrs, rows, stream, dev))) return rc;
     }
     return ULY_OK;
+}
+
+// Checks of a fused QK call (no CUDA call) and its argument block, without the unit tables.
+int fused_prepare(const Plan& p, const void* const* q_in, const void* const* k_in,
+                  void* const* q_out, void* const* k_out, const float* rms_w, float eps,
+                  float rope_theta, FusedArgs* a, int64_t* tokens_per_unit)
+{
+    if (p.dtype != ULY_BF16) return ULY_EINVAL;
+    if (!(p.d == 8 || p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128 || p.d == 256))
+        return ULY_EINVAL;
+    if (p.S >= (int64_t(1) << 24)) return ULY_EINVAL;  // positions must be exact in fp32
+    if (!(eps >= 0.0f) || !(rope_theta > 0.0f)) return ULY_EINVAL;
+    if (!rms_w) return ULY_EINVAL;
+    if (!aligned16(rms_w)) return ULY_EALIGN;
+    int64_t in_b[kMaxW], out_b[kMaxW];
+    side_bytes(p, 0, in_b, out_b);
+    int rc;
+    if ((rc = check_ptrs(q_in, in_b, p.W)) || (rc = check_ptrs(k_in, in_b, p.W)) ||
+        (rc = check_ptrs(const_cast<const void* const*>(q_out), out_b, p.W)) ||
+        (rc = check_ptrs(const_cast<const void* const*>(k_out), out_b, p.W)))
+        return rc;
+    // all four tensor sets at once: 2W inputs (plus the weights) against 2W outputs
+    const void* ins[2 * kMaxW + 1];
+    int64_t ins_b[2 * kMaxW + 1];
+    const void* outs[2 * kMaxW];
+    int64_t outs_b[2 * kMaxW];
+    for (int k = 0; k < p.W; ++k) {
+        ins[k] = q_in[k];
+        ins[p.W + k] = k_in[k];
+        ins_b[k] = ins_b[p.W + k] = in_b[k];
+        outs[k] = q_out[k];
+        outs[p.W + k] = k_out[k];
+        outs_b[k] = outs_b[p.W + k] = out_b[k];
+    }
+    ins[2 * p.W] = rms_w;
+    ins_b[2 * p.W] = 2 * p.d * int64_t(sizeof(float));
+    if ((rc = check_overlap(ins, ins_b, 2 * p.W + 1, outs, outs_b, 2 * p.W))) return rc;
+    int stages = 0;
+    uint32_t stage_bytes = 0;
+    fused_geometry(p, tokens_per_unit, &stages, &stage_bytes);
+    if (stages == 0) return ULY_EINVAL;  // one token's q and k rows do not fit the stages
+    std::memset(a, 0, sizeof *a);
+    for (int k = 0; k < p.W; ++k) {
+        a->q_in[k] = static_cast<const uint8_t*>(q_in[k]);
+        a->k_in[k] = static_cast<const uint8_t*>(k_in[k]);
+        a->q_out[k] = static_cast<uint8_t*>(q_out[k]);
+        a->k_out[k] = static_cast<uint8_t*>(k_out[k]);
+    }
+    a->rms_w = rms_w;
+    a->eps = eps;
+    a->stages = stages;
+    a->stage_bytes = stage_bytes;
+    rope_turns(p.d, double(rope_theta), a->turn_hi, a->turn_lo);
+    return ULY_OK;
+}
+
+// One launch of the fused kernel over the given rows of every sequence shard.
+int fused_rows(const Plan& p, FusedArgs* a, int64_t tokens_per_unit, const ChunkRows& rows,
+               cudaStream_t stream, const DeviceInfo& dev)
+{
+    build_fused_units(p, rows, tokens_per_unit, a);
+    cudaError_t e = fused_launch(*a, stream, dev.device, dev.sm_count);
+    return e == cudaSuccess ? ULY_OK : cuda_fail(e);
+}
+
+// ---- host-buffer entry points: chunked copy-in / kernel / copy-out pipeline ---------------------
+// Host<->device copies run on the copy engines in both directions at once, so the call is cut
+// into sequence chunks: chunk c's inputs are copied in and relaid out on the caller's stream, then
+// an event lets an auxiliary stream copy chunk c's outputs back while chunk c+1 is copied in. The
+// caller's stream finally waits for the auxiliary stream, so from the caller's side the whole call
+// is ordered on its stream like any other. The auxiliary stream and events are created once per
+// device, on first use, and reused; a mutex serialises the enqueueing of concurrent calls.
+constexpr int kPipeEvents = 4;
+#ifndef ULY_HOST_CHUNKS
+#define ULY_HOST_CHUNKS 8
+#endif
+constexpr int64_t kPipeChunks = ULY_HOST_CHUNKS;
+
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t aux = nullptr;
+    cudaEvent_t chunk_done[kPipeEvents] = {};
+    cudaEvent_t copied_out = nullptr;
+};
+
+std::mutex g_pipe_mu;
+HostPipe g_pipe[64];
+
+int host_pipe(int device, HostPipe** out)  // caller holds g_pipe_mu
+{
+    HostPipe& hp = g_pipe[device];
+    if (!hp.ready) {
+        cudaError_t e = cudaStreamCreateWithFlags(&hp.aux, cudaStreamNonBlocking);
+        for (int i = 0; e == cudaSuccess && i < kPipeEvents; ++i)
+            e = cudaEventCreateWithFlags(&hp.chunk_done[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.copied_out, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e);
+        hp.ready = true;
+    }
+    *out = &hp;
+    return ULY_OK;
+}
+
+// Rows [lo_q, lo_q + cnt_q) of every rank's sequence-side tensor (b, s_q, N, d), per batch index.
+cudaError_t copy_seq_rows(const Plan& p, const ChunkRows& rows, void* const* dst,
+                          const void* const* src, cudaMemcpyKind kind, cudaStream_t st)
+{
+    const int64_t row = p.N * p.d * p.e;
+    for (int q = 0; q < p.W; ++q) {
+        if (rows.cnt[q] == 0) continue;
+        for (int64_t bb = 0; bb < p.b; ++bb) {
+            const int64_t off = (bb * p.s[q] + rows.lo[q]) * row;
+            cudaError_t e = cudaMemcpyAsync(static_cast<uint8_t*>(dst[q]) + off,
+                                            static_cast<const uint8_t*>(src[q]) + off,
+                                            size_t(rows.cnt[q] * row), kind, st);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return cudaSuccess;
+}
+
+// The same rows on every rank's head-side tensor (b, S, n_r, d): rows seq_off(q) + [lo_q, ...).
+cudaError_t copy_head_rows(const Plan& p, const ChunkRows& rows, void* const* dst,
+                           const void* const* src, cudaMemcpyKind kind, cudaStream_t st)
+{
+    for (int r = 0; r < p.W; ++r) {
+        const int64_t row = p.n[r] * p.d * p.e;
+        if (row == 0) continue;
+        for (int64_t bb = 0; bb < p.b; ++bb)
+            for (int q = 0; q < p.W; ++q) {
+                if (rows.cnt[q] == 0) continue;
+                const int64_t off = (bb * p.S + p.seq_off[q] + rows.lo[q]) * row;
+                cudaError_t e = cudaMemcpyAsync(static_cast<uint8_t*>(dst[r]) + off,
+                                                static_cast<const uint8_t*>(src[r]) + off,
+                                                size_t(rows.cnt[q] * row), kind, st);
+                if (e != cudaSuccess) return e;
+            }
+    }
+    return cudaSuccess;
+}
+
+// The host pipeline cuts the global sequence into ranges of `span` rows (about kPipeChunks of
+// them, within the chunk cap): a range touches one or two sequence shards and is one contiguous
+// span of every head-side tensor, so each chunk needs few, large copies.
+struct PipeChunks {
+    int64_t span = 0;
+    int64_t count(const Plan& p) const { return (p.S + span - 1) / span; }
+    void rows(const Plan& p, int64_t c, ChunkRows* out) const
+    {
+        const int64_t lo = c * span;
+        global_chunk_rows(p, lo, lo + span < p.S ? lo + span : p.S, out);
+    }
+};
+
+int pipe_chunks(const Plan& p, PipeChunks* pc)
+{
+    pc->span = global_chunk_span(p, kPipeChunks);
+    return pc->span > 0 ? ULY_OK : ULY_ECHUNK;
 }
 
 }  // namespace
@@ -248,66 +419,18 @@ int ulysses_a2a_4d_qk_fused(ulysses_plan_t plan, const void* const* q_in, const 
 {
     if (!plan) return ULY_EINVAL;
     const Plan& p = plan->p;
-    if (p.dtype != ULY_BF16) return ULY_EINVAL;
-    if (!(p.d == 8 || p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128 || p.d == 256))
-        return ULY_EINVAL;
-    if (p.S >= (int64_t(1) << 24)) return ULY_EINVAL;  // positions must be exact in fp32
-    if (!(eps >= 0.0f) || !(rope_theta > 0.0f)) return ULY_EINVAL;
-    if (!rms_w) return ULY_EINVAL;
-    if (!aligned16(rms_w)) return ULY_EALIGN;
-    int64_t in_b[kMaxW], out_b[kMaxW];
-    side_bytes(p, 0, in_b, out_b);
-    int rc;
-    if ((rc = check_ptrs(q_in, in_b, p.W)) || (rc = check_ptrs(k_in, in_b, p.W)) ||
-        (rc = check_ptrs(const_cast<const void* const*>(q_out), out_b, p.W)) ||
-        (rc = check_ptrs(const_cast<const void* const*>(k_out), out_b, p.W)))
-        return rc;
-    // all four tensor sets at once: 2W inputs (plus the weights) against 2W outputs
-    const void* ins[2 * kMaxW + 1];
-    int64_t ins_b[2 * kMaxW + 1];
-    const void* outs[2 * kMaxW];
-    int64_t outs_b[2 * kMaxW];
-    for (int k = 0; k < p.W; ++k) {
-        ins[k] = q_in[k];
-        ins[p.W + k] = k_in[k];
-        ins_b[k] = ins_b[p.W + k] = in_b[k];
-        outs[k] = q_out[k];
-        outs[p.W + k] = k_out[k];
-        outs_b[k] = outs_b[p.W + k] = out_b[k];
-    }
-    ins[2 * p.W] = rms_w;
-    ins_b[2 * p.W] = 2 * p.d * int64_t(sizeof(float));
-    rc = check_overlap(ins, ins_b, 2 * p.W + 1, outs, outs_b, 2 * p.W);
-    if (rc) return rc;
+    FusedArgs a;
     int64_t T = 0;
-    int stages = 0;
-    uint32_t stage_bytes = 0;
-    fused_geometry(p, &T, &stages, &stage_bytes);
-    if (stages == 0) return ULY_EINVAL;  // one token's q and k rows do not fit twice in smem
+    int rc = fused_prepare(p, q_in, k_in, q_out, k_out, rms_w, eps, rope_theta, &a, &T);
+    if (rc) return rc;
     int64_t C = 0;
     if ((rc = num_chunks(p, &C))) return rc;
     DeviceInfo dev;
     if ((rc = current_device(&dev))) return rc;
-
-    FusedArgs a;
-    std::memset(&a, 0, sizeof a);
-    for (int k = 0; k < p.W; ++k) {
-        a.q_in[k] = static_cast<const uint8_t*>(q_in[k]);
-        a.k_in[k] = static_cast<const uint8_t*>(k_in[k]);
-        a.q_out[k] = static_cast<uint8_t*>(q_out[k]);
-        a.k_out[k] = static_cast<uint8_t*>(k_out[k]);
-    }
-    a.rms_w = rms_w;
-    a.eps = eps;
-    a.stages = stages;
-    a.stage_bytes = stage_bytes;
-    rope_turns(p.d, double(rope_theta), a.turn_hi, a.turn_lo);
     for (int64_t c = 0; c < C; ++c) {
         ChunkRows rows;
         chunk_rows(p, C, c, &rows);
-        build_fused_units(p, rows, T, &a);
-        cudaError_t e = fused_launch(a, static_cast<cudaStream_t>(stream), dev.device, dev.sm_count);
-        if (e != cudaSuccess) return cuda_fail(e);
+        if ((rc = fused_rows(p, &a, T, rows, static_cast<cudaStream_t>(stream), dev))) return rc;
     }
     return ULY_OK;
 }
@@ -331,20 +454,36 @@ int ulysses_a2a_4d_host(ulysses_plan_t plan, int mode, const void* const* host_i
     rc = check_overlap(const_cast<const void* const*>(dev_in), in_b, p.W,
                        const_cast<const void* const*>(dev_out), out_b, p.W);
     if (rc) return rc;
+    PipeChunks pc;
+    if ((rc = pipe_chunks(p, &pc))) return rc;
+    const int64_t C = pc.count(p);
+    DeviceInfo dev;
+    if ((rc = current_device(&dev))) return rc;
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe* hp = nullptr;
+    if ((rc = host_pipe(dev.device, &hp))) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    for (int k = 0; k < p.W; ++k) {
-        if (!in_b[k]) continue;
-        cudaError_t e = cudaMemcpyAsync(dev_in[k], host_in[k], size_t(in_b[k]), cudaMemcpyHostToDevice, st);
+    const void* const* din = const_cast<const void* const*>(dev_in);
+    for (int64_t c = 0; c < C; ++c) {
+        ChunkRows rows;
+        pc.rows(p, c, &rows);
+        cudaError_t e = mode == 0
+                            ? copy_seq_rows(p, rows, dev_in, host_in, cudaMemcpyHostToDevice, st)
+                            : copy_head_rows(p, rows, dev_in, host_in, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if ((rc = relayout_rows(p, mode, ULY_ENGINE_AUTO, din, dev_out, rows, st, dev))) return rc;
+        cudaEvent_t done = hp->chunk_done[c % kPipeEvents];
+        if ((e = cudaEventRecord(done, st)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(hp->aux, done, 0)) != cudaSuccess)
+            return cuda_fail(e);
+        const void* const* dout = const_cast<const void* const*>(dev_out);
+        e = mode == 0 ? copy_head_rows(p, rows, host_out, dout, cudaMemcpyDeviceToHost, hp->aux)
+                      : copy_seq_rows(p, rows, host_out, dout, cudaMemcpyDeviceToHost, hp->aux);
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    rc = relayout_impl(p, mode, ULY_ENGINE_AUTO, const_cast<const void* const*>(dev_in), dev_out, st);
-    if (rc) return rc;
-    for (int k = 0; k < p.W; ++k) {
-        if (!out_b[k]) continue;
-        cudaError_t e = cudaMemcpyAsync(host_out[k], dev_out[k], size_t(out_b[k]), cudaMemcpyDeviceToHost, st);
-        if (e != cudaSuccess) return cuda_fail(e);
-    }
-    return ULY_OK;
+    cudaError_t e = cudaEventRecord(hp->copied_out, hp->aux);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hp->copied_out, 0);
+    return e == cudaSuccess ? ULY_OK : cuda_fail(e);
 }
 
 int ulysses_a2a_4d_qk_fused_host(ulysses_plan_t plan, const void* const* q_host_in,
@@ -363,30 +502,40 @@ int ulysses_a2a_4d_qk_fused_host(ulysses_plan_t plan, const void* const* q_host_
             (out_b[k] && (!q_host_out[k] || !k_host_out[k])))
             return ULY_EINVAL;
     }
+    FusedArgs a;
+    int64_t T = 0;
+    int rc = fused_prepare(p, const_cast<const void* const*>(q_in), const_cast<const void* const*>(k_in),
+                           q_out, k_out, rms_w, eps, rope_theta, &a, &T);
+    if (rc) return rc;
+    PipeChunks pc;
+    if ((rc = pipe_chunks(p, &pc))) return rc;
+    const int64_t C = pc.count(p);
+    DeviceInfo dev;
+    if ((rc = current_device(&dev))) return rc;
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe* hp = nullptr;
+    if ((rc = host_pipe(dev.device, &hp))) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // the device call validates everything device-side; check pointers before the first copy
-    int rc = check_ptrs(const_cast<const void* const*>(q_in), in_b, p.W);
-    if (!rc) rc = check_ptrs(const_cast<const void* const*>(k_in), in_b, p.W);
-    if (rc) return rc;
-    for (int k = 0; k < p.W; ++k) {
-        if (!in_b[k]) continue;
-        cudaError_t e = cudaMemcpyAsync(q_in[k], q_host_in[k], size_t(in_b[k]), cudaMemcpyHostToDevice, st);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(k_in[k], k_host_in[k], size_t(in_b[k]), cudaMemcpyHostToDevice, st);
+    const void* const* qo = const_cast<const void* const*>(q_out);
+    const void* const* ko = const_cast<const void* const*>(k_out);
+    for (int64_t c = 0; c < C; ++c) {
+        ChunkRows rows;
+        pc.rows(p, c, &rows);
+        cudaError_t e = copy_seq_rows(p, rows, q_in, q_host_in, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = copy_seq_rows(p, rows, k_in, k_host_in, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if ((rc = fused_rows(p, &a, T, rows, st, dev))) return rc;
+        cudaEvent_t done = hp->chunk_done[c % kPipeEvents];
+        if ((e = cudaEventRecord(done, st)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(hp->aux, done, 0)) != cudaSuccess)
+            return cuda_fail(e);
+        e = copy_head_rows(p, rows, q_host_out, qo, cudaMemcpyDeviceToHost, hp->aux);
+        if (e == cudaSuccess) e = copy_head_rows(p, rows, k_host_out, ko, cudaMemcpyDeviceToHost, hp->aux);
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    rc = ulysses_a2a_4d_qk_fused(plan, const_cast<const void* const*>(q_in),
-                                 const_cast<const void* const*>(k_in), q_out, k_out, rms_w, eps,
-                                 rope_theta, stream);
-    if (rc) return rc;
-    for (int k = 0; k < p.W; ++k) {
-        if (!out_b[k]) continue;
-        cudaError_t e = cudaMemcpyAsync(q_host_out[k], q_out[k], size_t(out_b[k]), cudaMemcpyDeviceToHost, st);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(k_host_out[k], k_out[k], size_t(out_b[k]), cudaMemcpyDeviceToHost, st);
-        if (e != cudaSuccess) return cuda_fail(e);
-    }
-    return ULY_OK;
+    cudaError_t e = cudaEventRecord(hp->copied_out, hp->aux);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hp->copied_out, 0);
+    return e == cudaSuccess ? ULY_OK : cuda_fail(e);
 }
 
 int ulysses_device_status(unsigned* status)

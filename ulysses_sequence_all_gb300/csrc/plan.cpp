@@ -4,6 +4,7 @@
 // plan, testable without a GPU).
 #include "plan.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 
@@ -113,6 +114,26 @@ void chunk_rows(const Plan& p, int64_t C, int64_t c, ChunkRows* out)
         out->lo[q] = lo;
         out->cnt[q] = hi - lo;
     }
+}
+
+void global_chunk_rows(const Plan& p, int64_t lo, int64_t hi, ChunkRows* out)
+{
+    std::memset(out, 0, sizeof *out);
+    for (int q = 0; q < p.W; ++q) {
+        const int64_t a = std::min(std::max(lo - p.seq_off[q], int64_t(0)), p.s[q]);
+        const int64_t b = std::min(std::max(hi - p.seq_off[q], int64_t(0)), p.s[q]);
+        out->lo[q] = a;
+        out->cnt[q] = b - a;
+    }
+}
+
+int64_t global_chunk_span(const Plan& p, int64_t target_chunks)
+{
+    const int64_t seq_row = p.b * p.N * p.d * p.e;  // one global row, all ranks' heads, all batches
+    if (seq_row > p.chunk_cap) return 0;
+    int64_t span = (p.S + target_chunks - 1) / target_chunks;
+    const int64_t cap_rows = p.chunk_cap / seq_row;
+    return span < cap_rows ? (span > 0 ? span : 1) : cap_rows;
 }
 
 void build_relayout_units(const Plan& p, const ChunkRows& rows, int64_t unit_bytes, RelayoutArgs* a)

@@ -32,6 +32,12 @@ int64_t seq_side_bytes(const Plan& p, int q);   // rank q's (b, s_q, N, d) tenso
 int64_t head_side_bytes(const Plan& p, int r);  // rank r's (b, S, n_r, d) tensor
 int num_chunks(const Plan& p, int64_t* n_chunks);  // ULY_OK or ULY_ECHUNK
 void chunk_rows(const Plan& p, int64_t n_chunks, int64_t chunk, ChunkRows* out);
+// Rows of each shard inside the global sequence range [lo, hi) (the shards tile [0, S) in rank
+// order): a range touches few shards and is contiguous on every head-side tensor.
+void global_chunk_rows(const Plan& p, int64_t lo, int64_t hi, ChunkRows* out);
+// Global rows per range so that about target_chunks ranges cover S and no rank reads or writes
+// more than the chunk cap in one launch; 0 when one global row already exceeds the cap.
+int64_t global_chunk_span(const Plan& p, int64_t target_chunks);
 
 // ---- relayout kernels' argument block (passed by value, lives in the parameter bank) ----------
 // A work unit is a block of up to rows_per_unit[r] consecutive rows of one segment (q, r) and one
