@@ -73,6 +73,8 @@ SMALL = [
     (4, 1, [3, 4, 5, 6], [2, 2, 1, 3], 32),
     (2, 1, [7, 2], [3, 1], 8),
     (2, 1, [75000, 600], [1, 1], 128),   # positions up to 75,599 on every pair
+    (2, 1, [3, 2], [64, 64], 128),       # 64 KiB per token of q and k: fewer CTAs per SM
+    (1, 1, [4], [100], 256),             # 100 KiB per token: one CTA per SM
 ]
 
 

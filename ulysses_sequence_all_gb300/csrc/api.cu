@@ -20,7 +20,8 @@ cudaError_t relayout_status(unsigned* status, bool clear);
 int64_t relayout_tile_rows(int64_t row_bytes);
 cudaError_t relayout_rows_launch(const RowTileArgs& a, int mode, cudaStream_t stream, int device,
                                  int sm_count);
-void fused_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages, uint32_t* stage_bytes);
+void fused_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages, uint32_t* stage_bytes,
+                    int* ctas_per_sm);
 cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count);
 cudaError_t fused_status(unsigned* status, bool clear);
 cudaError_t selftest_timeout_launch(uint64_t limit_ns, cudaStream_t stream);
@@ -211,11 +212,12 @@ int fused_prepare(const Plan& p, const void* const* q_in, const void* const* k_i
     ins[2 * p.W] = rms_w;
     ins_b[2 * p.W] = 2 * p.d * int64_t(sizeof(float));
     if ((rc = check_overlap(ins, ins_b, 2 * p.W + 1, outs, outs_b, 2 * p.W))) return rc;
-    int stages = 0;
+    int stages = 0, ctas_per_sm = 1;
     uint32_t stage_bytes = 0;
-    fused_geometry(p, tokens_per_unit, &stages, &stage_bytes);
+    fused_geometry(p, tokens_per_unit, &stages, &stage_bytes, &ctas_per_sm);
     if (stages == 0) return ULY_EINVAL;  // one token's q and k rows do not fit the stages
     std::memset(a, 0, sizeof *a);
+    a->ctas_per_sm = ctas_per_sm;
     for (int k = 0; k < p.W; ++k) {
         a->q_in[k] = static_cast<const uint8_t*>(q_in[k]);
         a->k_in[k] = static_cast<const uint8_t*>(k_in[k]);

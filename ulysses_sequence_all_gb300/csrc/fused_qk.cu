@@ -15,13 +15,16 @@
 //    that sees the phase complete sees both the table and the data;
 //  * storer: when the consumers report a unit done ("computed"), the lanes issue one
 //    cp.async.bulk store per (token, q|k, destination rank): n_r heads that are contiguous in the
-//    stage and in the destination; kFusedDrain units later, once those stores have read shared
-//    memory, the stage is handed back to the loader ("empty");
+//    stage and in the destination; as soon as those stores have read shared memory (kFusedDrain
+//    units later; 0 by default, so right away) the stage is handed back to the loader ("empty");
 //  * consumers: half of them take q rows, half k rows. A group of d/8 lanes holds one head row
-//    (8 values per lane) and each group keeps kIlp rows in flight; the sum of squares is reduced
-//    with xor shuffles inside the group, the weight and rotation are applied in registers, and the
-//    bf16 result overwrites its input in shared memory. Each consumer warp then fences its writes
-//    for the async proxy and arrives on "computed".
+//    (8 values per lane, as packed fp32 pairs) and each group keeps kIlp rows in flight; the sum
+//    of squares is reduced with xor shuffles inside the group, the weight and rotation are
+//    applied in registers, and the bf16 result overwrites its input in shared memory. Each
+//    consumer warp then fences its writes for the async proxy and arrives on "computed".
+// Measured at the Wan shape, throughput grows with the number of CTAs issuing bulk copies per SM
+// more than with ring depth, so the default footprint is small (2 stages of one token's q and k)
+// and 4 CTAs share an SM; wider rows fall back to fewer CTAs per SM (see fused_geometry).
 //
 // RoPE angles: p * theta^(-2j/d) reaches ~75,600 rad at the Wan shape, where an fp32 product
 // alone is off by ~5e-3 rad. The angle is formed in turns (units of 2 pi): the host supplies
@@ -41,7 +44,7 @@ namespace uly {
 static __device__ unsigned g_fused_status;
 
 #ifndef ULY_FUSED_CTAS_PER_SM
-#define ULY_FUSED_CTAS_PER_SM 3
+#define ULY_FUSED_CTAS_PER_SM 4
 #endif
 #ifndef ULY_FUSED_CONSUMER_WARPS
 #define ULY_FUSED_CONSUMER_WARPS 4
@@ -50,19 +53,25 @@ static __device__ unsigned g_fused_status;
 #define ULY_FUSED_STAGE_TARGET 20480
 #endif
 #ifndef ULY_FUSED_MAX_STAGES
-#define ULY_FUSED_MAX_STAGES 3
+#define ULY_FUSED_MAX_STAGES 2
 #endif
 #ifndef ULY_FUSED_DRAIN
-#define ULY_FUSED_DRAIN 1
+#define ULY_FUSED_DRAIN 0
+#endif
+#ifndef ULY_FUSED_EVICT_FIRST  // loads carry an L2 evict-first hint (inputs are read once)
+#define ULY_FUSED_EVICT_FIRST 0
 #endif
 constexpr int kFusedCtasPerSm = ULY_FUSED_CTAS_PER_SM;
 constexpr int kFusedMaxStages = ULY_FUSED_MAX_STAGES;
 constexpr int kFusedDrain = ULY_FUSED_DRAIN;  // store groups left draining when a stage refills
-// an SM holds 228 KiB of shared memory, 1 KiB of it reserved per resident CTA
-constexpr int kFusedSmemBudget = (227 * 1024) / kFusedCtasPerSm - 1024;
+// an SM holds 228 KiB of shared memory, 1 KiB of it reserved per resident CTA; one CTA may use
+// at most 227 KiB of dynamic shared memory
+constexpr int kSmemPerSm = 228 * 1024;
+constexpr int kSmemReservedPerCta = 1024;
+constexpr int kSmemPerCtaMax = 227 * 1024;
 constexpr int kFusedHeader = 256;  // three barriers per stage
 static_assert(3 * 8 * kFusedMaxStages <= kFusedHeader, "stage barriers must fit the header");
-static_assert(kFusedDrain >= 1 && kFusedDrain < kFusedMaxStages, "need a load in flight");
+static_assert(kFusedDrain >= 0 && kFusedDrain < kFusedMaxStages, "need a load in flight");
 static_assert(ULY_FUSED_CONSUMER_WARPS % 2 == 0, "consumer warps split evenly between q and k");
 // warp roles
 constexpr int kLoaderWarp = 0, kTableWarp = 1, kStorerWarp = 2, kFirstConsumerWarp = 3;
@@ -192,8 +201,14 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
             const int64_t off = (t.bb * a.s[t.q] + t.i0) * row_bytes;
             uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
             mbar_arrive_expect_tx(&full[s], 2 * bytes);
+#if ULY_FUSED_EVICT_FIRST
             bulk_g2s_hint(dst, a.q_in[t.q] + off, bytes, &full[s], policy);
             bulk_g2s_hint(dst + bytes, a.k_in[t.q] + off, bytes, &full[s], policy);
+#else
+            (void)policy;
+            bulk_g2s(dst, a.q_in[t.q] + off, bytes, &full[s]);
+            bulk_g2s(dst + bytes, a.k_in[t.q] + off, bytes, &full[s]);
+#endif
         }
         // do not leave while copies into this CTA's shared memory may be in flight
         for (int64_t jj = (j > K ? j - K : 0); jj < j; ++jj) {
@@ -373,22 +388,36 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
 }
 
 // Stage geometry for a plan: tokens per unit and stage count (0 stages: does not fit).
-void fused_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages, uint32_t* stage_bytes)
+// Stage geometry for a plan: tokens per unit, stage count and CTAs per SM (0 stages: one
+// token's q and k rows do not fit even one CTA per SM). The preferred footprint lets
+// kFusedCtasPerSm CTAs share an SM; narrower units, fewer stages, then fewer CTAs per SM are
+// tried in that order.
+void fused_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages, uint32_t* stage_bytes,
+                    int* ctas_per_sm)
 {
     *stages = 0;
     *tokens_per_unit = 1;
     *stage_bytes = 0;
+    *ctas_per_sm = 1;
     const int64_t pair_bytes = 2 * p.N * p.d * 2;  // one token of q and of k
-    int64_t T = ULY_FUSED_STAGE_TARGET / pair_bytes;
-    if (T < 1) T = 1;
-    const int64_t sb = T * pair_bytes;
-    for (int K = kFusedMaxStages; K >= kFusedDrain + 1; --K) {
-        const FusedSmem m = fused_smem_layout(int(p.d), int(T), K, uint32_t(sb));
-        if (sb <= (1 << 20) && m.total <= kFusedSmemBudget) {
-            *tokens_per_unit = T;
-            *stages = K;
-            *stage_bytes = uint32_t(sb);
-            return;
+    int64_t T0 = ULY_FUSED_STAGE_TARGET / pair_bytes;
+    if (T0 < 1) T0 = 1;
+    const int min_k = kFusedDrain + 1 > 2 ? kFusedDrain + 1 : 2;
+    for (int ctas = kFusedCtasPerSm; ctas >= 1; --ctas) {
+        const int budget = kSmemPerSm / ctas - kSmemReservedPerCta;
+        for (int64_t T = T0; T >= 1; T = T > 1 ? T / 2 : 0) {
+            const int64_t sb = T * pair_bytes;
+            if (sb > (1 << 20)) continue;
+            for (int K = kFusedMaxStages; K >= min_k; --K) {
+                const FusedSmem m = fused_smem_layout(int(p.d), int(T), K, uint32_t(sb));
+                if (m.total <= budget && m.total <= kSmemPerCtaMax) {
+                    *tokens_per_unit = T;
+                    *stages = K;
+                    *stage_bytes = uint32_t(sb);
+                    *ctas_per_sm = ctas;
+                    return;
+                }
+            }
         }
     }
 }
@@ -402,7 +431,7 @@ static cudaError_t launch_g(const FusedArgs& a, cudaStream_t stream, int device,
     if (device >= 0 && device < 64 && !(g_fused_smem_set[device] & (1 << bit))) {
         cudaError_t e = cudaFuncSetAttribute(fused_qk_kernel<G>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kFusedSmemBudget);
+                                             kSmemPerCtaMax);
         if (e != cudaSuccess) return e;
         g_fused_smem_set[device] |= 1 << bit;
     }
@@ -414,7 +443,7 @@ static cudaError_t launch_g(const FusedArgs& a, cudaStream_t stream, int device,
 cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count)
 {
     if (a.total_units == 0) return cudaSuccess;
-    int64_t grid = int64_t(sm_count) * kFusedCtasPerSm;
+    int64_t grid = int64_t(sm_count) * (a.ctas_per_sm > 0 ? a.ctas_per_sm : 1);
     if (grid > a.total_units) grid = a.total_units;
     switch (a.d / 8) {
         case 1: return launch_g<1>(a, stream, device, int(grid));

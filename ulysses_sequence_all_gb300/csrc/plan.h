@@ -92,6 +92,7 @@ struct FusedArgs {
     int64_t S, N, b;
     int64_t total_units;
     int32_t W, d, tokens_per_unit, stages;
+    int32_t ctas_per_sm;  // resident CTAs per SM the shared-memory footprint allows
     uint32_t stage_bytes;
     float eps;
     // theta^(-2j/d) / (2 pi) as an unevaluated sum hi + lo of two floats, j < d/2.

@@ -43,7 +43,7 @@ static __device__ unsigned g_relayout_status;
 #ifndef ULY_TMA_LOOKAHEAD
 #define ULY_TMA_LOOKAHEAD 3
 #endif
-static_assert(ULY_TMA_LOOKAHEAD >= 1 && ULY_TMA_LOOKAHEAD < ULY_TMA_STAGES, "lookahead < stages");
+static_assert(ULY_TMA_LOOKAHEAD >= 1 && ULY_TMA_LOOKAHEAD <= ULY_TMA_STAGES, "lookahead <= stages");
 static_assert(ULY_TMA_STAGES <= 16, "stage barriers must fit the barrier area");
 constexpr int kTmaBarrierBytes = 128;  // the stage barriers sit before the first stage
 constexpr int kVecThreads = 256;
