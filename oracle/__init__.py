@@ -73,6 +73,9 @@ class Oracle:
         lib.orc_qk_fused_row.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, ctypes.c_int, _i64,
                                          _i64, _i64, _p, _p, ctypes.c_double, ctypes.c_double, _p]
         lib.orc_qk_fused_row.restype = ctypes.c_int
+        lib.orc_qkv_fused.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, _p, _p, _p,
+                                      ctypes.c_double, ctypes.c_double, _p, _p, _p]
+        lib.orc_qkv_fused.restype = ctypes.c_int
         lib.orc_rmsnorm.argtypes = [_p, _i64, _p, ctypes.c_double, _p]
         lib.orc_rmsnorm.restype = None
         lib.orc_rope.argtypes = [_p, _i64, ctypes.c_double, ctypes.c_double]
@@ -159,6 +162,27 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle rejected the query")
         return y
+
+    def qkv_fused(self, qkv_bf16, seq_splits, head_splits, wq, wk, eps, theta):
+        """Interleaved (b, s_q, 3, N, d) inputs: q and k transformed and placed (double), v placed
+        unchanged (uint16 bf16 bits). Returns (q_outs, k_outs, v_outs), each rank r (b, S, n_r, d)."""
+        W = len(qkv_bf16)
+        b, d = qkv_bf16[0].shape[0], qkv_bf16[0].shape[4]
+        xs = [np.ascontiguousarray(x).view(np.uint16) for x in qkv_bf16]
+        wq64 = np.ascontiguousarray(np.asarray(wq, dtype=np.float64))
+        wk64 = np.ascontiguousarray(np.asarray(wk, dtype=np.float64))
+        shapes = self.out_shapes(b, seq_splits, head_splits, d, 0)
+        qo = [np.empty(s, dtype=np.float64) for s in shapes]
+        ko = [np.empty(s, dtype=np.float64) for s in shapes]
+        vo = [np.empty(s, dtype=np.uint16) for s in shapes]
+        rc = self.lib.orc_qkv_fused(W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
+                                    ctypes.cast(_ptr_array(xs), _p), wq64.ctypes.data,
+                                    wk64.ctypes.data, float(eps), float(theta),
+                                    ctypes.cast(_ptr_array(qo), _p), ctypes.cast(_ptr_array(ko), _p),
+                                    ctypes.cast(_ptr_array(vo), _p))
+        if rc != 0:
+            raise ValueError("oracle rejected the geometry")
+        return qo, ko, vo
 
     def rmsnorm(self, x, w, eps):
         x = np.ascontiguousarray(x, dtype=np.float64)

@@ -334,3 +334,44 @@ void orc_double_to_bf16_array(const double* x, int64_t n, uint16_t* out)
 {
     for (int64_t k = 0; k < n; ++k) out[k] = orc_double_to_bf16(x[k]);
 }
+
+/*
+ * Interleaved packed QKV, the layout a fused QKV projection writes (FastVideo, "Ulysses
+ * performance on GB200": packed QKV): rank q holds one (b, s_q, 3, N, d) bf16 tensor whose plane 0
+ * is q, plane 1 is k and plane 2 is v. q and k rows are transformed as orc_qk_fused_A does (with
+ * wq and wk respectively) and placed where mode 0 puts them (double outputs); v rows are placed by
+ * mode 0 unchanged (bf16 bit patterns). q_out[r], k_out[r], v_out[r] are rank r's (b, S, n_r, d).
+ */
+int orc_qkv_fused(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                  int64_t d, const uint16_t* const* qkv_in, const double* wq, const double* wk,
+                  double eps, double theta, double* const* q_out, double* const* k_out,
+                  uint16_t* const* v_out)
+{
+    if (check_geometry(W, b, seq_splits, head_splits, d) || (d % 2) != 0) return -1;
+    const int64_t S = offset_of(seq_splits, W);
+    const int64_t N = offset_of(head_splits, W);
+    for (int q = 0; q < W; ++q) {
+        const int64_t s_q = seq_splits[q];
+        const int64_t seq_off_q = offset_of(seq_splits, q);
+        for (int64_t bb = 0; bb < b; ++bb)
+            for (int64_t i = 0; i < s_q; ++i)
+                for (int64_t g = 0; g < N; ++g) {
+                    int r = 0;
+                    while (!(g >= offset_of(head_splits, r) &&
+                             g < offset_of(head_splits, r) + head_splits[r]))
+                        ++r;
+                    const int64_t n_r = head_splits[r];
+                    const int64_t h = g - offset_of(head_splits, r);
+                    const int64_t dst_row = ((bb * S + seq_off_q + i) * n_r + h) * d;
+                    const double p = (double)(seq_off_q + i);
+                    /* row (bb, i, plane, g) of rank q's (b, s_q, 3, N, d) tensor */
+                    const uint16_t* qrow = qkv_in[q] + (((bb * s_q + i) * 3 + 0) * N + g) * d;
+                    const uint16_t* krow = qkv_in[q] + (((bb * s_q + i) * 3 + 1) * N + g) * d;
+                    const uint16_t* vrow = qkv_in[q] + (((bb * s_q + i) * 3 + 2) * N + g) * d;
+                    transform_row(qrow, d, wq, eps, p, theta, q_out[r] + dst_row);
+                    transform_row(krow, d, wk, eps, p, theta, k_out[r] + dst_row);
+                    for (int64_t j = 0; j < d; ++j) v_out[r][dst_row + j] = vrow[j];
+                }
+    }
+    return 0;
+}

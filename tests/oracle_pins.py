@@ -358,6 +358,31 @@ def pin_fused_placement_decode(orc, quick=False):
                 assert abs(p - s) < 1e-6, f"rotation angle decodes to p={p}, expected {s}"
 
 
+def pin_qkv_interleaved(orc, quick=False):
+    """Interleaved (b, s, 3, N, d) QKV: torch.unbind of the plane axis gives q, k, v; the result
+    must equal the separately pinned fused transform on q and k and the mode-0 relayout of v."""
+    rng = np.random.default_rng(27)
+    cases = [(2, 1, [3, 2], [2, 1], 8), (3, 2, [2, 0, 3], [1, 2, 1], 16), (1, 1, [4], [3], 8),
+             (4, 1, [1, 2, 1, 2], [2, 0, 1, 1], 8)]
+    for W, b, seq, heads, d in cases:
+        N = sum(heads)
+        qkv = []
+        for s in seq:
+            v = torch.from_numpy(rng.standard_normal((b, s, 3, N, d)).astype(np.float32))
+            qkv.append(v.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+        wq = 1.0 + 0.1 * rng.standard_normal(d)
+        wk = 1.0 + 0.1 * rng.standard_normal(d)
+        planes = [[t.contiguous().numpy().view(np.uint16)
+                   for t in torch.unbind(torch.from_numpy(x.view(np.int16)), dim=2)] for x in qkv]
+        q_in = [p[0] for p in planes]
+        k_in = [p[1] for p in planes]
+        v_in = [p[2] for p in planes]
+        qo, ko, vo = orc.qkv_fused(qkv, seq, heads, wq, wk, 1e-6, 1e4)
+        _same(qo, orc.qk_fused_A(q_in, seq, heads, wq, 1e-6, 1e4), "qkv: q plane")
+        _same(ko, orc.qk_fused_A(k_in, seq, heads, wk, 1e-6, 1e4), "qkv: k plane")
+        _same(vo, split_cat_mode0(v_in, heads), "qkv: v plane")
+
+
 def pin_bf16_rounding(orc, quick=False):
     """double -> bf16 on float32-representable values equals torch's float32 -> bf16 (one
     round-to-nearest-even); bf16 -> double equals torch's widening."""
@@ -396,6 +421,7 @@ PINS = [
     pin_unit_weight_rms,
     pin_fused_formulations_agree,
     pin_fused_placement_decode,
+    pin_qkv_interleaved,
     pin_bf16_rounding,
 ]
 

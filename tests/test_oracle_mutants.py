@@ -57,6 +57,11 @@ MUTANTS = {
     "fused_row_local_position": [
         ("transform_row(src, d, w, eps, (double)s, theta, y);",
          "transform_row(src, d, w, eps, (double)i, theta, y);")],
+    "qkv_planes_swapped": [("qrow = qkv_in[q] + (((bb * s_q + i) * 3 + 0)", "qrow = qkv_in[q] + (((bb * s_q + i) * 3 + 1)"),
+                           ("krow = qkv_in[q] + (((bb * s_q + i) * 3 + 1)", "krow = qkv_in[q] + (((bb * s_q + i) * 3 + 0)")],
+    "qkv_plane_stride": [("(((bb * s_q + i) * 3 + 2) * N + g) * d;", "((bb * s_q + i) * N + 2 * N + g) * d;")],
+    "qkv_k_uses_q_weight": [("transform_row(krow, d, wk, eps, p, theta, k_out[r] + dst_row);",
+                             "transform_row(krow, d, wq, eps, p, theta, k_out[r] + dst_row);")],
     "bf16_truncates": [("nearbyint(a / quantum)", "floor(a / quantum)")],
     "bf16_one_bit_too_many": [("ldexp(1.0, ex - 7)", "ldexp(1.0, ex - 8)")],
     "bf16_widening_drops_low_bits": [("uint32_t bits = (uint32_t)h << 16;",
