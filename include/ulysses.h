@@ -149,6 +149,21 @@ int ulysses_a2a_4d_qk_fused(ulysses_plan_t plan, const void* const* q_in, const 
                             float rope_theta, void* stream);
 
 /*
+ * The fused call on interleaved packed QKV, the layout a fused QKV projection writes (FastVideo,
+ * "Ulysses performance on GB200": packed QKV or QKVG): rank q's input is one (b, s_q, 3, N, d)
+ * bf16 tensor whose planes are q, k and v. In one launch per chunk, q and k are normalised,
+ * rotated and placed as ulysses_a2a_4d_qk_fused does, and v is placed by mode 0 unchanged
+ * (bit-exact).
+ *   qkv_in          W device pointers, rank q's (b, s_q, 3, N, d) bf16.
+ *   q_out, k_out, v_out   W device pointers each, rank r's (b, S, n_r, d) bf16.
+ *   rms_w, eps, rope_theta, plan requirements: as ulysses_a2a_4d_qk_fused. The chunk cap applies
+ *   per plane (one launch reads up to three times the cap from a rank).
+ */
+int ulysses_a2a_4d_qkv_fused(ulysses_plan_t plan, const void* const* qkv_in, void* const* q_out,
+                             void* const* k_out, void* const* v_out, const float* rms_w, float eps,
+                             float rope_theta, void* stream);
+
+/*
  * End-to-end form for host-resident data: copy each rank's input from host_in[k] to dev_in[k],
  * run the relayout, and copy each dev_out[k] back to host_out[k]. The work is cut into about
  * eight sequence chunks so that copies in and copies out overlap: chunk c is copied in and

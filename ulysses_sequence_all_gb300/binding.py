@@ -25,6 +25,7 @@ DTYPE_CODES = {"uint8": ULY_U8, "float8_e4m3fn": ULY_F8E4M3, "float8_e5m2": ULY_
 EXPORTS = ["ulysses_plan", "ulysses_plan_destroy", "ulysses_plan_set_chunk_bytes",
            "ulysses_plan_bytes", "ulysses_plan_num_chunks", "ulysses_plan_chunk_rows",
            "ulysses_a2a_4d", "ulysses_a2a_4d_engine", "ulysses_a2a_4d_qk_fused",
+           "ulysses_a2a_4d_qkv_fused",
            "ulysses_a2a_4d_host", "ulysses_a2a_4d_qk_fused_host", "ulysses_device_status",
            "ulysses_selftest_wait_timeout", "ulysses_last_cuda_error", "ulysses_strerror",
            "ulysses_version"]
@@ -65,6 +66,8 @@ def _lib():
         lib.ulysses_a2a_4d_engine.argtypes = [_p, ctypes.c_int, ctypes.c_int, _pp, _pp, _p]
         lib.ulysses_a2a_4d_qk_fused.argtypes = [_p, _pp, _pp, _pp, _pp, _p, ctypes.c_float,
                                                 ctypes.c_float, _p]
+        lib.ulysses_a2a_4d_qkv_fused.argtypes = [_p, _pp, _pp, _pp, _pp, _p, ctypes.c_float,
+                                                 ctypes.c_float, _p]
         lib.ulysses_a2a_4d_host.argtypes = [_p, ctypes.c_int, _pp, _pp, _pp, _pp, _p]
         lib.ulysses_a2a_4d_qk_fused_host.argtypes = [_p, _pp, _pp, _pp, _pp, _pp, _pp, _pp, _pp, _p,
                                                      ctypes.c_float, ctypes.c_float, _p]
@@ -177,6 +180,13 @@ def ulysses_a2a_4d_qk_fused(plan: Plan, q_in, k_in, q_out, k_out, rms_w, eps: fl
     _check(_lib().ulysses_a2a_4d_qk_fused(plan, _ptrs(q_in), _ptrs(k_in), _ptrs(q_out), _ptrs(k_out),
                                           _addr(rms_w), eps, rope_theta, _stream(stream)),
            "ulysses_a2a_4d_qk_fused")
+
+
+def ulysses_a2a_4d_qkv_fused(plan: Plan, qkv_in, q_out, k_out, v_out, rms_w, eps: float,
+                             rope_theta: float, stream=None):
+    _check(_lib().ulysses_a2a_4d_qkv_fused(plan, _ptrs(qkv_in), _ptrs(q_out), _ptrs(k_out),
+                                           _ptrs(v_out), _addr(rms_w), eps, rope_theta,
+                                           _stream(stream)), "ulysses_a2a_4d_qkv_fused")
 
 
 def ulysses_a2a_4d_host(plan: Plan, mode: int, host_in, host_out, dev_in, dev_out, stream=None):

@@ -20,8 +20,8 @@ cudaError_t relayout_status(unsigned* status, bool clear);
 int64_t relayout_tile_rows(int64_t row_bytes);
 cudaError_t relayout_rows_launch(const RowTileArgs& a, int mode, cudaStream_t stream, int device,
                                  int sm_count);
-void fused_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages, uint32_t* stage_bytes,
-                    int* ctas_per_sm);
+void fused_geometry(const Plan& p, int planes, int64_t* tokens_per_unit, int* stages,
+                    uint32_t* stage_bytes, int* ctas_per_sm);
 cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count);
 cudaError_t fused_status(unsigned* status, bool clear);
 cudaError_t selftest_timeout_launch(uint64_t limit_ns, cudaStream_t stream);
@@ -177,50 +177,78 @@ int relayout_impl(const Plan& p, int mode, int engine, const void* const* in_ptr
     return ULY_OK;
 }
 
-// Checks of a fused QK call (no CUDA call) and its argument block, without the unit tables.
+// Checks of a fused call (no CUDA call) and its argument block, without the unit tables. Either
+// q_in and k_in are given (separate tensors) or qkv_in and v_out (interleaved (b, s, 3, N, d)).
 int fused_prepare(const Plan& p, const void* const* q_in, const void* const* k_in,
-                  void* const* q_out, void* const* k_out, const float* rms_w, float eps,
-                  float rope_theta, FusedArgs* a, int64_t* tokens_per_unit)
+                  const void* const* qkv_in, void* const* q_out, void* const* k_out,
+                  void* const* v_out, const float* rms_w, float eps, float rope_theta, FusedArgs* a,
+                  int64_t* tokens_per_unit)
 {
+    const bool qkv = qkv_in != nullptr;
     if (p.dtype != ULY_BF16) return ULY_EINVAL;
     if (!(p.d == 8 || p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128 || p.d == 256))
         return ULY_EINVAL;
     if (p.S >= (int64_t(1) << 24)) return ULY_EINVAL;  // positions must be exact in fp32
     if (!(eps >= 0.0f) || !(rope_theta > 0.0f)) return ULY_EINVAL;
-    if (!rms_w) return ULY_EINVAL;
+    if (!rms_w || (qkv && !v_out)) return ULY_EINVAL;
     if (!aligned16(rms_w)) return ULY_EALIGN;
-    int64_t in_b[kMaxW], out_b[kMaxW];
+    int64_t in_b[kMaxW], out_b[kMaxW], qkv_b[kMaxW];
     side_bytes(p, 0, in_b, out_b);
+    for (int k = 0; k < p.W; ++k) qkv_b[k] = 3 * in_b[k];
     int rc;
-    if ((rc = check_ptrs(q_in, in_b, p.W)) || (rc = check_ptrs(k_in, in_b, p.W)) ||
-        (rc = check_ptrs(const_cast<const void* const*>(q_out), out_b, p.W)) ||
+    if (qkv) {
+        if ((rc = check_ptrs(qkv_in, qkv_b, p.W)) ||
+            (rc = check_ptrs(const_cast<const void* const*>(v_out), out_b, p.W)))
+            return rc;
+    } else if ((rc = check_ptrs(q_in, in_b, p.W)) || (rc = check_ptrs(k_in, in_b, p.W))) {
+        return rc;
+    }
+    if ((rc = check_ptrs(const_cast<const void* const*>(q_out), out_b, p.W)) ||
         (rc = check_ptrs(const_cast<const void* const*>(k_out), out_b, p.W)))
         return rc;
-    // all four tensor sets at once: 2W inputs (plus the weights) against 2W outputs
+    // every input (plus the weights) against every output
     const void* ins[2 * kMaxW + 1];
     int64_t ins_b[2 * kMaxW + 1];
-    const void* outs[2 * kMaxW];
-    int64_t outs_b[2 * kMaxW];
+    const void* outs[3 * kMaxW];
+    int64_t outs_b[3 * kMaxW];
+    int n_in = 0, n_out = 0;
     for (int k = 0; k < p.W; ++k) {
-        ins[k] = q_in[k];
-        ins[p.W + k] = k_in[k];
-        ins_b[k] = ins_b[p.W + k] = in_b[k];
-        outs[k] = q_out[k];
-        outs[p.W + k] = k_out[k];
-        outs_b[k] = outs_b[p.W + k] = out_b[k];
+        if (qkv) {
+            ins[n_in] = qkv_in[k];
+            ins_b[n_in++] = qkv_b[k];
+        } else {
+            ins[n_in] = q_in[k];
+            ins_b[n_in++] = in_b[k];
+            ins[n_in] = k_in[k];
+            ins_b[n_in++] = in_b[k];
+        }
+        outs[n_out] = q_out[k];
+        outs_b[n_out++] = out_b[k];
+        outs[n_out] = k_out[k];
+        outs_b[n_out++] = out_b[k];
+        if (qkv) {
+            outs[n_out] = v_out[k];
+            outs_b[n_out++] = out_b[k];
+        }
     }
-    ins[2 * p.W] = rms_w;
-    ins_b[2 * p.W] = 2 * p.d * int64_t(sizeof(float));
-    if ((rc = check_overlap(ins, ins_b, 2 * p.W + 1, outs, outs_b, 2 * p.W))) return rc;
+    ins[n_in] = rms_w;
+    ins_b[n_in++] = 2 * p.d * int64_t(sizeof(float));
+    if ((rc = check_overlap(ins, ins_b, n_in, outs, outs_b, n_out))) return rc;
     int stages = 0, ctas_per_sm = 1;
     uint32_t stage_bytes = 0;
-    fused_geometry(p, tokens_per_unit, &stages, &stage_bytes, &ctas_per_sm);
-    if (stages == 0) return ULY_EINVAL;  // one token's q and k rows do not fit the stages
+    fused_geometry(p, qkv ? 3 : 2, tokens_per_unit, &stages, &stage_bytes, &ctas_per_sm);
+    if (stages == 0) return ULY_EINVAL;  // one token's rows do not fit the stages
     std::memset(a, 0, sizeof *a);
     a->ctas_per_sm = ctas_per_sm;
+    a->interleaved = qkv ? 1 : 0;
     for (int k = 0; k < p.W; ++k) {
-        a->q_in[k] = static_cast<const uint8_t*>(q_in[k]);
-        a->k_in[k] = static_cast<const uint8_t*>(k_in[k]);
+        if (qkv) {
+            a->qkv_in[k] = static_cast<const uint8_t*>(qkv_in[k]);
+            a->v_out[k] = static_cast<uint8_t*>(v_out[k]);
+        } else {
+            a->q_in[k] = static_cast<const uint8_t*>(q_in[k]);
+            a->k_in[k] = static_cast<const uint8_t*>(k_in[k]);
+        }
         a->q_out[k] = static_cast<uint8_t*>(q_out[k]);
         a->k_out[k] = static_cast<uint8_t*>(k_out[k]);
     }
@@ -239,6 +267,28 @@ int fused_rows(const Plan& p, FusedArgs* a, int64_t tokens_per_unit, const Chunk
     build_fused_units(p, rows, tokens_per_unit, a);
     cudaError_t e = fused_launch(*a, stream, dev.device, dev.sm_count);
     return e == cudaSuccess ? ULY_OK : cuda_fail(e);
+}
+
+// The device forms of both fused calls: checks, then one launch per chunk of the plan.
+int fused_device(const Plan& p, const void* const* q_in, const void* const* k_in,
+                 const void* const* qkv_in, void* const* q_out, void* const* k_out,
+                 void* const* v_out, const float* rms_w, float eps, float rope_theta,
+                 cudaStream_t stream)
+{
+    FusedArgs a;
+    int64_t T = 0;
+    int rc = fused_prepare(p, q_in, k_in, qkv_in, q_out, k_out, v_out, rms_w, eps, rope_theta, &a, &T);
+    if (rc) return rc;
+    int64_t C = 0;
+    if ((rc = num_chunks(p, &C))) return rc;
+    DeviceInfo dev;
+    if ((rc = current_device(&dev))) return rc;
+    for (int64_t c = 0; c < C; ++c) {
+        ChunkRows rows;
+        chunk_rows(p, C, c, &rows);
+        if ((rc = fused_rows(p, &a, T, rows, stream, dev))) return rc;
+    }
+    return ULY_OK;
 }
 
 // ---- host-buffer entry points: chunked copy-in / kernel / copy-out pipeline ---------------------
@@ -420,21 +470,17 @@ int ulysses_a2a_4d_qk_fused(ulysses_plan_t plan, const void* const* q_in, const 
                             float rope_theta, void* stream)
 {
     if (!plan) return ULY_EINVAL;
-    const Plan& p = plan->p;
-    FusedArgs a;
-    int64_t T = 0;
-    int rc = fused_prepare(p, q_in, k_in, q_out, k_out, rms_w, eps, rope_theta, &a, &T);
-    if (rc) return rc;
-    int64_t C = 0;
-    if ((rc = num_chunks(p, &C))) return rc;
-    DeviceInfo dev;
-    if ((rc = current_device(&dev))) return rc;
-    for (int64_t c = 0; c < C; ++c) {
-        ChunkRows rows;
-        chunk_rows(p, C, c, &rows);
-        if ((rc = fused_rows(p, &a, T, rows, static_cast<cudaStream_t>(stream), dev))) return rc;
-    }
-    return ULY_OK;
+    return fused_device(plan->p, q_in, k_in, nullptr, q_out, k_out, nullptr, rms_w, eps, rope_theta,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int ulysses_a2a_4d_qkv_fused(ulysses_plan_t plan, const void* const* qkv_in, void* const* q_out,
+                             void* const* k_out, void* const* v_out, const float* rms_w, float eps,
+                             float rope_theta, void* stream)
+{
+    if (!plan || !qkv_in) return ULY_EINVAL;
+    return fused_device(plan->p, nullptr, nullptr, qkv_in, q_out, k_out, v_out, rms_w, eps,
+                        rope_theta, static_cast<cudaStream_t>(stream));
 }
 
 int ulysses_a2a_4d_host(ulysses_plan_t plan, int mode, const void* const* host_in,
@@ -507,7 +553,7 @@ int ulysses_a2a_4d_qk_fused_host(ulysses_plan_t plan, const void* const* q_host_
     FusedArgs a;
     int64_t T = 0;
     int rc = fused_prepare(p, const_cast<const void* const*>(q_in), const_cast<const void* const*>(k_in),
-                           q_out, k_out, rms_w, eps, rope_theta, &a, &T);
+                           nullptr, q_out, k_out, nullptr, rms_w, eps, rope_theta, &a, &T);
     if (rc) return rc;
     PipeChunks pc;
     if ((rc = pipe_chunks(p, &pc))) return rc;

@@ -185,10 +185,16 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     __syncthreads();
     if (n == 0) return;
     const int row_bytes = N * D * 2;  // one token, all heads, one tensor
+    const bool qkv = a.interleaved != 0;
+    const int planes = qkv ? 3 : 2;
+    // Stage layout: separate q and k inputs are loaded as two spans (all q rows, then all k
+    // rows); an interleaved (b, s, 3, N, d) input is one span with the planes inside each token.
+    // Row (token t, plane c, head h) sits at t * tok_stride + c * plane_stride(ntok) + h * 2d.
+    const int tok_stride = qkv ? 3 * row_bytes : row_bytes;
+    auto plane_stride = [&](int ntok) { return qkv ? row_bytes : ntok * row_bytes; };
 
     if (warp == kLoaderWarp) {  // one lane streams units into the stages
         if (lane != 0) return;
-        const uint64_t policy = policy_evict_first();
         int64_t j = 0;
         for (; j < n; ++j) {
             const int s = int(j % K);
@@ -197,18 +203,16 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
                 break;
             }
             const FusedUnit t = fused_decode(a, first + j * step);
-            const uint32_t bytes = uint32_t(t.ntok) * uint32_t(row_bytes);
-            const int64_t off = (t.bb * a.s[t.q] + t.i0) * row_bytes;
+            const uint32_t bytes = uint32_t(t.ntok) * uint32_t(row_bytes);  // one plane
+            const int64_t tok0 = t.bb * a.s[t.q] + t.i0;                      // first source row
             uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
-            mbar_arrive_expect_tx(&full[s], 2 * bytes);
-#if ULY_FUSED_EVICT_FIRST
-            bulk_g2s_hint(dst, a.q_in[t.q] + off, bytes, &full[s], policy);
-            bulk_g2s_hint(dst + bytes, a.k_in[t.q] + off, bytes, &full[s], policy);
-#else
-            (void)policy;
-            bulk_g2s(dst, a.q_in[t.q] + off, bytes, &full[s]);
-            bulk_g2s(dst + bytes, a.k_in[t.q] + off, bytes, &full[s]);
-#endif
+            mbar_arrive_expect_tx(&full[s], uint32_t(planes) * bytes);
+            if (qkv) {
+                bulk_g2s(dst, a.qkv_in[t.q] + tok0 * 3 * row_bytes, 3 * bytes, &full[s]);
+            } else {
+                bulk_g2s(dst, a.q_in[t.q] + tok0 * row_bytes, bytes, &full[s]);
+                bulk_g2s(dst + bytes, a.k_in[t.q] + tok0 * row_bytes, bytes, &full[s]);
+            }
         }
         // do not leave while copies into this CTA's shared memory may be in flight
         for (int64_t jj = (j > K ? j - K : 0); jj < j; ++jj) {
@@ -247,9 +251,10 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     }
 
     if (warp == kStorerWarp) {
-        // The results sit where their inputs were: for each token, q|k and destination rank one
-        // run of n_r heads, contiguous in the stage and in the destination tensor. A stage is
-        // handed back to the loader kFusedDrain units later, once its stores have read it.
+        // The results sit where their inputs were (v untouched): for each token, plane and
+        // destination rank one run of n_r heads, contiguous in the stage and in the destination
+        // tensor. A stage is handed back to the loader kFusedDrain units later, once its stores
+        // have read it.
         int64_t j = 0;
         for (; j < n; ++j) {
             const int s = int(j % K);
@@ -261,15 +266,16 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
             const uint8_t* st = smem + L.stages + size_t(s) * a.stage_bytes;
             const int64_t row0 = t.bb * a.S + a.seq_off[t.q] + t.i0;
             const int W = a.W;
-            const int runs = t.ntok * 2 * W;
+            const int pstride = plane_stride(t.ntok);
+            const int runs = t.ntok * planes * W;
             for (int idx = lane; idx < runs; idx += 32) {
                 const int rest = idx / W, r = idx - rest * W;
-                const int which = rest & 1, tok = rest >> 1;
+                const int tok = rest / planes, plane = rest - tok * planes;
                 const int64_t run = a.n[r] * (D * 2);
                 if (run == 0) continue;
-                const uint8_t* src = st + (which * t.ntok + tok) * row_bytes + a.head_off[r] * (D * 2);
-                uint8_t* dst = (which ? a.k_out[r] : a.q_out[r]) + (row0 + tok) * run;
-                bulk_s2g(dst, src, uint32_t(run));
+                const uint8_t* src = st + tok * tok_stride + plane * pstride + a.head_off[r] * (D * 2);
+                uint8_t* out = plane == 0 ? a.q_out[r] : plane == 1 ? a.k_out[r] : a.v_out[r];
+                bulk_s2g(out + (row0 + tok) * run, src, uint32_t(run));
             }
             bulk_commit();
             if (j >= kFusedDrain) {
@@ -307,8 +313,8 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
             if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
             break;
         }
-        // this tensor's rows in the stage: (token, head) row ri at byte ri * 2d
-        uint8_t* rows_base = smem + L.stages + size_t(s) * a.stage_bytes + which * t.ntok * row_bytes;
+        // this tensor's plane in the stage; row (token, head) at token * tok_stride + head * 2d
+        uint8_t* rows_base = smem + L.stages + size_t(s) * a.stage_bytes + which * plane_stride(t.ntok);
         const float4* table = reinterpret_cast<const float4*>(smem + L.tables + s * L.table_bytes);
         const int rows = t.ntok * N;
         const int steps = (rows + PER_STEP - 1) / PER_STEP;
@@ -327,12 +333,12 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
             for (int u = 0; u < kIlp; ++u) {
                 const int o = u * GPW + group;
                 ok[u] = base + o < rows;
-                slot[u] = rows_base + (base + o) * (D * 2) + sub * 16;
                 int hh = base_head + o, tk = base_tok;
                 while (hh >= N) {
                     hh -= N;
                     ++tk;
                 }
+                slot[u] = rows_base + tk * tok_stride + hh * (D * 2) + sub * 16;
                 tok[u] = tk;
                 uint4 x = make_uint4(0, 0, 0, 0);
                 if (ok[u]) x = ld_shared_v4(slot[u]);
@@ -392,14 +398,14 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
 // token's q and k rows do not fit even one CTA per SM). The preferred footprint lets
 // kFusedCtasPerSm CTAs share an SM; narrower units, fewer stages, then fewer CTAs per SM are
 // tried in that order.
-void fused_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages, uint32_t* stage_bytes,
-                    int* ctas_per_sm)
+void fused_geometry(const Plan& p, int planes, int64_t* tokens_per_unit, int* stages,
+                    uint32_t* stage_bytes, int* ctas_per_sm)
 {
     *stages = 0;
     *tokens_per_unit = 1;
     *stage_bytes = 0;
     *ctas_per_sm = 1;
-    const int64_t pair_bytes = 2 * p.N * p.d * 2;  // one token of q and of k
+    const int64_t pair_bytes = planes * p.N * p.d * 2;  // one token of q and k (and v)
     int64_t T0 = ULY_FUSED_STAGE_TARGET / pair_bytes;
     if (T0 < 1) T0 = 1;
     const int min_k = kFusedDrain + 1 > 2 ? kFusedDrain + 1 : 2;

@@ -80,11 +80,16 @@ void build_row_tiles(const Plan& p, const ChunkRows& rows, int64_t tile_rows, Ro
 // ---- fused QK kernel's argument block ---------------------------------------------------------
 // A work unit is `tokens_per_unit` consecutive source rows (tokens) of one shard q and one batch
 // index; it covers all N heads of both q and k for those tokens.
+// With `interleaved` set the input is qkv_in[q], one (b, s_q, 3, N, d) tensor per rank (planes q,
+// k, v), a unit covers the token block's three planes, and v_out receives v unchanged.
 struct FusedArgs {
     const uint8_t* q_in[kMaxW];
     const uint8_t* k_in[kMaxW];
+    const uint8_t* qkv_in[kMaxW];
     uint8_t* q_out[kMaxW];
     uint8_t* k_out[kMaxW];
+    uint8_t* v_out[kMaxW];
+    int32_t interleaved;
     const float* rms_w;  // [2][d]
     int64_t s[kMaxW], seq_off[kMaxW], n[kMaxW], head_off[kMaxW];
     int64_t row_lo[kMaxW], rows[kMaxW];
