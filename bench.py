@@ -366,6 +366,19 @@ def run_ours(args):
         kt["mode0"].append(ev[1].elapsed_time(ev[2]))
         kt["mode1"].append(ev[2].elapsed_time(ev[3]))
 
+    # outside the step: the interleaved (b, s, 3, N, d) QKV form of its first two launches
+    qkv = [torch.stack([a, b, c], dim=2) for a, b, c in zip(wk.q, wk.k, wk.v)]
+    qkv_ms = []
+    for rep in range(min(args.steps, 20) + 3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        B.ulysses_a2a_4d_qkv_fused(wk.plan, qkv, wk.qo, wk.ko, wk.vo, wk.w, EPS, THETA, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if rep >= 3:
+            qkv_ms.append(e0.elapsed_time(e1))
+    del qkv
+
     clocks = ClockSampler(local)
     clocks.start()
     if pg:
@@ -423,6 +436,12 @@ def run_ours(args):
                         "frac_of_peak": round(gbs[k] / peak, 4),
                         "frac_of_d2d": round(gbs[k] / d2d, 4) if d2d else None} for k in med},
         "d2d_copy_GBps": round(d2d, 1) if d2d else None,
+        "qkv_fused": {
+            "note": "outside the step: q, k, v interleaved (b, s, 3, N, d), one launch in place of "
+                    "the step's fused_qk + mode0 launches",
+            "median_ms": round(statistics.median(qkv_ms), 4),
+            "GB/s": round(6 * wk.side / (statistics.median(qkv_ms) * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(6 * wk.side / (statistics.median(qkv_ms) * 1e-3) / 1e9 / peak, 4)},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
