@@ -76,6 +76,12 @@ class Oracle:
         lib.orc_qkv_fused.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, _p, _p, _p,
                                       ctypes.c_double, ctypes.c_double, _p, _p, _p]
         lib.orc_qkv_fused.restype = ctypes.c_int
+        lib.orc_fused_row_bwd.argtypes = [_p, _p, _i64, _p, ctypes.c_double, ctypes.c_double,
+                                          ctypes.c_double, _p, _p]
+        lib.orc_fused_row_bwd.restype = None
+        lib.orc_qk_fused_bwd.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, _p, _p, _p,
+                                         ctypes.c_double, ctypes.c_double, _p, _p]
+        lib.orc_qk_fused_bwd.restype = ctypes.c_int
         lib.orc_rmsnorm.argtypes = [_p, _i64, _p, ctypes.c_double, _p]
         lib.orc_rmsnorm.restype = None
         lib.orc_rope.argtypes = [_p, _i64, ctypes.c_double, ctypes.c_double]
@@ -183,6 +189,37 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle rejected the geometry")
         return qo, ko, vo
+
+    def fused_row_bwd(self, x, g, w, eps, p, theta):
+        """(dL/dx, dL/dw) of one row y = R(p)(x * w / rms(x)) for dL/dy = g, in double."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        g = np.ascontiguousarray(g, dtype=np.float64)
+        w = np.ascontiguousarray(w, dtype=np.float64)
+        dx = np.empty_like(x)
+        dw = np.zeros_like(x)
+        self.lib.orc_fused_row_bwd(x.ctypes.data, g.ctypes.data, x.size, w.ctypes.data,
+                                   float(eps), float(p), float(theta), dx.ctypes.data, dw.ctypes.data)
+        return dx, dw
+
+    def qk_fused_bwd(self, x_bf16, g_bf16, seq_splits, head_splits, w, eps, theta):
+        """Backward of the fused mode-0 call for one tensor: forward inputs x (rank q's
+        (b, s_q, N, d) bf16) and output gradients g (rank r's (b, S, n_r, d) bf16). Returns
+        (dx per rank in double, (b, s_q, N, d); dw, d values)."""
+        W = len(x_bf16)
+        b, d = x_bf16[0].shape[0], x_bf16[0].shape[3]
+        xs = [np.ascontiguousarray(x).view(np.uint16) for x in x_bf16]
+        gs = [np.ascontiguousarray(x).view(np.uint16) for x in g_bf16]
+        w64 = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
+        dx = [np.empty(x.shape, dtype=np.float64) for x in xs]
+        dw = np.full(d, np.nan)  # the oracle clears it
+        rc = self.lib.orc_qk_fused_bwd(W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
+                                       ctypes.cast(_ptr_array(xs), _p),
+                                       ctypes.cast(_ptr_array(gs), _p), w64.ctypes.data,
+                                       float(eps), float(theta), ctypes.cast(_ptr_array(dx), _p),
+                                       dw.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle rejected the geometry")
+        return dx, dw
 
     def rmsnorm(self, x, w, eps):
         x = np.ascontiguousarray(x, dtype=np.float64)

@@ -375,3 +375,74 @@ int orc_qkv_fused(int W, int64_t b, const int64_t* seq_splits, const int64_t* he
     }
     return 0;
 }
+
+/*
+ * Backward of the fused transform for one row (vector-Jacobian product). The forward row is
+ * y = R(p) (x * w / rms(x)) with rms(x) = sqrt(mean(x^2) + eps) and R(p) the rotation above.
+ * Given g = dL/dy: u = R(-p) g (the rotation is orthogonal), a = u * w,
+ * dL/dx = (a - xh * mean(a * xh)) / rms(x) with xh = x / rms(x), and dL/dw += u * xh.
+ */
+void orc_fused_row_bwd(const double* x, const double* g, int64_t d, const double* w, double eps,
+                       double p, double theta, double* dx, double* dw_acc)
+{
+    double* u = (double*)malloc((size_t)d * sizeof(double));
+    for (int64_t j = 0; j < d; ++j) u[j] = g[j];
+    orc_rope(u, d, -p, theta);
+    double sum_sq = 0.0;
+    for (int64_t j = 0; j < d; ++j) sum_sq += x[j] * x[j];
+    const double inv_rms = 1.0 / sqrt(sum_sq / (double)d + eps);
+    double dot = 0.0;
+    for (int64_t j = 0; j < d; ++j) {
+        const double xh = x[j] * inv_rms;
+        dot += u[j] * w[j] * xh;
+        dw_acc[j] += u[j] * xh;
+    }
+    for (int64_t j = 0; j < d; ++j) {
+        const double xh = x[j] * inv_rms;
+        dx[j] = inv_rms * (u[j] * w[j] - xh * dot / (double)d);
+    }
+    free(u);
+}
+
+/*
+ * Backward of the fused mode-0 call for one tensor: x_in[q] is rank q's forward input
+ * (b, s_q, N, d) bf16, g_out[r] rank r's gradient with respect to the forward output
+ * (b, S, n_r, d) bf16. dx[q] receives rank q's gradient with respect to its input (double,
+ * (b, s_q, N, d)); dw (d values) is set to the gradient with respect to the weight.
+ */
+int orc_qk_fused_bwd(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                     int64_t d, const uint16_t* const* x_in, const uint16_t* const* g_out,
+                     const double* w, double eps, double theta, double* const* dx, double* dw)
+{
+    if (check_geometry(W, b, seq_splits, head_splits, d) || (d % 2) != 0) return -1;
+    const int64_t S = offset_of(seq_splits, W);
+    const int64_t N = offset_of(head_splits, W);
+    double* x = (double*)malloc((size_t)d * sizeof(double));
+    double* g = (double*)malloc((size_t)d * sizeof(double));
+    for (int64_t j = 0; j < d; ++j) dw[j] = 0.0;
+    for (int q = 0; q < W; ++q) {
+        const int64_t s_q = seq_splits[q];
+        const int64_t seq_off_q = offset_of(seq_splits, q);
+        for (int64_t bb = 0; bb < b; ++bb)
+            for (int64_t i = 0; i < s_q; ++i)
+                for (int64_t hg = 0; hg < N; ++hg) {
+                    int r = 0;
+                    while (!(hg >= offset_of(head_splits, r) &&
+                             hg < offset_of(head_splits, r) + head_splits[r]))
+                        ++r;
+                    const int64_t n_r = head_splits[r];
+                    const int64_t h = hg - offset_of(head_splits, r);
+                    const int64_t src_row = ((bb * s_q + i) * N + hg) * d;
+                    const int64_t out_row = ((bb * S + seq_off_q + i) * n_r + h) * d;
+                    for (int64_t j = 0; j < d; ++j) {
+                        x[j] = orc_bf16_to_double(x_in[q][src_row + j]);
+                        g[j] = orc_bf16_to_double(g_out[r][out_row + j]);
+                    }
+                    orc_fused_row_bwd(x, g, d, w, eps, (double)(seq_off_q + i), theta,
+                                      dx[q] + src_row, dw);
+                }
+    }
+    free(x);
+    free(g);
+    return 0;
+}

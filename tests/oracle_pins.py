@@ -383,6 +383,89 @@ def pin_qkv_interleaved(orc, quick=False):
         _same(vo, split_cat_mode0(v_in, heads), "qkv: v plane")
 
 
+def _torch_row_forward(x, w, eps, p, theta):
+    """The fused row transform built from library pieces (F.rms_norm, complex multiplication),
+    differentiable by torch.autograd."""
+    d = x.shape[-1]
+    y = F.rms_norm(x[None], (d,), weight=w, eps=eps)[0]
+    ang = torch.tensor([p * _freq(theta, j, d) for j in range(d // 2)], dtype=torch.float64)
+    z = torch.view_as_complex(y.reshape(d // 2, 2)) * torch.polar(torch.ones_like(ang), ang)
+    return torch.view_as_real(z).reshape(d)
+
+
+def pin_fused_bwd_vs_autograd(orc, quick=False):
+    """The row backward equals torch.autograd's gradients of the library-built forward."""
+    rng = np.random.default_rng(28)
+    for d in (2, 8, 128):
+        for p in (0, 3, 9450, 75599):
+            for eps in (1e-6, 0.3):
+                x = torch.tensor(rng.standard_normal(d), dtype=torch.float64, requires_grad=True)
+                w = torch.tensor(1.0 + 0.1 * rng.standard_normal(d), dtype=torch.float64,
+                                 requires_grad=True)
+                g = torch.tensor(rng.standard_normal(d), dtype=torch.float64)
+                _torch_row_forward(x, w, eps, p, 1e4).backward(g)
+                dx, dw = orc.fused_row_bwd(x.detach().numpy(), g.numpy(), w.detach().numpy(), eps,
+                                           p, 1e4)
+                np.testing.assert_allclose(dx, x.grad.numpy(), rtol=1e-9, atol=1e-11)
+                np.testing.assert_allclose(dw, w.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def pin_fused_bwd_finite_differences(orc, quick=False):
+    """Adjoint identity against the forward oracle: <g, (f(x + h v) - f(x - h v)) / 2h>
+    equals <dL/dx, v> (and the same for w)."""
+    rng = np.random.default_rng(29)
+    d, eps, theta, h = 16, 1e-3, 1e4, 1e-5
+    for p in (0, 5, 1234):
+        x, w, g, v = (rng.standard_normal(d) for _ in range(4))
+        w = 1.0 + 0.1 * w
+        f = lambda xx, ww: orc.rope(orc.rmsnorm(xx, ww, eps), p, theta)  # noqa: E731
+        dx, dw = orc.fused_row_bwd(x, g, w, eps, p, theta)
+        num_x = np.dot(g, (f(x + h * v, w) - f(x - h * v, w)) / (2 * h))
+        num_w = np.dot(g, (f(x, w + h * v) - f(x, w - h * v)) / (2 * h))
+        assert abs(num_x - np.dot(dx, v)) < 1e-6 * (1 + abs(num_x))
+        assert abs(num_w - np.dot(dw, v)) < 1e-6 * (1 + abs(num_w))
+
+
+def pin_fused_bwd_placement(orc, quick=False):
+    """The whole-call backward equals: mode 1 (pinned above) brings the output gradients back to
+    the sequence side, then the row backward at each row's global position; dw is the sum."""
+    rng = np.random.default_rng(30)
+    for W, b, seq, heads, d in [(2, 1, [3, 2], [2, 1], 8), (3, 2, [2, 0, 3], [1, 2, 1], 16)]:
+        N, S = sum(heads), sum(seq)
+        bf = lambda shape: torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(  # noqa: E731
+            torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        xs = [bf((b, s, N, d)) for s in seq]
+        gs = [bf((b, S, n, d)) for n in heads]
+        w = 1.0 + 0.1 * rng.standard_normal(d)
+        dx, dw = orc.qk_fused_bwd(xs, gs, seq, heads, w, 1e-6, 1e4)
+        g_seq = orc.a2a_4d(gs, seq, heads, 1)
+        dw_want = np.zeros(d)
+        seq_off = np.cumsum([0] + list(seq))
+        for q in range(W):
+            for bb in range(b):
+                for i in range(seq[q]):
+                    for hh in range(N):
+                        x = orc.bf16_to_double(xs[q][bb, i, hh])
+                        g = orc.bf16_to_double(g_seq[q][bb, i, hh])
+                        want, dwr = orc.fused_row_bwd(x, g, w, 1e-6, seq_off[q] + i, 1e4)
+                        dw_want += dwr
+                        np.testing.assert_allclose(dx[q][bb, i, hh], want, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(dw, dw_want, rtol=1e-12, atol=1e-12)
+
+
+def pin_relayout_adjoint(orc, quick=False):
+    """Mode 1 is the adjoint of mode 0 (the backward pairing): <mode0(x), y> = <x, mode1(y)>."""
+    rng = np.random.default_rng(31)
+    for W, b, seq, heads, d, _ in _random_geometries(rng, 20):
+        N, S = sum(heads), sum(seq)
+        xs = [rng.standard_normal((b, s, N, d)).astype(np.float32) for s in seq]
+        ys = [rng.standard_normal((b, S, n, d)).astype(np.float32) for n in heads]
+        dot = lambda a, c: float(np.sum(a.astype(np.float64) * c))  # noqa: E731
+        lhs = sum(dot(a, c) for a, c in zip(orc.a2a_4d(xs, seq, heads, 0), ys))
+        rhs = sum(dot(a, c) for a, c in zip(xs, orc.a2a_4d(ys, seq, heads, 1)))
+        assert abs(lhs - rhs) < 1e-9 * (1 + abs(lhs))
+
+
 def pin_bf16_rounding(orc, quick=False):
     """double -> bf16 on float32-representable values equals torch's float32 -> bf16 (one
     round-to-nearest-even); bf16 -> double equals torch's widening."""
@@ -422,6 +505,10 @@ PINS = [
     pin_fused_formulations_agree,
     pin_fused_placement_decode,
     pin_qkv_interleaved,
+    pin_fused_bwd_vs_autograd,
+    pin_fused_bwd_finite_differences,
+    pin_fused_bwd_placement,
+    pin_relayout_adjoint,
     pin_bf16_rounding,
 ]
 

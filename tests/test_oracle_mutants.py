@@ -41,7 +41,7 @@ MUTANTS = {
     "source_query_drops_head_offset": [
         ("N + offset_of(head_splits, r) + h) * d + j;", "N + h) * d + j;")],
     "rmsnorm_drops_eps": [("sqrt(mean_sq + eps)", "sqrt(mean_sq)")],
-    "rmsnorm_sum_not_mean": [("sum_sq / (double)d", "sum_sq")],
+    "rmsnorm_sum_not_mean": [("mean_sq = sum_sq / (double)d", "mean_sq = sum_sq")],
     "rmsnorm_drops_weight": [("x[j] * inv_rms * w[j]", "x[j] * inv_rms")],
     "rmsnorm_eps_outside_sqrt": [("1.0 / sqrt(mean_sq + eps)", "1.0 / (sqrt(mean_sq) + eps)")],
     "rope_sin_sign": [("y[2 * j] = a * c - bq * s;", "y[2 * j] = a * c + bq * s;"),
@@ -62,6 +62,16 @@ MUTANTS = {
     "qkv_plane_stride": [("(((bb * s_q + i) * 3 + 2) * N + g) * d;", "((bb * s_q + i) * N + 2 * N + g) * d;")],
     "qkv_k_uses_q_weight": [("transform_row(krow, d, wk, eps, p, theta, k_out[r] + dst_row);",
                              "transform_row(krow, d, wq, eps, p, theta, k_out[r] + dst_row);")],
+    "bwd_rope_forward_direction": [("orc_rope(u, d, -p, theta);", "orc_rope(u, d, p, theta);")],
+    "bwd_drops_norm_projection": [("dx[j] = inv_rms * (u[j] * w[j] - xh * dot / (double)d);",
+                                   "dx[j] = inv_rms * u[j] * w[j];")],
+    "bwd_eps_dropped": [("sqrt(sum_sq / (double)d + eps)", "sqrt(sum_sq / (double)d)")],
+    "bwd_dot_misses_weight": [("dot += u[j] * w[j] * xh;", "dot += u[j] * xh;")],
+    "bwd_dw_unnormalised": [("dw_acc[j] += u[j] * xh;", "dw_acc[j] += u[j] * x[j];")],
+    "bwd_position_rank_local": [("(double)(seq_off_q + i), theta,\n                                      dx[q]", "(double)i, theta,\n                                      dx[q]")],
+    "bwd_dw_not_cleared": [("for (int64_t j = 0; j < d; ++j) dw[j] = 0.0;", "")],
+    "bwd_gradient_from_wrong_token": [("g[j] = orc_bf16_to_double(g_out[r][out_row + j]);",
+                                       "g[j] = orc_bf16_to_double(g_out[r][out_row - (i > 0 ? n_r * d : 0) + j]);")],
     "bf16_truncates": [("nearbyint(a / quantum)", "floor(a / quantum)")],
     "bf16_one_bit_too_many": [("ldexp(1.0, ex - 7)", "ldexp(1.0, ex - 8)")],
     "bf16_widening_drops_low_bits": [("uint32_t bits = (uint32_t)h << 16;",
