@@ -149,6 +149,40 @@ int ulysses_a2a_4d_qk_fused(ulysses_plan_t plan, const void* const* q_in, const 
                             float rope_theta, void* stream);
 
 /*
+ * Backward of ulysses_a2a_4d_qk_fused on the same plan. The relayout is differentiable and its
+ * backward uses the plan saved by the forward (fast-ulysses 0.2.1, README, "Quick start" and
+ * "Limits"; FastVideo, "Ulysses performance on GB200"); the backward of mode 0 is mode 1 (the
+ * plain relayout's gradient is ulysses_a2a_4d with mode 1). Here the vector-Jacobian product of
+ * the RMSNorm + RoPE transform is applied inside that mode-1 gather. For q and k separately, per
+ * head row x at global position p with output gradient gy (the row mode 0 made of x):
+ *     r = 1 / sqrt(mean(x^2) + eps),  u = gy rotated back by p * rope_theta^(-2j/d) per pair j,
+ *     dx = r * (u * w - x * r * <u * w, x * r> / d)      -> dq_out / dk_out, bf16, rounded once
+ *     dw = sum over all rows of all ranks of u * x * r   -> dw[0][:] (q), dw[1][:] (k), fp32
+ * computed in fp32 (the sums over rows in fp32, in an order that does not depend on timing).
+ *   dq_out, dk_out  W device pointers, rank q's (b, s_q, N, d) bf16 (the forward's inputs' shape).
+ *   q_in, k_in      W device pointers, the forward's inputs (rank q's (b, s_q, N, d) bf16).
+ *   dq_in, dk_in    W device pointers, gradients of the forward's outputs, rank r's (b, S, n_r, d).
+ *   rms_w           device pointer, 2 * d fp32 (as the forward); dw: device pointer, 2 * d fp32,
+ *                   overwritten.
+ *   eps, rope_theta, plan requirements: as ulysses_a2a_4d_qk_fused.
+ *   workspace       device memory of at least ulysses_qk_fused_backward_workspace bytes, 16-byte
+ *                   aligned, the caller's; partial sums of dw live there while the call runs, so
+ *                   two calls in flight at once need two workspaces. No initial contents needed.
+ * Queues two launches per chunk on `stream`. ULY_EINVAL for a short workspace; outputs (with dw
+ * and the workspace) may not overlap inputs or each other (ULY_EOVERLAP).
+ */
+int ulysses_a2a_4d_qk_fused_backward(ulysses_plan_t plan, void* const* dq_out, void* const* dk_out,
+                                     const void* const* q_in, const void* const* k_in,
+                                     const void* const* dq_in, const void* const* dk_in,
+                                     const float* rms_w, float* dw, float eps, float rope_theta,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes ulysses_a2a_4d_qk_fused_backward needs for `plan` on the current device (one
+ * 2 * d fp32 slot per CTA it launches: at most a few MB). ULY_EINVAL if the plan does not meet
+ * the fused call's requirements. */
+int ulysses_qk_fused_backward_workspace(ulysses_plan_t plan, size_t* bytes);
+
+/*
  * The fused call on interleaved packed QKV, the layout a fused QKV projection writes (FastVideo,
  * "Ulysses performance on GB200": packed QKV or QKVG): rank q's input is one (b, s_q, 3, N, d)
  * bf16 tensor whose planes are q, k and v. In one launch per chunk, q and k are normalised,

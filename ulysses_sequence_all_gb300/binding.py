@@ -25,7 +25,8 @@ DTYPE_CODES = {"uint8": ULY_U8, "float8_e4m3fn": ULY_F8E4M3, "float8_e5m2": ULY_
 EXPORTS = ["ulysses_plan", "ulysses_plan_destroy", "ulysses_plan_set_chunk_bytes",
            "ulysses_plan_bytes", "ulysses_plan_num_chunks", "ulysses_plan_chunk_rows",
            "ulysses_a2a_4d", "ulysses_a2a_4d_engine", "ulysses_a2a_4d_qk_fused",
-           "ulysses_a2a_4d_qkv_fused",
+           "ulysses_a2a_4d_qkv_fused", "ulysses_a2a_4d_qk_fused_backward",
+           "ulysses_qk_fused_backward_workspace",
            "ulysses_a2a_4d_host", "ulysses_a2a_4d_qk_fused_host", "ulysses_device_status",
            "ulysses_selftest_wait_timeout", "ulysses_last_cuda_error", "ulysses_strerror",
            "ulysses_version"]
@@ -68,6 +69,10 @@ def _lib():
                                                 ctypes.c_float, _p]
         lib.ulysses_a2a_4d_qkv_fused.argtypes = [_p, _pp, _pp, _pp, _pp, _p, ctypes.c_float,
                                                  ctypes.c_float, _p]
+        lib.ulysses_a2a_4d_qk_fused_backward.argtypes = [_p, _pp, _pp, _pp, _pp, _pp, _pp, _p, _p,
+                                                         ctypes.c_float, ctypes.c_float, _p,
+                                                         ctypes.c_size_t, _p]
+        lib.ulysses_qk_fused_backward_workspace.argtypes = [_p, ctypes.POINTER(ctypes.c_size_t)]
         lib.ulysses_a2a_4d_host.argtypes = [_p, ctypes.c_int, _pp, _pp, _pp, _pp, _p]
         lib.ulysses_a2a_4d_qk_fused_host.argtypes = [_p, _pp, _pp, _pp, _pp, _pp, _pp, _pp, _pp, _p,
                                                      ctypes.c_float, ctypes.c_float, _p]
@@ -100,6 +105,13 @@ def _addr(x) -> int:
     if isinstance(x, int):
         return x
     return x.data_ptr()  # torch.Tensor
+
+
+def _nbytes(x) -> int:
+    """Size in bytes of a torch tensor (0 for None)."""
+    if x is None:
+        return 0
+    return x.numel() * x.element_size()
 
 
 def _ptrs(xs: Sequence) -> ctypes.Array:
@@ -187,6 +199,24 @@ def ulysses_a2a_4d_qkv_fused(plan: Plan, qkv_in, q_out, k_out, v_out, rms_w, eps
     _check(_lib().ulysses_a2a_4d_qkv_fused(plan, _ptrs(qkv_in), _ptrs(q_out), _ptrs(k_out),
                                            _ptrs(v_out), _addr(rms_w), eps, rope_theta,
                                            _stream(stream)), "ulysses_a2a_4d_qkv_fused")
+
+
+def ulysses_qk_fused_backward_workspace(plan: Plan) -> int:
+    """Workspace bytes ulysses_a2a_4d_qk_fused_backward needs for `plan` on the current device."""
+    n = ctypes.c_size_t()
+    _check(_lib().ulysses_qk_fused_backward_workspace(plan, ctypes.byref(n)),
+           "ulysses_qk_fused_backward_workspace")
+    return n.value
+
+
+def ulysses_a2a_4d_qk_fused_backward(plan: Plan, dq_out, dk_out, q_in, k_in, dq_in, dk_in, rms_w,
+                                     dw, eps: float, rope_theta: float, workspace, stream=None):
+    """Backward of the fused call. `workspace` is a device tensor of at least
+    ulysses_qk_fused_backward_workspace(plan) bytes."""
+    _check(_lib().ulysses_a2a_4d_qk_fused_backward(
+        plan, _ptrs(dq_out), _ptrs(dk_out), _ptrs(q_in), _ptrs(k_in), _ptrs(dq_in), _ptrs(dk_in),
+        _addr(rms_w), _addr(dw), eps, rope_theta, _addr(workspace), _nbytes(workspace),
+        _stream(stream)), "ulysses_a2a_4d_qk_fused_backward")
 
 
 def ulysses_a2a_4d_host(plan: Plan, mode: int, host_in, host_out, dev_in, dev_out, stream=None):

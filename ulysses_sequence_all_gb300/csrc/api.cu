@@ -24,6 +24,12 @@ void fused_geometry(const Plan& p, int planes, int64_t* tokens_per_unit, int* st
                     uint32_t* stage_bytes, int* ctas_per_sm);
 cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count);
 cudaError_t fused_status(unsigned* status, bool clear);
+void fused_bwd_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages,
+                        uint32_t* stage_bytes, int* ctas_per_sm);
+int64_t fused_bwd_grid(const FusedBwdArgs& a, int sm_count);
+cudaError_t fused_bwd_launch(const FusedBwdArgs& a, float* dw, bool accumulate, cudaStream_t stream,
+                             int device, int sm_count);
+cudaError_t fused_bwd_status(unsigned* status, bool clear);
 cudaError_t selftest_timeout_launch(uint64_t limit_ns, cudaStream_t stream);
 }  // namespace uly
 
@@ -291,6 +297,101 @@ int fused_device(const Plan& p, const void* const* q_in, const void* const* k_in
     return ULY_OK;
 }
 
+// ---- backward of the fused QK call -------------------------------------------------------------
+// Plan requirements (as the forward), geometry, and the partial-sum bytes for the device the
+// caller is on: one 2 x d fp32 slot per CTA of the largest launch.
+int fused_bwd_setup(const Plan& p, const DeviceInfo& dev, int64_t* tokens_per_unit, int* stages,
+                    uint32_t* stage_bytes, int* ctas_per_sm, size_t* workspace_bytes)
+{
+    if (p.dtype != ULY_BF16) return ULY_EINVAL;
+    if (!(p.d == 8 || p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128 || p.d == 256))
+        return ULY_EINVAL;
+    if (p.S >= (int64_t(1) << 24)) return ULY_EINVAL;  // positions must be exact in fp32
+    fused_bwd_geometry(p, tokens_per_unit, stages, stage_bytes, ctas_per_sm);
+    if (*stages == 0) return ULY_EINVAL;  // one token's rows do not fit the stages
+    *workspace_bytes = size_t(dev.sm_count) * size_t(*ctas_per_sm) * size_t(2 * p.d) * sizeof(float);
+    return ULY_OK;
+}
+
+int fused_bwd_device(const Plan& p, void* const* dq_out, void* const* dk_out,
+                     const void* const* q_in, const void* const* k_in, const void* const* dq_in,
+                     const void* const* dk_in, const float* rms_w, float* dw, float eps,
+                     float rope_theta, void* workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    int64_t T = 0;
+    int stages = 0, ctas_per_sm = 1;
+    uint32_t stage_bytes = 0;
+    size_t need = 0;
+    if ((rc = fused_bwd_setup(p, dev, &T, &stages, &stage_bytes, &ctas_per_sm, &need))) return rc;
+    if (!(eps >= 0.0f) || !(rope_theta > 0.0f)) return ULY_EINVAL;
+    if (!rms_w || !dw || !workspace || workspace_bytes < need) return ULY_EINVAL;
+    if (!aligned16(rms_w) || !aligned16(dw) || !aligned16(workspace)) return ULY_EALIGN;
+    int64_t seq_b[kMaxW], head_b[kMaxW];
+    side_bytes(p, 0, seq_b, head_b);
+    if ((rc = check_ptrs(q_in, seq_b, p.W)) || (rc = check_ptrs(k_in, seq_b, p.W)) ||
+        (rc = check_ptrs(dq_in, head_b, p.W)) || (rc = check_ptrs(dk_in, head_b, p.W)) ||
+        (rc = check_ptrs(const_cast<const void* const*>(dq_out), seq_b, p.W)) ||
+        (rc = check_ptrs(const_cast<const void* const*>(dk_out), seq_b, p.W)))
+        return rc;
+    // every input (plus the weights) against every output (plus dw and the workspace)
+    const void* ins[4 * kMaxW + 1];
+    int64_t ins_b[4 * kMaxW + 1];
+    const void* outs[2 * kMaxW + 2];
+    int64_t outs_b[2 * kMaxW + 2];
+    int n_in = 0, n_out = 0;
+    for (int k = 0; k < p.W; ++k) {
+        ins[n_in] = q_in[k];
+        ins_b[n_in++] = seq_b[k];
+        ins[n_in] = k_in[k];
+        ins_b[n_in++] = seq_b[k];
+        ins[n_in] = dq_in[k];
+        ins_b[n_in++] = head_b[k];
+        ins[n_in] = dk_in[k];
+        ins_b[n_in++] = head_b[k];
+        outs[n_out] = dq_out[k];
+        outs_b[n_out++] = seq_b[k];
+        outs[n_out] = dk_out[k];
+        outs_b[n_out++] = seq_b[k];
+    }
+    ins[n_in] = rms_w;
+    ins_b[n_in++] = 2 * p.d * int64_t(sizeof(float));
+    outs[n_out] = dw;
+    outs_b[n_out++] = 2 * p.d * int64_t(sizeof(float));
+    outs[n_out] = workspace;
+    outs_b[n_out++] = int64_t(need);
+    if ((rc = check_overlap(ins, ins_b, n_in, outs, outs_b, n_out))) return rc;
+    int64_t C = 0;
+    if ((rc = num_chunks(p, &C))) return rc;
+    FusedBwdArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int k = 0; k < p.W; ++k) {
+        a.x_in[0][k] = static_cast<const uint8_t*>(q_in[k]);
+        a.x_in[1][k] = static_cast<const uint8_t*>(k_in[k]);
+        a.g_in[0][k] = static_cast<const uint8_t*>(dq_in[k]);
+        a.g_in[1][k] = static_cast<const uint8_t*>(dk_in[k]);
+        a.dx_out[0][k] = static_cast<uint8_t*>(dq_out[k]);
+        a.dx_out[1][k] = static_cast<uint8_t*>(dk_out[k]);
+    }
+    a.rms_w = rms_w;
+    a.dw_part = static_cast<float*>(workspace);
+    a.eps = eps;
+    a.stages = stages;
+    a.stage_bytes = stage_bytes;
+    a.ctas_per_sm = ctas_per_sm;
+    rope_turns(p.d, double(rope_theta), a.turn_hi, a.turn_lo);
+    for (int64_t c = 0; c < C; ++c) {
+        ChunkRows rows;
+        chunk_rows(p, C, c, &rows);
+        build_fused_bwd_units(p, rows, T, &a);
+        cudaError_t e = fused_bwd_launch(a, dw, c > 0, stream, dev.device, dev.sm_count);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return ULY_OK;
+}
+
 // ---- host-buffer entry points: chunked copy-in / kernel / copy-out pipeline ---------------------
 // Host<->device copies run on the copy engines in both directions at once, so the call is cut
 // into sequence chunks: chunk c's inputs are copied in and relaid out on the caller's stream, then
@@ -474,6 +575,29 @@ int ulysses_a2a_4d_qk_fused(ulysses_plan_t plan, const void* const* q_in, const 
                         static_cast<cudaStream_t>(stream));
 }
 
+int ulysses_qk_fused_backward_workspace(ulysses_plan_t plan, size_t* bytes)
+{
+    if (!plan || !bytes) return ULY_EINVAL;
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    int64_t T = 0;
+    int stages = 0, ctas_per_sm = 1;
+    uint32_t stage_bytes = 0;
+    return fused_bwd_setup(plan->p, dev, &T, &stages, &stage_bytes, &ctas_per_sm, bytes);
+}
+
+int ulysses_a2a_4d_qk_fused_backward(ulysses_plan_t plan, void* const* dq_out, void* const* dk_out,
+                                     const void* const* q_in, const void* const* k_in,
+                                     const void* const* dq_in, const void* const* dk_in,
+                                     const float* rms_w, float* dw, float eps, float rope_theta,
+                                     void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (!plan) return ULY_EINVAL;
+    return fused_bwd_device(plan->p, dq_out, dk_out, q_in, k_in, dq_in, dk_in, rms_w, dw, eps,
+                            rope_theta, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
 int ulysses_a2a_4d_qkv_fused(ulysses_plan_t plan, const void* const* qkv_in, void* const* q_out,
                              void* const* k_out, void* const* v_out, const float* rms_w, float eps,
                              float rope_theta, void* stream)
@@ -591,10 +715,11 @@ int ulysses_device_status(unsigned* status)
     if (!status) return ULY_EINVAL;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e);
-    unsigned a = 0, b = 0;
+    unsigned a = 0, b = 0, c = 0;
     if ((e = relayout_status(&a, true)) != cudaSuccess) return cuda_fail(e);
     if ((e = fused_status(&b, true)) != cudaSuccess) return cuda_fail(e);
-    *status = a | b;
+    if ((e = fused_bwd_status(&c, true)) != cudaSuccess) return cuda_fail(e);
+    *status = a | b | c;
     return *status ? ULY_EDEVICE : ULY_OK;
 }
 

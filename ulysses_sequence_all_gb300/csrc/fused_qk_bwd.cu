@@ -1,0 +1,548 @@
+// fused_qk_bwd.cu -- backward of the fused QK call: the gradients of q, k and of the two RMSNorm
+// weights from the gradients of the call's outputs, with the mode-1 gather fused in. The
+// relayout is differentiable and its backward uses the forward's plan (fast-ulysses 0.2.1,
+// README, "Quick start" and "Limits"; FastVideo, "Ulysses performance on GB200": backward uses
+// the plan saved by its forward), and the backward of mode 0 is mode 1 on that plan.
+//
+// Forward, per head row x of d values at global sequence position p (fast-ulysses 0.1.0, "Fusion
+// examples"): xh = x * r with r = 1 / sqrt(mean(x^2) + eps), y = R(p) (w * xh), where R(p)
+// rotates each pair (2j, 2j+1) by p * theta^(-2j/d). For gy = dL/dy, in fp32:
+//     u   = R(p)^T gy                          (the rotation by -p)
+//     dw += u * xh                             (summed over every row of the tensor)
+//     dx  = r * (u * w - xh * <u * w, xh> / d) = r * u * w - x * (r^3 <u * w, x> / d)
+// dx is rounded once to bf16 and written on the sequence side, where x came from; gy is read
+// on the head side, where mode 0 put y, so the rows arrive through the mode-1 gather.
+//
+// Structure: the forward kernel's pipeline (persistent grid, several CTAs per SM, a ring of
+// shared-memory stages; loader, table, storer and consumer warps). A unit is one tensor (q or k)
+// of a block of tokens of one shard: the loader brings the forward input span (one bulk copy)
+// and the W runs of the output gradient (one bulk copy per rank) into a stage; the consumers
+// overwrite the input rows with dx; the storer writes the span back with one bulk store. Each
+// consumer lane keeps dw partial sums for its 8 columns; they are summed over the lanes of a
+// warp at the end of each unit and added to the warp's row of a small shared array; at the end
+// the CTA's sums (summed over its warps in a fixed order) fill its slot of a partial-sum array,
+// which a second kernel adds up in a fixed order, so dw does not depend on timing.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/ulysses.h"
+#include "plan.h"
+#include "ptx.cuh"
+
+namespace uly {
+
+static __device__ unsigned g_fused_bwd_status;
+
+#ifndef ULY_BWD_CTAS_PER_SM
+#define ULY_BWD_CTAS_PER_SM 4
+#endif
+#ifndef ULY_BWD_CONSUMER_WARPS
+#define ULY_BWD_CONSUMER_WARPS 4
+#endif
+#ifndef ULY_BWD_STAGE_TARGET
+#define ULY_BWD_STAGE_TARGET 20480
+#endif
+#ifndef ULY_BWD_MAX_STAGES
+#define ULY_BWD_MAX_STAGES 2
+#endif
+#ifndef ULY_BWD_ILP
+#define ULY_BWD_ILP 1
+#endif
+constexpr int kBwdCtasPerSm = ULY_BWD_CTAS_PER_SM;
+constexpr int kBwdMaxStages = ULY_BWD_MAX_STAGES;
+constexpr int kBwdNW = ULY_BWD_CONSUMER_WARPS;
+constexpr int kBwdIlp = ULY_BWD_ILP;
+constexpr int kBwdSmemPerSm = 228 * 1024;
+constexpr int kBwdSmemReservedPerCta = 1024;
+constexpr int kBwdSmemPerCtaMax = 227 * 1024;
+constexpr int kBwdHeader = 256;         // barriers, then the head-offset table
+constexpr int kBwdHeadOffAt = 3 * 8 * 8;  // room for 8 stages' barriers
+static_assert(kBwdMaxStages <= 8 && kBwdHeadOffAt + 4 * (kMaxW + 1) <= kBwdHeader, "header");
+constexpr int kBwdLoaderWarp = 0, kBwdTableWarp = 1, kBwdStorerWarp = 2, kBwdFirstConsumer = 3;
+constexpr int kBwdThreads = 32 * (kBwdFirstConsumer + kBwdNW);
+constexpr int kBwdConsumerBarrier = 1;  // named barrier of the consumer warps (0: __syncthreads)
+
+struct BwdUnit {
+    int t;  // 0: q, 1: k
+    int q;
+    int64_t bb, i0;
+    int ntok;
+};
+
+__device__ __forceinline__ BwdUnit bwd_decode(const FusedBwdArgs& a, int64_t u)
+{
+    BwdUnit x;
+    x.t = int(u & 1);
+    const int64_t blk_id = u >> 1;
+    int lo = 0, hi = a.W - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.block_begin[mid] <= blk_id)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    x.q = lo;
+    const int64_t T = a.tokens_per_unit;
+    const int64_t rows = a.rows[lo];
+    const int64_t blocks = (rows + T - 1) / T;
+    const int64_t local = blk_id - a.block_begin[lo];
+    x.bb = div_fast(local, blocks);
+    const int64_t blk = local - x.bb * blocks;
+    x.i0 = a.row_lo[lo] + blk * T;
+    x.ntok = int(min(T, rows - blk * T));
+    return x;
+}
+
+__device__ __forceinline__ float bwd_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bwd_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t bwd_pack(float lo, float hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// cos and sin of 2 pi * frac(p * (hi + lo)), p a non-negative integer below 2^24; the angle is
+// reduced in turns with an error-free product (see the forward kernel).
+__device__ __forceinline__ float2 bwd_cos_sin(float p, float hi, float lo)
+{
+    const float ph = p * hi;
+    const float pe = fmaf(p, hi, -ph);
+    float f = ph - rintf(ph);
+    f += fmaf(p, lo, pe);
+    float s, c;
+    sincospif(2.0f * f, &s, &c);
+    return make_float2(c, s);
+}
+
+// Shared-memory layout (byte offsets), shared by the kernel and its launcher.
+struct BwdSmem {
+    int turns;   // float2 (hi, lo) per pair j < d/2
+    int tables;  // per stage: (cos, sin) per (token, pair)
+    int red;     // per consumer warp: 2 x d fp32 dw sums
+    int stages;  // per stage: forward input span, then output-gradient runs
+    int table_bytes;
+    int total;
+};
+
+__host__ __device__ inline BwdSmem bwd_smem_layout(int d, int tokens, int stages,
+                                                   uint32_t stage_bytes)
+{
+    auto up = [](int x) { return (x + 127) & ~127; };
+    BwdSmem m;
+    m.turns = kBwdHeader;
+    m.tables = up(m.turns + (d / 2) * 8);
+    m.table_bytes = up(tokens * (d / 2) * 8);
+    m.red = up(m.tables + stages * m.table_bytes);
+    m.stages = up(m.red + kBwdNW * 2 * d * 4);
+    m.total = m.stages + stages * int(stage_bytes);
+    return m;
+}
+
+template <int G>  // lanes per head row; d = 8 * G
+__global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
+    fused_qk_bwd_kernel(const __grid_constant__ FusedBwdArgs a)
+{
+    constexpr int D = 8 * G;
+    constexpr int HALF = D / 2;
+    constexpr int GPW = 32 / G;  // head rows per warp per slot
+    constexpr int PER_STEP = GPW * kBwdIlp;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int K = a.stages;
+    const int N = int(a.N);
+    const BwdSmem L = bwd_smem_layout(D, a.tokens_per_unit, K, a.stage_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // data landed + table written
+    uint64_t* computed = full + kBwdMaxStages;           // consumers done with the stage
+    uint64_t* empty = computed + kBwdMaxStages;          // the store has read the stage
+    int* hoff = reinterpret_cast<int*>(smem + kBwdHeadOffAt);
+    float2* turns = reinterpret_cast<float2*>(smem + L.turns);
+    float* red = reinterpret_cast<float*>(smem + L.red);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    const int64_t n = first < a.total_units ? (a.total_units - 1 - first) / step + 1 : 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < K; ++s) {
+            mbar_init(&full[s], 1 + 32);  // loader lane + the table warp's lanes
+            mbar_init(&computed[s], kBwdNW);
+            mbar_init(&empty[s], 1);
+        }
+        fence_barrier_init();
+    }
+    for (int j = threadIdx.x; j < HALF; j += blockDim.x) turns[j] = make_float2(a.turn_hi[j], a.turn_lo[j]);
+    for (int j = threadIdx.x; j <= kMaxW; j += blockDim.x) hoff[j] = int(a.head_off[j]);
+    for (int j = threadIdx.x; j < kBwdNW * 2 * D; j += blockDim.x) red[j] = 0.0f;
+    __syncthreads();
+    const int row_bytes = N * D * 2;                // one token, all heads, one tensor
+    const uint32_t grad_at = a.stage_bytes / 2;     // the gradient runs' offset in a stage
+
+    if (warp == kBwdLoaderWarp) {
+        // Per unit: lane 0 the input span, lane 1 + r the gradient run of rank r. The runs land
+        // rank after rank: rank r's ntok * n_r rows start at row ntok * head_off[r].
+        int64_t j = 0;
+        for (; j < n; ++j) {
+            const int s = int(j % K);
+            int ok = 1;
+            if (lane == 0 && j >= K) ok = mbar_wait_bounded(&empty[s], uint32_t(((j / K) - 1) & 1));
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) atomicOr(&g_fused_bwd_status, kStatusWaitTimeout);
+                break;
+            }
+            const BwdUnit t = bwd_decode(a, first + j * step);
+            const uint32_t span = uint32_t(t.ntok) * uint32_t(row_bytes);
+            uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], 2 * span);
+            __syncwarp();
+            if (lane == 0) {
+                const int64_t tok0 = t.bb * a.s[t.q] + t.i0;
+                bulk_g2s(dst, a.x_in[t.t][t.q] + tok0 * row_bytes, span, &full[s]);
+            } else if (lane <= a.W) {
+                const int r = lane - 1;
+                const int64_t run = a.n[r] * (D * 2);  // bytes per token on rank r
+                if (run > 0) {
+                    const int64_t row0 = t.bb * a.S + a.seq_off[t.q] + t.i0;
+                    bulk_g2s(dst + grad_at + uint32_t(t.ntok) * uint32_t(a.head_off[r] * (D * 2)),
+                             a.g_in[t.t][r] + row0 * run, uint32_t(t.ntok * run), &full[s]);
+                }
+            }
+        }
+        // do not leave while copies into this CTA's shared memory may be in flight
+        if (lane == 0) {
+            for (int64_t jj = (j > K ? j - K : 0); jj < j; ++jj) {
+                if (!mbar_wait_bounded(&full[jj % K], uint32_t((jj / K) & 1))) {
+                    atomicOr(&g_fused_bwd_status, kStatusDrainTimeout);
+                    break;
+                }
+            }
+        }
+        return;
+    }
+
+    if (warp == kBwdTableWarp) {  // cos/sin of each unit's positions (layout as the forward's)
+        for (int64_t j = 0; j < n; ++j) {
+            const int s = int(j % K);
+            if (j >= K && !mbar_wait_bounded(&computed[s], uint32_t(((j / K) - 1) & 1))) {
+                if (lane == 0) atomicOr(&g_fused_bwd_status, kStatusWaitTimeout);
+                break;
+            }
+            const BwdUnit t = bwd_decode(a, first + j * step);
+            float* table = reinterpret_cast<float*>(smem + L.tables + s * L.table_bytes);
+            const float p0 = float(a.seq_off[t.q] + t.i0);
+            for (int e = lane; e < t.ntok * HALF; e += 32) {
+                const int tok = e / HALF, jj = e % HALF;
+                const float2 tj = turns[jj];
+                const float2 cs = bwd_cos_sin(p0 + float(tok), tj.x, tj.y);
+                const int at = ((tok * 2 + ((jj >> 1) & 1)) * G + (jj >> 2)) * 4 + (jj & 1);
+                table[at] = cs.x;
+                table[at + 2] = cs.y;
+            }
+            mbar_arrive(&full[s]);
+        }
+        return;
+    }
+
+    if (warp == kBwdStorerWarp) {  // one bulk store of dx per unit, then the stage is free
+        if (lane != 0) return;
+        for (int64_t j = 0; j < n; ++j) {
+            const int s = int(j % K);
+            if (!mbar_wait_bounded(&computed[s], uint32_t((j / K) & 1))) {
+                atomicOr(&g_fused_bwd_status, kStatusWaitTimeout);
+                break;
+            }
+            const BwdUnit t = bwd_decode(a, first + j * step);
+            const int64_t tok0 = t.bb * a.s[t.q] + t.i0;
+            bulk_s2g(a.dx_out[t.t][t.q] + tok0 * row_bytes, smem + L.stages + size_t(s) * a.stage_bytes,
+                     uint32_t(t.ntok) * uint32_t(row_bytes));
+            bulk_commit();
+            bulk_wait_read<0>();
+            mbar_arrive(&empty[s]);
+        }
+        bulk_wait<0>();
+        return;
+    }
+
+    // consumers: all warps work on the unit's tensor, each on a contiguous share of its rows. A
+    // group of d/8 lanes holds one head row (8 values per lane, as packed fp32 pairs: the even
+    // and the odd elements of pairs (0,1) and (2,3)).
+    const int cw = warp - kBwdFirstConsumer;
+    const int sub = lane % G;    // which 8 values of the row this lane holds
+    const int group = lane / G;  // which head row of the warp slot
+    const float inv_d = 1.0f / float(D);
+    for (int64_t k = 0; k < n; ++k) {
+        const int s = int(k % K);
+        const BwdUnit t = bwd_decode(a, first + k * step);
+        float2 wE[2], wO[2];  // this lane's weights of the unit's tensor (even / odd elements)
+        {
+            const float4* wp = reinterpret_cast<const float4*>(a.rms_w + t.t * D + sub * 8);
+            const float4 a0 = __ldg(wp), a1 = __ldg(wp + 1);
+            wE[0] = make_float2(a0.x, a0.z);
+            wO[0] = make_float2(a0.y, a0.w);
+            wE[1] = make_float2(a1.x, a1.z);
+            wO[1] = make_float2(a1.y, a1.w);
+        }
+        if (!mbar_wait_bounded(&full[s], uint32_t((k / K) & 1))) {
+            if (lane == 0) atomicOr(&g_fused_bwd_status, kStatusWaitTimeout);
+            break;
+        }
+        uint8_t* xs = smem + L.stages + size_t(s) * a.stage_bytes;
+        const uint8_t* gs = xs + grad_at;
+        const float4* table = reinterpret_cast<const float4*>(smem + L.tables + s * L.table_bytes);
+        float2 aE[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // dw partial sums
+        float2 aO[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const int rows = t.ntok * N;
+        const int steps = (rows + PER_STEP - 1) / PER_STEP;
+        const int m_lo = cw * steps / kBwdNW, m_hi = (cw + 1) * steps / kBwdNW;
+        int base = m_lo * PER_STEP;  // first row of the current step and its (token, head)
+        int base_tok = base / N;
+        int base_head = base - base_tok * N;
+        for (int m = m_lo; m < m_hi; ++m) {
+            // Two passes per step: the sums (mean square, <u * w, x>) need the whole row, so the
+            // raw bf16 words of x and gy are kept (4 registers each) and unpacked again after the
+            // reduction, rather than holding 24 fp32 values per row across it.
+            uint8_t* slot[kBwdIlp];
+            int tok[kBwdIlp];
+            bool ok[kBwdIlp];
+            uint4 xr[kBwdIlp], gr[kBwdIlp];
+            float ss[kBwdIlp], dp[kBwdIlp];
+#pragma unroll
+            for (int u = 0; u < kBwdIlp; ++u) {
+                const int o = u * GPW + group;
+                ok[u] = base + o < rows;
+                int hh = base_head + o, tk = base_tok;
+                while (hh >= N) {
+                    hh -= N;
+                    ++tk;
+                }
+                int r = 0;  // the rank whose head group holds head hh
+                while (hh >= hoff[r + 1]) ++r;
+                slot[u] = xs + (tk * N + hh) * (D * 2) + sub * 16;
+                tok[u] = tk;
+                const int grow = t.ntok * hoff[r] + tk * (hoff[r + 1] - hoff[r]) + (hh - hoff[r]);
+                xr[u] = make_uint4(0, 0, 0, 0);
+                gr[u] = make_uint4(0, 0, 0, 0);
+                if (ok[u]) {
+                    xr[u] = ld_shared_v4(slot[u]);
+                    gr[u] = ld_shared_v4(gs + grow * (D * 2) + sub * 16);
+                }
+                float2 acc_ss = make_float2(0.f, 0.f), acc_dp = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t x0 = h ? xr[u].z : xr[u].x, x1 = h ? xr[u].w : xr[u].y;
+                    const uint32_t g0 = h ? gr[u].z : gr[u].x, g1 = h ? gr[u].w : gr[u].y;
+                    const float2 xE = make_float2(bwd_lo(x0), bwd_lo(x1));
+                    const float2 xO = make_float2(bwd_hi(x0), bwd_hi(x1));
+                    const float2 gE = make_float2(bwd_lo(g0), bwd_lo(g1));
+                    const float2 gO = make_float2(bwd_hi(g0), bwd_hi(g1));
+                    // (c_j, c_j+1, s_j, s_j+1) for j = 4 sub + 2 h
+                    const float4 cs = table[(tk * 2 + h) * G + sub];
+                    const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
+                    const float2 ns2 = make_float2(-cs.z, -cs.w);
+                    // u = R^T gy: (c g_e + s g_o, c g_o - s g_e)
+                    const float2 uE = __ffma2_rn(gO, s2, __fmul2_rn(gE, c2));
+                    const float2 uO = __ffma2_rn(gE, ns2, __fmul2_rn(gO, c2));
+                    acc_ss = __ffma2_rn(xE, xE, acc_ss);
+                    acc_ss = __ffma2_rn(xO, xO, acc_ss);
+                    acc_dp = __ffma2_rn(__fmul2_rn(uE, wE[h]), xE, acc_dp);
+                    acc_dp = __ffma2_rn(__fmul2_rn(uO, wO[h]), xO, acc_dp);
+                }
+                ss[u] = acc_ss.x + acc_ss.y;
+                dp[u] = acc_dp.x + acc_dp.y;
+            }
+#pragma unroll
+            for (int off = G / 2; off > 0; off >>= 1) {
+#pragma unroll
+                for (int u = 0; u < kBwdIlp; ++u) {
+                    ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], off);
+                    dp[u] += __shfl_xor_sync(0xffffffffu, dp[u], off);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kBwdIlp; ++u) {
+                if (!ok[u]) continue;
+                const float rr = rsqrtf(ss[u] * inv_d + a.eps);
+                const float kk = rr * rr * rr * dp[u] * inv_d;
+                const float2 r2 = make_float2(rr, rr), nk2 = make_float2(-kk, -kk);
+                uint32_t o4[4];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t x0 = h ? xr[u].z : xr[u].x, x1 = h ? xr[u].w : xr[u].y;
+                    const uint32_t g0 = h ? gr[u].z : gr[u].x, g1 = h ? gr[u].w : gr[u].y;
+                    const float2 xE = make_float2(bwd_lo(x0), bwd_lo(x1));
+                    const float2 xO = make_float2(bwd_hi(x0), bwd_hi(x1));
+                    const float2 gE = make_float2(bwd_lo(g0), bwd_lo(g1));
+                    const float2 gO = make_float2(bwd_hi(g0), bwd_hi(g1));
+                    const float4 cs = table[(tok[u] * 2 + h) * G + sub];
+                    const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
+                    const float2 ns2 = make_float2(-cs.z, -cs.w);
+                    const float2 uE = __ffma2_rn(gO, s2, __fmul2_rn(gE, c2));
+                    const float2 uO = __ffma2_rn(gE, ns2, __fmul2_rn(gO, c2));
+                    const float2 dxE = __ffma2_rn(__fmul2_rn(uE, wE[h]), r2, __fmul2_rn(xE, nk2));
+                    const float2 dxO = __ffma2_rn(__fmul2_rn(uO, wO[h]), r2, __fmul2_rn(xO, nk2));
+                    aE[h] = __ffma2_rn(uE, __fmul2_rn(xE, r2), aE[h]);
+                    aO[h] = __ffma2_rn(uO, __fmul2_rn(xO, r2), aO[h]);
+                    o4[2 * h] = bwd_pack(dxE.x, dxO.x);
+                    o4[2 * h + 1] = bwd_pack(dxE.y, dxO.y);
+                }
+                st_shared_v4(slot[u], make_uint4(o4[0], o4[1], o4[2], o4[3]));  // in place
+            }
+            base += PER_STEP;
+            base_head += PER_STEP;
+            while (base_head >= N) {
+                base_head -= N;
+                ++base_tok;
+            }
+        }
+        // make this warp's dx rows visible to the bulk-copy unit, then report the stage done
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&computed[s]);
+        // the unit's dw sums: over the lane groups of the warp, then into the warp's shared row
+#pragma unroll
+        for (int off = G; off < 32; off <<= 1) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                aE[h].x += __shfl_xor_sync(0xffffffffu, aE[h].x, off);
+                aE[h].y += __shfl_xor_sync(0xffffffffu, aE[h].y, off);
+                aO[h].x += __shfl_xor_sync(0xffffffffu, aO[h].x, off);
+                aO[h].y += __shfl_xor_sync(0xffffffffu, aO[h].y, off);
+            }
+        }
+        if (group == 0) {
+            float* row = red + (cw * 2 + t.t) * D + sub * 8;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                row[4 * h + 0] += aE[h].x;
+                row[4 * h + 1] += aO[h].x;
+                row[4 * h + 2] += aE[h].y;
+                row[4 * h + 3] += aO[h].y;
+            }
+        }
+    }
+    // the CTA's dw sums, over its consumer warps in a fixed order, into its slot
+    asm volatile("bar.sync %0, %1;" ::"r"(kBwdConsumerBarrier), "r"(kBwdNW * 32) : "memory");
+    const int ct = threadIdx.x - kBwdFirstConsumer * 32;
+    float* slot_out = a.dw_part + size_t(blockIdx.x) * (2 * D);
+    for (int j = ct; j < 2 * D; j += kBwdNW * 32) {
+        float sum = 0.0f;
+        for (int w = 0; w < kBwdNW; ++w) sum += red[w * 2 * D + j];
+        slot_out[j] = sum;
+    }
+}
+
+// dw[j] = (dw[j] if accumulate) + the sum over slots c < slots of part[c][j], j < n, in a fixed
+// order: warp w of a block adds slots w, w + 16, ... for 32 columns, then warp 0 adds the 16.
+__global__ void __launch_bounds__(512) fused_bwd_reduce_kernel(const float* __restrict__ part,
+                                                               int slots, int n,
+                                                               float* __restrict__ dw,
+                                                               int accumulate)
+{
+    __shared__ float acc[16][33];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int j = blockIdx.x * 32 + lane;
+    float s = 0.0f;
+    if (j < n) {
+        for (int c = w; c < slots; c += 16) s += part[size_t(c) * n + j];
+    }
+    acc[w][lane] = s;
+    __syncthreads();
+    if (w == 0 && j < n) {
+        float total = 0.0f;
+        for (int k = 0; k < 16; ++k) total += acc[k][lane];
+        dw[j] = accumulate ? dw[j] + total : total;
+    }
+}
+
+// Stage geometry for a plan: tokens per unit, stage count and CTAs per SM (0 stages: one token's
+// input and gradient rows do not fit even one CTA per SM). Narrower units, fewer stages, then
+// fewer CTAs per SM are tried in that order.
+void fused_bwd_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages,
+                        uint32_t* stage_bytes, int* ctas_per_sm)
+{
+    *stages = 0;
+    *tokens_per_unit = 1;
+    *stage_bytes = 0;
+    *ctas_per_sm = 1;
+    const int64_t tok_bytes = 2 * p.N * p.d * 2;  // one token's input and gradient rows
+    int64_t T0 = ULY_BWD_STAGE_TARGET / tok_bytes;
+    if (T0 < 1) T0 = 1;
+    for (int ctas = kBwdCtasPerSm; ctas >= 1; --ctas) {
+        const int budget = kBwdSmemPerSm / ctas - kBwdSmemReservedPerCta;
+        for (int64_t T = T0; T >= 1; T = T > 1 ? T / 2 : 0) {
+            const int64_t sb = T * tok_bytes;
+            if (sb >= (1 << 20)) continue;  // an mbarrier counts fewer than 2^20 bytes
+            for (int K = kBwdMaxStages; K >= 2; --K) {
+                const BwdSmem m = bwd_smem_layout(int(p.d), int(T), K, uint32_t(sb));
+                if (m.total <= budget && m.total <= kBwdSmemPerCtaMax) {
+                    *tokens_per_unit = T;
+                    *stages = K;
+                    *stage_bytes = uint32_t(sb);
+                    *ctas_per_sm = ctas;
+                    return;
+                }
+            }
+        }
+    }
+}
+
+static int g_bwd_smem_set[64];
+
+template <int G>
+static cudaError_t bwd_launch_g(const FusedBwdArgs& a, cudaStream_t stream, int device, int grid)
+{
+    constexpr int bit = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : G == 8 ? 3 : G == 16 ? 4 : 5;
+    if (device >= 0 && device < 64 && !(g_bwd_smem_set[device] & (1 << bit))) {
+        cudaError_t e = cudaFuncSetAttribute(fused_qk_bwd_kernel<G>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kBwdSmemPerCtaMax);
+        if (e != cudaSuccess) return e;
+        g_bwd_smem_set[device] |= 1 << bit;
+    }
+    const BwdSmem m = bwd_smem_layout(a.d, a.tokens_per_unit, a.stages, a.stage_bytes);
+    fused_qk_bwd_kernel<G><<<grid, kBwdThreads, m.total, stream>>>(a);
+    return cudaGetLastError();
+}
+
+// CTAs of the main kernel for a launch of `a` (the number of partial-sum slots it fills).
+int64_t fused_bwd_grid(const FusedBwdArgs& a, int sm_count)
+{
+    int64_t grid = int64_t(sm_count) * (a.ctas_per_sm > 0 ? a.ctas_per_sm : 1);
+    return grid < a.total_units ? grid : a.total_units;
+}
+
+// One launch of the backward over `a` (its dw_part holds at least fused_bwd_grid slots), then
+// the reduction of its slots into dw (added to dw when `accumulate`, else written).
+cudaError_t fused_bwd_launch(const FusedBwdArgs& a, float* dw, bool accumulate, cudaStream_t stream,
+                             int device, int sm_count)
+{
+    const int64_t grid = fused_bwd_grid(a, sm_count);
+    if (grid > 0) {
+        cudaError_t e;
+        switch (a.d / 8) {
+            case 1: e = bwd_launch_g<1>(a, stream, device, int(grid)); break;
+            case 2: e = bwd_launch_g<2>(a, stream, device, int(grid)); break;
+            case 4: e = bwd_launch_g<4>(a, stream, device, int(grid)); break;
+            case 8: e = bwd_launch_g<8>(a, stream, device, int(grid)); break;
+            case 16: e = bwd_launch_g<16>(a, stream, device, int(grid)); break;
+            case 32: e = bwd_launch_g<32>(a, stream, device, int(grid)); break;
+            default: return cudaErrorInvalidValue;
+        }
+        if (e != cudaSuccess) return e;
+    } else if (accumulate) {
+        return cudaSuccess;  // nothing to add
+    }
+    const int n = 2 * a.d;
+    fused_bwd_reduce_kernel<<<(n + 31) / 32, 512, 0, stream>>>(a.dw_part, int(grid), n, dw,
+                                                              accumulate ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t fused_bwd_status(unsigned* status, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_fused_bwd_status, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_fused_bwd_status, &zero, sizeof(unsigned));
+}
+
+}  // namespace uly

@@ -226,6 +226,33 @@ void build_fused_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_
     a->total_units = total;
 }
 
+void build_fused_bwd_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_unit,
+                           FusedBwdArgs* a)
+{
+    const int W = p.W;
+    a->W = W;
+    a->d = int32_t(p.d);
+    a->S = p.S;
+    a->N = p.N;
+    a->b = p.b;
+    a->tokens_per_unit = int32_t(tokens_per_unit);
+    int64_t blocks = 0;
+    for (int k = 0; k < kMaxW; ++k) {
+        const bool live = k < W;
+        a->s[k] = live ? p.s[k] : 0;
+        a->seq_off[k] = live ? p.seq_off[k] : 0;
+        a->n[k] = live ? p.n[k] : 0;
+        a->head_off[k] = live ? p.head_off[k] : p.N;
+        a->row_lo[k] = live ? rows.lo[k] : 0;
+        a->rows[k] = live ? rows.cnt[k] : 0;
+        a->block_begin[k] = blocks;
+        if (live) blocks += p.b * ceil_div(a->rows[k], tokens_per_unit);
+    }
+    a->head_off[kMaxW] = p.N;
+    a->block_begin[kMaxW] = blocks;
+    a->total_units = 2 * blocks;
+}
+
 // theta^(-2j/d) expressed in turns (divided by 2 pi), split into a float pair whose sum carries
 // about 48 significant bits, so that p * turn can be reduced modulo 1 exactly enough in fp32.
 void rope_turns(int64_t d, double theta, float* turn_hi, float* turn_lo)

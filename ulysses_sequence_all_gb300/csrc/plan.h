@@ -106,6 +106,34 @@ struct FusedArgs {
 };
 
 void build_fused_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_unit, FusedArgs* a);
+
+// ---- fused QK backward's argument block -------------------------------------------------------
+// A token block is tokens_per_unit consecutive rows (tokens) of one shard q and one batch index;
+// it makes two work units, one per tensor (even unit q, odd unit k). A unit reads the tensor's
+// forward input for those tokens (all N heads: one contiguous span on the sequence side) and the
+// gradient of its output (W runs, rank r's n_r heads of those tokens, contiguous on rank r's head
+// side), and writes the gradient of the input (one span on the sequence side).
+struct FusedBwdArgs {
+    const uint8_t* x_in[2][kMaxW];  // forward inputs q, k: rank q's (b, s_q, N, d) bf16
+    const uint8_t* g_in[2][kMaxW];  // gradients of the forward outputs: rank r's (b, S, n_r, d)
+    uint8_t* dx_out[2][kMaxW];      // gradients of the forward inputs: rank q's (b, s_q, N, d)
+    const float* rms_w;             // [2][d]
+    float* dw_part;                 // [grid][2][d]: one slot per CTA, fully written by it
+    int64_t s[kMaxW], seq_off[kMaxW], n[kMaxW], head_off[kMaxW + 1];
+    int64_t row_lo[kMaxW], rows[kMaxW];
+    int64_t block_begin[kMaxW + 1];  // prefix of token-block counts over q
+    int64_t S, N, b;
+    int64_t total_units;  // two per token block
+    int32_t W, d, tokens_per_unit, stages;
+    int32_t ctas_per_sm;
+    uint32_t stage_bytes;  // forward input then output gradient of tokens_per_unit tokens
+    float eps;
+    float turn_hi[kMaxFusedD / 2];
+    float turn_lo[kMaxFusedD / 2];
+};
+
+void build_fused_bwd_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_unit,
+                           FusedBwdArgs* a);
 void rope_turns(int64_t d, double theta, float* turn_hi, float* turn_lo);
 
 }  // namespace uly
