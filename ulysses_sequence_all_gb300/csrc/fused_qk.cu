@@ -101,7 +101,7 @@ __device__ __forceinline__ FusedUnit fused_decode(const FusedArgs& a, int64_t u)
     t.q = lo;
     const int64_t T = a.tokens_per_unit;
     const int64_t rows = a.rows[lo];
-    const int64_t blocks = (rows + T - 1) / T;
+    const int64_t blocks = a.blocks[lo];  // token blocks per batch index of shard q
     const int64_t local = u - a.unit_begin[lo];
     t.bb = div_fast(local, blocks);
     const int64_t blk = local - t.bb * blocks;
@@ -109,6 +109,20 @@ __device__ __forceinline__ FusedUnit fused_decode(const FusedArgs& a, int64_t u)
     t.ntok = int(min(T, rows - blk * T));
     return t;
 }
+
+// Position in the ring of K stages: the stage of the current unit and the parity of its use
+// (unit j uses stage j mod K for the (j div K)-th time), advanced without division.
+struct FusedRing {
+    int s = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next(int K)
+    {
+        if (++s == K) {
+            s = 0;
+            phase ^= 1u;
+        }
+    }
+};
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -196,9 +210,10 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     if (warp == kLoaderWarp) {  // one lane streams units into the stages
         if (lane != 0) return;
         int64_t j = 0;
-        for (; j < n; ++j) {
-            const int s = int(j % K);
-            if (j >= K && !mbar_wait_bounded(&empty[s], uint32_t(((j / K) - 1) & 1))) {
+        FusedRing ring;
+        for (; j < n; ++j, ring.next(K)) {
+            const int s = ring.s;
+            if (j >= K && !mbar_wait_bounded(&empty[s], ring.phase ^ 1u)) {
                 atomicOr(&g_fused_status, kStatusWaitTimeout);
                 break;
             }
@@ -225,9 +240,10 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     }
 
     if (warp == kTableWarp) {  // cos/sin of each unit's positions, once the stage's table is free
-        for (int64_t j = 0; j < n; ++j) {
-            const int s = int(j % K);
-            if (j >= K && !mbar_wait_bounded(&computed[s], uint32_t(((j / K) - 1) & 1))) {
+        FusedRing ring;
+        for (int64_t j = 0; j < n; ++j, ring.next(K)) {
+            const int s = ring.s;
+            if (j >= K && !mbar_wait_bounded(&computed[s], ring.phase ^ 1u)) {
                 if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
                 break;
             }
@@ -256,9 +272,10 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
         // tensor. A stage is handed back to the loader kFusedDrain units later, once its stores
         // have read it.
         int64_t j = 0;
-        for (; j < n; ++j) {
-            const int s = int(j % K);
-            if (!mbar_wait_bounded(&computed[s], uint32_t((j / K) & 1))) {
+        FusedRing ring;
+        for (; j < n; ++j, ring.next(K)) {
+            const int s = ring.s;
+            if (!mbar_wait_bounded(&computed[s], ring.phase)) {
                 if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
                 break;
             }
@@ -306,10 +323,11 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
         for (int h = 0; h < 2; ++h) wOn[h] = make_float2(-wO[h].x, -wO[h].y);
     }
     const float inv_d = 1.0f / float(D);
-    for (int64_t k = 0; k < n; ++k) {
-        const int s = int(k % K);
+    FusedRing ring;
+    for (int64_t k = 0; k < n; ++k, ring.next(K)) {
+        const int s = ring.s;
         const FusedUnit t = fused_decode(a, first + k * step);
-        if (!mbar_wait_bounded(&full[s], uint32_t((k / K) & 1))) {
+        if (!mbar_wait_bounded(&full[s], ring.phase)) {
             if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
             break;
         }

@@ -14,14 +14,16 @@
 // on the head side, where mode 0 put y, so the rows arrive through the mode-1 gather.
 //
 // Structure: the forward kernel's pipeline (persistent grid, several CTAs per SM, a ring of
-// shared-memory stages; loader, table, storer and consumer warps). A unit is one tensor (q or k)
-// of a block of tokens of one shard: the loader brings the forward input span (one bulk copy)
-// and the W runs of the output gradient (one bulk copy per rank) into a stage; the consumers
-// overwrite the input rows with dx; the storer writes the span back with one bulk store. Each
-// consumer lane keeps dw partial sums for its 8 columns; they are summed over the lanes of a
-// warp at the end of each unit and added to the warp's row of a small shared array; at the end
-// the CTA's sums (summed over its warps in a fixed order) fill its slot of a partial-sum array,
-// which a second kernel adds up in a fixed order, so dw does not depend on timing.
+// shared-memory stages; a loader warp, which also fills the rope table, a storer warp and
+// consumer warps). A unit is one tensor (q or k) of a block of tokens of one shard: the loader
+// brings the forward input span (one bulk copy) and the output gradient (one bulk copy per token
+// and rank: rank r's n_r heads, placed so that the gradient rows follow the input's (token, head)
+// order) into a stage; the consumers overwrite the input rows with dx; the storer writes the span
+// back with one bulk store. Each consumer lane keeps dw partial sums for its 8 columns; they are
+// summed over the lanes of a warp at the end of each unit and added to the warp's row of a small
+// shared array; at the end the CTA's sums (over its warps, in a fixed order) fill its slot of a
+// partial-sum array, which a second kernel adds up in a fixed order, so dw does not depend on
+// timing.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -55,10 +57,9 @@ constexpr int kBwdIlp = ULY_BWD_ILP;
 constexpr int kBwdSmemPerSm = 228 * 1024;
 constexpr int kBwdSmemReservedPerCta = 1024;
 constexpr int kBwdSmemPerCtaMax = 227 * 1024;
-constexpr int kBwdHeader = 256;         // barriers, then the head-offset table
-constexpr int kBwdHeadOffAt = 3 * 8 * 8;  // room for 8 stages' barriers
-static_assert(kBwdMaxStages <= 8 && kBwdHeadOffAt + 4 * (kMaxW + 1) <= kBwdHeader, "header");
-constexpr int kBwdLoaderWarp = 0, kBwdTableWarp = 1, kBwdStorerWarp = 2, kBwdFirstConsumer = 3;
+constexpr int kBwdHeader = 256;  // three barriers per stage
+static_assert(3 * 8 * kBwdMaxStages <= kBwdHeader, "stage barriers must fit the header");
+constexpr int kBwdLoaderWarp = 0, kBwdStorerWarp = 1, kBwdFirstConsumer = 2;
 constexpr int kBwdThreads = 32 * (kBwdFirstConsumer + kBwdNW);
 constexpr int kBwdConsumerBarrier = 1;  // named barrier of the consumer warps (0: __syncthreads)
 
@@ -84,15 +85,28 @@ __device__ __forceinline__ BwdUnit bwd_decode(const FusedBwdArgs& a, int64_t u)
     }
     x.q = lo;
     const int64_t T = a.tokens_per_unit;
-    const int64_t rows = a.rows[lo];
-    const int64_t blocks = (rows + T - 1) / T;
+    const int64_t blocks = a.blocks[lo];  // token blocks per batch index of shard q
     const int64_t local = blk_id - a.block_begin[lo];
     x.bb = div_fast(local, blocks);
     const int64_t blk = local - x.bb * blocks;
     x.i0 = a.row_lo[lo] + blk * T;
-    x.ntok = int(min(T, rows - blk * T));
+    x.ntok = int(min(T, a.rows[lo] - blk * T));
     return x;
 }
+
+// Position in the ring of K stages: the stage of the current unit and the parity of its use
+// (units j = 0, 1, ... use stage j mod K for the (j div K)-th time), advanced without division.
+struct BwdRing {
+    int s = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next(int K)
+    {
+        if (++s == K) {
+            s = 0;
+            phase ^= 1u;
+        }
+    }
+};
 
 __device__ __forceinline__ float bwd_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bwd_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -120,6 +134,7 @@ __device__ __forceinline__ float2 bwd_cos_sin(float p, float hi, float lo)
 struct BwdSmem {
     int turns;   // float2 (hi, lo) per pair j < d/2
     int tables;  // per stage: (cos, sin) per (token, pair)
+    int weights; // 2 x d fp32 RMSNorm weights
     int red;     // per consumer warp: 2 x d fp32 dw sums
     int stages;  // per stage: forward input span, then output-gradient runs
     int table_bytes;
@@ -134,7 +149,8 @@ __host__ __device__ inline BwdSmem bwd_smem_layout(int d, int tokens, int stages
     m.turns = kBwdHeader;
     m.tables = up(m.turns + (d / 2) * 8);
     m.table_bytes = up(tokens * (d / 2) * 8);
-    m.red = up(m.tables + stages * m.table_bytes);
+    m.weights = up(m.tables + stages * m.table_bytes);
+    m.red = m.weights + 2 * d * 4;
     m.stages = up(m.red + kBwdNW * 2 * d * 4);
     m.total = m.stages + stages * int(stage_bytes);
     return m;
@@ -155,35 +171,36 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // data landed + table written
     uint64_t* computed = full + kBwdMaxStages;           // consumers done with the stage
     uint64_t* empty = computed + kBwdMaxStages;          // the store has read the stage
-    int* hoff = reinterpret_cast<int*>(smem + kBwdHeadOffAt);
     float2* turns = reinterpret_cast<float2*>(smem + L.turns);
     float* red = reinterpret_cast<float*>(smem + L.red);
+    float* wsm = reinterpret_cast<float*>(smem + L.weights);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t first = blockIdx.x, step = gridDim.x;
     const int64_t n = first < a.total_units ? (a.total_units - 1 - first) / step + 1 : 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < K; ++s) {
-            mbar_init(&full[s], 1 + 32);  // loader lane + the table warp's lanes
+            mbar_init(&full[s], 1 + 32);  // the loader's expect_tx, then its lanes' table writes
             mbar_init(&computed[s], kBwdNW);
             mbar_init(&empty[s], 1);
         }
         fence_barrier_init();
     }
     for (int j = threadIdx.x; j < HALF; j += blockDim.x) turns[j] = make_float2(a.turn_hi[j], a.turn_lo[j]);
-    for (int j = threadIdx.x; j <= kMaxW; j += blockDim.x) hoff[j] = int(a.head_off[j]);
     for (int j = threadIdx.x; j < kBwdNW * 2 * D; j += blockDim.x) red[j] = 0.0f;
+    for (int j = threadIdx.x; j < 2 * D; j += blockDim.x) wsm[j] = a.rms_w[j];
     __syncthreads();
     const int row_bytes = N * D * 2;                // one token, all heads, one tensor
     const uint32_t grad_at = a.stage_bytes / 2;     // the gradient runs' offset in a stage
 
     if (warp == kBwdLoaderWarp) {
-        // Per unit: lane 0 the input span, lane 1 + r the gradient run of rank r. The runs land
-        // rank after rank: rank r's ntok * n_r rows start at row ntok * head_off[r].
+        // Per unit: lane 0 the input span; then one copy per (token, rank) of the gradient, so
+        // that the gradient rows land in the input's (token, head) order, grad_at bytes further.
         int64_t j = 0;
-        for (; j < n; ++j) {
-            const int s = int(j % K);
+        BwdRing ring;
+        for (; j < n; ++j, ring.next(K)) {
+            const int s = ring.s;
             int ok = 1;
-            if (lane == 0 && j >= K) ok = mbar_wait_bounded(&empty[s], uint32_t(((j / K) - 1) & 1));
+            if (lane == 0 && j >= K) ok = mbar_wait_bounded(&empty[s], ring.phase ^ 1u);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0) atomicOr(&g_fused_bwd_status, kStatusWaitTimeout);
@@ -192,20 +209,37 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
             const BwdUnit t = bwd_decode(a, first + j * step);
             const uint32_t span = uint32_t(t.ntok) * uint32_t(row_bytes);
             uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
-            if (lane == 0) mbar_arrive_expect_tx(&full[s], 2 * span);
-            __syncwarp();
             if (lane == 0) {
+                mbar_arrive_expect_tx(&full[s], 2 * span);
                 const int64_t tok0 = t.bb * a.s[t.q] + t.i0;
                 bulk_g2s(dst, a.x_in[t.t][t.q] + tok0 * row_bytes, span, &full[s]);
-            } else if (lane <= a.W) {
-                const int r = lane - 1;
-                const int64_t run = a.n[r] * (D * 2);  // bytes per token on rank r
-                if (run > 0) {
-                    const int64_t row0 = t.bb * a.S + a.seq_off[t.q] + t.i0;
-                    bulk_g2s(dst + grad_at + uint32_t(t.ntok) * uint32_t(a.head_off[r] * (D * 2)),
-                             a.g_in[t.t][r] + row0 * run, uint32_t(t.ntok * run), &full[s]);
-                }
             }
+            __syncwarp();
+            const int64_t row0 = t.bb * a.S + a.seq_off[t.q] + t.i0;  // first head-side row
+            const int copies = t.ntok * a.W;
+            for (int c = lane; c < copies; c += 32) {
+                const int tok = c / a.W, r = c - tok * a.W;
+                const int64_t run = a.n[r] * (D * 2);  // bytes per token on rank r
+                if (run == 0) continue;
+                bulk_g2s(dst + grad_at + tok * row_bytes + int(a.head_off[r]) * (D * 2),
+                         a.g_in[t.t][r] + (row0 + tok) * run, uint32_t(run), &full[s]);
+            }
+            // While the copies fly, the lanes fill the stage's cos/sin table for the unit's
+            // positions (free: the stage's previous unit has been stored, so its consumers are
+            // done) and arrive on "full", so a consumer that sees the phase complete sees both.
+            // Per token, lane i of a row group reads two 16-byte entries (c_j, c_j+1, s_j, s_j+1),
+            // j = 4i and 4i+2; all lanes' entries for j = 4i come first, then those for 4i+2.
+            float* table = reinterpret_cast<float*>(smem + L.tables + s * L.table_bytes);
+            const float p0 = float(a.seq_off[t.q] + t.i0);
+            for (int e = lane; e < t.ntok * HALF; e += 32) {
+                const int tok = e / HALF, jj = e % HALF;
+                const float2 tj = turns[jj];
+                const float2 cs = bwd_cos_sin(p0 + float(tok), tj.x, tj.y);
+                const int at = ((tok * 2 + ((jj >> 1) & 1)) * G + (jj >> 2)) * 4 + (jj & 1);
+                table[at] = cs.x;
+                table[at + 2] = cs.y;
+            }
+            mbar_arrive(&full[s]);
         }
         // do not leave while copies into this CTA's shared memory may be in flight
         if (lane == 0) {
@@ -219,34 +253,12 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
         return;
     }
 
-    if (warp == kBwdTableWarp) {  // cos/sin of each unit's positions (layout as the forward's)
-        for (int64_t j = 0; j < n; ++j) {
-            const int s = int(j % K);
-            if (j >= K && !mbar_wait_bounded(&computed[s], uint32_t(((j / K) - 1) & 1))) {
-                if (lane == 0) atomicOr(&g_fused_bwd_status, kStatusWaitTimeout);
-                break;
-            }
-            const BwdUnit t = bwd_decode(a, first + j * step);
-            float* table = reinterpret_cast<float*>(smem + L.tables + s * L.table_bytes);
-            const float p0 = float(a.seq_off[t.q] + t.i0);
-            for (int e = lane; e < t.ntok * HALF; e += 32) {
-                const int tok = e / HALF, jj = e % HALF;
-                const float2 tj = turns[jj];
-                const float2 cs = bwd_cos_sin(p0 + float(tok), tj.x, tj.y);
-                const int at = ((tok * 2 + ((jj >> 1) & 1)) * G + (jj >> 2)) * 4 + (jj & 1);
-                table[at] = cs.x;
-                table[at + 2] = cs.y;
-            }
-            mbar_arrive(&full[s]);
-        }
-        return;
-    }
-
     if (warp == kBwdStorerWarp) {  // one bulk store of dx per unit, then the stage is free
         if (lane != 0) return;
-        for (int64_t j = 0; j < n; ++j) {
-            const int s = int(j % K);
-            if (!mbar_wait_bounded(&computed[s], uint32_t((j / K) & 1))) {
+        BwdRing ring;
+        for (int64_t j = 0; j < n; ++j, ring.next(K)) {
+            const int s = ring.s;
+            if (!mbar_wait_bounded(&computed[s], ring.phase)) {
                 atomicOr(&g_fused_bwd_status, kStatusWaitTimeout);
                 break;
             }
@@ -269,19 +281,20 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
     const int sub = lane % G;    // which 8 values of the row this lane holds
     const int group = lane / G;  // which head row of the warp slot
     const float inv_d = 1.0f / float(D);
-    for (int64_t k = 0; k < n; ++k) {
-        const int s = int(k % K);
+    BwdRing ring;
+    for (int64_t k = 0; k < n; ++k, ring.next(K)) {
+        const int s = ring.s;
         const BwdUnit t = bwd_decode(a, first + k * step);
         float2 wE[2], wO[2];  // this lane's weights of the unit's tensor (even / odd elements)
         {
-            const float4* wp = reinterpret_cast<const float4*>(a.rms_w + t.t * D + sub * 8);
-            const float4 a0 = __ldg(wp), a1 = __ldg(wp + 1);
+            const float4* wp = reinterpret_cast<const float4*>(wsm + t.t * D + sub * 8);
+            const float4 a0 = wp[0], a1 = wp[1];
             wE[0] = make_float2(a0.x, a0.z);
             wO[0] = make_float2(a0.y, a0.w);
             wE[1] = make_float2(a1.x, a1.z);
             wO[1] = make_float2(a1.y, a1.w);
         }
-        if (!mbar_wait_bounded(&full[s], uint32_t((k / K) & 1))) {
+        if (!mbar_wait_bounded(&full[s], ring.phase)) {
             if (lane == 0) atomicOr(&g_fused_bwd_status, kStatusWaitTimeout);
             break;
         }
@@ -297,13 +310,13 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
         int base_tok = base / N;
         int base_head = base - base_tok * N;
         for (int m = m_lo; m < m_hi; ++m) {
-            // Two passes per step: the sums (mean square, <u * w, x>) need the whole row, so the
-            // raw bf16 words of x and gy are kept (4 registers each) and unpacked again after the
-            // reduction, rather than holding 24 fp32 values per row across it.
-            uint8_t* slot[kBwdIlp];
-            int tok[kBwdIlp];
+            // The sums (mean square, <u * w, x>) need the whole row: u = R^T gy (8 fp32 values)
+            // and the raw bf16 words of x are kept across the reduction, then dx and the dw
+            // terms are formed.
+            int off[kBwdIlp];
             bool ok[kBwdIlp];
-            uint4 xr[kBwdIlp], gr[kBwdIlp];
+            uint4 xr[kBwdIlp];
+            float2 uE[kBwdIlp][2], uO[kBwdIlp][2];
             float ss[kBwdIlp], dp[kBwdIlp];
 #pragma unroll
             for (int u = 0; u < kBwdIlp; ++u) {
@@ -314,22 +327,18 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
                     hh -= N;
                     ++tk;
                 }
-                int r = 0;  // the rank whose head group holds head hh
-                while (hh >= hoff[r + 1]) ++r;
-                slot[u] = xs + (tk * N + hh) * (D * 2) + sub * 16;
-                tok[u] = tk;
-                const int grow = t.ntok * hoff[r] + tk * (hoff[r + 1] - hoff[r]) + (hh - hoff[r]);
+                off[u] = (base + o) * (D * 2) + sub * 16;  // row (tk, hh) of the unit
+                uint4 g = make_uint4(0, 0, 0, 0);
                 xr[u] = make_uint4(0, 0, 0, 0);
-                gr[u] = make_uint4(0, 0, 0, 0);
                 if (ok[u]) {
-                    xr[u] = ld_shared_v4(slot[u]);
-                    gr[u] = ld_shared_v4(gs + grow * (D * 2) + sub * 16);
+                    xr[u] = ld_shared_v4(xs + off[u]);
+                    g = ld_shared_v4(gs + off[u]);
                 }
                 float2 acc_ss = make_float2(0.f, 0.f), acc_dp = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t x0 = h ? xr[u].z : xr[u].x, x1 = h ? xr[u].w : xr[u].y;
-                    const uint32_t g0 = h ? gr[u].z : gr[u].x, g1 = h ? gr[u].w : gr[u].y;
+                    const uint32_t g0 = h ? g.z : g.x, g1 = h ? g.w : g.y;
                     const float2 xE = make_float2(bwd_lo(x0), bwd_lo(x1));
                     const float2 xO = make_float2(bwd_hi(x0), bwd_hi(x1));
                     const float2 gE = make_float2(bwd_lo(g0), bwd_lo(g1));
@@ -339,22 +348,22 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
                     const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
                     const float2 ns2 = make_float2(-cs.z, -cs.w);
                     // u = R^T gy: (c g_e + s g_o, c g_o - s g_e)
-                    const float2 uE = __ffma2_rn(gO, s2, __fmul2_rn(gE, c2));
-                    const float2 uO = __ffma2_rn(gE, ns2, __fmul2_rn(gO, c2));
+                    uE[u][h] = __ffma2_rn(gO, s2, __fmul2_rn(gE, c2));
+                    uO[u][h] = __ffma2_rn(gE, ns2, __fmul2_rn(gO, c2));
                     acc_ss = __ffma2_rn(xE, xE, acc_ss);
                     acc_ss = __ffma2_rn(xO, xO, acc_ss);
-                    acc_dp = __ffma2_rn(__fmul2_rn(uE, wE[h]), xE, acc_dp);
-                    acc_dp = __ffma2_rn(__fmul2_rn(uO, wO[h]), xO, acc_dp);
+                    acc_dp = __ffma2_rn(__fmul2_rn(uE[u][h], wE[h]), xE, acc_dp);
+                    acc_dp = __ffma2_rn(__fmul2_rn(uO[u][h], wO[h]), xO, acc_dp);
                 }
                 ss[u] = acc_ss.x + acc_ss.y;
                 dp[u] = acc_dp.x + acc_dp.y;
             }
 #pragma unroll
-            for (int off = G / 2; off > 0; off >>= 1) {
+            for (int sh = G / 2; sh > 0; sh >>= 1) {
 #pragma unroll
                 for (int u = 0; u < kBwdIlp; ++u) {
-                    ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], off);
-                    dp[u] += __shfl_xor_sync(0xffffffffu, dp[u], off);
+                    ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], sh);
+                    dp[u] += __shfl_xor_sync(0xffffffffu, dp[u], sh);
                 }
             }
 #pragma unroll
@@ -367,24 +376,16 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t x0 = h ? xr[u].z : xr[u].x, x1 = h ? xr[u].w : xr[u].y;
-                    const uint32_t g0 = h ? gr[u].z : gr[u].x, g1 = h ? gr[u].w : gr[u].y;
                     const float2 xE = make_float2(bwd_lo(x0), bwd_lo(x1));
                     const float2 xO = make_float2(bwd_hi(x0), bwd_hi(x1));
-                    const float2 gE = make_float2(bwd_lo(g0), bwd_lo(g1));
-                    const float2 gO = make_float2(bwd_hi(g0), bwd_hi(g1));
-                    const float4 cs = table[(tok[u] * 2 + h) * G + sub];
-                    const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
-                    const float2 ns2 = make_float2(-cs.z, -cs.w);
-                    const float2 uE = __ffma2_rn(gO, s2, __fmul2_rn(gE, c2));
-                    const float2 uO = __ffma2_rn(gE, ns2, __fmul2_rn(gO, c2));
-                    const float2 dxE = __ffma2_rn(__fmul2_rn(uE, wE[h]), r2, __fmul2_rn(xE, nk2));
-                    const float2 dxO = __ffma2_rn(__fmul2_rn(uO, wO[h]), r2, __fmul2_rn(xO, nk2));
-                    aE[h] = __ffma2_rn(uE, __fmul2_rn(xE, r2), aE[h]);
-                    aO[h] = __ffma2_rn(uO, __fmul2_rn(xO, r2), aO[h]);
+                    const float2 dxE = __ffma2_rn(__fmul2_rn(uE[u][h], wE[h]), r2, __fmul2_rn(xE, nk2));
+                    const float2 dxO = __ffma2_rn(__fmul2_rn(uO[u][h], wO[h]), r2, __fmul2_rn(xO, nk2));
+                    aE[h] = __ffma2_rn(uE[u][h], __fmul2_rn(xE, r2), aE[h]);
+                    aO[h] = __ffma2_rn(uO[u][h], __fmul2_rn(xO, r2), aO[h]);
                     o4[2 * h] = bwd_pack(dxE.x, dxO.x);
                     o4[2 * h + 1] = bwd_pack(dxE.y, dxO.y);
                 }
-                st_shared_v4(slot[u], make_uint4(o4[0], o4[1], o4[2], o4[3]));  // in place
+                st_shared_v4(xs + off[u], make_uint4(o4[0], o4[1], o4[2], o4[3]));  // in place
             }
             base += PER_STEP;
             base_head += PER_STEP;

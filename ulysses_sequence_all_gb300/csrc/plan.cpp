@@ -220,7 +220,8 @@ void build_fused_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_
         a->row_lo[k] = live ? rows.lo[k] : 0;
         a->rows[k] = live ? rows.cnt[k] : 0;
         a->unit_begin[k] = total;
-        if (live) total += p.b * ceil_div(a->rows[k], tokens_per_unit);
+        a->blocks[k] = live ? ceil_div(a->rows[k], tokens_per_unit) : 0;
+        total += p.b * a->blocks[k];
     }
     a->unit_begin[kMaxW] = total;
     a->total_units = total;
@@ -246,7 +247,8 @@ void build_fused_bwd_units(const Plan& p, const ChunkRows& rows, int64_t tokens_
         a->row_lo[k] = live ? rows.lo[k] : 0;
         a->rows[k] = live ? rows.cnt[k] : 0;
         a->block_begin[k] = blocks;
-        if (live) blocks += p.b * ceil_div(a->rows[k], tokens_per_unit);
+        a->blocks[k] = live ? ceil_div(a->rows[k], tokens_per_unit) : 0;
+        blocks += p.b * a->blocks[k];
     }
     a->head_off[kMaxW] = p.N;
     a->block_begin[kMaxW] = blocks;

@@ -94,6 +94,7 @@ struct FusedArgs {
     int64_t s[kMaxW], seq_off[kMaxW], n[kMaxW], head_off[kMaxW];
     int64_t row_lo[kMaxW], rows[kMaxW];
     int64_t unit_begin[kMaxW + 1];
+    int64_t blocks[kMaxW];  // token blocks per batch index of shard q
     int64_t S, N, b;
     int64_t total_units;
     int32_t W, d, tokens_per_unit, stages;
@@ -122,6 +123,7 @@ struct FusedBwdArgs {
     int64_t s[kMaxW], seq_off[kMaxW], n[kMaxW], head_off[kMaxW + 1];
     int64_t row_lo[kMaxW], rows[kMaxW];
     int64_t block_begin[kMaxW + 1];  // prefix of token-block counts over q
+    int64_t blocks[kMaxW];           // token blocks per batch index of shard q
     int64_t S, N, b;
     int64_t total_units;  // two per token block
     int32_t W, d, tokens_per_unit, stages;

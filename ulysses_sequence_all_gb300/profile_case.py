@@ -4,7 +4,8 @@
 
 Allocates only what the chosen kernels need (the Wan-720p shape: 774,144,000 bytes per tensor
 set, about 3.1 GB for the fused call's inputs and outputs), launches each kernel `iters` times,
-synchronises and checks the device status word. It reports no timing.
+synchronises and checks the device status word. It reports no timing. The backward (`bwd`)
+holds six tensor sets (4.6 GB at the Wan shape; `wan_half` halves the sequence).
 """
 from __future__ import annotations
 
@@ -15,12 +16,14 @@ import torch
 from . import binding as B
 from . import workloads as wl
 
-WORKLOADS = {"wan": wl.WAN, "long": wl.LONG_QKV, "tiny": wl.TINY}
+# half the Wan sequence (37,800 tokens; 387 MB per tensor set) for captures with many passes
+WAN_HALF = wl.Workload("wan720p_half", 8, 1, (4725,) * 8, (5,) * 8, 128, "bfloat16", seed=1)
+WORKLOADS = {"wan": wl.WAN, "wan_half": WAN_HALF, "long": wl.LONG_QKV, "tiny": wl.TINY}
 
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["fused", "mode0", "mode1", "all"], default="all")
+    ap.add_argument("--kernel", choices=["fused", "bwd", "mode0", "mode1", "all"], default="all")
     ap.add_argument("--engine", choices=["tma", "vec"], default="tma")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="wan")
     ap.add_argument("--iters", type=int, default=2)
@@ -50,6 +53,20 @@ def main():
         ko = [torch.empty_like(t) for t in head]
         for _ in range(args.iters):
             B.ulysses_a2a_4d_qk_fused(plan, q, k, head, ko, w, 1e-6, 1e4)
+        torch.cuda.synchronize()
+    if args.kernel in ("bwd", "all"):
+        q = wl.seq_side_inputs(cfg, "cuda", seed=3)
+        k = wl.seq_side_inputs(cfg, "cuda", seed=4)
+        gq = wl.head_side_inputs(cfg, "cuda", seed=5)
+        gk = wl.head_side_inputs(cfg, "cuda", seed=6)
+        w = wl.rms_weights(cfg.d).cuda()
+        dq = [torch.empty_like(t) for t in q]
+        dk = [torch.empty_like(t) for t in k]
+        dw = torch.empty((2, cfg.d), dtype=torch.float32, device="cuda")
+        ws = torch.empty(B.ulysses_qk_fused_backward_workspace(plan), dtype=torch.uint8,
+                         device="cuda")
+        for _ in range(args.iters):
+            B.ulysses_a2a_4d_qk_fused_backward(plan, dq, dk, q, k, gq, gk, w, dw, 1e-6, 1e4, ws)
         torch.cuda.synchronize()
     status = B.ulysses_device_status()
     if status:
