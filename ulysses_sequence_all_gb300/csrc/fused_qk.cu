@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
         FusedRing ring;
         for (int64_t j = 0; j < n; ++j, ring.next(K)) {
             const int s = ring.s;
-            if (j >= K && !mbar_wait_bounded(&computed[s], ring.phase ^ 1u)) {
+            if (j >= K && !__all_sync(0xffffffffu, mbar_wait_bounded(&computed[s], ring.phase ^ 1u))) {
                 if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
                 break;
             }
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
         FusedRing ring;
         for (; j < n; ++j, ring.next(K)) {
             const int s = ring.s;
-            if (!mbar_wait_bounded(&computed[s], ring.phase)) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&computed[s], ring.phase))) {
                 if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
                 break;
             }
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     for (int64_t k = 0; k < n; ++k, ring.next(K)) {
         const int s = ring.s;
         const FusedUnit t = fused_decode(a, first + k * step);
-        if (!mbar_wait_bounded(&full[s], ring.phase)) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], ring.phase))) {
             if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
             break;
         }

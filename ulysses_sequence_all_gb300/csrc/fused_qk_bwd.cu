@@ -281,6 +281,39 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
     const int sub = lane % G;    // which 8 values of the row this lane holds
     const int group = lane / G;  // which head row of the warp slot
     const float inv_d = 1.0f / float(D);
+    // dw partial sums of this lane's 8 columns for tensor acc_t; with an even grid a CTA only
+    // ever sees one tensor (units alternate q, k), so they are flushed once at the end
+    float2 aE[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float2 aO[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    int acc_t = -1;
+    // sums over the lane groups of the warp, added to the warp's shared row, then cleared
+    auto flush_dw = [&]() {
+#pragma unroll
+        for (int off = G; off < 32; off <<= 1) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                aE[h].x += __shfl_xor_sync(0xffffffffu, aE[h].x, off);
+                aE[h].y += __shfl_xor_sync(0xffffffffu, aE[h].y, off);
+                aO[h].x += __shfl_xor_sync(0xffffffffu, aO[h].x, off);
+                aO[h].y += __shfl_xor_sync(0xffffffffu, aO[h].y, off);
+            }
+        }
+        if (group == 0 && acc_t >= 0) {
+            float* row = red + (cw * 2 + acc_t) * D + sub * 8;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                row[4 * h + 0] += aE[h].x;
+                row[4 * h + 1] += aO[h].x;
+                row[4 * h + 2] += aE[h].y;
+                row[4 * h + 3] += aO[h].y;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            aE[h] = make_float2(0.f, 0.f);
+            aO[h] = make_float2(0.f, 0.f);
+        }
+    };
     BwdRing ring;
     for (int64_t k = 0; k < n; ++k, ring.next(K)) {
         const int s = ring.s;
@@ -294,15 +327,17 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
             wE[1] = make_float2(a1.x, a1.z);
             wO[1] = make_float2(a1.y, a1.w);
         }
-        if (!mbar_wait_bounded(&full[s], ring.phase)) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], ring.phase))) {
             if (lane == 0) atomicOr(&g_fused_bwd_status, kStatusWaitTimeout);
             break;
         }
         uint8_t* xs = smem + L.stages + size_t(s) * a.stage_bytes;
         const uint8_t* gs = xs + grad_at;
         const float4* table = reinterpret_cast<const float4*>(smem + L.tables + s * L.table_bytes);
-        float2 aE[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // dw partial sums
-        float2 aO[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        if (t.t != acc_t) {  // the sums so far belong to the other tensor
+            flush_dw();
+            acc_t = t.t;
+        }
         const int rows = t.ntok * N;
         const int steps = (rows + PER_STEP - 1) / PER_STEP;
         const int m_lo = cw * steps / kBwdNW, m_hi = (cw + 1) * steps / kBwdNW;
@@ -398,28 +433,8 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) mbar_arrive(&computed[s]);
-        // the unit's dw sums: over the lane groups of the warp, then into the warp's shared row
-#pragma unroll
-        for (int off = G; off < 32; off <<= 1) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                aE[h].x += __shfl_xor_sync(0xffffffffu, aE[h].x, off);
-                aE[h].y += __shfl_xor_sync(0xffffffffu, aE[h].y, off);
-                aO[h].x += __shfl_xor_sync(0xffffffffu, aO[h].x, off);
-                aO[h].y += __shfl_xor_sync(0xffffffffu, aO[h].y, off);
-            }
-        }
-        if (group == 0) {
-            float* row = red + (cw * 2 + t.t) * D + sub * 8;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                row[4 * h + 0] += aE[h].x;
-                row[4 * h + 1] += aO[h].x;
-                row[4 * h + 2] += aE[h].y;
-                row[4 * h + 3] += aO[h].y;
-            }
-        }
     }
+    flush_dw();
     // the CTA's dw sums, over its consumer warps in a fixed order, into its slot
     asm volatile("bar.sync %0, %1;" ::"r"(kBwdConsumerBarrier), "r"(kBwdNW * 32) : "memory");
     const int ct = threadIdx.x - kBwdFirstConsumer * 32;

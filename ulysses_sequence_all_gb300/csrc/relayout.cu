@@ -52,7 +52,8 @@ constexpr int kVecThreads = 256;
 // k % K. Loads run L units ahead of the unit being stored; a stage is refilled only when the
 // bulk stores that last read it (unit k + L - K, K - L groups back) have finished reading shared
 // memory. So up to L loads and K - L store groups are in flight, and the loop never waits on the
-// stores it has just issued. Every wait is bounded; on a timeout the status word records it,
+// stores it has just issued. Every wait is bounded and its outcome is made uniform across the
+// warp (a lane that timed out stops them all); on a timeout the status word records it,
 // loads still in flight are waited for (bounded again), and the warp returns.
 template <class Load, class Store>
 __device__ __forceinline__ void run_stage_ring(uint64_t* full, int64_t n, int lane, Load load,
@@ -64,7 +65,7 @@ __device__ __forceinline__ void run_stage_ring(uint64_t* full, int64_t n, int la
     int64_t k = 0;
     bool ok = true;
     for (; k < n; ++k) {
-        if (!mbar_wait_bounded(&full[k % K], uint32_t((k / K) & 1))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[k % K], uint32_t((k / K) & 1)))) {
             ok = false;
             break;
         }
@@ -80,7 +81,7 @@ __device__ __forceinline__ void run_stage_ring(uint64_t* full, int64_t n, int la
     if (!ok) {
         if (lane == 0) atomicOr(&g_relayout_status, kStatusWaitTimeout);
         for (int64_t j = k; j < loaded; ++j) {
-            if (!mbar_wait_bounded(&full[j % K], uint32_t((j / K) & 1))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[j % K], uint32_t((j / K) & 1)))) {
                 if (lane == 0) atomicOr(&g_relayout_status, kStatusDrainTimeout);
                 break;
             }
