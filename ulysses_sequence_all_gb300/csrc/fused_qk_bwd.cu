@@ -13,17 +13,17 @@
 // dx is rounded once to bf16 and written on the sequence side, where x came from; gy is read
 // on the head side, where mode 0 put y, so the rows arrive through the mode-1 gather.
 //
-// Structure: the forward kernel's pipeline (persistent grid, several CTAs per SM, a ring of
-// shared-memory stages; a loader warp, which also fills the rope table, a storer warp and
-// consumer warps). A unit is one tensor (q or k) of a block of tokens of one shard: the loader
-// brings the forward input span (one bulk copy) and the output gradient (one bulk copy per token
-// and rank: rank r's n_r heads, placed so that the gradient rows follow the input's (token, head)
-// order) into a stage; the consumers overwrite the input rows with dx; the storer writes the span
-// back with one bulk store. Each consumer lane keeps dw partial sums for its 8 columns; they are
-// summed over the lanes of a warp at the end of each unit and added to the warp's row of a small
-// shared array; at the end the CTA's sums (over its warps, in a fixed order) fill its slot of a
-// partial-sum array, which a second kernel adds up in a fixed order, so dw does not depend on
-// timing.
+// Structure: the forward kernel's pipeline (persistent grid, several CTAs per SM, a ring of shared-
+// memory stages; a loader warp, which also fills the rope table, a storer warp and consumer warps).
+// A unit is one tensor (q or k) of a block of tokens of one shard: the loader brings the forward
+// input span (one bulk copy) and the output gradient (one bulk copy per token and rank: rank r's
+// n_r heads, placed so that the gradient rows follow the input's (token, head) order) into a stage;
+// the consumers overwrite the input rows with dx; the storer writes the span back with one bulk
+// store. The loader decodes each unit once and leaves a small record of it beside the stage for the
+// other roles. Each consumer lane keeps dw partial sums for its 8 columns; they are summed over the
+// lanes of a warp when the tensor of its units changes (never, with an even grid) and at the end,
+// and added to the warp's row of a small shared array; at the end the CTA's sums (over its warps, in a fixed order) fill its slot of a partial-sum array,
+// which a second kernel adds up in a fixed order, so dw does not depend on timing.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -50,6 +50,9 @@ static __device__ unsigned g_fused_bwd_status;
 #ifndef ULY_BWD_ILP
 #define ULY_BWD_ILP 1
 #endif
+#ifndef ULY_BWD_WAIT_HINT_NS  // suspend-time hint of the barrier waits (0: plain polling)
+#define ULY_BWD_WAIT_HINT_NS 10000
+#endif
 constexpr int kBwdCtasPerSm = ULY_BWD_CTAS_PER_SM;
 constexpr int kBwdMaxStages = ULY_BWD_MAX_STAGES;
 constexpr int kBwdNW = ULY_BWD_CONSUMER_WARPS;
@@ -57,8 +60,10 @@ constexpr int kBwdIlp = ULY_BWD_ILP;
 constexpr int kBwdSmemPerSm = 228 * 1024;
 constexpr int kBwdSmemReservedPerCta = 1024;
 constexpr int kBwdSmemPerCtaMax = 227 * 1024;
-constexpr int kBwdHeader = 256;  // three barriers per stage
-static_assert(3 * 8 * kBwdMaxStages <= kBwdHeader, "stage barriers must fit the header");
+constexpr int kBwdHeader = 256;  // three barriers per stage, then one unit record per stage
+constexpr int kBwdRecordsAt = 128;
+static_assert(3 * 8 * kBwdMaxStages <= kBwdRecordsAt, "stage barriers must fit the header");
+static_assert(kBwdRecordsAt + 16 * kBwdMaxStages <= kBwdHeader, "unit records must fit");
 constexpr int kBwdLoaderWarp = 0, kBwdStorerWarp = 1, kBwdFirstConsumer = 2;
 constexpr int kBwdThreads = 32 * (kBwdFirstConsumer + kBwdNW);
 constexpr int kBwdConsumerBarrier = 1;  // named barrier of the consumer warps (0: __syncthreads)
@@ -69,6 +74,23 @@ struct BwdUnit {
     int64_t bb, i0;
     int ntok;
 };
+
+// What the consumers and the storer need of a unit, written by the loader next to the stage
+// before it arrives on "full" (the loader decodes each unit once).
+struct BwdRecord {
+    int64_t seq_row0;  // first row (token) of the unit in rank q's (b, s_q) sequence side
+    int32_t t_q;       // tensor (bit 0) and shard q (bits 1..)
+    int32_t ntok;
+};
+
+__device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity)
+{
+#if ULY_BWD_WAIT_HINT_NS > 0
+    return mbar_wait_bounded_hint<ULY_BWD_WAIT_HINT_NS>(bar, parity);
+#else
+    return mbar_wait_bounded(bar, parity);
+#endif
+}
 
 __device__ __forceinline__ BwdUnit bwd_decode(const FusedBwdArgs& a, int64_t u)
 {
@@ -174,6 +196,7 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
     float2* turns = reinterpret_cast<float2*>(smem + L.turns);
     float* red = reinterpret_cast<float*>(smem + L.red);
     float* wsm = reinterpret_cast<float*>(smem + L.weights);
+    BwdRecord* records = reinterpret_cast<BwdRecord*>(smem + kBwdRecordsAt);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t first = blockIdx.x, step = gridDim.x;
     const int64_t n = first < a.total_units ? (a.total_units - 1 - first) / step + 1 : 0;
@@ -200,7 +223,7 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
         for (; j < n; ++j, ring.next(K)) {
             const int s = ring.s;
             int ok = 1;
-            if (lane == 0 && j >= K) ok = mbar_wait_bounded(&empty[s], ring.phase ^ 1u);
+            if (lane == 0 && j >= K) ok = bwd_wait(&empty[s], ring.phase ^ 1u);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0) atomicOr(&g_fused_bwd_status, kStatusWaitTimeout);
@@ -213,6 +236,10 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
                 mbar_arrive_expect_tx(&full[s], 2 * span);
                 const int64_t tok0 = t.bb * a.s[t.q] + t.i0;
                 bulk_g2s(dst, a.x_in[t.t][t.q] + tok0 * row_bytes, span, &full[s]);
+                BwdRecord& rec = records[s];  // published by this lane's arrive below
+                rec.seq_row0 = tok0;
+                rec.t_q = t.t | (t.q << 1);
+                rec.ntok = t.ntok;
             }
             __syncwarp();
             const int64_t row0 = t.bb * a.S + a.seq_off[t.q] + t.i0;  // first head-side row
@@ -258,14 +285,13 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
         BwdRing ring;
         for (int64_t j = 0; j < n; ++j, ring.next(K)) {
             const int s = ring.s;
-            if (!mbar_wait_bounded(&computed[s], ring.phase)) {
+            if (!bwd_wait(&computed[s], ring.phase)) {
                 atomicOr(&g_fused_bwd_status, kStatusWaitTimeout);
                 break;
             }
-            const BwdUnit t = bwd_decode(a, first + j * step);
-            const int64_t tok0 = t.bb * a.s[t.q] + t.i0;
-            bulk_s2g(a.dx_out[t.t][t.q] + tok0 * row_bytes, smem + L.stages + size_t(s) * a.stage_bytes,
-                     uint32_t(t.ntok) * uint32_t(row_bytes));
+            const BwdRecord rec = records[s];
+            bulk_s2g(a.dx_out[rec.t_q & 1][rec.t_q >> 1] + rec.seq_row0 * row_bytes,
+                     smem + L.stages + size_t(s) * a.stage_bytes, uint32_t(rec.ntok) * uint32_t(row_bytes));
             bulk_commit();
             bulk_wait_read<0>();
             mbar_arrive(&empty[s]);
@@ -286,6 +312,12 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
     float2 aE[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     float2 aO[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     int acc_t = -1;
+    // this warp's share of the rows of a full token block (steps m_lo .. m_hi - 1 of PER_STEP
+    // rows), and the (token, head) of its first row
+    const int full_steps = (a.tokens_per_unit * N + PER_STEP - 1) / PER_STEP;
+    const int full_m_lo = cw * full_steps / kBwdNW, full_m_hi = (cw + 1) * full_steps / kBwdNW;
+    const int full_base_tok = full_m_lo * PER_STEP / N;
+    const int full_base_head = full_m_lo * PER_STEP - full_base_tok * N;
     // sums over the lane groups of the warp, added to the warp's shared row, then cleared
     auto flush_dw = [&]() {
 #pragma unroll
@@ -317,33 +349,39 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
     BwdRing ring;
     for (int64_t k = 0; k < n; ++k, ring.next(K)) {
         const int s = ring.s;
-        const BwdUnit t = bwd_decode(a, first + k * step);
+        if (!__all_sync(0xffffffffu, bwd_wait(&full[s], ring.phase))) {
+            if (lane == 0) atomicOr(&g_fused_bwd_status, kStatusWaitTimeout);
+            break;
+        }
+        const BwdRecord rec = records[s];
+        const int tt = rec.t_q & 1, ntok = rec.ntok;
         float2 wE[2], wO[2];  // this lane's weights of the unit's tensor (even / odd elements)
         {
-            const float4* wp = reinterpret_cast<const float4*>(wsm + t.t * D + sub * 8);
+            const float4* wp = reinterpret_cast<const float4*>(wsm + tt * D + sub * 8);
             const float4 a0 = wp[0], a1 = wp[1];
             wE[0] = make_float2(a0.x, a0.z);
             wO[0] = make_float2(a0.y, a0.w);
             wE[1] = make_float2(a1.x, a1.z);
             wO[1] = make_float2(a1.y, a1.w);
         }
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], ring.phase))) {
-            if (lane == 0) atomicOr(&g_fused_bwd_status, kStatusWaitTimeout);
-            break;
-        }
         uint8_t* xs = smem + L.stages + size_t(s) * a.stage_bytes;
         const uint8_t* gs = xs + grad_at;
         const float4* table = reinterpret_cast<const float4*>(smem + L.tables + s * L.table_bytes);
-        if (t.t != acc_t) {  // the sums so far belong to the other tensor
+        if (tt != acc_t) {  // the sums so far belong to the other tensor
             flush_dw();
-            acc_t = t.t;
+            acc_t = tt;
         }
-        const int rows = t.ntok * N;
-        const int steps = (rows + PER_STEP - 1) / PER_STEP;
-        const int m_lo = cw * steps / kBwdNW, m_hi = (cw + 1) * steps / kBwdNW;
+        const int rows = ntok * N;
+        int m_lo = full_m_lo, m_hi = full_m_hi;
+        int base_tok = full_base_tok, base_head = full_base_head;
+        if (ntok != a.tokens_per_unit) {  // a short block: this warp's share of its rows
+            const int steps = (rows + PER_STEP - 1) / PER_STEP;
+            m_lo = cw * steps / kBwdNW;
+            m_hi = (cw + 1) * steps / kBwdNW;
+            base_tok = m_lo * PER_STEP / N;
+            base_head = m_lo * PER_STEP - base_tok * N;
+        }
         int base = m_lo * PER_STEP;  // first row of the current step and its (token, head)
-        int base_tok = base / N;
-        int base_head = base - base_tok * N;
         for (int m = m_lo; m < m_hi; ++m) {
             // The sums (mean square, <u * w, x>) need the whole row: u = R^T gy (8 fp32 values)
             // and the raw bf16 words of x are kept across the reduction, then dx and the dw

@@ -99,6 +99,35 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return true;
 }
 
+// The same with a suspend-time hint: a waiting thread may be parked by the hardware for up to
+// HINT_NS nanoseconds (woken early when the phase completes) instead of polling, which leaves
+// issue slots to the warps doing the work.
+template <uint32_t HINT_NS>
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "n"(HINT_NS)
+        : "memory");
+    return done != 0;
+}
+
+template <uint32_t HINT_NS>
+__device__ __forceinline__ bool mbar_wait_bounded_hint(uint64_t* bar, uint32_t parity,
+                                                       uint64_t limit_ns = kWaitLimitNs)
+{
+    if (mbar_try_wait_hint<HINT_NS>(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait_hint<HINT_NS>(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+}
+
 // Bulk copy global -> shared; completion is signalled as transaction bytes on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes,
