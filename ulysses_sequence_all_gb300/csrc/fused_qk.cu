@@ -8,11 +8,11 @@
 // Structure: a persistent grid of several CTAs per SM, each with a ring of K shared-memory
 // stages. A work unit is a few consecutive tokens of one source rank: all N heads of q and of k,
 // two contiguous spans of the sequence-side tensors. Warp roles per CTA:
-//  * loader: one lane waits for the stage to be free ("empty" mbarrier), then starts the two
-//    cp.async.bulk loads, completing on the stage's "full" mbarrier as transaction bytes;
-//  * table: once the consumers of the stage's previous unit are done ("computed"), the lanes
-//    fill the stage's cos/sin table for the unit's positions and arrive on "full", so a consumer
-//    that sees the phase complete sees both the table and the data;
+//  * loader: lane 0 waits for the stage to be free ("empty" mbarrier), starts the cp.async.bulk
+//    loads (completing on the stage's "full" mbarrier as transaction bytes) and leaves a record
+//    of the unit beside the stage; while the copies fly, all lanes fill the stage's cos/sin
+//    table for the unit's positions and arrive on "full", so a consumer that sees the phase
+//    complete sees data, table and record (each unit is decoded once, by the loader);
 //  * storer: when the consumers report a unit done ("computed"), the lanes issue one
 //    cp.async.bulk store per (token, q|k, destination rank): n_r heads that are contiguous in the
 //    stage and in the destination; as soon as those stores have read shared memory (kFusedDrain
@@ -69,17 +69,40 @@ constexpr int kFusedDrain = ULY_FUSED_DRAIN;  // store groups left draining when
 constexpr int kSmemPerSm = 228 * 1024;
 constexpr int kSmemReservedPerCta = 1024;
 constexpr int kSmemPerCtaMax = 227 * 1024;
-constexpr int kFusedHeader = 256;  // three barriers per stage
-static_assert(3 * 8 * kFusedMaxStages <= kFusedHeader, "stage barriers must fit the header");
+constexpr int kFusedHeader = 256;  // three barriers per stage, then one unit record per stage
+constexpr int kFusedRecordsAt = 128;
+static_assert(3 * 8 * kFusedMaxStages <= kFusedRecordsAt, "stage barriers must fit the header");
+static_assert(kFusedRecordsAt + 16 * kFusedMaxStages <= kFusedHeader, "unit records must fit");
 static_assert(kFusedDrain >= 0 && kFusedDrain < kFusedMaxStages, "need a load in flight");
 static_assert(ULY_FUSED_CONSUMER_WARPS % 2 == 0, "consumer warps split evenly between q and k");
 // warp roles
-constexpr int kLoaderWarp = 0, kTableWarp = 1, kStorerWarp = 2, kFirstConsumerWarp = 3;
+constexpr int kLoaderWarp = 0, kStorerWarp = 1, kFirstConsumerWarp = 2;
 constexpr int kFusedThreads = 32 * (kFirstConsumerWarp + ULY_FUSED_CONSUMER_WARPS);
 #ifndef ULY_FUSED_ILP
-#define ULY_FUSED_ILP 2
+#define ULY_FUSED_ILP 3
 #endif
 constexpr int kIlp = ULY_FUSED_ILP;  // head rows in flight per lane group
+
+// What the storer and the consumers need of a unit, written by the loader beside the stage
+// before its last arrive on "full" (the loader decodes each unit once).
+struct FusedRecord {
+    int64_t head_row0;  // first row of the unit on the head side: bb * S + seq_off(q) + i0
+    int32_t ntok;
+    int32_t pad;
+};
+
+#ifndef ULY_FUSED_WAIT_HINT_NS  // suspend-time hint of the barrier waits (0: plain polling)
+#define ULY_FUSED_WAIT_HINT_NS 10000
+#endif
+
+__device__ __forceinline__ bool fused_wait(uint64_t* bar, uint32_t parity)
+{
+#if ULY_FUSED_WAIT_HINT_NS > 0
+    return mbar_wait_bounded_hint<ULY_FUSED_WAIT_HINT_NS>(bar, parity);
+#else
+    return mbar_wait_bounded(bar, parity);
+#endif
+}
 
 struct FusedUnit {
     int q;
@@ -184,12 +207,13 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     uint64_t* computed = full + kFusedMaxStages;           // consumers done with the stage
     uint64_t* empty = computed + kFusedMaxStages;          // stores have read the stage
     float2* turns = reinterpret_cast<float2*>(smem + L.turns);
+    FusedRecord* records = reinterpret_cast<FusedRecord*>(smem + kFusedRecordsAt);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t first = blockIdx.x, step = gridDim.x;
     const int64_t n = first < a.total_units ? (a.total_units - 1 - first) / step + 1 : 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < K; ++s) {
-            mbar_init(&full[s], 1 + 32);  // loader lane + the table warp's lanes
+            mbar_init(&full[s], 1 + 32);  // the loader's expect_tx, then its lanes' table writes
             mbar_init(&computed[s], NW);
             mbar_init(&empty[s], 1);
         }
@@ -207,61 +231,61 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     const int tok_stride = qkv ? 3 * row_bytes : row_bytes;
     auto plane_stride = [&](int ntok) { return qkv ? row_bytes : ntok * row_bytes; };
 
-    if (warp == kLoaderWarp) {  // one lane streams units into the stages
-        if (lane != 0) return;
+    if (warp == kLoaderWarp) {
+        // Lane 0 streams units into the stages and leaves each unit's record beside its stage;
+        // while the copies fly, the lanes fill the stage's cos/sin table for the unit's positions
+        // (free: the stage's previous unit has been stored, so its consumers are done) and
+        // arrive on "full", so a consumer that sees the phase complete sees data, table and
+        // record.
         int64_t j = 0;
         FusedRing ring;
         for (; j < n; ++j, ring.next(K)) {
             const int s = ring.s;
-            if (j >= K && !mbar_wait_bounded(&empty[s], ring.phase ^ 1u)) {
-                atomicOr(&g_fused_status, kStatusWaitTimeout);
-                break;
-            }
-            const FusedUnit t = fused_decode(a, first + j * step);
-            const uint32_t bytes = uint32_t(t.ntok) * uint32_t(row_bytes);  // one plane
-            const int64_t tok0 = t.bb * a.s[t.q] + t.i0;                      // first source row
-            uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
-            mbar_arrive_expect_tx(&full[s], uint32_t(planes) * bytes);
-            if (qkv) {
-                bulk_g2s(dst, a.qkv_in[t.q] + tok0 * 3 * row_bytes, 3 * bytes, &full[s]);
-            } else {
-                bulk_g2s(dst, a.q_in[t.q] + tok0 * row_bytes, bytes, &full[s]);
-                bulk_g2s(dst + bytes, a.k_in[t.q] + tok0 * row_bytes, bytes, &full[s]);
-            }
-        }
-        // do not leave while copies into this CTA's shared memory may be in flight
-        for (int64_t jj = (j > K ? j - K : 0); jj < j; ++jj) {
-            if (!mbar_wait_bounded(&full[jj % K], uint32_t((jj / K) & 1))) {
-                atomicOr(&g_fused_status, kStatusDrainTimeout);
-                break;
-            }
-        }
-        return;
-    }
-
-    if (warp == kTableWarp) {  // cos/sin of each unit's positions, once the stage's table is free
-        FusedRing ring;
-        for (int64_t j = 0; j < n; ++j, ring.next(K)) {
-            const int s = ring.s;
-            if (j >= K && !__all_sync(0xffffffffu, mbar_wait_bounded(&computed[s], ring.phase ^ 1u))) {
+            int ok = 1;
+            if (lane == 0 && j >= K) ok = fused_wait(&empty[s], ring.phase ^ 1u);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
                 if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
                 break;
             }
             const FusedUnit t = fused_decode(a, first + j * step);
+            if (lane == 0) {
+                const uint32_t bytes = uint32_t(t.ntok) * uint32_t(row_bytes);  // one plane
+                const int64_t tok0 = t.bb * a.s[t.q] + t.i0;                      // first source row
+                uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
+                mbar_arrive_expect_tx(&full[s], uint32_t(planes) * bytes);
+                if (qkv) {
+                    bulk_g2s(dst, a.qkv_in[t.q] + tok0 * 3 * row_bytes, 3 * bytes, &full[s]);
+                } else {
+                    bulk_g2s(dst, a.q_in[t.q] + tok0 * row_bytes, bytes, &full[s]);
+                    bulk_g2s(dst + bytes, a.k_in[t.q] + tok0 * row_bytes, bytes, &full[s]);
+                }
+                FusedRecord& rec = records[s];  // published by this lane's arrive below
+                rec.head_row0 = t.bb * a.S + a.seq_off[t.q] + t.i0;
+                rec.ntok = t.ntok;
+            }
             float* table = reinterpret_cast<float*>(smem + L.tables + s * L.table_bytes);
             const float p0 = float(a.seq_off[t.q] + t.i0);
             // Per token, lane i of a row group owns pairs 4i .. 4i+3, read as two 16-byte
             // entries (c_j, c_j+1, s_j, s_j+1) for j = 4i and j = 4i+2; the entries of all lanes
             // for j = 4i come first, then those for j = 4i+2, so each read is contiguous.
             for (int e = lane; e < t.ntok * HALF; e += 32) {
-                const int tok = e / HALF, j = e % HALF;
-                const float2 tj = turns[j];
+                const int tok = e / HALF, jj = e % HALF;
+                const float2 tj = turns[jj];
                 const float2 cs = rope_cos_sin(p0 + float(tok), tj.x, tj.y);
-                const int at = ((tok * 2 + ((j >> 1) & 1)) * G + (j >> 2)) * 4 + (j & 1);
+                const int at = ((tok * 2 + ((jj >> 1) & 1)) * G + (jj >> 2)) * 4 + (jj & 1);
                 table[at] = cs.x;
                 table[at + 2] = cs.y;
             }
-            mbar_arrive(&full[s]);  // release: this lane's table entries
+            mbar_arrive(&full[s]);
+        }
+        // do not leave while copies into this CTA's shared memory may be in flight
+        if (lane == 0) {
+            for (int64_t jj = (j > K ? j - K : 0); jj < j; ++jj) {
+                if (!mbar_wait_bounded(&full[jj % K], uint32_t((jj / K) & 1))) {
+                    atomicOr(&g_fused_status, kStatusDrainTimeout);
+                    break;
+                }
+            }
         }
         return;
     }
@@ -275,16 +299,16 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
         FusedRing ring;
         for (; j < n; ++j, ring.next(K)) {
             const int s = ring.s;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&computed[s], ring.phase))) {
+            if (!__all_sync(0xffffffffu, fused_wait(&computed[s], ring.phase))) {
                 if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
                 break;
             }
-            const FusedUnit t = fused_decode(a, first + j * step);
+            const FusedRecord rec = records[s];
             const uint8_t* st = smem + L.stages + size_t(s) * a.stage_bytes;
-            const int64_t row0 = t.bb * a.S + a.seq_off[t.q] + t.i0;
+            const int64_t row0 = rec.head_row0;
             const int W = a.W;
-            const int pstride = plane_stride(t.ntok);
-            const int runs = t.ntok * planes * W;
+            const int pstride = plane_stride(rec.ntok);
+            const int runs = rec.ntok * planes * W;
             for (int idx = lane; idx < runs; idx += 32) {
                 const int rest = idx / W, r = idx - rest * W;
                 const int tok = rest / planes, plane = rest - tok * planes;
@@ -323,23 +347,34 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
         for (int h = 0; h < 2; ++h) wOn[h] = make_float2(-wO[h].x, -wO[h].y);
     }
     const float inv_d = 1.0f / float(D);
+    // this warp's share of the rows of a full token block (steps m_lo .. m_hi - 1 of PER_STEP
+    // rows) and the (token, head) of its first row
+    const int full_steps = (a.tokens_per_unit * N + PER_STEP - 1) / PER_STEP;
+    const int full_m_lo = cwi * full_steps / HALF_NW, full_m_hi = (cwi + 1) * full_steps / HALF_NW;
+    const int full_base_tok = full_m_lo * PER_STEP / N;
+    const int full_base_head = full_m_lo * PER_STEP - full_base_tok * N;
     FusedRing ring;
     for (int64_t k = 0; k < n; ++k, ring.next(K)) {
         const int s = ring.s;
-        const FusedUnit t = fused_decode(a, first + k * step);
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], ring.phase))) {
+        if (!__all_sync(0xffffffffu, fused_wait(&full[s], ring.phase))) {
             if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
             break;
         }
+        const int ntok = records[s].ntok;
         // this tensor's plane in the stage; row (token, head) at token * tok_stride + head * 2d
-        uint8_t* rows_base = smem + L.stages + size_t(s) * a.stage_bytes + which * plane_stride(t.ntok);
+        uint8_t* rows_base = smem + L.stages + size_t(s) * a.stage_bytes + which * plane_stride(ntok);
         const float4* table = reinterpret_cast<const float4*>(smem + L.tables + s * L.table_bytes);
-        const int rows = t.ntok * N;
-        const int steps = (rows + PER_STEP - 1) / PER_STEP;
-        const int m_lo = cwi * steps / HALF_NW, m_hi = (cwi + 1) * steps / HALF_NW;
+        const int rows = ntok * N;
+        int m_lo = full_m_lo, m_hi = full_m_hi;
+        int base_tok = full_base_tok, base_head = full_base_head;
+        if (ntok != a.tokens_per_unit) {  // a short block: this warp's share of its rows
+            const int steps = (rows + PER_STEP - 1) / PER_STEP;
+            m_lo = cwi * steps / HALF_NW;
+            m_hi = (cwi + 1) * steps / HALF_NW;
+            base_tok = m_lo * PER_STEP / N;
+            base_head = m_lo * PER_STEP - base_tok * N;
+        }
         int base = m_lo * PER_STEP;   // first row of the current step and its (token, head)
-        int base_tok = base / N;
-        int base_head = base - base_tok * N;
         for (int m = m_lo; m < m_hi; ++m) {
             uint8_t* slot[kIlp];
             int tok[kIlp];
