@@ -379,6 +379,25 @@ def run_ours(args):
             qkv_ms.append(e0.elapsed_time(e1))
     del qkv
 
+    # outside the step: the backward of the fused call (dq, dk and dw from the gradients of q_out
+    # and k_out; the step's own outputs serve as those gradients)
+    dq = [torch.empty_like(t) for t in wk.q]
+    dk = [torch.empty_like(t) for t in wk.k]
+    dw = torch.empty((2, wk.cfg.d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(B.ulysses_qk_fused_backward_workspace(wk.plan), dtype=torch.uint8,
+                     device="cuda")
+    bwd_ms = []
+    for rep in range(min(args.steps, 20) + 3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        B.ulysses_a2a_4d_qk_fused_backward(wk.plan, dq, dk, wk.q, wk.k, wk.qo, wk.ko, wk.w, dw,
+                                           EPS, THETA, ws, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if rep >= 3:
+            bwd_ms.append(e0.elapsed_time(e1))
+    del dq, dk, dw, ws
+
     clocks = ClockSampler(local)
     clocks.start()
     if pg:
@@ -442,6 +461,13 @@ def run_ours(args):
             "median_ms": round(statistics.median(qkv_ms), 4),
             "GB/s": round(6 * wk.side / (statistics.median(qkv_ms) * 1e-3) / 1e9, 1),
             "frac_of_peak": round(6 * wk.side / (statistics.median(qkv_ms) * 1e-3) / 1e9 / peak, 4)},
+        "qk_fused_backward": {
+            "note": "outside the step: dq, dk (bf16) and dw (fp32) of the fused call, the RMSNorm + "
+                    "RoPE VJP inside the mode-1 gather (2 launches: kernel + dw reduction); reads "
+                    "q, k and the two output gradients, writes dq and dk",
+            "median_ms": round(statistics.median(bwd_ms), 4),
+            "GB/s": round(6 * wk.side / (statistics.median(bwd_ms) * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(6 * wk.side / (statistics.median(bwd_ms) * 1e-3) / 1e9 / peak, 4)},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
