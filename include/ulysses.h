@@ -36,6 +36,7 @@
 #ifndef ULYSSES_H
 #define ULYSSES_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
