@@ -52,7 +52,8 @@ enum {
     ULY_ECHUNK = -4,   /* the chunk cap is smaller than one sequence row on some rank */
     ULY_ECUDA = -5,    /* a CUDA runtime call failed; ulysses_last_cuda_error() has the code */
     ULY_ENOMEM = -6,   /* host memory for a plan could not be allocated */
-    ULY_EDEVICE = -7   /* a kernel recorded a wait timeout in the device status word */
+    ULY_EDEVICE = -7,  /* a kernel recorded a wait timeout in the device status word */
+    ULY_ESCRATCH = -8  /* the call needs more scratch than the library's static array holds */
 };
 
 /* Element types (fast-ulysses 0.2.1, README, "Limits": float16 / bfloat16 / float32 /
@@ -182,6 +183,40 @@ int ulysses_a2a_4d_qk_fused_backward(ulysses_plan_t plan, void* const* dq_out, v
  * 2 * d fp32 slot per CTA it launches: at most a few MB). ULY_EINVAL if the plan does not meet
  * the fused call's requirements. */
 int ulysses_qk_fused_backward_workspace(ulysses_plan_t plan, size_t* bytes);
+
+/* Size of the scratch array compiled into the library for
+ * ulysses_a2a_4d_qk_fused_backward_static: 2 MiB, which holds the dw partial sums of 1,024 CTAs
+ * at d = 256 (a GB300 launches at most 608). */
+#define ULYSSES_STATIC_SCRATCH_BYTES (2u * 1024u * 1024u)
+
+/*
+ * ulysses_a2a_4d_qk_fused_backward without a workspace argument: the same kernels, arguments,
+ * results and errors, with the dw partial sums kept in a fixed scratch array inside the library
+ * (a file-scope __device__ array of ULYSSES_STATIC_SCRATCH_BYTES). The pages describe no
+ * counterpart: it exists for callers that cannot allocate device memory around the call, such as
+ * a C caller with no allocator of its own, or code whose device memory is all held by another
+ * allocator (a framework's caching pool) or that must not enter an allocator between launches,
+ * where cudaMalloc and cudaFree may synchronise the device. The call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library call.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, checked) and keeps it; the CUDA runtime may load the library's device
+ *   code, array included, at that point (the array is part of the loaded module, not a per-call
+ *   allocation). As with the library's other first-call set-up (device attributes, kernel
+ *   attributes), make that first call before any stream capture.
+ *   Contents: nothing in the array needs to start at zero; every slot the reduction reads is
+ *   written in full by the same call's kernel first.
+ *   Concurrency: the array is one per device and per process. Calls queued on one stream are
+ *   ordered and safe; two calls that may run at the same time on one device (different streams,
+ *   or different host threads without ordering) race on it and give wrong dw. Use
+ *   ulysses_a2a_4d_qk_fused_backward with separate workspaces for those.
+ *   ULY_ESCRATCH when ulysses_qk_fused_backward_workspace for `plan` exceeds
+ *   ULYSSES_STATIC_SCRATCH_BYTES (nothing is queued then).
+ */
+int ulysses_a2a_4d_qk_fused_backward_static(ulysses_plan_t plan, void* const* dq_out,
+                                            void* const* dk_out, const void* const* q_in,
+                                            const void* const* k_in, const void* const* dq_in,
+                                            const void* const* dk_in, const float* rms_w,
+                                            float* dw, float eps, float rope_theta, void* stream);
 
 /*
  * The fused call on interleaved packed QKV, the layout a fused QKV projection writes (FastVideo,

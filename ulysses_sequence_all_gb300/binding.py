@@ -15,6 +15,8 @@ LIBRARY = os.environ.get("ULYSSES_LIBRARY", os.path.join(PKG, "libulysses.so"))
 
 ULY_OK, ULY_EINVAL, ULY_EALIGN, ULY_EOVERLAP, ULY_ECHUNK, ULY_ECUDA, ULY_ENOMEM, ULY_EDEVICE = (
     0, -1, -2, -3, -4, -5, -6, -7)
+ULY_ESCRATCH = -8
+ULYSSES_STATIC_SCRATCH_BYTES = 2 * 1024 * 1024
 ULY_U8, ULY_F8E4M3, ULY_F8E5M2, ULY_I8, ULY_F16, ULY_BF16, ULY_F32 = 1, 2, 3, 4, 5, 6, 7
 ULY_ENGINE_AUTO, ULY_ENGINE_TMA, ULY_ENGINE_VEC = 0, 1, 2
 
@@ -26,7 +28,7 @@ EXPORTS = ["ulysses_plan", "ulysses_plan_destroy", "ulysses_plan_set_chunk_bytes
            "ulysses_plan_bytes", "ulysses_plan_num_chunks", "ulysses_plan_chunk_rows",
            "ulysses_a2a_4d", "ulysses_a2a_4d_engine", "ulysses_a2a_4d_qk_fused",
            "ulysses_a2a_4d_qkv_fused", "ulysses_a2a_4d_qk_fused_backward",
-           "ulysses_qk_fused_backward_workspace",
+           "ulysses_qk_fused_backward_workspace", "ulysses_a2a_4d_qk_fused_backward_static",
            "ulysses_a2a_4d_host", "ulysses_a2a_4d_qk_fused_host", "ulysses_device_status",
            "ulysses_selftest_wait_timeout", "ulysses_last_cuda_error", "ulysses_strerror",
            "ulysses_version"]
@@ -73,6 +75,9 @@ def _lib():
                                                          ctypes.c_float, ctypes.c_float, _p,
                                                          ctypes.c_size_t, _p]
         lib.ulysses_qk_fused_backward_workspace.argtypes = [_p, ctypes.POINTER(ctypes.c_size_t)]
+        lib.ulysses_a2a_4d_qk_fused_backward_static.argtypes = [_p, _pp, _pp, _pp, _pp, _pp, _pp,
+                                                                _p, _p, ctypes.c_float,
+                                                                ctypes.c_float, _p]
         lib.ulysses_a2a_4d_host.argtypes = [_p, ctypes.c_int, _pp, _pp, _pp, _pp, _p]
         lib.ulysses_a2a_4d_qk_fused_host.argtypes = [_p, _pp, _pp, _pp, _pp, _pp, _pp, _pp, _pp, _p,
                                                      ctypes.c_float, ctypes.c_float, _p]
@@ -217,6 +222,17 @@ def ulysses_a2a_4d_qk_fused_backward(plan: Plan, dq_out, dk_out, q_in, k_in, dq_
         plan, _ptrs(dq_out), _ptrs(dk_out), _ptrs(q_in), _ptrs(k_in), _ptrs(dq_in), _ptrs(dk_in),
         _addr(rms_w), _addr(dw), eps, rope_theta, _addr(workspace), _nbytes(workspace),
         _stream(stream)), "ulysses_a2a_4d_qk_fused_backward")
+
+
+def ulysses_a2a_4d_qk_fused_backward_static(plan: Plan, dq_out, dk_out, q_in, k_in, dq_in, dk_in,
+                                            rms_w, dw, eps: float, rope_theta: float, stream=None):
+    """Backward of the fused call with the dw partial sums in the library's static scratch array
+    (no workspace argument; the call allocates nothing). Calls that may run at the same time on
+    one device race on that array."""
+    _check(_lib().ulysses_a2a_4d_qk_fused_backward_static(
+        plan, _ptrs(dq_out), _ptrs(dk_out), _ptrs(q_in), _ptrs(k_in), _ptrs(dq_in), _ptrs(dk_in),
+        _addr(rms_w), _addr(dw), eps, rope_theta, _stream(stream)),
+        "ulysses_a2a_4d_qk_fused_backward_static")
 
 
 def ulysses_a2a_4d_host(plan: Plan, mode: int, host_in, host_out, dev_in, dev_out, stream=None):

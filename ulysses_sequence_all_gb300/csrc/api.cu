@@ -392,6 +392,29 @@ int fused_bwd_device(const Plan& p, void* const* dq_out, void* const* dk_out,
     return ULY_OK;
 }
 
+// ---- backward with library-owned scratch ----------------------------------------------------------
+// The dw partial sums of ulysses_a2a_4d_qk_fused_backward_static live in this array; its device
+// address is looked up once per device and kept. No part of it needs initial contents: each
+// launch's CTAs write their slots in full before the reduction reads them.
+static __device__ __align__(256) float g_static_scratch[ULYSSES_STATIC_SCRATCH_BYTES / sizeof(float)];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64];
+
+int static_scratch(int device, void** out)
+{
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[device]) {
+        void* addr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&addr, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (!addr || !aligned16(addr)) return ULY_EALIGN;
+        g_scratch_addr[device] = addr;
+    }
+    *out = g_scratch_addr[device];
+    return ULY_OK;
+}
+
 // ---- host-buffer entry points: chunked copy-in / kernel / copy-out pipeline ---------------------
 // Host<->device copies run on the copy engines in both directions at once, so the call is cut
 // into sequence chunks: chunk c's inputs are copied in and relaid out on the caller's stream, then
@@ -598,6 +621,30 @@ int ulysses_a2a_4d_qk_fused_backward(ulysses_plan_t plan, void* const* dq_out, v
                             rope_theta, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
+int ulysses_a2a_4d_qk_fused_backward_static(ulysses_plan_t plan, void* const* dq_out,
+                                            void* const* dk_out, const void* const* q_in,
+                                            const void* const* k_in, const void* const* dq_in,
+                                            const void* const* dk_in, const float* rms_w,
+                                            float* dw, float eps, float rope_theta, void* stream)
+{
+    if (!plan) return ULY_EINVAL;
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    int64_t T = 0;
+    int stages = 0, ctas_per_sm = 1;
+    uint32_t stage_bytes = 0;
+    size_t need = 0;
+    if ((rc = fused_bwd_setup(plan->p, dev, &T, &stages, &stage_bytes, &ctas_per_sm, &need)))
+        return rc;
+    if (need > ULYSSES_STATIC_SCRATCH_BYTES) return ULY_ESCRATCH;
+    void* scratch = nullptr;
+    if ((rc = static_scratch(dev.device, &scratch))) return rc;
+    return fused_bwd_device(plan->p, dq_out, dk_out, q_in, k_in, dq_in, dk_in, rms_w, dw, eps,
+                            rope_theta, scratch, ULYSSES_STATIC_SCRATCH_BYTES,
+                            static_cast<cudaStream_t>(stream));
+}
+
 int ulysses_a2a_4d_qkv_fused(ulysses_plan_t plan, const void* const* qkv_in, void* const* q_out,
                              void* const* k_out, void* const* v_out, const float* rms_w, float eps,
                              float rope_theta, void* stream)
@@ -743,6 +790,7 @@ const char* ulysses_strerror(int status)
         case ULY_ECUDA: return "CUDA runtime error (see ulysses_last_cuda_error)";
         case ULY_ENOMEM: return "out of host memory";
         case ULY_EDEVICE: return "a kernel wait timed out (device status word set)";
+        case ULY_ESCRATCH: return "needs more scratch than the library's static array holds";
         default: return "unknown status";
     }
 }
