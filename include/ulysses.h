@@ -69,8 +69,12 @@ enum {
     ULY_F32 = 7
 };
 
-/* Relayout engines: ULY_ENGINE_AUTO picks the fastest measured one. */
-enum { ULY_ENGINE_AUTO = 0, ULY_ENGINE_TMA = 1, ULY_ENGINE_VEC = 2 };
+/* Relayout engines: ULY_ENGINE_AUTO picks the fastest measured one (the TMA kernel).
+ * ULY_ENGINE_CE issues one pitched cudaMemcpy2DAsync per (source shard, destination rank, batch
+ * index) on the copy engines, no kernel: the pages' own transport design (fast-ulysses 0.1.0,
+ * opening paragraph: pitched 2D/3D copies on the copy engines) run between buffers of one GPU,
+ * kept for comparison and for overlapping with SM-bound work. */
+enum { ULY_ENGINE_AUTO = 0, ULY_ENGINE_TMA = 1, ULY_ENGINE_VEC = 2, ULY_ENGINE_CE = 3 };
 
 typedef struct ulysses_plan_s* ulysses_plan_t;
 
@@ -103,6 +107,16 @@ int ulysses_plan_destroy(ulysses_plan_t plan);
  */
 int ulysses_plan_set_chunk_bytes(ulysses_plan_t plan, int64_t max_chunk_bytes);
 
+/*
+ * Cap on the CTAs (thread blocks) of every kernel launched with this plan; 0 (the default)
+ * means no cap: the kernels' persistent grids cover every SM. A cap leaves the remaining SMs
+ * free for work on other streams (a GEMM, attention) at the cost of this call's bandwidth; it
+ * changes no result. The pages have no such setting (their transfer runs on copy engines, which
+ * use no SMs); it exists for overlapping the relayout with compute on one GPU.
+ * max_ctas >= 0. Like the chunk cap, it must not race with launches using the plan.
+ */
+int ulysses_plan_set_max_ctas(ulysses_plan_t plan, int64_t max_ctas);
+
 /* Bytes of rank `rank`'s input and output tensors for `mode` (either pointer may be NULL). */
 int ulysses_plan_bytes(ulysses_plan_t plan, int mode, int rank, int64_t* in_bytes,
                        int64_t* out_bytes);
@@ -128,7 +142,9 @@ int ulysses_a2a_4d(ulysses_plan_t plan, int mode, const void* const* in_ptrs,
                    void* const* out_ptrs, void* stream);
 
 /* Same as ulysses_a2a_4d with an explicit engine (ULY_ENGINE_*): TMA bulk copies through shared
- * memory, or 16-byte vector loads and stores. Both give identical bytes. */
+ * memory, 16-byte vector loads and stores, or copy-engine pitched copies. All give identical
+ * bytes. With ULY_ENGINE_CE the call queues W * W * b copies per chunk (fewer when a split is
+ * zero) and no kernel. */
 int ulysses_a2a_4d_engine(ulysses_plan_t plan, int mode, int engine, const void* const* in_ptrs,
                           void* const* out_ptrs, void* stream);
 

@@ -155,6 +155,15 @@ def test_launch_argument_errors_before_cuda():
     assert ei.value.status == B.ULY_EINVAL
 
 
+def test_max_ctas_setter():
+    plan = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "bfloat16")
+    B.ulysses_plan_set_max_ctas(plan, 0)
+    B.ulysses_plan_set_max_ctas(plan, 17)
+    with pytest.raises(B.UlyssesError) as ei:
+        B.ulysses_plan_set_max_ctas(plan, -1)
+    assert ei.value.status == B.ULY_EINVAL
+
+
 def test_fused_argument_errors_before_cuda():
     plan16 = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "float16")
     plan = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "bfloat16")

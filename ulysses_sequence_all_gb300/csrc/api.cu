@@ -15,20 +15,21 @@
 namespace uly {
 int64_t relayout_unit_bytes(int engine);
 cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStream_t stream,
-                            int device, int sm_count);
+                            int device, int sm_count, int64_t max_grid);
 cudaError_t relayout_status(unsigned* status, bool clear);
 int64_t relayout_tile_rows(int64_t row_bytes);
 cudaError_t relayout_rows_launch(const RowTileArgs& a, int mode, cudaStream_t stream, int device,
-                                 int sm_count);
+                                 int sm_count, int64_t max_grid);
 void fused_geometry(const Plan& p, int planes, int64_t* tokens_per_unit, int* stages,
                     uint32_t* stage_bytes, int* ctas_per_sm);
-cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count);
+cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count,
+                         int64_t max_grid);
 cudaError_t fused_status(unsigned* status, bool clear);
 void fused_bwd_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages,
                         uint32_t* stage_bytes, int* ctas_per_sm);
-int64_t fused_bwd_grid(const FusedBwdArgs& a, int sm_count);
+int64_t fused_bwd_grid(const FusedBwdArgs& a, int sm_count, int64_t max_grid);
 cudaError_t fused_bwd_launch(const FusedBwdArgs& a, float* dw, bool accumulate, cudaStream_t stream,
-                             int device, int sm_count);
+                             int device, int sm_count, int64_t max_grid);
 cudaError_t fused_bwd_status(unsigned* status, bool clear);
 cudaError_t selftest_timeout_launch(uint64_t limit_ns, cudaStream_t stream);
 }  // namespace uly
@@ -116,7 +117,8 @@ int relayout_check(const Plan& p, int mode, int engine, const void* const* in_pt
                    void* const* out_ptrs)
 {
     if (mode != 0 && mode != 1) return ULY_EINVAL;
-    if (engine != ULY_ENGINE_AUTO && engine != ULY_ENGINE_TMA && engine != ULY_ENGINE_VEC)
+    if (engine != ULY_ENGINE_AUTO && engine != ULY_ENGINE_TMA && engine != ULY_ENGINE_VEC &&
+        engine != ULY_ENGINE_CE)
         return ULY_EINVAL;
     int64_t in_b[kMaxW], out_b[kMaxW];
     side_bytes(p, mode, in_b, out_b);
@@ -127,12 +129,47 @@ int relayout_check(const Plan& p, int mode, int engine, const void* const* in_pt
     return check_overlap(in_ptrs, in_b, p.W, const_cast<const void* const*>(out_ptrs), out_b, p.W);
 }
 
+// The copy-engine form of one chunk: per (source shard q, destination rank r, batch index) one
+// pitched 2D copy of the chunk's rows of shard q: n_r * d * e bytes wide, the row pitch N * d * e
+// on the sequence side and n_r * d * e on the head side (the pages' design, pitched copies on the
+// copy engines, here between buffers of one GPU).
+int relayout_rows_ce(const Plan& p, int mode, const void* const* in_ptrs, void* const* out_ptrs,
+                     const ChunkRows& rows, cudaStream_t stream)
+{
+    const int64_t elem_row = p.d * p.e;  // bytes of one head row
+    for (int q = 0; q < p.W; ++q) {
+        const int64_t cnt = rows.cnt[q];
+        if (cnt == 0) continue;
+        for (int r = 0; r < p.W; ++r) {
+            const int64_t width = p.n[r] * elem_row;
+            if (width == 0) continue;
+            for (int64_t bb = 0; bb < p.b; ++bb) {
+                uint8_t* seq = static_cast<uint8_t*>(mode == 0 ? const_cast<void*>(in_ptrs[q])
+                                                               : out_ptrs[q]) +
+                               ((bb * p.s[q] + rows.lo[q]) * p.N + p.head_off[r]) * elem_row;
+                uint8_t* head = static_cast<uint8_t*>(mode == 0 ? out_ptrs[r]
+                                                                : const_cast<void*>(in_ptrs[r])) +
+                                (bb * p.S + p.seq_off[q] + rows.lo[q]) * width;
+                const size_t seq_pitch = size_t(p.N * elem_row), head_pitch = size_t(width);
+                cudaError_t e = mode == 0
+                    ? cudaMemcpy2DAsync(head, head_pitch, seq, seq_pitch, size_t(width), size_t(cnt),
+                                        cudaMemcpyDeviceToDevice, stream)
+                    : cudaMemcpy2DAsync(seq, seq_pitch, head, head_pitch, size_t(width), size_t(cnt),
+                                        cudaMemcpyDeviceToDevice, stream);
+                if (e != cudaSuccess) return cuda_fail(e);
+            }
+        }
+    }
+    return ULY_OK;
+}
+
 // One launch of the relayout over the given rows of every sequence shard.
 int relayout_rows(const Plan& p, int mode, int engine, const void* const* in_ptrs,
                   void* const* out_ptrs, const ChunkRows& rows, cudaStream_t stream,
                   const DeviceInfo& dev)
 {
     if (engine == ULY_ENGINE_AUTO) engine = ULY_ENGINE_TMA;
+    if (engine == ULY_ENGINE_CE) return relayout_rows_ce(p, mode, in_ptrs, out_ptrs, rows, stream);
     uint8_t* seq[kMaxW];
     uint8_t* head[kMaxW];
     for (int k = 0; k < p.W; ++k) {
@@ -152,7 +189,7 @@ int relayout_rows(const Plan& p, int mode, int engine, const void* const* in_ptr
             t.head_ptr[k] = head[k];
         }
         build_row_tiles(p, rows, tile_rows, &t);
-        e = relayout_rows_launch(t, mode, stream, dev.device, dev.sm_count);
+        e = relayout_rows_launch(t, mode, stream, dev.device, dev.sm_count, p.max_ctas);
     } else {
         RelayoutArgs a;
         std::memset(&a, 0, sizeof a);
@@ -161,7 +198,7 @@ int relayout_rows(const Plan& p, int mode, int engine, const void* const* in_ptr
             a.head_ptr[k] = head[k];
         }
         build_relayout_units(p, rows, relayout_unit_bytes(engine), &a);
-        e = relayout_launch(a, mode, engine, stream, dev.device, dev.sm_count);
+        e = relayout_launch(a, mode, engine, stream, dev.device, dev.sm_count, p.max_ctas);
     }
     return e == cudaSuccess ? ULY_OK : cuda_fail(e);
 }
@@ -271,7 +308,7 @@ int fused_rows(const Plan& p, FusedArgs* a, int64_t tokens_per_unit, const Chunk
                cudaStream_t stream, const DeviceInfo& dev)
 {
     build_fused_units(p, rows, tokens_per_unit, a);
-    cudaError_t e = fused_launch(*a, stream, dev.device, dev.sm_count);
+    cudaError_t e = fused_launch(*a, stream, dev.device, dev.sm_count, p.max_ctas);
     return e == cudaSuccess ? ULY_OK : cuda_fail(e);
 }
 
@@ -386,7 +423,7 @@ int fused_bwd_device(const Plan& p, void* const* dq_out, void* const* dk_out,
         ChunkRows rows;
         chunk_rows(p, C, c, &rows);
         build_fused_bwd_units(p, rows, T, &a);
-        cudaError_t e = fused_bwd_launch(a, dw, c > 0, stream, dev.device, dev.sm_count);
+        cudaError_t e = fused_bwd_launch(a, dw, c > 0, stream, dev.device, dev.sm_count, p.max_ctas);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return ULY_OK;
@@ -539,6 +576,13 @@ int ulysses_plan_set_chunk_bytes(ulysses_plan_t plan, int64_t max_chunk_bytes)
 {
     if (!plan || max_chunk_bytes < 1) return ULY_EINVAL;
     plan->p.chunk_cap = max_chunk_bytes;
+    return ULY_OK;
+}
+
+int ulysses_plan_set_max_ctas(ulysses_plan_t plan, int64_t max_ctas)
+{
+    if (!plan || max_ctas < 0) return ULY_EINVAL;
+    plan->p.max_ctas = max_ctas;
     return ULY_OK;
 }
 

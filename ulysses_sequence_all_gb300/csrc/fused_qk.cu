@@ -499,10 +499,12 @@ static cudaError_t launch_g(const FusedArgs& a, cudaStream_t stream, int device,
     return cudaGetLastError();
 }
 
-cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count)
+cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count,
+                         int64_t max_grid)
 {
     if (a.total_units == 0) return cudaSuccess;
     int64_t grid = int64_t(sm_count) * (a.ctas_per_sm > 0 ? a.ctas_per_sm : 1);
+    if (max_grid > 0 && grid > max_grid) grid = max_grid;
     if (grid > a.total_units) grid = a.total_units;
     switch (a.d / 8) {
         case 1: return launch_g<1>(a, stream, device, int(grid));

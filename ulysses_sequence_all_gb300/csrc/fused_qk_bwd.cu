@@ -557,19 +557,21 @@ static cudaError_t bwd_launch_g(const FusedBwdArgs& a, cudaStream_t stream, int 
     return cudaGetLastError();
 }
 
-// CTAs of the main kernel for a launch of `a` (the number of partial-sum slots it fills).
-int64_t fused_bwd_grid(const FusedBwdArgs& a, int sm_count)
+// CTAs of the main kernel for a launch of `a` (the number of partial-sum slots it fills); at
+// most max_grid when that is positive.
+int64_t fused_bwd_grid(const FusedBwdArgs& a, int sm_count, int64_t max_grid)
 {
     int64_t grid = int64_t(sm_count) * (a.ctas_per_sm > 0 ? a.ctas_per_sm : 1);
+    if (max_grid > 0 && grid > max_grid) grid = max_grid;
     return grid < a.total_units ? grid : a.total_units;
 }
 
 // One launch of the backward over `a` (its dw_part holds at least fused_bwd_grid slots), then
 // the reduction of its slots into dw (added to dw when `accumulate`, else written).
 cudaError_t fused_bwd_launch(const FusedBwdArgs& a, float* dw, bool accumulate, cudaStream_t stream,
-                             int device, int sm_count)
+                             int device, int sm_count, int64_t max_grid)
 {
-    const int64_t grid = fused_bwd_grid(a, sm_count);
+    const int64_t grid = fused_bwd_grid(a, sm_count, max_grid);
     if (grid > 0) {
         cudaError_t e;
         switch (a.d / 8) {

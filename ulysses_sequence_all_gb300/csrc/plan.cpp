@@ -63,6 +63,7 @@ int plan_init(Plan* p, int W, int64_t b, const int64_t* seq_splits, const int64_
         return ULY_EINVAL;
     if ((d * e) % 16 != 0) return ULY_EALIGN;
     p->chunk_cap = int64_t(1) << 30;
+    p->max_ctas = 0;
     return ULY_OK;
 }
 

@@ -17,6 +17,7 @@ struct Plan {
     int64_t s[kMaxW], n[kMaxW];
     int64_t seq_off[kMaxW + 1], head_off[kMaxW + 1];
     int64_t chunk_cap;  // max bytes one rank reads or writes per launch
+    int64_t max_ctas;   // cap on the CTAs of any launch (0: none)
 };
 
 // Rows of each sequence shard covered by one launch.

@@ -359,7 +359,7 @@ static cudaError_t ensure_tma_smem(int device, int smem)
 constexpr int kTmaSmem = kTmaBarrierBytes + ULY_TMA_STAGES * ULY_TMA_UNIT_BYTES;
 
 cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStream_t stream,
-                            int device, int sm_count)
+                            int device, int sm_count, int64_t max_grid)
 {
     if (a.total_units == 0) return cudaSuccess;
     if (engine == ULY_ENGINE_VEC) {
@@ -371,8 +371,9 @@ cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStr
         }
         const int64_t warps_needed = a.total_units;
         int64_t grid = int64_t(sm_count) * blocks_per_sm;
-        const int64_t max_grid = (warps_needed * 32 + kVecThreads - 1) / kVecThreads;
-        if (grid > max_grid) grid = max_grid;
+        if (max_grid > 0 && grid > max_grid) grid = max_grid;
+        const int64_t useful = (warps_needed * 32 + kVecThreads - 1) / kVecThreads;
+        if (grid > useful) grid = useful;
         if (mode == 0)
             relayout_vec_kernel<0><<<unsigned(grid), kVecThreads, 0, stream>>>(a);
         else
@@ -382,6 +383,7 @@ cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStr
     cudaError_t e = ensure_tma_smem(device, kTmaSmem);
     if (e != cudaSuccess) return e;
     int64_t grid = int64_t(sm_count) * ULY_TMA_CTAS_PER_SM;
+    if (max_grid > 0 && grid > max_grid) grid = max_grid;
     if (grid > a.total_units) grid = a.total_units;
     if (mode == 0)
         relayout_tma_kernel<0><<<unsigned(grid), 32, kTmaSmem, stream>>>(a);
@@ -397,12 +399,13 @@ int64_t relayout_tile_rows(int64_t row_bytes)
 }
 
 cudaError_t relayout_rows_launch(const RowTileArgs& a, int mode, cudaStream_t stream, int device,
-                                 int sm_count)
+                                 int sm_count, int64_t max_grid)
 {
     if (a.total_units == 0) return cudaSuccess;
     cudaError_t e = ensure_tma_smem(device, kTmaSmem);
     if (e != cudaSuccess) return e;
     int64_t grid = int64_t(sm_count) * ULY_TMA_CTAS_PER_SM;
+    if (max_grid > 0 && grid > max_grid) grid = max_grid;
     if (grid > a.total_units) grid = a.total_units;
     if (mode == 0)
         relayout_rows_kernel<0><<<unsigned(grid), 32, kTmaSmem, stream>>>(a);
