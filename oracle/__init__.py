@@ -90,6 +90,25 @@ class Oracle:
         lib.orc_bf16_to_double_array.restype = None
         lib.orc_double_to_bf16_array.argtypes = [_p, _i64, _p]
         lib.orc_double_to_bf16_array.restype = None
+        lib.orc_f16_to_double_array.argtypes = [_p, _i64, _p]
+        lib.orc_f16_to_double_array.restype = None
+        lib.orc_double_to_f16_array.argtypes = [_p, _i64, _p]
+        lib.orc_double_to_f16_array.restype = None
+        lib.orc_rope_half.argtypes = [_p, _i64, ctypes.c_double, ctypes.c_double]
+        lib.orc_rope_half.restype = None
+        lib.orc_fused_row_var.argtypes = [_p, _i64, ctypes.c_int, ctypes.c_int, _p, ctypes.c_double,
+                                          ctypes.c_double, ctypes.c_double, _p]
+        lib.orc_fused_row_var.restype = None
+        lib.orc_qk_fused_var.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, ctypes.c_int,
+                                         ctypes.c_int, _p, _p, ctypes.c_double, ctypes.c_double, _p]
+        lib.orc_qk_fused_var.restype = ctypes.c_int
+        lib.orc_fused_row_bwd_var.argtypes = [_p, _p, _i64, ctypes.c_int, _p, ctypes.c_double,
+                                              ctypes.c_double, ctypes.c_double, _p, _p]
+        lib.orc_fused_row_bwd_var.restype = None
+        lib.orc_qk_fused_bwd_var.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, ctypes.c_int,
+                                             ctypes.c_int, _p, _p, _p, ctypes.c_double,
+                                             ctypes.c_double, _p, _p]
+        lib.orc_qk_fused_bwd_var.restype = ctypes.c_int
         self.lib = lib
 
     # ---- relayout -------------------------------------------------------------------------
@@ -244,6 +263,83 @@ class Oracle:
         out = np.empty(x.shape, dtype=np.uint16)
         self.lib.orc_double_to_bf16_array(x.ctypes.data, x.size, out.ctypes.data)
         return out
+
+
+    # ---- variants of the fused call: fp16 elements, rotate-half pairs ----------------------
+    def f16_to_double(self, h):
+        h = np.ascontiguousarray(h, dtype=np.uint16)
+        out = np.empty(h.shape, dtype=np.float64)
+        self.lib.orc_f16_to_double_array(h.ctypes.data, h.size, out.ctypes.data)
+        return out
+
+    def double_to_f16(self, x):
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        out = np.empty(x.shape, dtype=np.uint16)
+        self.lib.orc_double_to_f16_array(x.ctypes.data, x.size, out.ctypes.data)
+        return out
+
+    def decode(self, h, f16):
+        """Element bit patterns (uint16) -> double, bf16 or fp16."""
+        return self.f16_to_double(h) if f16 else self.bf16_to_double(h)
+
+    def rope_half(self, y, p, theta):
+        y = np.array(y, dtype=np.float64, copy=True)
+        self.lib.orc_rope_half(y.ctypes.data, y.size, float(p), float(theta))
+        return y
+
+    def fused_row_var(self, x_raw, f16, half_pairs, w, eps, p, theta):
+        """One row of a variant: decode, RMSNorm, RoPE (adjacent or rotate-half pairs)."""
+        x = np.ascontiguousarray(x_raw).view(np.uint16)
+        w = np.ascontiguousarray(w, dtype=np.float64)
+        y = np.empty(x.size, dtype=np.float64)
+        self.lib.orc_fused_row_var(x.ctypes.data, x.size, int(f16), int(half_pairs), w.ctypes.data,
+                                   float(eps), float(p), float(theta), y.ctypes.data)
+        return y
+
+    def qk_fused_var(self, xs, seq_splits, head_splits, w, eps, theta, f16, half_pairs):
+        """The fused call of a variant for one tensor (unrounded double outputs)."""
+        W = len(xs)
+        b, d = xs[0].shape[0], xs[0].shape[3]
+        xs = [np.ascontiguousarray(x).view(np.uint16) for x in xs]
+        w = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
+        outs = [np.empty(sh, dtype=np.float64)
+                for sh in self.out_shapes(b, seq_splits, head_splits, d, 0)]
+        rc = self.lib.orc_qk_fused_var(W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
+                                       int(f16), int(half_pairs), ctypes.cast(_ptr_array(xs), _p),
+                                       w.ctypes.data, float(eps), float(theta),
+                                       ctypes.cast(_ptr_array(outs), _p))
+        if rc != 0:
+            raise ValueError("oracle rejected the geometry")
+        return outs
+
+    def fused_row_bwd_var(self, x, g, half_pairs, w, eps, p, theta):
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        g = np.ascontiguousarray(g, dtype=np.float64)
+        w = np.ascontiguousarray(w, dtype=np.float64)
+        dx = np.empty_like(x)
+        dw = np.zeros_like(x)
+        self.lib.orc_fused_row_bwd_var(x.ctypes.data, g.ctypes.data, x.size, int(half_pairs),
+                                       w.ctypes.data, float(eps), float(p), float(theta),
+                                       dx.ctypes.data, dw.ctypes.data)
+        return dx, dw
+
+    def qk_fused_bwd_var(self, xs, gs, seq_splits, head_splits, w, eps, theta, f16, half_pairs):
+        W = len(xs)
+        b, d = xs[0].shape[0], xs[0].shape[3]
+        xs = [np.ascontiguousarray(x).view(np.uint16) for x in xs]
+        gs = [np.ascontiguousarray(x).view(np.uint16) for x in gs]
+        w64 = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
+        dx = [np.empty(x.shape, dtype=np.float64) for x in xs]
+        dw = np.full(d, np.nan)  # the oracle clears it
+        rc = self.lib.orc_qk_fused_bwd_var(W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
+                                           int(f16), int(half_pairs),
+                                           ctypes.cast(_ptr_array(xs), _p),
+                                           ctypes.cast(_ptr_array(gs), _p), w64.ctypes.data,
+                                           float(eps), float(theta),
+                                           ctypes.cast(_ptr_array(dx), _p), dw.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle rejected the geometry")
+        return dx, dw
 
 
 _default: Oracle | None = None

@@ -28,7 +28,9 @@
  * d values (bf16 in), RMSNorm over d with eps inside the square root and one weight vector of
  * length d, then rotary embedding on adjacent pairs (2j, 2j+1) with angle p * theta^(-2j/d),
  * where p is the token's global sequence index. Everything is in double; the result is left
- * unrounded (a bf16 round-to-nearest-even helper is provided separately).
+ * unrounded (a bf16 round-to-nearest-even helper is provided separately). Its backward (the
+ * vector-Jacobian product per row, the output gradient brought back by mode 1) and two variants
+ * (fp16 elements; rotate-half pairs (j, j + d/2)) follow at the end of the file.
  *
  * All functions return 0 on success and -1 on invalid arguments.
  */
@@ -381,13 +383,11 @@ int orc_qkv_fused(int W, int64_t b, const int64_t* seq_splits, const int64_t* he
  * y = R(p) (x * w / rms(x)) with rms(x) = sqrt(mean(x^2) + eps) and R(p) the rotation above.
  * Given g = dL/dy: u = R(-p) g (the rotation is orthogonal), a = u * w,
  * dL/dx = (a - xh * mean(a * xh)) / rms(x) with xh = x / rms(x), and dL/dw += u * xh.
+ * row_bwd_core is the RMSNorm part, given u; orc_fused_row_bwd rotates g back first.
  */
-void orc_fused_row_bwd(const double* x, const double* g, int64_t d, const double* w, double eps,
-                       double p, double theta, double* dx, double* dw_acc)
+static void row_bwd_core(const double* x, const double* u, int64_t d, const double* w, double eps,
+                         double* dx, double* dw_acc)
 {
-    double* u = (double*)malloc((size_t)d * sizeof(double));
-    for (int64_t j = 0; j < d; ++j) u[j] = g[j];
-    orc_rope(u, d, -p, theta);
     double sum_sq = 0.0;
     for (int64_t j = 0; j < d; ++j) sum_sq += x[j] * x[j];
     const double inv_rms = 1.0 / sqrt(sum_sq / (double)d + eps);
@@ -401,6 +401,15 @@ void orc_fused_row_bwd(const double* x, const double* g, int64_t d, const double
         const double xh = x[j] * inv_rms;
         dx[j] = inv_rms * (u[j] * w[j] - xh * dot / (double)d);
     }
+}
+
+void orc_fused_row_bwd(const double* x, const double* g, int64_t d, const double* w, double eps,
+                       double p, double theta, double* dx, double* dw_acc)
+{
+    double* u = (double*)malloc((size_t)d * sizeof(double));
+    for (int64_t j = 0; j < d; ++j) u[j] = g[j];
+    orc_rope(u, d, -p, theta);
+    row_bwd_core(x, u, d, w, eps, dx, dw_acc);
     free(u);
 }
 
@@ -441,6 +450,195 @@ int orc_qk_fused_bwd(int W, int64_t b, const int64_t* seq_splits, const int64_t*
                     orc_fused_row_bwd(x, g, d, w, eps, (double)(seq_off_q + i), theta,
                                       dx[q] + src_row, dw);
                 }
+    }
+    free(x);
+    free(g);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Variants of the fused call: fp16 elements and rotate-half RoPE pairs.                        */
+/* ------------------------------------------------------------------------------------------ */
+/*
+ * The pages list float16 among the element types (fast-ulysses 0.2.1, "Limits") and name the
+ * fused QK RMSNorm + RoPE without fixing its pair layout. Besides adjacent pairs (2j, 2j+1), the
+ * other common layout ("rotate half") pairs element j with element j + d/2; both use the angle
+ * p * theta^(-2j/d) for pair j. Functions below take f16 (0: bf16 elements, 1: IEEE binary16)
+ * and half_pairs (0: adjacent, 1: rotate half).
+ */
+
+/* binary16 bit pattern -> value (exact): 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+double orc_f16_to_double(uint16_t h)
+{
+    const int negative = (h >> 15) & 1;
+    const int field = (h >> 10) & 0x1F;
+    const int fraction = h & 0x3FF;
+    double v;
+    if (field == 0)
+        v = ldexp((double)fraction, -24);                /* zero or subnormal: fraction * 2^-24 */
+    else if (field == 31)
+        v = fraction ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + fraction), field - 25); /* (1.fraction) * 2^(field - 15) */
+    return negative ? -v : v;
+}
+
+/*
+ * double -> binary16 bit pattern with one round-to-nearest-even step (11 significand bits,
+ * normal exponents down to -14, gradual underflow in steps of 2^-24, overflow to infinity).
+ */
+uint16_t orc_double_to_f16(double x)
+{
+    const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x)) return (uint16_t)(sign | 0x7E00u);
+    const double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sign | 0x7C00u);
+    if (a == 0.0) return sign;
+    int E;
+    frexp(a, &E);
+    int ex = E - 1;           /* a in [2^ex, 2^(ex+1)) */
+    if (ex < -14) ex = -14;   /* below the normal range the spacing stays 2^-24 */
+    const double step = ldexp(1.0, ex - 10);
+    const double v = nearbyint(a / step) * step; /* default rounding mode: nearest, ties to even */
+    if (v >= 65536.0) return (uint16_t)(sign | 0x7C00u); /* 65520 and up round past 65504 */
+    if (v == 0.0) return sign;                             /* below 2^-25: rounds to zero */
+    int Ev;
+    frexp(v, &Ev);
+    const int ev = Ev - 1;
+    if (ev < -14) return (uint16_t)(sign | (uint16_t)(v / ldexp(1.0, -24))); /* subnormal */
+    const uint16_t frac = (uint16_t)(v / ldexp(1.0, ev - 10) - 1024.0);
+    return (uint16_t)(sign | (uint16_t)((ev + 15) << 10) | frac);
+}
+
+void orc_f16_to_double_array(const uint16_t* h, int64_t n, double* out)
+{
+    for (int64_t k = 0; k < n; ++k) out[k] = orc_f16_to_double(h[k]);
+}
+
+void orc_double_to_f16_array(const double* x, int64_t n, uint16_t* out)
+{
+    for (int64_t k = 0; k < n; ++k) out[k] = orc_double_to_f16(x[k]);
+}
+
+/*
+ * Rotary embedding of one row in place, rotate-half pairs: for j < d/2 the pair
+ * (y[j], y[j + d/2]) is rotated by the angle p * theta^(-2j/d).
+ */
+void orc_rope_half(double* y, int64_t d, double p, double theta)
+{
+    const int64_t half = d / 2;
+    for (int64_t j = 0; j < half; ++j) {
+        const double angle = p * pow(theta, -(double)(2 * j) / (double)d);
+        const double c = cos(angle), s = sin(angle);
+        const double first = y[j], second = y[half + j];
+        y[j] = first * c - second * s;
+        y[half + j] = first * s + second * c;
+    }
+}
+
+static double decode_elem(uint16_t h, int f16)
+{
+    return f16 ? orc_f16_to_double(h) : orc_bf16_to_double(h);
+}
+
+static void rope_pairs(double* y, int64_t d, double p, double theta, int half_pairs)
+{
+    if (half_pairs)
+        orc_rope_half(y, d, p, theta);
+    else
+        orc_rope(y, d, p, theta);
+}
+
+/* One head row of a variant: decode, RMSNorm, RoPE at position p; double out. */
+void orc_fused_row_var(const uint16_t* x_raw, int64_t d, int f16, int half_pairs, const double* w,
+                       double eps, double p, double theta, double* y)
+{
+    double* x = (double*)malloc((size_t)d * sizeof(double));
+    for (int64_t j = 0; j < d; ++j) x[j] = decode_elem(x_raw[j], f16);
+    orc_rmsnorm(x, d, w, eps, y);
+    rope_pairs(y, d, p, theta, half_pairs);
+    free(x);
+}
+
+/*
+ * The fused mode-0 call of a variant for one tensor: every source row is transformed at its
+ * global position seq_off(q) + i and placed where mode 0 puts it. x_in[q]: rank q's
+ * (b, s_q, N, d) elements; y_out[r]: rank r's (b, S, n_r, d) in double.
+ */
+int orc_qk_fused_var(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                     int64_t d, int f16, int half_pairs, const uint16_t* const* x_in,
+                     const double* w, double eps, double theta, double* const* y_out)
+{
+    if (check_geometry(W, b, seq_splits, head_splits, d) || (d % 2) != 0) return -1;
+    const int64_t S = offset_of(seq_splits, W);
+    const int64_t N = offset_of(head_splits, W);
+    for (int r = 0; r < W; ++r) {
+        const int64_t n_r = head_splits[r];
+        const int64_t first_head = offset_of(head_splits, r);
+        for (int q = 0; q < W; ++q) {
+            const int64_t s_q = seq_splits[q];
+            const int64_t seq_off_q = offset_of(seq_splits, q);
+            for (int64_t bb = 0; bb < b; ++bb)
+                for (int64_t i = 0; i < s_q; ++i)
+                    for (int64_t h = 0; h < n_r; ++h) {
+                        const uint16_t* src = x_in[q] + ((bb * s_q + i) * N + first_head + h) * d;
+                        double* dst = y_out[r] + ((bb * S + seq_off_q + i) * n_r + h) * d;
+                        orc_fused_row_var(src, d, f16, half_pairs, w, eps,
+                                          (double)(seq_off_q + i), theta, dst);
+                    }
+        }
+    }
+    return 0;
+}
+
+/* Row backward of a variant: g rotated back with the variant's pairs, then the RMSNorm part. */
+void orc_fused_row_bwd_var(const double* x, const double* g, int64_t d, int half_pairs,
+                           const double* w, double eps, double p, double theta, double* dx,
+                           double* dw_acc)
+{
+    double* u = (double*)malloc((size_t)d * sizeof(double));
+    for (int64_t j = 0; j < d; ++j) u[j] = g[j];
+    rope_pairs(u, d, -p, theta, half_pairs);
+    row_bwd_core(x, u, d, w, eps, dx, dw_acc);
+    free(u);
+}
+
+/*
+ * Backward of a variant's fused call for one tensor: x_in[q] rank q's forward input
+ * (b, s_q, N, d), g_out[r] rank r's output gradient (b, S, n_r, d), both in the variant's
+ * element type; dx[q] (double, (b, s_q, N, d)) and dw (d values, cleared first) as
+ * orc_qk_fused_bwd.
+ */
+int orc_qk_fused_bwd_var(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                         int64_t d, int f16, int half_pairs, const uint16_t* const* x_in,
+                         const uint16_t* const* g_out, const double* w, double eps, double theta,
+                         double* const* dx, double* dw)
+{
+    if (check_geometry(W, b, seq_splits, head_splits, d) || (d % 2) != 0) return -1;
+    const int64_t S = offset_of(seq_splits, W);
+    const int64_t N = offset_of(head_splits, W);
+    double* x = (double*)malloc((size_t)d * sizeof(double));
+    double* g = (double*)malloc((size_t)d * sizeof(double));
+    memset(dw, 0, (size_t)d * sizeof(double));
+    for (int r = 0; r < W; ++r) {
+        const int64_t n_r = head_splits[r];
+        const int64_t first_head = offset_of(head_splits, r);
+        for (int q = 0; q < W; ++q) {
+            const int64_t s_q = seq_splits[q];
+            const int64_t seq_off_q = offset_of(seq_splits, q);
+            for (int64_t bb = 0; bb < b; ++bb)
+                for (int64_t i = 0; i < s_q; ++i)
+                    for (int64_t h = 0; h < n_r; ++h) {
+                        const int64_t in_row = ((bb * s_q + i) * N + first_head + h) * d;
+                        const int64_t grad_row = ((bb * S + seq_off_q + i) * n_r + h) * d;
+                        for (int64_t j = 0; j < d; ++j) {
+                            x[j] = decode_elem(x_in[q][in_row + j], f16);
+                            g[j] = decode_elem(g_out[r][grad_row + j], f16);
+                        }
+                        orc_fused_row_bwd_var(x, g, d, half_pairs, w, eps,
+                                              (double)(seq_off_q + i), theta, dx[q] + in_row, dw);
+                    }
+        }
     }
     free(x);
     free(g);

@@ -466,6 +466,192 @@ def pin_relayout_adjoint(orc, quick=False):
         assert abs(lhs - rhs) < 1e-9 * (1 + abs(lhs))
 
 
+# ---- variants: fp16 elements, rotate-half pairs ------------------------------------------------
+def pin_f16_decode(orc, quick=False):
+    """Every binary16 bit pattern decodes as numpy's float16 does (NaNs as NaNs)."""
+    h = np.arange(65536, dtype=np.uint16)
+    got = orc.f16_to_double(h)
+    want = h.view(np.float16).astype(np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(want[ok]))
+
+
+def pin_f16_encode(orc, quick=False):
+    """double -> binary16 against numpy's correctly rounded conversion on random values over the
+    whole range, exact ties, the subnormal range and the overflow edge, plus closed forms."""
+    rng = np.random.default_rng(40)
+    vals = [rng.standard_normal(20000) * np.exp2(rng.integers(-30, 17, 20000)),
+            (rng.integers(0, 2048, 4000) + 0.5) * np.exp2(rng.integers(-24, 6, 4000)),  # ties
+            rng.uniform(-2.0 ** -14, 2.0 ** -14, 4000),                                # subnormal
+            np.array([65504.0, 65519.99, 65520.0, 65535.0, 1e6, 2.0 ** -25, 3 * 2.0 ** -25,
+                      2.0 ** -26, -0.0, 0.0, np.inf, -np.inf])]
+    x = np.concatenate(vals)
+    got = orc.double_to_f16(x)
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, want), int((got != want).sum())
+    closed = {1.0 + 2.0 ** -11: 0x3C00, 1.0 + 3 * 2.0 ** -11: 0x3C02, 65519.0: 0x7BFF,
+              65520.0: 0x7C00, 2.0 ** -25: 0x0000, 3 * 2.0 ** -25: 0x0002, -2.0: 0xC000}
+    for v, bits in closed.items():
+        assert int(orc.double_to_f16(np.array([v]))[0]) == bits, v
+
+
+def pin_rope_half_vs_complex(orc, quick=False):
+    """Rotate-half pairs (y_j, y_(j+d/2)) as complex numbers times exp(i p theta^(-2j/d))."""
+    rng = np.random.default_rng(41)
+    for d in (2, 8, 128):
+        for p in (0, 1, 9450, 75599):
+            y = rng.standard_normal(d)
+            h = d // 2
+            z = torch.complex(torch.from_numpy(y[:h].copy()), torch.from_numpy(y[h:].copy()))
+            ang = torch.tensor([p * _freq(1e4, j, d) for j in range(h)], dtype=torch.float64)
+            rot = z * torch.polar(torch.ones_like(ang), ang)
+            want = np.concatenate([rot.real.numpy(), rot.imag.numpy()])
+            np.testing.assert_allclose(orc.rope_half(y, p, 1e4), want, rtol=1e-12, atol=1e-12)
+
+
+def pin_rope_half_is_permuted_adjacent(orc, quick=False):
+    """Rotate-half equals adjacent pairs on the interleaved row: (P y)_(2j) = y_j,
+    (P y)_(2j+1) = y_(j+d/2), rope_half(y) = P^-1 rope(P y)."""
+    rng = np.random.default_rng(42)
+    for d in (4, 64, 256):
+        h = d // 2
+        perm = np.empty(d, dtype=np.int64)
+        perm[0::2] = np.arange(h)
+        perm[1::2] = np.arange(h, d)
+        for p in (3, 1000, 75599):
+            y = rng.standard_normal(d)
+            adj = orc.rope(y[perm], p, 1e4)
+            back = np.empty(d)
+            back[perm] = adj
+            np.testing.assert_array_equal(orc.rope_half(y, p, 1e4), back)
+
+
+def _torch_row_half(x, w, eps, p, theta):
+    """RMSNorm then the usual rotate-half formula y*cos + rotate_half(y)*sin, with cos and sin of
+    pair j repeated in both halves; differentiable."""
+    d = x.shape[-1]
+    y = F.rms_norm(x[None], (d,), weight=w, eps=eps)[0]
+    ang = torch.tensor([p * _freq(theta, j, d) for j in range(d // 2)], dtype=torch.float64)
+    cos, sin = torch.cat([ang.cos(), ang.cos()]), torch.cat([ang.sin(), ang.sin()])
+    rot = torch.cat([-y[d // 2:], y[:d // 2]])
+    return y * cos + rot * sin
+
+
+def pin_fused_row_variants(orc, quick=False):
+    """A variant row equals the library-built forward on the decoded values: adjacent pairs via
+    the pinned complex formulation, rotate-half via the rotate_half formula; bf16 and fp16
+    decoding via torch's own bf16 and numpy's float16."""
+    rng = np.random.default_rng(43)
+    for d in (8, 128):
+        for f16 in (0, 1):
+            for half in (0, 1):
+                for p in (0, 5, 75599):
+                    xf = rng.standard_normal(d).astype(np.float32)
+                    if f16:
+                        raw = xf.astype(np.float16).view(np.uint16)
+                        x = raw.view(np.float16).astype(np.float64)
+                    else:
+                        t = torch.from_numpy(xf).to(torch.bfloat16)
+                        raw = t.view(torch.int16).numpy().view(np.uint16)
+                        x = t.double().numpy()
+                    w = 1.0 + 0.1 * rng.standard_normal(d)
+                    xt, wt = torch.from_numpy(x), torch.from_numpy(w)
+                    if half:
+                        want = _torch_row_half(xt, wt, 1e-6, p, 1e4).numpy()
+                    else:
+                        want = _torch_row_forward(xt, wt, 1e-6, p, 1e4).detach().numpy()
+                    got = orc.fused_row_var(raw, f16, half, w, 1e-6, p, 1e4)
+                    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def pin_fused_var_whole_call(orc, quick=False):
+    """The whole call of a variant: (bf16, adjacent) is bit-identical to the pinned formulation
+    A; every variant equals mode 0 of the raw elements (pinned above) followed by the variant row
+    at the destination row's sequence index."""
+    rng = np.random.default_rng(44)
+    for W, b, seq, heads, d in [(2, 1, [3, 2], [2, 1], 8), (3, 2, [2, 0, 3], [1, 2, 1], 16)]:
+        N, S = sum(heads), sum(seq)
+        raw = [rng.integers(0, 1 << 16, (b, s, N, d)).astype(np.uint16) for s in seq]
+        # keep the elements finite and moderate for both decodings
+        raw = [(r & 0x3FFF) | 0x3000 for r in raw]
+        w = 1.0 + 0.1 * rng.standard_normal(d)
+        a = orc.qk_fused_var(raw, seq, heads, w, 1e-6, 1e4, 0, 0)
+        ref = orc.qk_fused_A(raw, seq, heads, w, 1e-6, 1e4)
+        for x, y in zip(a, ref):
+            assert np.array_equal(x, y)
+        placed = orc.a2a_4d(raw, seq, heads, 0)
+        for f16 in (0, 1):
+            for half in (0, 1):
+                got = orc.qk_fused_var(raw, seq, heads, w, 1e-6, 1e4, f16, half)
+                for r in range(W):
+                    for bb in range(b):
+                        for t in range(S):
+                            for h in range(heads[r]):
+                                want = orc.fused_row_var(placed[r][bb, t, h], f16, half, w, 1e-6,
+                                                         t, 1e4)
+                                np.testing.assert_array_equal(got[r][bb, t, h], want)
+
+
+def pin_fused_bwd_variants(orc, quick=False):
+    """Row backward of a variant: adjacent pairs bit-identical to the pinned row backward;
+    rotate-half against torch.autograd of the rotate_half formula (fp64), x.grad and w.grad."""
+    rng = np.random.default_rng(45)
+    for d in (2, 8, 128):
+        for p in (0, 3, 75599):
+            x, g = rng.standard_normal(d), rng.standard_normal(d)
+            w = 1.0 + 0.1 * rng.standard_normal(d)
+            a = orc.fused_row_bwd_var(x, g, 0, w, 1e-6, p, 1e4)
+            b_ = orc.fused_row_bwd(x, g, w, 1e-6, p, 1e4)
+            assert np.array_equal(a[0], b_[0]) and np.array_equal(a[1], b_[1])
+            xt = torch.tensor(x, requires_grad=True)
+            wt = torch.tensor(w, requires_grad=True)
+            _torch_row_half(xt, wt, 1e-6, p, 1e4).backward(torch.from_numpy(g))
+            dx, dw = orc.fused_row_bwd_var(x, g, 1, w, 1e-6, p, 1e4)
+            np.testing.assert_allclose(dx, xt.grad.numpy(), rtol=1e-9, atol=1e-11)
+            np.testing.assert_allclose(dw, wt.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def pin_fused_bwd_var_whole_call(orc, quick=False):
+    """Whole-call backward of a variant: (bf16, adjacent) dx bit-identical to the pinned one (dw up
+    to the order of its sum); every
+    variant equals mode 1 (pinned) of the output gradients, then the variant row backward at
+    each row's global position, dw the sum over rows."""
+    rng = np.random.default_rng(46)
+    for W, b, seq, heads, d in [(2, 1, [3, 2], [2, 1], 8), (3, 2, [2, 0, 3], [1, 2, 1], 16)]:
+        N, S = sum(heads), sum(seq)
+        mk = lambda shape: ((rng.integers(0, 1 << 16, shape).astype(np.uint16) & 0x3FFF)  # noqa: E731
+                            | 0x3000).astype(np.uint16)
+        xs = [mk((b, s, N, d)) for s in seq]
+        gs = [mk((b, S, n, d)) for n in heads]
+        w = 1.0 + 0.1 * rng.standard_normal(d)
+        a = orc.qk_fused_bwd_var(xs, gs, seq, heads, w, 1e-6, 1e4, 0, 0)
+        ref = orc.qk_fused_bwd(xs, gs, seq, heads, w, 1e-6, 1e4)
+        for x, y in zip(a[0], ref[0]):
+            assert np.array_equal(x, y)
+        np.testing.assert_allclose(a[1], ref[1], rtol=1e-13, atol=1e-13)  # rows summed in another order
+        g_seq = orc.a2a_4d(gs, seq, heads, 1)
+        seq_off = np.cumsum([0] + list(seq))
+        for f16 in (0, 1):
+            for half in (0, 1):
+                dx, dw = orc.qk_fused_bwd_var(xs, gs, seq, heads, w, 1e-6, 1e4, f16, half)
+                dw_want = np.zeros(d)
+                for q in range(W):
+                    for bb in range(b):
+                        for i in range(seq[q]):
+                            for hh in range(N):
+                                want, dwr = orc.fused_row_bwd_var(
+                                    orc.decode(xs[q][bb, i, hh], f16),
+                                    orc.decode(g_seq[q][bb, i, hh], f16), half, w, 1e-6,
+                                    seq_off[q] + i, 1e4)
+                                dw_want += dwr
+                                np.testing.assert_allclose(dx[q][bb, i, hh], want, rtol=1e-13,
+                                                           atol=1e-15)
+                np.testing.assert_allclose(dw, dw_want, rtol=1e-12, atol=1e-12)
+
+
 def pin_bf16_rounding(orc, quick=False):
     """double -> bf16 on float32-representable values equals torch's float32 -> bf16 (one
     round-to-nearest-even); bf16 -> double equals torch's widening."""
@@ -509,6 +695,14 @@ PINS = [
     pin_fused_bwd_finite_differences,
     pin_fused_bwd_placement,
     pin_relayout_adjoint,
+    pin_f16_decode,
+    pin_f16_encode,
+    pin_rope_half_vs_complex,
+    pin_rope_half_is_permuted_adjacent,
+    pin_fused_row_variants,
+    pin_fused_var_whole_call,
+    pin_fused_bwd_variants,
+    pin_fused_bwd_var_whole_call,
     pin_bf16_rounding,
 ]
 

@@ -72,6 +72,24 @@ MUTANTS = {
     "bwd_dw_not_cleared": [("for (int64_t j = 0; j < d; ++j) dw[j] = 0.0;", "")],
     "bwd_gradient_from_wrong_token": [("g[j] = orc_bf16_to_double(g_out[r][out_row + j]);",
                                        "g[j] = orc_bf16_to_double(g_out[r][out_row - (i > 0 ? n_r * d : 0) + j]);")],
+    "f16_decode_bias": [("ldexp((double)(1024 + fraction), field - 25)",
+                         "ldexp((double)(1024 + fraction), field - 24)")],
+    "f16_decode_subnormal_scale": [("v = ldexp((double)fraction, -24);", "v = ldexp((double)fraction, -25);")],
+    "f16_encode_one_bit_short": [("ldexp(1.0, ex - 10)", "ldexp(1.0, ex - 9)")],
+    "f16_encode_truncates": [("nearbyint(a / step)", "floor(a / step)")],
+    "f16_encode_normal_floor": [("if (ex < -14) ex = -14;", "if (ex < -15) ex = -15;")],
+    "rope_half_sin_sign": [("y[j] = first * c - second * s;", "y[j] = first * c + second * s;")],
+    "rope_half_wrong_partner": [("second = y[half + j];", "second = y[half + j - (j > 0)];")],
+    "rope_half_freq_exponent": [("pow(theta, -(double)(2 * j) / (double)d)", "pow(theta, -(double)j / (double)d)")],
+    "variant_ignores_half_pairs": [("    if (half_pairs)\n        orc_rope_half", "    if (0)\n        orc_rope_half")],
+    "variant_ignores_f16": [("return f16 ? orc_f16_to_double(h) : orc_bf16_to_double(h);",
+                             "return orc_bf16_to_double(h);")],
+    "variant_local_position": [("eps,\n                                          (double)(seq_off_q + i), theta, dst);",
+                                "eps,\n                                          (double)i, theta, dst);")],
+    "variant_bwd_forward_rotation": [("rope_pairs(u, d, -p, theta, half_pairs);",
+                                      "rope_pairs(u, d, p, theta, half_pairs);")],
+    "variant_bwd_grad_drops_seq_offset": [("const int64_t grad_row = ((bb * S + seq_off_q + i) * n_r + h) * d;",
+                                           "const int64_t grad_row = ((bb * S + i) * n_r + h) * d;")],
     "bf16_truncates": [("nearbyint(a / quantum)", "floor(a / quantum)")],
     "bf16_one_bit_too_many": [("ldexp(1.0, ex - 7)", "ldexp(1.0, ex - 8)")],
     "bf16_widening_drops_low_bits": [("uint32_t bits = (uint32_t)h << 16;",
