@@ -58,7 +58,7 @@ enum {
 
 /* Element types (fast-ulysses 0.2.1, README, "Limits": float16 / bfloat16 / float32 /
  * float8_e4m3fn / float8_e5m2 / int8 / uint8). The relayout moves bytes, so only the size
- * matters to it; the fused QK call requires ULY_BF16. */
+ * matters to it; the fused QK calls require ULY_BF16 or ULY_F16. */
 enum {
     ULY_U8 = 1,
     ULY_F8E4M3 = 2,
@@ -68,6 +68,12 @@ enum {
     ULY_BF16 = 6,
     ULY_F32 = 7
 };
+
+/* RoPE pair layouts of the fused QK calls (ulysses_plan_set_rope_pairs): pair j is
+ * (x[2j], x[2j+1]) (ULY_ROPE_ADJACENT, the default) or (x[j], x[j + d/2]) (ULY_ROPE_HALF, the
+ * "rotate half" layout); both rotate pair j by p * rope_theta^(-2j/d). The pages name the fused
+ * QK RMSNorm + RoPE without fixing its layout; both common ones are provided. */
+enum { ULY_ROPE_ADJACENT = 0, ULY_ROPE_HALF = 1 };
 
 /* Relayout engines: ULY_ENGINE_AUTO picks the fastest measured one (the TMA kernel).
  * ULY_ENGINE_CE issues one pitched cudaMemcpy2DAsync per (source shard, destination rank, batch
@@ -117,6 +123,11 @@ int ulysses_plan_set_chunk_bytes(ulysses_plan_t plan, int64_t max_chunk_bytes);
  */
 int ulysses_plan_set_max_ctas(ulysses_plan_t plan, int64_t max_ctas);
 
+/* RoPE pair layout (ULY_ROPE_ADJACENT or ULY_ROPE_HALF) of the fused calls made with this plan:
+ * the forward, the interleaved QKV form, the host-buffer form and the backward. Default
+ * ULY_ROPE_ADJACENT. Must not race with launches using the plan. */
+int ulysses_plan_set_rope_pairs(ulysses_plan_t plan, int pairs);
+
 /* Bytes of rank `rank`'s input and output tensors for `mode` (either pointer may be NULL). */
 int ulysses_plan_bytes(ulysses_plan_t plan, int mode, int rank, int64_t* in_bytes,
                        int64_t* out_bytes);
@@ -150,14 +161,16 @@ int ulysses_a2a_4d_engine(ulysses_plan_t plan, int mode, int engine, const void*
 
 /*
  * Mode 0 with QK RMSNorm + RoPE applied inside the scatter (fast-ulysses 0.1.0, "Fusion
- * examples"). For q and k separately, every head row x of d bf16 values at global sequence
+ * examples"). For q and k separately, every head row x of d values at global sequence
  * position p = seq_off(q) + i becomes
  *     y = x / sqrt(mean(x^2) + eps) * w                  (w: rms_w[0][:] for q, rms_w[1][:] for k)
- *     (y[2j], y[2j+1]) rotated by the angle p * rope_theta^(-2j/d), j < d/2
- * computed in fp32 and rounded once to bf16 (nearest even), then placed where mode 0 puts it.
- *   plan     must have dtype ULY_BF16 and d in {8, 16, 32, 64, 128, 256}; S < 2^24.
- *   q_in, k_in     W device pointers, rank q's (b, s_q, N, d) bf16.
- *   q_out, k_out   W device pointers, rank r's (b, S, n_r, d) bf16.
+ *     pair j of y rotated by the angle p * rope_theta^(-2j/d), j < d/2 (pairs (y[2j], y[2j+1]),
+ *     or (y[j], y[j + d/2]) after ulysses_plan_set_rope_pairs(plan, ULY_ROPE_HALF))
+ * computed in fp32 and rounded once to the element type (nearest even), then placed where mode 0
+ * puts it.
+ *   plan     must have dtype ULY_BF16 or ULY_F16 and d in {8, 16, 32, 64, 128, 256}; S < 2^24.
+ *   q_in, k_in     W device pointers, rank q's (b, s_q, N, d) elements of the plan's dtype.
+ *   q_out, k_out   W device pointers, rank r's (b, S, n_r, d), same dtype.
  *   rms_w    device pointer to 2 * d fp32 values, q's weight then k's.
  *   eps      > 0 or 0; rope_theta > 0.
  * V and the attention output go through ulysses_a2a_4d (mode 0 / mode 1).
@@ -174,11 +187,12 @@ int ulysses_a2a_4d_qk_fused(ulysses_plan_t plan, const void* const* q_in, const 
  * the RMSNorm + RoPE transform is applied inside that mode-1 gather. For q and k separately, per
  * head row x at global position p with output gradient gy (the row mode 0 made of x):
  *     r = 1 / sqrt(mean(x^2) + eps),  u = gy rotated back by p * rope_theta^(-2j/d) per pair j,
- *     dx = r * (u * w - x * r * <u * w, x * r> / d)      -> dq_out / dk_out, bf16, rounded once
+ *     dx = r * (u * w - x * r * <u * w, x * r> / d)      -> dq_out / dk_out, rounded once
  *     dw = sum over all rows of all ranks of u * x * r   -> dw[0][:] (q), dw[1][:] (k), fp32
  * computed in fp32 (the sums over rows in fp32, in an order that does not depend on timing).
- *   dq_out, dk_out  W device pointers, rank q's (b, s_q, N, d) bf16 (the forward's inputs' shape).
- *   q_in, k_in      W device pointers, the forward's inputs (rank q's (b, s_q, N, d) bf16).
+ *   dq_out, dk_out  W device pointers, rank q's (b, s_q, N, d) of the plan's dtype (bf16 or
+ *                   fp16; the forward's inputs' shape). The pair layout is the plan's.
+ *   q_in, k_in      W device pointers, the forward's inputs (rank q's (b, s_q, N, d)).
  *   dq_in, dk_in    W device pointers, gradients of the forward's outputs, rank r's (b, S, n_r, d).
  *   rms_w           device pointer, 2 * d fp32 (as the forward); dw: device pointer, 2 * d fp32,
  *                   overwritten.
@@ -237,11 +251,11 @@ int ulysses_a2a_4d_qk_fused_backward_static(ulysses_plan_t plan, void* const* dq
 /*
  * The fused call on interleaved packed QKV, the layout a fused QKV projection writes (FastVideo,
  * "Ulysses performance on GB200": packed QKV or QKVG): rank q's input is one (b, s_q, 3, N, d)
- * bf16 tensor whose planes are q, k and v. In one launch per chunk, q and k are normalised,
+ * tensor (bf16 or fp16) whose planes are q, k and v. In one launch per chunk, q and k are normalised,
  * rotated and placed as ulysses_a2a_4d_qk_fused does, and v is placed by mode 0 unchanged
  * (bit-exact).
- *   qkv_in          W device pointers, rank q's (b, s_q, 3, N, d) bf16.
- *   q_out, k_out, v_out   W device pointers each, rank r's (b, S, n_r, d) bf16.
+ *   qkv_in          W device pointers, rank q's (b, s_q, 3, N, d) of the plan's dtype.
+ *   q_out, k_out, v_out   W device pointers each, rank r's (b, S, n_r, d), same dtype.
  *   rms_w, eps, rope_theta, plan requirements: as ulysses_a2a_4d_qk_fused. The chunk cap applies
  *   per plane (one launch reads up to three times the cap from a rank).
  */

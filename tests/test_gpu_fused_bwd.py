@@ -141,9 +141,9 @@ def test_backward_workspace_and_argument_checks():
     with pytest.raises(B.UlyssesError):  # dw inside the workspace
         B.ulysses_a2a_4d_qk_fused_backward(plan, dqo, dko, q, k, dq, dk, w,
                                            ws[:2 * d * 4].view(torch.float32), EPS, THETA, ws)
-    fp16 = B.ulysses_plan(*g, "float16")
+    fp32 = B.ulysses_plan(*g, "float32")
     with pytest.raises(B.UlyssesError):
-        B.ulysses_qk_fused_backward_workspace(fp16)
+        B.ulysses_qk_fused_backward_workspace(fp32)
 
 
 def _wan_inputs(seed):

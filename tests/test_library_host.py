@@ -40,7 +40,7 @@ def test_exports_every_declared_symbol():
 
 def test_version_and_strerror():
     assert B.ulysses_version() == 100
-    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         assert B.ulysses_strerror(code) != "unknown status"
 
 
@@ -155,6 +155,15 @@ def test_launch_argument_errors_before_cuda():
     assert ei.value.status == B.ULY_EINVAL
 
 
+def test_rope_pairs_setter():
+    plan = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "bfloat16")
+    B.ulysses_plan_set_rope_pairs(plan, B.ULY_ROPE_HALF)
+    B.ulysses_plan_set_rope_pairs(plan, B.ULY_ROPE_ADJACENT)
+    with pytest.raises(B.UlyssesError) as ei:
+        B.ulysses_plan_set_rope_pairs(plan, 2)
+    assert ei.value.status == B.ULY_EINVAL
+
+
 def test_max_ctas_setter():
     plan = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "bfloat16")
     B.ulysses_plan_set_max_ctas(plan, 0)
@@ -165,7 +174,7 @@ def test_max_ctas_setter():
 
 
 def test_fused_argument_errors_before_cuda():
-    plan16 = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "float16")
+    plan32 = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "float32")
     plan = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "bfloat16")
     plan_d = B.ulysses_plan(2, 1, [4, 4], [2, 2], 24, "bfloat16")  # 48-byte rows: not a power of 2
     in_b = [B.ulysses_plan_bytes(plan, 0, k)[0] for k in range(2)]
@@ -174,7 +183,7 @@ def test_fused_argument_errors_before_cuda():
     qo, ko = _fake_ptrs(1 << 41, out_b), _fake_ptrs(1 << 42, out_b)
     w = 1 << 43
     for p, args, status in [
-        (plan16, (q, k, qo, ko, w, 1e-6, 1e4), B.ULY_EINVAL),   # not bf16
+        (plan32, (q, k, qo, ko, w, 1e-6, 1e4), B.ULY_EINVAL),   # neither bf16 nor fp16
         (plan_d, (q, k, qo, ko, w, 1e-6, 1e4), B.ULY_EINVAL),   # unsupported d
         (plan, (q, k, qo, ko, w + 4, 1e-6, 1e4), B.ULY_EALIGN), # weights misaligned
         (plan, (q, k, qo, ko, 0, 1e-6, 1e4), B.ULY_EINVAL),     # no weights

@@ -83,8 +83,8 @@ def test_static_scratch_checks_arguments_like_the_workspace_form():
     dw = torch.empty((2, d), dtype=torch.float32, device="cuda")
     with pytest.raises(B.UlyssesError):  # dq output on top of the forward input
         B.ulysses_a2a_4d_qk_fused_backward_static(plan, q, dko, q, k, dq, dk, w, dw, EPS, THETA)
-    with pytest.raises(B.UlyssesError):  # the fused path needs bf16
-        B.ulysses_a2a_4d_qk_fused_backward_static(B.ulysses_plan(*g, "float16"), dqo, dko, q, k,
+    with pytest.raises(B.UlyssesError):  # the fused path needs bf16 or fp16
+        B.ulysses_a2a_4d_qk_fused_backward_static(B.ulysses_plan(*g, "float32"), dqo, dko, q, k,
                                                   dq, dk, w, dw, EPS, THETA)
     B.ulysses_a2a_4d_qk_fused_backward_static(plan, dqo, dko, q, k, dq, dk, w, dw, EPS, THETA)
     assert B.ulysses_device_status() == 0

@@ -19,13 +19,14 @@ ULY_ESCRATCH = -8
 ULYSSES_STATIC_SCRATCH_BYTES = 2 * 1024 * 1024
 ULY_U8, ULY_F8E4M3, ULY_F8E5M2, ULY_I8, ULY_F16, ULY_BF16, ULY_F32 = 1, 2, 3, 4, 5, 6, 7
 ULY_ENGINE_AUTO, ULY_ENGINE_TMA, ULY_ENGINE_VEC, ULY_ENGINE_CE = 0, 1, 2, 3
+ULY_ROPE_ADJACENT, ULY_ROPE_HALF = 0, 1
 
 DTYPE_CODES = {"uint8": ULY_U8, "float8_e4m3fn": ULY_F8E4M3, "float8_e5m2": ULY_F8E5M2,
                "int8": ULY_I8, "float16": ULY_F16, "bfloat16": ULY_BF16, "float32": ULY_F32}
 
 # Every symbol include/ulysses.h declares.
 EXPORTS = ["ulysses_plan", "ulysses_plan_destroy", "ulysses_plan_set_chunk_bytes",
-           "ulysses_plan_set_max_ctas",
+           "ulysses_plan_set_max_ctas", "ulysses_plan_set_rope_pairs",
            "ulysses_plan_bytes", "ulysses_plan_num_chunks", "ulysses_plan_chunk_rows",
            "ulysses_a2a_4d", "ulysses_a2a_4d_engine", "ulysses_a2a_4d_qk_fused",
            "ulysses_a2a_4d_qkv_fused", "ulysses_a2a_4d_qk_fused_backward",
@@ -62,6 +63,7 @@ def _lib():
         lib.ulysses_plan_destroy.argtypes = [_p]
         lib.ulysses_plan_set_chunk_bytes.argtypes = [_p, _i64]
         lib.ulysses_plan_set_max_ctas.argtypes = [_p, _i64]
+        lib.ulysses_plan_set_rope_pairs.argtypes = [_p, ctypes.c_int]
         lib.ulysses_plan_bytes.argtypes = [_p, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_i64),
                                            ctypes.POINTER(_i64)]
         lib.ulysses_plan_num_chunks.argtypes = [_p, ctypes.c_int, ctypes.POINTER(_i64)]
@@ -162,6 +164,11 @@ def ulysses_plan(W: int, b: int, seq_splits, head_splits, d: int, dtype: str) ->
 
 def ulysses_plan_set_chunk_bytes(plan: Plan, max_chunk_bytes: int):
     _check(_lib().ulysses_plan_set_chunk_bytes(plan, max_chunk_bytes), "ulysses_plan_set_chunk_bytes")
+
+
+def ulysses_plan_set_rope_pairs(plan: Plan, pairs: int):
+    """RoPE pair layout of the fused calls with this plan: ULY_ROPE_ADJACENT or ULY_ROPE_HALF."""
+    _check(_lib().ulysses_plan_set_rope_pairs(plan, pairs), "ulysses_plan_set_rope_pairs")
 
 
 def ulysses_plan_set_max_ctas(plan: Plan, max_ctas: int):

@@ -228,7 +228,7 @@ int fused_prepare(const Plan& p, const void* const* q_in, const void* const* k_i
                   int64_t* tokens_per_unit)
 {
     const bool qkv = qkv_in != nullptr;
-    if (p.dtype != ULY_BF16) return ULY_EINVAL;
+    if (p.dtype != ULY_BF16 && p.dtype != ULY_F16) return ULY_EINVAL;
     if (!(p.d == 8 || p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128 || p.d == 256))
         return ULY_EINVAL;
     if (p.S >= (int64_t(1) << 24)) return ULY_EINVAL;  // positions must be exact in fp32
@@ -284,6 +284,8 @@ int fused_prepare(const Plan& p, const void* const* q_in, const void* const* k_i
     std::memset(a, 0, sizeof *a);
     a->ctas_per_sm = ctas_per_sm;
     a->interleaved = qkv ? 1 : 0;
+    a->elem_f16 = p.dtype == ULY_F16 ? 1 : 0;
+    a->rope_half = p.rope_half;
     for (int k = 0; k < p.W; ++k) {
         if (qkv) {
             a->qkv_in[k] = static_cast<const uint8_t*>(qkv_in[k]);
@@ -340,7 +342,7 @@ int fused_device(const Plan& p, const void* const* q_in, const void* const* k_in
 int fused_bwd_setup(const Plan& p, const DeviceInfo& dev, int64_t* tokens_per_unit, int* stages,
                     uint32_t* stage_bytes, int* ctas_per_sm, size_t* workspace_bytes)
 {
-    if (p.dtype != ULY_BF16) return ULY_EINVAL;
+    if (p.dtype != ULY_BF16 && p.dtype != ULY_F16) return ULY_EINVAL;
     if (!(p.d == 8 || p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128 || p.d == 256))
         return ULY_EINVAL;
     if (p.S >= (int64_t(1) << 24)) return ULY_EINVAL;  // positions must be exact in fp32
@@ -414,6 +416,8 @@ int fused_bwd_device(const Plan& p, void* const* dq_out, void* const* dk_out,
     }
     a.rms_w = rms_w;
     a.dw_part = static_cast<float*>(workspace);
+    a.elem_f16 = p.dtype == ULY_F16 ? 1 : 0;
+    a.rope_half = p.rope_half;
     a.eps = eps;
     a.stages = stages;
     a.stage_bytes = stage_bytes;
@@ -576,6 +580,13 @@ int ulysses_plan_set_chunk_bytes(ulysses_plan_t plan, int64_t max_chunk_bytes)
 {
     if (!plan || max_chunk_bytes < 1) return ULY_EINVAL;
     plan->p.chunk_cap = max_chunk_bytes;
+    return ULY_OK;
+}
+
+int ulysses_plan_set_rope_pairs(ulysses_plan_t plan, int pairs)
+{
+    if (!plan || (pairs != ULY_ROPE_ADJACENT && pairs != ULY_ROPE_HALF)) return ULY_EINVAL;
+    plan->p.rope_half = pairs == ULY_ROPE_HALF ? 1 : 0;
     return ULY_OK;
 }
 

@@ -36,6 +36,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/ulysses.h"
+#include "fused_row.cuh"
 #include "plan.h"
 #include "ptx.cuh"
 
@@ -147,15 +148,6 @@ struct FusedRing {
     }
 };
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
-{
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
-
 // cos and sin of 2 pi * frac(p * (hi + lo)), p a non-negative integer below 2^24.
 __device__ __forceinline__ float2 rope_cos_sin(float p, float hi, float lo)
 {
@@ -190,7 +182,9 @@ __host__ __device__ inline FusedSmem fused_smem_layout(int d, int tokens, int st
     return m;
 }
 
-template <int G>  // lanes per head row; d = 8 * G
+// G: lanes per head row (d = 8 G); F16: fp16 elements (else bf16); HALF_PAIRS: rotate-half RoPE
+// pairs (else adjacent pairs). The row layouts are in fused_row.cuh.
+template <int G, bool F16, bool HALF_PAIRS>
 __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     fused_qk_kernel(const __grid_constant__ FusedArgs a)
 {
@@ -336,16 +330,12 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     const int cwi = cw - which * HALF_NW;     // rank among the warps of this tensor
     const int sub = lane % G;                 // which 8 values of the row this lane holds
     const int group = lane / G;               // which head row of the warp slot
-    // This lane's 8 weights as packed pairs: even / odd elements of pairs (0,1) and (2,3), plus the
-    // negated odd ones (the rotation subtracts them).
+    using IO = RowIO<F16, HALF_PAIRS, D>;
+    // This lane's 8 weights as packed pairs: first / second elements of its pairs, plus the
+    // negated second ones (the rotation subtracts them).
     float2 wE[2], wO[2], wOn[2];
-    {
-        const float4* wp = reinterpret_cast<const float4*>(a.rms_w + which * D + sub * 8);
-        const float4 a0 = wp[0], a1 = wp[1];
-        wE[0] = make_float2(a0.x, a0.z); wO[0] = make_float2(a0.y, a0.w);
-        wE[1] = make_float2(a1.x, a1.z); wO[1] = make_float2(a1.y, a1.w);
-        for (int h = 0; h < 2; ++h) wOn[h] = make_float2(-wO[h].x, -wO[h].y);
-    }
+    IO::weights(a.rms_w + which * D, sub, wE, wO);
+    for (int h = 0; h < 2; ++h) wOn[h] = make_float2(-wO[h].x, -wO[h].y);
     const float inv_d = 1.0f / float(D);
     // this warp's share of the rows of a full token block (steps m_lo .. m_hi - 1 of PER_STEP
     // rows) and the (token, head) of its first row
@@ -379,7 +369,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
             uint8_t* slot[kIlp];
             int tok[kIlp];
             bool ok[kIlp];
-            // even / odd elements of pairs (0,1) and (2,3) of this lane's 8 values, packed
+            // first / second elements of this lane's pairs, packed
             float2 vE[kIlp][2], vO[kIlp][2];
             float ss[kIlp];
 #pragma unroll
@@ -391,14 +381,12 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
                     hh -= N;
                     ++tk;
                 }
-                slot[u] = rows_base + tk * tok_stride + hh * (D * 2) + sub * 16;
+                slot[u] = rows_base + tk * tok_stride + hh * (D * 2);
                 tok[u] = tk;
                 uint4 x = make_uint4(0, 0, 0, 0);
-                if (ok[u]) x = ld_shared_v4(slot[u]);
-                vE[u][0] = make_float2(bf16_lo(x.x), bf16_lo(x.y));
-                vO[u][0] = make_float2(bf16_hi(x.x), bf16_hi(x.y));
-                vE[u][1] = make_float2(bf16_lo(x.z), bf16_lo(x.w));
-                vO[u][1] = make_float2(bf16_hi(x.z), bf16_hi(x.w));
+                if (ok[u]) x = IO::load(slot[u], sub);
+                IO::unpack(x, 0, vE[u][0], vO[u][0]);
+                IO::unpack(x, 1, vE[u][1], vO[u][1]);
                 float2 acc = __fmul2_rn(vE[u][0], vE[u][0]);
                 acc = __ffma2_rn(vO[u][0], vO[u][0], acc);
                 acc = __ffma2_rn(vE[u][1], vE[u][1], acc);
@@ -415,22 +403,20 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
                 if (!ok[u]) continue;
                 const float inv = rsqrtf(ss[u] * inv_d + a.eps);
                 const float2 inv2 = make_float2(inv, inv);
-                uint32_t o4[4];
+                float2 oEs[2], oOs[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     // (c_j, c_j+1, s_j, s_j+1) for j = 4 sub + 2 h (see the table layout)
                     const float4 cs = table[(tok[u] * 2 + h) * G + sub];
                     const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
-                    const float2 A = __fmul2_rn(vE[u][h], wE[h]);   // weighted even elements
-                    const float2 Bp = __fmul2_rn(vO[u][h], wO[h]);  // weighted odd elements
+                    const float2 A = __fmul2_rn(vE[u][h], wE[h]);   // weighted first elements
+                    const float2 Bp = __fmul2_rn(vO[u][h], wO[h]);  // weighted second elements
                     const float2 Bn = __fmul2_rn(vO[u][h], wOn[h]);
                     // rotation, then the 1/rms factor (the rotation is linear)
-                    const float2 oE = __fmul2_rn(__ffma2_rn(Bn, s2, __fmul2_rn(A, c2)), inv2);
-                    const float2 oO = __fmul2_rn(__ffma2_rn(A, s2, __fmul2_rn(Bp, c2)), inv2);
-                    o4[2 * h] = pack_bf16(oE.x, oO.x);
-                    o4[2 * h + 1] = pack_bf16(oE.y, oO.y);
+                    oEs[h] = __fmul2_rn(__ffma2_rn(Bn, s2, __fmul2_rn(A, c2)), inv2);
+                    oOs[h] = __fmul2_rn(__ffma2_rn(A, s2, __fmul2_rn(Bp, c2)), inv2);
                 }
-                st_shared_v4(slot[u], make_uint4(o4[0], o4[1], o4[2], o4[3]));  // in place
+                IO::store(slot[u], sub, IO::pack(oEs, oOs));  // in place
             }
             base += PER_STEP;
             base_head += PER_STEP;
@@ -481,22 +467,33 @@ void fused_geometry(const Plan& p, int planes, int64_t* tokens_per_unit, int* st
     }
 }
 
-static int g_fused_smem_set[64];
+static unsigned g_fused_smem_set[64];
 
-template <int G>
+template <int G, bool F16, bool HALF>
 static cudaError_t launch_g(const FusedArgs& a, cudaStream_t stream, int device, int grid)
 {
-    constexpr int bit = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : G == 8 ? 3 : G == 16 ? 4 : 5;
-    if (device >= 0 && device < 64 && !(g_fused_smem_set[device] & (1 << bit))) {
-        cudaError_t e = cudaFuncSetAttribute(fused_qk_kernel<G>,
+    constexpr int gbit = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : G == 8 ? 3 : G == 16 ? 4 : 5;
+    constexpr unsigned bit = 1u << (gbit * 4 + (F16 ? 2 : 0) + (HALF ? 1 : 0));
+    if (device >= 0 && device < 64 && !(g_fused_smem_set[device] & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(fused_qk_kernel<G, F16, HALF>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemPerCtaMax);
         if (e != cudaSuccess) return e;
-        g_fused_smem_set[device] |= 1 << bit;
+        g_fused_smem_set[device] |= bit;
     }
     const FusedSmem m = fused_smem_layout(a.d, a.tokens_per_unit, a.stages, a.stage_bytes);
-    fused_qk_kernel<G><<<grid, kFusedThreads, m.total, stream>>>(a);
+    fused_qk_kernel<G, F16, HALF><<<grid, kFusedThreads, m.total, stream>>>(a);
     return cudaGetLastError();
+}
+
+template <int G>
+static cudaError_t launch_variant(const FusedArgs& a, cudaStream_t stream, int device, int grid)
+{
+    if (a.elem_f16)
+        return a.rope_half ? launch_g<G, true, true>(a, stream, device, grid)
+                           : launch_g<G, true, false>(a, stream, device, grid);
+    return a.rope_half ? launch_g<G, false, true>(a, stream, device, grid)
+                       : launch_g<G, false, false>(a, stream, device, grid);
 }
 
 cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count,
@@ -507,12 +504,12 @@ cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, in
     if (max_grid > 0 && grid > max_grid) grid = max_grid;
     if (grid > a.total_units) grid = a.total_units;
     switch (a.d / 8) {
-        case 1: return launch_g<1>(a, stream, device, int(grid));
-        case 2: return launch_g<2>(a, stream, device, int(grid));
-        case 4: return launch_g<4>(a, stream, device, int(grid));
-        case 8: return launch_g<8>(a, stream, device, int(grid));
-        case 16: return launch_g<16>(a, stream, device, int(grid));
-        case 32: return launch_g<32>(a, stream, device, int(grid));
+        case 1: return launch_variant<1>(a, stream, device, int(grid));
+        case 2: return launch_variant<2>(a, stream, device, int(grid));
+        case 4: return launch_variant<4>(a, stream, device, int(grid));
+        case 8: return launch_variant<8>(a, stream, device, int(grid));
+        case 16: return launch_variant<16>(a, stream, device, int(grid));
+        case 32: return launch_variant<32>(a, stream, device, int(grid));
         default: return cudaErrorInvalidValue;
     }
 }

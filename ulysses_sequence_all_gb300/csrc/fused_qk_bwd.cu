@@ -28,6 +28,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/ulysses.h"
+#include "fused_row.cuh"
 #include "plan.h"
 #include "ptx.cuh"
 
@@ -130,15 +131,6 @@ struct BwdRing {
     }
 };
 
-__device__ __forceinline__ float bwd_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bwd_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ uint32_t bwd_pack(float lo, float hi)
-{
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
-
 // cos and sin of 2 pi * frac(p * (hi + lo)), p a non-negative integer below 2^24; the angle is
 // reduced in turns with an error-free product (see the forward kernel).
 __device__ __forceinline__ float2 bwd_cos_sin(float p, float hi, float lo)
@@ -178,10 +170,13 @@ __host__ __device__ inline BwdSmem bwd_smem_layout(int d, int tokens, int stages
     return m;
 }
 
-template <int G>  // lanes per head row; d = 8 * G
+// G: lanes per head row (d = 8 G); F16: fp16 elements (else bf16); HALF_PAIRS: rotate-half RoPE
+// pairs (else adjacent pairs). The row layouts are in fused_row.cuh.
+template <int G, bool F16, bool HALF_PAIRS>
 __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
     fused_qk_bwd_kernel(const __grid_constant__ FusedBwdArgs a)
 {
+    using IO = RowIO<F16, HALF_PAIRS, 8 * G>;
     constexpr int D = 8 * G;
     constexpr int HALF = D / 2;
     constexpr int GPW = 32 / G;  // head rows per warp per slot
@@ -331,13 +326,13 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
             }
         }
         if (group == 0 && acc_t >= 0) {
-            float* row = red + (cw * 2 + acc_t) * D + sub * 8;
+            float* row = red + (cw * 2 + acc_t) * D;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                row[4 * h + 0] += aE[h].x;
-                row[4 * h + 1] += aO[h].x;
-                row[4 * h + 2] += aE[h].y;
-                row[4 * h + 3] += aO[h].y;
+                row[IO::col(sub, h, false, 0)] += aE[h].x;
+                row[IO::col(sub, h, true, 0)] += aO[h].x;
+                row[IO::col(sub, h, false, 1)] += aE[h].y;
+                row[IO::col(sub, h, true, 1)] += aO[h].y;
             }
         }
 #pragma unroll
@@ -355,15 +350,8 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
         }
         const BwdRecord rec = records[s];
         const int tt = rec.t_q & 1, ntok = rec.ntok;
-        float2 wE[2], wO[2];  // this lane's weights of the unit's tensor (even / odd elements)
-        {
-            const float4* wp = reinterpret_cast<const float4*>(wsm + tt * D + sub * 8);
-            const float4 a0 = wp[0], a1 = wp[1];
-            wE[0] = make_float2(a0.x, a0.z);
-            wO[0] = make_float2(a0.y, a0.w);
-            wE[1] = make_float2(a1.x, a1.z);
-            wO[1] = make_float2(a1.y, a1.w);
-        }
+        float2 wE[2], wO[2];  // this lane's weights of the unit's tensor (first / second elements)
+        IO::weights(wsm + tt * D, sub, wE, wO);
         uint8_t* xs = smem + L.stages + size_t(s) * a.stage_bytes;
         const uint8_t* gs = xs + grad_at;
         const float4* table = reinterpret_cast<const float4*>(smem + L.tables + s * L.table_bytes);
@@ -384,8 +372,8 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
         int base = m_lo * PER_STEP;  // first row of the current step and its (token, head)
         for (int m = m_lo; m < m_hi; ++m) {
             // The sums (mean square, <u * w, x>) need the whole row: u = R^T gy (8 fp32 values)
-            // and the raw bf16 words of x are kept across the reduction, then dx and the dw
-            // terms are formed.
+            // and the raw words of x are kept across the reduction, then dx and the dw terms are
+            // formed.
             int off[kBwdIlp];
             bool ok[kBwdIlp];
             uint4 xr[kBwdIlp];
@@ -400,22 +388,19 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
                     hh -= N;
                     ++tk;
                 }
-                off[u] = (base + o) * (D * 2) + sub * 16;  // row (tk, hh) of the unit
+                off[u] = (base + o) * (D * 2);  // row (tk, hh) of the unit
                 uint4 g = make_uint4(0, 0, 0, 0);
                 xr[u] = make_uint4(0, 0, 0, 0);
                 if (ok[u]) {
-                    xr[u] = ld_shared_v4(xs + off[u]);
-                    g = ld_shared_v4(gs + off[u]);
+                    xr[u] = IO::load(xs + off[u], sub);
+                    g = IO::load(gs + off[u], sub);
                 }
                 float2 acc_ss = make_float2(0.f, 0.f), acc_dp = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const uint32_t x0 = h ? xr[u].z : xr[u].x, x1 = h ? xr[u].w : xr[u].y;
-                    const uint32_t g0 = h ? g.z : g.x, g1 = h ? g.w : g.y;
-                    const float2 xE = make_float2(bwd_lo(x0), bwd_lo(x1));
-                    const float2 xO = make_float2(bwd_hi(x0), bwd_hi(x1));
-                    const float2 gE = make_float2(bwd_lo(g0), bwd_lo(g1));
-                    const float2 gO = make_float2(bwd_hi(g0), bwd_hi(g1));
+                    float2 xE, xO, gE, gO;  // first / second elements of the lane's pairs
+                    IO::unpack(xr[u], h, xE, xO);
+                    IO::unpack(g, h, gE, gO);
                     // (c_j, c_j+1, s_j, s_j+1) for j = 4 sub + 2 h
                     const float4 cs = table[(tk * 2 + h) * G + sub];
                     const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
@@ -445,20 +430,17 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
                 const float rr = rsqrtf(ss[u] * inv_d + a.eps);
                 const float kk = rr * rr * rr * dp[u] * inv_d;
                 const float2 r2 = make_float2(rr, rr), nk2 = make_float2(-kk, -kk);
-                uint32_t o4[4];
+                float2 dxE[2], dxO[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const uint32_t x0 = h ? xr[u].z : xr[u].x, x1 = h ? xr[u].w : xr[u].y;
-                    const float2 xE = make_float2(bwd_lo(x0), bwd_lo(x1));
-                    const float2 xO = make_float2(bwd_hi(x0), bwd_hi(x1));
-                    const float2 dxE = __ffma2_rn(__fmul2_rn(uE[u][h], wE[h]), r2, __fmul2_rn(xE, nk2));
-                    const float2 dxO = __ffma2_rn(__fmul2_rn(uO[u][h], wO[h]), r2, __fmul2_rn(xO, nk2));
+                    float2 xE, xO;
+                    IO::unpack(xr[u], h, xE, xO);
+                    dxE[h] = __ffma2_rn(__fmul2_rn(uE[u][h], wE[h]), r2, __fmul2_rn(xE, nk2));
+                    dxO[h] = __ffma2_rn(__fmul2_rn(uO[u][h], wO[h]), r2, __fmul2_rn(xO, nk2));
                     aE[h] = __ffma2_rn(uE[u][h], __fmul2_rn(xE, r2), aE[h]);
                     aO[h] = __ffma2_rn(uO[u][h], __fmul2_rn(xO, r2), aO[h]);
-                    o4[2 * h] = bwd_pack(dxE.x, dxO.x);
-                    o4[2 * h + 1] = bwd_pack(dxE.y, dxO.y);
                 }
-                st_shared_v4(xs + off[u], make_uint4(o4[0], o4[1], o4[2], o4[3]));  // in place
+                IO::store(xs + off[u], sub, IO::pack(dxE, dxO));  // in place
             }
             base += PER_STEP;
             base_head += PER_STEP;
@@ -539,22 +521,34 @@ void fused_bwd_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages,
     }
 }
 
-static int g_bwd_smem_set[64];
+static unsigned g_bwd_smem_set[64];
 
-template <int G>
+template <int G, bool F16, bool HALF>
 static cudaError_t bwd_launch_g(const FusedBwdArgs& a, cudaStream_t stream, int device, int grid)
 {
-    constexpr int bit = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : G == 8 ? 3 : G == 16 ? 4 : 5;
-    if (device >= 0 && device < 64 && !(g_bwd_smem_set[device] & (1 << bit))) {
-        cudaError_t e = cudaFuncSetAttribute(fused_qk_bwd_kernel<G>,
+    constexpr int gbit = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : G == 8 ? 3 : G == 16 ? 4 : 5;
+    constexpr unsigned bit = 1u << (gbit * 4 + (F16 ? 2 : 0) + (HALF ? 1 : 0));
+    if (device >= 0 && device < 64 && !(g_bwd_smem_set[device] & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(fused_qk_bwd_kernel<G, F16, HALF>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kBwdSmemPerCtaMax);
         if (e != cudaSuccess) return e;
-        g_bwd_smem_set[device] |= 1 << bit;
+        g_bwd_smem_set[device] |= bit;
     }
     const BwdSmem m = bwd_smem_layout(a.d, a.tokens_per_unit, a.stages, a.stage_bytes);
-    fused_qk_bwd_kernel<G><<<grid, kBwdThreads, m.total, stream>>>(a);
+    fused_qk_bwd_kernel<G, F16, HALF><<<grid, kBwdThreads, m.total, stream>>>(a);
     return cudaGetLastError();
+}
+
+template <int G>
+static cudaError_t bwd_launch_variant(const FusedBwdArgs& a, cudaStream_t stream, int device,
+                                      int grid)
+{
+    if (a.elem_f16)
+        return a.rope_half ? bwd_launch_g<G, true, true>(a, stream, device, grid)
+                           : bwd_launch_g<G, true, false>(a, stream, device, grid);
+    return a.rope_half ? bwd_launch_g<G, false, true>(a, stream, device, grid)
+                       : bwd_launch_g<G, false, false>(a, stream, device, grid);
 }
 
 // CTAs of the main kernel for a launch of `a` (the number of partial-sum slots it fills); at
@@ -575,12 +569,12 @@ cudaError_t fused_bwd_launch(const FusedBwdArgs& a, float* dw, bool accumulate, 
     if (grid > 0) {
         cudaError_t e;
         switch (a.d / 8) {
-            case 1: e = bwd_launch_g<1>(a, stream, device, int(grid)); break;
-            case 2: e = bwd_launch_g<2>(a, stream, device, int(grid)); break;
-            case 4: e = bwd_launch_g<4>(a, stream, device, int(grid)); break;
-            case 8: e = bwd_launch_g<8>(a, stream, device, int(grid)); break;
-            case 16: e = bwd_launch_g<16>(a, stream, device, int(grid)); break;
-            case 32: e = bwd_launch_g<32>(a, stream, device, int(grid)); break;
+            case 1: e = bwd_launch_variant<1>(a, stream, device, int(grid)); break;
+            case 2: e = bwd_launch_variant<2>(a, stream, device, int(grid)); break;
+            case 4: e = bwd_launch_variant<4>(a, stream, device, int(grid)); break;
+            case 8: e = bwd_launch_variant<8>(a, stream, device, int(grid)); break;
+            case 16: e = bwd_launch_variant<16>(a, stream, device, int(grid)); break;
+            case 32: e = bwd_launch_variant<32>(a, stream, device, int(grid)); break;
             default: return cudaErrorInvalidValue;
         }
         if (e != cudaSuccess) return e;

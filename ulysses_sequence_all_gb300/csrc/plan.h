@@ -18,6 +18,7 @@ struct Plan {
     int64_t seq_off[kMaxW + 1], head_off[kMaxW + 1];
     int64_t chunk_cap;  // max bytes one rank reads or writes per launch
     int64_t max_ctas;   // cap on the CTAs of any launch (0: none)
+    int rope_half;      // the fused calls' RoPE pairs: (j, j + d/2) when set, else (2j, 2j + 1)
 };
 
 // Rows of each sequence shard covered by one launch.
@@ -91,6 +92,8 @@ struct FusedArgs {
     uint8_t* k_out[kMaxW];
     uint8_t* v_out[kMaxW];
     int32_t interleaved;
+    int32_t elem_f16;   // elements are fp16 (else bf16)
+    int32_t rope_half;  // RoPE pairs (j, j + d/2) (else (2j, 2j + 1))
     const float* rms_w;  // [2][d]
     int64_t s[kMaxW], seq_off[kMaxW], n[kMaxW], head_off[kMaxW];
     int64_t row_lo[kMaxW], rows[kMaxW];
@@ -121,6 +124,8 @@ struct FusedBwdArgs {
     uint8_t* dx_out[2][kMaxW];      // gradients of the forward inputs: rank q's (b, s_q, N, d)
     const float* rms_w;             // [2][d]
     float* dw_part;                 // [grid][2][d]: one slot per CTA, fully written by it
+    int32_t elem_f16;               // elements are fp16 (else bf16)
+    int32_t rope_half;              // RoPE pairs (j, j + d/2) (else (2j, 2j + 1))
     int64_t s[kMaxW], seq_off[kMaxW], n[kMaxW], head_off[kMaxW + 1];
     int64_t row_lo[kMaxW], rows[kMaxW];
     int64_t block_begin[kMaxW + 1];  // prefix of token-block counts over q

@@ -213,6 +213,18 @@ __device__ __forceinline__ void fence_proxy_async_shared()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+__device__ __forceinline__ void st_shared_v2(void* p, uint32_t a, uint32_t b)
+{
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(smem_u32(p)), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ uint2 ld_shared_v2(const void* p)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p)));
+    return v;
+}
+
 __device__ __forceinline__ uint4 ld_shared_v4(const void* p)
 {
     uint4 v;
