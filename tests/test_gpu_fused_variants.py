@@ -205,3 +205,27 @@ def test_wan720p_f16_half_sampled(oracle):
             grow = oracle.decode(host_raw(gy[r][0, p, hg - head_off[r]]), 1)
             want_dx, _ = oracle.fused_row_bwd_var(oracle.decode(raw, 1), grow, 1, wn[t], EPS, p, THETA)
             _check(oracle, host_raw(dx[qr][0, i, hg]), want_dx, 1, 1e-4, f"bwd t{t} p{p}")
+
+
+def test_host_buffer_form_variant():
+    """The host-buffer form with fp16 elements and rotate-half pairs gives the device form's bytes."""
+    g = (5, 1, [30, 31, 29, 30, 30], [9, 8, 8, 8, 7], 128)
+    W, b, seq, heads, d = g
+    (q, k), w = _inputs(g, 1, seed=91)
+    plan = _plan(g, 1, 1)
+    qo = [torch.empty((b, sum(seq), n, d), dtype=torch.float16, device="cuda") for n in heads]
+    ko = [torch.empty_like(x) for x in qo]
+    B.ulysses_a2a_4d_qk_fused(plan, q, k, qo, ko, w, EPS, THETA)
+    hq = [x.cpu().pin_memory() for x in q]
+    hk = [x.cpu().pin_memory() for x in k]
+    hqo = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in qo]
+    hko = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in ko]
+    dq = [torch.empty_like(x) for x in q]
+    dk = [torch.empty_like(x) for x in k]
+    dqo = [torch.empty_like(x) for x in qo]
+    dko = [torch.empty_like(x) for x in ko]
+    B.ulysses_a2a_4d_qk_fused_host(plan, hq, hk, hqo, hko, dq, dk, dqo, dko, w, EPS, THETA)
+    torch.cuda.synchronize()
+    for a, c in zip(hqo + hko, qo + ko):
+        assert torch.equal(a.view(torch.int16), c.cpu().view(torch.int16))
+
