@@ -114,6 +114,35 @@ def test_fused_wan720p_sampled(oracle):
             check_close(oracle, oh[r][0, s, h], ref, f"{name} r={r} s={s} h={h}")
 
 
+def test_fused_long_sequence_sampled(oracle):
+    """The long packed-QKV geometry (W=4, 250,000 tokens, 56 heads, d=128: 896,000,000 bytes per
+    rank and tensor), positions up to 249,999: 1,000 sampled rows per tensor plus every head of
+    the last 16 positions, each against the oracle's single-row rule."""
+    cfg = wl.LONG_QKV
+    g = (cfg.W, cfg.b, list(cfg.seq_splits), list(cfg.head_splits), cfg.d)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(13)
+    q = [torch.randn((1, s, cfg.N, cfg.d), generator=gen, device="cuda").to(torch.bfloat16)
+         for s in cfg.seq_splits]
+    k = [torch.randn((1, s, cfg.N, cfg.d), generator=gen, device="cuda").to(torch.bfloat16)
+         for s in cfg.seq_splits]
+    w = wl.rms_weights(cfg.d, seed=14).cuda()
+    qo, ko = run_fused(g, q, k, w)
+    wn = w.cpu().numpy().astype(np.float64)
+    seq_off = np.cumsum([0] + list(cfg.seq_splits))
+    head_off = np.cumsum([0] + list(cfg.head_splits))
+    rng = np.random.default_rng(15)
+    picks = [(int(rng.integers(0, cfg.S)), int(rng.integers(0, cfg.N))) for _ in range(1000)]
+    picks += [(p, h) for p in range(cfg.S - 16, cfg.S) for h in range(cfg.N)]
+    for t, (xin, out) in enumerate(((q, qo), (k, ko))):
+        for p, hg in picks:
+            qr = int(np.searchsorted(seq_off, p, side="right") - 1)
+            r = int(np.searchsorted(head_off, hg, side="right") - 1)
+            raw = host_raw(xin[qr][0, p - seq_off[qr], hg])
+            ref = oracle.fused_row_var(raw, 0, 0, wn[t], EPS, p, THETA)
+            check_close(oracle, host_raw(out[r][0, p, hg - head_off[r]]), ref, f"t{t} p={p} h={hg}")
+
+
 def test_fused_chunked_equals_unchunked():
     g = (5, 2, [300, 310, 290, 305, 295], [9, 8, 8, 8, 7], 128)
     q, k, w = make_inputs(g, seed=9)

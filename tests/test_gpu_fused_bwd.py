@@ -178,6 +178,37 @@ def test_backward_wan720p_sampled(oracle):
             check_dx(oracle, host_raw(got[qr][0, i, hg]), ref, f"tensor {t} q={qr} i={i} h={hg}")
 
 
+def test_backward_long_sequence_sampled(oracle):
+    """The long packed-QKV geometry (W=4, 250,000 tokens, 56 heads, d=128), positions up to
+    249,999: 600 sampled rows of dq and of dk against the oracle's single-row backward."""
+    cfg = wl.LONG_QKV
+    g = (cfg.W, 1, list(cfg.seq_splits), list(cfg.head_splits), cfg.d)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(71)
+    bf = lambda shape: torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)  # noqa: E731
+    q = [bf((1, s, cfg.N, cfg.d)) for s in cfg.seq_splits]
+    k = [bf((1, s, cfg.N, cfg.d)) for s in cfg.seq_splits]
+    dq = [bf((1, cfg.S, n, cfg.d)) for n in cfg.head_splits]
+    dk = [bf((1, cfg.S, n, cfg.d)) for n in cfg.head_splits]
+    w = wl.rms_weights(cfg.d, seed=72).cuda()
+    dqo, dko, _ = run_bwd(g, q, k, dq, dk, w)
+    wn = w.cpu().numpy().astype(np.float64)
+    seq_off = np.cumsum([0] + list(cfg.seq_splits))
+    head_off = np.cumsum([0] + list(cfg.head_splits))
+    rng = np.random.default_rng(73)
+    for t, (x, gy, got) in enumerate(((q, dq, dqo), (k, dk, dko))):
+        for _ in range(300):
+            p = int(rng.integers(cfg.S - 2000, cfg.S)) if rng.random() < 0.5 else int(rng.integers(0, cfg.S))
+            hg = int(rng.integers(0, cfg.N))
+            qr = int(np.searchsorted(seq_off, p, side="right") - 1)
+            r = int(np.searchsorted(head_off, hg, side="right") - 1)
+            i = p - seq_off[qr]
+            xrow = oracle.bf16_to_double(host_raw(x[qr][0, i, hg]))
+            grow = oracle.bf16_to_double(host_raw(gy[r][0, p, hg - head_off[r]]))
+            ref, _ = oracle.fused_row_bwd(xrow, grow, wn[t], EPS, p, THETA)
+            check_dx(oracle, host_raw(got[qr][0, i, hg]), ref, f"tensor {t} p={p} h={hg}")
+
+
 def test_backward_wan720p_sparse_gradient(oracle):
     """Full size with the output gradient zero except on 2,000 random rows: every dx row without
     a gradient is exactly zero, the others match the oracle's row backward, and dw equals the
