@@ -396,7 +396,20 @@ def run_ours(args):
         torch.cuda.synchronize()
         if rep >= 3:
             bwd_ms.append(e0.elapsed_time(e1))
-    del dq, dk, dw, ws
+    # the backward of the interleaved form: packed dqkv from the three output gradients
+    qkv = [torch.stack([a, b, c], dim=2) for a, b, c in zip(wk.q, wk.k, wk.v)]
+    dqkv = [torch.empty_like(t) for t in qkv]
+    qkv_bwd_ms = []
+    for rep in range(min(args.steps, 20) + 3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        B.ulysses_a2a_4d_qkv_fused_backward(wk.plan, dqkv, qkv, wk.qo, wk.ko, wk.vo, wk.w, dw, EPS,
+                                            THETA, ws, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if rep >= 3:
+            qkv_bwd_ms.append(e0.elapsed_time(e1))
+    del dq, dk, dw, ws, qkv, dqkv
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -468,6 +481,13 @@ def run_ours(args):
             "median_ms": round(statistics.median(bwd_ms), 4),
             "GB/s": round(6 * wk.side / (statistics.median(bwd_ms) * 1e-3) / 1e9, 1),
             "frac_of_peak": round(6 * wk.side / (statistics.median(bwd_ms) * 1e-3) / 1e9 / peak, 4)},
+        "qkv_fused_backward": {
+            "note": "outside the step: the interleaved call's backward, packed dq, dk, dv (b, s, 3, "
+                    "N, d) from the three output gradients (2 launches); reads the q and k planes "
+                    "and three gradients, writes three planes",
+            "median_ms": round(statistics.median(qkv_bwd_ms), 4),
+            "GB/s": round(8 * wk.side / (statistics.median(qkv_bwd_ms) * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(8 * wk.side / (statistics.median(qkv_bwd_ms) * 1e-3) / 1e9 / peak, 4)},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

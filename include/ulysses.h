@@ -264,6 +264,26 @@ int ulysses_a2a_4d_qkv_fused(ulysses_plan_t plan, const void* const* qkv_in, voi
                              float rope_theta, void* stream);
 
 /*
+ * Backward of ulysses_a2a_4d_qkv_fused on the same plan (the pairing of the interleaved call, as
+ * ulysses_a2a_4d_qk_fused_backward is of the separate one): the gradient of the packed input
+ * (b, s_q, 3, N, d) from the gradients of the three outputs. Planes q and k receive the fused
+ * RMSNorm + RoPE vector-Jacobian product exactly as ulysses_a2a_4d_qk_fused_backward computes it;
+ * plane v receives the v gradient moved by mode 1 (bit-exact). One launch per chunk covers all
+ * three planes, plus the dw reduction.
+ *   dqkv_out        W device pointers, rank q's (b, s_q, 3, N, d) of the plan's dtype.
+ *   qkv_in          W device pointers, the forward's packed inputs (only planes q and k are read).
+ *   dq_in, dk_in, dv_in   W device pointers each, gradients of q_out, k_out, v_out, rank r's
+ *                   (b, S, n_r, d).
+ *   rms_w, dw, eps, rope_theta, workspace, plan requirements and errors: as
+ *   ulysses_a2a_4d_qk_fused_backward (the same workspace size).
+ */
+int ulysses_a2a_4d_qkv_fused_backward(ulysses_plan_t plan, void* const* dqkv_out,
+                                      const void* const* qkv_in, const void* const* dq_in,
+                                      const void* const* dk_in, const void* const* dv_in,
+                                      const float* rms_w, float* dw, float eps, float rope_theta,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * End-to-end form for host-resident data: copy each rank's input from host_in[k] to dev_in[k],
  * run the relayout, and copy each dev_out[k] back to host_out[k]. The work is cut into about
  * eight sequence chunks so that copies in and copies out overlap: chunk c is copied in and

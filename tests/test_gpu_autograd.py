@@ -83,3 +83,26 @@ def test_fused_gradients_match_the_backward_call(oracle):
             check_dx(oracle, host_raw(got[r].grad), ref_dx[r], f"autograd t{t} r{r}")
         check_dw(wr.grad[t].cpu().numpy(), ref_dw, n_rows, f"autograd dw {t}")
     assert B.ulysses_device_status() == 0
+
+
+def test_qkv_gradients_match_the_backward_call():
+    W, b, seq, heads, d = G
+    plan = B.ulysses_plan(*G, "bfloat16")
+    q, k, w = make_inputs(G, seed=19)
+    v, _, _ = make_inputs(G, seed=20)
+    qkv = [torch.stack([a, c, e], dim=2) for a, c, e in zip(q, k, v)]
+    gq, gk = make_grads(G, seed=21)
+    gv, _ = make_grads(G, seed=22)
+    xr = [x.clone().requires_grad_() for x in qkv]
+    wr = w.clone().requires_grad_()
+    qo, ko, vo = A.qkv_fused(plan, xr, wr, EPS, THETA)
+    torch.autograd.backward(qo + ko + vo, gq + gk + gv)
+    dqkv = [torch.empty_like(x) for x in qkv]
+    dw = torch.empty_like(w)
+    ws = torch.empty(B.ulysses_qk_fused_backward_workspace(plan), dtype=torch.uint8, device="cuda")
+    B.ulysses_a2a_4d_qkv_fused_backward(plan, dqkv, qkv, gq, gk, gv, w, dw, EPS, THETA, ws)
+    torch.cuda.synchronize()
+    for x, ref in zip(xr, dqkv):
+        assert torch.equal(x.grad.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(wr.grad.view(torch.int32), dw.view(torch.int32))
+

@@ -10,6 +10,8 @@ plan for the backward:
 * ``qk_fused(plan, q, k, rms_w, eps, rope_theta)``: the fused mode-0 call; its backward is
   ``ulysses_a2a_4d_qk_fused_backward`` (dq, dk and the gradient of ``rms_w``), with a workspace
   allocated by torch.
+* ``qkv_fused(plan, qkv, rms_w, eps, rope_theta)``: the interleaved packed-QKV call; its backward
+  is ``ulysses_a2a_4d_qkv_fused_backward`` (packed dqkv and the gradient of ``rms_w``).
 
 Inputs and outputs are lists of W tensors (one per virtual rank) on the current CUDA device;
 the outputs are new tensors the caller owns. Nothing here computes: every step runs in the
@@ -100,6 +102,43 @@ class _QKFused(torch.autograd.Function):
         B.ulysses_a2a_4d_qk_fused_backward(plan, dq, dk, q, k, gq, gk, rms_w, dw, ctx.eps,
                                            ctx.theta, ws)
         return (None, None, None, dw, *dq, *dk)
+
+
+class _QKVFused(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, plan, eps, rope_theta, rms_w, *qkv):
+        qkv = [x.contiguous() for x in qkv]
+        rms_w = rms_w.contiguous()
+        like = qkv[0]
+        qo, ko, vo = _empty(plan, 0, like), _empty(plan, 0, like), _empty(plan, 0, like)
+        B.ulysses_a2a_4d_qkv_fused(plan, qkv, qo, ko, vo, rms_w, eps, rope_theta)
+        ctx.plan, ctx.eps, ctx.theta, ctx.W = plan, eps, rope_theta, len(qkv)
+        ctx.save_for_backward(rms_w, *qkv)
+        return tuple(qo + ko + vo)
+
+    @staticmethod
+    def backward(ctx, *grads):
+        plan, W = ctx.plan, ctx.W
+        rms_w, *qkv = ctx.saved_tensors
+        like = qkv[0]
+        gq = _grads(grads[:W], plan, 0, like)
+        gk = _grads(grads[W:2 * W], plan, 0, like)
+        gv = _grads(grads[2 * W:], plan, 0, like)
+        dqkv = [torch.empty_like(x) for x in qkv]
+        dw = torch.empty_like(rms_w, dtype=torch.float32)
+        ws = torch.empty(B.ulysses_qk_fused_backward_workspace(plan), dtype=torch.uint8,
+                         device=like.device)
+        B.ulysses_a2a_4d_qkv_fused_backward(plan, dqkv, qkv, gq, gk, gv, rms_w, dw, ctx.eps,
+                                            ctx.theta, ws)
+        return (None, None, None, dw, *dqkv)
+
+
+def qkv_fused(plan: B.Plan, qkv, rms_w: torch.Tensor, eps: float, rope_theta: float):
+    """The interleaved call on packed (b, s_q, 3, N, d) inputs, differentiable in qkv and rms_w.
+    Returns (q_out, k_out, v_out), lists of W tensors."""
+    out = _QKVFused.apply(plan, eps, rope_theta, rms_w, *qkv)
+    W = len(qkv)
+    return list(out[:W]), list(out[W:2 * W]), list(out[2 * W:])
 
 
 def qk_fused(plan: B.Plan, q, k, rms_w: torch.Tensor, eps: float, rope_theta: float):

@@ -31,6 +31,7 @@ EXPORTS = ["ulysses_plan", "ulysses_plan_destroy", "ulysses_plan_set_chunk_bytes
            "ulysses_a2a_4d", "ulysses_a2a_4d_engine", "ulysses_a2a_4d_qk_fused",
            "ulysses_a2a_4d_qkv_fused", "ulysses_a2a_4d_qk_fused_backward",
            "ulysses_qk_fused_backward_workspace", "ulysses_a2a_4d_qk_fused_backward_static",
+           "ulysses_a2a_4d_qkv_fused_backward",
            "ulysses_a2a_4d_host", "ulysses_a2a_4d_qk_fused_host", "ulysses_device_status",
            "ulysses_selftest_wait_timeout", "ulysses_last_cuda_error", "ulysses_strerror",
            "ulysses_version"]
@@ -79,6 +80,9 @@ def _lib():
                                                          ctypes.c_float, ctypes.c_float, _p,
                                                          ctypes.c_size_t, _p]
         lib.ulysses_qk_fused_backward_workspace.argtypes = [_p, ctypes.POINTER(ctypes.c_size_t)]
+        lib.ulysses_a2a_4d_qkv_fused_backward.argtypes = [_p, _pp, _pp, _pp, _pp, _pp, _p, _p,
+                                                          ctypes.c_float, ctypes.c_float, _p,
+                                                          ctypes.c_size_t, _p]
         lib.ulysses_a2a_4d_qk_fused_backward_static.argtypes = [_p, _pp, _pp, _pp, _pp, _pp, _pp,
                                                                 _p, _p, ctypes.c_float,
                                                                 ctypes.c_float, _p]
@@ -236,6 +240,15 @@ def ulysses_a2a_4d_qk_fused_backward(plan: Plan, dq_out, dk_out, q_in, k_in, dq_
         plan, _ptrs(dq_out), _ptrs(dk_out), _ptrs(q_in), _ptrs(k_in), _ptrs(dq_in), _ptrs(dk_in),
         _addr(rms_w), _addr(dw), eps, rope_theta, _addr(workspace), _nbytes(workspace),
         _stream(stream)), "ulysses_a2a_4d_qk_fused_backward")
+
+
+def ulysses_a2a_4d_qkv_fused_backward(plan: Plan, dqkv_out, qkv_in, dq_in, dk_in, dv_in, rms_w,
+                                      dw, eps: float, rope_theta: float, workspace, stream=None):
+    """Backward of the interleaved QKV call into packed (b, s_q, 3, N, d) gradients."""
+    _check(_lib().ulysses_a2a_4d_qkv_fused_backward(
+        plan, _ptrs(dqkv_out), _ptrs(qkv_in), _ptrs(dq_in), _ptrs(dk_in), _ptrs(dv_in),
+        _addr(rms_w), _addr(dw), eps, rope_theta, _addr(workspace), _nbytes(workspace),
+        _stream(stream)), "ulysses_a2a_4d_qkv_fused_backward")
 
 
 def ulysses_a2a_4d_qk_fused_backward_static(plan: Plan, dq_out, dk_out, q_in, k_in, dq_in, dk_in,

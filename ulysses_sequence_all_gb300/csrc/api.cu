@@ -352,6 +352,46 @@ int fused_bwd_setup(const Plan& p, const DeviceInfo& dev, int64_t* tokens_per_un
     return ULY_OK;
 }
 
+// The launches of a backward whose pointers, tensor count and token stride are set in `a`.
+int fused_bwd_run(const Plan& p, FusedBwdArgs& a, const DeviceInfo& dev, int64_t T, int stages,
+                  uint32_t stage_bytes, int ctas_per_sm, const float* rms_w, float* dw, float eps,
+                  float rope_theta, void* workspace, cudaStream_t stream)
+{
+    int64_t C = 0;
+    int rc = num_chunks(p, &C);
+    if (rc) return rc;
+    a.rms_w = rms_w;
+    a.dw_part = static_cast<float*>(workspace);
+    a.elem_f16 = p.dtype == ULY_F16 ? 1 : 0;
+    a.rope_half = p.rope_half;
+    a.eps = eps;
+    a.stages = stages;
+    a.stage_bytes = stage_bytes;
+    a.ctas_per_sm = ctas_per_sm;
+    rope_turns(p.d, double(rope_theta), a.turn_hi, a.turn_lo);
+    for (int64_t c = 0; c < C; ++c) {
+        ChunkRows rows;
+        chunk_rows(p, C, c, &rows);
+        build_fused_bwd_units(p, rows, T, &a);
+        cudaError_t e = fused_bwd_launch(a, dw, c > 0, stream, dev.device, dev.sm_count, p.max_ctas);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return ULY_OK;
+}
+
+// Checks shared by both backward forms: plan, scalars, weights, dw and workspace.
+int fused_bwd_common(const Plan& p, const DeviceInfo& dev, const float* rms_w, float* dw,
+                     float eps, float rope_theta, void* workspace, size_t workspace_bytes,
+                     int64_t* T, int* stages, uint32_t* stage_bytes, int* ctas_per_sm, size_t* need)
+{
+    int rc = fused_bwd_setup(p, dev, T, stages, stage_bytes, ctas_per_sm, need);
+    if (rc) return rc;
+    if (!(eps >= 0.0f) || !(rope_theta > 0.0f)) return ULY_EINVAL;
+    if (!rms_w || !dw || !workspace || workspace_bytes < *need) return ULY_EINVAL;
+    if (!aligned16(rms_w) || !aligned16(dw) || !aligned16(workspace)) return ULY_EALIGN;
+    return ULY_OK;
+}
+
 int fused_bwd_device(const Plan& p, void* const* dq_out, void* const* dk_out,
                      const void* const* q_in, const void* const* k_in, const void* const* dq_in,
                      const void* const* dk_in, const float* rms_w, float* dw, float eps,
@@ -364,10 +404,9 @@ int fused_bwd_device(const Plan& p, void* const* dq_out, void* const* dk_out,
     int stages = 0, ctas_per_sm = 1;
     uint32_t stage_bytes = 0;
     size_t need = 0;
-    if ((rc = fused_bwd_setup(p, dev, &T, &stages, &stage_bytes, &ctas_per_sm, &need))) return rc;
-    if (!(eps >= 0.0f) || !(rope_theta > 0.0f)) return ULY_EINVAL;
-    if (!rms_w || !dw || !workspace || workspace_bytes < need) return ULY_EINVAL;
-    if (!aligned16(rms_w) || !aligned16(dw) || !aligned16(workspace)) return ULY_EALIGN;
+    if ((rc = fused_bwd_common(p, dev, rms_w, dw, eps, rope_theta, workspace, workspace_bytes, &T,
+                               &stages, &stage_bytes, &ctas_per_sm, &need)))
+        return rc;
     int64_t seq_b[kMaxW], head_b[kMaxW];
     side_bytes(p, 0, seq_b, head_b);
     if ((rc = check_ptrs(q_in, seq_b, p.W)) || (rc = check_ptrs(k_in, seq_b, p.W)) ||
@@ -402,8 +441,6 @@ int fused_bwd_device(const Plan& p, void* const* dq_out, void* const* dk_out,
     outs[n_out] = workspace;
     outs_b[n_out++] = int64_t(need);
     if ((rc = check_overlap(ins, ins_b, n_in, outs, outs_b, n_out))) return rc;
-    int64_t C = 0;
-    if ((rc = num_chunks(p, &C))) return rc;
     FusedBwdArgs a;
     std::memset(&a, 0, sizeof a);
     for (int k = 0; k < p.W; ++k) {
@@ -414,23 +451,79 @@ int fused_bwd_device(const Plan& p, void* const* dq_out, void* const* dk_out,
         a.dx_out[0][k] = static_cast<uint8_t*>(dq_out[k]);
         a.dx_out[1][k] = static_cast<uint8_t*>(dk_out[k]);
     }
-    a.rms_w = rms_w;
-    a.dw_part = static_cast<float*>(workspace);
-    a.elem_f16 = p.dtype == ULY_F16 ? 1 : 0;
-    a.rope_half = p.rope_half;
-    a.eps = eps;
-    a.stages = stages;
-    a.stage_bytes = stage_bytes;
-    a.ctas_per_sm = ctas_per_sm;
-    rope_turns(p.d, double(rope_theta), a.turn_hi, a.turn_lo);
-    for (int64_t c = 0; c < C; ++c) {
-        ChunkRows rows;
-        chunk_rows(p, C, c, &rows);
-        build_fused_bwd_units(p, rows, T, &a);
-        cudaError_t e = fused_bwd_launch(a, dw, c > 0, stream, dev.device, dev.sm_count, p.max_ctas);
-        if (e != cudaSuccess) return cuda_fail(e);
+    a.tensors = 2;
+    a.tok_stride = int32_t(p.N * p.d * p.e);
+    return fused_bwd_run(p, a, dev, T, stages, stage_bytes, ctas_per_sm, rms_w, dw, eps,
+                         rope_theta, workspace, stream);
+}
+
+// The backward of the interleaved QKV call: dq, dk (the fused VJP) and dv (mode 1) written into
+// one (b, s_q, 3, N, d) tensor per rank.
+int qkv_bwd_device(const Plan& p, void* const* dqkv_out, const void* const* qkv_in,
+                   const void* const* dq_in, const void* const* dk_in, const void* const* dv_in,
+                   const float* rms_w, float* dw, float eps, float rope_theta, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream)
+{
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    int64_t T = 0;
+    int stages = 0, ctas_per_sm = 1;
+    uint32_t stage_bytes = 0;
+    size_t need = 0;
+    if ((rc = fused_bwd_common(p, dev, rms_w, dw, eps, rope_theta, workspace, workspace_bytes, &T,
+                               &stages, &stage_bytes, &ctas_per_sm, &need)))
+        return rc;
+    int64_t seq_b[kMaxW], head_b[kMaxW], qkv_b[kMaxW];
+    side_bytes(p, 0, seq_b, head_b);
+    for (int k = 0; k < p.W; ++k) qkv_b[k] = 3 * seq_b[k];
+    if ((rc = check_ptrs(qkv_in, qkv_b, p.W)) || (rc = check_ptrs(dq_in, head_b, p.W)) ||
+        (rc = check_ptrs(dk_in, head_b, p.W)) || (rc = check_ptrs(dv_in, head_b, p.W)) ||
+        (rc = check_ptrs(const_cast<const void* const*>(dqkv_out), qkv_b, p.W)))
+        return rc;
+    const void* ins[4 * kMaxW + 1];
+    int64_t ins_b[4 * kMaxW + 1];
+    const void* outs[kMaxW + 2];
+    int64_t outs_b[kMaxW + 2];
+    int n_in = 0, n_out = 0;
+    for (int k = 0; k < p.W; ++k) {
+        ins[n_in] = qkv_in[k];
+        ins_b[n_in++] = qkv_b[k];
+        ins[n_in] = dq_in[k];
+        ins_b[n_in++] = head_b[k];
+        ins[n_in] = dk_in[k];
+        ins_b[n_in++] = head_b[k];
+        ins[n_in] = dv_in[k];
+        ins_b[n_in++] = head_b[k];
+        outs[n_out] = dqkv_out[k];
+        outs_b[n_out++] = qkv_b[k];
     }
-    return ULY_OK;
+    ins[n_in] = rms_w;
+    ins_b[n_in++] = 2 * p.d * int64_t(sizeof(float));
+    outs[n_out] = dw;
+    outs_b[n_out++] = 2 * p.d * int64_t(sizeof(float));
+    outs[n_out] = workspace;
+    outs_b[n_out++] = int64_t(need);
+    if ((rc = check_overlap(ins, ins_b, n_in, outs, outs_b, n_out))) return rc;
+    const int64_t row = p.N * p.d * p.e;  // one token's heads of one plane
+    FusedBwdArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int k = 0; k < p.W; ++k) {
+        const uint8_t* in = static_cast<const uint8_t*>(qkv_in[k]);
+        uint8_t* out = static_cast<uint8_t*>(dqkv_out[k]);
+        a.x_in[0][k] = in ? in : nullptr;
+        a.x_in[1][k] = in ? in + row : nullptr;
+        a.dx_out[0][k] = out ? out : nullptr;
+        a.dx_out[1][k] = out ? out + row : nullptr;
+        a.dx_out[2][k] = out ? out + 2 * row : nullptr;
+        a.g_in[0][k] = static_cast<const uint8_t*>(dq_in[k]);
+        a.g_in[1][k] = static_cast<const uint8_t*>(dk_in[k]);
+        a.g_in[2][k] = static_cast<const uint8_t*>(dv_in[k]);
+    }
+    a.tensors = 3;
+    a.tok_stride = int32_t(3 * row);
+    return fused_bwd_run(p, a, dev, T, stages, stage_bytes, ctas_per_sm, rms_w, dw, eps,
+                         rope_theta, workspace, stream);
 }
 
 // ---- backward with library-owned scratch ----------------------------------------------------------
@@ -674,6 +767,17 @@ int ulysses_a2a_4d_qk_fused_backward(ulysses_plan_t plan, void* const* dq_out, v
     if (!plan) return ULY_EINVAL;
     return fused_bwd_device(plan->p, dq_out, dk_out, q_in, k_in, dq_in, dk_in, rms_w, dw, eps,
                             rope_theta, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int ulysses_a2a_4d_qkv_fused_backward(ulysses_plan_t plan, void* const* dqkv_out,
+                                      const void* const* qkv_in, const void* const* dq_in,
+                                      const void* const* dk_in, const void* const* dv_in,
+                                      const float* rms_w, float* dw, float eps, float rope_theta,
+                                      void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (!plan || !qkv_in || !dqkv_out || !dq_in || !dk_in || !dv_in) return ULY_EINVAL;
+    return qkv_bwd_device(plan->p, dqkv_out, qkv_in, dq_in, dk_in, dv_in, rms_w, dw, eps,
+                          rope_theta, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 int ulysses_a2a_4d_qk_fused_backward_static(ulysses_plan_t plan, void* const* dq_out,

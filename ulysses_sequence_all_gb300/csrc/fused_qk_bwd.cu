@@ -70,7 +70,7 @@ constexpr int kBwdThreads = 32 * (kBwdFirstConsumer + kBwdNW);
 constexpr int kBwdConsumerBarrier = 1;  // named barrier of the consumer warps (0: __syncthreads)
 
 struct BwdUnit {
-    int t;  // 0: q, 1: k
+    int t;  // 0: q, 1: k, 2: v (interleaved QKV only)
     int q;
     int64_t bb, i0;
     int ntok;
@@ -80,7 +80,7 @@ struct BwdUnit {
 // before it arrives on "full" (the loader decodes each unit once).
 struct BwdRecord {
     int64_t seq_row0;  // first row (token) of the unit in rank q's (b, s_q) sequence side
-    int32_t t_q;       // tensor (bit 0) and shard q (bits 1..)
+    int32_t t_q;       // tensor (bits 0-1) and shard q (bits 2..)
     int32_t ntok;
 };
 
@@ -96,8 +96,8 @@ __device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity)
 __device__ __forceinline__ BwdUnit bwd_decode(const FusedBwdArgs& a, int64_t u)
 {
     BwdUnit x;
-    x.t = int(u & 1);
-    const int64_t blk_id = u >> 1;
+    const int64_t blk_id = a.tensors == 2 ? (u >> 1) : div_fast(u, a.tensors);
+    x.t = int(u - blk_id * a.tensors);
     int lo = 0, hi = a.W - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -209,10 +209,14 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
     __syncthreads();
     const int row_bytes = N * D * 2;                // one token, all heads, one tensor
     const uint32_t grad_at = a.stage_bytes / 2;     // the gradient runs' offset in a stage
+    const bool packed_rows = a.tok_stride == row_bytes;  // a block's rows are one span
 
     if (warp == kBwdLoaderWarp) {
-        // Per unit: lane 0 the input span; then one copy per (token, rank) of the gradient, so
-        // that the gradient rows land in the input's (token, head) order, grad_at bytes further.
+        // Per unit: lane 0 the input span (one copy per token when the tokens are interleaved
+        // with other planes); then one copy per (token, rank) of the gradient, so that the
+        // gradient rows land in the input's (token, head) order, grad_at bytes further. A v unit
+        // (interleaved QKV) has no input: its gradient rows land at the start of the stage and
+        // leave unchanged (mode 1).
         int64_t j = 0;
         BwdRing ring;
         for (; j < n; ++j, ring.next(K)) {
@@ -225,25 +229,33 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
                 break;
             }
             const BwdUnit t = bwd_decode(a, first + j * step);
+            const bool is_v = t.t == 2;
             const uint32_t span = uint32_t(t.ntok) * uint32_t(row_bytes);
             uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
+            const int64_t tok0 = t.bb * a.s[t.q] + t.i0;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&full[s], 2 * span);
-                const int64_t tok0 = t.bb * a.s[t.q] + t.i0;
-                bulk_g2s(dst, a.x_in[t.t][t.q] + tok0 * row_bytes, span, &full[s]);
+                mbar_arrive_expect_tx(&full[s], is_v ? span : 2 * span);
+                if (!is_v && packed_rows)
+                    bulk_g2s(dst, a.x_in[t.t][t.q] + tok0 * row_bytes, span, &full[s]);
                 BwdRecord& rec = records[s];  // published by this lane's arrive below
                 rec.seq_row0 = tok0;
-                rec.t_q = t.t | (t.q << 1);
+                rec.t_q = t.t | (t.q << 2);
                 rec.ntok = t.ntok;
             }
             __syncwarp();
+            if (!is_v && !packed_rows) {
+                for (int tok = lane; tok < t.ntok; tok += 32)
+                    bulk_g2s(dst + tok * row_bytes, a.x_in[t.t][t.q] + (tok0 + tok) * a.tok_stride,
+                             uint32_t(row_bytes), &full[s]);
+            }
+            uint8_t* gdst = is_v ? dst : dst + grad_at;
             const int64_t row0 = t.bb * a.S + a.seq_off[t.q] + t.i0;  // first head-side row
             const int copies = t.ntok * a.W;
             for (int c = lane; c < copies; c += 32) {
                 const int tok = c / a.W, r = c - tok * a.W;
                 const int64_t run = a.n[r] * (D * 2);  // bytes per token on rank r
                 if (run == 0) continue;
-                bulk_g2s(dst + grad_at + tok * row_bytes + int(a.head_off[r]) * (D * 2),
+                bulk_g2s(gdst + tok * row_bytes + int(a.head_off[r]) * (D * 2),
                          a.g_in[t.t][r] + (row0 + tok) * run, uint32_t(run), &full[s]);
             }
             // While the copies fly, the lanes fill the stage's cos/sin table for the unit's
@@ -253,7 +265,7 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
             // j = 4i and 4i+2; all lanes' entries for j = 4i come first, then those for 4i+2.
             float* table = reinterpret_cast<float*>(smem + L.tables + s * L.table_bytes);
             const float p0 = float(a.seq_off[t.q] + t.i0);
-            for (int e = lane; e < t.ntok * HALF; e += 32) {
+            for (int e = lane; e < (is_v ? 0 : t.ntok * HALF); e += 32) {
                 const int tok = e / HALF, jj = e % HALF;
                 const float2 tj = turns[jj];
                 const float2 cs = bwd_cos_sin(p0 + float(tok), tj.x, tj.y);
@@ -275,7 +287,7 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
         return;
     }
 
-    if (warp == kBwdStorerWarp) {  // one bulk store of dx per unit, then the stage is free
+    if (warp == kBwdStorerWarp) {  // the unit's dx rows (one store, or one per token), then free
         if (lane != 0) return;
         BwdRing ring;
         for (int64_t j = 0; j < n; ++j, ring.next(K)) {
@@ -285,8 +297,14 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
                 break;
             }
             const BwdRecord rec = records[s];
-            bulk_s2g(a.dx_out[rec.t_q & 1][rec.t_q >> 1] + rec.seq_row0 * row_bytes,
-                     smem + L.stages + size_t(s) * a.stage_bytes, uint32_t(rec.ntok) * uint32_t(row_bytes));
+            uint8_t* out = a.dx_out[rec.t_q & 3][rec.t_q >> 2] + rec.seq_row0 * a.tok_stride;
+            const uint8_t* st = smem + L.stages + size_t(s) * a.stage_bytes;
+            if (packed_rows) {
+                bulk_s2g(out, st, uint32_t(rec.ntok) * uint32_t(row_bytes));
+            } else {
+                for (int tok = 0; tok < rec.ntok; ++tok)
+                    bulk_s2g(out + int64_t(tok) * a.tok_stride, st + tok * row_bytes, uint32_t(row_bytes));
+            }
             bulk_commit();
             bulk_wait_read<0>();
             mbar_arrive(&empty[s]);
@@ -349,7 +367,13 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
             break;
         }
         const BwdRecord rec = records[s];
-        const int tt = rec.t_q & 1, ntok = rec.ntok;
+        const int tt = rec.t_q & 3, ntok = rec.ntok;
+        if (tt == 2) {  // a v unit: its rows leave as they came (mode 1)
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&computed[s]);
+            continue;
+        }
         float2 wE[2], wO[2];  // this lane's weights of the unit's tensor (first / second elements)
         IO::weights(wsm + tt * D, sub, wE, wO);
         uint8_t* xs = smem + L.stages + size_t(s) * a.stage_bytes;

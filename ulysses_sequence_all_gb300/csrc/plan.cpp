@@ -254,7 +254,7 @@ void build_fused_bwd_units(const Plan& p, const ChunkRows& rows, int64_t tokens_
     }
     a->head_off[kMaxW] = p.N;
     a->block_begin[kMaxW] = blocks;
-    a->total_units = 2 * blocks;
+    a->total_units = int64_t(a->tensors) * blocks;
 }
 
 // theta^(-2j/d) expressed in turns (divided by 2 pi), split into a float pair whose sum carries

@@ -114,14 +114,19 @@ void build_fused_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_
 
 // ---- fused QK backward's argument block -------------------------------------------------------
 // A token block is tokens_per_unit consecutive rows (tokens) of one shard q and one batch index;
-// it makes two work units, one per tensor (even unit q, odd unit k). A unit reads the tensor's
+// it makes one work unit per tensor (unit u: tensor u mod tensors). A unit reads the tensor's
 // forward input for those tokens (all N heads: one contiguous span on the sequence side) and the
 // gradient of its output (W runs, rank r's n_r heads of those tokens, contiguous on rank r's head
 // side), and writes the gradient of the input (one span on the sequence side).
+// For the interleaved QKV call (tensors = 3) the forward input and the gradient are
+// (b, s_q, 3, N, d): x_in / dx_out point at a rank's plane (q, k, v) and consecutive tokens are
+// tok_stride = 3 N d e bytes apart; units of tensor 2 (v) only gather g_in[2] (mode 1).
 struct FusedBwdArgs {
     const uint8_t* x_in[2][kMaxW];  // forward inputs q, k: rank q's (b, s_q, N, d) bf16
-    const uint8_t* g_in[2][kMaxW];  // gradients of the forward outputs: rank r's (b, S, n_r, d)
-    uint8_t* dx_out[2][kMaxW];      // gradients of the forward inputs: rank q's (b, s_q, N, d)
+    const uint8_t* g_in[3][kMaxW];  // gradients of the forward outputs: rank r's (b, S, n_r, d)
+    uint8_t* dx_out[3][kMaxW];      // gradients of the forward inputs: rank q's (b, s_q, N, d)
+    int32_t tensors;                // 2 (q, k) or 3 (interleaved q, k, v)
+    int32_t tok_stride;             // bytes between consecutive tokens of x_in / dx_out
     const float* rms_w;             // [2][d]
     float* dw_part;                 // [grid][2][d]: one slot per CTA, fully written by it
     int32_t elem_f16;               // elements are fp16 (else bf16)
@@ -131,7 +136,7 @@ struct FusedBwdArgs {
     int64_t block_begin[kMaxW + 1];  // prefix of token-block counts over q
     int64_t blocks[kMaxW];           // token blocks per batch index of shard q
     int64_t S, N, b;
-    int64_t total_units;  // two per token block
+    int64_t total_units;  // `tensors` per token block
     int32_t W, d, tokens_per_unit, stages;
     int32_t ctas_per_sm;
     uint32_t stage_bytes;  // forward input then output gradient of tokens_per_unit tokens
