@@ -99,10 +99,16 @@ MUTANTS = {
 CHILD = r"""
 import json, sys
 sys.path.insert(0, {tests!r}); sys.path.insert(0, {root!r})
+import torch
+torch.set_num_threads(1)
 import oracle, oracle_pins
 orc = oracle.Oracle({lib!r})
 print(json.dumps(oracle_pins.run_all(orc, quick=True)))
 """
+
+
+# the children run side by side: one thread each, so that they do not oversubscribe the cores
+_CHILD_ENV = dict(os.environ, OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
 
 
 def _check(name, tmpdir):
@@ -116,7 +122,11 @@ def _check(name, tmpdir):
         f.write(src)
     lib = oracle_pkg.build(os.path.join(tmpdir, f"lib{name}.so"), c_path)
     code = CHILD.format(tests=TESTS, root=os.path.dirname(TESTS), lib=lib)
-    proc = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    try:
+        proc = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                              timeout=1200, env=_CHILD_ENV)
+    except subprocess.TimeoutExpired:
+        return name, []  # not caught: reported by name below
     if proc.returncode != 0:
         return name, ["crashed"]
     return name, json.loads(proc.stdout.strip().splitlines()[-1])
@@ -133,7 +143,8 @@ def test_unmutated_copy_passes(tmp_path):
     """The same child-process harness on an unmodified copy reports no failure."""
     lib = oracle_pkg.build(os.path.join(str(tmp_path), "libclean.so"))
     code = CHILD.format(tests=TESTS, root=os.path.dirname(TESTS), lib=lib)
-    proc = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    proc = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                          timeout=1200, env=_CHILD_ENV)
     assert proc.returncode == 0, proc.stderr[-2000:]
     assert json.loads(proc.stdout.strip().splitlines()[-1]) == []
 
