@@ -40,10 +40,17 @@ static __device__ unsigned g_relayout_status;
 #ifndef ULY_VEC_UNROLL
 #define ULY_VEC_UNROLL 4
 #endif
-#ifndef ULY_TMA_LOOKAHEAD
-#define ULY_TMA_LOOKAHEAD 3
+// Loads in flight ahead of the unit being stored, per mode. Mode 0 loads one long span and stores
+// many short runs; mode 1 gathers short runs and stores one span, and measures faster with more of
+// the ring left to store groups (at the Wan shape: 6,020 GB/s with 3 loads ahead, 6,360 with 2).
+#ifndef ULY_TMA_LOOKAHEAD0
+#define ULY_TMA_LOOKAHEAD0 3
 #endif
-static_assert(ULY_TMA_LOOKAHEAD >= 1 && ULY_TMA_LOOKAHEAD <= ULY_TMA_STAGES, "lookahead <= stages");
+#ifndef ULY_TMA_LOOKAHEAD1
+#define ULY_TMA_LOOKAHEAD1 2
+#endif
+static_assert(ULY_TMA_LOOKAHEAD0 >= 1 && ULY_TMA_LOOKAHEAD0 <= ULY_TMA_STAGES, "lookahead <= stages");
+static_assert(ULY_TMA_LOOKAHEAD1 >= 1 && ULY_TMA_LOOKAHEAD1 <= ULY_TMA_STAGES, "lookahead <= stages");
 static_assert(ULY_TMA_STAGES <= 16, "stage barriers must fit the barrier area");
 constexpr int kTmaBarrierBytes = 128;  // the stage barriers sit before the first stage
 constexpr int kVecThreads = 256;
@@ -55,11 +62,11 @@ constexpr int kVecThreads = 256;
 // stores it has just issued. Every wait is bounded and its outcome is made uniform across the
 // warp (a lane that timed out stops them all); on a timeout the status word records it,
 // loads still in flight are waited for (bounded again), and the warp returns.
-template <class Load, class Store>
+template <int L, class Load, class Store>
 __device__ __forceinline__ void run_stage_ring(uint64_t* full, int64_t n, int lane, Load load,
                                                Store store)
 {
-    constexpr int K = ULY_TMA_STAGES, L = ULY_TMA_LOOKAHEAD;
+    constexpr int K = ULY_TMA_STAGES;
     int64_t loaded = n < L ? n : L;
     for (int64_t k = 0; k < loaded; ++k) load(k);
     int64_t k = 0;
@@ -188,7 +195,8 @@ __global__ void __launch_bounds__(32, 1) relayout_tma_kernel(const __grid_consta
                 bulk_s2g(seq_addr(a, t, row), src + row * t.cols, uint32_t(t.cols));
         }
     };
-    run_stage_ring(full, n, lane, issue_load, issue_store);
+    run_stage_ring<MODE == 0 ? ULY_TMA_LOOKAHEAD0 : ULY_TMA_LOOKAHEAD1>(full, n, lane, issue_load,
+                                                                     issue_store);
 }
 
 // ---- row tiles: whole rows through shared memory ------------------------------------------------
@@ -290,7 +298,8 @@ __global__ void __launch_bounds__(32, 1) relayout_rows_kernel(const __grid_const
             if (lane == 0) bulk_s2g(seq_span(t), stage, uint32_t(t.nrows * row_bytes));
         }
     };
-    run_stage_ring(full, n, lane, issue_load, issue_store);
+    run_stage_ring<MODE == 0 ? ULY_TMA_LOOKAHEAD0 : ULY_TMA_LOOKAHEAD1>(full, n, lane, issue_load,
+                                                                     issue_store);
 }
 
 template <int MODE>
