@@ -286,13 +286,16 @@ int ulysses_a2a_4d_qkv_fused_backward(ulysses_plan_t plan, void* const* dqkv_out
 /*
  * End-to-end form for host-resident data: copy each rank's input from host_in[k] to dev_in[k],
  * run the relayout, and copy each dev_out[k] back to host_out[k]. The work is cut into about
- * eight sequence chunks so that copies in and copies out overlap: chunk c is copied in and
- * relaid out on `stream`, then copied out on an auxiliary stream while chunk c+1 is copied in;
- * `stream` finally waits for the auxiliary stream, so the call is ordered on `stream` as a whole
- * (when `stream` has completed, host_out holds the result). The auxiliary stream and a few events
- * are created once per device on the first such call (no device memory) and reused; concurrent
- * calls from several host threads are serialised while they enqueue. Host buffers should be
- * page-locked for the copies to be asynchronous. Device buffers are the caller's, as above.
+ * eight ranges of the global sequence (within the chunk cap) so that copies in and copies out
+ * overlap: range c is copied in on an auxiliary input stream (after all work queued on `stream`
+ * before the call), relaid out on `stream` once its copy in is done, and copied out on an
+ * auxiliary output stream while later ranges are copied in; `stream` finally waits for the
+ * output stream, so the call is
+ * ordered on `stream` as a whole (when `stream` has completed, host_out holds the result). The
+ * auxiliary streams and a few events are created once per device on the first such call (no
+ * device memory) and reused; concurrent calls from several host threads are serialised while
+ * they enqueue. Host buffers should be page-locked for the copies to be asynchronous. Device
+ * buffers are the caller's, as above.
  */
 int ulysses_a2a_4d_host(ulysses_plan_t plan, int mode, const void* const* host_in,
                         void* const* host_out, void* const* dev_in, void* const* dev_out,

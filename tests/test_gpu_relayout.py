@@ -249,6 +249,59 @@ def test_end_to_end_host_buffers_edges(oracle, g):
                 assert np.array_equal(host_raw(h), w)
 
 
+@pytest.mark.parametrize("cap", [None, 96 * 1024], ids=["default_ranges", "capped_ranges"])
+def test_end_to_end_host_buffers_ranges(oracle, cap):
+    """The host pipeline's ranges of the global sequence (a few hundred rows, ranges that cross
+    shards of unequal length, b = 2), also when the chunk cap forces many short ranges: identical
+    to the oracle in both modes, twice in a row on the same buffers."""
+    W, b, seq, heads, d, dtype = 4, 2, [301, 257, 0, 410], [3, 1, 4, 2], 64, "bfloat16"
+    plan = B.ulysses_plan(W, b, seq, heads, d, dtype)
+    if cap is not None:
+        B.ulysses_plan_set_chunk_bytes(plan, cap)
+    N, S = sum(heads), sum(seq)
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(97)
+    for mode in (0, 1):
+        in_shapes = [(b, s, N, d) for s in seq] if mode == 0 else [(b, S, n, d) for n in heads]
+        out_shapes = [(b, S, n, d) for n in heads] if mode == 0 else [(b, s, N, d) for s in seq]
+        src = [random_bytes_tensor(sh, torch.bfloat16, gen, "cpu") for sh in in_shapes]
+        host_in = [x.pin_memory() for x in src]
+        host_out = [torch.full(sh, 7, dtype=torch.bfloat16).pin_memory() for sh in out_shapes]
+        dev_in = [torch.empty(sh, dtype=torch.bfloat16, device="cuda") for sh in in_shapes]
+        dev_out = [torch.empty(sh, dtype=torch.bfloat16, device="cuda") for sh in out_shapes]
+        want = oracle.a2a_4d([host_raw(x) for x in src], seq, heads, mode)
+        for _ in range(2):
+            B.ulysses_a2a_4d_host(plan, mode, host_in, host_out, dev_in, dev_out)
+            torch.cuda.synchronize()
+            for h, w in zip(host_out, want):
+                assert np.array_equal(host_raw(h), w)
+
+
+def test_end_to_end_host_copies_wait_for_the_stream(oracle):
+    """The host call's copies in run on a stream of their own, but only after the work already
+    queued on the caller's stream: a fill of the device inputs queued behind a long wait on that
+    stream must not land after the copies in (the result would then be the fill's bytes)."""
+    W, b, seq, heads, d = 2, 1, [640, 512], [2, 2], 128
+    plan = B.ulysses_plan(W, b, seq, heads, d, "bfloat16")
+    N, S = sum(heads), sum(seq)
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(98)
+    src = [random_bytes_tensor((b, s, N, d), torch.bfloat16, gen, "cpu") for s in seq]
+    host_in = [x.pin_memory() for x in src]
+    host_out = [torch.zeros((b, S, n, d), dtype=torch.bfloat16).pin_memory() for n in heads]
+    dev_in = [torch.empty((b, s, N, d), dtype=torch.bfloat16, device="cuda") for s in seq]
+    dev_out = [torch.empty((b, S, n, d), dtype=torch.bfloat16, device="cuda") for n in heads]
+    want = oracle.a2a_4d([host_raw(x) for x in src], seq, heads, 0)
+    stream = torch.cuda.current_stream()
+    torch.cuda._sleep(20_000_000)  # roughly 10 ms of spinning on the caller's stream
+    for t in dev_in:
+        t.view(torch.int16).fill_(0x7F7F)
+    B.ulysses_a2a_4d_host(plan, 0, host_in, host_out, dev_in, dev_out, stream)
+    torch.cuda.synchronize()
+    for h, w in zip(host_out, want):
+        assert np.array_equal(host_raw(h), w)
+
+
 def test_misaligned_and_overlapping_on_device():
     plan = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "bfloat16")
     x = [torch.zeros(1, 4, 4, 64, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
