@@ -435,6 +435,7 @@ def run_ours(args):
     e2e["ms_per_step"], e2e_value = aggregate_throughput(e2e["ms_per_step"], wk.bytes_step, pg, "cuda")
     e2e["value"] = round(e2e_value, 3)
 
+    tg = torch_gpu_step(torch, wk, stream) if rank == 0 else None
     med = {k: statistics.median(v) for k, v in kt.items()}
     gbs = {"fused_qk": wk.bytes_fused / (med["fused_qk"] * 1e-3) / 1e9,
            "mode0": wk.bytes_plain / (med["mode0"] * 1e-3) / 1e9,
@@ -469,6 +470,12 @@ def run_ours(args):
                         "frac_of_peak": round(gbs[k] / peak, 4),
                         "frac_of_d2d": round(gbs[k] / d2d, 4) if d2d else None} for k in med},
         "d2d_copy_GBps": round(d2d, 1) if d2d else None,
+        "torch_gpu": None if tg is None else {
+            "note": "context: the same three operations as plain PyTorch GPU ops (torch.cat per "
+                    "output rank; fp32 RMSNorm + RoPE as separate kernels before the cat), same "
+                    "tensors, CUDA events; speedup = its time / this library's kernel time",
+            **{k: dict(v, speedup=round(v["median_ms"] / med[k], 2)) for k, v in tg.items()},
+            "step_ms": round(sum(v["median_ms"] for v in tg.values()), 4)},
         "qkv_fused": {
             "note": "outside the step: q, k, v interleaved (b, s, 3, N, d), one launch in place of "
                     "the step's fused_qk + mode0 launches",
@@ -497,6 +504,64 @@ def run_ours(args):
     if pg:
         pg.barrier()
         pg.destroy_process_group()
+
+
+def torch_gpu_step(torch, wk, stream, reps=5):
+    """Context baseline: the step's three operations written with plain PyTorch ops on the GPU
+    (the single-GPU analogue of the pages' baseline, a permute + all-to-all + permute with the
+    norm and the rotation as separate kernels): per output rank one torch.cat of the slices each
+    input rank sends, and for q and k an fp32 RMSNorm and adjacent-pair RoPE (cos/sin of every
+    position built once, outside the timing) before the cat. Not the product path; timed with
+    CUDA events on the same tensors, median of `reps`."""
+    cfg = wk.cfg
+    W, d = cfg.W, cfg.d
+    seq_off = [sum(cfg.seq_splits[:q]) for q in range(W)]
+    head_off = [sum(cfg.head_splits[:r]) for r in range(W)]
+    j = torch.arange(d // 2, dtype=torch.float64, device="cuda")
+    ang = torch.arange(cfg.S, dtype=torch.float64, device="cuda")[:, None] * (THETA ** (-2.0 * j / d))
+    cos, sin = torch.cos(ang).float(), torch.sin(ang).float()
+
+    def norm_rope(x, w, q):
+        xf = x.float()
+        y = xf * torch.rsqrt(xf.pow(2).mean(-1, keepdim=True) + EPS) * w
+        c = cos[seq_off[q]:seq_off[q] + x.shape[1]][None, :, None, :]
+        sn = sin[seq_off[q]:seq_off[q] + x.shape[1]][None, :, None, :]
+        e, o = y[..., 0::2], y[..., 1::2]
+        return torch.stack((e * c - o * sn, e * sn + o * c), dim=-1).flatten(-2).to(x.dtype)
+
+    def mode0(xs, outs):
+        for r in range(W):
+            n = cfg.head_splits[r]
+            torch.cat([x[:, :, head_off[r]:head_off[r] + n] for x in xs], dim=1, out=outs[r])
+
+    def mode1(ys, outs):
+        for q in range(W):
+            s = cfg.seq_splits[q]
+            torch.cat([y[:, seq_off[q]:seq_off[q] + s] for y in ys], dim=2, out=outs[q])
+
+    ops = {
+        "fused_qk": (lambda: (mode0([norm_rope(x, wk.w[0], q) for q, x in enumerate(wk.q)], wk.qo),
+                              mode0([norm_rope(x, wk.w[1], q) for q, x in enumerate(wk.k)], wk.ko)),
+                     wk.bytes_fused),
+        "mode0": (lambda: mode0(wk.v, wk.vo), wk.bytes_plain),
+        "mode1": (lambda: mode1(wk.o, wk.oo), wk.bytes_plain),
+    }
+    out = {}
+    with torch.cuda.stream(stream):
+        for name, (fn, nbytes) in ops.items():
+            fn()
+            ts = []
+            for _ in range(reps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            ms = statistics.median(ts)
+            out[name] = {"median_ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+    return out
 
 
 def run_e2e(torch, B, wk, stream, args):

@@ -59,9 +59,6 @@ static __device__ unsigned g_fused_status;
 #ifndef ULY_FUSED_DRAIN
 #define ULY_FUSED_DRAIN 0
 #endif
-#ifndef ULY_FUSED_EVICT_FIRST  // loads carry an L2 evict-first hint (inputs are read once)
-#define ULY_FUSED_EVICT_FIRST 0
-#endif
 constexpr int kFusedCtasPerSm = ULY_FUSED_CTAS_PER_SM;
 constexpr int kFusedMaxStages = ULY_FUSED_MAX_STAGES;
 constexpr int kFusedDrain = ULY_FUSED_DRAIN;  // store groups left draining when a stage refills
