@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -53,19 +54,19 @@ struct DeviceInfo {
 
 int current_device(DeviceInfo* info)
 {
-    static int sm_counts[64];
+    static std::atomic<int> sm_counts[64];  // per device, filled on first use by any thread
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
     if (dev < 0 || dev >= 64) return ULY_EINVAL;
-    if (sm_counts[dev] == 0) {
-        int sms = 0;
+    int sms = sm_counts[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e);
-        sm_counts[dev] = sms;
+        sm_counts[dev].store(sms, std::memory_order_relaxed);
     }
     info->device = dev;
-    info->sm_count = sm_counts[dev];
+    info->sm_count = sms;
     return ULY_OK;
 }
 

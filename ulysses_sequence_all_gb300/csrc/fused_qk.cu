@@ -35,6 +35,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "../../include/ulysses.h"
 #include "fused_row.cuh"
 #include "plan.h"
@@ -464,19 +466,20 @@ void fused_geometry(const Plan& p, int planes, int64_t* tokens_per_unit, int* st
     }
 }
 
-static unsigned g_fused_smem_set[64];
+// per device: the kernel variants whose shared-memory limit has been raised (any host thread)
+static std::atomic<unsigned> g_fused_smem_set[64];
 
 template <int G, bool F16, bool HALF>
 static cudaError_t launch_g(const FusedArgs& a, cudaStream_t stream, int device, int grid)
 {
     constexpr int gbit = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : G == 8 ? 3 : G == 16 ? 4 : 5;
     constexpr unsigned bit = 1u << (gbit * 4 + (F16 ? 2 : 0) + (HALF ? 1 : 0));
-    if (device >= 0 && device < 64 && !(g_fused_smem_set[device] & bit)) {
+    if (device >= 0 && device < 64 && !(g_fused_smem_set[device].load() & bit)) {
         cudaError_t e = cudaFuncSetAttribute(fused_qk_kernel<G, F16, HALF>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemPerCtaMax);
         if (e != cudaSuccess) return e;
-        g_fused_smem_set[device] |= bit;
+        g_fused_smem_set[device].fetch_or(bit);
     }
     const FusedSmem m = fused_smem_layout(a.d, a.tokens_per_unit, a.stages, a.stage_bytes);
     fused_qk_kernel<G, F16, HALF><<<grid, kFusedThreads, m.total, stream>>>(a);

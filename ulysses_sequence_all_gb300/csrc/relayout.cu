@@ -17,6 +17,8 @@
 //    in flight per lane.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "../../include/ulysses.h"
 #include "plan.h"
 #include "ptx.cuh"
@@ -348,11 +350,12 @@ __global__ void __launch_bounds__(kVecThreads) relayout_vec_kernel(const __grid_
 
 int64_t relayout_unit_bytes(int engine) { return engine == ULY_ENGINE_VEC ? ULY_VEC_UNIT_BYTES : ULY_TMA_UNIT_BYTES; }
 
-static int g_smem_set[64];
+// per device: whether the TMA kernels' shared-memory limit has been raised (any host thread)
+static std::atomic<int> g_smem_set[64];
 
 static cudaError_t ensure_tma_smem(int device, int smem)
 {
-    if (device < 0 || device >= 64 || g_smem_set[device]) return cudaSuccess;
+    if (device < 0 || device >= 64 || g_smem_set[device].load()) return cudaSuccess;
     const void* kernels[] = {reinterpret_cast<const void*>(relayout_tma_kernel<0>),
                              reinterpret_cast<const void*>(relayout_tma_kernel<1>),
                              reinterpret_cast<const void*>(relayout_rows_kernel<0>),
@@ -361,7 +364,7 @@ static cudaError_t ensure_tma_smem(int device, int smem)
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
     }
-    g_smem_set[device] = 1;
+    g_smem_set[device].store(1);
     return cudaSuccess;
 }
 
@@ -372,11 +375,13 @@ cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStr
 {
     if (a.total_units == 0) return cudaSuccess;
     if (engine == ULY_ENGINE_VEC) {
-        static int blocks_per_sm = 0;
+        static std::atomic<int> vec_blocks_per_sm{0};  // the same on every GB300; any thread
+        int blocks_per_sm = vec_blocks_per_sm.load();
         if (blocks_per_sm == 0) {
             int nb = 0;
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, relayout_vec_kernel<0>, kVecThreads, 0);
             blocks_per_sm = nb > 0 ? nb : 1;
+            vec_blocks_per_sm.store(blocks_per_sm);
         }
         const int64_t warps_needed = a.total_units;
         int64_t grid = int64_t(sm_count) * blocks_per_sm;
