@@ -40,6 +40,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", action="store_true",
+                    help="instead of the step: time modes 0 and 1 on every other configuration "
+                         "(uneven W/dtype points, long packed QKV) and print one JSON line")
     return ap.parse_args()
 
 
@@ -623,10 +626,83 @@ def run_e2e(torch, B, wk, stream, args):
             "per_call_ms": per_call, "window_ms": [round(w, 3) for w in windows]}
 
 
+def run_configs(args):
+    """Modes 0 and 1 on the parity-test configurations (not the headline): the 12 uneven
+    (W, dtype) points (b=2, 75,000 tokens, 40 heads, d=128) and the long packed-QKV geometry
+    (W=4, 250,000 tokens, 56 heads; three planes of 896,000,000 bytes per rank, one call per
+    plane on views of a (3, b, s, N, d) buffer per rank). Inputs already in HBM and larger than
+    L2; CUDA events, median of 20 launches after 5 warm-up launches."""
+    import torch
+    from ulysses_sequence_all_gb300 import binding as B
+    from ulysses_sequence_all_gb300 import workloads as wl
+
+    peak, peak_kind = read_peaks()
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, reps=20, warm=5):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    rows = []
+    for cfg in wl.UNEVEN:
+        plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
+        dt = wl.torch_dtype(cfg.dtype)
+        seq = wl.seq_side_inputs(cfg, "cuda")
+        head = [torch.empty(cfg.head_side_shape(r), dtype=dt, device="cuda") for r in range(cfg.W)]
+        seq_out = [torch.empty_like(t) for t in seq]
+        nbytes = cfg.relayout_bytes()
+        for mode, ins, outs in ((0, seq, head), (1, head, seq_out)):
+            ms = timed(lambda: B.ulysses_a2a_4d(plan, mode, ins, outs, stream))
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            rows.append({"config": cfg.name, "W": cfg.W, "dtype": cfg.dtype, "mode": mode,
+                         "bytes": nbytes, "median_ms": round(ms, 4), "GB/s": round(gbs, 1),
+                         "frac_of_peak": round(gbs / peak, 4)})
+        del seq, head, seq_out
+    cfg = wl.LONG_QKV
+    plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
+    dt = wl.torch_dtype(cfg.dtype)
+    packed_in = [torch.empty((3,) + cfg.seq_side_shape(q), dtype=dt, device="cuda")
+                 for q in range(cfg.W)]
+    for p in range(3):
+        for q, t in enumerate(wl.seq_side_inputs(cfg, "cuda", plane=p)):
+            packed_in[q][p].copy_(t)
+    packed_out = [torch.empty((3,) + cfg.head_side_shape(r), dtype=dt, device="cuda")
+                  for r in range(cfg.W)]
+    nbytes = cfg.relayout_bytes()
+    for mode in (0, 1):
+        src, dst = (packed_in, packed_out) if mode == 0 else (packed_out, packed_in)
+
+        def planes():
+            for p in range(3):
+                B.ulysses_a2a_4d(plan, mode, [t[p] for t in src], [t[p] for t in dst], stream)
+
+        ms = timed(planes, reps=10, warm=2)
+        gbs = 3 * nbytes / (ms * 1e-3) / 1e9
+        rows.append({"config": cfg.name + "_3planes", "W": cfg.W, "dtype": cfg.dtype,
+                     "mode": mode, "bytes": 3 * nbytes, "median_ms": round(ms, 4),
+                     "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)})
+    assert B.ulysses_device_status() == 0, "a kernel recorded a wait timeout"
+    print(json.dumps({"configs": rows, "peak": peak, "peak_source": f"{peak_kind} hbm_gbs",
+                      "note": "parity-test configurations, timed for context; not bench lines"}),
+          flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.configs:
+        run_configs(args)
     else:
         run_ours(args)
 

@@ -18,9 +18,10 @@ int64_t relayout_unit_bytes(int engine);
 cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStream_t stream,
                             int device, int sm_count, int64_t max_grid);
 cudaError_t relayout_status(unsigned* status, bool clear);
-int64_t relayout_tile_rows(int64_t row_bytes);
-cudaError_t relayout_rows_launch(const RowTileArgs& a, int mode, cudaStream_t stream, int device,
-                                 int sm_count, int64_t max_grid);
+RowRing relayout_row_ring(const Plan& p, int mode);
+int64_t relayout_tile_rows(int64_t row_bytes, int64_t stage_bytes);
+cudaError_t relayout_rows_launch(const RowTileArgs& a, int mode, const RowRing& ring,
+                                 cudaStream_t stream, int device, int sm_count, int64_t max_grid);
 void fused_geometry(const Plan& p, int planes, int64_t* tokens_per_unit, int* stages,
                     uint32_t* stage_bytes, int* ctas_per_sm);
 cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count,
@@ -180,7 +181,9 @@ int relayout_rows(const Plan& p, int mode, int engine, const void* const* in_ptr
         head[k] = mode == 0 ? out : in;
     }
     // TMA engine: whole-row tiles when a row fits a stage, row-run segments otherwise
-    const int64_t tile_rows = engine == ULY_ENGINE_TMA ? relayout_tile_rows(p.N * p.d * p.e) : 0;
+    const RowRing ring = relayout_row_ring(p, mode);
+    const int64_t tile_rows =
+        engine == ULY_ENGINE_TMA ? relayout_tile_rows(p.N * p.d * p.e, ring.stage_bytes) : 0;
     cudaError_t e;
     if (tile_rows > 0) {
         RowTileArgs t;
@@ -190,7 +193,8 @@ int relayout_rows(const Plan& p, int mode, int engine, const void* const* in_ptr
             t.head_ptr[k] = head[k];
         }
         build_row_tiles(p, rows, tile_rows, &t);
-        e = relayout_rows_launch(t, mode, stream, dev.device, dev.sm_count, p.max_ctas);
+        t.stage_bytes = ring.stage_bytes;
+        e = relayout_rows_launch(t, mode, ring, stream, dev.device, dev.sm_count, p.max_ctas);
     } else {
         RelayoutArgs a;
         std::memset(&a, 0, sizeof a);

@@ -75,6 +75,17 @@ struct RowTileArgs {
     int64_t S, N, b, d_bytes;
     int64_t tile_rows, total_units;
     int32_t W;
+    int32_t stage_bytes;  // bytes between consecutive stages in shared memory
+};
+
+// Shape of the row-tile kernel's pipeline for one plan and mode, chosen on the host from the
+// geometry (relayout_row_ring): loads in flight ahead of the unit being stored, CTAs per SM and
+// the bytes of one stage (the ring always has kRowStages stages).
+constexpr int kRowStages = 4;
+struct RowRing {
+    int lookahead;
+    int ctas_per_sm;
+    int stage_bytes;
 };
 
 void build_row_tiles(const Plan& p, const ChunkRows& rows, int64_t tile_rows, RowTileArgs* a);

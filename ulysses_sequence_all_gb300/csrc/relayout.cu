@@ -53,7 +53,7 @@ static __device__ unsigned g_relayout_status;
 #endif
 static_assert(ULY_TMA_LOOKAHEAD0 >= 1 && ULY_TMA_LOOKAHEAD0 <= ULY_TMA_STAGES, "lookahead <= stages");
 static_assert(ULY_TMA_LOOKAHEAD1 >= 1 && ULY_TMA_LOOKAHEAD1 <= ULY_TMA_STAGES, "lookahead <= stages");
-static_assert(ULY_TMA_STAGES <= 16, "stage barriers must fit the barrier area");
+static_assert(ULY_TMA_STAGES <= 16 && kRowStages <= 16, "stage barriers must fit the barrier area");
 constexpr int kTmaBarrierBytes = 128;  // the stage barriers sit before the first stage
 constexpr int kVecThreads = 256;
 
@@ -64,11 +64,10 @@ constexpr int kVecThreads = 256;
 // stores it has just issued. Every wait is bounded and its outcome is made uniform across the
 // warp (a lane that timed out stops them all); on a timeout the status word records it,
 // loads still in flight are waited for (bounded again), and the warp returns.
-template <int L, class Load, class Store>
+template <int K, int L, class Load, class Store>
 __device__ __forceinline__ void run_stage_ring(uint64_t* full, int64_t n, int lane, Load load,
                                                Store store)
 {
-    constexpr int K = ULY_TMA_STAGES;
     int64_t loaded = n < L ? n : L;
     for (int64_t k = 0; k < loaded; ++k) load(k);
     int64_t k = 0;
@@ -197,8 +196,8 @@ __global__ void __launch_bounds__(32, 1) relayout_tma_kernel(const __grid_consta
                 bulk_s2g(seq_addr(a, t, row), src + row * t.cols, uint32_t(t.cols));
         }
     };
-    run_stage_ring<MODE == 0 ? ULY_TMA_LOOKAHEAD0 : ULY_TMA_LOOKAHEAD1>(full, n, lane, issue_load,
-                                                                     issue_store);
+    run_stage_ring<ULY_TMA_STAGES, MODE == 0 ? ULY_TMA_LOOKAHEAD0 : ULY_TMA_LOOKAHEAD1>(
+        full, n, lane, issue_load, issue_store);
 }
 
 // ---- row tiles: whole rows through shared memory ------------------------------------------------
@@ -236,11 +235,12 @@ __device__ __forceinline__ RowTile decode_rows(const RowTileArgs& a, int64_t u)
     return t;
 }
 
-template <int MODE>
+template <int MODE, int L>
 __global__ void __launch_bounds__(32, 1) relayout_rows_kernel(const __grid_constant__ RowTileArgs a)
 {
+    static_assert(L >= 1 && L <= kRowStages, "lookahead <= stages");
     extern __shared__ __align__(1024) uint8_t smem[];
-    constexpr int K = ULY_TMA_STAGES;
+    constexpr int K = kRowStages;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint8_t* stage0 = smem + kTmaBarrierBytes;
     const int lane = threadIdx.x;
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(32, 1) relayout_rows_kernel(const __grid_const
     auto issue_load = [&](int64_t k) {
         const RowTile t = decode_rows(a, first + k * step);
         const int s = int(k % K);
-        uint8_t* stage = stage0 + size_t(s) * ULY_TMA_UNIT_BYTES;
+        uint8_t* stage = stage0 + size_t(s) * a.stage_bytes;
         const uint32_t bytes = uint32_t(t.nrows * row_bytes);
         if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
         __syncwarp();
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(32, 1) relayout_rows_kernel(const __grid_const
     };
     auto issue_store = [&](int64_t k) {
         const RowTile t = decode_rows(a, first + k * step);
-        const uint8_t* stage = stage0 + size_t(k % K) * ULY_TMA_UNIT_BYTES;
+        const uint8_t* stage = stage0 + size_t(k % K) * a.stage_bytes;
         if (MODE == 0) {
             const int pairs = int(t.nrows) * W;
             for (int idx = lane; idx < pairs; idx += 32) {
@@ -300,8 +300,7 @@ __global__ void __launch_bounds__(32, 1) relayout_rows_kernel(const __grid_const
             if (lane == 0) bulk_s2g(seq_span(t), stage, uint32_t(t.nrows * row_bytes));
         }
     };
-    run_stage_ring<MODE == 0 ? ULY_TMA_LOOKAHEAD0 : ULY_TMA_LOOKAHEAD1>(full, n, lane, issue_load,
-                                                                     issue_store);
+    run_stage_ring<K, L>(full, n, lane, issue_load, issue_store);
 }
 
 template <int MODE>
@@ -353,15 +352,25 @@ int64_t relayout_unit_bytes(int engine) { return engine == ULY_ENGINE_VEC ? ULY_
 // per device: whether the TMA kernels' shared-memory limit has been raised (any host thread)
 static std::atomic<int> g_smem_set[64];
 
-static cudaError_t ensure_tma_smem(int device, int smem)
+// one CTA may use at most 227 KiB of dynamic shared memory; an SM holds 228 KiB, 1 KiB of it
+// reserved per resident CTA
+constexpr int kSmemPerCtaMax = 227 * 1024;
+constexpr int kSmemPerSm = 228 * 1024;
+constexpr int kSmemReservedPerCta = 1024;
+
+// Raise every TMA kernel's dynamic shared-memory limit to the per-CTA maximum, once per device.
+static cudaError_t ensure_tma_smem(int device)
 {
     if (device < 0 || device >= 64 || g_smem_set[device].load()) return cudaSuccess;
     const void* kernels[] = {reinterpret_cast<const void*>(relayout_tma_kernel<0>),
                              reinterpret_cast<const void*>(relayout_tma_kernel<1>),
-                             reinterpret_cast<const void*>(relayout_rows_kernel<0>),
-                             reinterpret_cast<const void*>(relayout_rows_kernel<1>)};
+                             reinterpret_cast<const void*>(relayout_rows_kernel<0, 2>),
+                             reinterpret_cast<const void*>(relayout_rows_kernel<0, 3>),
+                             reinterpret_cast<const void*>(relayout_rows_kernel<1, 2>),
+                             reinterpret_cast<const void*>(relayout_rows_kernel<1, 3>)};
     for (const void* k : kernels) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e =
+            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCtaMax);
         if (e != cudaSuccess) return e;
     }
     g_smem_set[device].store(1);
@@ -369,6 +378,7 @@ static cudaError_t ensure_tma_smem(int device, int smem)
 }
 
 constexpr int kTmaSmem = kTmaBarrierBytes + ULY_TMA_STAGES * ULY_TMA_UNIT_BYTES;
+static_assert(kTmaSmem <= kSmemPerCtaMax, "segment ring must fit one CTA");
 
 cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStream_t stream,
                             int device, int sm_count, int64_t max_grid)
@@ -394,7 +404,7 @@ cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStr
             relayout_vec_kernel<1><<<unsigned(grid), kVecThreads, 0, stream>>>(a);
         return cudaGetLastError();
     }
-    cudaError_t e = ensure_tma_smem(device, kTmaSmem);
+    cudaError_t e = ensure_tma_smem(device);
     if (e != cudaSuccess) return e;
     int64_t grid = int64_t(sm_count) * ULY_TMA_CTAS_PER_SM;
     if (max_grid > 0 && grid > max_grid) grid = max_grid;
@@ -406,25 +416,70 @@ cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStr
     return cudaGetLastError();
 }
 
-// Rows per tile for the row-tile kernel, 0 when one row does not fit a stage.
-int64_t relayout_tile_rows(int64_t row_bytes)
+// The row-tile kernel's pipeline shape for a plan and mode, from its geometry: `row` = one
+// token's bytes (N d e), `run` = the mean bytes of one (token, rank) run (row / W), `unit` = the
+// whole rows that fit a 24 KiB stage. Measured on a GB300 (CUDA events, the uneven configurations
+// of fp8 / fp16 / fp32 at W = 3, 5, 7, 8, the Wan shape and the long packed-QKV shape):
+//  * runs below ~900 bytes (fp8 at W >= 6): bulk copies are small and many, and three CTAs per SM
+//    with 18 KiB stages, two loads ahead in both modes, beat the default by 12-25%;
+//  * units below 20 KiB (one row of 12-20 KiB, as at 56 heads of bf16): three loads ahead in both
+//    modes (mode 1 of the long packed-QKV shape +12%);
+//  * otherwise mode 0 keeps three loads ahead while the runs are short (1,280 bytes at the Wan
+//    shape) and two from ~1,400 bytes on, where its long stores take longer to leave shared
+//    memory and want more of the ring (+11-16% at W = 3, 5 and for fp32); mode 1 keeps two.
+RowRing relayout_row_ring(const Plan& p, int mode)
 {
-    return row_bytes <= ULY_TMA_UNIT_BYTES ? ULY_TMA_UNIT_BYTES / row_bytes : 0;
+    const int64_t row = p.N * p.d * p.e;
+    const int64_t run = row / p.W;
+    RowRing r;
+    r.ctas_per_sm = 2;
+    r.stage_bytes = 24576;
+    if (run < 900) {
+        r.ctas_per_sm = 3;
+        r.stage_bytes = 18432;
+        r.lookahead = 2;
+        return r;
+    }
+    const int64_t unit = row <= r.stage_bytes ? (r.stage_bytes / row) * row : 0;
+    if (unit > 0 && unit < 20480)
+        r.lookahead = 3;
+    else
+        r.lookahead = mode == 0 && run < 1400 ? 3 : 2;
+    return r;
 }
 
-cudaError_t relayout_rows_launch(const RowTileArgs& a, int mode, cudaStream_t stream, int device,
-                                 int sm_count, int64_t max_grid)
+// Rows per tile for the row-tile kernel, 0 when one row does not fit a stage.
+int64_t relayout_tile_rows(int64_t row_bytes, int64_t stage_bytes)
+{
+    return row_bytes <= stage_bytes ? stage_bytes / row_bytes : 0;
+}
+
+cudaError_t relayout_rows_launch(const RowTileArgs& a, int mode, const RowRing& ring,
+                                 cudaStream_t stream, int device, int sm_count, int64_t max_grid)
 {
     if (a.total_units == 0) return cudaSuccess;
-    cudaError_t e = ensure_tma_smem(device, kTmaSmem);
+    const int smem = kTmaBarrierBytes + kRowStages * ring.stage_bytes;
+    if (smem > kSmemPerCtaMax ||
+        ring.ctas_per_sm * (smem + kSmemReservedPerCta) > kSmemPerSm ||
+        (ring.lookahead != 2 && ring.lookahead != 3) || a.stage_bytes != ring.stage_bytes)
+        return cudaErrorInvalidValue;
+    cudaError_t e = ensure_tma_smem(device);
     if (e != cudaSuccess) return e;
-    int64_t grid = int64_t(sm_count) * ULY_TMA_CTAS_PER_SM;
+    int64_t grid = int64_t(sm_count) * ring.ctas_per_sm;
     if (max_grid > 0 && grid > max_grid) grid = max_grid;
     if (grid > a.total_units) grid = a.total_units;
-    if (mode == 0)
-        relayout_rows_kernel<0><<<unsigned(grid), 32, kTmaSmem, stream>>>(a);
-    else
-        relayout_rows_kernel<1><<<unsigned(grid), 32, kTmaSmem, stream>>>(a);
+    const unsigned g = unsigned(grid);
+    if (mode == 0) {
+        if (ring.lookahead == 3)
+            relayout_rows_kernel<0, 3><<<g, 32, smem, stream>>>(a);
+        else
+            relayout_rows_kernel<0, 2><<<g, 32, smem, stream>>>(a);
+    } else {
+        if (ring.lookahead == 3)
+            relayout_rows_kernel<1, 3><<<g, 32, smem, stream>>>(a);
+        else
+            relayout_rows_kernel<1, 2><<<g, 32, smem, stream>>>(a);
+    }
     return cudaGetLastError();
 }
 
