@@ -630,8 +630,10 @@ def run_configs(args):
     """Modes 0 and 1 on the parity-test configurations (not the headline): the 12 uneven
     (W, dtype) points (b=2, 75,000 tokens, 40 heads, d=128) and the long packed-QKV geometry
     (W=4, 250,000 tokens, 56 heads; three planes of 896,000,000 bytes per rank, one call per
-    plane on views of a (3, b, s, N, d) buffer per rank). Inputs already in HBM and larger than
-    L2; CUDA events, median of 20 launches after 5 warm-up launches."""
+    plane on views of a (3, b, s, N, d) buffer per rank); then the fused call and its backward on
+    the fp16 uneven plans, the long geometry's q and k, and the Wan shape in fp16 with
+    rotate-half pairs. Inputs already in HBM and larger than L2; CUDA events, median of 20
+    launches after 5 warm-up launches."""
     import torch
     from ulysses_sequence_all_gb300 import binding as B
     from ulysses_sequence_all_gb300 import workloads as wl
@@ -664,8 +666,8 @@ def run_configs(args):
         for mode, ins, outs in ((0, seq, head), (1, head, seq_out)):
             ms = timed(lambda: B.ulysses_a2a_4d(plan, mode, ins, outs, stream))
             gbs = nbytes / (ms * 1e-3) / 1e9
-            rows.append({"config": cfg.name, "W": cfg.W, "dtype": cfg.dtype, "mode": mode,
-                         "bytes": nbytes, "median_ms": round(ms, 4), "GB/s": round(gbs, 1),
+            rows.append({"config": cfg.name, "kernel": "relayout", "W": cfg.W,
+                         "dtype": cfg.dtype, "mode": mode, "bytes": nbytes, "median_ms": round(ms, 4), "GB/s": round(gbs, 1),
                          "frac_of_peak": round(gbs / peak, 4)})
         del seq, head, seq_out
     cfg = wl.LONG_QKV
@@ -688,9 +690,46 @@ def run_configs(args):
 
         ms = timed(planes, reps=10, warm=2)
         gbs = 3 * nbytes / (ms * 1e-3) / 1e9
-        rows.append({"config": cfg.name + "_3planes", "W": cfg.W, "dtype": cfg.dtype,
-                     "mode": mode, "bytes": 3 * nbytes, "median_ms": round(ms, 4),
+        rows.append({"config": cfg.name + "_3planes", "kernel": "relayout", "W": cfg.W,
+                     "dtype": cfg.dtype, "mode": mode, "bytes": 3 * nbytes, "median_ms": round(ms, 4),
                      "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)})
+    del packed_in, packed_out
+
+    # the fused call (q, k: mode 0 + RMSNorm + RoPE) and its backward on other geometries
+    fused_cfgs = [(c, "adjacent") for c in wl.UNEVEN if c.dtype == "float16"]
+    fused_cfgs += [(wl.Workload("long_qk", 4, 1, (62500,) * 4, (14,) * 4, 128, "bfloat16", seed=20),
+                    "adjacent"),
+                   (wl.Workload("wan720p_fp16", 8, 1, (9450,) * 8, (5,) * 8, 128, "float16", seed=1),
+                    "half")]
+    for cfg, pairs in fused_cfgs:
+        plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
+        if pairs == "half":
+            B.ulysses_plan_set_rope_pairs(plan, B.ULY_ROPE_HALF)
+        dt = wl.torch_dtype(cfg.dtype)
+        q = wl.seq_side_inputs(cfg, "cuda", seed=3)
+        k = wl.seq_side_inputs(cfg, "cuda", seed=4)
+        w = wl.rms_weights(cfg.d).cuda()
+        qo = [torch.empty(cfg.head_side_shape(r), dtype=dt, device="cuda") for r in range(cfg.W)]
+        ko = [torch.empty_like(t) for t in qo]
+        side = cfg.plane_bytes()
+        ms = timed(lambda: B.ulysses_a2a_4d_qk_fused(plan, q, k, qo, ko, w, EPS, THETA, stream))
+        gbs = 4 * side / (ms * 1e-3) / 1e9
+        rows.append({"config": cfg.name, "kernel": "fused_qk", "W": cfg.W, "dtype": cfg.dtype,
+                     "rope_pairs": pairs, "bytes": 4 * side, "median_ms": round(ms, 4),
+                     "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)})
+        dq = [torch.empty_like(t) for t in q]
+        dk = [torch.empty_like(t) for t in k]
+        dw = torch.empty((2, cfg.d), dtype=torch.float32, device="cuda")
+        ws = torch.empty(B.ulysses_qk_fused_backward_workspace(plan), dtype=torch.uint8,
+                         device="cuda")
+        ms = timed(lambda: B.ulysses_a2a_4d_qk_fused_backward(plan, dq, dk, q, k, qo, ko, w, dw,
+                                                              EPS, THETA, ws, stream))
+        gbs = 6 * side / (ms * 1e-3) / 1e9
+        rows.append({"config": cfg.name, "kernel": "fused_qk_backward", "W": cfg.W,
+                     "dtype": cfg.dtype, "rope_pairs": pairs, "bytes": 6 * side,
+                     "median_ms": round(ms, 4), "GB/s": round(gbs, 1),
+                     "frac_of_peak": round(gbs / peak, 4)})
+        del q, k, qo, ko, dq, dk, ws
     assert B.ulysses_device_status() == 0, "a kernel recorded a wait timeout"
     print(json.dumps({"configs": rows, "peak": peak, "peak_source": f"{peak_kind} hbm_gbs",
                       "note": "parity-test configurations, timed for context; not bench lines"}),
