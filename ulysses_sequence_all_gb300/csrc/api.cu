@@ -284,7 +284,9 @@ int fused_prepare(const Plan& p, const void* const* q_in, const void* const* k_i
     if ((rc = check_overlap(ins, ins_b, n_in, outs, outs_b, n_out))) return rc;
     int stages = 0, ctas_per_sm = 1;
     uint32_t stage_bytes = 0;
-    fused_geometry(p, qkv ? 3 : 2, tokens_per_unit, &stages, &stage_bytes, &ctas_per_sm);
+    // a stage holds the q and k rows of tokens_per_unit tokens (an interleaved call's v units hold
+    // the v rows of twice as many tokens: the same bytes)
+    fused_geometry(p, 2, tokens_per_unit, &stages, &stage_bytes, &ctas_per_sm);
     if (stages == 0) return ULY_EINVAL;  // one token's rows do not fit the stages
     std::memset(a, 0, sizeof *a);
     a->ctas_per_sm = ctas_per_sm;
@@ -314,7 +316,10 @@ int fused_prepare(const Plan& p, const void* const* q_in, const void* const* k_i
 int fused_rows(const Plan& p, FusedArgs* a, int64_t tokens_per_unit, const ChunkRows& rows,
                cudaStream_t stream, const DeviceInfo& dev)
 {
-    build_fused_units(p, rows, tokens_per_unit, a);
+    if (a->interleaved)
+        build_fused_units(p, rows, tokens_per_unit, 2 * tokens_per_unit, 3, a);
+    else
+        build_fused_units(p, rows, tokens_per_unit, tokens_per_unit, 1, a);
     cudaError_t e = fused_launch(*a, stream, dev.device, dev.sm_count, p.max_ctas);
     return e == cudaSuccess ? ULY_OK : cuda_fail(e);
 }

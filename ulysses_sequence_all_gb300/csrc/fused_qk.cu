@@ -7,7 +7,10 @@
 //
 // Structure: a persistent grid of several CTAs per SM, each with a ring of K shared-memory
 // stages. A work unit is a few consecutive tokens of one source rank: all N heads of q and of k,
-// two contiguous spans of the sequence-side tensors. Warp roles per CTA:
+// two contiguous spans of the sequence-side tensors. An interleaved (b, s, 3, N, d) input is cut
+// into blocks of twice as many tokens with three units each (the q and k rows of the first half,
+// of the second half, and the v rows of the whole block), so that every unit fills the same
+// stage and the v rows pass through without arithmetic. Warp roles per CTA:
 //  * loader: lane 0 waits for the stage to be free ("empty" mbarrier), starts the cp.async.bulk
 //    loads (completing on the stage's "full" mbarrier as transaction bytes) and leaves a record
 //    of the unit beside the stage; while the copies fly, all lanes fill the stage's cos/sin
@@ -88,7 +91,7 @@ constexpr int kIlp = ULY_FUSED_ILP;  // head rows in flight per lane group
 struct FusedRecord {
     int64_t head_row0;  // first row of the unit on the head side: bb * S + seq_off(q) + i0
     int32_t ntok;
-    int32_t pad;
+    int32_t kind;       // 0, 1: q and k rows; 2: v rows (interleaved calls)
 };
 
 #ifndef ULY_FUSED_WAIT_HINT_NS  // suspend-time hint of the barrier waits (0: plain polling)
@@ -107,29 +110,45 @@ __device__ __forceinline__ bool fused_wait(uint64_t* bar, uint32_t parity)
 struct FusedUnit {
     int q;
     int64_t bb, i0;
-    int ntok;
+    int ntok;  // may be 0: the second q,k unit of an interleaved block that holds few tokens
+    int kind;  // 0, 1: q and k rows of the block's first / second tokens_per_unit tokens; 2: v rows
 };
 
 __device__ __forceinline__ FusedUnit fused_decode(const FusedArgs& a, int64_t u)
 {
+    FusedUnit t;
+    int64_t blk_id = u;
+    t.kind = 0;
+    if (a.units_per_block == 3) {
+        blk_id = div_fast(u, 3);
+        t.kind = int(u - 3 * blk_id);
+    }
     int lo = 0, hi = a.W - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (a.unit_begin[mid] <= u)
+        if (a.unit_begin[mid] <= blk_id)
             lo = mid;
         else
             hi = mid - 1;
     }
-    FusedUnit t;
     t.q = lo;
-    const int64_t T = a.tokens_per_unit;
+    const int64_t BT = a.block_tokens;
     const int64_t rows = a.rows[lo];
     const int64_t blocks = a.blocks[lo];  // token blocks per batch index of shard q
-    const int64_t local = u - a.unit_begin[lo];
+    const int64_t local = blk_id - a.unit_begin[lo];
     t.bb = div_fast(local, blocks);
     const int64_t blk = local - t.bb * blocks;
-    t.i0 = a.row_lo[lo] + blk * T;
-    t.ntok = int(min(T, rows - blk * T));
+    t.i0 = a.row_lo[lo] + blk * BT;
+    const int64_t nblk = min(BT, rows - blk * BT);  // tokens of the block
+    const int64_t T = a.tokens_per_unit;
+    if (t.kind == 0)
+        t.ntok = int(min(T, nblk));
+    else if (t.kind == 1) {
+        t.i0 += T;
+        t.ntok = int(nblk > T ? nblk - T : 0);
+    } else {
+        t.ntok = int(nblk);
+    }
     return t;
 }
 
@@ -217,11 +236,12 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     if (n == 0) return;
     const int row_bytes = N * D * 2;  // one token, all heads, one tensor
     const bool qkv = a.interleaved != 0;
-    const int planes = qkv ? 3 : 2;
-    // Stage layout: separate q and k inputs are loaded as two spans (all q rows, then all k
-    // rows); an interleaved (b, s, 3, N, d) input is one span with the planes inside each token.
-    // Row (token t, plane c, head h) sits at t * tok_stride + c * plane_stride(ntok) + h * 2d.
-    const int tok_stride = qkv ? 3 * row_bytes : row_bytes;
+    // Stage layouts. A q,k unit holds row (token t, plane c in {q, k}, head h) at
+    // t * tok_stride + c * plane_stride(ntok) + h * 2d: separate inputs arrive as two spans (all q
+    // rows, then all k rows), an interleaved input as one copy per token of its q and k rows,
+    // which are adjacent in the (b, s, 3, N, d) layout. A v unit (interleaved only) holds its
+    // tokens' v rows back to back, one copy per token.
+    const int tok_stride = qkv ? 2 * row_bytes : row_bytes;
     auto plane_stride = [&](int ntok) { return qkv ? row_bytes : ntok * row_bytes; };
 
     if (warp == kLoaderWarp) {
@@ -241,27 +261,34 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
                 break;
             }
             const FusedUnit t = fused_decode(a, first + j * step);
+            const bool v_unit = t.kind == 2;
+            const uint32_t bytes = uint32_t(t.ntok) * uint32_t(row_bytes);  // one plane
+            const int64_t tok0 = t.bb * a.s[t.q] + t.i0;                      // first source row
+            uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
             if (lane == 0) {
-                const uint32_t bytes = uint32_t(t.ntok) * uint32_t(row_bytes);  // one plane
-                const int64_t tok0 = t.bb * a.s[t.q] + t.i0;                      // first source row
-                uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
-                mbar_arrive_expect_tx(&full[s], uint32_t(planes) * bytes);
-                if (qkv) {
-                    bulk_g2s(dst, a.qkv_in[t.q] + tok0 * 3 * row_bytes, 3 * bytes, &full[s]);
-                } else {
+                mbar_arrive_expect_tx(&full[s], v_unit ? bytes : 2 * bytes);
+                if (!qkv) {
                     bulk_g2s(dst, a.q_in[t.q] + tok0 * row_bytes, bytes, &full[s]);
                     bulk_g2s(dst + bytes, a.k_in[t.q] + tok0 * row_bytes, bytes, &full[s]);
                 }
                 FusedRecord& rec = records[s];  // published by this lane's arrive below
                 rec.head_row0 = t.bb * a.S + a.seq_off[t.q] + t.i0;
                 rec.ntok = t.ntok;
+                rec.kind = t.kind;
+            }
+            if (qkv) {  // one copy per token: its q and k rows, or its v row
+                __syncwarp();  // after lane 0 registered the unit's bytes
+                const uint32_t each = v_unit ? uint32_t(row_bytes) : 2u * uint32_t(row_bytes);
+                const uint8_t* src = a.qkv_in[t.q] + tok0 * 3 * row_bytes + (v_unit ? 2 * row_bytes : 0);
+                for (int tok = lane; tok < t.ntok; tok += 32)
+                    bulk_g2s(dst + size_t(tok) * each, src + int64_t(tok) * 3 * row_bytes, each, &full[s]);
             }
             float* table = reinterpret_cast<float*>(smem + L.tables + s * L.table_bytes);
             const float p0 = float(a.seq_off[t.q] + t.i0);
             // Per token, lane i of a row group owns pairs 4i .. 4i+3, read as two 16-byte
             // entries (c_j, c_j+1, s_j, s_j+1) for j = 4i and j = 4i+2; the entries of all lanes
             // for j = 4i come first, then those for j = 4i+2, so each read is contiguous.
-            for (int e = lane; e < t.ntok * HALF; e += 32) {
+            for (int e = lane; e < (v_unit ? 0 : t.ntok * HALF); e += 32) {
                 const int tok = e / HALF, jj = e % HALF;
                 const float2 tj = turns[jj];
                 const float2 cs = rope_cos_sin(p0 + float(tok), tj.x, tj.y);
@@ -284,7 +311,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     }
 
     if (warp == kStorerWarp) {
-        // The results sit where their inputs were (v untouched): for each token, plane and
+        // The results sit where their inputs were (v rows untouched): for each token, plane and
         // destination rank one run of n_r heads, contiguous in the stage and in the destination
         // tensor. A stage is handed back to the loader kFusedDrain units later, once its stores
         // have read it.
@@ -300,15 +327,18 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
             const uint8_t* st = smem + L.stages + size_t(s) * a.stage_bytes;
             const int64_t row0 = rec.head_row0;
             const int W = a.W;
+            const bool v_unit = rec.kind == 2;
+            const int uplanes = v_unit ? 1 : 2;
+            const int ustride = v_unit ? row_bytes : tok_stride;
             const int pstride = plane_stride(rec.ntok);
-            const int runs = rec.ntok * planes * W;
+            const int runs = rec.ntok * uplanes * W;
             for (int idx = lane; idx < runs; idx += 32) {
                 const int rest = idx / W, r = idx - rest * W;
-                const int tok = rest / planes, plane = rest - tok * planes;
+                const int tok = rest / uplanes, plane = rest - tok * uplanes;
                 const int64_t run = a.n[r] * (D * 2);
                 if (run == 0) continue;
-                const uint8_t* src = st + tok * tok_stride + plane * pstride + a.head_off[r] * (D * 2);
-                uint8_t* out = plane == 0 ? a.q_out[r] : plane == 1 ? a.k_out[r] : a.v_out[r];
+                const uint8_t* src = st + tok * ustride + plane * pstride + a.head_off[r] * (D * 2);
+                uint8_t* out = v_unit ? a.v_out[r] : plane == 0 ? a.q_out[r] : a.k_out[r];
                 bulk_s2g(out + (row0 + tok) * run, src, uint32_t(run));
             }
             bulk_commit();
@@ -348,6 +378,11 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
         if (!__all_sync(0xffffffffu, fused_wait(&full[s], ring.phase))) {
             if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
             break;
+        }
+        if (records[s].kind == 2) {  // v rows: nothing to compute
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&computed[s]);
+            continue;
         }
         const int ntok = records[s].ntok;
         // this tensor's plane in the stage; row (token, head) at token * tok_stride + head * 2d

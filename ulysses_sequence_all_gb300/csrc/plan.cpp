@@ -203,7 +203,8 @@ void build_row_tiles(const Plan& p, const ChunkRows& rows, int64_t tile_rows, Ro
     a->total_units = total;
 }
 
-void build_fused_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_unit, FusedArgs* a)
+void build_fused_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_unit,
+                       int64_t block_tokens, int units_per_block, FusedArgs* a)
 {
     const int W = p.W;
     a->W = W;
@@ -212,7 +213,9 @@ void build_fused_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_
     a->N = p.N;
     a->b = p.b;
     a->tokens_per_unit = int32_t(tokens_per_unit);
-    int64_t total = 0;
+    a->block_tokens = int32_t(block_tokens);
+    a->units_per_block = units_per_block;
+    int64_t total = 0;  // blocks
     for (int k = 0; k < kMaxW; ++k) {
         const bool live = k < W;
         a->s[k] = live ? p.s[k] : 0;
@@ -222,11 +225,11 @@ void build_fused_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_
         a->row_lo[k] = live ? rows.lo[k] : 0;
         a->rows[k] = live ? rows.cnt[k] : 0;
         a->unit_begin[k] = total;
-        a->blocks[k] = live ? ceil_div(a->rows[k], tokens_per_unit) : 0;
+        a->blocks[k] = live ? ceil_div(a->rows[k], block_tokens) : 0;
         total += p.b * a->blocks[k];
     }
     a->unit_begin[kMaxW] = total;
-    a->total_units = total;
+    a->total_units = total * units_per_block;
 }
 
 void build_fused_bwd_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_unit,

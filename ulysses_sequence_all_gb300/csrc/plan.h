@@ -91,10 +91,16 @@ struct RowRing {
 void build_row_tiles(const Plan& p, const ChunkRows& rows, int64_t tile_rows, RowTileArgs* a);
 
 // ---- fused QK kernel's argument block ---------------------------------------------------------
-// A work unit is `tokens_per_unit` consecutive source rows (tokens) of one shard q and one batch
-// index; it covers all N heads of both q and k for those tokens.
-// With `interleaved` set the input is qkv_in[q], one (b, s_q, 3, N, d) tensor per rank (planes q,
-// k, v), a unit covers the token block's three planes, and v_out receives v unchanged.
+// Work is cut into blocks of `block_tokens` consecutive source rows (tokens) of one shard q and one
+// batch index, and each block into `units_per_block` work units:
+//  * separate q and k inputs: one unit per block (block_tokens = tokens_per_unit), all N heads of
+//    q and of k for those tokens;
+//  * `interleaved` (qkv_in[q], one (b, s_q, 3, N, d) tensor per rank, planes q, k, v): three units
+//    per block of 2 * tokens_per_unit tokens: the q and k rows of its first tokens_per_unit tokens,
+//    those of the next tokens_per_unit, and the v rows of all of them, which v_out receives
+//    unchanged. Each unit fills the same stage size, and consecutive units of a CTA rotate through
+//    the three kinds.
+// unit_begin counts blocks; total_units counts units.
 struct FusedArgs {
     const uint8_t* q_in[kMaxW];
     const uint8_t* k_in[kMaxW];
@@ -113,6 +119,7 @@ struct FusedArgs {
     int64_t S, N, b;
     int64_t total_units;
     int32_t W, d, tokens_per_unit, stages;
+    int32_t block_tokens, units_per_block;
     int32_t ctas_per_sm;  // resident CTAs per SM the shared-memory footprint allows
     uint32_t stage_bytes;
     float eps;
@@ -121,7 +128,8 @@ struct FusedArgs {
     float turn_lo[kMaxFusedD / 2];
 };
 
-void build_fused_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_unit, FusedArgs* a);
+void build_fused_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_unit,
+                       int64_t block_tokens, int units_per_block, FusedArgs* a);
 
 // ---- fused QK backward's argument block -------------------------------------------------------
 // A token block is tokens_per_unit consecutive rows (tokens) of one shard q and one batch index;
