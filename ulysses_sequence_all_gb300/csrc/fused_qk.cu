@@ -10,7 +10,9 @@
 // two contiguous spans of the sequence-side tensors. An interleaved (b, s, 3, N, d) input is cut
 // into blocks of twice as many tokens with three units each (the q and k rows of the first half,
 // of the second half, and the v rows of the whole block), so that every unit fills the same
-// stage and the v rows pass through without arithmetic. Warp roles per CTA:
+// stage and the v rows pass through without arithmetic. The grid takes every q,k unit first and
+// then every v unit: at any time it writes 16 destination streams (q, k of 8 ranks) or 8 (v),
+// not 24, which measured 6.5% faster than rotating through the three kinds. Warp roles per CTA:
 //  * loader: lane 0 waits for the stage to be free ("empty" mbarrier), starts the cp.async.bulk
 //    loads (completing on the stage's "full" mbarrier as transaction bytes) and leaves a record
 //    of the unit beside the stage; while the copies fly, all lanes fill the stage's cos/sin
@@ -119,9 +121,15 @@ __device__ __forceinline__ FusedUnit fused_decode(const FusedArgs& a, int64_t u)
     FusedUnit t;
     int64_t blk_id = u;
     t.kind = 0;
-    if (a.units_per_block == 3) {
-        blk_id = div_fast(u, 3);
-        t.kind = int(u - 3 * blk_id);
+    if (a.units_per_block == 3) {  // two phases: every q,k unit (two per block), then every v unit
+        const int64_t blocks_all = a.total_units / 3;
+        if (u < 2 * blocks_all) {
+            blk_id = u >> 1;
+            t.kind = int(u & 1);
+        } else {
+            blk_id = u - 2 * blocks_all;
+            t.kind = 2;
+        }
     }
     int lo = 0, hi = a.W - 1;
     while (lo < hi) {

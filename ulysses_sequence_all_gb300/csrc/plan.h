@@ -98,8 +98,8 @@ void build_row_tiles(const Plan& p, const ChunkRows& rows, int64_t tile_rows, Ro
 //  * `interleaved` (qkv_in[q], one (b, s_q, 3, N, d) tensor per rank, planes q, k, v): three units
 //    per block of 2 * tokens_per_unit tokens: the q and k rows of its first tokens_per_unit tokens,
 //    those of the next tokens_per_unit, and the v rows of all of them, which v_out receives
-//    unchanged. Each unit fills the same stage size, and consecutive units of a CTA rotate through
-//    the three kinds.
+//    unchanged. Each unit fills the same stage size. Units 0 .. 2B-1 (B blocks) are the q,k units
+//    (two per block, in block order), units 2B .. 3B-1 the v units.
 // unit_begin counts blocks; total_units counts units.
 struct FusedArgs {
     const uint8_t* q_in[kMaxW];
@@ -133,7 +133,8 @@ void build_fused_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_
 
 // ---- fused QK backward's argument block -------------------------------------------------------
 // A token block is tokens_per_unit consecutive rows (tokens) of one shard q and one batch index;
-// it makes one work unit per tensor (unit u: tensor u mod tensors). A unit reads the tensor's
+// it makes one work unit per tensor (for q, k: unit u is tensor u mod 2 of block u div 2; for the
+// interleaved q, k, v: unit u is tensor u div B of block u mod B, B blocks). A unit reads the tensor's
 // forward input for those tokens (all N heads: one contiguous span on the sequence side) and the
 // gradient of its output (W runs, rank r's n_r heads of those tokens, contiguous on rank r's head
 // side), and writes the gradient of the input (one span on the sequence side).
