@@ -42,9 +42,9 @@ static __device__ unsigned g_relayout_status;
 #ifndef ULY_VEC_UNROLL
 #define ULY_VEC_UNROLL 4
 #endif
-// Loads in flight ahead of the unit being stored, per mode. Mode 0 loads one long span and stores
-// many short runs; mode 1 gathers short runs and stores one span, and measures faster with more of
-// the ring left to store groups (at the Wan shape: 6,020 GB/s with 3 loads ahead, 6,360 with 2).
+// Loads in flight ahead of the unit being stored by the segment kernel (relayout_tma_kernel), per
+// mode: mode 0 loads strided runs and stores one span, mode 1 the reverse. The row-tile kernel's
+// lookahead is chosen per plan instead (relayout_row_ring).
 #ifndef ULY_TMA_LOOKAHEAD0
 #define ULY_TMA_LOOKAHEAD0 3
 #endif
