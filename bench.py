@@ -730,6 +730,34 @@ def run_configs(args):
                      "median_ms": round(ms, 4), "GB/s": round(gbs, 1),
                      "frac_of_peak": round(gbs / peak, 4)})
         del q, k, qo, ko, dq, dk, ws
+
+    # the interleaved (b, s, 3, N, d) call and its backward on the long packed-QKV geometry
+    cfg = wl.Workload("long_qkv_interleaved", 4, 1, (62500,) * 4, (14,) * 4, 128, "bfloat16",
+                      seed=20)
+    plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
+    qkv = [torch.stack(list(planes), dim=2) for planes in
+           zip(*(wl.seq_side_inputs(cfg, "cuda", seed=sd) for sd in (3, 4, 5)))]
+    w = wl.rms_weights(cfg.d).cuda()
+    outs = [[torch.empty(cfg.head_side_shape(r), dtype=torch.bfloat16, device="cuda")
+             for r in range(cfg.W)] for _ in range(3)]
+    side = cfg.plane_bytes()
+    ms = timed(lambda: B.ulysses_a2a_4d_qkv_fused(plan, qkv, outs[0], outs[1], outs[2], w, EPS,
+                                                  THETA, stream))
+    gbs = 6 * side / (ms * 1e-3) / 1e9
+    rows.append({"config": cfg.name, "kernel": "qkv_fused", "W": cfg.W, "dtype": cfg.dtype,
+                 "rope_pairs": "adjacent", "bytes": 6 * side, "median_ms": round(ms, 4),
+                 "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)})
+    dqkv = [torch.empty_like(t) for t in qkv]
+    dw = torch.empty((2, cfg.d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(B.ulysses_qk_fused_backward_workspace(plan), dtype=torch.uint8, device="cuda")
+    ms = timed(lambda: B.ulysses_a2a_4d_qkv_fused_backward(plan, dqkv, qkv, outs[0], outs[1],
+                                                           outs[2], w, dw, EPS, THETA, ws, stream))
+    gbs = 8 * side / (ms * 1e-3) / 1e9
+    rows.append({"config": cfg.name, "kernel": "qkv_fused_backward", "W": cfg.W,
+                 "dtype": cfg.dtype, "rope_pairs": "adjacent", "bytes": 8 * side,
+                 "median_ms": round(ms, 4), "GB/s": round(gbs, 1),
+                 "frac_of_peak": round(gbs / peak, 4)})
+    del qkv, outs, dqkv, ws
     assert B.ulysses_device_status() == 0, "a kernel recorded a wait timeout"
     print(json.dumps({"configs": rows, "peak": peak, "peak_source": f"{peak_kind} hbm_gbs",
                       "note": "parity-test configurations, timed for context; not bench lines"}),
