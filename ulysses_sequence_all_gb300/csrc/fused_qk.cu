@@ -69,11 +69,6 @@ static __device__ unsigned g_fused_status;
 constexpr int kFusedCtasPerSm = ULY_FUSED_CTAS_PER_SM;
 constexpr int kFusedMaxStages = ULY_FUSED_MAX_STAGES;
 constexpr int kFusedDrain = ULY_FUSED_DRAIN;  // store groups left draining when a stage refills
-// an SM holds 228 KiB of shared memory, 1 KiB of it reserved per resident CTA; one CTA may use
-// at most 227 KiB of dynamic shared memory
-constexpr int kSmemPerSm = 228 * 1024;
-constexpr int kSmemReservedPerCta = 1024;
-constexpr int kSmemPerCtaMax = 227 * 1024;
 constexpr int kFusedHeader = 256;  // three barriers per stage, then one unit record per stage
 constexpr int kFusedRecordsAt = 128;
 static_assert(3 * 8 * kFusedMaxStages <= kFusedRecordsAt, "stage barriers must fit the header");
@@ -160,32 +155,6 @@ __device__ __forceinline__ FusedUnit fused_decode(const FusedArgs& a, int64_t u)
     return t;
 }
 
-// Position in the ring of K stages: the stage of the current unit and the parity of its use
-// (unit j uses stage j mod K for the (j div K)-th time), advanced without division.
-struct FusedRing {
-    int s = 0;
-    uint32_t phase = 0;
-    __device__ __forceinline__ void next(int K)
-    {
-        if (++s == K) {
-            s = 0;
-            phase ^= 1u;
-        }
-    }
-};
-
-// cos and sin of 2 pi * frac(p * (hi + lo)), p a non-negative integer below 2^24.
-__device__ __forceinline__ float2 rope_cos_sin(float p, float hi, float lo)
-{
-    const float ph = p * hi;
-    const float pe = fmaf(p, hi, -ph);  // exact residual of the product
-    float f = ph - rintf(ph);           // exact: drops whole turns
-    f += fmaf(p, lo, pe);
-    float s, c;
-    sincospif(2.0f * f, &s, &c);
-    return make_float2(c, s);
-}
-
 // Shared-memory layout (byte offsets), shared by the kernel and its launcher.
 struct FusedSmem {
     int turns;      // float2 (hi, lo) per pair j < d/2
@@ -259,7 +228,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
         // arrive on "full", so a consumer that sees the phase complete sees data, table and
         // record.
         int64_t j = 0;
-        FusedRing ring;
+        StageRing ring;
         for (; j < n; ++j, ring.next(K)) {
             const int s = ring.s;
             int ok = 1;
@@ -324,7 +293,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
         // tensor. A stage is handed back to the loader kFusedDrain units later, once its stores
         // have read it.
         int64_t j = 0;
-        FusedRing ring;
+        StageRing ring;
         for (; j < n; ++j, ring.next(K)) {
             const int s = ring.s;
             if (!__all_sync(0xffffffffu, fused_wait(&computed[s], ring.phase))) {
@@ -380,7 +349,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     const int full_m_lo = cwi * full_steps / HALF_NW, full_m_hi = (cwi + 1) * full_steps / HALF_NW;
     const int full_base_tok = full_m_lo * PER_STEP / N;
     const int full_base_head = full_m_lo * PER_STEP - full_base_tok * N;
-    FusedRing ring;
+    StageRing ring;
     for (int64_t k = 0; k < n; ++k, ring.next(K)) {
         const int s = ring.s;
         if (!__all_sync(0xffffffffu, fused_wait(&full[s], ring.phase))) {

@@ -62,9 +62,6 @@ constexpr int kBwdCtasPerSm = ULY_BWD_CTAS_PER_SM;
 constexpr int kBwdMaxStages = ULY_BWD_MAX_STAGES;
 constexpr int kBwdNW = ULY_BWD_CONSUMER_WARPS;
 constexpr int kBwdIlp = ULY_BWD_ILP;
-constexpr int kBwdSmemPerSm = 228 * 1024;
-constexpr int kBwdSmemReservedPerCta = 1024;
-constexpr int kBwdSmemPerCtaMax = 227 * 1024;
 constexpr int kBwdHeader = 256;  // three barriers per stage, then one unit record per stage
 constexpr int kBwdRecordsAt = 128;
 static_assert(3 * 8 * kBwdMaxStages <= kBwdRecordsAt, "stage barriers must fit the header");
@@ -127,33 +124,6 @@ __device__ __forceinline__ BwdUnit bwd_decode(const FusedBwdArgs& a, int64_t u)
     x.i0 = a.row_lo[lo] + blk * T;
     x.ntok = int(min(T, a.rows[lo] - blk * T));
     return x;
-}
-
-// Position in the ring of K stages: the stage of the current unit and the parity of its use
-// (units j = 0, 1, ... use stage j mod K for the (j div K)-th time), advanced without division.
-struct BwdRing {
-    int s = 0;
-    uint32_t phase = 0;
-    __device__ __forceinline__ void next(int K)
-    {
-        if (++s == K) {
-            s = 0;
-            phase ^= 1u;
-        }
-    }
-};
-
-// cos and sin of 2 pi * frac(p * (hi + lo)), p a non-negative integer below 2^24; the angle is
-// reduced in turns with an error-free product (see the forward kernel).
-__device__ __forceinline__ float2 bwd_cos_sin(float p, float hi, float lo)
-{
-    const float ph = p * hi;
-    const float pe = fmaf(p, hi, -ph);
-    float f = ph - rintf(ph);
-    f += fmaf(p, lo, pe);
-    float s, c;
-    sincospif(2.0f * f, &s, &c);
-    return make_float2(c, s);
 }
 
 // Shared-memory layout (byte offsets), shared by the kernel and its launcher.
@@ -230,7 +200,7 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
         // (interleaved QKV) has no input: its gradient rows land at the start of the stage and
         // leave unchanged (mode 1).
         int64_t j = 0;
-        BwdRing ring;
+        StageRing ring;
         for (; j < n; ++j, ring.next(K)) {
             const int s = ring.s;
             int ok = 1;
@@ -280,7 +250,7 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
             for (int e = lane; e < (is_v ? 0 : t.ntok * HALF); e += 32) {
                 const int tok = e / HALF, jj = e % HALF;
                 const float2 tj = turns[jj];
-                const float2 cs = bwd_cos_sin(p0 + float(tok), tj.x, tj.y);
+                const float2 cs = rope_cos_sin(p0 + float(tok), tj.x, tj.y);
                 const int at = ((tok * 2 + ((jj >> 1) & 1)) * G + (jj >> 2)) * 4 + (jj & 1);
                 table[at] = cs.x;
                 table[at + 2] = cs.y;
@@ -301,7 +271,7 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
 
     if (warp == kBwdStorerWarp) {  // the unit's dx rows (one store, or one per token), then free
         if (lane != 0) return;
-        BwdRing ring;
+        StageRing ring;
         for (int64_t j = 0; j < n; ++j, ring.next(K)) {
             const int s = ring.s;
             if (!bwd_wait(&computed[s], ring.phase)) {
@@ -371,7 +341,7 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
             aO[h] = make_float2(0.f, 0.f);
         }
     };
-    BwdRing ring;
+    StageRing ring;
     for (int64_t k = 0; k < n; ++k, ring.next(K)) {
         const int s = ring.s;
         if (!__all_sync(0xffffffffu, bwd_wait(&full[s], ring.phase))) {
@@ -539,13 +509,13 @@ void fused_bwd_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages,
     int64_t T0 = ULY_BWD_STAGE_TARGET / tok_bytes;
     if (T0 < 1) T0 = 1;
     for (int ctas = kBwdCtasPerSm; ctas >= 1; --ctas) {
-        const int budget = kBwdSmemPerSm / ctas - kBwdSmemReservedPerCta;
+        const int budget = kSmemPerSm / ctas - kSmemReservedPerCta;
         for (int64_t T = T0; T >= 1; T = T > 1 ? T / 2 : 0) {
             const int64_t sb = T * tok_bytes;
             if (sb >= (1 << 20)) continue;  // an mbarrier counts fewer than 2^20 bytes
             for (int K = kBwdMaxStages; K >= 2; --K) {
                 const BwdSmem m = bwd_smem_layout(int(p.d), int(T), K, uint32_t(sb));
-                if (m.total <= budget && m.total <= kBwdSmemPerCtaMax) {
+                if (m.total <= budget && m.total <= kSmemPerCtaMax) {
                     *tokens_per_unit = T;
                     *stages = K;
                     *stage_bytes = uint32_t(sb);
@@ -568,7 +538,7 @@ static cudaError_t bwd_launch_g(const FusedBwdArgs& a, cudaStream_t stream, int 
     if (device >= 0 && device < 64 && !(g_bwd_smem_set[device].load() & bit)) {
         cudaError_t e = cudaFuncSetAttribute(fused_qk_bwd_kernel<G, F16, HALF>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kBwdSmemPerCtaMax);
+                                             kSmemPerCtaMax);
         if (e != cudaSuccess) return e;
         g_bwd_smem_set[device].fetch_or(bit);
     }

@@ -19,6 +19,34 @@
 
 namespace uly {
 
+// Position in a ring of K shared-memory stages: the stage of the current unit and the parity of
+// its use (unit j uses stage j mod K for the (j div K)-th time), advanced without division.
+struct StageRing {
+    int s = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next(int K)
+    {
+        if (++s == K) {
+            s = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// cos and sin of 2 pi * frac(p * (hi + lo)), p a non-negative integer below 2^24: the angle in
+// turns, with p * hi split exactly into a product and its fma residual (an error-free product),
+// the whole turns dropped (exact), then the small terms added.
+__device__ __forceinline__ float2 rope_cos_sin(float p, float hi, float lo)
+{
+    const float ph = p * hi;
+    const float pe = fmaf(p, hi, -ph);  // exact residual of the product
+    float f = ph - rintf(ph);           // exact: drops whole turns
+    f += fmaf(p, lo, pe);
+    float s, c;
+    sincospif(2.0f * f, &s, &c);
+    return make_float2(c, s);
+}
+
 template <bool F16>
 struct ElemT;
 

@@ -9,6 +9,12 @@ namespace uly {
 // an error in the device status word and lets the kernel return.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// Shared memory of one SM (GB300): 228 KiB per SM, 1 KiB of it reserved per resident CTA, and at
+// most 227 KiB of dynamic shared memory for one CTA.
+constexpr int kSmemPerSm = 228 * 1024;
+constexpr int kSmemReservedPerCta = 1024;
+constexpr int kSmemPerCtaMax = 227 * 1024;
+
 // Bits of the device status word.
 constexpr unsigned kStatusWaitTimeout = 1u;
 constexpr unsigned kStatusDrainTimeout = 2u;
@@ -140,17 +146,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
         : "memory");
 }
 
-// Same, with an L2 eviction-priority hint (a createpolicy value).
-__device__ __forceinline__ void bulk_g2s_hint(void* dst_smem, const void* src_gmem, uint32_t bytes,
-                                              uint64_t* bar, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst_smem)),
-        "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
 // Bulk copy shared -> global, tracked by this thread's bulk async-groups.
 __device__ __forceinline__ void bulk_s2g(void* dst_gmem, const void* src_smem, uint32_t bytes)
 {
@@ -173,13 +168,6 @@ template <int N>
 __device__ __forceinline__ void bulk_wait()
 {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
 }
 
 // 16-byte global load that bypasses L1 (data is read once) and 16-byte store.

@@ -352,12 +352,6 @@ int64_t relayout_unit_bytes(int engine) { return engine == ULY_ENGINE_VEC ? ULY_
 // per device: whether the TMA kernels' shared-memory limit has been raised (any host thread)
 static std::atomic<int> g_smem_set[64];
 
-// one CTA may use at most 227 KiB of dynamic shared memory; an SM holds 228 KiB, 1 KiB of it
-// reserved per resident CTA
-constexpr int kSmemPerCtaMax = 227 * 1024;
-constexpr int kSmemPerSm = 228 * 1024;
-constexpr int kSmemReservedPerCta = 1024;
-
 // Raise every TMA kernel's dynamic shared-memory limit to the per-CTA maximum, once per device.
 static cudaError_t ensure_tma_smem(int device)
 {
