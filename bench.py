@@ -164,19 +164,34 @@ class Workload:
                                   B.ulysses_plan_num_chunks(self.plan, 1))
 
     def step(self, stream, ev=None):
+        """One exchange step on `stream`; `ev`, if given, holds three events recorded after the
+        fused call, after the v relayout and after the attention-output relayout."""
         B = self.B
-        if ev:
-            ev[0].record(stream)
         B.ulysses_a2a_4d_qk_fused(self.plan, self.q, self.k, self.qo, self.ko, self.w, EPS, THETA,
                                   stream)
         if ev:
-            ev[1].record(stream)
+            ev[0].record(stream)
         B.ulysses_a2a_4d(self.plan, 0, self.v, self.vo, stream)
         if ev:
-            ev[2].record(stream)
+            ev[1].record(stream)
         B.ulysses_a2a_4d(self.plan, 1, self.o, self.oo, stream)
         if ev:
-            ev[3].record(stream)
+            ev[2].record(stream)
+
+
+def back_to_back_ms(torch, stream, fn, n):
+    """Durations (ms) of n launches of fn enqueued back to back, from CUDA events recorded on
+    `stream` between consecutive calls. One call is enqueued before the first event, so the GPU is
+    busy whenever an event is recorded and the host's launch latency is not counted (an event
+    recorded on an idle GPU would time the host's enqueueing of the next call as well)."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    fn()
+    evs[0].record(stream)
+    for i in range(n):
+        fn()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
 
 
 def d2d_gbs(torch, nbytes, reps=20):
@@ -359,27 +374,12 @@ def run_ours(args):
     torch.cuda.synchronize()
     assert B.ulysses_device_status() == 0
 
-    # per-kernel timing pass (events between launches, on the launching stream)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    kt = {"fused_qk": [], "mode0": [], "mode1": []}
-    for _ in range(min(args.steps, 50)):
-        wk.step(stream, ev)
-        torch.cuda.synchronize()
-        kt["fused_qk"].append(ev[0].elapsed_time(ev[1]))
-        kt["mode0"].append(ev[1].elapsed_time(ev[2]))
-        kt["mode1"].append(ev[2].elapsed_time(ev[3]))
-
     # outside the step: the interleaved (b, s, 3, N, d) QKV form of its first two launches
     qkv = [torch.stack([a, b, c], dim=2) for a, b, c in zip(wk.q, wk.k, wk.v)]
-    qkv_ms = []
-    for rep in range(min(args.steps, 20) + 3):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+    for _ in range(3):
         B.ulysses_a2a_4d_qkv_fused(wk.plan, qkv, wk.qo, wk.ko, wk.vo, wk.w, EPS, THETA, stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if rep >= 3:
-            qkv_ms.append(e0.elapsed_time(e1))
+    qkv_ms = back_to_back_ms(torch, stream, lambda: B.ulysses_a2a_4d_qkv_fused(
+        wk.plan, qkv, wk.qo, wk.ko, wk.vo, wk.w, EPS, THETA, stream), min(args.steps, 20))
     del qkv
 
     # outside the step: the backward of the fused call (dq, dk and dw from the gradients of q_out
@@ -389,30 +389,35 @@ def run_ours(args):
     dw = torch.empty((2, wk.cfg.d), dtype=torch.float32, device="cuda")
     ws = torch.empty(B.ulysses_qk_fused_backward_workspace(wk.plan), dtype=torch.uint8,
                      device="cuda")
-    bwd_ms = []
-    for rep in range(min(args.steps, 20) + 3):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        B.ulysses_a2a_4d_qk_fused_backward(wk.plan, dq, dk, wk.q, wk.k, wk.qo, wk.ko, wk.w, dw,
-                                           EPS, THETA, ws, stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if rep >= 3:
-            bwd_ms.append(e0.elapsed_time(e1))
+    bwd = lambda: B.ulysses_a2a_4d_qk_fused_backward(  # noqa: E731
+        wk.plan, dq, dk, wk.q, wk.k, wk.qo, wk.ko, wk.w, dw, EPS, THETA, ws, stream)
+    for _ in range(3):
+        bwd()
+    bwd_ms = back_to_back_ms(torch, stream, bwd, min(args.steps, 20))
     # the backward of the interleaved form: packed dqkv from the three output gradients
     qkv = [torch.stack([a, b, c], dim=2) for a, b, c in zip(wk.q, wk.k, wk.v)]
     dqkv = [torch.empty_like(t) for t in qkv]
-    qkv_bwd_ms = []
-    for rep in range(min(args.steps, 20) + 3):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        B.ulysses_a2a_4d_qkv_fused_backward(wk.plan, dqkv, qkv, wk.qo, wk.ko, wk.vo, wk.w, dw, EPS,
-                                            THETA, ws, stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if rep >= 3:
-            qkv_bwd_ms.append(e0.elapsed_time(e1))
+    qkv_bwd = lambda: B.ulysses_a2a_4d_qkv_fused_backward(  # noqa: E731
+        wk.plan, dqkv, qkv, wk.qo, wk.ko, wk.vo, wk.w, dw, EPS, THETA, ws, stream)
+    for _ in range(3):
+        qkv_bwd()
+    qkv_bwd_ms = back_to_back_ms(torch, stream, qkv_bwd, min(args.steps, 20))
     del dq, dk, dw, ws, qkv, dqkv
+
+    # Per-kernel durations: the same steps enqueued back to back, one event per kernel boundary
+    # (bounds[3 i] precedes step i's fused call, bounds[3 i + 1..3] follow its three launches).
+    # The GPU stays busy across the pass, so consecutive events time each launch without the
+    # host's launch latency. Kept out of the timed region, whose steps carry no extra events.
+    nk = max(2, min(args.steps, 50))
+    bounds = [torch.cuda.Event(enable_timing=True) for _ in range(3 * nk + 1)]
+    wk.step(stream)  # keeps the GPU busy while bounds[0] is recorded
+    bounds[0].record(stream)
+    for i in range(nk):
+        wk.step(stream, bounds[3 * i + 1:3 * i + 4])
+    torch.cuda.synchronize()
+    kt = {name: [bounds[3 * i + j].elapsed_time(bounds[3 * i + j + 1]) for i in range(nk)]
+          for j, name in enumerate(("fused_qk", "mode0", "mode1"))}
+    del bounds
 
     clocks = ClockSampler(local)
     clocks.start()
