@@ -649,16 +649,7 @@ def run_configs(args):
     def timed(fn, reps=20, warm=5):
         for _ in range(warm):
             fn()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(reps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
+        return statistics.median(back_to_back_ms(torch, stream, fn, reps))
 
     rows = []
     for cfg in wl.UNEVEN:
