@@ -519,8 +519,8 @@ def torch_gpu_step(torch, wk, stream, reps=5):
     (the single-GPU analogue of the pages' baseline, a permute + all-to-all + permute with the
     norm and the rotation as separate kernels): per output rank one torch.cat of the slices each
     input rank sends, and for q and k an fp32 RMSNorm and adjacent-pair RoPE (cos/sin of every
-    position built once, outside the timing) before the cat. Not the product path; timed with
-    CUDA events on the same tensors, median of `reps`."""
+    position built once, outside the timing) before the cat. Not the product path; timed back to
+    back with CUDA events like the library's calls, on the same tensors, median of `reps`."""
     cfg = wk.cfg
     W, d = cfg.W, cfg.d
     seq_off = [sum(cfg.seq_splits[:q]) for q in range(W)]
@@ -558,16 +558,7 @@ def torch_gpu_step(torch, wk, stream, reps=5):
     with torch.cuda.stream(stream):
         for name, (fn, nbytes) in ops.items():
             fn()
-            ts = []
-            for _ in range(reps):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                torch.cuda.synchronize()
-                a.record(stream)
-                fn()
-                b.record(stream)
-                torch.cuda.synchronize()
-                ts.append(a.elapsed_time(b))
-            ms = statistics.median(ts)
+            ms = statistics.median(back_to_back_ms(torch, stream, fn, reps))
             out[name] = {"median_ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
     return out
 
