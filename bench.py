@@ -69,8 +69,105 @@ def dist_env():
 # ------------------------------------------------------------------------------------------------
 # clocks
 # ------------------------------------------------------------------------------------------------
-class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+def _reason_summary(rows):
+    """Union of the active throttle reasons over sample rows (dicts with a 'reasons' set)."""
+    out = set()
+    for r in rows:
+        out |= r["reasons"]
+    return sorted(out)
+
+
+class NvmlSampler:
+    """SM clock, power and clock-event (throttle) reasons of one GPU, read through NVML
+    (libnvidia-ml via ctypes; read-only queries, no setting is changed) every `period_s` on a
+    background thread, each sample with its host time. At 2 ms a timed region of a few tens of
+    milliseconds holds samples, which a 50 ms nvidia-smi poll would miss."""
+
+    CLOCK_SM = 1  # NVML_CLOCK_SM
+    REASON_BITS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
+                   ("hw_thermal_slowdown", 0x40), ("hw_power_brake_slowdown", 0x80))
+
+    def __init__(self, cuda_index: int, period_s: float = 0.002):
+        import ctypes
+        self.ct = ctypes
+        self.period = period_s
+        self.samples = []
+        self.marks = {}
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        ok = False
+        try:  # the CUDA device's own UUID: robust to CUDA_VISIBLE_DEVICES renumbering
+            import torch
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(cuda_index).uuid)
+            ok = self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) == 0
+        except Exception:  # noqa: BLE001
+            ok = False
+        if not ok:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            ids = [v for v in vis.split(",") if v.strip().isdigit()]
+            idx = int(ids[cuda_index]) if cuda_index < len(ids) else cuda_index
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.dev)) != 0:
+                raise OSError("no NVML handle for the device")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.max_mhz = (float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(
+            self.dev, self.CLOCK_SM, ctypes.byref(mx)) == 0 else None)
+        self._stop = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+
+    def _read(self):
+        ct = self.ct
+        clk, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        t = time.perf_counter()
+        sm = float(clk.value) if self.lib.nvmlDeviceGetClockInfo(self.dev, self.CLOCK_SM,
+                                                                  ct.byref(clk)) == 0 else None
+        watts = pw.value / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.dev, ct.byref(pw)) == 0 else None
+        bits = rs.value if self.reasons_fn(self.dev, ct.byref(rs)) == 0 else 0
+        return {"t": t, "sm": sm, "w": watts,
+                "reasons": {name for name, bit in self.REASON_BITS if bits & bit}}
+
+    def _run(self):
+        while not self._stop.is_set():
+            self.samples.append(self._read())
+            self._stop.wait(self.period)
+
+    def start(self):
+        self.thread.start()
+        time.sleep(0.05)
+
+    def mark(self, which):
+        self.marks[which] = time.perf_counter()
+
+    def window(self, t0, t1):
+        """Summary of the samples taken between host times t0 and t1."""
+        inside = [r for r in self.samples if t0 <= r["t"] <= t1]
+        sm = [r["sm"] for r in inside if r["sm"] is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": _reason_summary(inside), "samples": len(inside),
+                "power_w_max": max((r["w"] or 0.0) for r in inside) if inside else None}
+
+    def stop(self):
+        self._stop.set()
+        self.thread.join(timeout=5)
+        self.lib.nvmlShutdown()
+        t0, t1 = self.marks.get("t0"), self.marks.get("t1")
+        if t0 is None or t1 is None:
+            return None
+        out = self.window(t0, t1)
+        out["samples_in_timed_region"] = out.pop("samples")
+        out["source"] = f"NVML every {self.period * 1e3:.0f} ms, samples inside the timed region"
+        out["timed_region_ms_host"] = round((t1 - t0) * 1e3, 2)
+        k0, k1 = self.marks.get("k0"), self.marks.get("k1")
+        if k0 is not None and k1 is not None:
+            out["per_kernel_pass"] = self.window(k0, k1)
+        return out
+
+
+class SmiSampler:
+    """Fallback when NVML cannot be loaded: nvidia-smi samples (50 ms) of the same fields."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -80,7 +177,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
-        self.t0 = self.t1 = None
+        self.marks = {}
 
     def start(self):
         try:
@@ -97,10 +194,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append((time.time(), line.strip()))
+            self.lines.append((time.perf_counter(), line.strip()))
 
     def mark(self, which):
-        setattr(self, which, time.time())
+        self.marks[which] = time.perf_counter()
 
     def stop(self):
         if self.proc is None:
@@ -111,145 +208,35 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        t0, t1 = self.marks.get("t0"), self.marks.get("t1")
         rows = [(t, l.split(", ")) for t, l in self.lines if l.count(",") >= 8]
-        inside = [r for t, r in rows if self.t0 is not None and self.t0 <= t <= self.t1]
-        use = inside or [r for _, r in rows[-3:]]
-        if not use:
-            return None
+        inside = [r for t, r in rows if t0 is not None and t0 <= t <= t1]
 
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return None
-        sm = [num(r[1]) for r in use if num(r[1]) is not None]
+        sm = [num(r[1]) for r in inside if num(r[1]) is not None]
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in use:
+        for r in inside:
             for name, val in zip(names, r[5:9]):
                 if val.strip().lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": num(use[0][2]), "reasons": sorted(reasons),
-                "samples": len(use), "samples_in_timed_region": len(inside),
-                "power_w_max": max((num(r[3]) or 0.0) for r in use)}
+                "sm_max_mhz": num(rows[0][1][2]) if rows else None, "reasons": sorted(reasons),
+                "samples_in_timed_region": len(inside),
+                "source": "nvidia-smi every 50 ms, samples inside the timed region only "
+                          "(none when the region is shorter than the period)",
+                "power_w_max": max((num(r[3]) or 0.0) for r in inside) if inside else None}
 
 
-# ------------------------------------------------------------------------------------------------
-# the GPU workload
-# ------------------------------------------------------------------------------------------------
-class Workload:
-    def __init__(self, torch, B, wl, device):
-        self.torch, self.B = torch, B
-        cfg = wl.WAN
-        self.cfg = cfg
-        bf16 = torch.bfloat16
-        self.plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
-        self.q = wl.seq_side_inputs(cfg, device, seed=wl.FUSED.seed)
-        self.k = wl.seq_side_inputs(cfg, device, seed=wl.FUSED.extra["k_seed"])
-        self.v = wl.seq_side_inputs(cfg, device, seed=5)
-        self.o = wl.head_side_inputs(cfg, device, seed=6)
-        self.w = wl.rms_weights(cfg.d, seed=wl.FUSED.extra["w_seed"]).to(device)
-        head = [cfg.head_side_shape(r) for r in range(cfg.W)]
-        seq = [cfg.seq_side_shape(q) for q in range(cfg.W)]
-        self.qo = [torch.empty(s, dtype=bf16, device=device) for s in head]
-        self.ko = [torch.empty(s, dtype=bf16, device=device) for s in head]
-        self.vo = [torch.empty(s, dtype=bf16, device=device) for s in head]
-        self.oo = [torch.empty(s, dtype=bf16, device=device) for s in seq]
-        self.side = cfg.plane_bytes()          # one tensor set, all ranks: 774,144,000 bytes
-        self.bytes_fused = 4 * self.side       # q, k in; q, k out
-        self.bytes_plain = 2 * self.side       # in + out
-        self.bytes_step = self.bytes_fused + 2 * self.bytes_plain
-        self.launches_per_step = (B.ulysses_plan_num_chunks(self.plan, 0) * 2 +
-                                  B.ulysses_plan_num_chunks(self.plan, 1))
-
-    def step(self, stream, ev=None):
-        """One exchange step on `stream`; `ev`, if given, holds three events recorded after the
-        fused call, after the v relayout and after the attention-output relayout."""
-        B = self.B
-        B.ulysses_a2a_4d_qk_fused(self.plan, self.q, self.k, self.qo, self.ko, self.w, EPS, THETA,
-                                  stream)
-        if ev:
-            ev[0].record(stream)
-        B.ulysses_a2a_4d(self.plan, 0, self.v, self.vo, stream)
-        if ev:
-            ev[1].record(stream)
-        B.ulysses_a2a_4d(self.plan, 1, self.o, self.oo, stream)
-        if ev:
-            ev[2].record(stream)
-
-
-def back_to_back_ms(torch, stream, fn, n):
-    """Durations (ms) of n launches of fn enqueued back to back, from CUDA events recorded on
-    `stream` between consecutive calls. One call is enqueued before the first event, so the GPU is
-    busy whenever an event is recorded and the host's launch latency is not counted (an event
-    recorded on an idle GPU would time the host's enqueueing of the next call as well)."""
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
-    fn()
-    evs[0].record(stream)
-    for i in range(n):
-        fn()
-        evs[i + 1].record(stream)
-    torch.cuda.synchronize()
-    return [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
-
-
-def d2d_gbs(torch, nbytes, reps=20):
-    """Flat device-to-device copy (cudaMemcpyAsync) of nbytes, counted as read + write."""
-    a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    b = torch.empty_like(a)
-    a.fill_(1)
-    for _ in range(3):
-        b.copy_(a)
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    s.record()
-    for _ in range(reps):
-        b.copy_(a)
-    e.record()
-    torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / reps
-    del a, b
-    return 2 * nbytes / (ms * 1e-3) / 1e9
-
-
-def read_peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def clock_sampler(cuda_index: int):
     try:
-        with open(path) as f:
-            pk = json.load(f)
-        return float(pk["hbm_gbs"]), "measured"
-    except (OSError, KeyError, ValueError):
-        return 6800.0, "fallback"
-
-
-def source_digest(files) -> str | None:
-    """sha256 (first 16 hex digits) of the named csrc files, concatenated in the given order."""
-    import hashlib
-    h = hashlib.sha256()
-    for name in files:
-        try:
-            with open(os.path.join(ROOT, "ulysses_sequence_all_gb300", "csrc", name), "rb") as f:
-                h.update(f.read())
-        except OSError:
-            return None
-    return h.hexdigest()[:16]
-
-
-def read_traffic(kernel: str):
-    """Per-launch DRAM bytes (read + write) from the committed ncu summary, or None when the
-    kernel's sources have changed since the counters were taken. Lines of profiles/traffic.txt:
-    kernel  comma-separated-source-files  digest  bytes-per-launch."""
-    path = os.path.join(ROOT, "profiles", "traffic.txt")
-    try:
-        with open(path) as f:
-            lines = [l.split() for l in f if l.strip() and not l.startswith("#")]
-    except OSError:
-        return None
-    for parts in lines:
-        if len(parts) >= 4 and parts[0] == kernel:
-            return int(parts[3]) if source_digest(parts[1].split(",")) == parts[2] else None
-    return None
+        return NvmlSampler(cuda_index)
+    except (OSError, AttributeError):
+        return SmiSampler(cuda_index)
 
 
 # ------------------------------------------------------------------------------------------------
@@ -289,7 +276,33 @@ def sample_bytes(tokens_per_rank: int) -> int:
     return 4 * side + 2 * (2 * side)
 
 
-def cpu_baseline(budget_s: float = 15.0):
+def host_description():
+    """The host's logical CPU count and CPU model (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.machine()}
+
+
+def oracle_leg(budget_s: float = 15.0):
+    """The single-threaded C oracle on one step of the Wan geometry, a token slice sized to
+    about budget_s seconds."""
     import oracle
     orc = oracle.get()
     t = 64
@@ -307,6 +320,51 @@ def cpu_baseline(budget_s: float = 15.0):
             "sample": (f"one step (fused q,k mode 0 + v mode 0 + o mode 1) on the Wan-720p geometry "
                        f"with {tokens} of 9,450 tokens per rank (W=8, 40 heads, d=128, bf16), "
                        f"single-threaded C oracle, {dt:.1f} s")}
+
+
+def memcpy_leg(reps: int = 5):
+    """The multi-threaded CPU relayout (one memcpy per row and destination rank, rows shared
+    among OpenMP threads; oracle/segment_memcpy.c, byte-equal to the oracle) on the full Wan-720p
+    tensor set: mode 0 of a sequence-side set and mode 1 of a head-side set, every host thread,
+    median of `reps` calls each."""
+    import numpy as np
+    import oracle
+    seg = oracle.SegmentMemcpy()
+    W, N, d, s_local = 8, 40, 128, 9450
+    seq, heads = [s_local] * W, [5] * W
+    rng = np.random.default_rng(3)
+    v = [rng.integers(0, 1 << 16, (1, s_local, N, d), dtype=np.uint16) for _ in range(W)]
+    o = [rng.integers(0, 1 << 16, (1, W * s_local, 5, d), dtype=np.uint16) for _ in range(W)]
+    vo = [np.empty_like(x) for x in o]
+    oo = [np.empty_like(x) for x in v]
+    side = sum(x.nbytes for x in v)
+    threads = seg.max_threads()
+    per_mode = {}
+    for mode, ins, outs in ((0, v, vo), (1, o, oo)):
+        seg.a2a_4d(ins, seq, heads, mode, outs=outs)  # first touch of the outputs
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            seg.a2a_4d(ins, seq, heads, mode, outs=outs)
+            ts.append(time.perf_counter() - t0)
+        per_mode[f"mode{mode}"] = round(2 * side / statistics.median(ts) / 1e9, 3)
+    value = 2 * (2 * side) / (2 * side / (per_mode["mode0"] * 1e9) + 2 * side / (per_mode["mode1"] * 1e9)) / 1e9
+    return {"value": round(value, 3), "unit": "GB/s", "cores": threads,
+            "kind": "segment_memcpy_openmp", **{f"{k}_GBps": v_ for k, v_ in per_mode.items()},
+            "sample": (f"relayout only (no norm or rotation): modes 0 and 1 of the full Wan-720p "
+                       f"tensor set ({side:,} bytes per side), {threads} OpenMP threads, median "
+                       f"of {reps} calls per mode; value = both modes' bytes over both modes' "
+                       f"time")}
+
+
+def cpu_baseline(budget_s: float = 15.0):
+    """Both CPU legs on the host cores: the oracle (single thread, the contract's reported
+    baseline: its figure is `value`) and the multi-threaded memcpy relayout."""
+    orc = oracle_leg(budget_s)
+    out = dict(orc)
+    out["host"] = host_description()
+    out["legs"] = {"oracle_single_thread": orc, "segment_memcpy_all_threads": memcpy_leg()}
+    return out
 
 
 def run_reference(args):
@@ -338,7 +396,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(), "gpu_launches": 0,
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host": host_description()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0}}))
 
@@ -408,19 +466,21 @@ def run_ours(args):
     # (bounds[3 i] precedes step i's fused call, bounds[3 i + 1..3] follow its three launches).
     # The GPU stays busy across the pass, so consecutive events time each launch without the
     # host's launch latency. Kept out of the timed region, whose steps carry no extra events.
+    clocks = clock_sampler(local)
+    clocks.start()
     nk = max(2, min(args.steps, 50))
     bounds = [torch.cuda.Event(enable_timing=True) for _ in range(3 * nk + 1)]
     wk.step(stream)  # keeps the GPU busy while bounds[0] is recorded
     bounds[0].record(stream)
+    clocks.mark("k0")
     for i in range(nk):
         wk.step(stream, bounds[3 * i + 1:3 * i + 4])
     torch.cuda.synchronize()
+    clocks.mark("k1")
     kt = {name: [bounds[3 * i + j].elapsed_time(bounds[3 * i + j + 1]) for i in range(nk)]
           for j, name in enumerate(("fused_qk", "mode0", "mode1"))}
     del bounds
 
-    clocks = ClockSampler(local)
-    clocks.start()
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
@@ -436,6 +496,8 @@ def run_ours(args):
         pg.barrier()
     clock_info = clocks.stop()
     ms, value = aggregate_throughput(start.elapsed_time(end) / args.steps, wk.bytes_step, pg, "cuda")
+    if clock_info and clock_info.get("sm_mhz"):
+        clock_info["ms_per_step_x_sm_mhz"] = round(ms * clock_info["sm_mhz"], 1)
     assert B.ulysses_device_status() == 0, "a kernel recorded a wait timeout"
 
     # end to end through the host-buffer entry points: pinned host in, device, pinned host out
@@ -622,8 +684,42 @@ def run_e2e(torch, B, wk, stream, args):
             "per_call_ms": per_call, "window_ms": [round(w, 3) for w in windows]}
 
 
+def tiny_latency(torch, B, wl, stream, reps=200):
+    """The tiny configuration (W=2, b=1, 16 tokens per rank, 8 heads, d=128, bf16; 65,536 bytes
+    per side) is a latency point: the device time of one mode-0 and one mode-1 launch (CUDA events
+    between back-to-back launches, median), the host time of a whole round trip through the C ABI
+    from Python (perf_counter over `reps` round trips, then one synchronize), and a bit-exact
+    check that the round trip returns the input."""
+    cfg = wl.TINY
+    plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
+    x = wl.seq_side_inputs(cfg, "cuda")
+    y = [torch.empty(cfg.head_side_shape(r), dtype=torch.bfloat16, device="cuda") for r in range(cfg.W)]
+    z = [torch.empty_like(t) for t in x]
+    m0 = lambda: B.ulysses_a2a_4d(plan, 0, x, y, stream)  # noqa: E731
+    m1 = lambda: B.ulysses_a2a_4d(plan, 1, y, z, stream)  # noqa: E731
+    for _ in range(10):
+        m0()
+        m1()
+    us0 = statistics.median(back_to_back_ms(torch, stream, m0, reps)) * 1e3
+    us1 = statistics.median(back_to_back_ms(torch, stream, m1, reps)) * 1e3
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        m0()
+        m1()
+    torch.cuda.synchronize()
+    host_us = (time.perf_counter() - t0) / reps * 1e6
+    exact = all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(x, z))
+    assert exact, "tiny round trip did not return its input"
+    return {"config": cfg.name, "kernel": "relayout round trip (latency point)", "W": cfg.W,
+            "dtype": cfg.dtype, "bytes": cfg.relayout_bytes(), "mode0_device_us": round(us0, 2),
+            "mode1_device_us": round(us1, 2), "round_trip_host_us": round(host_us, 2),
+            "round_trip_bit_exact": exact}
+
+
 def run_configs(args):
-    """Modes 0 and 1 on the parity-test configurations (not the headline): the 12 uneven
+    """The tiny configuration's latency (tiny_latency), then modes 0 and 1 on the parity-test
+    configurations (not the headline): the 12 uneven
     (W, dtype) points (b=2, 75,000 tokens, 40 heads, d=128) and the long packed-QKV geometry
     (W=4, 250,000 tokens, 56 heads; three planes of 896,000,000 bytes per rank, one call per
     plane on views of a (3, b, s, N, d) buffer per rank); then the fused call and its backward on
@@ -642,7 +738,7 @@ def run_configs(args):
             fn()
         return statistics.median(back_to_back_ms(torch, stream, fn, reps))
 
-    rows = []
+    rows = [tiny_latency(torch, B, wl, stream)]
     for cfg in wl.UNEVEN:
         plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
         dt = wl.torch_dtype(cfg.dtype)

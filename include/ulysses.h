@@ -315,7 +315,12 @@ int ulysses_a2a_4d_qk_fused_host(ulysses_plan_t plan, const void* const* q_host_
 
 /* Synchronise the current device, then return in *status the device status word accumulated by
  * this library's kernels since the last call (0 = no kernel timed out) and clear it. Returns
- * ULY_EDEVICE when the word was non-zero. */
+ * ULY_EDEVICE when the word was non-zero. Bits: 1 (a pipeline wait gave up after 2 s: the
+ * outputs of the calls since the last check are incomplete; discard them), 2 (a kernel gave up
+ * waiting for its own bulk copies into shared memory before exiting: such a copy never completed,
+ * so it may still land in shared memory a later kernel owns; discard the outputs and treat the
+ * CUDA context as suspect, i.e. reset it with cudaDeviceReset before further work). Neither bit
+ * is set unless the hardware stalls for seconds. */
 int ulysses_device_status(unsigned* status);
 
 /*

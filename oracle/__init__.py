@@ -18,6 +18,7 @@ from __future__ import annotations
 import ctypes
 import os
 import subprocess
+from concurrent.futures import ThreadPoolExecutor
 from typing import Sequence
 
 import numpy as np
@@ -25,6 +26,8 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(HERE, "ulysses_oracle.c")
 LIBRARY = os.path.join(HERE, "liboracle.so")
+SEGMENT_SOURCE = os.path.join(HERE, "segment_memcpy.c")
+SEGMENT_LIBRARY = os.path.join(HERE, "libsegment_memcpy.so")
 
 _i64 = ctypes.c_int64
 _p = ctypes.c_void_p
@@ -38,6 +41,19 @@ def build(out: str = LIBRARY, source: str = SOURCE) -> str:
     return out
 
 
+def build_segment(out: str = SEGMENT_LIBRARY, source: str = SEGMENT_SOURCE) -> str:
+    """Compile the multi-threaded CPU baseline relayout (segment_memcpy.c, OpenMP)."""
+    cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-fopenmp", "-shared", "-fPIC", "-o", out, source]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def build_all() -> None:
+    """Everything in this directory that compiles: the oracle and the CPU baseline relayout."""
+    build()
+    build_segment()
+
+
 def _needs_build(lib: str, source: str) -> bool:
     return not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(source)
 
@@ -48,6 +64,35 @@ def _i64_array(values: Sequence[int]):
 
 def _ptr_array(arrays):
     return (ctypes.c_void_p * len(arrays))(*[a.ctypes.data for a in arrays])
+
+
+_PART = [ctypes.c_int, ctypes.c_int, _i64, _i64]  # q_lo, q_hi, i_lo, i_hi
+_WHOLE = (0, None, 0, 2 ** 63 - 1)
+
+
+def _parts(seq_splits, threads: int):
+    """(q_lo, q_hi, i_lo, i_hi) ranges that cover every (shard, row) of a call once: each shard's
+    rows cut into about 4 * threads / W pieces, so that `threads` workers stay busy."""
+    W = len(seq_splits)
+    per = max(1, -(-4 * threads // W))
+    out = []
+    for q, s in enumerate(seq_splits):
+        s = int(s)
+        step = max(1, -(-s // per))
+        for lo in range(0, s, step):
+            out.append((q, q + 1, lo, min(s, lo + step)))
+    return out
+
+
+def _run_parts(call, seq_splits, threads: int):
+    """call(q_lo, q_hi, i_lo, i_hi) -> status, over the whole call (threads <= 1) or its parts on
+    a pool of host threads (the oracle's C functions run without the interpreter lock)."""
+    if threads <= 1:
+        q_lo, _, i_lo, i_hi = _WHOLE
+        return [call(q_lo, len(seq_splits), i_lo, i_hi)]
+    parts = _parts(seq_splits, threads)
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        return list(pool.map(lambda pr: call(*pr), parts))
 
 
 class Oracle:
@@ -70,18 +115,24 @@ class Oracle:
         for name in ("orc_qk_fused_A", "orc_qk_fused_B"):
             getattr(lib, name).argtypes = fused_args
             getattr(lib, name).restype = ctypes.c_int
+        lib.orc_qk_fused_A_part.argtypes = fused_args + _PART
+        lib.orc_qk_fused_A_part.restype = ctypes.c_int
         lib.orc_qk_fused_row.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, ctypes.c_int, _i64,
                                          _i64, _i64, _p, _p, ctypes.c_double, ctypes.c_double, _p]
         lib.orc_qk_fused_row.restype = ctypes.c_int
         lib.orc_qkv_fused.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, _p, _p, _p,
                                       ctypes.c_double, ctypes.c_double, _p, _p, _p]
         lib.orc_qkv_fused.restype = ctypes.c_int
+        lib.orc_qkv_fused_part.argtypes = lib.orc_qkv_fused.argtypes + _PART
+        lib.orc_qkv_fused_part.restype = ctypes.c_int
         lib.orc_fused_row_bwd.argtypes = [_p, _p, _i64, _p, ctypes.c_double, ctypes.c_double,
                                           ctypes.c_double, _p, _p]
         lib.orc_fused_row_bwd.restype = None
         lib.orc_qk_fused_bwd.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, _p, _p, _p,
                                          ctypes.c_double, ctypes.c_double, _p, _p]
         lib.orc_qk_fused_bwd.restype = ctypes.c_int
+        lib.orc_qk_fused_bwd_part.argtypes = lib.orc_qk_fused_bwd.argtypes + _PART
+        lib.orc_qk_fused_bwd_part.restype = ctypes.c_int
         lib.orc_rmsnorm.argtypes = [_p, _i64, _p, ctypes.c_double, _p]
         lib.orc_rmsnorm.restype = None
         lib.orc_rope.argtypes = [_p, _i64, ctypes.c_double, ctypes.c_double]
@@ -102,6 +153,8 @@ class Oracle:
         lib.orc_qk_fused_var.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, ctypes.c_int,
                                          ctypes.c_int, _p, _p, ctypes.c_double, ctypes.c_double, _p]
         lib.orc_qk_fused_var.restype = ctypes.c_int
+        lib.orc_qk_fused_var_part.argtypes = lib.orc_qk_fused_var.argtypes + _PART
+        lib.orc_qk_fused_var_part.restype = ctypes.c_int
         lib.orc_fused_row_bwd_var.argtypes = [_p, _p, _i64, ctypes.c_int, _p, ctypes.c_double,
                                               ctypes.c_double, ctypes.c_double, _p, _p]
         lib.orc_fused_row_bwd_var.restype = None
@@ -109,6 +162,8 @@ class Oracle:
                                              ctypes.c_int, _p, _p, _p, ctypes.c_double,
                                              ctypes.c_double, _p, _p]
         lib.orc_qk_fused_bwd_var.restype = ctypes.c_int
+        lib.orc_qk_fused_bwd_var_part.argtypes = lib.orc_qk_fused_bwd_var.argtypes + _PART
+        lib.orc_qk_fused_bwd_var_part.restype = ctypes.c_int
         self.lib = lib
 
     # ---- relayout -------------------------------------------------------------------------
@@ -153,22 +208,30 @@ class Oracle:
         return src_rank.value, src_elem.value
 
     # ---- fused QK RMSNorm + RoPE ----------------------------------------------------------
-    def _fused(self, fn, xs_bf16: Sequence[np.ndarray], seq_splits, head_splits, w, eps, theta):
+    def _fused(self, fn, xs_bf16: Sequence[np.ndarray], seq_splits, head_splits, w, eps, theta,
+               part_fn=None, threads=1):
         W = len(xs_bf16)
         b, d = xs_bf16[0].shape[0], xs_bf16[0].shape[3]
         xs = [np.ascontiguousarray(x).view(np.uint16) for x in xs_bf16]
         w64 = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
         outs = [np.empty(s, dtype=np.float64) for s in self.out_shapes(b, seq_splits, head_splits, d, 0)]
-        rc = fn(W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
+        args = (W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
                 ctypes.cast(_ptr_array(xs), _p), w64.ctypes.data, float(eps), float(theta),
                 ctypes.cast(_ptr_array(outs), _p))
-        if rc != 0:
+        if part_fn is None:
+            rcs = [fn(*args)]
+        else:
+            rcs = _run_parts(lambda *pr: part_fn(*args, *pr), seq_splits, threads)
+        if any(rc != 0 for rc in rcs):
             raise ValueError("oracle rejected the geometry")
         return outs
 
-    def qk_fused_A(self, xs_bf16, seq_splits, head_splits, w, eps, theta):
-        """Transform at the source row, then place (unrounded double outputs)."""
-        return self._fused(self.lib.orc_qk_fused_A, xs_bf16, seq_splits, head_splits, w, eps, theta)
+    def qk_fused_A(self, xs_bf16, seq_splits, head_splits, w, eps, theta, threads=1):
+        """Transform at the source row, then place (unrounded double outputs). threads > 1 splits
+        the call into parts (ranges of shards and rows) computed on that many host threads; the
+        result is the same array."""
+        return self._fused(self.lib.orc_qk_fused_A, xs_bf16, seq_splits, head_splits, w, eps, theta,
+                           part_fn=self.lib.orc_qk_fused_A_part, threads=threads)
 
     def qk_fused_B(self, xs_bf16, seq_splits, head_splits, w, eps, theta):
         """Place the bf16 bytes, then transform at the destination row."""
@@ -188,9 +251,10 @@ class Oracle:
             raise ValueError("oracle rejected the query")
         return y
 
-    def qkv_fused(self, qkv_bf16, seq_splits, head_splits, wq, wk, eps, theta):
+    def qkv_fused(self, qkv_bf16, seq_splits, head_splits, wq, wk, eps, theta, threads=1):
         """Interleaved (b, s_q, 3, N, d) inputs: q and k transformed and placed (double), v placed
-        unchanged (uint16 bf16 bits). Returns (q_outs, k_outs, v_outs), each rank r (b, S, n_r, d)."""
+        unchanged (uint16 bf16 bits). Returns (q_outs, k_outs, v_outs), each rank r (b, S, n_r, d).
+        threads > 1: computed in parts on that many host threads (same result)."""
         W = len(qkv_bf16)
         b, d = qkv_bf16[0].shape[0], qkv_bf16[0].shape[4]
         xs = [np.ascontiguousarray(x).view(np.uint16) for x in qkv_bf16]
@@ -200,12 +264,15 @@ class Oracle:
         qo = [np.empty(s, dtype=np.float64) for s in shapes]
         ko = [np.empty(s, dtype=np.float64) for s in shapes]
         vo = [np.empty(s, dtype=np.uint16) for s in shapes]
-        rc = self.lib.orc_qkv_fused(W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
-                                    ctypes.cast(_ptr_array(xs), _p), wq64.ctypes.data,
-                                    wk64.ctypes.data, float(eps), float(theta),
-                                    ctypes.cast(_ptr_array(qo), _p), ctypes.cast(_ptr_array(ko), _p),
-                                    ctypes.cast(_ptr_array(vo), _p))
-        if rc != 0:
+        args = (W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
+                ctypes.cast(_ptr_array(xs), _p), wq64.ctypes.data, wk64.ctypes.data, float(eps),
+                float(theta), ctypes.cast(_ptr_array(qo), _p), ctypes.cast(_ptr_array(ko), _p),
+                ctypes.cast(_ptr_array(vo), _p))
+        if threads <= 1:
+            rcs = [self.lib.orc_qkv_fused(*args)]
+        else:
+            rcs = _run_parts(lambda *pr: self.lib.orc_qkv_fused_part(*args, *pr), seq_splits, threads)
+        if any(rc != 0 for rc in rcs):
             raise ValueError("oracle rejected the geometry")
         return qo, ko, vo
 
@@ -220,25 +287,46 @@ class Oracle:
                                    float(eps), float(p), float(theta), dx.ctypes.data, dw.ctypes.data)
         return dx, dw
 
-    def qk_fused_bwd(self, x_bf16, g_bf16, seq_splits, head_splits, w, eps, theta):
+    def qk_fused_bwd(self, x_bf16, g_bf16, seq_splits, head_splits, w, eps, theta, threads=1):
         """Backward of the fused mode-0 call for one tensor: forward inputs x (rank q's
         (b, s_q, N, d) bf16) and output gradients g (rank r's (b, S, n_r, d) bf16). Returns
-        (dx per rank in double, (b, s_q, N, d); dw, d values)."""
+        (dx per rank in double, (b, s_q, N, d); dw, d values). threads > 1: computed in parts on
+        that many host threads; dx is the same array, dw the parts' sums added in part order."""
         W = len(x_bf16)
         b, d = x_bf16[0].shape[0], x_bf16[0].shape[3]
         xs = [np.ascontiguousarray(x).view(np.uint16) for x in x_bf16]
         gs = [np.ascontiguousarray(x).view(np.uint16) for x in g_bf16]
         w64 = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
         dx = [np.empty(x.shape, dtype=np.float64) for x in xs]
-        dw = np.full(d, np.nan)  # the oracle clears it
-        rc = self.lib.orc_qk_fused_bwd(W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
-                                       ctypes.cast(_ptr_array(xs), _p),
-                                       ctypes.cast(_ptr_array(gs), _p), w64.ctypes.data,
-                                       float(eps), float(theta), ctypes.cast(_ptr_array(dx), _p),
-                                       dw.ctypes.data)
-        if rc != 0:
+        args = (W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
+                ctypes.cast(_ptr_array(xs), _p), ctypes.cast(_ptr_array(gs), _p), w64.ctypes.data,
+                float(eps), float(theta), ctypes.cast(_ptr_array(dx), _p))
+        return dx, self._bwd_parts(self.lib.orc_qk_fused_bwd, self.lib.orc_qk_fused_bwd_part,
+                                   args, seq_splits, d, threads)
+
+    @staticmethod
+    def _bwd_parts(whole_fn, part_fn, args, seq_splits, d, threads):
+        """dw of a backward call (its dx is written through args): the whole call, or one dw per
+        part (each cleared by the oracle) added in part order."""
+        if threads <= 1:
+            dw = np.full(d, np.nan)  # the oracle clears it
+            if whole_fn(*args, dw.ctypes.data) != 0:
+                raise ValueError("oracle rejected the geometry")
+            return dw
+        parts = _parts(seq_splits, threads)
+        dws = [np.full(d, np.nan) for _ in parts]
+
+        def run(k):
+            return part_fn(*args, dws[k].ctypes.data, *parts[k])
+
+        with ThreadPoolExecutor(max_workers=threads) as pool:
+            rcs = list(pool.map(run, range(len(parts))))
+        if any(rc != 0 for rc in rcs):
             raise ValueError("oracle rejected the geometry")
-        return dx, dw
+        dw = np.zeros(d)
+        for x in dws:
+            dw += x
+        return dw
 
     def rmsnorm(self, x, w, eps):
         x = np.ascontiguousarray(x, dtype=np.float64)
@@ -296,19 +384,24 @@ class Oracle:
                                    float(eps), float(p), float(theta), y.ctypes.data)
         return y
 
-    def qk_fused_var(self, xs, seq_splits, head_splits, w, eps, theta, f16, half_pairs):
-        """The fused call of a variant for one tensor (unrounded double outputs)."""
+    def qk_fused_var(self, xs, seq_splits, head_splits, w, eps, theta, f16, half_pairs, threads=1):
+        """The fused call of a variant for one tensor (unrounded double outputs); threads > 1:
+        computed in parts on that many host threads (same result)."""
         W = len(xs)
         b, d = xs[0].shape[0], xs[0].shape[3]
         xs = [np.ascontiguousarray(x).view(np.uint16) for x in xs]
         w = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
         outs = [np.empty(sh, dtype=np.float64)
                 for sh in self.out_shapes(b, seq_splits, head_splits, d, 0)]
-        rc = self.lib.orc_qk_fused_var(W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
-                                       int(f16), int(half_pairs), ctypes.cast(_ptr_array(xs), _p),
-                                       w.ctypes.data, float(eps), float(theta),
-                                       ctypes.cast(_ptr_array(outs), _p))
-        if rc != 0:
+        args = (W, b, _i64_array(seq_splits), _i64_array(head_splits), d, int(f16),
+                int(half_pairs), ctypes.cast(_ptr_array(xs), _p), w.ctypes.data, float(eps),
+                float(theta), ctypes.cast(_ptr_array(outs), _p))
+        if threads <= 1:
+            rcs = [self.lib.orc_qk_fused_var(*args)]
+        else:
+            rcs = _run_parts(lambda *pr: self.lib.orc_qk_fused_var_part(*args, *pr), seq_splits,
+                             threads)
+        if any(rc != 0 for rc in rcs):
             raise ValueError("oracle rejected the geometry")
         return outs
 
@@ -323,23 +416,57 @@ class Oracle:
                                        dx.ctypes.data, dw.ctypes.data)
         return dx, dw
 
-    def qk_fused_bwd_var(self, xs, gs, seq_splits, head_splits, w, eps, theta, f16, half_pairs):
+    def qk_fused_bwd_var(self, xs, gs, seq_splits, head_splits, w, eps, theta, f16, half_pairs,
+                         threads=1):
+        """Backward of a variant's fused call for one tensor: (dx per rank in double, dw);
+        threads > 1 as qk_fused_bwd."""
         W = len(xs)
         b, d = xs[0].shape[0], xs[0].shape[3]
         xs = [np.ascontiguousarray(x).view(np.uint16) for x in xs]
         gs = [np.ascontiguousarray(x).view(np.uint16) for x in gs]
         w64 = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
         dx = [np.empty(x.shape, dtype=np.float64) for x in xs]
-        dw = np.full(d, np.nan)  # the oracle clears it
-        rc = self.lib.orc_qk_fused_bwd_var(W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
-                                           int(f16), int(half_pairs),
-                                           ctypes.cast(_ptr_array(xs), _p),
-                                           ctypes.cast(_ptr_array(gs), _p), w64.ctypes.data,
-                                           float(eps), float(theta),
-                                           ctypes.cast(_ptr_array(dx), _p), dw.ctypes.data)
+        args = (W, b, _i64_array(seq_splits), _i64_array(head_splits), d, int(f16), int(half_pairs),
+                ctypes.cast(_ptr_array(xs), _p), ctypes.cast(_ptr_array(gs), _p), w64.ctypes.data,
+                float(eps), float(theta), ctypes.cast(_ptr_array(dx), _p))
+        return dx, self._bwd_parts(self.lib.orc_qk_fused_bwd_var, self.lib.orc_qk_fused_bwd_var_part,
+                                   args, seq_splits, d, threads)
+
+
+class SegmentMemcpy:
+    """ctypes view of segment_memcpy.c: the relayout as one memcpy per (row, destination rank) run,
+    rows shared among OpenMP threads. A timed CPU baseline, not the oracle; the tests check its
+    bytes against the oracle's relayout."""
+
+    def __init__(self):
+        if _needs_build(SEGMENT_LIBRARY, SEGMENT_SOURCE):
+            build_segment()
+        lib = ctypes.CDLL(SEGMENT_LIBRARY)
+        lib.seg_a2a_4d.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, _i64, ctypes.c_int, _p,
+                                   _p, ctypes.c_int]
+        lib.seg_a2a_4d.restype = ctypes.c_int
+        lib.seg_max_threads.argtypes = []
+        lib.seg_max_threads.restype = ctypes.c_int
+        self.lib = lib
+
+    def max_threads(self) -> int:
+        return int(self.lib.seg_max_threads())
+
+    def a2a_4d(self, xs, seq_splits, head_splits, mode: int, threads: int = 0, outs=None):
+        """Relayout W host arrays (raw bytes of any dtype) into `outs` (allocated when None)."""
+        W = len(xs)
+        b, d = xs[0].shape[0], xs[0].shape[3]
+        e = xs[0].dtype.itemsize
+        xs = [np.ascontiguousarray(x) for x in xs]
+        if outs is None:
+            outs = [np.empty(sh, dtype=xs[0].dtype)
+                    for sh in Oracle.out_shapes(b, seq_splits, head_splits, d, mode)]
+        rc = self.lib.seg_a2a_4d(W, b, _i64_array(seq_splits), _i64_array(head_splits), d, e, mode,
+                                 ctypes.cast(_ptr_array(xs), _p), ctypes.cast(_ptr_array(outs), _p),
+                                 int(threads))
         if rc != 0:
-            raise ValueError("oracle rejected the geometry")
-        return dx, dw
+            raise ValueError("segment relayout rejected the geometry")
+        return outs
 
 
 _default: Oracle | None = None

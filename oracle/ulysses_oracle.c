@@ -71,6 +71,20 @@ static int check_geometry(int W, int64_t b, const int64_t* seq_splits, const int
 }
 
 /*
+ * Parts of the fused calls. A whole call walks the source shards q in [0, W) and, in each, the
+ * rows i in [0, s_q) of every batch index. The *_part functions below walk only shards
+ * q in [q_lo, q_hi) and rows i in [i_lo, min(i_hi, s_q)), in the same order and with the same
+ * arithmetic, so that a large check can be split over host threads (the parts write disjoint
+ * output rows). The whole-call functions are their part (0, W, 0, INT64_MAX).
+ */
+static int part_range_ok(int W, int q_lo, int q_hi, int64_t i_lo, int64_t i_hi)
+{
+    return q_lo >= 0 && q_hi <= W && q_lo <= q_hi && i_lo >= 0 && i_lo <= i_hi ? 0 : -1;
+}
+
+static int64_t part_row_end(int64_t s_q, int64_t i_hi) { return i_hi < s_q ? i_hi : s_q; }
+
+/*
  * The relayout, six nested loops, one element (e bytes) per innermost step.
  * in[k] and out[k] are the W ranks' buffers. Mode 0: in[q] is (b, s_q, N, d) and out[r] is
  * (b, S, n_r, d). Mode 1: in[r] is (b, S, n_r, d) and out[q] is (b, s_q, N, d).
@@ -241,18 +255,20 @@ static void transform_row(const uint16_t* x_bf16, int64_t d, const double* w, do
  * place it where mode 0 puts it. x_in[q] holds rank q's (b, s_q, N, d) bf16 tensor; y_out[r]
  * receives rank r's (b, S, n_r, d) tensor in double.
  */
-int orc_qk_fused_A(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
-                   int64_t d, const uint16_t* const* x_in, const double* w, double eps,
-                   double theta, double* const* y_out)
+int orc_qk_fused_A_part(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                        int64_t d, const uint16_t* const* x_in, const double* w, double eps,
+                        double theta, double* const* y_out, int q_lo, int q_hi, int64_t i_lo,
+                        int64_t i_hi)
 {
     if (check_geometry(W, b, seq_splits, head_splits, d) || (d % 2) != 0) return -1;
+    if (part_range_ok(W, q_lo, q_hi, i_lo, i_hi)) return -1;
     const int64_t S = offset_of(seq_splits, W);
     const int64_t N = offset_of(head_splits, W);
-    for (int q = 0; q < W; ++q) {
+    for (int q = q_lo; q < q_hi; ++q) {
         const int64_t s_q = seq_splits[q];
         const int64_t seq_off_q = offset_of(seq_splits, q);
         for (int64_t bb = 0; bb < b; ++bb)
-            for (int64_t i = 0; i < s_q; ++i)
+            for (int64_t i = i_lo; i < part_row_end(s_q, i_hi); ++i)
                 for (int64_t g = 0; g < N; ++g) {
                     /* the destination rank owns global head g */
                     int r = 0;
@@ -267,6 +283,14 @@ int orc_qk_fused_A(int W, int64_t b, const int64_t* seq_splits, const int64_t* h
                 }
     }
     return 0;
+}
+
+int orc_qk_fused_A(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                   int64_t d, const uint16_t* const* x_in, const double* w, double eps,
+                   double theta, double* const* y_out)
+{
+    return orc_qk_fused_A_part(W, b, seq_splits, head_splits, d, x_in, w, eps, theta, y_out, 0, W,
+                               0, INT64_MAX);
 }
 
 /*
@@ -344,19 +368,21 @@ void orc_double_to_bf16_array(const double* x, int64_t n, uint16_t* out)
  * wq and wk respectively) and placed where mode 0 puts them (double outputs); v rows are placed by
  * mode 0 unchanged (bf16 bit patterns). q_out[r], k_out[r], v_out[r] are rank r's (b, S, n_r, d).
  */
-int orc_qkv_fused(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
-                  int64_t d, const uint16_t* const* qkv_in, const double* wq, const double* wk,
-                  double eps, double theta, double* const* q_out, double* const* k_out,
-                  uint16_t* const* v_out)
+int orc_qkv_fused_part(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                       int64_t d, const uint16_t* const* qkv_in, const double* wq,
+                       const double* wk, double eps, double theta, double* const* q_out,
+                       double* const* k_out, uint16_t* const* v_out, int q_lo, int q_hi,
+                       int64_t i_lo, int64_t i_hi)
 {
     if (check_geometry(W, b, seq_splits, head_splits, d) || (d % 2) != 0) return -1;
+    if (part_range_ok(W, q_lo, q_hi, i_lo, i_hi)) return -1;
     const int64_t S = offset_of(seq_splits, W);
     const int64_t N = offset_of(head_splits, W);
-    for (int q = 0; q < W; ++q) {
+    for (int q = q_lo; q < q_hi; ++q) {
         const int64_t s_q = seq_splits[q];
         const int64_t seq_off_q = offset_of(seq_splits, q);
         for (int64_t bb = 0; bb < b; ++bb)
-            for (int64_t i = 0; i < s_q; ++i)
+            for (int64_t i = i_lo; i < part_row_end(s_q, i_hi); ++i)
                 for (int64_t g = 0; g < N; ++g) {
                     int r = 0;
                     while (!(g >= offset_of(head_splits, r) &&
@@ -376,6 +402,15 @@ int orc_qkv_fused(int W, int64_t b, const int64_t* seq_splits, const int64_t* he
                 }
     }
     return 0;
+}
+
+int orc_qkv_fused(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                  int64_t d, const uint16_t* const* qkv_in, const double* wq, const double* wk,
+                  double eps, double theta, double* const* q_out, double* const* k_out,
+                  uint16_t* const* v_out)
+{
+    return orc_qkv_fused_part(W, b, seq_splits, head_splits, d, qkv_in, wq, wk, eps, theta, q_out,
+                              k_out, v_out, 0, W, 0, INT64_MAX);
 }
 
 /*
@@ -417,23 +452,27 @@ void orc_fused_row_bwd(const double* x, const double* g, int64_t d, const double
  * Backward of the fused mode-0 call for one tensor: x_in[q] is rank q's forward input
  * (b, s_q, N, d) bf16, g_out[r] rank r's gradient with respect to the forward output
  * (b, S, n_r, d) bf16. dx[q] receives rank q's gradient with respect to its input (double,
- * (b, s_q, N, d)); dw (d values) is set to the gradient with respect to the weight.
+ * (b, s_q, N, d)); dw (d values) is set to the gradient with respect to the weight (for a part,
+ * to the sum over that part's rows).
  */
-int orc_qk_fused_bwd(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
-                     int64_t d, const uint16_t* const* x_in, const uint16_t* const* g_out,
-                     const double* w, double eps, double theta, double* const* dx, double* dw)
+int orc_qk_fused_bwd_part(int W, int64_t b, const int64_t* seq_splits,
+                          const int64_t* head_splits, int64_t d, const uint16_t* const* x_in,
+                          const uint16_t* const* g_out, const double* w, double eps, double theta,
+                          double* const* dx, double* dw, int q_lo, int q_hi, int64_t i_lo,
+                          int64_t i_hi)
 {
     if (check_geometry(W, b, seq_splits, head_splits, d) || (d % 2) != 0) return -1;
+    if (part_range_ok(W, q_lo, q_hi, i_lo, i_hi)) return -1;
     const int64_t S = offset_of(seq_splits, W);
     const int64_t N = offset_of(head_splits, W);
     double* x = (double*)malloc((size_t)d * sizeof(double));
     double* g = (double*)malloc((size_t)d * sizeof(double));
     for (int64_t j = 0; j < d; ++j) dw[j] = 0.0;
-    for (int q = 0; q < W; ++q) {
+    for (int q = q_lo; q < q_hi; ++q) {
         const int64_t s_q = seq_splits[q];
         const int64_t seq_off_q = offset_of(seq_splits, q);
         for (int64_t bb = 0; bb < b; ++bb)
-            for (int64_t i = 0; i < s_q; ++i)
+            for (int64_t i = i_lo; i < part_row_end(s_q, i_hi); ++i)
                 for (int64_t hg = 0; hg < N; ++hg) {
                     int r = 0;
                     while (!(hg >= offset_of(head_splits, r) &&
@@ -454,6 +493,14 @@ int orc_qk_fused_bwd(int W, int64_t b, const int64_t* seq_splits, const int64_t*
     free(x);
     free(g);
     return 0;
+}
+
+int orc_qk_fused_bwd(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                     int64_t d, const uint16_t* const* x_in, const uint16_t* const* g_out,
+                     const double* w, double eps, double theta, double* const* dx, double* dw)
+{
+    return orc_qk_fused_bwd_part(W, b, seq_splits, head_splits, d, x_in, g_out, w, eps, theta, dx,
+                                 dw, 0, W, 0, INT64_MAX);
 }
 
 /* ------------------------------------------------------------------------------------------ */
@@ -565,21 +612,23 @@ void orc_fused_row_var(const uint16_t* x_raw, int64_t d, int f16, int half_pairs
  * global position seq_off(q) + i and placed where mode 0 puts it. x_in[q]: rank q's
  * (b, s_q, N, d) elements; y_out[r]: rank r's (b, S, n_r, d) in double.
  */
-int orc_qk_fused_var(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
-                     int64_t d, int f16, int half_pairs, const uint16_t* const* x_in,
-                     const double* w, double eps, double theta, double* const* y_out)
+int orc_qk_fused_var_part(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                          int64_t d, int f16, int half_pairs, const uint16_t* const* x_in,
+                          const double* w, double eps, double theta, double* const* y_out,
+                          int q_lo, int q_hi, int64_t i_lo, int64_t i_hi)
 {
     if (check_geometry(W, b, seq_splits, head_splits, d) || (d % 2) != 0) return -1;
+    if (part_range_ok(W, q_lo, q_hi, i_lo, i_hi)) return -1;
     const int64_t S = offset_of(seq_splits, W);
     const int64_t N = offset_of(head_splits, W);
     for (int r = 0; r < W; ++r) {
         const int64_t n_r = head_splits[r];
         const int64_t first_head = offset_of(head_splits, r);
-        for (int q = 0; q < W; ++q) {
+        for (int q = q_lo; q < q_hi; ++q) {
             const int64_t s_q = seq_splits[q];
             const int64_t seq_off_q = offset_of(seq_splits, q);
             for (int64_t bb = 0; bb < b; ++bb)
-                for (int64_t i = 0; i < s_q; ++i)
+                for (int64_t i = i_lo; i < part_row_end(s_q, i_hi); ++i)
                     for (int64_t h = 0; h < n_r; ++h) {
                         const uint16_t* src = x_in[q] + ((bb * s_q + i) * N + first_head + h) * d;
                         double* dst = y_out[r] + ((bb * S + seq_off_q + i) * n_r + h) * d;
@@ -589,6 +638,14 @@ int orc_qk_fused_var(int W, int64_t b, const int64_t* seq_splits, const int64_t*
         }
     }
     return 0;
+}
+
+int orc_qk_fused_var(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                     int64_t d, int f16, int half_pairs, const uint16_t* const* x_in,
+                     const double* w, double eps, double theta, double* const* y_out)
+{
+    return orc_qk_fused_var_part(W, b, seq_splits, head_splits, d, f16, half_pairs, x_in, w, eps,
+                                 theta, y_out, 0, W, 0, INT64_MAX);
 }
 
 /* Row backward of a variant: g rotated back with the variant's pairs, then the RMSNorm part. */
@@ -607,14 +664,16 @@ void orc_fused_row_bwd_var(const double* x, const double* g, int64_t d, int half
  * Backward of a variant's fused call for one tensor: x_in[q] rank q's forward input
  * (b, s_q, N, d), g_out[r] rank r's output gradient (b, S, n_r, d), both in the variant's
  * element type; dx[q] (double, (b, s_q, N, d)) and dw (d values, cleared first) as
- * orc_qk_fused_bwd.
+ * orc_qk_fused_bwd (for a part, dw is the sum over that part's rows).
  */
-int orc_qk_fused_bwd_var(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
-                         int64_t d, int f16, int half_pairs, const uint16_t* const* x_in,
-                         const uint16_t* const* g_out, const double* w, double eps, double theta,
-                         double* const* dx, double* dw)
+int orc_qk_fused_bwd_var_part(int W, int64_t b, const int64_t* seq_splits,
+                              const int64_t* head_splits, int64_t d, int f16, int half_pairs,
+                              const uint16_t* const* x_in, const uint16_t* const* g_out,
+                              const double* w, double eps, double theta, double* const* dx,
+                              double* dw, int q_lo, int q_hi, int64_t i_lo, int64_t i_hi)
 {
     if (check_geometry(W, b, seq_splits, head_splits, d) || (d % 2) != 0) return -1;
+    if (part_range_ok(W, q_lo, q_hi, i_lo, i_hi)) return -1;
     const int64_t S = offset_of(seq_splits, W);
     const int64_t N = offset_of(head_splits, W);
     double* x = (double*)malloc((size_t)d * sizeof(double));
@@ -623,11 +682,11 @@ int orc_qk_fused_bwd_var(int W, int64_t b, const int64_t* seq_splits, const int6
     for (int r = 0; r < W; ++r) {
         const int64_t n_r = head_splits[r];
         const int64_t first_head = offset_of(head_splits, r);
-        for (int q = 0; q < W; ++q) {
+        for (int q = q_lo; q < q_hi; ++q) {
             const int64_t s_q = seq_splits[q];
             const int64_t seq_off_q = offset_of(seq_splits, q);
             for (int64_t bb = 0; bb < b; ++bb)
-                for (int64_t i = 0; i < s_q; ++i)
+                for (int64_t i = i_lo; i < part_row_end(s_q, i_hi); ++i)
                     for (int64_t h = 0; h < n_r; ++h) {
                         const int64_t in_row = ((bb * s_q + i) * N + first_head + h) * d;
                         const int64_t grad_row = ((bb * S + seq_off_q + i) * n_r + h) * d;
@@ -643,4 +702,13 @@ int orc_qk_fused_bwd_var(int W, int64_t b, const int64_t* seq_splits, const int6
     free(x);
     free(g);
     return 0;
+}
+
+int orc_qk_fused_bwd_var(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                         int64_t d, int f16, int half_pairs, const uint16_t* const* x_in,
+                         const uint16_t* const* g_out, const double* w, double eps, double theta,
+                         double* const* dx, double* dw)
+{
+    return orc_qk_fused_bwd_var_part(W, b, seq_splits, head_splits, d, f16, half_pairs, x_in,
+                                     g_out, w, eps, theta, dx, dw, 0, W, 0, INT64_MAX);
 }

@@ -652,6 +652,48 @@ def pin_fused_bwd_var_whole_call(orc, quick=False):
                 np.testing.assert_allclose(dw, dw_want, rtol=1e-12, atol=1e-12)
 
 
+def pin_parts_cover_the_call(orc, quick=False):
+    """A call split into parts on host threads (ranges of shards and rows, the form the full-size
+    GPU checks use) covers every row once: outputs prefilled with NaN come back bit-identical to
+    the whole call, and dw, summed part by part, equals the whole call's dw up to the order of its
+    double sum (a row computed twice or skipped moves it by a whole term)."""
+    rng = np.random.default_rng(47)
+    mk = lambda shape: ((rng.integers(0, 1 << 16, shape).astype(np.uint16) & 0x3FFF)  # noqa: E731
+                        | 0x3000).astype(np.uint16)
+    for W, b, seq, heads, d in [(3, 2, [5, 0, 7], [2, 1, 2], 16), (4, 1, [9, 3, 1, 6], [1, 2, 1, 1], 8)]:
+        N, S = sum(heads), sum(seq)
+        xs = [mk((b, s, N, d)) for s in seq]
+        gs = [mk((b, S, n, d)) for n in heads]
+        qkv = [mk((b, s, 3, N, d)) for s in seq]
+        w = 1.0 + 0.1 * rng.standard_normal(d)
+        w2 = 1.0 + 0.1 * rng.standard_normal(d)
+        for threads in (2, 3, 5):
+            for got, want in zip(orc.qk_fused_A(xs, seq, heads, w, 1e-6, 1e4, threads=threads),
+                                 orc.qk_fused_A(xs, seq, heads, w, 1e-6, 1e4)):
+                assert np.array_equal(got, want)
+            a = orc.qkv_fused(qkv, seq, heads, w, w2, 1e-6, 1e4, threads=threads)
+            c = orc.qkv_fused(qkv, seq, heads, w, w2, 1e-6, 1e4)
+            for got, want in zip(a[0] + a[1] + a[2], c[0] + c[1] + c[2]):
+                assert np.array_equal(got, want)
+            dx, dw = orc.qk_fused_bwd(xs, gs, seq, heads, w, 1e-6, 1e4, threads=threads)
+            dx1, dw1 = orc.qk_fused_bwd(xs, gs, seq, heads, w, 1e-6, 1e4)
+            for got, want in zip(dx, dx1):
+                assert np.array_equal(got, want)
+            np.testing.assert_allclose(dw, dw1, rtol=1e-12, atol=1e-12)
+            for f16 in (0, 1):
+                for half in (0, 1):
+                    for got, want in zip(
+                            orc.qk_fused_var(xs, seq, heads, w, 1e-6, 1e4, f16, half, threads=threads),
+                            orc.qk_fused_var(xs, seq, heads, w, 1e-6, 1e4, f16, half)):
+                        assert np.array_equal(got, want)
+                    dx, dw = orc.qk_fused_bwd_var(xs, gs, seq, heads, w, 1e-6, 1e4, f16, half,
+                                                  threads=threads)
+                    dx1, dw1 = orc.qk_fused_bwd_var(xs, gs, seq, heads, w, 1e-6, 1e4, f16, half)
+                    for got, want in zip(dx, dx1):
+                        assert np.array_equal(got, want)
+                    np.testing.assert_allclose(dw, dw1, rtol=1e-12, atol=1e-12)
+
+
 def pin_bf16_rounding(orc, quick=False):
     """double -> bf16 on float32-representable values equals torch's float32 -> bf16 (one
     round-to-nearest-even); bf16 -> double equals torch's widening."""
@@ -703,6 +745,7 @@ PINS = [
     pin_fused_var_whole_call,
     pin_fused_bwd_variants,
     pin_fused_bwd_var_whole_call,
+    pin_parts_cover_the_call,
     pin_bf16_rounding,
 ]
 

@@ -4,9 +4,16 @@ gather) against the CPU oracle (double precision).
 dx tolerance: |gpu - ref| <= 1e-2 + 1e-2 * |ref| (the forward's bound), and the tighter bound the
 fp32 arithmetic and one bf16 rounding allow at these magnitudes (inputs and gradients of unit
 scale): |gpu - ref| <= 2^-8 * |ref| + 1e-4.
-dw tolerance: dw is a sum over n = b * S * N rows of terms of unit scale, accumulated in fp32;
-the rounding of such a sum stays far below n * 2^-20, which is what the tests allow (plus 1e-4),
-while a wrong term would move dw by about sqrt(n).
+dw tolerance (dw_bound): dw is a sum over n = b * S * N rows of terms of unit scale with mean
+zero (independent N(0, 1) inputs and gradients), accumulated in fp32 in blocks: each lane adds the
+terms of the m rows it handles in sequence, then lanes, warps and CTAs are added in a fixed tree.
+The rounding of such a sum behaves like a random walk whose steps scale with the partial sums,
+about 2^-24 sigma sqrt(n m / 6) in all (sigma the terms' rms, about 1): 1.5e-3 at the Wan shape
+(n = 3,024,000, m about 1,250). The tests allow min(n 2^-20, 1e-4 sqrt(n)) + 1e-4: at the Wan
+shape 0.17, over 100 times that, and it stays above it for chains up to about 10^6 rows; while one
+row dropped or counted twice moves some element of dw by that row's largest term, u_j xh_j, which
+for a row of 128 unit-scale products exceeds 0.17 with overwhelming probability (the full-size
+tests check it on sampled rows).
 """
 import numpy as np
 import pytest
@@ -39,9 +46,14 @@ def check_dx(oracle, got_bf16_u16, ref, what):
     assert tight.all(), f"{what}: {int((~tight).sum())} elements beyond the fp32 + bf16 bound"
 
 
+def dw_bound(n_rows):
+    """Allowed |gpu - oracle| for each element of dw, a sum over n_rows rows (module docstring)."""
+    return min(n_rows * 2.0 ** -20, 1e-4 * float(np.sqrt(n_rows))) + 1e-4
+
+
 def check_dw(got, ref, n_rows, what):
     err = np.abs(np.asarray(got, dtype=np.float64) - ref)
-    bound = n_rows * 2.0 ** -20 + 1e-4
+    bound = dw_bound(n_rows)
     assert np.all(err <= bound), f"{what}: max err {err.max():.3e} > {bound:.3e}"
 
 

@@ -90,6 +90,13 @@ MUTANTS = {
                                       "rope_pairs(u, d, p, theta, half_pairs);")],
     "variant_bwd_grad_drops_seq_offset": [("const int64_t grad_row = ((bb * S + seq_off_q + i) * n_r + h) * d;",
                                            "const int64_t grad_row = ((bb * S + i) * n_r + h) * d;")],
+    "part_row_range_ignored": [("static int64_t part_row_end(int64_t s_q, int64_t i_hi) { return i_hi < s_q ? i_hi : s_q; }",
+                                "static int64_t part_row_end(int64_t s_q, int64_t i_hi) { (void)i_hi; return s_q; }")],
+    "bwd_part_starts_at_row_zero": [
+        ("""            for (int64_t i = i_lo; i < part_row_end(s_q, i_hi); ++i)
+                for (int64_t hg = 0; hg < N; ++hg) {""",
+         """            for (int64_t i = 0; i < part_row_end(s_q, i_hi); ++i)
+                for (int64_t hg = 0; hg < N; ++hg) {""")],
     "bf16_truncates": [("nearbyint(a / quantum)", "floor(a / quantum)")],
     "bf16_one_bit_too_many": [("ldexp(1.0, ex - 7)", "ldexp(1.0, ex - 8)")],
     "bf16_widening_drops_low_bits": [("uint32_t bits = (uint32_t)h << 16;",
