@@ -125,6 +125,10 @@ class Oracle:
         lib.orc_qkv_fused.restype = ctypes.c_int
         lib.orc_qkv_fused_part.argtypes = lib.orc_qkv_fused.argtypes + _PART
         lib.orc_qkv_fused_part.restype = ctypes.c_int
+        lib.orc_packed_fused.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, _i64, _p, _p, _p,
+                                         ctypes.c_double, ctypes.c_double, _p, _p, _p]
+        lib.orc_packed_fused.restype = ctypes.c_int
         lib.orc_fused_row_bwd.argtypes = [_p, _p, _i64, _p, ctypes.c_double, ctypes.c_double,
                                           ctypes.c_double, _p, _p]
         lib.orc_fused_row_bwd.restype = None
@@ -275,6 +279,36 @@ class Oracle:
         if any(rc != 0 for rc in rcs):
             raise ValueError("oracle rejected the geometry")
         return qo, ko, vo
+
+    def packed_fused(self, packed, seq_splits, head_splits, d, planes, q_plane, k_plane, pitch,
+                     wq, wk, eps, theta):
+        """Packed inputs: rank q's array holds b * s_q tokens of `pitch` elements (uint16 bit
+        patterns, any shape whose leading axes are (b, s_q)); plane c's head g of a token is at
+        element c * N * d + g * d. Returns (q_outs, k_outs, plain_outs): the q and k planes
+        transformed and placed (double), plain_outs[c] the other planes placed unchanged (uint16;
+        None for the q and k planes); each rank r (b, S, n_r, d)."""
+        W = len(packed)
+        b = packed[0].shape[0]
+        xs = [np.ascontiguousarray(x).view(np.uint16) for x in packed]
+        wq64 = np.ascontiguousarray(np.asarray(wq, dtype=np.float64))
+        wk64 = np.ascontiguousarray(np.asarray(wk, dtype=np.float64))
+        shapes = self.out_shapes(b, seq_splits, head_splits, d, 0)
+        qo = [np.empty(s, dtype=np.float64) for s in shapes]
+        ko = [np.empty(s, dtype=np.float64) for s in shapes]
+        plain = [None if c in (q_plane, k_plane) else [np.empty(s, dtype=np.uint16) for s in shapes]
+                 for c in range(planes)]
+        dummy = np.empty(1, dtype=np.uint16)
+        flat = [plain[c][r] if plain[c] is not None else dummy for c in range(planes) for r in range(W)]
+        rc = self.lib.orc_packed_fused(W, b, _i64_array(seq_splits), _i64_array(head_splits), d,
+                                       planes, q_plane, k_plane, pitch,
+                                       ctypes.cast(_ptr_array(xs), _p), wq64.ctypes.data,
+                                       wk64.ctypes.data, float(eps), float(theta),
+                                       ctypes.cast(_ptr_array(qo), _p),
+                                       ctypes.cast(_ptr_array(ko), _p),
+                                       ctypes.cast(_ptr_array(flat), _p))
+        if rc != 0:
+            raise ValueError("oracle rejected the geometry")
+        return qo, ko, plain
 
     def fused_row_bwd(self, x, g, w, eps, p, theta):
         """(dL/dx, dL/dw) of one row y = R(p)(x * w / rms(x)) for dL/dy = g, in double."""

@@ -414,6 +414,57 @@ int orc_qkv_fused(int W, int64_t b, const int64_t* seq_splits, const int64_t* he
 }
 
 /*
+ * Packed inputs with C planes per token, the general form of the interleaved layout (FastVideo,
+ * "Ulysses performance on GB200": packed QKV or QKVG). Rank q's input holds b * s_q tokens; token
+ * (bb, i) starts (bb * s_q + i) * pitch elements into it (pitch >= C * N * d: a token may carry
+ * further columns, which are never read), and within a token plane c's head g is the d elements at
+ * c * N * d + g * d. Planes q_plane and k_plane are transformed as orc_qk_fused_A does (with wq and
+ * wk) and placed where mode 0 puts them (double, q_out[r] and k_out[r]); every other plane c is
+ * placed by mode 0 unchanged (bf16 bit patterns, plain_out[c * W + r]; the entries of the q and k
+ * planes are not touched). Every output is rank r's (b, S, n_r, d).
+ */
+int orc_packed_fused(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                     int64_t d, int planes, int q_plane, int k_plane, int64_t pitch,
+                     const uint16_t* const* in, const double* wq, const double* wk, double eps,
+                     double theta, double* const* q_out, double* const* k_out,
+                     uint16_t* const* plain_out)
+{
+    if (check_geometry(W, b, seq_splits, head_splits, d) || (d % 2) != 0) return -1;
+    const int64_t S = offset_of(seq_splits, W);
+    const int64_t N = offset_of(head_splits, W);
+    if (planes < 2 || q_plane < 0 || q_plane >= planes || k_plane < 0 || k_plane >= planes ||
+        q_plane == k_plane || pitch < planes * N * d)
+        return -1;
+    for (int q = 0; q < W; ++q) {
+        const int64_t s_q = seq_splits[q];
+        const int64_t seq_off_q = offset_of(seq_splits, q);
+        for (int64_t bb = 0; bb < b; ++bb)
+            for (int64_t i = 0; i < s_q; ++i) {
+                const uint16_t* token = in[q] + (bb * s_q + i) * pitch;
+                const double p = (double)(seq_off_q + i);
+                for (int c = 0; c < planes; ++c)
+                    for (int64_t g = 0; g < N; ++g) {
+                        int r = 0;
+                        while (!(g >= offset_of(head_splits, r) &&
+                                 g < offset_of(head_splits, r) + head_splits[r]))
+                            ++r;
+                        const int64_t n_r = head_splits[r];
+                        const int64_t h = g - offset_of(head_splits, r);
+                        const int64_t dst_row = ((bb * S + seq_off_q + i) * n_r + h) * d;
+                        const uint16_t* row = token + (c * N + g) * d;
+                        if (c == q_plane)
+                            transform_row(row, d, wq, eps, p, theta, q_out[r] + dst_row);
+                        else if (c == k_plane)
+                            transform_row(row, d, wk, eps, p, theta, k_out[r] + dst_row);
+                        else
+                            for (int64_t j = 0; j < d; ++j) plain_out[c * W + r][dst_row + j] = row[j];
+                    }
+            }
+    }
+    return 0;
+}
+
+/*
  * Backward of the fused transform for one row (vector-Jacobian product). The forward row is
  * y = R(p) (x * w / rms(x)) with rms(x) = sqrt(mean(x^2) + eps) and R(p) the rotation above.
  * Given g = dL/dy: u = R(-p) g (the rotation is orthogonal), a = u * w,

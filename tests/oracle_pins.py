@@ -383,6 +383,51 @@ def pin_qkv_interleaved(orc, quick=False):
         _same(vo, split_cat_mode0(v_in, heads), "qkv: v plane")
 
 
+def pin_packed_planes(orc, quick=False):
+    """Packed inputs with C planes per token and a token pitch: slicing each token's row into its
+    planes (plane c = columns c*N*d .. (c+1)*N*d of the (b, s, pitch) view, a numpy view) gives the
+    plane tensors; the q and k planes must equal the pinned fused transform (with their own
+    weights), every other plane the pinned split/cat relayout, whatever the extra columns of a
+    token hold. With 3 planes (q, k, v) and no extra columns it is the interleaved QKV form."""
+    rng = np.random.default_rng(48)
+    cases = [(2, 1, [3, 2], [2, 1], 8), (3, 2, [2, 0, 3], [1, 2, 1], 16), (1, 1, [4], [3], 8),
+             (4, 1, [1, 2, 1, 2], [2, 0, 1, 1], 8)]
+    bf16 = lambda shape: (torch.from_numpy(rng.standard_normal(shape).astype(np.float32))  # noqa: E731
+                          .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    for W, b, seq, heads, d in cases:
+        N = sum(heads)
+        wq = 1.0 + 0.1 * rng.standard_normal(d)
+        wk = 1.0 + 0.1 * rng.standard_normal(d)
+        # the interleaved QKV form as a special case
+        qkv = [bf16((b, s, 3, N, d)) for s in seq]
+        got = orc.packed_fused(qkv, seq, heads, d, 3, 0, 1, 3 * N * d, wq, wk, 1e-6, 1e4)
+        want = orc.qkv_fused(qkv, seq, heads, wq, wk, 1e-6, 1e4)
+        _same(got[0], want[0], "packed 3 planes: q")
+        _same(got[1], want[1], "packed 3 planes: k")
+        _same(got[2][2], want[2], "packed 3 planes: v")
+        for C, qp, kp, extra in [(4, 0, 1, 0), (4, 2, 0, 24), (2, 1, 0, 8), (6, 3, 5, 16)]:
+            pitch = C * N * d + extra
+            packed = [bf16((b, s, pitch)) for s in seq]
+            qo, ko, plain = orc.packed_fused(packed, seq, heads, d, C, qp, kp, pitch, wq, wk, 1e-6,
+                                             1e4)
+            plane = lambda c: [np.ascontiguousarray(x[:, :, c * N * d:(c + 1) * N * d])  # noqa: E731
+                               .reshape(b, x.shape[1], N, d) for x in packed]
+            _same(qo, orc.qk_fused_A(plane(qp), seq, heads, wq, 1e-6, 1e4), f"packed C={C}: q")
+            _same(ko, orc.qk_fused_A(plane(kp), seq, heads, wk, 1e-6, 1e4), f"packed C={C}: k")
+            for c in range(C):
+                if c in (qp, kp):
+                    assert plain[c] is None
+                else:
+                    _same(plain[c], split_cat_mode0(plane(c), heads), f"packed C={C}: plane {c}")
+            if extra:  # the extra columns are never read
+                other = [x.copy() for x in packed]
+                for x in other:
+                    x[:, :, C * N * d:] = rng.integers(0, 1 << 16, x[:, :, C * N * d:].shape)
+                again = orc.packed_fused(other, seq, heads, d, C, qp, kp, pitch, wq, wk, 1e-6, 1e4)
+                _same(again[0], qo, "extra columns: q")
+                _same(again[1], ko, "extra columns: k")
+
+
 def _torch_row_forward(x, w, eps, p, theta):
     """The fused row transform built from library pieces (F.rms_norm, complex multiplication),
     differentiable by torch.autograd."""
@@ -733,6 +778,7 @@ PINS = [
     pin_fused_formulations_agree,
     pin_fused_placement_decode,
     pin_qkv_interleaved,
+    pin_packed_planes,
     pin_fused_bwd_vs_autograd,
     pin_fused_bwd_finite_differences,
     pin_fused_bwd_placement,

@@ -62,6 +62,14 @@ MUTANTS = {
     "qkv_plane_stride": [("(((bb * s_q + i) * 3 + 2) * N + g) * d;", "((bb * s_q + i) * N + 2 * N + g) * d;")],
     "qkv_k_uses_q_weight": [("transform_row(krow, d, wk, eps, p, theta, k_out[r] + dst_row);",
                              "transform_row(krow, d, wq, eps, p, theta, k_out[r] + dst_row);")],
+    "packed_planes_transposed": [("const uint16_t* row = token + (c * N + g) * d;",
+                                  "const uint16_t* row = token + (g * planes + c) * d;")],
+    "packed_pitch_ignored": [("const uint16_t* token = in[q] + (bb * s_q + i) * pitch;",
+                              "const uint16_t* token = in[q] + (bb * s_q + i) * planes * N * d;")],
+    "packed_k_uses_q_weight": [("transform_row(row, d, wk, eps, p, theta, k_out[r] + dst_row);",
+                                "transform_row(row, d, wq, eps, p, theta, k_out[r] + dst_row);")],
+    "packed_plain_to_wrong_plane": [("plain_out[c * W + r][dst_row + j] = row[j];",
+                                     "plain_out[c * W + r][dst_row + j] = row[j - (c > 0 ? N * d : 0)];")],
     "bwd_rope_forward_direction": [("orc_rope(u, d, -p, theta);", "orc_rope(u, d, p, theta);")],
     "bwd_drops_norm_projection": [("dx[j] = inv_rms * (u[j] * w[j] - xh * dot / (double)d);",
                                    "dx[j] = inv_rms * u[j] * w[j];")],
