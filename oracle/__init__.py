@@ -129,6 +129,10 @@ class Oracle:
                                          ctypes.c_int, ctypes.c_int, _i64, _p, _p, _p,
                                          ctypes.c_double, ctypes.c_double, _p, _p, _p]
         lib.orc_packed_fused.restype = ctypes.c_int
+        lib.orc_packed_fused_bwd.argtypes = [ctypes.c_int, _i64, _pi64, _pi64, _i64, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, _i64, _p, _p, _p, _p,
+                                             ctypes.c_double, ctypes.c_double, _p, _p]
+        lib.orc_packed_fused_bwd.restype = ctypes.c_int
         lib.orc_fused_row_bwd.argtypes = [_p, _p, _i64, _p, ctypes.c_double, ctypes.c_double,
                                           ctypes.c_double, _p, _p]
         lib.orc_fused_row_bwd.restype = None
@@ -309,6 +313,31 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle rejected the geometry")
         return qo, ko, plain
+
+    def packed_fused_bwd(self, packed, grads, seq_splits, head_splits, d, planes, q_plane, k_plane,
+                         pitch, wq, wk, eps, theta):
+        """Backward of packed_fused: packed (rank q's b * s_q tokens of `pitch` uint16 elements,
+        leading axes (b, s_q)), grads[c][r] rank r's gradient of plane c's output (uint16 bf16 bit
+        patterns, (b, S, n_r, d)). Returns (dpacked, dw): dpacked[q] a double array shaped like
+        packed[q] (columns beyond the planes NaN: never written), dw (2, d)."""
+        W = len(packed)
+        b = packed[0].shape[0]
+        xs = [np.ascontiguousarray(x).view(np.uint16) for x in packed]
+        gs = [np.ascontiguousarray(grads[c][r]).view(np.uint16) for c in range(planes)
+              for r in range(W)]
+        wq64 = np.ascontiguousarray(np.asarray(wq, dtype=np.float64))
+        wk64 = np.ascontiguousarray(np.asarray(wk, dtype=np.float64))
+        dx = [np.full(x.shape, np.nan) for x in xs]
+        dw = np.full(2 * d, np.nan)  # the oracle clears it
+        rc = self.lib.orc_packed_fused_bwd(W, b, _i64_array(seq_splits), _i64_array(head_splits),
+                                           d, planes, q_plane, k_plane, pitch,
+                                           ctypes.cast(_ptr_array(xs), _p),
+                                           ctypes.cast(_ptr_array(gs), _p), wq64.ctypes.data,
+                                           wk64.ctypes.data, float(eps), float(theta),
+                                           ctypes.cast(_ptr_array(dx), _p), dw.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle rejected the geometry")
+        return dx, dw.reshape(2, d)
 
     def fused_row_bwd(self, x, g, w, eps, p, theta):
         """(dL/dx, dL/dw) of one row y = R(p)(x * w / rms(x)) for dL/dy = g, in double."""

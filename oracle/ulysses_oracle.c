@@ -554,6 +554,67 @@ int orc_qk_fused_bwd(int W, int64_t b, const int64_t* seq_splits, const int64_t*
                                  dw, 0, W, 0, INT64_MAX);
 }
 
+/*
+ * Backward of orc_packed_fused (same packing and planes): packed_in holds the forward's packed
+ * inputs (only the q and k planes are read), grads[c * W + r] rank r's gradient of plane c's
+ * output ((b, S, n_r, d) bf16). Written into dpacked (rank q's packed layout, the same pitch):
+ * for the q and k planes the gradient of their rows through the fused transform (double, as
+ * orc_qk_fused_bwd computes it, with wq and wk), for every other plane its gradient brought back
+ * by mode 1 (the bf16 bit patterns, widened exactly to double); the columns of a token beyond its
+ * planes are not touched. dw[0 .. d) and dw[d .. 2d) are set to the gradients of wq and wk.
+ */
+int orc_packed_fused_bwd(int W, int64_t b, const int64_t* seq_splits, const int64_t* head_splits,
+                         int64_t d, int planes, int q_plane, int k_plane, int64_t pitch,
+                         const uint16_t* const* packed_in, const uint16_t* const* grads,
+                         const double* wq, const double* wk, double eps, double theta,
+                         double* const* dpacked, double* dw)
+{
+    if (check_geometry(W, b, seq_splits, head_splits, d) || (d % 2) != 0) return -1;
+    const int64_t S = offset_of(seq_splits, W);
+    const int64_t N = offset_of(head_splits, W);
+    if (planes < 2 || q_plane < 0 || q_plane >= planes || k_plane < 0 || k_plane >= planes ||
+        q_plane == k_plane || pitch < planes * N * d)
+        return -1;
+    double* x = (double*)malloc((size_t)d * sizeof(double));
+    double* g = (double*)malloc((size_t)d * sizeof(double));
+    for (int64_t j = 0; j < 2 * d; ++j) dw[j] = 0.0;
+    for (int q = 0; q < W; ++q) {
+        const int64_t s_q = seq_splits[q];
+        const int64_t seq_off_q = offset_of(seq_splits, q);
+        for (int64_t bb = 0; bb < b; ++bb)
+            for (int64_t i = 0; i < s_q; ++i) {
+                const int64_t token = (bb * s_q + i) * pitch;
+                for (int c = 0; c < planes; ++c)
+                    for (int64_t hg = 0; hg < N; ++hg) {
+                        int r = 0;
+                        while (!(hg >= offset_of(head_splits, r) &&
+                                 hg < offset_of(head_splits, r) + head_splits[r]))
+                            ++r;
+                        const int64_t n_r = head_splits[r];
+                        const int64_t h = hg - offset_of(head_splits, r);
+                        const int64_t at = token + (c * N + hg) * d;
+                        const int64_t head_row = ((bb * S + seq_off_q + i) * n_r + h) * d;
+                        const uint16_t* gr = grads[c * W + r] + head_row;
+                        if (c == q_plane || c == k_plane) {
+                            for (int64_t j = 0; j < d; ++j) {
+                                x[j] = orc_bf16_to_double(packed_in[q][at + j]);
+                                g[j] = orc_bf16_to_double(gr[j]);
+                            }
+                            orc_fused_row_bwd(x, g, d, c == q_plane ? wq : wk, eps,
+                                              (double)(seq_off_q + i), theta, dpacked[q] + at,
+                                              c == q_plane ? dw : dw + d);
+                        } else {
+                            for (int64_t j = 0; j < d; ++j)
+                                dpacked[q][at + j] = orc_bf16_to_double(gr[j]);
+                        }
+                    }
+            }
+    }
+    free(x);
+    free(g);
+    return 0;
+}
+
 /* ------------------------------------------------------------------------------------------ */
 /* Variants of the fused call: fp16 elements and rotate-half RoPE pairs.                        */
 /* ------------------------------------------------------------------------------------------ */

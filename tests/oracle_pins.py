@@ -428,6 +428,41 @@ def pin_packed_planes(orc, quick=False):
                 _same(again[1], ko, "extra columns: k")
 
 
+def pin_packed_planes_backward(orc, quick=False):
+    """Backward of the packed form: slicing the planes as in pin_packed_planes, the q and k planes'
+    gradients must equal the pinned backward of the fused call on those slices (bit for bit, dw
+    too: the rows are visited in the same order), every other plane's the pinned mode 1 of its
+    output gradient; the extra columns of a token are never written."""
+    rng = np.random.default_rng(49)
+    bf16 = lambda shape: (torch.from_numpy(rng.standard_normal(shape).astype(np.float32))  # noqa: E731
+                          .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    for W, b, seq, heads, d in [(2, 1, [3, 2], [2, 1], 8), (3, 2, [2, 0, 3], [1, 2, 1], 16),
+                                (4, 1, [1, 2, 1, 2], [2, 0, 1, 1], 8)]:
+        N, S = sum(heads), sum(seq)
+        wq = 1.0 + 0.1 * rng.standard_normal(d)
+        wk = 1.0 + 0.1 * rng.standard_normal(d)
+        for C, qp, kp, extra in [(3, 0, 1, 0), (4, 2, 0, 24), (2, 1, 0, 8)]:
+            pitch = C * N * d + extra
+            packed = [bf16((b, s, pitch)) for s in seq]
+            grads = [[bf16((b, S, n, d)) for n in heads] for _ in range(C)]
+            dx, dw = orc.packed_fused_bwd(packed, grads, seq, heads, d, C, qp, kp, pitch, wq, wk,
+                                          1e-6, 1e4)
+            plane = lambda arrs, c: [arr[:, :, c * N * d:(c + 1) * N * d].reshape(b, arr.shape[1], N, d)  # noqa: E731
+                                     for arr in arrs]
+            for c, w, row in ((qp, wq, 0), (kp, wk, 1)):
+                want_dx, want_dw = orc.qk_fused_bwd(plane(packed, c), grads[c], seq, heads, w, 1e-6,
+                                                    1e4)
+                _same(plane(dx, c), want_dx, f"packed bwd C={C}: plane {c}")
+                assert np.array_equal(dw[row], want_dw), f"packed bwd C={C}: dw {row}"
+            for c in range(C):
+                if c not in (qp, kp):
+                    want = orc.a2a_4d(grads[c], seq, heads, 1)
+                    got = [orc.double_to_bf16(x) for x in plane(dx, c)]
+                    _same(got, want, f"packed bwd C={C}: plane {c}")
+            for x in dx:
+                assert np.all(np.isnan(x[:, :, C * N * d:])), "extra columns written"
+
+
 def _torch_row_forward(x, w, eps, p, theta):
     """The fused row transform built from library pieces (F.rms_norm, complex multiplication),
     differentiable by torch.autograd."""
@@ -779,6 +814,7 @@ PINS = [
     pin_fused_placement_decode,
     pin_qkv_interleaved,
     pin_packed_planes,
+    pin_packed_planes_backward,
     pin_fused_bwd_vs_autograd,
     pin_fused_bwd_finite_differences,
     pin_fused_bwd_placement,

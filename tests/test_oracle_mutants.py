@@ -70,6 +70,10 @@ MUTANTS = {
                                 "transform_row(row, d, wq, eps, p, theta, k_out[r] + dst_row);")],
     "packed_plain_to_wrong_plane": [("plain_out[c * W + r][dst_row + j] = row[j];",
                                      "plain_out[c * W + r][dst_row + j] = row[j - (c > 0 ? N * d : 0)];")],
+    "packed_bwd_k_uses_q_weight": [("c == q_plane ? wq : wk, eps,", "wq, eps,")],
+    "packed_bwd_dw_shared": [("c == q_plane ? dw : dw + d);", "dw);")],
+    "packed_bwd_plain_from_wrong_plane": [("const uint16_t* gr = grads[c * W + r] + head_row;",
+                                           "const uint16_t* gr = grads[(c == q_plane || c == k_plane ? c : q_plane) * W + r] + head_row;")],
     "bwd_rope_forward_direction": [("orc_rope(u, d, -p, theta);", "orc_rope(u, d, p, theta);")],
     "bwd_drops_norm_projection": [("dx[j] = inv_rms * (u[j] * w[j] - xh * dot / (double)d);",
                                    "dx[j] = inv_rms * u[j] * w[j];")],
