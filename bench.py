@@ -240,6 +240,121 @@ def clock_sampler(cuda_index: int):
 
 
 # ------------------------------------------------------------------------------------------------
+class Workload:
+    def __init__(self, torch, B, wl, device):
+        self.torch, self.B = torch, B
+        cfg = wl.WAN
+        self.cfg = cfg
+        bf16 = torch.bfloat16
+        self.plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
+        self.q = wl.seq_side_inputs(cfg, device, seed=wl.FUSED.seed)
+        self.k = wl.seq_side_inputs(cfg, device, seed=wl.FUSED.extra["k_seed"])
+        self.v = wl.seq_side_inputs(cfg, device, seed=5)
+        self.o = wl.head_side_inputs(cfg, device, seed=6)
+        self.w = wl.rms_weights(cfg.d, seed=wl.FUSED.extra["w_seed"]).to(device)
+        head = [cfg.head_side_shape(r) for r in range(cfg.W)]
+        seq = [cfg.seq_side_shape(q) for q in range(cfg.W)]
+        self.qo = [torch.empty(s, dtype=bf16, device=device) for s in head]
+        self.ko = [torch.empty(s, dtype=bf16, device=device) for s in head]
+        self.vo = [torch.empty(s, dtype=bf16, device=device) for s in head]
+        self.oo = [torch.empty(s, dtype=bf16, device=device) for s in seq]
+        self.side = cfg.plane_bytes()          # one tensor set, all ranks: 774,144,000 bytes
+        self.bytes_fused = 4 * self.side       # q, k in; q, k out
+        self.bytes_plain = 2 * self.side       # in + out
+        self.bytes_step = self.bytes_fused + 2 * self.bytes_plain
+        self.launches_per_step = (B.ulysses_plan_num_chunks(self.plan, 0) * 2 +
+                                  B.ulysses_plan_num_chunks(self.plan, 1))
+
+    def step(self, stream, ev=None):
+        """One exchange step on `stream`; `ev`, if given, holds three events recorded after the
+        fused call, after the v relayout and after the attention-output relayout."""
+        B = self.B
+        B.ulysses_a2a_4d_qk_fused(self.plan, self.q, self.k, self.qo, self.ko, self.w, EPS, THETA,
+                                  stream)
+        if ev:
+            ev[0].record(stream)
+        B.ulysses_a2a_4d(self.plan, 0, self.v, self.vo, stream)
+        if ev:
+            ev[1].record(stream)
+        B.ulysses_a2a_4d(self.plan, 1, self.o, self.oo, stream)
+        if ev:
+            ev[2].record(stream)
+
+
+def back_to_back_ms(torch, stream, fn, n):
+    """Durations (ms) of n launches of fn enqueued back to back, from CUDA events recorded on
+    `stream` between consecutive calls. One call is enqueued before the first event, so the GPU is
+    busy whenever an event is recorded and the host's launch latency is not counted (an event
+    recorded on an idle GPU would time the host's enqueueing of the next call as well)."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    fn()
+    evs[0].record(stream)
+    for i in range(n):
+        fn()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
+
+
+def d2d_gbs(torch, nbytes, reps=20):
+    """Flat device-to-device copy (cudaMemcpyAsync) of nbytes, counted as read + write."""
+    a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    b = torch.empty_like(a)
+    a.fill_(1)
+    for _ in range(3):
+        b.copy_(a)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(reps):
+        b.copy_(a)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / reps
+    del a, b
+    return 2 * nbytes / (ms * 1e-3) / 1e9
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def source_digest(files) -> str | None:
+    """sha256 (first 16 hex digits) of the named csrc files, concatenated in the given order."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in files:
+        try:
+            with open(os.path.join(ROOT, "ulysses_sequence_all_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        except OSError:
+            return None
+    return h.hexdigest()[:16]
+
+
+def read_traffic(kernel: str):
+    """Per-launch DRAM bytes (read + write) from the committed ncu summary, or None when the
+    kernel's sources have changed since the counters were taken. Lines of profiles/traffic.txt:
+    kernel  comma-separated-source-files  digest  bytes-per-launch."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(path) as f:
+            lines = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    except OSError:
+        return None
+    for parts in lines:
+        if len(parts) >= 4 and parts[0] == kernel:
+            return int(parts[3]) if source_digest(parts[1].split(",")) == parts[2] else None
+    return None
+
+
+# ------------------------------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline and --impl reference)
 # ------------------------------------------------------------------------------------------------
 def oracle_step_sample(tokens_per_rank: int, seed: int = 0):
@@ -440,6 +555,20 @@ def run_ours(args):
         wk.plan, qkv, wk.qo, wk.ko, wk.vo, wk.w, EPS, THETA, stream), min(args.steps, 20))
     del qkv
 
+    # outside the step: QKVG packed as (b, s, 4, N, d) (the step's q, k, v and a gate plane), one
+    # launch for all four planes
+    cfg = wk.cfg
+    gate = wl.seq_side_inputs(cfg, "cuda", seed=7)
+    qkvg = [torch.stack([a, b, c, g], dim=2) for a, b, c, g in zip(wk.q, wk.k, wk.v, gate)]
+    go = [torch.empty_like(t) for t in wk.vo]
+    packed = lambda: B.ulysses_a2a_4d_packed_fused(  # noqa: E731
+        wk.plan, 4, 0, 1, 4 * cfg.N * cfg.d * 2, qkvg, [wk.qo, wk.ko, wk.vo, go], wk.w, EPS, THETA,
+        stream)
+    for _ in range(3):
+        packed()
+    qkvg_ms = back_to_back_ms(torch, stream, packed, min(args.steps, 20))
+    del gate, qkvg, go
+
     # outside the step: the backward of the fused call (dq, dk and dw from the gradients of q_out
     # and k_out; the step's own outputs serve as those gradients)
     dq = [torch.empty_like(t) for t in wk.q]
@@ -552,6 +681,12 @@ def run_ours(args):
             "median_ms": round(statistics.median(qkv_ms), 4),
             "GB/s": round(6 * wk.side / (statistics.median(qkv_ms) * 1e-3) / 1e9, 1),
             "frac_of_peak": round(6 * wk.side / (statistics.median(qkv_ms) * 1e-3) / 1e9 / peak, 4)},
+        "packed_qkvg_fused": {
+            "note": "outside the step: q, k, v and a gate plane packed as (b, s, 4, N, d), one "
+                    "launch: q, k normalised and rotated, v and g moved (mode 0)",
+            "median_ms": round(statistics.median(qkvg_ms), 4),
+            "GB/s": round(8 * wk.side / (statistics.median(qkvg_ms) * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(8 * wk.side / (statistics.median(qkvg_ms) * 1e-3) / 1e9 / peak, 4)},
         "qk_fused_backward": {
             "note": "outside the step: dq, dk (bf16) and dw (fp32) of the fused call, the RMSNorm + "
                     "RoPE VJP inside the mode-1 gather (2 launches: kernel + dw reduction); reads "
@@ -684,37 +819,53 @@ def run_e2e(torch, B, wk, stream, args):
             "per_call_ms": per_call, "window_ms": [round(w, 3) for w in windows]}
 
 
-def tiny_latency(torch, B, wl, stream, reps=200):
+def tiny_latency(torch, B, wl, stream, reps=200, in_graph=100):
     """The tiny configuration (W=2, b=1, 16 tokens per rank, 8 heads, d=128, bf16; 65,536 bytes
-    per side) is a latency point: the device time of one mode-0 and one mode-1 launch (CUDA events
-    between back-to-back launches, median), the host time of a whole round trip through the C ABI
-    from Python (perf_counter over `reps` round trips, then one synchronize), and a bit-exact
-    check that the round trip returns the input."""
+    per side) is a latency point. Reported: the device time of one round trip (mode 0 then mode 1
+    back), from a CUDA graph of `in_graph` round trips replayed on an otherwise idle GPU (no host
+    launch cost inside; median of 5 replays); the host time of a round trip through the C ABI from
+    Python (perf_counter over `reps` round trips, one synchronize at the end), which is what a
+    caller launching one call at a time sees; and a bit-exact check of the round trip."""
     cfg = wl.TINY
     plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
     x = wl.seq_side_inputs(cfg, "cuda")
     y = [torch.empty(cfg.head_side_shape(r), dtype=torch.bfloat16, device="cuda") for r in range(cfg.W)]
     z = [torch.empty_like(t) for t in x]
-    m0 = lambda: B.ulysses_a2a_4d(plan, 0, x, y, stream)  # noqa: E731
-    m1 = lambda: B.ulysses_a2a_4d(plan, 1, y, z, stream)  # noqa: E731
+
+    def round_trip():  # on the current stream
+        B.ulysses_a2a_4d(plan, 0, x, y)
+        B.ulysses_a2a_4d(plan, 1, y, z)
+
     for _ in range(10):
-        m0()
-        m1()
-    us0 = statistics.median(back_to_back_ms(torch, stream, m0, reps)) * 1e3
-    us1 = statistics.median(back_to_back_ms(torch, stream, m1, reps)) * 1e3
+        round_trip()
     torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    with torch.cuda.graph(graph, stream=side):
+        for _ in range(in_graph):
+            round_trip()
+    graph.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    device_us = statistics.median(ts) * 1e3 / in_graph
     t0 = time.perf_counter()
     for _ in range(reps):
-        m0()
-        m1()
+        round_trip()
     torch.cuda.synchronize()
     host_us = (time.perf_counter() - t0) / reps * 1e6
     exact = all(torch.equal(a.view(torch.int16), b.view(torch.int16)) for a, b in zip(x, z))
     assert exact, "tiny round trip did not return its input"
     return {"config": cfg.name, "kernel": "relayout round trip (latency point)", "W": cfg.W,
-            "dtype": cfg.dtype, "bytes": cfg.relayout_bytes(), "mode0_device_us": round(us0, 2),
-            "mode1_device_us": round(us1, 2), "round_trip_host_us": round(host_us, 2),
-            "round_trip_bit_exact": exact}
+            "dtype": cfg.dtype, "bytes": 2 * cfg.relayout_bytes(),
+            "round_trip_device_us": round(device_us, 2), "round_trip_host_us": round(host_us, 2),
+            "launches_per_round_trip": 2, "round_trip_bit_exact": exact}
 
 
 def run_configs(args):

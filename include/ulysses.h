@@ -264,6 +264,30 @@ int ulysses_a2a_4d_qkv_fused(ulysses_plan_t plan, const void* const* qkv_in, voi
                              float rope_theta, void* stream);
 
 /*
+ * The fused call on any packed input of C planes per token (FastVideo, "Ulysses performance on
+ * GB200": packed QKV or QKVG, the layouts a fused projection writes): rank q's input holds b * s_q
+ * tokens, token (bb, i) starting (bb * s_q + i) * token_pitch bytes in, and within a token plane
+ * c's rows (N heads of d elements) start at byte c * N * d * elem_size. In one launch per chunk,
+ * the rows of plane q_plane and of plane k_plane are normalised, rotated and placed as
+ * ulysses_a2a_4d_qk_fused does (q_plane with rms_w's first row, k_plane with its second), and
+ * every other plane is placed by mode 0 unchanged (bit-exact). ulysses_a2a_4d_qkv_fused is the
+ * case planes = 3, q_plane = 0, k_plane = 1, token_pitch = 3 * N * d * elem_size.
+ *   planes          2 .. 8.
+ *   q_plane, k_plane   distinct, in [0, planes).
+ *   token_pitch     bytes between consecutive tokens, >= planes * N * d * elem_size and a multiple
+ *                   of 16 (ULY_EALIGN otherwise); bytes of a token beyond its planes are not read.
+ *   packed_in       W device pointers, rank q's b * s_q * token_pitch bytes (plan's dtype).
+ *   outs            planes * W device pointers, plane-major: outs[c * W + r] is rank r's
+ *                   (b, S, n_r, d) output of plane c.
+ *   rms_w, eps, rope_theta, plan requirements: as ulysses_a2a_4d_qk_fused. The chunk cap applies
+ *   per plane. Outputs may not overlap inputs or each other (ULY_EOVERLAP).
+ */
+int ulysses_a2a_4d_packed_fused(ulysses_plan_t plan, int planes, int q_plane, int k_plane,
+                                int64_t token_pitch, const void* const* packed_in,
+                                void* const* outs, const float* rms_w, float eps, float rope_theta,
+                                void* stream);
+
+/*
  * Backward of ulysses_a2a_4d_qkv_fused on the same plan (the pairing of the interleaved call, as
  * ulysses_a2a_4d_qk_fused_backward is of the separate one): the gradient of the packed input
  * (b, s_q, 3, N, d) from the gradients of the three outputs. Planes q and k receive the fused
@@ -282,6 +306,30 @@ int ulysses_a2a_4d_qkv_fused_backward(ulysses_plan_t plan, void* const* dqkv_out
                                       const void* const* dk_in, const void* const* dv_in,
                                       const float* rms_w, float* dw, float eps, float rope_theta,
                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward of ulysses_a2a_4d_packed_fused on the same plan and packing (the general form of
+ * ulysses_a2a_4d_qkv_fused_backward, which is its case planes = 3, q_plane = 0, k_plane = 1,
+ * token_pitch = 3 * N * d * elem_size): the gradient of the packed input from the gradients of
+ * every plane's output. The q and k planes receive the fused RMSNorm + RoPE vector-Jacobian
+ * product exactly as ulysses_a2a_4d_qk_fused_backward computes it; every other plane receives its
+ * output gradient moved by mode 1 (bit-exact). Bytes of a token beyond its planes are not written.
+ * One launch per chunk covers all planes, plus the dw reduction.
+ *   planes, q_plane, k_plane, token_pitch   as ulysses_a2a_4d_packed_fused.
+ *   dpacked_out     W device pointers, rank q's b * s_q * token_pitch bytes.
+ *   packed_in       W device pointers, the forward's packed inputs (only the q and k planes are
+ *                   read).
+ *   grads           planes * W device pointers, plane-major: grads[c * W + r] is rank r's
+ *                   (b, S, n_r, d) gradient of plane c's output.
+ *   rms_w, dw, eps, rope_theta, workspace, plan requirements and errors: as
+ *   ulysses_a2a_4d_qk_fused_backward (the same workspace size).
+ */
+int ulysses_a2a_4d_packed_fused_backward(ulysses_plan_t plan, int planes, int q_plane,
+                                         int k_plane, int64_t token_pitch,
+                                         void* const* dpacked_out, const void* const* packed_in,
+                                         const void* const* grads, const float* rms_w, float* dw,
+                                         float eps, float rope_theta, void* workspace,
+                                         size_t workspace_bytes, void* stream);
 
 /*
  * End-to-end form for host-resident data: copy each rank's input from host_in[k] to dev_in[k],

@@ -106,3 +106,34 @@ def test_qkv_gradients_match_the_backward_call():
         assert torch.equal(x.grad.view(torch.int16), ref.view(torch.int16))
     assert torch.equal(wr.grad.view(torch.int32), dw.view(torch.int32))
 
+
+
+def test_packed_gradients_match_the_backward_call():
+    """QKVG packed with extra columns per token (q plane 2, k plane 0): autograd's gradients equal
+    the direct backward call's bytes, and the extra columns get exactly zero gradient."""
+    W, b, seq, heads, d = G
+    N, S = sum(heads), sum(seq)
+    planes, extra = 4, 16
+    pitch = planes * N * d + extra
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(23)
+    packed = [torch.randn((b, s, pitch), generator=gen).to(torch.bfloat16).cuda() for s in seq]
+    grads = [[torch.randn((b, S, n, d), generator=gen).to(torch.bfloat16).cuda() for n in heads]
+             for _ in range(planes)]
+    w = make_inputs(G, seed=24)[2]
+    plan = B.ulysses_plan(*G, "bfloat16")
+    xr = [x.clone().requires_grad_() for x in packed]
+    wr = w.clone().requires_grad_()
+    outs = A.packed_fused(plan, xr, planes, 2, 0, wr, EPS, THETA)
+    torch.autograd.backward([t for plane in outs for t in plane],
+                            [t for plane in grads for t in plane])
+    dpk = [torch.zeros_like(x) for x in packed]
+    dw = torch.empty_like(w)
+    ws = torch.empty(B.ulysses_qk_fused_backward_workspace(plan), dtype=torch.uint8, device="cuda")
+    B.ulysses_a2a_4d_packed_fused_backward(plan, planes, 2, 0, pitch * 2, dpk, packed, grads, w, dw,
+                                           EPS, THETA, ws)
+    torch.cuda.synchronize()
+    for x, ref in zip(xr, dpk):
+        assert torch.equal(x.grad.view(torch.int16), ref.view(torch.int16))
+        assert int(torch.count_nonzero(x.grad[:, :, planes * N * d:].float())) == 0
+    assert torch.equal(wr.grad.view(torch.int32), dw.view(torch.int32))

@@ -1,7 +1,7 @@
 """Full-size, element-by-element parity of the fused kernels against the oracle.
 
-Every output element of the fused forward, the interleaved QKV call and the two backwards is
-compared at the Wan-720p shape (W=8, b=1, 75,600 tokens, 40 heads, d=128), and the fused forward
+Every output element of the fused forward, the interleaved QKV call, the packed QKVG call and the
+two backwards is compared at the Wan-720p shape (W=8, b=1, 75,600 tokens, 40 heads, d=128), and the fused forward
 also on the long packed-QKV geometry (W=4, 250,000 tokens, 56 heads, positions to 249,999). The
 plans, and so the launch configurations (grid, work units, stages, CTAs per SM), are the ones the
 benchmark times; its inputs too where it draws them: q, k, v of the step (seeds 3, 4, 5, weights
@@ -193,6 +193,33 @@ def test_fused_long_sequence_full(oracle):
         del ref
 
 
+def test_packed_qkvg_wan720p_full(oracle):
+    """QKVG packed as (b, s, 4, N, d) (q, k, v of the step, seeds 3, 4, 5, and a gate plane, seed
+    6): one call; every element of q and k, v and g byte for byte."""
+    cfg, plan = _wan_plan()
+    planes = [wl.seq_side_inputs(cfg, "cuda", seed=sd) for sd in (3, 4, 5, 6)]
+    packed = [torch.stack(list(p), dim=2) for p in zip(*planes)]
+    w = wl.rms_weights(cfg.d, seed=2).cuda()
+    outs = _head_outputs(cfg, torch.bfloat16, 4)
+    B.ulysses_a2a_4d_packed_fused(plan, 4, 0, 1, 4 * cfg.N * cfg.d * 2, packed,
+                                  [o.tensors for o in outs], w, EPS, THETA)
+    torch.cuda.synchronize()
+    assert all(o.guards_intact() for o in outs), "a kernel wrote outside its output"
+    del packed
+    wn = w.cpu().numpy().astype(np.float64)
+    # the packed oracle is the planes' slices through the fused transform and mode 0 (pinned)
+    for t in (0, 1):
+        ref = oracle.qk_fused_A([host_raw(x) for x in planes[t]], cfg.seq_splits,
+                                cfg.head_splits, wn[t], EPS, THETA, threads=THREADS)
+        for r in range(cfg.W):
+            check_all(outs[t].tensors[r], ref[r], 2.0 ** -8, 1e-5, f"plane {t} rank {r}")
+        del ref
+    for c in (2, 3):
+        want = oracle.a2a_4d([host_raw(x) for x in planes[c]], cfg.seq_splits, cfg.head_splits, 0)
+        for r in range(cfg.W):
+            check_bytes(outs[c].tensors[r], want[r], f"plane {c} rank {r}")
+
+
 # ---- backward ---------------------------------------------------------------------------------
 def _wan_grads(cfg, dtype, seeds):
     """Output gradients of q and k, N(0, 1) head-side tensors (independent of the outputs, so
@@ -259,6 +286,42 @@ def test_qkv_backward_wan720p_full(oracle):
         for qr in range(cfg.W):
             check_all(dqkv.tensors[qr][:, :, t], ref_dx[qr], 2.0 ** -8, 1e-4,
                       f"plane {t} rank {qr}")
+        del ref_dx
+        check_dw(dwo.tensors[0][t].cpu().numpy(), ref_dw, n_rows, f"dw {t}")
+
+
+def test_packed_qkvg_backward_wan720p_full(oracle):
+    """Backward of the QKVG packed call at the Wan shape: packed q, k, v, g (seeds 3, 4, 5, 6),
+    output gradients N(0, 1) (seeds 52, 53, 54, 55): every element of the q and k planes of the
+    packed gradient, the v and g planes byte for byte (mode 1 of their gradients), and dw."""
+    cfg, plan = _wan_plan()
+    planes = [wl.seq_side_inputs(cfg, "cuda", seed=sd) for sd in (3, 4, 5, 6)]
+    packed = [torch.stack(list(p), dim=2) for p in zip(*planes)]
+    w = wl.rms_weights(cfg.d, seed=2).cuda()
+    grads = _wan_grads(cfg, "bfloat16", (52, 53, 54, 55))
+    shape = lambda q: (1, cfg.seq_splits[q], 4, cfg.N, cfg.d)  # noqa: E731
+    dpk = _seq_outputs(cfg, torch.bfloat16, shape)
+    dwo = GuardedOutputs([(2, cfg.d)], torch.float32)
+    ws = torch.empty(B.ulysses_qk_fused_backward_workspace(plan), dtype=torch.uint8, device="cuda")
+    B.ulysses_a2a_4d_packed_fused_backward(plan, 4, 0, 1, 4 * cfg.N * cfg.d * 2, dpk.tensors,
+                                           packed, grads, w, dwo.tensors[0], EPS, THETA, ws)
+    torch.cuda.synchronize()
+    assert dpk.guards_intact() and dwo.guards_intact(), "a kernel wrote outside its output"
+    del packed
+    wn = w.cpu().numpy().astype(np.float64)
+    n_rows = cfg.S * cfg.N
+    for c in (2, 3):
+        want = oracle.a2a_4d([host_raw(x) for x in grads[c]], cfg.seq_splits, cfg.head_splits, 1)
+        for qr in range(cfg.W):
+            check_bytes(dpk.tensors[qr][:, :, c].contiguous(), want[qr], f"plane {c} rank {qr}")
+        del want
+    # the packed backward oracle is the planes' slices through the pinned backward (pinned)
+    for t in (0, 1):
+        ref_dx, ref_dw = oracle.qk_fused_bwd([host_raw(x) for x in planes[t]],
+                                             [host_raw(v) for v in grads[t]], cfg.seq_splits,
+                                             cfg.head_splits, wn[t], EPS, THETA, threads=THREADS)
+        for qr in range(cfg.W):
+            check_all(dpk.tensors[qr][:, :, t], ref_dx[qr], 2.0 ** -8, 1e-4, f"plane {t} rank {qr}")
         del ref_dx
         check_dw(dwo.tensors[0][t].cpu().numpy(), ref_dw, n_rows, f"dw {t}")
 

@@ -195,3 +195,35 @@ def test_fused_argument_errors_before_cuda():
         with pytest.raises(B.UlyssesError) as ei:
             B.ulysses_a2a_4d_qk_fused(p, *args, stream=0)
         assert ei.value.status == status
+
+
+def test_packed_argument_errors_before_cuda():
+    """The packed fused call refuses bad plane counts and roles, a short or unaligned token pitch,
+    and overlapping outputs on the host."""
+    plan = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "bfloat16")
+    row = 4 * 64 * 2                                  # one plane of one token: N * d * e bytes
+    out_b = [B.ulysses_plan_bytes(plan, 0, k)[1] for k in range(2)]
+    w = 1 << 43
+
+    def call(planes, qp, kp, pitch, outs=None):
+        ins = _fake_ptrs(1 << 40, [4 * pitch] * 2)
+        outs = outs or [_fake_ptrs((1 << 41) + (c << 30), out_b) for c in range(planes)]
+        B.ulysses_a2a_4d_packed_fused(plan, planes, qp, kp, pitch, ins, outs, w, 1e-6, 1e4,
+                                      stream=0)
+
+    for args, status in [
+        ((1, 0, 1, row), B.ULY_EINVAL),          # fewer than two planes
+        ((9, 0, 1, 9 * row), B.ULY_EINVAL),      # more than eight
+        ((3, 1, 1, 3 * row), B.ULY_EINVAL),      # q and k the same plane
+        ((3, 0, 3, 3 * row), B.ULY_EINVAL),      # k plane out of range
+        ((3, -1, 1, 3 * row), B.ULY_EINVAL),     # q plane out of range
+        ((3, 0, 1, 3 * row - 16), B.ULY_EINVAL), # pitch shorter than the planes
+        ((3, 0, 1, 3 * row + 8), B.ULY_EALIGN),  # pitch not a multiple of 16 bytes
+    ]:
+        with pytest.raises(B.UlyssesError) as ei:
+            call(*args)
+        assert ei.value.status == status, args
+    same = _fake_ptrs(1 << 41, out_b)
+    with pytest.raises(B.UlyssesError) as ei:        # two planes' outputs on the same buffers
+        call(3, 0, 1, 3 * row, outs=[same, same, _fake_ptrs(1 << 42, out_b)])
+    assert ei.value.status == B.ULY_EOVERLAP

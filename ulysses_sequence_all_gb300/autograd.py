@@ -12,6 +12,9 @@ plan for the backward:
   allocated by torch.
 * ``qkv_fused(plan, qkv, rms_w, eps, rope_theta)``: the interleaved packed-QKV call; its backward
   is ``ulysses_a2a_4d_qkv_fused_backward`` (packed dqkv and the gradient of ``rms_w``).
+* ``packed_fused(plan, packed, planes, q_plane, k_plane, rms_w, eps, rope_theta)``: the call on
+  any packing of C planes per token (QKVG, ...); its backward is
+  ``ulysses_a2a_4d_packed_fused_backward``; a token's columns beyond its planes get zero gradient.
 
 Inputs and outputs are lists of W tensors (one per virtual rank) on the current CUDA device;
 the outputs are new tensors the caller owns. Nothing here computes: every step runs in the
@@ -147,3 +150,44 @@ def qk_fused(plan: B.Plan, q, k, rms_w: torch.Tensor, eps: float, rope_theta: fl
     out = _QKFused.apply(plan, eps, rope_theta, rms_w, *q, *k)
     W = len(q)
     return list(out[:W]), list(out[W:])
+
+
+class _PackedFused(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, plan, planes, q_plane, k_plane, eps, rope_theta, rms_w, *packed):
+        packed = [x.contiguous() for x in packed]
+        rms_w = rms_w.contiguous()
+        like = packed[0]
+        pitch = like[0, 0].numel() * like.element_size() if like.dim() > 2 else like.element_size()
+        outs = [_empty(plan, 0, like) for _ in range(planes)]
+        B.ulysses_a2a_4d_packed_fused(plan, planes, q_plane, k_plane, pitch, packed, outs, rms_w,
+                                      eps, rope_theta)
+        ctx.plan, ctx.eps, ctx.theta, ctx.W = plan, eps, rope_theta, len(packed)
+        ctx.planes, ctx.q_plane, ctx.k_plane, ctx.pitch = planes, q_plane, k_plane, pitch
+        ctx.save_for_backward(rms_w, *packed)
+        return tuple(t for plane in outs for t in plane)
+
+    @staticmethod
+    def backward(ctx, *grads):
+        plan, W = ctx.plan, ctx.W
+        rms_w, *packed = ctx.saved_tensors
+        like = packed[0]
+        gs = [_grads(grads[c * W:(c + 1) * W], plan, 0, like) for c in range(ctx.planes)]
+        dpacked = [torch.zeros_like(x) for x in packed]  # columns beyond the planes: zero
+        dw = torch.empty_like(rms_w, dtype=torch.float32)
+        ws = torch.empty(B.ulysses_qk_fused_backward_workspace(plan), dtype=torch.uint8,
+                         device=like.device)
+        B.ulysses_a2a_4d_packed_fused_backward(plan, ctx.planes, ctx.q_plane, ctx.k_plane,
+                                               ctx.pitch, dpacked, packed, gs, rms_w, dw, ctx.eps,
+                                               ctx.theta, ws)
+        return (None, None, None, None, None, None, dw, *dpacked)
+
+
+def packed_fused(plan: B.Plan, packed, planes: int, q_plane: int, k_plane: int,
+                 rms_w: torch.Tensor, eps: float, rope_theta: float):
+    """The fused call on packed inputs (rank q's tensor: (b, s_q, ...) with `planes` planes of
+    N * d elements at the start of each token, the token pitch being the product of the trailing
+    dimensions), differentiable in packed and rms_w. Returns one list of W tensors per plane."""
+    out = _PackedFused.apply(plan, planes, q_plane, k_plane, eps, rope_theta, rms_w, *packed)
+    W = len(packed)
+    return [list(out[c * W:(c + 1) * W]) for c in range(planes)]

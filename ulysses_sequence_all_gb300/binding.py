@@ -29,9 +29,10 @@ EXPORTS = ["ulysses_plan", "ulysses_plan_destroy", "ulysses_plan_set_chunk_bytes
            "ulysses_plan_set_max_ctas", "ulysses_plan_set_rope_pairs",
            "ulysses_plan_bytes", "ulysses_plan_num_chunks", "ulysses_plan_chunk_rows",
            "ulysses_a2a_4d", "ulysses_a2a_4d_engine", "ulysses_a2a_4d_qk_fused",
-           "ulysses_a2a_4d_qkv_fused", "ulysses_a2a_4d_qk_fused_backward",
+           "ulysses_a2a_4d_qkv_fused", "ulysses_a2a_4d_packed_fused",
+           "ulysses_a2a_4d_qk_fused_backward",
            "ulysses_qk_fused_backward_workspace", "ulysses_a2a_4d_qk_fused_backward_static",
-           "ulysses_a2a_4d_qkv_fused_backward",
+           "ulysses_a2a_4d_qkv_fused_backward", "ulysses_a2a_4d_packed_fused_backward",
            "ulysses_a2a_4d_host", "ulysses_a2a_4d_qk_fused_host", "ulysses_device_status",
            "ulysses_selftest_wait_timeout", "ulysses_last_cuda_error", "ulysses_strerror",
            "ulysses_version"]
@@ -76,6 +77,9 @@ def _lib():
                                                 ctypes.c_float, _p]
         lib.ulysses_a2a_4d_qkv_fused.argtypes = [_p, _pp, _pp, _pp, _pp, _p, ctypes.c_float,
                                                  ctypes.c_float, _p]
+        lib.ulysses_a2a_4d_packed_fused.argtypes = [_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    _i64, _pp, _pp, _p, ctypes.c_float,
+                                                    ctypes.c_float, _p]
         lib.ulysses_a2a_4d_qk_fused_backward.argtypes = [_p, _pp, _pp, _pp, _pp, _pp, _pp, _p, _p,
                                                          ctypes.c_float, ctypes.c_float, _p,
                                                          ctypes.c_size_t, _p]
@@ -83,6 +87,10 @@ def _lib():
         lib.ulysses_a2a_4d_qkv_fused_backward.argtypes = [_p, _pp, _pp, _pp, _pp, _pp, _p, _p,
                                                           ctypes.c_float, ctypes.c_float, _p,
                                                           ctypes.c_size_t, _p]
+        lib.ulysses_a2a_4d_packed_fused_backward.argtypes = [_p, ctypes.c_int, ctypes.c_int,
+                                                             ctypes.c_int, _i64, _pp, _pp, _pp, _p,
+                                                             _p, ctypes.c_float, ctypes.c_float,
+                                                             _p, ctypes.c_size_t, _p]
         lib.ulysses_a2a_4d_qk_fused_backward_static.argtypes = [_p, _pp, _pp, _pp, _pp, _pp, _pp,
                                                                 _p, _p, ctypes.c_float,
                                                                 ctypes.c_float, _p]
@@ -224,6 +232,17 @@ def ulysses_a2a_4d_qkv_fused(plan: Plan, qkv_in, q_out, k_out, v_out, rms_w, eps
                                            _stream(stream)), "ulysses_a2a_4d_qkv_fused")
 
 
+def ulysses_a2a_4d_packed_fused(plan: Plan, planes: int, q_plane: int, k_plane: int,
+                                token_pitch: int, packed_in, outs, rms_w, eps: float,
+                                rope_theta: float, stream=None):
+    """outs: one sequence of W output tensors per plane (planes lists), flattened plane-major."""
+    flat = [t for plane in outs for t in plane]
+    _check(_lib().ulysses_a2a_4d_packed_fused(plan, planes, q_plane, k_plane, token_pitch,
+                                              _ptrs(packed_in), _ptrs(flat), _addr(rms_w), eps,
+                                              rope_theta, _stream(stream)),
+           "ulysses_a2a_4d_packed_fused")
+
+
 def ulysses_qk_fused_backward_workspace(plan: Plan) -> int:
     """Workspace bytes ulysses_a2a_4d_qk_fused_backward needs for `plan` on the current device."""
     n = ctypes.c_size_t()
@@ -249,6 +268,18 @@ def ulysses_a2a_4d_qkv_fused_backward(plan: Plan, dqkv_out, qkv_in, dq_in, dk_in
         plan, _ptrs(dqkv_out), _ptrs(qkv_in), _ptrs(dq_in), _ptrs(dk_in), _ptrs(dv_in),
         _addr(rms_w), _addr(dw), eps, rope_theta, _addr(workspace), _nbytes(workspace),
         _stream(stream)), "ulysses_a2a_4d_qkv_fused_backward")
+
+
+def ulysses_a2a_4d_packed_fused_backward(plan: Plan, planes: int, q_plane: int, k_plane: int,
+                                         token_pitch: int, dpacked_out, packed_in, grads, rms_w,
+                                         dw, eps: float, rope_theta: float, workspace,
+                                         stream=None):
+    """grads: one sequence of W gradient tensors per plane, flattened plane-major."""
+    flat = [t for plane in grads for t in plane]
+    _check(_lib().ulysses_a2a_4d_packed_fused_backward(
+        plan, planes, q_plane, k_plane, token_pitch, _ptrs(dpacked_out), _ptrs(packed_in),
+        _ptrs(flat), _addr(rms_w), _addr(dw), eps, rope_theta, _addr(workspace),
+        _nbytes(workspace), _stream(stream)), "ulysses_a2a_4d_packed_fused_backward")
 
 
 def ulysses_a2a_4d_qk_fused_backward_static(plan: Plan, dq_out, dk_out, q_in, k_in, dq_in, dk_in,

@@ -225,57 +225,77 @@ int relayout_impl(const Plan& p, int mode, int engine, const void* const* in_ptr
     return ULY_OK;
 }
 
+// A packed fused input: rank q's b * s_q tokens, `pitch` bytes apart, each holding `planes` planes
+// of N * d elements (plane c at byte c * N * d * e of the token); outs[c * W + r] is rank r's
+// (b, S, n_r, d) output of plane c (q_plane's and k_plane's receive the transformed rows).
+struct PackedIn {
+    const void* const* in;
+    int planes, q_plane, k_plane;
+    int64_t pitch;
+    void* const* outs;
+};
+
 // Checks of a fused call (no CUDA call) and its argument block, without the unit tables. Either
-// q_in and k_in are given (separate tensors) or qkv_in and v_out (interleaved (b, s, 3, N, d)).
+// q_in, k_in, q_out and k_out are given (separate tensors) or a packed input (pk).
 int fused_prepare(const Plan& p, const void* const* q_in, const void* const* k_in,
-                  const void* const* qkv_in, void* const* q_out, void* const* k_out,
-                  void* const* v_out, const float* rms_w, float eps, float rope_theta, FusedArgs* a,
-                  int64_t* tokens_per_unit)
+                  void* const* q_out, void* const* k_out, const PackedIn* pk, const float* rms_w,
+                  float eps, float rope_theta, FusedArgs* a, int64_t* tokens_per_unit)
 {
-    const bool qkv = qkv_in != nullptr;
     if (p.dtype != ULY_BF16 && p.dtype != ULY_F16) return ULY_EINVAL;
     if (!(p.d == 8 || p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128 || p.d == 256))
         return ULY_EINVAL;
     if (p.S >= (int64_t(1) << 24)) return ULY_EINVAL;  // positions must be exact in fp32
     if (!(eps >= 0.0f) || !(rope_theta > 0.0f)) return ULY_EINVAL;
-    if (!rms_w || (qkv && !v_out)) return ULY_EINVAL;
+    if (!rms_w) return ULY_EINVAL;
     if (!aligned16(rms_w)) return ULY_EALIGN;
-    int64_t in_b[kMaxW], out_b[kMaxW], qkv_b[kMaxW];
+    const int W = p.W;
+    const int64_t row_bytes = p.N * p.d * p.e;
+    int64_t in_b[kMaxW], out_b[kMaxW], packed_b[kMaxW];
     side_bytes(p, 0, in_b, out_b);
-    for (int k = 0; k < p.W; ++k) qkv_b[k] = 3 * in_b[k];
+    if (pk) {
+        if (!pk->in || !pk->outs || pk->planes < 2 || pk->planes > kMaxPlanes ||
+            pk->q_plane < 0 || pk->q_plane >= pk->planes || pk->k_plane < 0 ||
+            pk->k_plane >= pk->planes || pk->q_plane == pk->k_plane ||
+            pk->pitch < pk->planes * row_bytes)
+            return ULY_EINVAL;
+        if (pk->pitch % 16 != 0) return ULY_EALIGN;
+        for (int k = 0; k < W; ++k) packed_b[k] = p.b * p.s[k] * pk->pitch;
+        q_out = pk->outs + size_t(pk->q_plane) * W;
+        k_out = pk->outs + size_t(pk->k_plane) * W;
+    }
     int rc;
-    if (qkv) {
-        if ((rc = check_ptrs(qkv_in, qkv_b, p.W)) ||
-            (rc = check_ptrs(const_cast<const void* const*>(v_out), out_b, p.W)))
-            return rc;
-    } else if ((rc = check_ptrs(q_in, in_b, p.W)) || (rc = check_ptrs(k_in, in_b, p.W))) {
+    if (pk) {
+        if ((rc = check_ptrs(pk->in, packed_b, W))) return rc;
+        for (int c = 0; c < pk->planes; ++c)
+            if ((rc = check_ptrs(const_cast<const void* const*>(pk->outs + size_t(c) * W), out_b, W)))
+                return rc;
+    } else if ((rc = check_ptrs(q_in, in_b, W)) || (rc = check_ptrs(k_in, in_b, W)) ||
+               (rc = check_ptrs(const_cast<const void* const*>(q_out), out_b, W)) ||
+               (rc = check_ptrs(const_cast<const void* const*>(k_out), out_b, W))) {
         return rc;
     }
-    if ((rc = check_ptrs(const_cast<const void* const*>(q_out), out_b, p.W)) ||
-        (rc = check_ptrs(const_cast<const void* const*>(k_out), out_b, p.W)))
-        return rc;
     // every input (plus the weights) against every output
     const void* ins[2 * kMaxW + 1];
     int64_t ins_b[2 * kMaxW + 1];
-    const void* outs[3 * kMaxW];
-    int64_t outs_b[3 * kMaxW];
+    const void* outs[kMaxPlanes * kMaxW];
+    int64_t outs_b[kMaxPlanes * kMaxW];
     int n_in = 0, n_out = 0;
-    for (int k = 0; k < p.W; ++k) {
-        if (qkv) {
-            ins[n_in] = qkv_in[k];
-            ins_b[n_in++] = qkv_b[k];
+    for (int k = 0; k < W; ++k) {
+        if (pk) {
+            ins[n_in] = pk->in[k];
+            ins_b[n_in++] = packed_b[k];
+            for (int c = 0; c < pk->planes; ++c) {
+                outs[n_out] = pk->outs[size_t(c) * W + k];
+                outs_b[n_out++] = out_b[k];
+            }
         } else {
             ins[n_in] = q_in[k];
             ins_b[n_in++] = in_b[k];
             ins[n_in] = k_in[k];
             ins_b[n_in++] = in_b[k];
-        }
-        outs[n_out] = q_out[k];
-        outs_b[n_out++] = out_b[k];
-        outs[n_out] = k_out[k];
-        outs_b[n_out++] = out_b[k];
-        if (qkv) {
-            outs[n_out] = v_out[k];
+            outs[n_out] = q_out[k];
+            outs_b[n_out++] = out_b[k];
+            outs[n_out] = k_out[k];
             outs_b[n_out++] = out_b[k];
         }
     }
@@ -284,19 +304,30 @@ int fused_prepare(const Plan& p, const void* const* q_in, const void* const* k_i
     if ((rc = check_overlap(ins, ins_b, n_in, outs, outs_b, n_out))) return rc;
     int stages = 0, ctas_per_sm = 1;
     uint32_t stage_bytes = 0;
-    // a stage holds the q and k rows of tokens_per_unit tokens (an interleaved call's v units hold
-    // the v rows of twice as many tokens: the same bytes)
+    // a stage holds the q and k rows of tokens_per_unit tokens (a packed call's other-plane units
+    // hold one plane's rows of twice as many tokens: the same bytes)
     fused_geometry(p, 2, tokens_per_unit, &stages, &stage_bytes, &ctas_per_sm);
     if (stages == 0) return ULY_EINVAL;  // one token's rows do not fit the stages
     std::memset(a, 0, sizeof *a);
     a->ctas_per_sm = ctas_per_sm;
-    a->interleaved = qkv ? 1 : 0;
+    a->interleaved = pk ? 1 : 0;
     a->elem_f16 = p.dtype == ULY_F16 ? 1 : 0;
     a->rope_half = p.rope_half;
-    for (int k = 0; k < p.W; ++k) {
-        if (qkv) {
-            a->qkv_in[k] = static_cast<const uint8_t*>(qkv_in[k]);
-            a->v_out[k] = static_cast<uint8_t*>(v_out[k]);
+    if (pk) {
+        a->planes = pk->planes;
+        a->q_plane = pk->q_plane;
+        a->k_plane = pk->k_plane;
+        a->tok_pitch = pk->pitch;
+        int n_plain = 0;
+        for (int c = 0; c < pk->planes; ++c) {
+            if (c != pk->q_plane && c != pk->k_plane) a->plain_plane[n_plain++] = c;
+            for (int k = 0; k < W; ++k)
+                a->plane_out[c][k] = static_cast<uint8_t*>(pk->outs[size_t(c) * W + k]);
+        }
+    }
+    for (int k = 0; k < W; ++k) {
+        if (pk) {
+            a->packed_in[k] = static_cast<const uint8_t*>(pk->in[k]);
         } else {
             a->q_in[k] = static_cast<const uint8_t*>(q_in[k]);
             a->k_in[k] = static_cast<const uint8_t*>(k_in[k]);
@@ -317,22 +348,21 @@ int fused_rows(const Plan& p, FusedArgs* a, int64_t tokens_per_unit, const Chunk
                cudaStream_t stream, const DeviceInfo& dev)
 {
     if (a->interleaved)
-        build_fused_units(p, rows, tokens_per_unit, 2 * tokens_per_unit, 3, a);
+        build_fused_units(p, rows, tokens_per_unit, 2 * tokens_per_unit, a->planes, a);
     else
         build_fused_units(p, rows, tokens_per_unit, tokens_per_unit, 1, a);
     cudaError_t e = fused_launch(*a, stream, dev.device, dev.sm_count, p.max_ctas);
     return e == cudaSuccess ? ULY_OK : cuda_fail(e);
 }
 
-// The device forms of both fused calls: checks, then one launch per chunk of the plan.
+// The device forms of the fused calls: checks, then one launch per chunk of the plan.
 int fused_device(const Plan& p, const void* const* q_in, const void* const* k_in,
-                 const void* const* qkv_in, void* const* q_out, void* const* k_out,
-                 void* const* v_out, const float* rms_w, float eps, float rope_theta,
-                 cudaStream_t stream)
+                 void* const* q_out, void* const* k_out, const PackedIn* pk, const float* rms_w,
+                 float eps, float rope_theta, cudaStream_t stream)
 {
     FusedArgs a;
     int64_t T = 0;
-    int rc = fused_prepare(p, q_in, k_in, qkv_in, q_out, k_out, v_out, rms_w, eps, rope_theta, &a, &T);
+    int rc = fused_prepare(p, q_in, k_in, q_out, k_out, pk, rms_w, eps, rope_theta, &a, &T);
     if (rc) return rc;
     int64_t C = 0;
     if ((rc = num_chunks(p, &C))) return rc;
@@ -467,13 +497,23 @@ int fused_bwd_device(const Plan& p, void* const* dq_out, void* const* dk_out,
                          rope_theta, workspace, stream);
 }
 
-// The backward of the interleaved QKV call: dq, dk (the fused VJP) and dv (mode 1) written into
-// one (b, s_q, 3, N, d) tensor per rank.
-int qkv_bwd_device(const Plan& p, void* const* dqkv_out, const void* const* qkv_in,
-                   const void* const* dq_in, const void* const* dk_in, const void* const* dv_in,
-                   const float* rms_w, float* dw, float eps, float rope_theta, void* workspace,
-                   size_t workspace_bytes, cudaStream_t stream)
+// The backward of a packed fused call: for the q and k planes the fused VJP, for every other plane
+// its gradient by mode 1, all written into rank q's packed gradient (the same pitch; a token's
+// columns beyond its planes are not written). grads[c * W + r] is rank r's gradient of plane c's
+// output.
+int packed_bwd_device(const Plan& p, void* const* dpacked_out, const void* const* packed_in,
+                      int planes, int q_plane, int k_plane, int64_t pitch,
+                      const void* const* grads, const float* rms_w, float* dw, float eps,
+                      float rope_theta, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream)
 {
+    const int W = p.W;
+    const int64_t row = p.N * p.d * p.e;  // one token's heads of one plane
+    if (!dpacked_out || !packed_in || !grads || planes < 2 || planes > kMaxPlanes ||
+        q_plane < 0 || q_plane >= planes || k_plane < 0 || k_plane >= planes ||
+        q_plane == k_plane || pitch < planes * row || pitch >= (int64_t(1) << 31))
+        return ULY_EINVAL;
+    if (pitch % 16 != 0) return ULY_EALIGN;
     DeviceInfo dev;
     int rc = current_device(&dev);
     if (rc) return rc;
@@ -484,29 +524,28 @@ int qkv_bwd_device(const Plan& p, void* const* dqkv_out, const void* const* qkv_
     if ((rc = fused_bwd_common(p, dev, rms_w, dw, eps, rope_theta, workspace, workspace_bytes, &T,
                                &stages, &stage_bytes, &ctas_per_sm, &need)))
         return rc;
-    int64_t seq_b[kMaxW], head_b[kMaxW], qkv_b[kMaxW];
+    int64_t seq_b[kMaxW], head_b[kMaxW], packed_b[kMaxW];
     side_bytes(p, 0, seq_b, head_b);
-    for (int k = 0; k < p.W; ++k) qkv_b[k] = 3 * seq_b[k];
-    if ((rc = check_ptrs(qkv_in, qkv_b, p.W)) || (rc = check_ptrs(dq_in, head_b, p.W)) ||
-        (rc = check_ptrs(dk_in, head_b, p.W)) || (rc = check_ptrs(dv_in, head_b, p.W)) ||
-        (rc = check_ptrs(const_cast<const void* const*>(dqkv_out), qkv_b, p.W)))
+    for (int k = 0; k < W; ++k) packed_b[k] = p.b * p.s[k] * pitch;
+    if ((rc = check_ptrs(packed_in, packed_b, W)) ||
+        (rc = check_ptrs(const_cast<const void* const*>(dpacked_out), packed_b, W)))
         return rc;
-    const void* ins[4 * kMaxW + 1];
-    int64_t ins_b[4 * kMaxW + 1];
+    for (int c = 0; c < planes; ++c)
+        if ((rc = check_ptrs(grads + size_t(c) * W, head_b, W))) return rc;
+    const void* ins[(kMaxPlanes + 1) * kMaxW + 1];
+    int64_t ins_b[(kMaxPlanes + 1) * kMaxW + 1];
     const void* outs[kMaxW + 2];
     int64_t outs_b[kMaxW + 2];
     int n_in = 0, n_out = 0;
-    for (int k = 0; k < p.W; ++k) {
-        ins[n_in] = qkv_in[k];
-        ins_b[n_in++] = qkv_b[k];
-        ins[n_in] = dq_in[k];
-        ins_b[n_in++] = head_b[k];
-        ins[n_in] = dk_in[k];
-        ins_b[n_in++] = head_b[k];
-        ins[n_in] = dv_in[k];
-        ins_b[n_in++] = head_b[k];
-        outs[n_out] = dqkv_out[k];
-        outs_b[n_out++] = qkv_b[k];
+    for (int k = 0; k < W; ++k) {
+        ins[n_in] = packed_in[k];
+        ins_b[n_in++] = packed_b[k];
+        for (int c = 0; c < planes; ++c) {
+            ins[n_in] = grads[size_t(c) * W + k];
+            ins_b[n_in++] = head_b[k];
+        }
+        outs[n_out] = dpacked_out[k];
+        outs_b[n_out++] = packed_b[k];
     }
     ins[n_in] = rms_w;
     ins_b[n_in++] = 2 * p.d * int64_t(sizeof(float));
@@ -515,23 +554,26 @@ int qkv_bwd_device(const Plan& p, void* const* dqkv_out, const void* const* qkv_
     outs[n_out] = workspace;
     outs_b[n_out++] = int64_t(need);
     if ((rc = check_overlap(ins, ins_b, n_in, outs, outs_b, n_out))) return rc;
-    const int64_t row = p.N * p.d * p.e;  // one token's heads of one plane
+    // tensor t of the kernel: 0 the q plane, 1 the k plane, 2 .. the other planes in order
+    int plane_of[kMaxPlanes];
+    plane_of[0] = q_plane;
+    plane_of[1] = k_plane;
+    for (int c = 0, t = 2; c < planes; ++c)
+        if (c != q_plane && c != k_plane) plane_of[t++] = c;
     FusedBwdArgs a;
     std::memset(&a, 0, sizeof a);
-    for (int k = 0; k < p.W; ++k) {
-        const uint8_t* in = static_cast<const uint8_t*>(qkv_in[k]);
-        uint8_t* out = static_cast<uint8_t*>(dqkv_out[k]);
-        a.x_in[0][k] = in ? in : nullptr;
-        a.x_in[1][k] = in ? in + row : nullptr;
-        a.dx_out[0][k] = out ? out : nullptr;
-        a.dx_out[1][k] = out ? out + row : nullptr;
-        a.dx_out[2][k] = out ? out + 2 * row : nullptr;
-        a.g_in[0][k] = static_cast<const uint8_t*>(dq_in[k]);
-        a.g_in[1][k] = static_cast<const uint8_t*>(dk_in[k]);
-        a.g_in[2][k] = static_cast<const uint8_t*>(dv_in[k]);
+    for (int k = 0; k < W; ++k) {
+        const uint8_t* in = static_cast<const uint8_t*>(packed_in[k]);
+        uint8_t* out = static_cast<uint8_t*>(dpacked_out[k]);
+        for (int t = 0; t < planes; ++t) {
+            const int64_t off = int64_t(plane_of[t]) * row;
+            if (t < 2) a.x_in[t][k] = in ? in + off : nullptr;
+            a.dx_out[t][k] = out ? out + off : nullptr;
+            a.g_in[t][k] = static_cast<const uint8_t*>(grads[size_t(plane_of[t]) * W + k]);
+        }
     }
-    a.tensors = 3;
-    a.tok_stride = int32_t(3 * row);
+    a.tensors = planes;
+    a.tok_stride = int32_t(pitch);
     return fused_bwd_run(p, a, dev, T, stages, stage_bytes, ctas_per_sm, rms_w, dw, eps,
                          rope_theta, workspace, stream);
 }
@@ -797,7 +839,7 @@ int ulysses_a2a_4d_qk_fused(ulysses_plan_t plan, const void* const* q_in, const 
                             float rope_theta, void* stream)
 {
     if (!plan) return ULY_EINVAL;
-    return fused_device(plan->p, q_in, k_in, nullptr, q_out, k_out, nullptr, rms_w, eps, rope_theta,
+    return fused_device(plan->p, q_in, k_in, q_out, k_out, nullptr, rms_w, eps, rope_theta,
                         static_cast<cudaStream_t>(stream));
 }
 
@@ -831,8 +873,29 @@ int ulysses_a2a_4d_qkv_fused_backward(ulysses_plan_t plan, void* const* dqkv_out
                                       void* workspace, size_t workspace_bytes, void* stream)
 {
     if (!plan || !qkv_in || !dqkv_out || !dq_in || !dk_in || !dv_in) return ULY_EINVAL;
-    return qkv_bwd_device(plan->p, dqkv_out, qkv_in, dq_in, dk_in, dv_in, rms_w, dw, eps,
-                          rope_theta, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+    const Plan& p = plan->p;
+    const void* grads[3 * kMaxW];
+    for (int k = 0; k < p.W; ++k) {
+        grads[k] = dq_in[k];
+        grads[p.W + k] = dk_in[k];
+        grads[2 * p.W + k] = dv_in[k];
+    }
+    return packed_bwd_device(p, dqkv_out, qkv_in, 3, 0, 1, 3 * p.N * p.d * p.e, grads, rms_w, dw,
+                             eps, rope_theta, workspace, workspace_bytes,
+                             static_cast<cudaStream_t>(stream));
+}
+
+int ulysses_a2a_4d_packed_fused_backward(ulysses_plan_t plan, int planes, int q_plane,
+                                         int k_plane, int64_t token_pitch,
+                                         void* const* dpacked_out, const void* const* packed_in,
+                                         const void* const* grads, const float* rms_w, float* dw,
+                                         float eps, float rope_theta, void* workspace,
+                                         size_t workspace_bytes, void* stream)
+{
+    if (!plan) return ULY_EINVAL;
+    return packed_bwd_device(plan->p, dpacked_out, packed_in, planes, q_plane, k_plane,
+                             token_pitch, grads, rms_w, dw, eps, rope_theta, workspace,
+                             workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 int ulysses_a2a_4d_qk_fused_backward_static(ulysses_plan_t plan, void* const* dq_out,
@@ -863,9 +926,28 @@ int ulysses_a2a_4d_qkv_fused(ulysses_plan_t plan, const void* const* qkv_in, voi
                              void* const* k_out, void* const* v_out, const float* rms_w, float eps,
                              float rope_theta, void* stream)
 {
-    if (!plan || !qkv_in) return ULY_EINVAL;
-    return fused_device(plan->p, nullptr, nullptr, qkv_in, q_out, k_out, v_out, rms_w, eps,
-                        rope_theta, static_cast<cudaStream_t>(stream));
+    if (!plan || !qkv_in || !q_out || !k_out || !v_out) return ULY_EINVAL;
+    const Plan& p = plan->p;
+    void* outs[3 * kMaxW];
+    for (int k = 0; k < p.W; ++k) {
+        outs[k] = q_out[k];
+        outs[p.W + k] = k_out[k];
+        outs[2 * p.W + k] = v_out[k];
+    }
+    const PackedIn pk{qkv_in, 3, 0, 1, 3 * p.N * p.d * p.e, outs};
+    return fused_device(p, nullptr, nullptr, nullptr, nullptr, &pk, rms_w, eps, rope_theta,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int ulysses_a2a_4d_packed_fused(ulysses_plan_t plan, int planes, int q_plane, int k_plane,
+                                int64_t token_pitch, const void* const* packed_in,
+                                void* const* outs, const float* rms_w, float eps, float rope_theta,
+                                void* stream)
+{
+    if (!plan || !packed_in || !outs) return ULY_EINVAL;
+    const PackedIn pk{packed_in, planes, q_plane, k_plane, token_pitch, outs};
+    return fused_device(plan->p, nullptr, nullptr, nullptr, nullptr, &pk, rms_w, eps, rope_theta,
+                        static_cast<cudaStream_t>(stream));
 }
 
 int ulysses_a2a_4d_host(ulysses_plan_t plan, int mode, const void* const* host_in,
@@ -930,7 +1012,7 @@ int ulysses_a2a_4d_qk_fused_host(ulysses_plan_t plan, const void* const* q_host_
     FusedArgs a;
     int64_t T = 0;
     int rc = fused_prepare(p, const_cast<const void* const*>(q_in), const_cast<const void* const*>(k_in),
-                           nullptr, q_out, k_out, nullptr, rms_w, eps, rope_theta, &a, &T);
+                           q_out, k_out, nullptr, rms_w, eps, rope_theta, &a, &T);
     if (rc) return rc;
     PipeChunks pc;
     if ((rc = pipe_chunks(p, &pc))) return rc;

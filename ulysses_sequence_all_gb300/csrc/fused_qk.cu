@@ -7,12 +7,14 @@
 //
 // Structure: a persistent grid of several CTAs per SM, each with a ring of K shared-memory
 // stages. A work unit is a few consecutive tokens of one source rank: all N heads of q and of k,
-// two contiguous spans of the sequence-side tensors. An interleaved (b, s, 3, N, d) input is cut
-// into blocks of twice as many tokens with three units each (the q and k rows of the first half,
-// of the second half, and the v rows of the whole block), so that every unit fills the same
-// stage and the v rows pass through without arithmetic. The grid takes every q,k unit first and
-// then every v unit: at any time it writes 16 destination streams (q, k of 8 ranks) or 8 (v),
-// not 24, which measured 6.5% faster than rotating through the three kinds. Warp roles per CTA:
+// two contiguous spans of the sequence-side tensors. A packed input (C planes per token, such as
+// the interleaved (b, s, 3, N, d) QKV or QKVG layouts, FastVideo, "Ulysses performance on GB200")
+// is cut into blocks of twice as many tokens with C units each (the q and k rows of the first
+// half, of the second half, and one unit per other plane with that plane's rows of the whole
+// block), so that every unit fills the same stage and the other planes pass through without
+// arithmetic. The grid takes every q,k unit first and then each other plane's units in turn: at
+// any time it writes 16 destination streams (q, k of 8 ranks) or 8 (one plane), not 24, which
+// measured 6.5% faster than rotating through the three kinds of a QKV input. Warp roles per CTA:
 //  * loader: lane 0 waits for the stage to be free ("empty" mbarrier), starts the cp.async.bulk
 //    loads (completing on the stage's "full" mbarrier as transaction bytes) and leaves a record
 //    of the unit beside the stage; while the copies fly, all lanes fill the stage's cos/sin
@@ -22,14 +24,17 @@
 //    cp.async.bulk store per (token, q|k, destination rank): n_r heads that are contiguous in the
 //    stage and in the destination; as soon as those stores have read shared memory (kFusedDrain
 //    units later; 0 by default, so right away) the stage is handed back to the loader ("empty");
-//  * consumers: half of them take q rows, half k rows. A group of d/8 lanes holds one head row
-//    (8 values per lane, as packed fp32 pairs) and each group keeps kIlp rows in flight; the sum
-//    of squares is reduced with xor shuffles inside the group, the weight and rotation are
-//    applied in registers, and the bf16 result overwrites its input in shared memory. Each
-//    consumer warp then fences its writes for the async proxy and arrives on "computed".
+//  * consumers: one warp takes the q rows, one the k rows. A group of 8 lanes holds one head
+//    row (each lane 8 of its RoPE pairs as packed fp32 values, two 16-byte shared-memory
+//    accesses per lane; fused_row.cuh) and keeps 3 rows in flight; the sum of squares is reduced
+//    with xor shuffles inside the group, the weight and rotation are applied in registers, and
+//    the result overwrites its input in shared memory. Each consumer warp then fences its writes
+//    for the async proxy and arrives on "computed".
 // Measured at the Wan shape, throughput grows with the number of CTAs issuing bulk copies per SM
 // more than with ring depth, so the default footprint is small (2 stages of one token's q and k)
-// and 4 CTAs share an SM; wider rows fall back to fewer CTAs per SM (see fused_geometry).
+// and 4 CTAs share an SM; wider rows fall back to fewer CTAs per SM (see fused_geometry). Two
+// consumer warps of 8-lane rows with 3 rows in flight (128 registers a thread) measured faster
+// than four of 16-lane rows (80 registers), for both RoPE pair layouts.
 //
 // RoPE angles: p * theta^(-2j/d) reaches ~75,600 rad at the Wan shape, where an fp32 product
 // alone is off by ~5e-3 rad. The angle is formed in turns (units of 2 pi): the host supplies
@@ -55,7 +60,7 @@ static __device__ unsigned g_fused_status;
 #define ULY_FUSED_CTAS_PER_SM 4
 #endif
 #ifndef ULY_FUSED_CONSUMER_WARPS
-#define ULY_FUSED_CONSUMER_WARPS 4
+#define ULY_FUSED_CONSUMER_WARPS 2
 #endif
 #ifndef ULY_FUSED_STAGE_TARGET
 #define ULY_FUSED_STAGE_TARGET 20480
@@ -82,13 +87,21 @@ constexpr int kFusedThreads = 32 * (kFirstConsumerWarp + ULY_FUSED_CONSUMER_WARP
 #define ULY_FUSED_ILP 3
 #endif
 constexpr int kIlp = ULY_FUSED_ILP;  // head rows in flight per lane group
+#ifndef ULY_FUSED_ILP_WIDE  // the same for the 8-pair row layout (rotate half), twice the values
+#define ULY_FUSED_ILP_WIDE 3
+#endif
+constexpr int kIlpWide = ULY_FUSED_ILP_WIDE;
+#ifndef ULY_FUSED_WIDE  // 1: 8 RoPE pairs per lane for adjacent pairs too (fused_row.cuh)
+#define ULY_FUSED_WIDE 1
+#endif
+constexpr bool kFusedWide = ULY_FUSED_WIDE != 0;
 
 // What the storer and the consumers need of a unit, written by the loader beside the stage
 // before its last arrive on "full" (the loader decodes each unit once).
 struct FusedRecord {
     int64_t head_row0;  // first row of the unit on the head side: bb * S + seq_off(q) + i0
     int32_t ntok;
-    int32_t kind;       // 0, 1: q and k rows; 2: v rows (interleaved calls)
+    int32_t kind;       // 0, 1: q and k rows; 2 + 4 c: plane c's rows, moved plain (packed calls)
 };
 
 #ifndef ULY_FUSED_WAIT_HINT_NS  // suspend-time hint of the barrier waits (0: plain polling)
@@ -107,8 +120,10 @@ __device__ __forceinline__ bool fused_wait(uint64_t* bar, uint32_t parity)
 struct FusedUnit {
     int q;
     int64_t bb, i0;
-    int ntok;  // may be 0: the second q,k unit of an interleaved block that holds few tokens
-    int kind;  // 0, 1: q and k rows of the block's first / second tokens_per_unit tokens; 2: v rows
+    int ntok;   // may be 0: the second q,k unit of a packed block that holds few tokens
+    int kind;   // 0, 1: q and k rows of the block's first / second tokens_per_unit tokens; 2: a
+                // plain plane's rows
+    int plane;  // kind 2: the plane
 };
 
 __device__ __forceinline__ FusedUnit fused_decode(const FusedArgs& a, int64_t u)
@@ -116,14 +131,18 @@ __device__ __forceinline__ FusedUnit fused_decode(const FusedArgs& a, int64_t u)
     FusedUnit t;
     int64_t blk_id = u;
     t.kind = 0;
-    if (a.units_per_block == 3) {  // two phases: every q,k unit (two per block), then every v unit
-        const int64_t blocks_all = a.total_units / 3;
+    t.plane = 0;
+    if (a.interleaved) {  // phases: every q,k unit (two per block), then each plain plane's units
+        const int64_t blocks_all = a.unit_begin[kMaxW];
         if (u < 2 * blocks_all) {
             blk_id = u >> 1;
             t.kind = int(u & 1);
         } else {
-            blk_id = u - 2 * blocks_all;
+            const int64_t v = u - 2 * blocks_all;
+            const int pp = int(div_fast(v, blocks_all));
+            blk_id = v - int64_t(pp) * blocks_all;
             t.kind = 2;
+            t.plane = a.plain_plane[pp];
         }
     }
     int lo = 0, hi = a.W - 1;
@@ -177,16 +196,21 @@ __host__ __device__ inline FusedSmem fused_smem_layout(int d, int tokens, int st
     return m;
 }
 
-// G: lanes per head row (d = 8 G); F16: fp16 elements (else bf16); HALF_PAIRS: rotate-half RoPE
-// pairs (else adjacent pairs). The row layouts are in fused_row.cuh.
-template <int G, bool F16, bool HALF_PAIRS>
+// D: head dimension; F16: fp16 elements (else bf16); HALF_PAIRS: rotate-half RoPE pairs (else
+// adjacent pairs). The row layouts (G lanes per row, H packed slots per lane) are in
+// fused_row.cuh.
+template <int D, bool F16, bool HALF_PAIRS>
 __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     fused_qk_kernel(const __grid_constant__ FusedArgs a)
 {
-    constexpr int D = 8 * G;
+    using IO = RowIO<F16, HALF_PAIRS, D, kFusedWide>;
+    constexpr int G = IO::G;
+    constexpr int H = IO::H;
     constexpr int HALF = D / 2;
     constexpr int GPW = 32 / G;         // head rows per warp per slot
-    constexpr int PER_STEP = GPW * kIlp;
+    // rows in flight per lane group: a lane of an 8-pair layout holds twice the values
+    constexpr int ILP = IO::P == 8 ? kIlpWide : kIlp;
+    constexpr int PER_STEP = GPW * ILP;
     constexpr int NW = ULY_FUSED_CONSUMER_WARPS;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int K = a.stages;
@@ -215,9 +239,9 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     const bool qkv = a.interleaved != 0;
     // Stage layouts. A q,k unit holds row (token t, plane c in {q, k}, head h) at
     // t * tok_stride + c * plane_stride(ntok) + h * 2d: separate inputs arrive as two spans (all q
-    // rows, then all k rows), an interleaved input as one copy per token of its q and k rows,
-    // which are adjacent in the (b, s, 3, N, d) layout. A v unit (interleaved only) holds its
-    // tokens' v rows back to back, one copy per token.
+    // rows, then all k rows), a packed input as one copy per token of its q and k rows (two when
+    // the k plane does not follow the q plane). A plain-plane unit (packed only) holds its tokens'
+    // rows of that plane back to back, one copy per token.
     const int tok_stride = qkv ? 2 * row_bytes : row_bytes;
     auto plane_stride = [&](int ntok) { return qkv ? row_bytes : ntok * row_bytes; };
 
@@ -251,25 +275,42 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
                 FusedRecord& rec = records[s];  // published by this lane's arrive below
                 rec.head_row0 = t.bb * a.S + a.seq_off[t.q] + t.i0;
                 rec.ntok = t.ntok;
-                rec.kind = t.kind;
+                rec.kind = t.kind + 4 * t.plane;
             }
-            if (qkv) {  // one copy per token: its q and k rows, or its v row
+            if (qkv) {  // per token: its q and k rows (one copy when k's plane follows q's), or
+                        // its row of the unit's plane
                 __syncwarp();  // after lane 0 registered the unit's bytes
-                const uint32_t each = v_unit ? uint32_t(row_bytes) : 2u * uint32_t(row_bytes);
-                const uint8_t* src = a.qkv_in[t.q] + tok0 * 3 * row_bytes + (v_unit ? 2 * row_bytes : 0);
-                for (int tok = lane; tok < t.ntok; tok += 32)
-                    bulk_g2s(dst + size_t(tok) * each, src + int64_t(tok) * 3 * row_bytes, each, &full[s]);
+                const uint8_t* src = a.packed_in[t.q] + tok0 * a.tok_pitch;
+                if (v_unit) {
+                    const uint8_t* from = src + int64_t(t.plane) * row_bytes;
+                    for (int tok = lane; tok < t.ntok; tok += 32)
+                        bulk_g2s(dst + size_t(tok) * row_bytes, from + int64_t(tok) * a.tok_pitch,
+                                 uint32_t(row_bytes), &full[s]);
+                } else if (a.k_plane == a.q_plane + 1) {
+                    const uint8_t* from = src + int64_t(a.q_plane) * row_bytes;
+                    for (int tok = lane; tok < t.ntok; tok += 32)
+                        bulk_g2s(dst + size_t(tok) * 2 * row_bytes, from + int64_t(tok) * a.tok_pitch,
+                                 2u * uint32_t(row_bytes), &full[s]);
+                } else {
+                    for (int c = lane; c < 2 * t.ntok; c += 32) {
+                        const int tok = c >> 1, which = c & 1;
+                        const int plane = which ? a.k_plane : a.q_plane;
+                        bulk_g2s(dst + size_t(c) * row_bytes,
+                                 src + int64_t(tok) * a.tok_pitch + int64_t(plane) * row_bytes,
+                                 uint32_t(row_bytes), &full[s]);
+                    }
+                }
             }
             float* table = reinterpret_cast<float*>(smem + L.tables + s * L.table_bytes);
             const float p0 = float(a.seq_off[t.q] + t.i0);
-            // Per token, lane i of a row group owns pairs 4i .. 4i+3, read as two 16-byte
-            // entries (c_j, c_j+1, s_j, s_j+1) for j = 4i and j = 4i+2; the entries of all lanes
-            // for j = 4i come first, then those for j = 4i+2, so each read is contiguous.
+            // Per token, lane i of a row group owns pairs P i .. P i + P - 1, read as P / 2
+            // 16-byte entries (c_j, c_j+1, s_j, s_j+1) for j = P i + 2h; for each h the entries
+            // of all lanes are adjacent, so each read is contiguous.
             for (int e = lane; e < (v_unit ? 0 : t.ntok * HALF); e += 32) {
                 const int tok = e / HALF, jj = e % HALF;
                 const float2 tj = turns[jj];
                 const float2 cs = rope_cos_sin(p0 + float(tok), tj.x, tj.y);
-                const int at = ((tok * 2 + ((jj >> 1) & 1)) * G + (jj >> 2)) * 4 + (jj & 1);
+                const int at = IO::table_at(tok, jj);
                 table[at] = cs.x;
                 table[at + 2] = cs.y;
             }
@@ -304,7 +345,8 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
             const uint8_t* st = smem + L.stages + size_t(s) * a.stage_bytes;
             const int64_t row0 = rec.head_row0;
             const int W = a.W;
-            const bool v_unit = rec.kind == 2;
+            const bool v_unit = (rec.kind & 3) == 2;
+            uint8_t* const* plain_out = a.plane_out[rec.kind >> 2];
             const int uplanes = v_unit ? 1 : 2;
             const int ustride = v_unit ? row_bytes : tok_stride;
             const int pstride = plane_stride(rec.ntok);
@@ -315,7 +357,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
                 const int64_t run = a.n[r] * (D * 2);
                 if (run == 0) continue;
                 const uint8_t* src = st + tok * ustride + plane * pstride + a.head_off[r] * (D * 2);
-                uint8_t* out = v_unit ? a.v_out[r] : plane == 0 ? a.q_out[r] : a.k_out[r];
+                uint8_t* out = v_unit ? plain_out[r] : plane == 0 ? a.q_out[r] : a.k_out[r];
                 bulk_s2g(out + (row0 + tok) * run, src, uint32_t(run));
             }
             bulk_commit();
@@ -334,14 +376,13 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     const int cw = warp - kFirstConsumerWarp;
     const int which = cw >= HALF_NW;          // 0: q, 1: k (uniform per warp)
     const int cwi = cw - which * HALF_NW;     // rank among the warps of this tensor
-    const int sub = lane % G;                 // which 8 values of the row this lane holds
+    const int sub = lane % G;                 // which pairs of the row this lane holds
     const int group = lane / G;               // which head row of the warp slot
-    using IO = RowIO<F16, HALF_PAIRS, D>;
-    // This lane's 8 weights as packed pairs: first / second elements of its pairs, plus the
+    // This lane's weights as packed pairs: first / second elements of its pairs, plus the
     // negated second ones (the rotation subtracts them).
-    float2 wE[2], wO[2], wOn[2];
+    float2 wE[H], wO[H], wOn[H];
     IO::weights(a.rms_w + which * D, sub, wE, wO);
-    for (int h = 0; h < 2; ++h) wOn[h] = make_float2(-wO[h].x, -wO[h].y);
+    for (int h = 0; h < H; ++h) wOn[h] = make_float2(-wO[h].x, -wO[h].y);
     const float inv_d = 1.0f / float(D);
     // this warp's share of the rows of a full token block (steps m_lo .. m_hi - 1 of PER_STEP
     // rows) and the (token, head) of its first row
@@ -356,7 +397,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
             if (lane == 0) atomicOr(&g_fused_status, kStatusWaitTimeout);
             break;
         }
-        if (records[s].kind == 2) {  // v rows: nothing to compute
+        if ((records[s].kind & 3) == 2) {  // a plain plane's rows: nothing to compute
             __syncwarp();
             if (lane == 0) mbar_arrive(&computed[s]);
             continue;
@@ -377,14 +418,14 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
         }
         int base = m_lo * PER_STEP;   // first row of the current step and its (token, head)
         for (int m = m_lo; m < m_hi; ++m) {
-            uint8_t* slot[kIlp];
-            int tok[kIlp];
-            bool ok[kIlp];
+            uint8_t* slot[ILP];
+            int tok[ILP];
+            bool ok[ILP];
             // first / second elements of this lane's pairs, packed
-            float2 vE[kIlp][2], vO[kIlp][2];
-            float ss[kIlp];
+            float2 vE[ILP][H], vO[ILP][H];
+            float ss[ILP];
 #pragma unroll
-            for (int u = 0; u < kIlp; ++u) {
+            for (int u = 0; u < ILP; ++u) {
                 const int o = u * GPW + group;
                 ok[u] = base + o < rows;
                 int hh = base_head + o, tk = base_tok;
@@ -394,31 +435,32 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
                 }
                 slot[u] = rows_base + tk * tok_stride + hh * (D * 2);
                 tok[u] = tk;
-                uint4 x = make_uint4(0, 0, 0, 0);
+                typename IO::Words x = {};
                 if (ok[u]) x = IO::load(slot[u], sub);
-                IO::unpack(x, 0, vE[u][0], vO[u][0]);
-                IO::unpack(x, 1, vE[u][1], vO[u][1]);
-                float2 acc = __fmul2_rn(vE[u][0], vE[u][0]);
-                acc = __ffma2_rn(vO[u][0], vO[u][0], acc);
-                acc = __ffma2_rn(vE[u][1], vE[u][1], acc);
-                acc = __ffma2_rn(vO[u][1], vO[u][1], acc);
+                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    IO::unpack(x, h, vE[u][h], vO[u][h]);
+                    acc = __ffma2_rn(vE[u][h], vE[u][h], acc);
+                    acc = __ffma2_rn(vO[u][h], vO[u][h], acc);
+                }
                 ss[u] = acc.x + acc.y;
             }
 #pragma unroll
             for (int off = G / 2; off > 0; off >>= 1) {
 #pragma unroll
-                for (int u = 0; u < kIlp; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], off);
+                for (int u = 0; u < ILP; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], off);
             }
 #pragma unroll
-            for (int u = 0; u < kIlp; ++u) {
+            for (int u = 0; u < ILP; ++u) {
                 if (!ok[u]) continue;
                 const float inv = rsqrtf(ss[u] * inv_d + a.eps);
                 const float2 inv2 = make_float2(inv, inv);
-                float2 oEs[2], oOs[2];
+                float2 oEs[H], oOs[H];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    // (c_j, c_j+1, s_j, s_j+1) for j = 4 sub + 2 h (see the table layout)
-                    const float4 cs = table[(tok[u] * 2 + h) * G + sub];
+                for (int h = 0; h < H; ++h) {
+                    // (c_j, c_j+1, s_j, s_j+1) for j = P sub + 2 h (see the table layout)
+                    const float4 cs = table[IO::table_entry(tok[u], h, sub)];
                     const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
                     const float2 A = __fmul2_rn(vE[u][h], wE[h]);   // weighted first elements
                     const float2 Bp = __fmul2_rn(vO[u][h], wO[h]);  // weighted second elements
@@ -481,31 +523,31 @@ void fused_geometry(const Plan& p, int planes, int64_t* tokens_per_unit, int* st
 // per device: the kernel variants whose shared-memory limit has been raised (any host thread)
 static std::atomic<unsigned> g_fused_smem_set[64];
 
-template <int G, bool F16, bool HALF>
-static cudaError_t launch_g(const FusedArgs& a, cudaStream_t stream, int device, int grid)
+template <int D, bool F16, bool HALF>
+static cudaError_t launch_d(const FusedArgs& a, cudaStream_t stream, int device, int grid)
 {
-    constexpr int gbit = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : G == 8 ? 3 : G == 16 ? 4 : 5;
-    constexpr unsigned bit = 1u << (gbit * 4 + (F16 ? 2 : 0) + (HALF ? 1 : 0));
+    constexpr int dbit = D == 8 ? 0 : D == 16 ? 1 : D == 32 ? 2 : D == 64 ? 3 : D == 128 ? 4 : 5;
+    constexpr unsigned bit = 1u << (dbit * 4 + (F16 ? 2 : 0) + (HALF ? 1 : 0));
     if (device >= 0 && device < 64 && !(g_fused_smem_set[device].load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(fused_qk_kernel<G, F16, HALF>,
+        cudaError_t e = cudaFuncSetAttribute(fused_qk_kernel<D, F16, HALF>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemPerCtaMax);
         if (e != cudaSuccess) return e;
         g_fused_smem_set[device].fetch_or(bit);
     }
     const FusedSmem m = fused_smem_layout(a.d, a.tokens_per_unit, a.stages, a.stage_bytes);
-    fused_qk_kernel<G, F16, HALF><<<grid, kFusedThreads, m.total, stream>>>(a);
+    fused_qk_kernel<D, F16, HALF><<<grid, kFusedThreads, m.total, stream>>>(a);
     return cudaGetLastError();
 }
 
-template <int G>
+template <int D>
 static cudaError_t launch_variant(const FusedArgs& a, cudaStream_t stream, int device, int grid)
 {
     if (a.elem_f16)
-        return a.rope_half ? launch_g<G, true, true>(a, stream, device, grid)
-                           : launch_g<G, true, false>(a, stream, device, grid);
-    return a.rope_half ? launch_g<G, false, true>(a, stream, device, grid)
-                       : launch_g<G, false, false>(a, stream, device, grid);
+        return a.rope_half ? launch_d<D, true, true>(a, stream, device, grid)
+                           : launch_d<D, true, false>(a, stream, device, grid);
+    return a.rope_half ? launch_d<D, false, true>(a, stream, device, grid)
+                       : launch_d<D, false, false>(a, stream, device, grid);
 }
 
 cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count,
@@ -515,13 +557,13 @@ cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, in
     int64_t grid = int64_t(sm_count) * (a.ctas_per_sm > 0 ? a.ctas_per_sm : 1);
     if (max_grid > 0 && grid > max_grid) grid = max_grid;
     if (grid > a.total_units) grid = a.total_units;
-    switch (a.d / 8) {
-        case 1: return launch_variant<1>(a, stream, device, int(grid));
-        case 2: return launch_variant<2>(a, stream, device, int(grid));
-        case 4: return launch_variant<4>(a, stream, device, int(grid));
+    switch (a.d) {
         case 8: return launch_variant<8>(a, stream, device, int(grid));
         case 16: return launch_variant<16>(a, stream, device, int(grid));
         case 32: return launch_variant<32>(a, stream, device, int(grid));
+        case 64: return launch_variant<64>(a, stream, device, int(grid));
+        case 128: return launch_variant<128>(a, stream, device, int(grid));
+        case 256: return launch_variant<256>(a, stream, device, int(grid));
         default: return cudaErrorInvalidValue;
     }
 }

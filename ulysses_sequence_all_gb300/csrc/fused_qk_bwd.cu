@@ -13,19 +13,25 @@
 // dx is rounded once to bf16 and written on the sequence side, where x came from; gy is read
 // on the head side, where mode 0 put y, so the rows arrive through the mode-1 gather.
 //
-// Structure: the forward kernel's pipeline (persistent grid, several CTAs per SM, a ring of shared-
-// memory stages; a loader warp, which also fills the rope table, a storer warp and consumer warps).
-// A unit is one tensor (q or k) of a block of tokens of one shard: the loader brings the forward
-// input span (one bulk copy) and the output gradient (one bulk copy per token and rank: rank r's
-// n_r heads, placed so that the gradient rows follow the input's (token, head) order) into a stage;
-// the consumers overwrite the input rows with dx; the storer writes the span back with one bulk
-// store. The loader decodes each unit once and leaves a small record of it beside the stage for the
-// other roles. Each consumer lane keeps dw partial sums for its 8 columns; they are summed over the
-// lanes of a warp when the tensor of its units changes (never for q, k alone with an even grid,
-// where units alternate; once or twice for the interleaved call, whose units come in tensor
-// phases) and at the end, and added to the warp's row of a small shared array; at the end the
-// CTA's sums (over its warps, in a fixed order) fill its slot of a partial-sum array, which a
-// second kernel adds up in a fixed order, so dw does not depend on timing.
+// Structure: a persistent grid of several CTAs per SM, each with a ring of shared-memory stages;
+// a loader warp (which also fills the rope table) and consumer warps. A unit is one tensor (q or
+// k) of a block of tokens of one shard: the loader brings the forward input span (one bulk copy)
+// and the output gradient (one bulk copy per token and rank: rank r's n_r heads, placed so that
+// the gradient rows follow the input's (token, head) order) into a stage, decodes the unit once
+// and leaves a small record of it beside the stage. The consumers compute dx row by row and store
+// it from registers straight to the sequence side (16-byte stores; a token's rows are one
+// contiguous span there, so the stores coalesce), then hand the stage back: a stage is held only
+// while it loads and while it is computed, not while a store drains it. A group of 8 lanes holds
+// a row (each lane 8 of its RoPE pairs; fused_row.cuh); three consumer warps share a unit's rows,
+// and three CTAs with three stages each share an SM (at the Wan shape this measured faster than
+// four CTAs of two stages, or four consumer warps of 16-lane rows). Each consumer lane keeps dw
+// partial sums for its 16 columns; they are summed over the lanes of a warp when the tensor of
+// its units changes (never for q, k alone with an even grid, where units alternate; once or twice
+// for the interleaved call, whose units come in tensor phases) and at the end, and added to the
+// warp's row of a small shared array; at the end the CTA's sums (over its warps, in a fixed
+// order) fill its slot of a partial-sum array, which a second kernel adds up in a fixed order, so
+// dw does not depend on timing. A v unit of the interleaved call (gradient rows only, mode 1)
+// leaves by bulk stores from its stage.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -41,19 +47,22 @@ namespace uly {
 static __device__ unsigned g_fused_bwd_status;
 
 #ifndef ULY_BWD_CTAS_PER_SM
-#define ULY_BWD_CTAS_PER_SM 4
+#define ULY_BWD_CTAS_PER_SM 3
 #endif
 #ifndef ULY_BWD_CONSUMER_WARPS
-#define ULY_BWD_CONSUMER_WARPS 4
+#define ULY_BWD_CONSUMER_WARPS 3
 #endif
 #ifndef ULY_BWD_STAGE_TARGET
 #define ULY_BWD_STAGE_TARGET 20480
 #endif
 #ifndef ULY_BWD_MAX_STAGES
-#define ULY_BWD_MAX_STAGES 2
+#define ULY_BWD_MAX_STAGES 3
 #endif
 #ifndef ULY_BWD_ILP
 #define ULY_BWD_ILP 1
+#endif
+#ifndef ULY_BWD_WIDE  // 1: 8 RoPE pairs per lane for adjacent pairs too (fused_row.cuh)
+#define ULY_BWD_WIDE 1
 #endif
 #ifndef ULY_BWD_WAIT_HINT_NS  // suspend-time hint of the barrier waits (0: plain polling)
 #define ULY_BWD_WAIT_HINT_NS 10000
@@ -61,17 +70,22 @@ static __device__ unsigned g_fused_bwd_status;
 constexpr int kBwdCtasPerSm = ULY_BWD_CTAS_PER_SM;
 constexpr int kBwdMaxStages = ULY_BWD_MAX_STAGES;
 constexpr int kBwdNW = ULY_BWD_CONSUMER_WARPS;
-constexpr int kBwdIlp = ULY_BWD_ILP;
-constexpr int kBwdHeader = 256;  // three barriers per stage, then one unit record per stage
+constexpr int kBwdIlp = ULY_BWD_ILP;  // head rows in flight per lane group
+#ifndef ULY_BWD_ILP_WIDE  // the same for the 8-pair row layout (rotate half), twice the values
+#define ULY_BWD_ILP_WIDE 1
+#endif
+constexpr int kBwdIlpWide = ULY_BWD_ILP_WIDE;
+constexpr bool kBwdWide = ULY_BWD_WIDE != 0;
+constexpr int kBwdHeader = 256;  // two barriers per stage, then one unit record per stage
 constexpr int kBwdRecordsAt = 128;
-static_assert(3 * 8 * kBwdMaxStages <= kBwdRecordsAt, "stage barriers must fit the header");
+static_assert(2 * 8 * kBwdMaxStages <= kBwdRecordsAt, "stage barriers must fit the header");
 static_assert(kBwdRecordsAt + 16 * kBwdMaxStages <= kBwdHeader, "unit records must fit");
-constexpr int kBwdLoaderWarp = 0, kBwdStorerWarp = 1, kBwdFirstConsumer = 2;
+constexpr int kBwdLoaderWarp = 0, kBwdFirstConsumer = 1;
 constexpr int kBwdThreads = 32 * (kBwdFirstConsumer + kBwdNW);
 constexpr int kBwdConsumerBarrier = 1;  // named barrier of the consumer warps (0: __syncthreads)
 
 struct BwdUnit {
-    int t;  // 0: q, 1: k, 2: v (interleaved QKV only)
+    int t;  // 0: q, 1: k, 2 ..: the packed call's other planes (gradient gathered by mode 1)
     int q;
     int64_t bb, i0;
     int ntok;
@@ -81,7 +95,7 @@ struct BwdUnit {
 // before it arrives on "full" (the loader decodes each unit once).
 struct BwdRecord {
     int64_t seq_row0;  // first row (token) of the unit in rank q's (b, s_q) sequence side
-    int32_t t_q;       // tensor (bits 0-1) and shard q (bits 2..)
+    int32_t t_q;       // tensor (bits 0-2) and shard q (bits 3..)
     int32_t ntok;
 };
 
@@ -101,8 +115,8 @@ __device__ __forceinline__ BwdUnit bwd_decode(const FusedBwdArgs& a, int64_t u)
     if (a.tensors == 2) {  // q and k units alternate
         blk_id = u >> 1;
         x.t = int(u & 1);
-    } else {  // interleaved q, k, v: every q unit, then every k unit, then every v unit (the
-              // alternating order measured 2% slower here, and 1% faster for q, k alone)
+    } else {  // packed: every q unit, then every k unit, then each other plane's units (for QKV
+              // the alternating order measured 2% slower, and 1% faster for q, k alone)
         const int64_t blocks_all = a.block_begin[kMaxW];
         x.t = int(div_fast(u, blocks_all));
         blk_id = u - int64_t(x.t) * blocks_all;
@@ -152,24 +166,28 @@ __host__ __device__ inline BwdSmem bwd_smem_layout(int d, int tokens, int stages
     return m;
 }
 
-// G: lanes per head row (d = 8 G); F16: fp16 elements (else bf16); HALF_PAIRS: rotate-half RoPE
-// pairs (else adjacent pairs). The row layouts are in fused_row.cuh.
-template <int G, bool F16, bool HALF_PAIRS>
+// D: head dimension; F16: fp16 elements (else bf16); HALF_PAIRS: rotate-half RoPE pairs (else
+// adjacent pairs). The row layouts (G lanes per row, H packed slots per lane) are in
+// fused_row.cuh.
+template <int D, bool F16, bool HALF_PAIRS>
 __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
     fused_qk_bwd_kernel(const __grid_constant__ FusedBwdArgs a)
 {
-    using IO = RowIO<F16, HALF_PAIRS, 8 * G>;
-    constexpr int D = 8 * G;
+    using IO = RowIO<F16, HALF_PAIRS, D, kBwdWide>;
+    using Words = typename IO::Words;
+    constexpr int G = IO::G;
+    constexpr int H = IO::H;
     constexpr int HALF = D / 2;
     constexpr int GPW = 32 / G;  // head rows per warp per slot
-    constexpr int PER_STEP = GPW * kBwdIlp;
+    // rows in flight per lane group: a lane of an 8-pair layout holds twice the values
+    constexpr int ILP = IO::P == 8 ? kBwdIlpWide : kBwdIlp;
+    constexpr int PER_STEP = GPW * ILP;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int K = a.stages;
     const int N = int(a.N);
     const BwdSmem L = bwd_smem_layout(D, a.tokens_per_unit, K, a.stage_bytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // data landed + table written
-    uint64_t* computed = full + kBwdMaxStages;           // consumers done with the stage
-    uint64_t* empty = computed + kBwdMaxStages;          // the store has read the stage
+    uint64_t* empty = full + kBwdMaxStages;              // consumers done with the stage
     float2* turns = reinterpret_cast<float2*>(smem + L.turns);
     float* red = reinterpret_cast<float*>(smem + L.red);
     float* wsm = reinterpret_cast<float*>(smem + L.weights);
@@ -180,8 +198,7 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
     if (threadIdx.x == 0) {
         for (int s = 0; s < K; ++s) {
             mbar_init(&full[s], 1 + 32);  // the loader's expect_tx, then its lanes' table writes
-            mbar_init(&computed[s], kBwdNW);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], kBwdNW);
         }
         fence_barrier_init();
     }
@@ -211,7 +228,7 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
                 break;
             }
             const BwdUnit t = bwd_decode(a, first + j * step);
-            const bool is_v = t.t == 2;
+            const bool is_v = t.t >= 2;
             const uint32_t span = uint32_t(t.ntok) * uint32_t(row_bytes);
             uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
             const int64_t tok0 = t.bb * a.s[t.q] + t.i0;
@@ -221,7 +238,7 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
                     bulk_g2s(dst, a.x_in[t.t][t.q] + tok0 * row_bytes, span, &full[s]);
                 BwdRecord& rec = records[s];  // published by this lane's arrive below
                 rec.seq_row0 = tok0;
-                rec.t_q = t.t | (t.q << 2);
+                rec.t_q = t.t | (t.q << 3);
                 rec.ntok = t.ntok;
             }
             __syncwarp();
@@ -241,17 +258,17 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
                          a.g_in[t.t][r] + (row0 + tok) * run, uint32_t(run), &full[s]);
             }
             // While the copies fly, the lanes fill the stage's cos/sin table for the unit's
-            // positions (free: the stage's previous unit has been stored, so its consumers are
-            // done) and arrive on "full", so a consumer that sees the phase complete sees both.
-            // Per token, lane i of a row group reads two 16-byte entries (c_j, c_j+1, s_j, s_j+1),
-            // j = 4i and 4i+2; all lanes' entries for j = 4i come first, then those for 4i+2.
+            // positions (free: the stage's previous unit has been consumed) and arrive on "full",
+            // so a consumer that sees the phase complete sees both.
+            // Per token, lane i of a row group reads P / 2 16-byte entries (c_j, c_j+1, s_j,
+            // s_j+1), j = P i + 2h; for each h the entries of all lanes are adjacent.
             float* table = reinterpret_cast<float*>(smem + L.tables + s * L.table_bytes);
             const float p0 = float(a.seq_off[t.q] + t.i0);
             for (int e = lane; e < (is_v ? 0 : t.ntok * HALF); e += 32) {
                 const int tok = e / HALF, jj = e % HALF;
                 const float2 tj = turns[jj];
                 const float2 cs = rope_cos_sin(p0 + float(tok), tj.x, tj.y);
-                const int at = ((tok * 2 + ((jj >> 1) & 1)) * G + (jj >> 2)) * 4 + (jj & 1);
+                const int at = IO::table_at(tok, jj);
                 table[at] = cs.x;
                 table[at + 2] = cs.y;
             }
@@ -269,44 +286,20 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
         return;
     }
 
-    if (warp == kBwdStorerWarp) {  // the unit's dx rows (one store, or one per token), then free
-        if (lane != 0) return;
-        StageRing ring;
-        for (int64_t j = 0; j < n; ++j, ring.next(K)) {
-            const int s = ring.s;
-            if (!bwd_wait(&computed[s], ring.phase)) {
-                atomicOr(&g_fused_bwd_status, kStatusWaitTimeout);
-                break;
-            }
-            const BwdRecord rec = records[s];
-            uint8_t* out = a.dx_out[rec.t_q & 3][rec.t_q >> 2] + rec.seq_row0 * a.tok_stride;
-            const uint8_t* st = smem + L.stages + size_t(s) * a.stage_bytes;
-            if (packed_rows) {
-                bulk_s2g(out, st, uint32_t(rec.ntok) * uint32_t(row_bytes));
-            } else {
-                for (int tok = 0; tok < rec.ntok; ++tok)
-                    bulk_s2g(out + int64_t(tok) * a.tok_stride, st + tok * row_bytes, uint32_t(row_bytes));
-            }
-            bulk_commit();
-            bulk_wait_read<0>();
-            mbar_arrive(&empty[s]);
-        }
-        bulk_wait<0>();
-        return;
-    }
-
     // consumers: all warps work on the unit's tensor, each on a contiguous share of its rows. A
-    // group of d/8 lanes holds one head row (8 values per lane, as packed fp32 pairs: the even
-    // and the odd elements of pairs (0,1) and (2,3)).
+    // group of G lanes holds one head row (a lane's RoPE pairs as packed fp32 values: the first
+    // and the second elements of its pairs), ILP rows in flight per group.
     const int cw = warp - kBwdFirstConsumer;
-    const int sub = lane % G;    // which 8 values of the row this lane holds
+    const int sub = lane % G;    // which pairs of the row this lane holds
     const int group = lane / G;  // which head row of the warp slot
     const float inv_d = 1.0f / float(D);
-    // dw partial sums of this lane's 8 columns for tensor acc_t, flushed when the tensor changes
+    // dw partial sums of this lane's columns for tensor acc_t, flushed when the tensor changes
     // (with an even grid a CTA of the q, k call only ever sees one tensor) and at the end
-    float2 aE[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    float2 aO[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float2 aE[H], aO[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) aE[h] = aO[h] = make_float2(0.f, 0.f);
     int acc_t = -1;
+    bool stored_v = false;  // this lane issued bulk stores (v units) that must finish before exit
     // this warp's share of the rows of a full token block (steps m_lo .. m_hi - 1 of PER_STEP
     // rows), and the (token, head) of its first row
     const int full_steps = (a.tokens_per_unit * N + PER_STEP - 1) / PER_STEP;
@@ -318,7 +311,7 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
 #pragma unroll
         for (int off = G; off < 32; off <<= 1) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < H; ++h) {
                 aE[h].x += __shfl_xor_sync(0xffffffffu, aE[h].x, off);
                 aE[h].y += __shfl_xor_sync(0xffffffffu, aE[h].y, off);
                 aO[h].x += __shfl_xor_sync(0xffffffffu, aO[h].x, off);
@@ -328,7 +321,7 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
         if (group == 0 && acc_t >= 0) {
             float* row = red + (cw * 2 + acc_t) * D;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < H; ++h) {
                 row[IO::col(sub, h, false, 0)] += aE[h].x;
                 row[IO::col(sub, h, true, 0)] += aO[h].x;
                 row[IO::col(sub, h, false, 1)] += aE[h].y;
@@ -336,7 +329,7 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
             }
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < H; ++h) {
             aE[h] = make_float2(0.f, 0.f);
             aO[h] = make_float2(0.f, 0.f);
         }
@@ -349,17 +342,31 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
             break;
         }
         const BwdRecord rec = records[s];
-        const int tt = rec.t_q & 3, ntok = rec.ntok;
-        if (tt == 2) {  // a v unit: its rows leave as they came (mode 1)
-            fence_proxy_async_shared();
+        const int tt = rec.t_q & 7, ntok = rec.ntok;
+        uint8_t* xs = smem + L.stages + size_t(s) * a.stage_bytes;
+        if (tt >= 2) {  // another plane's unit: its rows leave as they came (mode 1), stored
+                        // by the first consumer warp
+            if (cw == 0 && lane == 0) {
+                uint8_t* out = a.dx_out[tt][rec.t_q >> 3] + rec.seq_row0 * a.tok_stride;
+                if (packed_rows) {
+                    bulk_s2g(out, xs, uint32_t(ntok) * uint32_t(row_bytes));
+                } else {
+                    for (int tok = 0; tok < ntok; ++tok)
+                        bulk_s2g(out + int64_t(tok) * a.tok_stride, xs + tok * row_bytes,
+                                 uint32_t(row_bytes));
+                }
+                bulk_commit();
+                bulk_wait_read<0>();  // the stage may be refilled once the store has read it
+                stored_v = true;
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&computed[s]);
+            if (lane == 0) mbar_arrive(&empty[s]);
             continue;
         }
-        float2 wE[2], wO[2];  // this lane's weights of the unit's tensor (first / second elements)
+        float2 wE[H], wO[H];  // this lane's weights of the unit's tensor (first / second elements)
         IO::weights(wsm + tt * D, sub, wE, wO);
-        uint8_t* xs = smem + L.stages + size_t(s) * a.stage_bytes;
         const uint8_t* gs = xs + grad_at;
+        uint8_t* out_base = a.dx_out[tt][rec.t_q >> 3] + rec.seq_row0 * a.tok_stride;
         const float4* table = reinterpret_cast<const float4*>(smem + L.tables + s * L.table_bytes);
         if (tt != acc_t) {  // the sums so far belong to the other tensor
             flush_dw();
@@ -377,16 +384,15 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
         }
         int base = m_lo * PER_STEP;  // first row of the current step and its (token, head)
         for (int m = m_lo; m < m_hi; ++m) {
-            // The sums (mean square, <u * w, x>) need the whole row: u = R^T gy (8 fp32 values)
-            // and the raw words of x are kept across the reduction, then dx and the dw terms are
-            // formed.
-            int off[kBwdIlp];
-            bool ok[kBwdIlp];
-            uint4 xr[kBwdIlp];
-            float2 uE[kBwdIlp][2], uO[kBwdIlp][2];
-            float ss[kBwdIlp], dp[kBwdIlp];
+            // The sums (mean square, <u * w, x>) need the whole row: u = R^T gy (fp32) and the
+            // raw words of x are kept across the reduction, then dx and the dw terms are formed.
+            int tk_[ILP], hh_[ILP];
+            bool ok[ILP];
+            Words xr[ILP];
+            float2 uE[ILP][H], uO[ILP][H];
+            float ss[ILP], dp[ILP];
 #pragma unroll
-            for (int u = 0; u < kBwdIlp; ++u) {
+            for (int u = 0; u < ILP; ++u) {
                 const int o = u * GPW + group;
                 ok[u] = base + o < rows;
                 int hh = base_head + o, tk = base_tok;
@@ -394,21 +400,23 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
                     hh -= N;
                     ++tk;
                 }
-                off[u] = (base + o) * (D * 2);  // row (tk, hh) of the unit
-                uint4 g = make_uint4(0, 0, 0, 0);
-                xr[u] = make_uint4(0, 0, 0, 0);
+                tk_[u] = tk;
+                hh_[u] = hh;
+                const int off = (base + o) * (D * 2);  // row (tk, hh) of the unit in the stage
+                Words g = {};
+                xr[u] = Words{};
                 if (ok[u]) {
-                    xr[u] = IO::load(xs + off[u], sub);
-                    g = IO::load(gs + off[u], sub);
+                    xr[u] = IO::load(xs + off, sub);
+                    g = IO::load(gs + off, sub);
                 }
                 float2 acc_ss = make_float2(0.f, 0.f), acc_dp = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < H; ++h) {
                     float2 xE, xO, gE, gO;  // first / second elements of the lane's pairs
                     IO::unpack(xr[u], h, xE, xO);
                     IO::unpack(g, h, gE, gO);
-                    // (c_j, c_j+1, s_j, s_j+1) for j = 4 sub + 2 h
-                    const float4 cs = table[(tk * 2 + h) * G + sub];
+                    // (c_j, c_j+1, s_j, s_j+1) for j = P sub + 2 h
+                    const float4 cs = table[IO::table_entry(tk, h, sub)];
                     const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
                     const float2 ns2 = make_float2(-cs.z, -cs.w);
                     // u = R^T gy: (c g_e + s g_o, c g_o - s g_e)
@@ -425,20 +433,20 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
 #pragma unroll
             for (int sh = G / 2; sh > 0; sh >>= 1) {
 #pragma unroll
-                for (int u = 0; u < kBwdIlp; ++u) {
+                for (int u = 0; u < ILP; ++u) {
                     ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], sh);
                     dp[u] += __shfl_xor_sync(0xffffffffu, dp[u], sh);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < kBwdIlp; ++u) {
+            for (int u = 0; u < ILP; ++u) {
                 if (!ok[u]) continue;
                 const float rr = rsqrtf(ss[u] * inv_d + a.eps);
                 const float kk = rr * rr * rr * dp[u] * inv_d;
                 const float2 r2 = make_float2(rr, rr), nk2 = make_float2(-kk, -kk);
-                float2 dxE[2], dxO[2];
+                float2 dxE[H], dxO[H];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < H; ++h) {
                     float2 xE, xO;
                     IO::unpack(xr[u], h, xE, xO);
                     dxE[h] = __ffma2_rn(__fmul2_rn(uE[u][h], wE[h]), r2, __fmul2_rn(xE, nk2));
@@ -446,7 +454,9 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
                     aE[h] = __ffma2_rn(uE[u][h], __fmul2_rn(xE, r2), aE[h]);
                     aO[h] = __ffma2_rn(uO[u][h], __fmul2_rn(xO, r2), aO[h]);
                 }
-                IO::store(xs + off[u], sub, IO::pack(dxE, dxO));  // in place
+                // straight to the sequence side: row (token, head) of this unit's dx
+                IO::store_global(out_base + int64_t(tk_[u]) * a.tok_stride + hh_[u] * (D * 2), sub,
+                                 IO::pack(dxE, dxO));
             }
             base += PER_STEP;
             base_head += PER_STEP;
@@ -455,12 +465,12 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
                 ++base_tok;
             }
         }
-        // make this warp's dx rows visible to the bulk-copy unit, then report the stage done
-        fence_proxy_async_shared();
+        // this warp has read all it needs of the stage: hand it back
         __syncwarp();
-        if (lane == 0) mbar_arrive(&computed[s]);
+        if (lane == 0) mbar_arrive(&empty[s]);
     }
     flush_dw();
+    if (stored_v) bulk_wait<0>();
     // the CTA's dw sums, over its consumer warps in a fixed order, into its slot
     asm volatile("bar.sync %0, %1;" ::"r"(kBwdConsumerBarrier), "r"(kBwdNW * 32) : "memory");
     const int ct = threadIdx.x - kBwdFirstConsumer * 32;
@@ -530,32 +540,32 @@ void fused_bwd_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages,
 // per device: the kernel variants whose shared-memory limit has been raised (any host thread)
 static std::atomic<unsigned> g_bwd_smem_set[64];
 
-template <int G, bool F16, bool HALF>
-static cudaError_t bwd_launch_g(const FusedBwdArgs& a, cudaStream_t stream, int device, int grid)
+template <int D, bool F16, bool HALF>
+static cudaError_t bwd_launch_d(const FusedBwdArgs& a, cudaStream_t stream, int device, int grid)
 {
-    constexpr int gbit = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : G == 8 ? 3 : G == 16 ? 4 : 5;
-    constexpr unsigned bit = 1u << (gbit * 4 + (F16 ? 2 : 0) + (HALF ? 1 : 0));
+    constexpr int dbit = D == 8 ? 0 : D == 16 ? 1 : D == 32 ? 2 : D == 64 ? 3 : D == 128 ? 4 : 5;
+    constexpr unsigned bit = 1u << (dbit * 4 + (F16 ? 2 : 0) + (HALF ? 1 : 0));
     if (device >= 0 && device < 64 && !(g_bwd_smem_set[device].load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(fused_qk_bwd_kernel<G, F16, HALF>,
+        cudaError_t e = cudaFuncSetAttribute(fused_qk_bwd_kernel<D, F16, HALF>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemPerCtaMax);
         if (e != cudaSuccess) return e;
         g_bwd_smem_set[device].fetch_or(bit);
     }
     const BwdSmem m = bwd_smem_layout(a.d, a.tokens_per_unit, a.stages, a.stage_bytes);
-    fused_qk_bwd_kernel<G, F16, HALF><<<grid, kBwdThreads, m.total, stream>>>(a);
+    fused_qk_bwd_kernel<D, F16, HALF><<<grid, kBwdThreads, m.total, stream>>>(a);
     return cudaGetLastError();
 }
 
-template <int G>
+template <int D>
 static cudaError_t bwd_launch_variant(const FusedBwdArgs& a, cudaStream_t stream, int device,
                                       int grid)
 {
     if (a.elem_f16)
-        return a.rope_half ? bwd_launch_g<G, true, true>(a, stream, device, grid)
-                           : bwd_launch_g<G, true, false>(a, stream, device, grid);
-    return a.rope_half ? bwd_launch_g<G, false, true>(a, stream, device, grid)
-                       : bwd_launch_g<G, false, false>(a, stream, device, grid);
+        return a.rope_half ? bwd_launch_d<D, true, true>(a, stream, device, grid)
+                           : bwd_launch_d<D, true, false>(a, stream, device, grid);
+    return a.rope_half ? bwd_launch_d<D, false, true>(a, stream, device, grid)
+                       : bwd_launch_d<D, false, false>(a, stream, device, grid);
 }
 
 // CTAs of the main kernel for a launch of `a` (the number of partial-sum slots it fills); at
@@ -575,13 +585,13 @@ cudaError_t fused_bwd_launch(const FusedBwdArgs& a, float* dw, bool accumulate, 
     const int64_t grid = fused_bwd_grid(a, sm_count, max_grid);
     if (grid > 0) {
         cudaError_t e;
-        switch (a.d / 8) {
-            case 1: e = bwd_launch_variant<1>(a, stream, device, int(grid)); break;
-            case 2: e = bwd_launch_variant<2>(a, stream, device, int(grid)); break;
-            case 4: e = bwd_launch_variant<4>(a, stream, device, int(grid)); break;
+        switch (a.d) {
             case 8: e = bwd_launch_variant<8>(a, stream, device, int(grid)); break;
             case 16: e = bwd_launch_variant<16>(a, stream, device, int(grid)); break;
             case 32: e = bwd_launch_variant<32>(a, stream, device, int(grid)); break;
+            case 64: e = bwd_launch_variant<64>(a, stream, device, int(grid)); break;
+            case 128: e = bwd_launch_variant<128>(a, stream, device, int(grid)); break;
+            case 256: e = bwd_launch_variant<256>(a, stream, device, int(grid)); break;
             default: return cudaErrorInvalidValue;
         }
         if (e != cudaSuccess) return e;

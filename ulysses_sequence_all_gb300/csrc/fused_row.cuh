@@ -2,15 +2,21 @@
 // (bf16 or fp16) and the RoPE pair layout (adjacent pairs (2j, 2j+1), or rotate-half pairs
 // (j, j + d/2)), both with the angle p * theta^(-2j/d) for pair j.
 //
-// A group of d/8 lanes holds a row. In both layouts lane `sub` works on pairs j = 4 sub ..
-// 4 sub + 3, as packed float2 values: fst[h] holds the first elements of pairs 4 sub + 2h and
-// 4 sub + 2h + 1, snd[h] their second elements (h = 0, 1), so the rotation, the weights and the
-// cos/sin table are the same code for both layouts:
-//  * adjacent: the lane's pairs are elements 8 sub .. 8 sub + 7, one 16-byte word;
-//  * rotate half: first elements 4 sub .. 4 sub + 3 (8 bytes at byte 8 sub) and second elements
-//    d/2 + 4 sub .. d/2 + 4 sub + 3 (8 bytes at byte d + 8 sub).
-// A row's raw form is four 32-bit words (two elements each): the 16-byte word (adjacent), or the
-// first-half then the second-half 8 bytes (rotate half).
+// A lane holds P of the row's RoPE pairs and a group of G = d / (2P) lanes holds a row. The pairs
+// sit in registers as packed float2 values: fst[h] holds the first elements of two of the lane's
+// pairs, snd[h] their second elements (h < P / 2), so the rotation, the weights and the cos/sin
+// table are the same code for every layout. The layouts (WIDE selects P = 8 where d >= 16):
+//  * adjacent, P = 4: the lane's pairs are j = 4 sub .. 4 sub + 3, elements 8 sub .. 8 sub + 7,
+//    one 16-byte word;
+//  * adjacent, P = 8: two such words, one in each half of the row: pairs 4 sub .. 4 sub + 3 and
+//    d/4 + 4 sub .. d/4 + 4 sub + 3 (16 bytes at byte 16 sub and at byte d + 16 sub);
+//  * rotate half, P = 8 (always used for d >= 16): pairs j = 8 sub .. 8 sub + 7, first elements
+//    8 sub .. 8 sub + 7 (16 bytes at byte 16 sub) and second elements d/2 + 8 sub .. d/2 +
+//    8 sub + 7 (16 bytes at byte d + 16 sub);
+//  * rotate half, d = 8 (P = 4): 8 bytes of each half.
+// Every layout moves a lane's bytes with 16-byte shared-memory accesses (d = 8 aside), 8 lanes of
+// a quarter warp covering 128 contiguous bytes, so the accesses are free of bank conflicts. A
+// row's raw form is P 32-bit words (two elements each), in the order the lane loads them.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -78,83 +84,144 @@ struct ElemT<true> {  // IEEE binary16
     }
 };
 
-template <bool F16, bool HALF, int D>
+template <bool F16, bool HALF, int D, bool WIDE = false>
 struct RowIO {
     using E = ElemT<F16>;
+    static constexpr int P = ((HALF || WIDE) && D >= 16) ? 8 : 4;  // pairs per lane
+    static constexpr int H = P / 2;                               // float2 slots per lane and kind
+    static constexpr int G = D / (2 * P);                         // lanes per row
+    static_assert(G >= 1 && 32 % G == 0, "a row's lanes must divide a warp");
+    struct Words {
+        uint32_t w[P];
+    };
 
-    // The lane's four raw words of the row starting at `row` (shared memory).
-    static __device__ __forceinline__ uint4 load(const uint8_t* row, int sub)
+    // The lane's raw words of the row starting at `row` (shared memory).
+    static __device__ __forceinline__ Words load(const uint8_t* row, int sub)
     {
-        if constexpr (!HALF) {
-            return ld_shared_v4(row + sub * 16);
-        } else {
+        Words r;
+        if constexpr (!HALF && P == 4) {
+            const uint4 a = ld_shared_v4(row + sub * 16);
+            r.w[0] = a.x, r.w[1] = a.y, r.w[2] = a.z, r.w[3] = a.w;
+        } else if constexpr (P == 4) {
             const uint2 a = ld_shared_v2(row + sub * 8);
             const uint2 b = ld_shared_v2(row + D + sub * 8);
-            return make_uint4(a.x, a.y, b.x, b.y);
-        }
-    }
-
-    static __device__ __forceinline__ void store(uint8_t* row, int sub, const uint4& w)
-    {
-        if constexpr (!HALF) {
-            st_shared_v4(row + sub * 16, w);
+            r.w[0] = a.x, r.w[1] = a.y, r.w[2] = b.x, r.w[3] = b.y;
         } else {
-            st_shared_v2(row + sub * 8, w.x, w.y);
-            st_shared_v2(row + D + sub * 8, w.z, w.w);
+            const uint4 a = ld_shared_v4(row + sub * 16);
+            const uint4 b = ld_shared_v4(row + D + sub * 16);
+            r.w[0] = a.x, r.w[1] = a.y, r.w[2] = a.z, r.w[3] = a.w;
+            r.w[4] = b.x, r.w[5] = b.y, r.w[6] = b.z, r.w[7] = b.w;
+        }
+        return r;
+    }
+
+    static __device__ __forceinline__ void store(uint8_t* row, int sub, const Words& r)
+    {
+        if constexpr (!HALF && P == 4) {
+            st_shared_v4(row + sub * 16, make_uint4(r.w[0], r.w[1], r.w[2], r.w[3]));
+        } else if constexpr (P == 4) {
+            st_shared_v2(row + sub * 8, r.w[0], r.w[1]);
+            st_shared_v2(row + D + sub * 8, r.w[2], r.w[3]);
+        } else {
+            st_shared_v4(row + sub * 16, make_uint4(r.w[0], r.w[1], r.w[2], r.w[3]));
+            st_shared_v4(row + D + sub * 16, make_uint4(r.w[4], r.w[5], r.w[6], r.w[7]));
         }
     }
 
-    // raw words -> first / second elements of the lane's pairs, h = 0, 1
-    static __device__ __forceinline__ void unpack(const uint4& w, int h, float2& fst, float2& snd)
+    // The lane's raw words to the row starting at `row` in global memory.
+    static __device__ __forceinline__ void store_global(uint8_t* row, int sub, const Words& r)
     {
-        const uint32_t w0 = h ? w.z : w.x, w1 = h ? w.w : w.y;
+        if constexpr (!HALF && P == 4) {
+            st_v4(row + sub * 16, make_uint4(r.w[0], r.w[1], r.w[2], r.w[3]));
+        } else if constexpr (P == 4) {
+            st_v2(row + sub * 8, r.w[0], r.w[1]);
+            st_v2(row + D + sub * 8, r.w[2], r.w[3]);
+        } else {
+            st_v4(row + sub * 16, make_uint4(r.w[0], r.w[1], r.w[2], r.w[3]));
+            st_v4(row + D + sub * 16, make_uint4(r.w[4], r.w[5], r.w[6], r.w[7]));
+        }
+    }
+
+    // raw words -> first / second elements of the lane's pairs P sub + 2h, P sub + 2h + 1
+    static __device__ __forceinline__ void unpack(const Words& r, int h, float2& fst, float2& snd)
+    {
         if constexpr (!HALF) {
+            const uint32_t w0 = r.w[2 * h], w1 = r.w[2 * h + 1];
             fst = make_float2(E::lo(w0), E::lo(w1));
             snd = make_float2(E::hi(w0), E::hi(w1));
         } else {
-            const uint32_t f = h ? w.y : w.x, s = h ? w.w : w.z;
+            const uint32_t f = r.w[h], s = r.w[H + h];
             fst = make_float2(E::lo(f), E::hi(f));
             snd = make_float2(E::lo(s), E::hi(s));
         }
     }
 
     // first / second elements (rounded once to the element type) -> raw words
-    static __device__ __forceinline__ uint4 pack(const float2 fst[2], const float2 snd[2])
+    static __device__ __forceinline__ Words pack(const float2 fst[H], const float2 snd[H])
     {
-        if constexpr (!HALF) {
-            return make_uint4(E::pack(fst[0].x, snd[0].x), E::pack(fst[0].y, snd[0].y),
-                              E::pack(fst[1].x, snd[1].x), E::pack(fst[1].y, snd[1].y));
-        } else {
-            return make_uint4(E::pack(fst[0].x, fst[0].y), E::pack(fst[1].x, fst[1].y),
-                              E::pack(snd[0].x, snd[0].y), E::pack(snd[1].x, snd[1].y));
+        Words r;
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            if constexpr (!HALF) {
+                r.w[2 * h] = E::pack(fst[h].x, snd[h].x);
+                r.w[2 * h + 1] = E::pack(fst[h].y, snd[h].y);
+            } else {
+                r.w[h] = E::pack(fst[h].x, fst[h].y);
+                r.w[H + h] = E::pack(snd[h].x, snd[h].y);
+            }
         }
+        return r;
     }
 
     // Column (element index in the row) of fst[h] (second = false) or snd[h], component k.
     static __device__ __forceinline__ constexpr int col(int sub, int h, bool second, int k)
     {
-        return HALF ? (second ? D / 2 : 0) + 4 * sub + 2 * h + k
-                    : 8 * sub + 4 * h + 2 * k + (second ? 1 : 0);
+        return HALF ? (second ? D / 2 : 0) + P * sub + 2 * h + k
+                    : (h >= 2 ? D / 2 : 0) + 8 * sub + 4 * (h & 1) + 2 * k + (second ? 1 : 0);
+    }
+
+    // Index of the float4 table entry (c_j, c_j+1, s_j, s_j+1), j = P sub + 2h, of token tok.
+    static __device__ __forceinline__ constexpr int table_entry(int tok, int h, int sub)
+    {
+        return (tok * H + h) * G + sub;
+    }
+
+    // Float offset of pair jj's cosine in a token table (its sine is 2 floats further): the
+    // entry of the lane that holds the pair, component jj & 1.
+    static __device__ __forceinline__ constexpr int table_at(int tok, int jj)
+    {
+        if constexpr (HALF || P == 4) {  // the lane's pairs are P consecutive ones
+            return table_entry(tok, (jj % P) >> 1, jj / P) * 4 + (jj & 1);
+        } else {  // chunk c = jj / (d/4) of the row; 4 pairs per lane in each chunk
+            const int c = jj / (D / 4), jr = jj % (D / 4);
+            return table_entry(tok, 2 * c + ((jr & 3) >> 1), jr >> 2) * 4 + (jj & 1);
+        }
     }
 
     // The lane's weights in the same arrangement (w: d fp32 values, 16-byte aligned).
-    static __device__ __forceinline__ void weights(const float* w, int sub, float2 fst[2],
-                                                   float2 snd[2])
+    static __device__ __forceinline__ void weights(const float* w, int sub, float2 fst[H],
+                                                   float2 snd[H])
     {
         if constexpr (!HALF) {
-            const float4 a0 = *reinterpret_cast<const float4*>(w + 8 * sub);
-            const float4 a1 = *reinterpret_cast<const float4*>(w + 8 * sub + 4);
-            fst[0] = make_float2(a0.x, a0.z);
-            snd[0] = make_float2(a0.y, a0.w);
-            fst[1] = make_float2(a1.x, a1.z);
-            snd[1] = make_float2(a1.y, a1.w);
+#pragma unroll
+            for (int c = 0; c < P / 4; ++c) {  // the lane's chunk in each half of the row
+                const float4 a0 = *reinterpret_cast<const float4*>(w + c * (D / 2) + 8 * sub);
+                const float4 a1 = *reinterpret_cast<const float4*>(w + c * (D / 2) + 8 * sub + 4);
+                fst[2 * c] = make_float2(a0.x, a0.z);
+                snd[2 * c] = make_float2(a0.y, a0.w);
+                fst[2 * c + 1] = make_float2(a1.x, a1.z);
+                snd[2 * c + 1] = make_float2(a1.y, a1.w);
+            }
         } else {
-            const float4 f = *reinterpret_cast<const float4*>(w + 4 * sub);
-            const float4 s = *reinterpret_cast<const float4*>(w + D / 2 + 4 * sub);
-            fst[0] = make_float2(f.x, f.y);
-            fst[1] = make_float2(f.z, f.w);
-            snd[0] = make_float2(s.x, s.y);
-            snd[1] = make_float2(s.z, s.w);
+#pragma unroll
+            for (int q = 0; q < P / 4; ++q) {
+                const float4 f = *reinterpret_cast<const float4*>(w + P * sub + 4 * q);
+                const float4 s = *reinterpret_cast<const float4*>(w + D / 2 + P * sub + 4 * q);
+                fst[2 * q] = make_float2(f.x, f.y);
+                fst[2 * q + 1] = make_float2(f.z, f.w);
+                snd[2 * q] = make_float2(s.x, s.y);
+                snd[2 * q + 1] = make_float2(s.z, s.w);
+            }
         }
     }
 };

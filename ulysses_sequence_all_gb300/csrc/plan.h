@@ -95,20 +95,27 @@ void build_row_tiles(const Plan& p, const ChunkRows& rows, int64_t tile_rows, Ro
 // batch index, and each block into `units_per_block` work units:
 //  * separate q and k inputs: one unit per block (block_tokens = tokens_per_unit), all N heads of
 //    q and of k for those tokens;
-//  * `interleaved` (qkv_in[q], one (b, s_q, 3, N, d) tensor per rank, planes q, k, v): three units
-//    per block of 2 * tokens_per_unit tokens: the q and k rows of its first tokens_per_unit tokens,
-//    those of the next tokens_per_unit, and the v rows of all of them, which v_out receives
-//    unchanged. Each unit fills the same stage size. Units 0 .. 2B-1 (B blocks) are the q,k units
-//    (two per block, in block order), units 2B .. 3B-1 the v units.
+//  * `interleaved` (packed_in[q]: rank q's b * s_q tokens, tok_pitch bytes apart, each holding
+//    `planes` planes of N * d elements, plane c at byte c * N * d * e of the token): blocks of
+//    2 * tokens_per_unit tokens with `planes` units each: the q and k rows (planes q_plane and
+//    k_plane) of its first tokens_per_unit tokens, those of the next tokens_per_unit, and one unit
+//    per other plane (plain_plane[0 .. planes - 3], in order) with that plane's rows of all the
+//    block's tokens, which plane_out receives unchanged. Each unit fills the same stage size.
+//    Units 0 .. 2B-1 (B blocks) are the q,k units (two per block, in block order), then B units of
+//    each plain plane in turn.
 // unit_begin counts blocks; total_units counts units.
+constexpr int kMaxPlanes = 8;
 struct FusedArgs {
     const uint8_t* q_in[kMaxW];
     const uint8_t* k_in[kMaxW];
-    const uint8_t* qkv_in[kMaxW];
+    const uint8_t* packed_in[kMaxW];
     uint8_t* q_out[kMaxW];
     uint8_t* k_out[kMaxW];
-    uint8_t* v_out[kMaxW];
+    uint8_t* plane_out[kMaxPlanes][kMaxW];  // the plain planes' outputs (packed calls)
     int32_t interleaved;
+    int32_t planes, q_plane, k_plane;   // packed calls
+    int32_t plain_plane[kMaxPlanes];    // the planes other than q and k, in order
+    int64_t tok_pitch;                  // packed calls: bytes between consecutive tokens
     int32_t elem_f16;   // elements are fp16 (else bf16)
     int32_t rope_half;  // RoPE pairs (j, j + d/2) (else (2j, 2j + 1))
     const float* rms_w;  // [2][d]
@@ -127,25 +134,27 @@ struct FusedArgs {
     float turn_hi[kMaxFusedD / 2];
     float turn_lo[kMaxFusedD / 2];
 };
+static_assert(sizeof(FusedArgs) <= 4096, "kernel parameter block");
 
 void build_fused_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_unit,
                        int64_t block_tokens, int units_per_block, FusedArgs* a);
 
 // ---- fused QK backward's argument block -------------------------------------------------------
 // A token block is tokens_per_unit consecutive rows (tokens) of one shard q and one batch index;
-// it makes one work unit per tensor (for q, k: unit u is tensor u mod 2 of block u div 2; for the
-// interleaved q, k, v: unit u is tensor u div B of block u mod B, B blocks). A unit reads the tensor's
+// it makes one work unit per tensor (for q, k: unit u is tensor u mod 2 of block u div 2; for a
+// packed call with C planes: unit u is tensor u div B of block u mod B, B blocks, tensors 0 and 1
+// being the q and k planes and tensors 2 .. C-1 the other planes). A unit reads the tensor's
 // forward input for those tokens (all N heads: one contiguous span on the sequence side) and the
 // gradient of its output (W runs, rank r's n_r heads of those tokens, contiguous on rank r's head
 // side), and writes the gradient of the input (one span on the sequence side).
-// For the interleaved QKV call (tensors = 3) the forward input and the gradient are
-// (b, s_q, 3, N, d): x_in / dx_out point at a rank's plane (q, k, v) and consecutive tokens are
-// tok_stride = 3 N d e bytes apart; units of tensor 2 (v) only gather g_in[2] (mode 1).
+// For a packed call the forward input and the gradient are rank q's packed tokens: x_in / dx_out
+// point at a rank's plane and consecutive tokens are tok_stride bytes (the token pitch) apart;
+// units of tensors 2 and up only gather their gradient (mode 1).
 struct FusedBwdArgs {
-    const uint8_t* x_in[2][kMaxW];  // forward inputs q, k: rank q's (b, s_q, N, d) bf16
-    const uint8_t* g_in[3][kMaxW];  // gradients of the forward outputs: rank r's (b, S, n_r, d)
-    uint8_t* dx_out[3][kMaxW];      // gradients of the forward inputs: rank q's (b, s_q, N, d)
-    int32_t tensors;                // 2 (q, k) or 3 (interleaved q, k, v)
+    const uint8_t* x_in[2][kMaxW];           // forward inputs q, k: rank q's (b, s_q, N, d)
+    const uint8_t* g_in[kMaxPlanes][kMaxW];  // gradients of the forward outputs: (b, S, n_r, d)
+    uint8_t* dx_out[kMaxPlanes][kMaxW];      // gradients of the forward inputs: (b, s_q, N, d)
+    int32_t tensors;                // 2 (q, k) or the packed call's planes
     int32_t tok_stride;             // bytes between consecutive tokens of x_in / dx_out
     const float* rms_w;             // [2][d]
     float* dw_part;                 // [grid][2][d]: one slot per CTA, fully written by it
@@ -164,6 +173,7 @@ struct FusedBwdArgs {
     float turn_hi[kMaxFusedD / 2];
     float turn_lo[kMaxFusedD / 2];
 };
+static_assert(sizeof(FusedBwdArgs) <= 4096, "kernel parameter block");
 
 void build_fused_bwd_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_unit,
                            FusedBwdArgs* a);

@@ -187,6 +187,11 @@ __device__ __forceinline__ void st_v4(void* p, const uint4& v)
                  : "memory");
 }
 
+__device__ __forceinline__ void st_v2(void* p, uint32_t a, uint32_t b)
+{
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(void* p, const uint4& v)
 {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(v.x), "r"(v.y),
