@@ -142,6 +142,35 @@ int ulysses_plan_chunk_rows(ulysses_plan_t plan, int mode, int64_t chunk, int64_
                             int64_t* row_count);
 
 /*
+ * One rank's share of the exchange, for a transport that runs the ranks on separate GPUs
+ * (fast-ulysses 0.1.0, opening paragraph: pitched peer copies into the other ranks' windows).
+ * This library runs all W ranks on one GPU and issues no such copies; the description lets a
+ * multi-GPU caller (or a test) move each rank's bytes itself with the same plan.
+ * A segment is a strided block: for every batch index bb < b and row i < rows, the row_bytes at
+ *   src_offset + bb * src_batch_pitch + i * src_row_pitch   of the sending rank's tensor go to
+ *   dst_offset + bb * dst_batch_pitch + i * dst_row_pitch   of rank `peer`'s tensor.
+ * Tensors are those of ulysses_a2a_4d in `mode`: in mode 0 a rank sends from its (b, s_q, N, d)
+ * input to every rank's (b, S, n_r, d) output; in mode 1 from its (b, S, n_r, d) input to every
+ * rank's (b, s_q, N, d) output.
+ */
+typedef struct {
+    int64_t peer;             /* the receiving rank */
+    int64_t rows;             /* rows per batch index (0: nothing to send) */
+    int64_t row_bytes;        /* bytes of one row */
+    int64_t src_offset;       /* byte offset of row 0, batch index 0, in the sender's tensor */
+    int64_t src_row_pitch;    /* bytes between consecutive rows there */
+    int64_t src_batch_pitch;  /* bytes between consecutive batch indices there */
+    int64_t dst_offset;       /* the same three in the receiver's tensor */
+    int64_t dst_row_pitch;
+    int64_t dst_batch_pitch;
+} ulysses_segment_t;
+
+/* Fill segs[0 .. W-1] with the segments rank `rank` sends in `mode` (segs[r] goes to rank r,
+ * itself included). Host only: makes no CUDA call. Together the W ranks' segments move every
+ * byte of the relayout once. */
+int ulysses_plan_rank_segments(ulysses_plan_t plan, int mode, int rank, ulysses_segment_t* segs);
+
+/*
  * The relayout (fast-ulysses 0.2.1, README, "API": all_to_all_4d(x, mode, seq_splits,
  * head_splits)), for all W ranks in one call.
  *   mode     0 or 1 (see the top of this file).

@@ -28,6 +28,7 @@ DTYPE_CODES = {"uint8": ULY_U8, "float8_e4m3fn": ULY_F8E4M3, "float8_e5m2": ULY_
 EXPORTS = ["ulysses_plan", "ulysses_plan_destroy", "ulysses_plan_set_chunk_bytes",
            "ulysses_plan_set_max_ctas", "ulysses_plan_set_rope_pairs",
            "ulysses_plan_bytes", "ulysses_plan_num_chunks", "ulysses_plan_chunk_rows",
+           "ulysses_plan_rank_segments",
            "ulysses_a2a_4d", "ulysses_a2a_4d_engine", "ulysses_a2a_4d_qk_fused",
            "ulysses_a2a_4d_qkv_fused", "ulysses_a2a_4d_packed_fused",
            "ulysses_a2a_4d_qk_fused_backward",
@@ -71,6 +72,7 @@ def _lib():
         lib.ulysses_plan_num_chunks.argtypes = [_p, ctypes.c_int, ctypes.POINTER(_i64)]
         lib.ulysses_plan_chunk_rows.argtypes = [_p, ctypes.c_int, _i64, ctypes.POINTER(_i64),
                                                 ctypes.POINTER(_i64)]
+        lib.ulysses_plan_rank_segments.argtypes = [_p, ctypes.c_int, ctypes.c_int, _p]
         lib.ulysses_a2a_4d.argtypes = [_p, ctypes.c_int, _pp, _pp, _p]
         lib.ulysses_a2a_4d_engine.argtypes = [_p, ctypes.c_int, ctypes.c_int, _pp, _pp, _p]
         lib.ulysses_a2a_4d_qk_fused.argtypes = [_p, _pp, _pp, _pp, _pp, _p, ctypes.c_float,
@@ -205,6 +207,19 @@ def ulysses_plan_chunk_rows(plan: Plan, mode: int, chunk: int):
     lo, cnt = (_i64 * plan.W)(), (_i64 * plan.W)()
     _check(_lib().ulysses_plan_chunk_rows(plan, mode, chunk, lo, cnt), "ulysses_plan_chunk_rows")
     return list(lo), list(cnt)
+
+
+SEGMENT_FIELDS = ("peer", "rows", "row_bytes", "src_offset", "src_row_pitch", "src_batch_pitch",
+                  "dst_offset", "dst_row_pitch", "dst_batch_pitch")
+
+
+def ulysses_plan_rank_segments(plan: Plan, mode: int, rank: int) -> list:
+    """The W segments rank `rank` sends in `mode`, as dicts of the ulysses_segment_t fields."""
+    W = len(plan.seq_splits)
+    buf = (ctypes.c_int64 * (W * len(SEGMENT_FIELDS)))()
+    _check(_lib().ulysses_plan_rank_segments(plan, mode, rank, buf), "ulysses_plan_rank_segments")
+    n = len(SEGMENT_FIELDS)
+    return [dict(zip(SEGMENT_FIELDS, buf[k * n:(k + 1) * n])) for k in range(W)]
 
 
 def ulysses_a2a_4d(plan: Plan, mode: int, ins: Sequence, outs: Sequence, stream=None):

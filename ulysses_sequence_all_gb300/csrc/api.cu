@@ -819,6 +819,38 @@ int ulysses_plan_chunk_rows(ulysses_plan_t plan, int mode, int64_t chunk, int64_
     return ULY_OK;
 }
 
+int ulysses_plan_rank_segments(ulysses_plan_t plan, int mode, int rank, ulysses_segment_t* segs)
+{
+    if (!plan || !segs || (mode != 0 && mode != 1)) return ULY_EINVAL;
+    const Plan& p = plan->p;
+    if (rank < 0 || rank >= p.W) return ULY_EINVAL;
+    const int64_t de = p.d * p.e;
+    for (int peer = 0; peer < p.W; ++peer) {
+        // mode 0: rank q = `rank` sends head group r = peer of its sequence shard;
+        // mode 1: rank r = `rank` sends sequence shard q = peer of its head group
+        const int q = mode == 0 ? rank : peer;
+        const int r = mode == 0 ? peer : rank;
+        const int64_t seq_row = p.N * de;     // a row of rank q's (b, s_q, N, d)
+        const int64_t head_row = p.n[r] * de; // a row of rank r's (b, S, n_r, d)
+        const int64_t seq_at = p.head_off[r] * de, head_at = p.seq_off[q] * head_row;
+        ulysses_segment_t& g = segs[peer];
+        g.peer = peer;
+        g.rows = p.s[q];
+        g.row_bytes = p.n[r] * de;
+        const int64_t sp[3] = {seq_at, seq_row, p.s[q] * seq_row};
+        const int64_t hp[3] = {head_at, head_row, p.S * head_row};
+        const int64_t* src = mode == 0 ? sp : hp;
+        const int64_t* dst = mode == 0 ? hp : sp;
+        g.src_offset = src[0];
+        g.src_row_pitch = src[1];
+        g.src_batch_pitch = src[2];
+        g.dst_offset = dst[0];
+        g.dst_row_pitch = dst[1];
+        g.dst_batch_pitch = dst[2];
+    }
+    return ULY_OK;
+}
+
 int ulysses_a2a_4d(ulysses_plan_t plan, int mode, const void* const* in_ptrs, void* const* out_ptrs,
                    void* stream)
 {
