@@ -31,7 +31,7 @@ def _worker(rank, world, port, results):
 
 def test_replica_aggregation_world_2():
     port = _free_port()
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()
     results = manager.dict()
     mp.spawn(_worker, args=(2, port, results), nprocs=2, join=True)
     for rank in range(2):

@@ -113,7 +113,7 @@ def _worker(rank, world, port, g, mode, results):
 def test_segments_exchanged_between_processes(g, mode):
     world = g[0]
     port = _free_port()
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()
     results = manager.dict()
     mp.spawn(_worker, args=(world, port, g, mode, results), nprocs=world, join=True)
     assert all(results[r] for r in range(world)), dict(results)
