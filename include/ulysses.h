@@ -303,8 +303,9 @@ int ulysses_a2a_4d_qkv_fused(ulysses_plan_t plan, const void* const* qkv_in, voi
  * case planes = 3, q_plane = 0, k_plane = 1, token_pitch = 3 * N * d * elem_size.
  *   planes          2 .. 8.
  *   q_plane, k_plane   distinct, in [0, planes).
- *   token_pitch     bytes between consecutive tokens, >= planes * N * d * elem_size and a multiple
- *                   of 16 (ULY_EALIGN otherwise); bytes of a token beyond its planes are not read.
+ *   token_pitch     bytes between consecutive tokens, >= planes * N * d * elem_size, below 2^31
+ *                   and a multiple of 16 (ULY_EALIGN otherwise); bytes of a token beyond its planes
+ *                   are not read.
  *   packed_in       W device pointers, rank q's b * s_q * token_pitch bytes (plan's dtype).
  *   outs            planes * W device pointers, plane-major: outs[c * W + r] is rank r's
  *                   (b, S, n_r, d) output of plane c.

@@ -219,6 +219,7 @@ def test_packed_argument_errors_before_cuda():
         ((3, -1, 1, 3 * row), B.ULY_EINVAL),     # q plane out of range
         ((3, 0, 1, 3 * row - 16), B.ULY_EINVAL), # pitch shorter than the planes
         ((3, 0, 1, 3 * row + 8), B.ULY_EALIGN),  # pitch not a multiple of 16 bytes
+        ((3, 0, 1, 1 << 31), B.ULY_EINVAL),      # pitch of 2 GiB or more
     ]:
         with pytest.raises(B.UlyssesError) as ei:
             call(*args)

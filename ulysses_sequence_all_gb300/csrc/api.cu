@@ -256,10 +256,13 @@ int fused_prepare(const Plan& p, const void* const* q_in, const void* const* k_i
         if (!pk->in || !pk->outs || pk->planes < 2 || pk->planes > kMaxPlanes ||
             pk->q_plane < 0 || pk->q_plane >= pk->planes || pk->k_plane < 0 ||
             pk->k_plane >= pk->planes || pk->q_plane == pk->k_plane ||
-            pk->pitch < pk->planes * row_bytes)
+            pk->pitch < pk->planes * row_bytes || pk->pitch >= (int64_t(1) << 31))
             return ULY_EINVAL;
         if (pk->pitch % 16 != 0) return ULY_EALIGN;
-        for (int k = 0; k < W; ++k) packed_b[k] = p.b * p.s[k] * pk->pitch;
+        for (int k = 0; k < W; ++k) {
+            if (p.b * p.s[k] > INT64_MAX / pk->pitch) return ULY_EINVAL;  // bytes overflow
+            packed_b[k] = p.b * p.s[k] * pk->pitch;
+        }
         q_out = pk->outs + size_t(pk->q_plane) * W;
         k_out = pk->outs + size_t(pk->k_plane) * W;
     }
@@ -526,7 +529,10 @@ int packed_bwd_device(const Plan& p, void* const* dpacked_out, const void* const
         return rc;
     int64_t seq_b[kMaxW], head_b[kMaxW], packed_b[kMaxW];
     side_bytes(p, 0, seq_b, head_b);
-    for (int k = 0; k < W; ++k) packed_b[k] = p.b * p.s[k] * pitch;
+    for (int k = 0; k < W; ++k) {
+        if (p.b * p.s[k] > INT64_MAX / pitch) return ULY_EINVAL;  // bytes overflow
+        packed_b[k] = p.b * p.s[k] * pitch;
+    }
     if ((rc = check_ptrs(packed_in, packed_b, W)) ||
         (rc = check_ptrs(const_cast<const void* const*>(dpacked_out), packed_b, W)))
         return rc;
