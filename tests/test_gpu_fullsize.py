@@ -2,7 +2,8 @@
 
 Every output element of the fused forward, the interleaved QKV call, the packed QKVG call and the
 two backwards is compared at the Wan-720p shape (W=8, b=1, 75,600 tokens, 40 heads, d=128), and the fused forward
-also on the long packed-QKV geometry (W=4, 250,000 tokens, 56 heads, positions to 249,999). The
+and backward also on the long packed-QKV geometry (W=4, 250,000 tokens, 56 heads, positions to
+249,999). The
 plans, and so the launch configurations (grid, work units, stages, CTAs per SM), are the ones the
 benchmark times; its inputs too where it draws them: q, k, v of the step (seeds 3, 4, 5, weights
 seed 2), the long geometry's q, k (seeds 3, 4), the fp16 rotate-half Wan shape (seeds 3, 4).
@@ -324,6 +325,37 @@ def test_packed_qkvg_backward_wan720p_full(oracle):
             check_all(dpk.tensors[qr][:, :, t], ref_dx[qr], 2.0 ** -8, 1e-4, f"plane {t} rank {qr}")
         del ref_dx
         check_dw(dwo.tensors[0][t].cpu().numpy(), ref_dw, n_rows, f"dw {t}")
+
+
+def test_backward_long_sequence_full(oracle):
+    """Backward on the long packed-QKV geometry's q and k (W=4, 250,000 tokens, 56 heads, d=128;
+    seeds 3, 4 as the benchmark's configuration table), output gradients N(0, 1) (seeds 52, 53):
+    every element of dq and dk, positions to 249,999, and dw (n = 14,000,000 rows per tensor)."""
+    cfg = wl.Workload("long_qk", 4, 1, (62500,) * 4, (14,) * 4, 128, "bfloat16", seed=20)
+    plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
+    q = wl.seq_side_inputs(cfg, "cuda", seed=3)
+    k = wl.seq_side_inputs(cfg, "cuda", seed=4)
+    w = wl.rms_weights(cfg.d).cuda()
+    gq, gk = _wan_grads(cfg, "bfloat16", (52, 53))
+    dqo, dko = _seq_outputs(cfg, torch.bfloat16), _seq_outputs(cfg, torch.bfloat16)
+    dwo = GuardedOutputs([(2, cfg.d)], torch.float32)
+    ws = torch.empty(B.ulysses_qk_fused_backward_workspace(plan), dtype=torch.uint8, device="cuda")
+    B.ulysses_a2a_4d_qk_fused_backward(plan, dqo.tensors, dko.tensors, q, k, gq, gk, w,
+                                       dwo.tensors[0], EPS, THETA, ws)
+    torch.cuda.synchronize()
+    assert dqo.guards_intact() and dko.guards_intact() and dwo.guards_intact()
+    wn = w.cpu().numpy().astype(np.float64)
+    n_rows = cfg.S * cfg.N
+    for t, (x, gy, got) in enumerate(((q, gq, dqo), (k, gk, dko))):
+        ref_dx, ref_dw = oracle.qk_fused_bwd([host_raw(v) for v in x], [host_raw(v) for v in gy],
+                                             cfg.seq_splits, cfg.head_splits, wn[t], EPS, THETA,
+                                             threads=THREADS)
+        for qr in range(cfg.W):
+            check_all(got.tensors[qr], ref_dx[qr], 2.0 ** -8, 1e-4, f"tensor {t} rank {qr}")
+            ref_dx[qr] = None  # free as we go: 3.6 GB of doubles per rank
+        del ref_dx
+        check_dw(dwo.tensors[0][t].cpu().numpy(), ref_dw, n_rows, f"dw {t}")
+        _sensitivity(oracle, cfg, x, gy, wn[t], 0, 0, dw_bound(n_rows), f"dw {t}")
 
 
 def test_backward_wan720p_f16_half_full(oracle):
