@@ -75,12 +75,20 @@ enum {
  * QK RMSNorm + RoPE without fixing its layout; both common ones are provided. */
 enum { ULY_ROPE_ADJACENT = 0, ULY_ROPE_HALF = 1 };
 
-/* Relayout engines: ULY_ENGINE_AUTO picks the fastest measured one (the TMA kernel).
+/* Relayout engines: ULY_ENGINE_AUTO picks the faster measured kernel for the plan: the tensor
+ * engine when every head group's run (n_r * d * elem_size) has the same length of at most 2048
+ * bytes, or when the plan's CTA cap (ulysses_plan_set_max_ctas) is below the SM count and every
+ * run is at most 2048 bytes; the TMA kernel otherwise.
  * ULY_ENGINE_CE issues one pitched cudaMemcpy2DAsync per (source shard, destination rank, batch
  * index) on the copy engines, no kernel: the pages' own transport design (fast-ulysses 0.1.0,
  * opening paragraph: pitched 2D/3D copies on the copy engines) run between buffers of one GPU,
- * kept for comparison and for overlapping with SM-bound work. */
-enum { ULY_ENGINE_AUTO = 0, ULY_ENGINE_TMA = 1, ULY_ENGINE_VEC = 2, ULY_ENGINE_CE = 3 };
+ * kept for comparison and for overlapping with SM-bound work. ULY_ENGINE_TENSOR moves each
+ * (source shard, destination rank) block of up to 256 rows with one tiled tensor-map copy on its
+ * strided side and one bulk copy on its contiguous side (fewer copy instructions per byte than
+ * the TMA kernel's one per row; one CTA per SM); plans with a run above 2048 bytes use the TMA
+ * kernel instead. Every engine gives the same bytes. */
+enum { ULY_ENGINE_AUTO = 0, ULY_ENGINE_TMA = 1, ULY_ENGINE_VEC = 2, ULY_ENGINE_CE = 3,
+       ULY_ENGINE_TENSOR = 4 };
 
 typedef struct ulysses_plan_s* ulysses_plan_t;
 

@@ -20,7 +20,7 @@ def _plan(cap):
     return plan
 
 
-@pytest.mark.parametrize("engine", [B.ULY_ENGINE_TMA, B.ULY_ENGINE_VEC])
+@pytest.mark.parametrize("engine", [B.ULY_ENGINE_TMA, B.ULY_ENGINE_VEC, B.ULY_ENGINE_TENSOR])
 @pytest.mark.parametrize("cap", [1, 7, 152])
 def test_relayout_capped_equals_uncapped(engine, cap):
     W, b, seq, heads, d = G

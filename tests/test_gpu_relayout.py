@@ -16,7 +16,8 @@ from ulysses_sequence_all_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-ENGINES = {"tma": B.ULY_ENGINE_TMA, "vec": B.ULY_ENGINE_VEC, "ce": B.ULY_ENGINE_CE}
+ENGINES = {"tma": B.ULY_ENGINE_TMA, "vec": B.ULY_ENGINE_VEC, "ce": B.ULY_ENGINE_CE,
+           "tensor": B.ULY_ENGINE_TENSOR}
 
 
 @pytest.fixture(scope="module", autouse=True)

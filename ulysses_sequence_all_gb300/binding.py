@@ -18,7 +18,7 @@ ULY_OK, ULY_EINVAL, ULY_EALIGN, ULY_EOVERLAP, ULY_ECHUNK, ULY_ECUDA, ULY_ENOMEM,
 ULY_ESCRATCH = -8
 ULYSSES_STATIC_SCRATCH_BYTES = 2 * 1024 * 1024
 ULY_U8, ULY_F8E4M3, ULY_F8E5M2, ULY_I8, ULY_F16, ULY_BF16, ULY_F32 = 1, 2, 3, 4, 5, 6, 7
-ULY_ENGINE_AUTO, ULY_ENGINE_TMA, ULY_ENGINE_VEC, ULY_ENGINE_CE = 0, 1, 2, 3
+ULY_ENGINE_AUTO, ULY_ENGINE_TMA, ULY_ENGINE_VEC, ULY_ENGINE_CE, ULY_ENGINE_TENSOR = 0, 1, 2, 3, 4
 ULY_ROPE_ADJACENT, ULY_ROPE_HALF = 0, 1
 
 DTYPE_CODES = {"uint8": ULY_U8, "float8_e4m3fn": ULY_F8E4M3, "float8_e5m2": ULY_F8E5M2,

@@ -18,6 +18,11 @@ int64_t relayout_unit_bytes(int engine);
 cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStream_t stream,
                             int device, int sm_count, int64_t max_grid);
 cudaError_t relayout_status(unsigned* status, bool clear);
+bool relayout_tensor_fits(const Plan& p);
+bool relayout_tensor_preferred(const Plan& p, int sm_count);
+cudaError_t relayout_tensor_launch(const Plan& p, const ChunkRows& rows, uint8_t* const* seq,
+                                   uint8_t* const* head, int mode, cudaStream_t stream, int device,
+                                   int sm_count, int64_t max_grid);
 RowRing relayout_row_ring(const Plan& p, int mode);
 int64_t relayout_tile_rows(int64_t row_bytes, int64_t stage_bytes);
 cudaError_t relayout_rows_launch(const RowTileArgs& a, int mode, const RowRing& ring,
@@ -120,7 +125,7 @@ int relayout_check(const Plan& p, int mode, int engine, const void* const* in_pt
 {
     if (mode != 0 && mode != 1) return ULY_EINVAL;
     if (engine != ULY_ENGINE_AUTO && engine != ULY_ENGINE_TMA && engine != ULY_ENGINE_VEC &&
-        engine != ULY_ENGINE_CE)
+        engine != ULY_ENGINE_CE && engine != ULY_ENGINE_TENSOR)
         return ULY_EINVAL;
     int64_t in_b[kMaxW], out_b[kMaxW];
     side_bytes(p, mode, in_b, out_b);
@@ -170,7 +175,8 @@ int relayout_rows(const Plan& p, int mode, int engine, const void* const* in_ptr
                   void* const* out_ptrs, const ChunkRows& rows, cudaStream_t stream,
                   const DeviceInfo& dev)
 {
-    if (engine == ULY_ENGINE_AUTO) engine = ULY_ENGINE_TMA;
+    if (engine == ULY_ENGINE_AUTO)
+        engine = relayout_tensor_preferred(p, dev.sm_count) ? ULY_ENGINE_TENSOR : ULY_ENGINE_TMA;
     if (engine == ULY_ENGINE_CE) return relayout_rows_ce(p, mode, in_ptrs, out_ptrs, rows, stream);
     uint8_t* seq[kMaxW];
     uint8_t* head[kMaxW];
@@ -179,6 +185,14 @@ int relayout_rows(const Plan& p, int mode, int engine, const void* const* in_ptr
         uint8_t* out = static_cast<uint8_t*>(out_ptrs[k]);
         seq[k] = mode == 0 ? in : out;
         head[k] = mode == 0 ? out : in;
+    }
+    if (engine == ULY_ENGINE_TENSOR) {  // one tensor-map box per unit; runs over 2 KiB: TMA
+        if (relayout_tensor_fits(p)) {
+            cudaError_t e = relayout_tensor_launch(p, rows, seq, head, mode, stream, dev.device,
+                                                   dev.sm_count, p.max_ctas);
+            return e == cudaSuccess ? ULY_OK : cuda_fail(e);
+        }
+        engine = ULY_ENGINE_TMA;
     }
     // TMA engine: whole-row tiles when a row fits a stage, row-run segments otherwise
     const RowRing ring = relayout_row_ring(p, mode);

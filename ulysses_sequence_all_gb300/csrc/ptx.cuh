@@ -146,6 +146,32 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
         : "memory");
 }
 
+// Tiled tensor copy global -> shared of one box of a 3-D tensor map at coordinates (c0, c1, c2)
+// (elements; c0 counts the innermost dimension); completion is signalled as transaction bytes (the
+// whole box, out-of-range elements included) on `bar`. `map` is the address of a CUtensorMap in
+// parameter, constant or global memory; dst 128-byte aligned.
+__device__ __forceinline__ void tensor_g2s_3d(void* dst_smem, const void* map, int c0, int c1,
+                                              int c2, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst_smem)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Tiled tensor copy shared -> global of one box, tracked by this thread's bulk async-groups; the
+// parts of the box outside the tensor's extent are not written.
+__device__ __forceinline__ void tensor_s2g_3d(const void* map, int c0, int c1, int c2,
+                                              const void* src_smem)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            map),
+        "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src_smem))
+        : "memory");
+}
+
 // Bulk copy shared -> global, tracked by this thread's bulk async-groups.
 __device__ __forceinline__ void bulk_s2g(void* dst_gmem, const void* src_smem, uint32_t bytes)
 {

@@ -15,9 +15,12 @@
 //    the bytes; the SM only issues copies.
 //  * VEC: a grid-stride loop of warps, 16-byte vector loads (L1 no-allocate) and stores, several
 //    in flight per lane.
+#include <cuda.h>  // CUtensorMap and its encoder's types (the encoder itself is fetched at run time)
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstring>
+#include <mutex>
 
 #include "../../include/ulysses.h"
 #include "plan.h"
@@ -198,6 +201,128 @@ __global__ void __launch_bounds__(32, 1) relayout_tma_kernel(const __grid_consta
     };
     run_stage_ring<ULY_TMA_STAGES, MODE == 0 ? ULY_TMA_LOOKAHEAD0 : ULY_TMA_LOOKAHEAD1>(
         full, n, lane, issue_load, issue_store);
+}
+
+// ---- tensor engine: one tensor-map box per unit on the strided side --------------------------------
+// A unit is a block of up to R consecutive rows of one sequence shard q and batch index, for one
+// head group r: on the sequence side R runs of n_r d e bytes, strided by N d e; on the head side one
+// contiguous span. The strided side moves with one tiled tensor copy instead of one bulk copy per
+// row: for segment g = (q, r) a 3-D tensor map describes rank q's runs of head group r in this
+// launch's rows, (run / 8 eight-byte elements, chunk rows, b) with strides (N d e, s_q N d e) bytes,
+// starting at the run's first byte, so every box starts at x = 0. Mode 0: one tensor load of the
+// unit's rows (rows past the chunk are filled, not read from elsewhere) and one bulk store of the
+// contiguous head-side span; mode 1: one bulk load of the span and one tensor store, which the map
+// clips at the chunk's rows. Units are ordered (shard, batch index, row block, head group), so
+// consecutive units cover the same rows and the grid as a whole reads and writes whole rows in
+// sequence. R (at most 256, the box limit) is the same for every head group: the rows of the
+// widest run that fit a stage; a run is at most 2,048 bytes (256 eight-byte elements), and plans
+// with longer runs use the other engines.
+//
+// A unit costs a CTA about half a microsecond whatever its size (16 to 52 KiB measured), so a
+// CTA's throughput grows with its stage bytes, while a full grid of small stages spreads the
+// traffic more evenly. Two pipeline shapes per mode, one CTA per SM (stages fill shared memory):
+// a full grid takes many 24 KiB stages with most of them loading; a grid capped below the SM
+// count (the relayout sharing the GPU with other work) takes four stages of about 50 KiB, which
+// keeps 6 TB/s on half the SMs at the Wan-720p shape.
+struct TensorArgs {
+    CUtensorMap map[kMaxSeg];  // segment g = q * W + r
+    uint8_t* seq_ptr[kMaxW];
+    uint8_t* head_ptr[kMaxW];
+    int64_t s[kMaxW], seq_off[kMaxW], n[kMaxW], head_off[kMaxW];
+    int64_t row_lo[kMaxW], rows[kMaxW];  // this launch's rows of shard q
+    int64_t blocks[kMaxW];               // row blocks per batch index of shard q
+    int64_t unit_begin[kMaxW + 1];       // prefix of unit counts over q
+    int64_t S, N, b, d_bytes, R, total_units;
+    int32_t live_r[kMaxW];  // head groups with n_r > 0, in order
+    int32_t W, n_live;
+};
+
+struct TensorUnit {
+    int q, r;
+    int64_t bb, i0, nrows, run;
+};
+
+__device__ __forceinline__ TensorUnit decode_tensor(const TensorArgs& a, int64_t u)
+{
+    int lo = 0, hi = a.W - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.unit_begin[mid] <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    TensorUnit t;
+    t.q = lo;
+    const int64_t local = u - a.unit_begin[lo];
+    const int64_t rest = div_fast(local, a.n_live);
+    t.r = a.live_r[local - rest * a.n_live];
+    const int64_t blocks = a.blocks[lo];
+    t.bb = div_fast(rest, blocks);
+    const int64_t blk = rest - t.bb * blocks;
+    t.i0 = blk * a.R;  // in the chunk
+    t.nrows = min(a.R, a.rows[lo] - t.i0);
+    t.run = a.n[t.r] * a.d_bytes;
+    return t;
+}
+
+constexpr int kTensorStageAlign = 1024;  // stage buffers start here (tensor copies want 128 B)
+
+struct TensorShape {
+    int stages, unit_bytes, lookahead;
+};
+// [mode]: measured at the Wan-720p shape (W = 8, runs of 1,280 bytes), CUDA events back to back.
+constexpr TensorShape kTensorFull[2] = {{8, 24576, 7}, {9, 24576, 4}};
+constexpr TensorShape kTensorCapped[2] = {{4, 53248, 3}, {4, 49152, 3}};
+
+constexpr int tensor_smem(TensorShape t) { return kTensorStageAlign + t.stages * t.unit_bytes; }
+
+template <int MODE, int K, int UNIT, int L>
+__global__ void __launch_bounds__(32, 1) relayout_tensor_kernel(const __grid_constant__ TensorArgs a)
+{
+    static_assert(UNIT % 1024 == 0, "tensor-copy stages must stay 1024-byte aligned");
+    static_assert(L >= 1 && L <= K && K <= 16, "lookahead <= stages; barriers fit the area");
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint8_t* stage0 = smem + kTensorStageAlign;
+    const int lane = threadIdx.x;
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    const int64_t n = first < a.total_units ? (a.total_units - 1 - first) / step + 1 : 0;
+    if (n == 0) return;
+    if (lane == 0) {
+        for (int s = 0; s < K; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    // the unit's contiguous span on rank r's (b, S, n_r, d) head side
+    auto head_span = [&](const TensorUnit& t) {
+        return a.head_ptr[t.r] +
+               (t.bb * a.S + a.seq_off[t.q] + a.row_lo[t.q] + t.i0) * t.run;
+    };
+    auto issue_load = [&](int64_t k) {
+        if (lane != 0) return;
+        const TensorUnit t = decode_tensor(a, first + k * step);
+        const int s = int(k % K);
+        uint8_t* dst = stage0 + size_t(s) * UNIT;
+        if (MODE == 0) {  // the whole box arrives (rows past the chunk are filled)
+            mbar_arrive_expect_tx(&full[s], uint32_t(a.R * t.run));
+            tensor_g2s_3d(dst, &a.map[t.q * a.W + t.r], 0, int(t.i0), int(t.bb), &full[s]);
+        } else {
+            const uint32_t bytes = uint32_t(t.nrows * t.run);
+            mbar_arrive_expect_tx(&full[s], bytes);
+            bulk_g2s(dst, head_span(t), bytes, &full[s]);
+        }
+    };
+    auto issue_store = [&](int64_t k) {
+        if (lane != 0) return;
+        const TensorUnit t = decode_tensor(a, first + k * step);
+        const uint8_t* src = stage0 + size_t(k % K) * UNIT;
+        if (MODE == 0)
+            bulk_s2g(head_span(t), src, uint32_t(t.nrows * t.run));
+        else
+            tensor_s2g_3d(&a.map[t.q * a.W + t.r], 0, int(t.i0), int(t.bb), src);
+    };
+    run_stage_ring<K, L>(full, n, lane, issue_load, issue_store);
 }
 
 // ---- row tiles: whole rows through shared memory ------------------------------------------------
@@ -408,6 +533,152 @@ cudaError_t relayout_launch(const RelayoutArgs& a, int mode, int engine, cudaStr
     else
         relayout_tma_kernel<1><<<unsigned(grid), 32, kTmaSmem, stream>>>(a);
     return cudaGetLastError();
+}
+
+// The tensor-map encoder of the driver, fetched once through the runtime (no link to libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+template <int MODE, int K, int UNIT, int L>
+static cudaError_t tensor_launch_shape(const TensorArgs& a, unsigned grid, cudaStream_t stream,
+                                       int device)
+{
+    auto kernel = relayout_tensor_kernel<MODE, K, UNIT, L>;
+    constexpr int smem = tensor_smem({K, UNIT, L});
+    static std::atomic<int> smem_set[64];
+    if (device >= 0 && device < 64 && !smem_set[device].load()) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        smem_set[device].store(1);
+    }
+    kernel<<<grid, 32, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+#define ULY_TENSOR_SHAPE(M, T) M, T.stages, T.unit_bytes, T.lookahead
+
+static cudaError_t tensor_dispatch(int mode, bool capped, const TensorArgs& a, unsigned grid,
+                                   cudaStream_t stream, int device)
+{
+    if (mode == 0)
+        return capped ? tensor_launch_shape<ULY_TENSOR_SHAPE(0, kTensorCapped[0])>(a, grid, stream, device)
+                      : tensor_launch_shape<ULY_TENSOR_SHAPE(0, kTensorFull[0])>(a, grid, stream, device);
+    return capped ? tensor_launch_shape<ULY_TENSOR_SHAPE(1, kTensorCapped[1])>(a, grid, stream, device)
+                  : tensor_launch_shape<ULY_TENSOR_SHAPE(1, kTensorFull[1])>(a, grid, stream, device);
+}
+#undef ULY_TENSOR_SHAPE
+
+// Whether the tensor engine takes this plan: every run of at most 256 eight-byte elements.
+bool relayout_tensor_fits(const Plan& p)
+{
+    for (int r = 0; r < p.W; ++r)
+        if (p.n[r] * p.d * p.e > 256 * 8) return false;
+    return true;
+}
+
+// The automatic engine's choice. A tensor unit costs a CTA a fixed time, so the engine wins where
+// its units fill their stages: every head group's run equally long (measured: 1.03x the row tiles
+// at the Wan-720p shape; 0.85-0.99x on plans with unequal head splits, whose smaller groups leave
+// stages part-empty). Under a CTA cap below the SM count it wins on every plan it takes (measured
+// 2.3 to 5.3 times the row tiles' throughput at caps of 114, 76 and 38 CTAs), as its CTAs keep
+// more bytes in flight.
+bool relayout_tensor_preferred(const Plan& p, int sm_count)
+{
+    if (!relayout_tensor_fits(p)) return false;
+    if (p.max_ctas > 0 && p.max_ctas < sm_count) return true;
+    int64_t run = 0;
+    for (int r = 0; r < p.W; ++r) {
+        if (p.n[r] == 0) continue;
+        if (run != 0 && p.n[r] != run) return false;
+        run = p.n[r];
+    }
+    return true;
+}
+
+cudaError_t relayout_tensor_launch(const Plan& p, const ChunkRows& rows, uint8_t* const* seq,
+                                   uint8_t* const* head, int mode, cudaStream_t stream, int device,
+                                   int sm_count, int64_t max_grid)
+{
+    TensorArgs a;
+    std::memset(&a, 0, sizeof a);
+    const int W = p.W;
+    const int64_t de = p.d * p.e;
+    int64_t max_run = 0;
+    a.n_live = 0;
+    for (int r = 0; r < W; ++r) {
+        if (p.n[r] == 0) continue;
+        a.live_r[a.n_live++] = r;
+        if (p.n[r] * de > max_run) max_run = p.n[r] * de;
+    }
+    if (a.n_live == 0) return cudaSuccess;
+    // one CTA per SM; a cap below the SM count takes the large-stage shape
+    int64_t grid = sm_count;
+    if (max_grid > 0 && grid > max_grid) grid = max_grid;
+    const bool capped = grid < sm_count;
+    const TensorShape shape = capped ? kTensorCapped[mode] : kTensorFull[mode];
+    a.R = shape.unit_bytes / max_run;
+    if (a.R > 256) a.R = 256;
+    a.W = W;
+    a.S = p.S;
+    a.N = p.N;
+    a.b = p.b;
+    a.d_bytes = de;
+    int64_t total = 0;
+    for (int k = 0; k < kMaxW; ++k) {
+        const bool live = k < W;
+        a.seq_ptr[k] = live ? seq[k] : nullptr;
+        a.head_ptr[k] = live ? head[k] : nullptr;
+        a.s[k] = live ? p.s[k] : 0;
+        a.seq_off[k] = live ? p.seq_off[k] : 0;
+        a.n[k] = live ? p.n[k] : 0;
+        a.head_off[k] = live ? p.head_off[k] : 0;
+        a.row_lo[k] = live ? rows.lo[k] : 0;
+        a.rows[k] = live ? rows.cnt[k] : 0;
+        a.blocks[k] = (a.rows[k] + a.R - 1) / a.R;
+        a.unit_begin[k] = total;
+        total += p.b * a.blocks[k] * a.n_live;
+    }
+    a.unit_begin[kMaxW] = total;
+    a.total_units = total;
+    if (total == 0) return cudaSuccess;
+    EncodeTiledFn encode = encode_tiled_fn();
+    if (!encode) return cudaErrorNotSupported;
+    for (int q = 0; q < W; ++q) {
+        for (int r = 0; r < W; ++r) {
+            const int64_t run = a.n[r] * de;
+            if (a.rows[q] == 0 || run == 0) continue;
+            uint8_t* base = a.seq_ptr[q] + (a.row_lo[q] * a.N + a.head_off[r]) * de;
+            const cuuint64_t dims[3] = {cuuint64_t(run / 8), cuuint64_t(a.rows[q]), cuuint64_t(a.b)};
+            const cuuint64_t strides[2] = {cuuint64_t(a.N * de), cuuint64_t(a.s[q] * a.N * de)};
+            const cuuint32_t boxdim[3] = {cuuint32_t(run / 8), cuuint32_t(a.R), 1};
+            const cuuint32_t estrides[3] = {1, 1, 1};
+            const CUresult rc = encode(&a.map[q * W + r], CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, base,
+                                       dims, strides, boxdim, estrides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (rc != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        }
+    }
+    if (grid > a.total_units) grid = a.total_units;
+    return tensor_dispatch(mode, capped, a, unsigned(grid), stream, device);
 }
 
 // The row-tile kernel's pipeline shape for a plan and mode, from its geometry: `row` = one

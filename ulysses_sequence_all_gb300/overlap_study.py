@@ -28,7 +28,8 @@ import torch
 from . import binding as B
 from . import workloads as wl
 
-ENGINES = {"tma": B.ULY_ENGINE_TMA, "vec": B.ULY_ENGINE_VEC, "ce": B.ULY_ENGINE_CE}
+ENGINES = {"tma": B.ULY_ENGINE_TMA, "vec": B.ULY_ENGINE_VEC, "ce": B.ULY_ENGINE_CE,
+           "tensor": B.ULY_ENGINE_TENSOR}
 
 
 def main():
@@ -37,7 +38,7 @@ def main():
     ap.add_argument("--pairs", type=int, default=24)
     ap.add_argument("--reps", type=int, default=5)
     ap.add_argument("--gemm-size", type=int, default=8192)
-    ap.add_argument("--engines", default="tma,vec,ce")
+    ap.add_argument("--engines", default="tma,vec,ce,tensor")
     ap.add_argument("--max-ctas", default="0",
                     help="comma-separated CTA caps for the SM engines (0: no cap)")
     ap.add_argument("--priorities", default="default,high")
