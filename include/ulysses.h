@@ -140,6 +140,12 @@ int ulysses_plan_set_rope_pairs(ulysses_plan_t plan, int pairs);
 int ulysses_plan_bytes(ulysses_plan_t plan, int mode, int rank, int64_t* in_bytes,
                        int64_t* out_bytes);
 
+/* The engine that a call with ULY_ENGINE_AUTO takes for this plan on the calling thread's
+ * current device: ULY_ENGINE_TENSOR or ULY_ENGINE_TMA (see the engine list above), from the
+ * plan's splits, element size and CTA cap and the device's SM count. ULY_EINVAL for a null plan
+ * or engine pointer; a CUDA error status when the device cannot be queried. */
+int ulysses_plan_auto_engine(ulysses_plan_t plan, int* engine);
+
 /* Number of launches a call in `mode` makes under the current chunk cap (ULY_ECHUNK when no
  * split along whole sequence rows meets the cap). */
 int ulysses_plan_num_chunks(ulysses_plan_t plan, int mode, int64_t* n_chunks);

@@ -314,3 +314,24 @@ def test_misaligned_and_overlapping_on_device():
     with pytest.raises(B.UlyssesError) as ei:
         B.ulysses_a2a_4d(plan, 0, x, [x[0], y[1]])
     assert ei.value.status == B.ULY_EOVERLAP
+
+
+def test_auto_engine_choice():
+    """AUTO takes the tensor engine where every run has one length of at most 2048 bytes, or
+    under a CTA cap below the SM count when every run fits; the TMA kernel otherwise."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+
+    def auto(cfg, cap=0):
+        plan = B.ulysses_plan(*geom(cfg))
+        B.ulysses_plan_set_max_ctas(plan, cap)
+        return B.ulysses_plan_auto_engine(plan)
+
+    by_name = {c.name: c for c in wl.UNEVEN}
+    w8_f16, w3_f16 = by_name["uneven_W8_float16"], by_name["uneven_W3_float16"]
+    assert auto(wl.WAN) == B.ULY_ENGINE_TENSOR  # runs of 1,280 bytes
+    assert auto(wl.TINY) == B.ULY_ENGINE_TENSOR
+    assert auto(w8_f16) == B.ULY_ENGINE_TMA  # runs 1,024 to 1,536 bytes
+    assert auto(w8_f16, cap=sms // 2) == B.ULY_ENGINE_TENSOR
+    assert auto(w8_f16, cap=sms) == B.ULY_ENGINE_TMA  # a cap at the SM count caps nothing
+    assert auto(w3_f16, cap=sms // 2) == B.ULY_ENGINE_TMA  # runs above 2,048 bytes
+    assert auto(wl.LONG_QKV) == B.ULY_ENGINE_TMA  # 3,584-byte runs

@@ -173,6 +173,14 @@ def test_max_ctas_setter():
     assert ei.value.status == B.ULY_EINVAL
 
 
+def test_auto_engine_argument_errors():
+    lib = B.library()
+    engine = ctypes.c_int()
+    assert lib.ulysses_plan_auto_engine(None, ctypes.byref(engine)) == B.ULY_EINVAL
+    plan = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "bfloat16")
+    assert lib.ulysses_plan_auto_engine(plan, None) == B.ULY_EINVAL
+
+
 def test_fused_argument_errors_before_cuda():
     plan32 = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "float32")
     plan = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "bfloat16")

@@ -28,6 +28,7 @@ DTYPE_CODES = {"uint8": ULY_U8, "float8_e4m3fn": ULY_F8E4M3, "float8_e5m2": ULY_
 EXPORTS = ["ulysses_plan", "ulysses_plan_destroy", "ulysses_plan_set_chunk_bytes",
            "ulysses_plan_set_max_ctas", "ulysses_plan_set_rope_pairs",
            "ulysses_plan_bytes", "ulysses_plan_num_chunks", "ulysses_plan_chunk_rows",
+           "ulysses_plan_auto_engine",
            "ulysses_plan_rank_segments",
            "ulysses_a2a_4d", "ulysses_a2a_4d_engine", "ulysses_a2a_4d_qk_fused",
            "ulysses_a2a_4d_qkv_fused", "ulysses_a2a_4d_packed_fused",
@@ -70,6 +71,7 @@ def _lib():
         lib.ulysses_plan_bytes.argtypes = [_p, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_i64),
                                            ctypes.POINTER(_i64)]
         lib.ulysses_plan_num_chunks.argtypes = [_p, ctypes.c_int, ctypes.POINTER(_i64)]
+        lib.ulysses_plan_auto_engine.argtypes = [_p, ctypes.POINTER(ctypes.c_int)]
         lib.ulysses_plan_chunk_rows.argtypes = [_p, ctypes.c_int, _i64, ctypes.POINTER(_i64),
                                                 ctypes.POINTER(_i64)]
         lib.ulysses_plan_rank_segments.argtypes = [_p, ctypes.c_int, ctypes.c_int, _p]
@@ -195,6 +197,14 @@ def ulysses_plan_bytes(plan: Plan, mode: int, rank: int):
     _check(_lib().ulysses_plan_bytes(plan, mode, rank, ctypes.byref(i), ctypes.byref(o)),
            "ulysses_plan_bytes")
     return i.value, o.value
+
+
+def ulysses_plan_auto_engine(plan: Plan) -> int:
+    """The engine ULY_ENGINE_AUTO takes for this plan on the current device (ULY_ENGINE_TENSOR or
+    ULY_ENGINE_TMA)."""
+    e = ctypes.c_int()
+    _check(_lib().ulysses_plan_auto_engine(plan, ctypes.byref(e)), "ulysses_plan_auto_engine")
+    return e.value
 
 
 def ulysses_plan_num_chunks(plan: Plan, mode: int = 0) -> int:

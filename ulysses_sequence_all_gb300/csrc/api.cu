@@ -816,6 +816,16 @@ int ulysses_plan_bytes(ulysses_plan_t plan, int mode, int rank, int64_t* in_byte
     return ULY_OK;
 }
 
+int ulysses_plan_auto_engine(ulysses_plan_t plan, int* engine)
+{
+    if (!plan || !engine) return ULY_EINVAL;
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc) return rc;
+    *engine = relayout_tensor_preferred(plan->p, dev.sm_count) ? ULY_ENGINE_TENSOR : ULY_ENGINE_TMA;
+    return ULY_OK;
+}
+
 int ulysses_plan_num_chunks(ulysses_plan_t plan, int mode, int64_t* n_chunks)
 {
     if (!plan || !n_chunks || (mode != 0 && mode != 1)) return ULY_EINVAL;

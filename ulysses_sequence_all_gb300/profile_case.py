@@ -19,17 +19,19 @@ from . import workloads as wl
 # half the Wan sequence (37,800 tokens; 387 MB per tensor set) for captures with many passes
 WAN_HALF = wl.Workload("wan720p_half", 8, 1, (4725,) * 8, (5,) * 8, 128, "bfloat16", seed=1)
 WORKLOADS = {"wan": wl.WAN, "wan_half": WAN_HALF, "long": wl.LONG_QKV, "tiny": wl.TINY}
+ENGINES = {"auto": B.ULY_ENGINE_AUTO, "tma": B.ULY_ENGINE_TMA, "vec": B.ULY_ENGINE_VEC,
+           "tensor": B.ULY_ENGINE_TENSOR}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--kernel", choices=["fused", "bwd", "mode0", "mode1", "all"], default="all")
-    ap.add_argument("--engine", choices=["tma", "vec"], default="tma")
+    ap.add_argument("--engine", choices=sorted(ENGINES), default="auto")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="wan")
     ap.add_argument("--iters", type=int, default=2)
     args = ap.parse_args()
     cfg = WORKLOADS[args.workload]
-    engine = B.ULY_ENGINE_TMA if args.engine == "tma" else B.ULY_ENGINE_VEC
+    engine = ENGINES[args.engine]
     plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
     dt = wl.torch_dtype(cfg.dtype)
     head = [torch.empty(cfg.head_side_shape(r), dtype=dt, device="cuda") for r in range(cfg.W)]
