@@ -643,7 +643,9 @@ def run_ours(args):
     peak, peak_kind = read_peaks()
     relayout_kernel = ("relayout_tensor_kernel" if B.ulysses_plan_auto_engine(wk.plan) ==
                        B.ULY_ENGINE_TENSOR else "relayout_rows_kernel")
-    kernel_name = {"fused_qk": "fused_qk_kernel", "mode0": f"{relayout_kernel}<0>",
+    fused_kernel = ("fused_qk_tensor_kernel" if B.ulysses_plan_fused_kernel(wk.plan) ==
+                    B.ULY_ENGINE_TENSOR else "fused_qk_kernel")
+    kernel_name = {"fused_qk": fused_kernel, "mode0": f"{relayout_kernel}<0>",
                    "mode1": f"{relayout_kernel}<1>"}[dominant]
     traffic = read_traffic(kernel_name)
     d2d = d2d_gbs(torch, wk.side) if rank == 0 else None
@@ -667,7 +669,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": {"fused_qk": wk.bytes_fused,
                                                       "mode0": wk.bytes_plain,
                                                       "mode1": wk.bytes_plain}[dominant]},
-        "kernels": {k: {"kernel": {"fused_qk": "fused_qk_kernel"}.get(k, relayout_kernel),
+        "kernels": {k: {"kernel": {"fused_qk": fused_kernel}.get(k, relayout_kernel),
                         "median_ms": round(med[k], 4), "GB/s": round(gbs[k], 1),
                         "frac_of_peak": round(gbs[k] / peak, 4),
                         "frac_of_d2d": round(gbs[k] / d2d, 4) if d2d else None} for k in med},

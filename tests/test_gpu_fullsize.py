@@ -109,21 +109,28 @@ def _sensitivity(oracle, cfg, xs, gys, w, f16, half, bound, what, rows=16):
 
 # ---- forward ----------------------------------------------------------------------------------
 def test_fused_wan720p_full(oracle):
-    """The step's fused call: q (seed 3) and k (seed 4), weights seed 2, every element."""
+    """The step's fused call: q (seed 3) and k (seed 4), weights seed 2, every element, on the
+    automatic choice and on both kernels."""
     cfg, plan = _wan_plan()
     q = wl.seq_side_inputs(cfg, "cuda", seed=wl.FUSED.seed)
     k = wl.seq_side_inputs(cfg, "cuda", seed=wl.FUSED.extra["k_seed"])
     w = wl.rms_weights(cfg.d, seed=wl.FUSED.extra["w_seed"]).cuda()
-    qo, ko = _head_outputs(cfg, torch.bfloat16, 2)
-    B.ulysses_a2a_4d_qk_fused(plan, q, k, qo.tensors, ko.tensors, w, EPS, THETA)
-    torch.cuda.synchronize()
-    assert qo.guards_intact() and ko.guards_intact(), "a kernel wrote outside its output"
+    outs = {}
+    for name, engine in (("auto", B.ULY_ENGINE_AUTO), ("tokens", B.ULY_ENGINE_TMA),
+                         ("tensor", B.ULY_ENGINE_TENSOR)):
+        B.ulysses_plan_set_fused_engine(plan, engine)
+        qo, ko = _head_outputs(cfg, torch.bfloat16, 2)
+        B.ulysses_a2a_4d_qk_fused(plan, q, k, qo.tensors, ko.tensors, w, EPS, THETA)
+        torch.cuda.synchronize()
+        assert qo.guards_intact() and ko.guards_intact(), f"{name}: a kernel wrote outside its output"
+        outs[name] = (qo, ko)
     wn = w.cpu().numpy().astype(np.float64)
-    for t, (xin, out) in enumerate(((q, qo), (k, ko))):
+    for t, xin in enumerate((q, k)):
         ref = oracle.qk_fused_A([host_raw(x) for x in xin], cfg.seq_splits, cfg.head_splits,
                                 wn[t], EPS, THETA, threads=THREADS)
-        for r in range(cfg.W):
-            check_all(out.tensors[r], ref[r], 2.0 ** -8, 1e-5, f"tensor {t} rank {r}")
+        for name, pair in outs.items():
+            for r in range(cfg.W):
+                check_all(pair[t].tensors[r], ref[r], 2.0 ** -8, 1e-5, f"{name} tensor {t} rank {r}")
         del ref
 
 
@@ -136,16 +143,21 @@ def test_fused_wan720p_f16_half_full(oracle):
     q = wl.seq_side_inputs(cfg16, "cuda", seed=3)
     k = wl.seq_side_inputs(cfg16, "cuda", seed=4)
     w = wl.rms_weights(cfg.d).cuda()
-    qo, ko = _head_outputs(cfg, torch.float16, 2)
-    B.ulysses_a2a_4d_qk_fused(plan, q, k, qo.tensors, ko.tensors, w, EPS, THETA)
-    torch.cuda.synchronize()
-    assert qo.guards_intact() and ko.guards_intact(), "a kernel wrote outside its output"
+    outs = {}
+    for name, engine in (("tokens", B.ULY_ENGINE_TMA), ("tensor", B.ULY_ENGINE_TENSOR)):
+        B.ulysses_plan_set_fused_engine(plan, engine)
+        qo, ko = _head_outputs(cfg, torch.float16, 2)
+        B.ulysses_a2a_4d_qk_fused(plan, q, k, qo.tensors, ko.tensors, w, EPS, THETA)
+        torch.cuda.synchronize()
+        assert qo.guards_intact() and ko.guards_intact(), f"{name}: a kernel wrote outside its output"
+        outs[name] = (qo, ko)
     wn = w.cpu().numpy().astype(np.float64)
-    for t, (xin, out) in enumerate(((q, qo), (k, ko))):
+    for t, xin in enumerate((q, k)):
         ref = oracle.qk_fused_var([host_raw(x) for x in xin], cfg.seq_splits, cfg.head_splits,
                                   wn[t], EPS, THETA, 1, 1, threads=THREADS)
-        for r in range(cfg.W):
-            check_all(out.tensors[r], ref[r], 2.0 ** -10, 1e-5, f"tensor {t} rank {r}")
+        for name, pair in outs.items():
+            for r in range(cfg.W):
+                check_all(pair[t].tensors[r], ref[r], 2.0 ** -10, 1e-5, f"{name} tensor {t} rank {r}")
         del ref
 
 

@@ -38,9 +38,14 @@ def check_close(oracle, got_bf16_u16: np.ndarray, ref: np.ndarray, what: str):
     return float(err.max())
 
 
-def run_fused(g, q_in, k_in, w, cap=None):
+# the fused forward's kernels: token units and row blocks per head group (tensor maps)
+ENGINES = {"tokens": B.ULY_ENGINE_TMA, "tensor": B.ULY_ENGINE_TENSOR}
+
+
+def run_fused(g, q_in, k_in, w, cap=None, engine=B.ULY_ENGINE_AUTO):
     W, b, seq, heads, d = g
     plan = B.ulysses_plan(W, b, seq, heads, d, "bfloat16")
+    B.ulysses_plan_set_fused_engine(plan, engine)
     if cap is not None:
         B.ulysses_plan_set_chunk_bytes(plan, cap)
     shapes = [(b, sum(seq), n, d) for n in heads]
@@ -75,14 +80,22 @@ SMALL = [
     (2, 1, [75000, 600], [1, 1], 128),   # positions up to 75,599 on every pair
     (2, 1, [3, 2], [64, 64], 128),       # 64 KiB per token of q and k: fewer CTAs per SM
     (1, 1, [4], [100], 256),             # 100 KiB per token: one CTA per SM
+    # equal head groups: the shapes the row-block (tensor-map) kernel takes; others fall back
+    (3, 2, [5, 0, 7], [2, 2, 2], 64),
+    (4, 1, [3, 4, 5, 6], [2, 2, 2, 2], 32),
+    (2, 1, [7, 2], [3, 3], 8),
+    (4, 2, [3, 1, 0, 2], [1, 1, 1, 1], 16),
+    (5, 2, [300, 310, 290, 305, 295], [8] * 5, 128),
+    (8, 1, [1000, 999, 1001, 998, 1002, 997, 1003, 1000], [5] * 8, 128),
 ]
 
 
+@pytest.mark.parametrize("engine", list(ENGINES))
 @pytest.mark.parametrize("g", SMALL, ids=[f"f{i}" for i in range(len(SMALL))])
-def test_fused_full(oracle, g):
+def test_fused_full(oracle, g, engine):
     W, b, seq, heads, d = g
     q, k, w = make_inputs(g, seed=sum(seq) + d)
-    qo, ko = run_fused(g, q, k, w)
+    qo, ko = run_fused(g, q, k, w, engine=ENGINES[engine])
     wn = w.cpu().numpy().astype(np.float64)
     for name, xin, out, wrow in (("q", q, qo, wn[0]), ("k", k, ko, wn[1])):
         ref = oracle.qk_fused_A([host_raw(x) for x in xin], seq, heads, wrow, EPS, THETA)
@@ -143,23 +156,44 @@ def test_fused_long_sequence_sampled(oracle):
             check_close(oracle, host_raw(out[r][0, p, hg - head_off[r]]), ref, f"t{t} p={p} h={hg}")
 
 
-def test_fused_chunked_equals_unchunked():
-    g = (5, 2, [300, 310, 290, 305, 295], [9, 8, 8, 8, 7], 128)
+@pytest.mark.parametrize("g", [(5, 2, [300, 310, 290, 305, 295], [9, 8, 8, 8, 7], 128),
+                               (5, 2, [300, 310, 290, 305, 295], [8] * 5, 128)],
+                         ids=["uneven_heads", "equal_heads"])
+@pytest.mark.parametrize("engine", list(ENGINES))
+def test_fused_chunked_equals_unchunked(engine, g):
     q, k, w = make_inputs(g, seed=9)
-    qa, ka = run_fused(g, q, k, w)
-    qb, kb = run_fused(g, q, k, w, cap=1 << 20)
+    qa, ka = run_fused(g, q, k, w, engine=ENGINES[engine])
+    qb, kb = run_fused(g, q, k, w, cap=1 << 20, engine=ENGINES[engine])
+    for a, b in zip(qa + ka, qb + kb):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("g", [SMALL[2], SMALL[8], SMALL[-1], (3, 2, [37, 0, 41], [2, 2, 2], 64),
+                               (1, 1, [50], [4], 256)],
+                         ids=["wan_like", "long_positions", "w8_1000", "zero_split_b2", "run_2048"])
+def test_fused_engines_give_the_same_bytes(g):
+    """The token-unit and tensor-map kernels compute the same fp32 arithmetic per head row, so
+    their outputs are equal bit for bit."""
+    q, k, w = make_inputs(g, seed=21)
+    qa, ka = run_fused(g, q, k, w, engine=B.ULY_ENGINE_TMA)
+    qb, kb = run_fused(g, q, k, w, engine=B.ULY_ENGINE_TENSOR)
     for a, b in zip(qa + ka, qb + kb):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
 @pytest.mark.parametrize("g", [(5, 2, [300, 310, 290, 305, 295], [9, 8, 8, 8, 7], 128),
-                               (3, 1, [4, 0, 3], [2, 1, 1], 64)], ids=["uneven_b2", "zero_split"])
+                               (3, 1, [4, 0, 3], [2, 1, 1], 64),
+                               (5, 2, [300, 310, 290, 305, 295], [8] * 5, 128),
+                               (3, 1, [4, 0, 3], [2, 2, 2], 64)],
+                         ids=["uneven_b2", "zero_split", "equal_b2", "equal_zero_split"])
 def test_fused_host_buffers_match_device_path(oracle, g):
-    """The chunked host-buffer fused call gives the device call's bytes exactly (twice in a row)."""
+    """The chunked host-buffer fused call gives the device call's bytes exactly (twice in a row),
+    on either kernel."""
     W, b, seq, heads, d = g
     q, k, w = make_inputs(g, seed=11)
-    qa, ka = run_fused(g, q, k, w)
+    qa, ka = run_fused(g, q, k, w, engine=B.ULY_ENGINE_TMA)
     plan = B.ulysses_plan(W, b, seq, heads, d, "bfloat16")
+    B.ulysses_plan_set_fused_engine(plan, B.ULY_ENGINE_TENSOR)
     hq = [x.cpu().pin_memory() for x in q]
     hk = [x.cpu().pin_memory() for x in k]
     hqo = [torch.zeros(t.shape, dtype=torch.bfloat16).pin_memory() for t in qa]
@@ -181,6 +215,7 @@ def test_fused_zero_rows_stay_zero():
     q = [torch.zeros((1, s, 4, 128), dtype=torch.bfloat16, device="cuda") for s in g[2]]
     k = [torch.zeros_like(x) for x in q]
     w = wl.rms_weights(128).cuda()
-    qo, ko = run_fused(g, q, k, w)
-    for t in qo + ko:
-        assert torch.count_nonzero(t.float()) == 0
+    for engine in ENGINES.values():
+        qo, ko = run_fused(g, q, k, w, engine=engine)
+        for t in qo + ko:
+            assert torch.count_nonzero(t.float()) == 0

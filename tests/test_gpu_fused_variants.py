@@ -28,6 +28,11 @@ GEOMS = [
     (2, 1, [7, 2], [3, 1], 8),
     (1, 1, [4], [100], 256),
     (2, 1, [75000, 600], [1, 1], 128),
+    # equal head groups: the shapes the row-block (tensor-map) kernel takes
+    (3, 2, [5, 0, 7], [2, 2, 2], 64),
+    (4, 2, [3, 1, 0, 2], [1, 1, 1, 1], 16),
+    (2, 1, [7, 2], [3, 3], 8),
+    (8, 1, [37, 41, 29, 33, 40, 35, 31, 38], [5] * 8, 128),
 ]
 
 
@@ -74,13 +79,15 @@ def _inputs(g, f16, seed, planes=2):
     return xs, wl.rms_weights(d, seed=seed + 1).cuda()
 
 
+@pytest.mark.parametrize("engine", [B.ULY_ENGINE_TMA, B.ULY_ENGINE_TENSOR], ids=["tokens", "tensor"])
 @pytest.mark.parametrize("variant", VARIANTS, ids=VIDS)
 @pytest.mark.parametrize("g", GEOMS, ids=[f"g{i}" for i in range(len(GEOMS))])
-def test_forward_variant(oracle, g, variant):
+def test_forward_variant(oracle, g, variant, engine):
     f16, half = variant
     W, b, seq, heads, d = g
     (q, k), w = _inputs(g, f16, seed=sum(seq) + d + 10 * f16 + half)
     plan = _plan(g, f16, half)
+    B.ulysses_plan_set_fused_engine(plan, engine)
     shapes = [(b, sum(seq), n, d) for n in heads]
     qo, ko = GuardedOutputs(shapes, _dtype(f16)), GuardedOutputs(shapes, _dtype(f16))
     B.ulysses_a2a_4d_qk_fused(plan, q, k, qo.tensors, ko.tensors, w, EPS, THETA)

@@ -173,6 +173,40 @@ def test_max_ctas_setter():
     assert ei.value.status == B.ULY_EINVAL
 
 
+def test_fused_engine_setter():
+    plan = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "bfloat16")
+    for engine in (B.ULY_ENGINE_AUTO, B.ULY_ENGINE_TMA, B.ULY_ENGINE_TENSOR):
+        B.ulysses_plan_set_fused_engine(plan, engine)
+    for engine in (B.ULY_ENGINE_VEC, B.ULY_ENGINE_CE, 9, -1):
+        with pytest.raises(B.UlyssesError) as ei:
+            B.ulysses_plan_set_fused_engine(plan, engine)
+        assert ei.value.status == B.ULY_EINVAL
+
+
+def test_fused_kernel_choice():
+    """The fused forward's kernel, decided on the host: the row-block kernel for equal head groups
+    with runs of at most 2,048 bytes and rows of at most 10,240 bytes, else the token units."""
+    def kernel(W, heads, d, dtype="bfloat16", engine=None):
+        plan = B.ulysses_plan(W, 1, [8] * W, heads, d, dtype)
+        if engine is not None:
+            B.ulysses_plan_set_fused_engine(plan, engine)
+        return B.ulysses_plan_fused_kernel(plan)
+
+    T, K = B.ULY_ENGINE_TENSOR, B.ULY_ENGINE_TMA
+    assert kernel(8, [5] * 8, 128) == T                    # Wan-720p: rows of 10,240 bytes
+    assert kernel(4, [4] * 4, 128) == T
+    assert kernel(8, [8] * 8, 64, "float16") == T
+    assert kernel(8, [4] * 8, 256) == K                    # rows of 16,384 bytes
+    assert kernel(8, [4] * 8, 256, engine=T) == T          # forced: it fits (runs of 2,048)
+    assert kernel(5, [9, 8, 8, 8, 7], 128) == K            # unequal head groups
+    assert kernel(5, [9, 8, 8, 8, 7], 128, engine=T) == K  # does not fit: token units
+    assert kernel(2, [9, 9], 128) == K                     # runs of 2,304 bytes
+    assert kernel(8, [5] * 8, 128, engine=K) == K
+    lib = B.library()
+    engine = ctypes.c_int()
+    assert lib.ulysses_plan_fused_kernel(None, ctypes.byref(engine)) == B.ULY_EINVAL
+
+
 def test_auto_engine_argument_errors():
     lib = B.library()
     engine = ctypes.c_int()

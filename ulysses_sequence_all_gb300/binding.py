@@ -28,7 +28,7 @@ DTYPE_CODES = {"uint8": ULY_U8, "float8_e4m3fn": ULY_F8E4M3, "float8_e5m2": ULY_
 EXPORTS = ["ulysses_plan", "ulysses_plan_destroy", "ulysses_plan_set_chunk_bytes",
            "ulysses_plan_set_max_ctas", "ulysses_plan_set_rope_pairs",
            "ulysses_plan_bytes", "ulysses_plan_num_chunks", "ulysses_plan_chunk_rows",
-           "ulysses_plan_auto_engine",
+           "ulysses_plan_auto_engine", "ulysses_plan_set_fused_engine", "ulysses_plan_fused_kernel",
            "ulysses_plan_rank_segments",
            "ulysses_a2a_4d", "ulysses_a2a_4d_engine", "ulysses_a2a_4d_qk_fused",
            "ulysses_a2a_4d_qkv_fused", "ulysses_a2a_4d_packed_fused",
@@ -72,6 +72,8 @@ def _lib():
                                            ctypes.POINTER(_i64)]
         lib.ulysses_plan_num_chunks.argtypes = [_p, ctypes.c_int, ctypes.POINTER(_i64)]
         lib.ulysses_plan_auto_engine.argtypes = [_p, ctypes.POINTER(ctypes.c_int)]
+        lib.ulysses_plan_set_fused_engine.argtypes = [_p, ctypes.c_int]
+        lib.ulysses_plan_fused_kernel.argtypes = [_p, ctypes.POINTER(ctypes.c_int)]
         lib.ulysses_plan_chunk_rows.argtypes = [_p, ctypes.c_int, _i64, ctypes.POINTER(_i64),
                                                 ctypes.POINTER(_i64)]
         lib.ulysses_plan_rank_segments.argtypes = [_p, ctypes.c_int, ctypes.c_int, _p]
@@ -190,6 +192,20 @@ def ulysses_plan_set_rope_pairs(plan: Plan, pairs: int):
 def ulysses_plan_set_max_ctas(plan: Plan, max_ctas: int):
     """Cap the CTAs of every launch with this plan (0: no cap)."""
     _check(_lib().ulysses_plan_set_max_ctas(plan, max_ctas), "ulysses_plan_set_max_ctas")
+
+
+def ulysses_plan_set_fused_engine(plan: Plan, engine: int):
+    """Kernel of the fused forward calls with separate q and k inputs: ULY_ENGINE_AUTO,
+    ULY_ENGINE_TMA (token units) or ULY_ENGINE_TENSOR (row blocks per head group)."""
+    _check(_lib().ulysses_plan_set_fused_engine(plan, engine), "ulysses_plan_set_fused_engine")
+
+
+def ulysses_plan_fused_kernel(plan: Plan) -> int:
+    """The kernel the fused forward with separate q and k takes for this plan: ULY_ENGINE_TENSOR
+    (row blocks through tensor maps) or ULY_ENGINE_TMA (token units)."""
+    e = ctypes.c_int()
+    _check(_lib().ulysses_plan_fused_kernel(plan, ctypes.byref(e)), "ulysses_plan_fused_kernel")
+    return e.value
 
 
 def ulysses_plan_bytes(plan: Plan, mode: int, rank: int):

@@ -16,7 +16,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBRARY = os.path.join(PKG, "libulysses.so")
-SOURCES = ["api.cu", "relayout.cu", "fused_qk.cu", "fused_qk_bwd.cu", "plan.cpp"]
+SOURCES = ["api.cu", "relayout.cu", "fused_qk.cu", "fused_qk_tensor.cu", "fused_qk_bwd.cu",
+           "plan.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -32,6 +32,11 @@ void fused_geometry(const Plan& p, int planes, int64_t* tokens_per_unit, int* st
 cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, int sm_count,
                          int64_t max_grid);
 cudaError_t fused_status(unsigned* status, bool clear);
+bool fused_tensor_fits(const Plan& p);
+bool fused_tensor_preferred(const Plan& p);
+cudaError_t fused_tensor_launch(const Plan& p, const FusedArgs& f, const ChunkRows& rows,
+                                cudaStream_t stream, int device, int sm_count, int64_t max_grid);
+cudaError_t fused_tensor_status(unsigned* status, bool clear);
 void fused_bwd_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages,
                         uint32_t* stage_bytes, int* ctas_per_sm);
 int64_t fused_bwd_grid(const FusedBwdArgs& a, int sm_count, int64_t max_grid);
@@ -360,10 +365,21 @@ int fused_prepare(const Plan& p, const void* const* q_in, const void* const* k_i
     return ULY_OK;
 }
 
+// Whether a fused forward call with separate q and k inputs takes the tensor-map kernel.
+static bool fused_uses_tensor(const Plan& p)
+{
+    if (p.fused_engine == ULY_ENGINE_TMA || !fused_tensor_fits(p)) return false;
+    return p.fused_engine == ULY_ENGINE_TENSOR || fused_tensor_preferred(p);
+}
+
 // One launch of the fused kernel over the given rows of every sequence shard.
 int fused_rows(const Plan& p, FusedArgs* a, int64_t tokens_per_unit, const ChunkRows& rows,
                cudaStream_t stream, const DeviceInfo& dev)
 {
+    if (!a->interleaved && fused_uses_tensor(p)) {
+        cudaError_t e = fused_tensor_launch(p, *a, rows, stream, dev.device, dev.sm_count, p.max_ctas);
+        return e == cudaSuccess ? ULY_OK : cuda_fail(e);
+    }
     if (a->interleaved)
         build_fused_units(p, rows, tokens_per_unit, 2 * tokens_per_unit, a->planes, a);
     else
@@ -800,6 +816,21 @@ int ulysses_plan_set_rope_pairs(ulysses_plan_t plan, int pairs)
     return ULY_OK;
 }
 
+int ulysses_plan_set_fused_engine(ulysses_plan_t plan, int engine)
+{
+    if (!plan || (engine != ULY_ENGINE_AUTO && engine != ULY_ENGINE_TMA && engine != ULY_ENGINE_TENSOR))
+        return ULY_EINVAL;
+    plan->p.fused_engine = engine;
+    return ULY_OK;
+}
+
+int ulysses_plan_fused_kernel(ulysses_plan_t plan, int* engine)
+{
+    if (!plan || !engine) return ULY_EINVAL;
+    *engine = fused_uses_tensor(plan->p) ? ULY_ENGINE_TENSOR : ULY_ENGINE_TMA;
+    return ULY_OK;
+}
+
 int ulysses_plan_set_max_ctas(ulysses_plan_t plan, int64_t max_ctas)
 {
     if (!plan || max_ctas < 0) return ULY_EINVAL;
@@ -1105,11 +1136,12 @@ int ulysses_device_status(unsigned* status)
     if (!status) return ULY_EINVAL;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e);
-    unsigned a = 0, b = 0, c = 0;
+    unsigned a = 0, b = 0, c = 0, t = 0;
     if ((e = relayout_status(&a, true)) != cudaSuccess) return cuda_fail(e);
     if ((e = fused_status(&b, true)) != cudaSuccess) return cuda_fail(e);
     if ((e = fused_bwd_status(&c, true)) != cudaSuccess) return cuda_fail(e);
-    *status = a | b | c;
+    if ((e = fused_tensor_status(&t, true)) != cudaSuccess) return cuda_fail(e);
+    *status = a | b | c | t;
     return *status ? ULY_EDEVICE : ULY_OK;
 }
 

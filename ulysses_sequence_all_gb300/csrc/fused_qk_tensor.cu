@@ -1,0 +1,496 @@
+// fused_qk_tensor.cu -- the fused QK call (mode-0 relayout of q and k with QK RMSNorm + RoPE in the
+// scatter; fast-ulysses 0.1.0, "Fusion examples") with row-block units reordered by a tensor map.
+//
+// The arithmetic is the token-unit kernel's (fused_qk.cu): per head row x of d values at global
+// sequence position p, y = x / sqrt(mean(x^2) + eps) * w, pairs rotated by p * theta^(-2j/d), in
+// fp32, rounded once. What differs is how rows move. A unit is a block of R consecutive rows of
+// one sequence shard and batch index, all N heads, of q and of k. Each tensor's block arrives with
+// ONE tiled tensor-map copy whose map walks the heads as (run, row, head group): the box lands in
+// shared memory group-major, [group][row][run], so each destination rank's rows of the block are
+// already back to back, as its head-side tensor holds them. After the consumers normalise and
+// rotate in place, each (tensor, rank) leaves with one contiguous bulk store of R runs. Per unit
+// 2 copies in and 2 W out, for R tokens (the token-unit kernel: 2 in and 2 W out per token).
+// It needs every head group's run (n d e bytes) equal and at most 2,048 bytes (the box's inner
+// extent); other plans use the token units.
+//
+// Warp roles per CTA: a loader (lane 0 issues the two tensor loads and leaves the unit's record),
+// a storer (one lane per (tensor, rank) store, once the consumers are done; the stage goes back to
+// the loader when the stores have read it), and consumer warps, half on q rows and half on k rows,
+// with the token-unit kernel's row layout (fused_row.cuh: 8 lanes per head row, packed fp32x2
+// arithmetic). The consumers also fill the unit's cos/sin table, shared out among them while the
+// unit's copies are in flight, and meet at a named barrier before using it. Every wait is bounded.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+
+#include "../../include/ulysses.h"
+#include "fused_row.cuh"
+#include "plan.h"
+#include "ptx.cuh"
+#include "tensor_map.h"
+
+namespace uly {
+
+static __device__ unsigned g_fused_tensor_status;
+
+#ifndef ULY_FT_BOX_BYTES  // target bytes of one tensor's box (R whole rows) ...
+#define ULY_FT_BOX_BYTES 24576
+#endif
+#ifndef ULY_FT_MIN_ROWS  // ... but at least this many rows
+#define ULY_FT_MIN_ROWS 3
+#endif
+#ifndef ULY_FT_STAGES
+#define ULY_FT_STAGES 3
+#endif
+#ifndef ULY_FT_CTAS_PER_SM
+#define ULY_FT_CTAS_PER_SM 1
+#endif
+#ifndef ULY_FT_CONSUMER_WARPS
+#define ULY_FT_CONSUMER_WARPS 16
+#endif
+#ifndef ULY_FT_ILP  // head rows in flight per lane group
+#define ULY_FT_ILP 1
+#endif
+constexpr int kFtStages = ULY_FT_STAGES;
+constexpr int kFtConsumerWarps = ULY_FT_CONSUMER_WARPS;
+constexpr int kFtThreads = 32 * (2 + kFtConsumerWarps);
+constexpr int kFtRecordsAt = 128;  // barriers first, then one unit record per stage
+constexpr int kFtTurnsAt = 256;
+constexpr int kFtTableBarrier = 1;  // named barrier of the consumer warps (0 is __syncthreads)
+static_assert(3 * 8 * kFtStages <= kFtRecordsAt, "stage barriers must fit the header");
+static_assert(kFtRecordsAt + 16 * kFtStages <= kFtTurnsAt, "unit records must fit the header");
+static_assert(kFtConsumerWarps % 2 == 0, "consumer warps split evenly between q and k");
+
+struct FusedTensorArgs {
+    CUtensorMap qmap[kMaxW];  // per source shard: (run / 8, rows, W, b), see encode_group_map
+    CUtensorMap kmap[kMaxW];
+    uint8_t* q_out[kMaxW];
+    uint8_t* k_out[kMaxW];
+    const float* rms_w;  // [2][d]
+    int64_t seq_off[kMaxW];
+    int64_t row_lo[kMaxW], rows[kMaxW];  // this launch's rows of shard q
+    int64_t blocks[kMaxW];               // row blocks per batch index of shard q
+    int64_t unit_begin[kMaxW + 1];       // prefix of unit counts over q
+    int64_t S, R, total_units;
+    int32_t W, n;         // ranks; heads per rank (every rank the same)
+    uint32_t run;         // n * d * elem_size: bytes of one rank's part of a row
+    uint32_t box_bytes;   // R * W * run: one tensor's box
+    uint32_t box_stride;  // bytes from a stage's q box to its k box (a multiple of 128)
+    uint32_t stage_bytes;
+    uint32_t table_bytes;  // one stage's cos/sin table: R rows x d/2 pairs x 8 bytes
+    float eps;
+    float turn_hi[kMaxFusedD / 2];  // theta^(-2j/d) / (2 pi) as hi + lo, j < d/2
+    float turn_lo[kMaxFusedD / 2];
+};
+
+struct FtRecord {
+    int64_t head_row0;  // the unit's first row on the head side: bb * S + seq_off(q) + row
+    int32_t nrows;
+    int32_t pad;
+};
+
+struct FtUnit {
+    int q;
+    int64_t bb, i0, nrows;  // i0: first row in this launch's rows of shard q
+};
+
+__device__ __forceinline__ FtUnit ft_decode(const FusedTensorArgs& a, int64_t u)
+{
+    int lo = 0, hi = a.W - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.unit_begin[mid] <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    FtUnit t;
+    t.q = lo;
+    const int64_t local = u - a.unit_begin[lo];
+    const int64_t blocks = a.blocks[lo];
+    t.bb = div_fast(local, blocks);
+    t.i0 = (local - t.bb * blocks) * a.R;
+    t.nrows = min(a.R, a.rows[lo] - t.i0);
+    return t;
+}
+
+// Shared-memory layout (byte offsets), shared by the kernel and its launcher.
+struct FtSmem {
+    int turns, tables, stages, total;
+};
+
+__host__ __device__ inline FtSmem ft_smem_layout(int d, uint32_t table_bytes, uint32_t stage_bytes)
+{
+    auto up = [](int x, int a) { return (x + a - 1) / a * a; };
+    FtSmem m;
+    m.turns = kFtTurnsAt;
+    m.tables = up(m.turns + (d / 2) * 8, 128);
+    m.stages = up(m.tables + kFtStages * int(table_bytes), 1024);
+    m.total = m.stages + kFtStages * int(stage_bytes);
+    return m;
+}
+
+__device__ __forceinline__ bool ft_wait(uint64_t* bar, uint32_t parity)
+{
+    return mbar_wait_bounded_hint<10000>(bar, parity);
+}
+
+template <int D, bool F16, bool HALF_PAIRS>
+__global__ void __launch_bounds__(kFtThreads, ULY_FT_CTAS_PER_SM)
+    fused_qk_tensor_kernel(const __grid_constant__ FusedTensorArgs a)
+{
+    using IO = RowIO<F16, HALF_PAIRS, D, true>;
+    constexpr int G = IO::G;
+    constexpr int H = IO::H;
+    constexpr int HALF = D / 2;
+    constexpr int GPW = 32 / G;  // head rows per warp per slot
+    constexpr int ILP = ULY_FT_ILP;
+    constexpr int PER_STEP = GPW * ILP;
+    constexpr int K = kFtStages;
+    constexpr int NW = kFtConsumerWarps;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const FtSmem L = ft_smem_layout(D, a.table_bytes, a.stage_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // both boxes landed
+    uint64_t* computed = full + K;                       // consumers done with the stage
+    uint64_t* empty = computed + K;                      // the stores have read the stage
+    FtRecord* records = reinterpret_cast<FtRecord*>(smem + kFtRecordsAt);
+    float2* turns = reinterpret_cast<float2*>(smem + L.turns);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    const int64_t n = first < a.total_units ? (a.total_units - 1 - first) / step + 1 : 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < K; ++s) {
+            mbar_init(&full[s], 1);  // the loader's expect_tx
+            mbar_init(&computed[s], NW);
+            mbar_init(&empty[s], 1);
+        }
+        fence_barrier_init();
+    }
+    for (int j = threadIdx.x; j < HALF; j += blockDim.x)
+        turns[j] = make_float2(a.turn_hi[j], a.turn_lo[j]);
+    __syncthreads();
+    if (n == 0) return;
+
+    if (warp == 0) {  // loader
+        int64_t j = 0;
+        StageRing ring;
+        for (; j < n; ++j, ring.next(K)) {
+            const int s = ring.s;
+            int ok = 1;
+            if (lane == 0 && j >= K) ok = ft_wait(&empty[s], ring.phase ^ 1u);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                if (lane == 0) atomicOr(&g_fused_tensor_status, kStatusWaitTimeout);
+                break;
+            }
+            if (lane == 0) {
+                const FtUnit t = ft_decode(a, first + j * step);
+                uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
+                mbar_arrive_expect_tx(&full[s], 2 * a.box_bytes);  // rows past the chunk arrive filled
+                tensor_g2s_4d(dst, &a.qmap[t.q], 0, int(t.i0), 0, int(t.bb), &full[s]);
+                tensor_g2s_4d(dst + a.box_stride, &a.kmap[t.q], 0, int(t.i0), 0, int(t.bb), &full[s]);
+                FtRecord& rec = records[s];  // published by this lane's arrive
+                rec.head_row0 = t.bb * a.S + a.seq_off[t.q] + a.row_lo[t.q] + t.i0;
+                rec.nrows = int(t.nrows);
+            }
+            __syncwarp();
+        }
+        // do not leave while copies into this CTA's shared memory may be in flight
+        if (lane == 0) {
+            for (int64_t jj = (j > K ? j - K : 0); jj < j; ++jj) {
+                if (!mbar_wait_bounded(&full[jj % K], uint32_t((jj / K) & 1))) {
+                    atomicOr(&g_fused_tensor_status, kStatusDrainTimeout);
+                    break;
+                }
+            }
+        }
+        return;
+    }
+
+    if (warp == 1) {  // storer: lane c < 2 W stores tensor c / W's rows for rank c % W
+        StageRing ring;
+        for (int64_t j = 0; j < n; ++j, ring.next(K)) {
+            const int s = ring.s;
+            if (!__all_sync(0xffffffffu, ft_wait(&computed[s], ring.phase))) {
+                if (lane == 0) atomicOr(&g_fused_tensor_status, kStatusWaitTimeout);
+                break;
+            }
+            if (lane < 2 * a.W) {
+                const FtRecord rec = records[s];
+                const int t = lane >= a.W, r = lane - t * a.W;
+                const uint8_t* src = smem + L.stages + size_t(s) * a.stage_bytes +
+                                     t * a.box_stride + size_t(r) * a.R * a.run;
+                uint8_t* dst = (t ? a.k_out[r] : a.q_out[r]) + rec.head_row0 * a.run;
+                bulk_s2g(dst, src, uint32_t(rec.nrows) * a.run);
+                bulk_commit();
+                bulk_wait_read<0>();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        bulk_wait<0>();
+        return;
+    }
+
+    // consumers: the first half of the warps normalise q rows, the second half k rows
+    constexpr int HALF_NW = NW / 2;
+    const int cw = warp - 2;
+    const int which = cw >= HALF_NW;       // 0: q, 1: k (uniform per warp)
+    const int cwi = cw - which * HALF_NW;  // rank among the warps of this tensor
+    const int sub = lane % G;              // which pairs of the row this lane holds
+    const int group = lane / G;            // which head row of the warp slot
+    float2 wE[H], wO[H], wOn[H];
+    IO::weights(a.rms_w + which * D, sub, wE, wO);
+    for (int h = 0; h < H; ++h) wOn[h] = make_float2(-wO[h].x, -wO[h].y);
+    const float inv_d = 1.0f / float(D);
+    const int ctid = cw * 32 + lane;  // rank among the consumer threads
+    const int nr = a.n, R = int(a.R), W = a.W;
+    const int run = int(a.run);
+    // A box's head rows in order: (group g, row i, head h) at ((g R + i) n + h); this warp's
+    // share of the steps of PER_STEP rows, the same for every unit (short units skip the rows
+    // past their end).
+    const int box_rows = W * R * nr;
+    const int steps = (box_rows + PER_STEP - 1) / PER_STEP;
+    const int m_lo = cwi * steps / HALF_NW, m_hi = (cwi + 1) * steps / HALF_NW;
+    const int start = m_lo * PER_STEP;
+    const int start_pt = start / nr;  // pseudo-token g R + i of the first row, and its head
+    const int start_head = start - start_pt * nr;
+    const int start_g = start_pt / R, start_i = start_pt - start_g * R;
+    // Every consumer warp passes the per-unit barrier n times: a warp whose wait timed out keeps
+    // going round with its waits and work skipped (the status word records it), so the others
+    // never wait at the barrier for a warp that has left.
+    bool failed = false;
+    StageRing ring;
+    for (int64_t k = 0; k < n; ++k, ring.next(K)) {
+        const int s = ring.s;
+        // The unit's cos/sin table, shared out over the consumer threads while its copies fly:
+        // rows i0 .. i0 + nrows - 1 sit at global positions p0 + i. The slot was last read for
+        // unit k - K, which every consumer warp finished before the barrier of unit k - 1.
+        const FtUnit t = ft_decode(a, first + k * step);
+        const int nrows = int(t.nrows);
+        {
+            float* table = reinterpret_cast<float*>(smem + L.tables + s * a.table_bytes);
+            const float p0 = float(a.seq_off[t.q] + a.row_lo[t.q] + t.i0);
+            for (int e = ctid; e < nrows * HALF; e += NW * 32) {
+                const int tok = e / HALF, jj = e - tok * HALF;
+                const float2 tj = turns[jj];
+                const float2 cs = rope_cos_sin(p0 + float(tok), tj.x, tj.y);
+                const int at = IO::table_at(tok, jj);
+                table[at] = cs.x;
+                table[at + 2] = cs.y;
+            }
+        }
+        asm volatile("bar.sync %0, %1;" ::"r"(kFtTableBarrier), "r"(NW * 32) : "memory");
+        if (!failed && !__all_sync(0xffffffffu, ft_wait(&full[s], ring.phase))) {
+            if (lane == 0) atomicOr(&g_fused_tensor_status, kStatusWaitTimeout);
+            failed = true;
+        }
+        if (failed) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&computed[s]);
+            continue;
+        }
+        uint8_t* rows_base = smem + L.stages + size_t(s) * a.stage_bytes + which * a.box_stride;
+        const float4* table = reinterpret_cast<const float4*>(smem + L.tables + s * a.table_bytes);
+        int bg = start_g, bi = start_i, bh = start_head;  // (group, row, head) of the step's first row
+        for (int m = m_lo; m < m_hi; ++m) {
+            uint8_t* slot[ILP];
+            int tok[ILP];
+            bool ok[ILP];
+            float2 vE[ILP][H], vO[ILP][H];
+            float ss[ILP];
+#pragma unroll
+            for (int u = 0; u < ILP; ++u) {
+                int hh = bh + u * GPW + group, ii = bi, gg = bg;
+                while (hh >= nr) {
+                    hh -= nr;
+                    if (++ii == R) {
+                        ii = 0;
+                        ++gg;
+                    }
+                }
+                ok[u] = gg < W && ii < nrows;
+                slot[u] = rows_base + (gg * R + ii) * run + hh * (D * 2);
+                tok[u] = ii;
+                typename IO::Words x = {};
+                if (ok[u]) x = IO::load(slot[u], sub);
+                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    IO::unpack(x, h, vE[u][h], vO[u][h]);
+                    acc = __ffma2_rn(vE[u][h], vE[u][h], acc);
+                    acc = __ffma2_rn(vO[u][h], vO[u][h], acc);
+                }
+                ss[u] = acc.x + acc.y;
+            }
+#pragma unroll
+            for (int off = G / 2; off > 0; off >>= 1) {
+#pragma unroll
+                for (int u = 0; u < ILP; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], off);
+            }
+#pragma unroll
+            for (int u = 0; u < ILP; ++u) {
+                if (!ok[u]) continue;
+                const float inv = rsqrtf(ss[u] * inv_d + a.eps);
+                const float2 inv2 = make_float2(inv, inv);
+                float2 oEs[H], oOs[H];
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const float4 cs = table[IO::table_entry(tok[u], h, sub)];
+                    const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
+                    const float2 A = __fmul2_rn(vE[u][h], wE[h]);
+                    const float2 Bp = __fmul2_rn(vO[u][h], wO[h]);
+                    const float2 Bn = __fmul2_rn(vO[u][h], wOn[h]);
+                    oEs[h] = __fmul2_rn(__ffma2_rn(Bn, s2, __fmul2_rn(A, c2)), inv2);
+                    oOs[h] = __fmul2_rn(__ffma2_rn(A, s2, __fmul2_rn(Bp, c2)), inv2);
+                }
+                IO::store(slot[u], sub, IO::pack(oEs, oOs));  // in place
+            }
+            bh += PER_STEP;
+            while (bh >= nr) {
+                bh -= nr;
+                if (++bi == R) {
+                    bi = 0;
+                    ++bg;
+                }
+            }
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&computed[s]);
+    }
+}
+
+// Whether this kernel takes the plan: every head group's run the same length, at most 2,048
+// bytes (the tensor box's inner extent), and no empty group.
+bool fused_tensor_fits(const Plan& p)
+{
+    const int64_t run = p.n[0] * p.d * p.e;
+    if (run == 0 || run > 2048) return false;
+    for (int r = 1; r < p.W; ++r)
+        if (p.n[r] != p.n[0]) return false;
+    return true;
+}
+
+// The automatic choice between this kernel and the token units. Measured (CUDA events, back to
+// back, 75,600-token plans): this kernel's time per byte depends mostly on its stage size, best
+// at 48-60 KiB (3 stages), i.e. R = max(3, 24 KiB / row) rows; where three rows of q and k take
+// at most 60 KiB (rows of N d e <= 10,240 bytes) it ran at 0.94-1.02 of the copy peak against
+// the token units' 0.83-0.98, and with longer rows (fewer than 3 rows per box) below them.
+bool fused_tensor_preferred(const Plan& p)
+{
+    return fused_tensor_fits(p) && p.N * p.d * p.e <= 10240;
+}
+
+// per device: the kernel variants whose shared-memory limit has been raised (any host thread)
+static std::atomic<unsigned> g_ft_smem_set[64];
+
+template <int D, bool F16, bool HALF>
+static cudaError_t ft_launch_d(const FusedTensorArgs& a, int smem, cudaStream_t stream, int device,
+                               int grid)
+{
+    constexpr int dbit = D == 8 ? 0 : D == 16 ? 1 : D == 32 ? 2 : D == 64 ? 3 : D == 128 ? 4 : 5;
+    constexpr unsigned bit = 1u << (dbit * 4 + (F16 ? 2 : 0) + (HALF ? 1 : 0));
+    if (device >= 0 && device < 64 && !(g_ft_smem_set[device].load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(fused_qk_tensor_kernel<D, F16, HALF>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemPerCtaMax);
+        if (e != cudaSuccess) return e;
+        g_ft_smem_set[device].fetch_or(bit);
+    }
+    fused_qk_tensor_kernel<D, F16, HALF><<<grid, kFtThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t ft_launch_variant(const FusedTensorArgs& a, bool f16, bool half, int smem,
+                                     cudaStream_t stream, int device, int grid)
+{
+    if (f16)
+        return half ? ft_launch_d<D, true, true>(a, smem, stream, device, grid)
+                    : ft_launch_d<D, true, false>(a, smem, stream, device, grid);
+    return half ? ft_launch_d<D, false, true>(a, smem, stream, device, grid)
+                : ft_launch_d<D, false, false>(a, smem, stream, device, grid);
+}
+
+// One launch over the given rows of every shard (the plan must fit: fused_tensor_fits). `f`
+// holds the call's checked pointers, weights, eps and RoPE turns (fused_prepare).
+cudaError_t fused_tensor_launch(const Plan& p, const FusedArgs& f, const ChunkRows& rows,
+                                cudaStream_t stream, int device, int sm_count, int64_t max_grid)
+{
+    FusedTensorArgs a;
+    std::memset(&a, 0, sizeof a);
+    const int W = p.W;
+    const int64_t de = p.d * p.e;
+    const int64_t run = p.n[0] * de;
+    const int64_t row = W * run;  // N * d * e
+    a.R = ULY_FT_BOX_BYTES / row;
+    if (a.R < ULY_FT_MIN_ROWS) a.R = ULY_FT_MIN_ROWS;
+    if (a.R > 256) a.R = 256;
+    if (a.R < 1) a.R = 1;
+    auto up = [](int64_t x, int64_t m) { return (x + m - 1) / m * m; };
+    for (;; --a.R) {  // the largest block of rows whose stages fit one CTA's shared memory
+        a.box_bytes = uint32_t(a.R * row);
+        a.box_stride = uint32_t(up(a.box_bytes, 128));
+        a.stage_bytes = 2 * a.box_stride;
+        a.table_bytes = uint32_t(up(a.R * (p.d / 2) * 8, 128));
+        if (ft_smem_layout(int(p.d), a.table_bytes, a.stage_bytes).total <= kSmemPerCtaMax) break;
+        if (a.R == 1) return cudaErrorInvalidValue;
+    }
+    const int smem = ft_smem_layout(int(p.d), a.table_bytes, a.stage_bytes).total;
+    a.W = W;
+    a.n = int32_t(p.n[0]);
+    a.run = uint32_t(run);
+    a.S = p.S;
+    a.rms_w = f.rms_w;
+    a.eps = f.eps;
+    std::memcpy(a.turn_hi, f.turn_hi, sizeof a.turn_hi);
+    std::memcpy(a.turn_lo, f.turn_lo, sizeof a.turn_lo);
+    int64_t total = 0;
+    for (int k = 0; k < kMaxW; ++k) {
+        const bool live = k < W;
+        a.q_out[k] = live ? f.q_out[k] : nullptr;
+        a.k_out[k] = live ? f.k_out[k] : nullptr;
+        a.seq_off[k] = live ? p.seq_off[k] : 0;
+        a.row_lo[k] = live ? rows.lo[k] : 0;
+        a.rows[k] = live ? rows.cnt[k] : 0;
+        a.blocks[k] = (a.rows[k] + a.R - 1) / a.R;
+        a.unit_begin[k] = total;
+        total += p.b * a.blocks[k];
+    }
+    a.unit_begin[kMaxW] = total;
+    a.total_units = total;
+    if (total == 0) return cudaSuccess;
+    for (int q = 0; q < W; ++q) {
+        if (a.rows[q] == 0) continue;
+        const int64_t off = a.row_lo[q] * row;
+        const int64_t bs = p.s[q] * row;
+        if (!encode_group_map(&a.qmap[q], f.q_in[q] + off, run, a.rows[q], W, p.b, row, bs, a.R) ||
+            !encode_group_map(&a.kmap[q], f.k_in[q] + off, run, a.rows[q], W, p.b, row, bs, a.R))
+            return cudaErrorInvalidValue;
+    }
+    int64_t grid = int64_t(sm_count) * ULY_FT_CTAS_PER_SM;
+    if (max_grid > 0 && grid > max_grid) grid = max_grid;
+    if (grid > total) grid = total;
+    const bool f16 = f.elem_f16 != 0, half = f.rope_half != 0;
+    switch (p.d) {
+        case 8: return ft_launch_variant<8>(a, f16, half, smem, stream, device, int(grid));
+        case 16: return ft_launch_variant<16>(a, f16, half, smem, stream, device, int(grid));
+        case 32: return ft_launch_variant<32>(a, f16, half, smem, stream, device, int(grid));
+        case 64: return ft_launch_variant<64>(a, f16, half, smem, stream, device, int(grid));
+        case 128: return ft_launch_variant<128>(a, f16, half, smem, stream, device, int(grid));
+        case 256: return ft_launch_variant<256>(a, f16, half, smem, stream, device, int(grid));
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t fused_tensor_status(unsigned* status, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_fused_tensor_status, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_fused_tensor_status, &zero, sizeof(unsigned));
+}
+
+}  // namespace uly

@@ -65,6 +65,7 @@ int plan_init(Plan* p, int W, int64_t b, const int64_t* seq_splits, const int64_
     p->chunk_cap = int64_t(1) << 30;
     p->max_ctas = 0;
     p->rope_half = 0;
+    p->fused_engine = 0;
     return ULY_OK;
 }
 

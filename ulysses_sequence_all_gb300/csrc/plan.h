@@ -19,6 +19,7 @@ struct Plan {
     int64_t chunk_cap;  // max bytes one rank reads or writes per launch
     int64_t max_ctas;   // cap on the CTAs of any launch (0: none)
     int rope_half;      // the fused calls' RoPE pairs: (j, j + d/2) when set, else (2j, 2j + 1)
+    int fused_engine;   // the fused forward's kernel: ULY_ENGINE_AUTO, _TMA (token units), _TENSOR
 };
 
 // Rows of each sequence shard covered by one launch.

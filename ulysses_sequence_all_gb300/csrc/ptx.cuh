@@ -160,6 +160,17 @@ __device__ __forceinline__ void tensor_g2s_3d(void* dst_smem, const void* map, i
         : "memory");
 }
 
+// The same for a 4-D map: coordinates (c0, c1, c2, c3), c0 the innermost.
+__device__ __forceinline__ void tensor_g2s_4d(void* dst_smem, const void* map, int c0, int c1,
+                                              int c2, int c3, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst_smem)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Tiled tensor copy shared -> global of one box, tracked by this thread's bulk async-groups; the
 // parts of the box outside the tensor's extent are not written.
 __device__ __forceinline__ void tensor_s2g_3d(const void* map, int c0, int c1, int c2,

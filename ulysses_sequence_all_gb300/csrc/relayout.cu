@@ -15,7 +15,6 @@
 //    the bytes; the SM only issues copies.
 //  * VEC: a grid-stride loop of warps, 16-byte vector loads (L1 no-allocate) and stores, several
 //    in flight per lane.
-#include <cuda.h>  // CUtensorMap and its encoder's types (the encoder itself is fetched at run time)
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -25,6 +24,7 @@
 #include "../../include/ulysses.h"
 #include "plan.h"
 #include "ptx.cuh"
+#include "tensor_map.h"
 
 namespace uly {
 
@@ -556,6 +556,36 @@ static EncodeTiledFn encode_tiled_fn()
     return fn;
 }
 
+bool encode_run_map(CUtensorMap* map, const void* base, int64_t run, int64_t rows, int64_t b,
+                    int64_t row_stride, int64_t batch_stride, int64_t box_rows)
+{
+    EncodeTiledFn encode = encode_tiled_fn();
+    if (!encode) return false;
+    const cuuint64_t dims[3] = {cuuint64_t(run / 8), cuuint64_t(rows), cuuint64_t(b)};
+    const cuuint64_t strides[2] = {cuuint64_t(row_stride), cuuint64_t(batch_stride)};
+    const cuuint32_t boxdim[3] = {cuuint32_t(run / 8), cuuint32_t(box_rows), 1};
+    const cuuint32_t estrides[3] = {1, 1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void*>(base), dims, strides,
+                  boxdim, estrides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_group_map(CUtensorMap* map, const void* base, int64_t run, int64_t rows, int64_t W,
+                      int64_t b, int64_t row_stride, int64_t batch_stride, int64_t box_rows)
+{
+    EncodeTiledFn encode = encode_tiled_fn();
+    if (!encode) return false;
+    const cuuint64_t dims[4] = {cuuint64_t(run / 8), cuuint64_t(rows), cuuint64_t(W), cuuint64_t(b)};
+    const cuuint64_t strides[3] = {cuuint64_t(row_stride), cuuint64_t(run), cuuint64_t(batch_stride)};
+    const cuuint32_t boxdim[4] = {cuuint32_t(run / 8), cuuint32_t(box_rows), cuuint32_t(W), 1};
+    const cuuint32_t estrides[4] = {1, 1, 1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, const_cast<void*>(base), dims, strides,
+                  boxdim, estrides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int MODE, int K, int UNIT, int L>
 static cudaError_t tensor_launch_shape(const TensorArgs& a, unsigned grid, cudaStream_t stream,
                                        int device)
@@ -659,22 +689,14 @@ cudaError_t relayout_tensor_launch(const Plan& p, const ChunkRows& rows, uint8_t
     a.unit_begin[kMaxW] = total;
     a.total_units = total;
     if (total == 0) return cudaSuccess;
-    EncodeTiledFn encode = encode_tiled_fn();
-    if (!encode) return cudaErrorNotSupported;
     for (int q = 0; q < W; ++q) {
         for (int r = 0; r < W; ++r) {
             const int64_t run = a.n[r] * de;
             if (a.rows[q] == 0 || run == 0) continue;
-            uint8_t* base = a.seq_ptr[q] + (a.row_lo[q] * a.N + a.head_off[r]) * de;
-            const cuuint64_t dims[3] = {cuuint64_t(run / 8), cuuint64_t(a.rows[q]), cuuint64_t(a.b)};
-            const cuuint64_t strides[2] = {cuuint64_t(a.N * de), cuuint64_t(a.s[q] * a.N * de)};
-            const cuuint32_t boxdim[3] = {cuuint32_t(run / 8), cuuint32_t(a.R), 1};
-            const cuuint32_t estrides[3] = {1, 1, 1};
-            const CUresult rc = encode(&a.map[q * W + r], CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, base,
-                                       dims, strides, boxdim, estrides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-            if (rc != CUDA_SUCCESS) return cudaErrorInvalidValue;
+            const uint8_t* base = a.seq_ptr[q] + (a.row_lo[q] * a.N + a.head_off[r]) * de;
+            if (!encode_run_map(&a.map[q * W + r], base, run, a.rows[q], a.b, a.N * de,
+                                a.s[q] * a.N * de, a.R))
+                return cudaErrorInvalidValue;
         }
     }
     if (grid > a.total_units) grid = a.total_units;
