@@ -131,19 +131,20 @@ int ulysses_plan_set_chunk_bytes(ulysses_plan_t plan, int64_t max_chunk_bytes);
  */
 int ulysses_plan_set_max_ctas(ulysses_plan_t plan, int64_t max_ctas);
 
-/* Kernel of the fused forward calls with separate q and k inputs (ulysses_a2a_4d_qk_fused and
- * its host-buffer form) made with this plan: ULY_ENGINE_TMA, units of whole tokens (one bulk
+/* Kernel of the fused forward calls (ulysses_a2a_4d_qk_fused, its host-buffer form, and the
+ * packed forms ulysses_a2a_4d_qkv_fused / ulysses_a2a_4d_packed_fused) made with this plan: ULY_ENGINE_TMA, units of whole tokens (one bulk
  * copy in per tensor, one out per (token, tensor, destination rank)); ULY_ENGINE_TENSOR, units of
  * a block of whole rows (one tiled tensor-map copy in per tensor that lands the rows grouped by
  * destination rank, one bulk copy out per (tensor, rank)), for plans whose head groups all have
  * the same run n * d * elem_size of at most 2048 bytes (other plans use the token units);
  * ULY_ENGINE_AUTO (the default) takes the tensor-map kernel where it fits and a row
  * (N * d * elem_size) is at most 10,240 bytes, where it measured faster, else the token units.
- * All give the same bytes. Packed calls always use the token units. ULY_EINVAL for another
- * engine. Must not race with launches using the plan. */
+ * All give the same bytes. The setting applies to the packed calls too (their q and k planes as
+ * above, the other planes moved in blocks of 2R rows). ULY_EINVAL for another engine. Must not
+ * race with launches using the plan. */
 int ulysses_plan_set_fused_engine(ulysses_plan_t plan, int engine);
 
-/* The kernel that a fused forward call with separate q and k inputs takes for this plan, after
+/* The kernel that a fused forward call (separate or packed inputs) takes for this plan, after
  * its fused-engine setting: ULY_ENGINE_TENSOR (row blocks through tensor maps) or ULY_ENGINE_TMA
  * (token units). No CUDA call. ULY_EINVAL for a null plan or engine pointer. */
 int ulysses_plan_fused_kernel(ulysses_plan_t plan, int* engine);

@@ -206,10 +206,13 @@ def test_fused_long_sequence_full(oracle):
         del ref
 
 
-def test_packed_qkvg_wan720p_full(oracle):
+@pytest.mark.parametrize("engine", [B.ULY_ENGINE_AUTO, B.ULY_ENGINE_TMA], ids=["auto", "tokens"])
+def test_packed_qkvg_wan720p_full(oracle, engine):
     """QKVG packed as (b, s, 4, N, d) (q, k, v of the step, seeds 3, 4, 5, and a gate plane, seed
-    6): one call; every element of q and k, v and g byte for byte."""
+    6): one call; every element of q and k, v and g byte for byte (the automatic choice, row
+    blocks at this shape, and the token units)."""
     cfg, plan = _wan_plan()
+    B.ulysses_plan_set_fused_engine(plan, engine)
     planes = [wl.seq_side_inputs(cfg, "cuda", seed=sd) for sd in (3, 4, 5, 6)]
     packed = [torch.stack(list(p), dim=2) for p in zip(*planes)]
     w = wl.rms_weights(cfg.d, seed=2).cuda()

@@ -36,7 +36,14 @@ CASES = [
     ((8, 1, [64] * 8, [5] * 8, 128), 8, 1, 2, 24),                 # eight planes
     ((2, 1, [75000, 600], [1, 1], 128), 4, 0, 1, 0),               # positions to 75,599
     ((2, 1, [3, 2], [64, 64], 128), 3, 1, 0, 0),                   # wide rows: fewer CTAs per SM
+    # equal head groups: the shapes the row-block (tensor-map) kernel takes
+    ((3, 2, [5, 0, 7], [2, 2, 2], 64), 4, 2, 0, 8),
+    ((4, 2, [3, 1, 0, 2], [1, 1, 1, 1], 16), 6, 5, 2, 16),
+    ((8, 1, [37, 41, 29, 33, 40, 35, 31, 38], [5] * 8, 128), 3, 0, 1, 0),
+    ((4, 1, [300, 280, 310, 290], [4] * 4, 128), 5, 3, 1, 8),
 ]
+
+ENGINES = {"tokens": B.ULY_ENGINE_TMA, "tensor": B.ULY_ENGINE_TENSOR}
 
 
 def _packed_inputs(g, planes, extra, seed, dtype=torch.bfloat16):
@@ -56,9 +63,10 @@ def _plane(xs, c, N, d):
 
 
 def run_packed(g, planes, q_plane, k_plane, xs, pitch_elems, w, dtype=torch.bfloat16, cap=None,
-               half=False):
+               half=False, engine=B.ULY_ENGINE_AUTO):
     W, b, seq, heads, d = g
     plan = B.ulysses_plan(W, b, seq, heads, d, "float16" if dtype == torch.float16 else "bfloat16")
+    B.ulysses_plan_set_fused_engine(plan, engine)
     if half:
         B.ulysses_plan_set_rope_pairs(plan, B.ULY_ROPE_HALF)
     if cap is not None:
@@ -71,13 +79,14 @@ def run_packed(g, planes, q_plane, k_plane, xs, pitch_elems, w, dtype=torch.bflo
     return [o.tensors for o in outs]
 
 
+@pytest.mark.parametrize("engine", list(ENGINES))
 @pytest.mark.parametrize("case", CASES, ids=[f"p{i}" for i in range(len(CASES))])
-def test_packed_full(oracle, case):
+def test_packed_full(oracle, case, engine):
     g, planes, qp, kp, extra = case
     W, b, seq, heads, d = g
     xs, pitch = _packed_inputs(g, planes, extra, seed=sum(seq) + planes)
     w = wl.rms_weights(d, seed=planes + 1).cuda()
-    outs = run_packed(g, planes, qp, kp, xs, pitch, w)
+    outs = run_packed(g, planes, qp, kp, xs, pitch, w, engine=ENGINES[engine])
     wn = w.cpu().numpy().astype(np.float64)
     qo, ko, plain = oracle.packed_fused([host_raw(x) for x in xs], seq, heads, d, planes, qp, kp,
                                         pitch, wn[0], wn[1], EPS, THETA)
@@ -89,15 +98,16 @@ def test_packed_full(oracle, case):
                 assert np.array_equal(host_raw(outs[c][r]), plain[c][r]), f"{case} plane {c} rank {r}"
 
 
-def test_packed_matches_separate_calls():
+@pytest.mark.parametrize("engine", list(ENGINES))
+def test_packed_matches_separate_calls(engine):
     """QKVG packed in one tensor gives, byte for byte, what the separate fused call on its q and k
-    planes and mode 0 of its v and g planes give."""
+    planes and mode 0 of its v and g planes give, on either kernel."""
     g = (8, 1, [300] * 8, [5] * 8, 128)
     W, b, seq, heads, d = g
     N = sum(heads)
     xs, pitch = _packed_inputs(g, 4, 0, seed=41)
     w = wl.rms_weights(d, seed=42).cuda()
-    outs = run_packed(g, 4, 0, 1, xs, pitch, w)
+    outs = run_packed(g, 4, 0, 1, xs, pitch, w, engine=ENGINES[engine])
     plan = B.ulysses_plan(*g, "bfloat16")
     sl = lambda c: [x[:, :, c * N * d:(c + 1) * N * d].reshape(b, x.shape[1], N, d).contiguous()  # noqa: E731
                     for x in xs]
@@ -129,8 +139,10 @@ def test_packed_qkv_equals_interleaved_call():
             assert torch.equal(a.view(torch.int16), b_.view(torch.int16)), f"plane {c}"
 
 
-def test_packed_chunked_equals_unchunked():
-    g = (5, 2, [300, 310, 290, 305, 295], [9, 8, 8, 8, 7], 128)
+@pytest.mark.parametrize("g", [(5, 2, [300, 310, 290, 305, 295], [9, 8, 8, 8, 7], 128),
+                               (5, 2, [300, 310, 290, 305, 295], [8] * 5, 128)],
+                         ids=["uneven_heads", "equal_heads"])
+def test_packed_chunked_equals_unchunked(g):
     xs, pitch = _packed_inputs(g, 4, 16, seed=45)
     w = wl.rms_weights(g[4], seed=46).cuda()
     a = run_packed(g, 4, 2, 0, xs, pitch, w)
@@ -140,12 +152,13 @@ def test_packed_chunked_equals_unchunked():
             assert torch.equal(x.view(torch.int16), y.view(torch.int16))
 
 
+@pytest.mark.parametrize("g", [(3, 2, [5, 0, 7], [3, 2, 1], 64), (3, 2, [5, 0, 7], [2, 2, 2], 64)],
+                         ids=["tokens", "row_blocks"])
 @pytest.mark.parametrize("f16,half", [(1, 1), (0, 1), (1, 0)], ids=["f16-half", "bf16-half", "f16-adj"])
-def test_packed_variants(oracle, f16, half):
+def test_packed_variants(oracle, f16, half, g):
     """fp16 elements and rotate-half pairs: the q and k planes against the oracle's variant of the
     fused call on each plane (the oracle's packed form is the planes' slices through it), the
-    others byte-exact."""
-    g = (3, 2, [5, 0, 7], [3, 2, 1], 64)
+    others byte-exact. Unequal head groups take the token units, equal ones the row blocks."""
     W, b, seq, heads, d = g
     N = sum(heads)
     dtype = torch.float16 if f16 else torch.bfloat16

@@ -202,6 +202,7 @@ def test_fused_kernel_choice():
     assert kernel(5, [9, 8, 8, 8, 7], 128, engine=T) == K  # does not fit: token units
     assert kernel(2, [9, 9], 128) == K                     # runs of 2,304 bytes
     assert kernel(8, [5] * 8, 128, engine=K) == K
+    assert kernel(2, [64, 64], 128, engine=T) == K         # runs of 16 KiB: token units
     lib = B.library()
     engine = ctypes.c_int()
     assert lib.ulysses_plan_fused_kernel(None, ctypes.byref(engine)) == B.ULY_EINVAL

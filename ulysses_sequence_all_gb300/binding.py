@@ -195,7 +195,7 @@ def ulysses_plan_set_max_ctas(plan: Plan, max_ctas: int):
 
 
 def ulysses_plan_set_fused_engine(plan: Plan, engine: int):
-    """Kernel of the fused forward calls with separate q and k inputs: ULY_ENGINE_AUTO,
+    """Kernel of the fused forward calls (separate or packed inputs): ULY_ENGINE_AUTO,
     ULY_ENGINE_TMA (token units) or ULY_ENGINE_TENSOR (row blocks per head group)."""
     _check(_lib().ulysses_plan_set_fused_engine(plan, engine), "ulysses_plan_set_fused_engine")
 

@@ -365,7 +365,7 @@ int fused_prepare(const Plan& p, const void* const* q_in, const void* const* k_i
     return ULY_OK;
 }
 
-// Whether a fused forward call with separate q and k inputs takes the tensor-map kernel.
+// Whether a fused forward call (separate or packed inputs) takes the row-block tensor-map kernel.
 static bool fused_uses_tensor(const Plan& p)
 {
     if (p.fused_engine == ULY_ENGINE_TMA || !fused_tensor_fits(p)) return false;
@@ -376,7 +376,7 @@ static bool fused_uses_tensor(const Plan& p)
 int fused_rows(const Plan& p, FusedArgs* a, int64_t tokens_per_unit, const ChunkRows& rows,
                cudaStream_t stream, const DeviceInfo& dev)
 {
-    if (!a->interleaved && fused_uses_tensor(p)) {
+    if (fused_uses_tensor(p)) {
         cudaError_t e = fused_tensor_launch(p, *a, rows, stream, dev.device, dev.sm_count, p.max_ctas);
         return e == cudaSuccess ? ULY_OK : cuda_fail(e);
     }

@@ -13,6 +13,12 @@
 // It needs every head group's run (n d e bytes) equal and at most 2,048 bytes (the box's inner
 // extent); other plans use the token units.
 //
+// Packed inputs (C planes per token at a token pitch, such as the interleaved (b, s, 3, N, d) QKV
+// or QKVG layouts; FastVideo, "Ulysses performance on GB200") take the same maps with the token
+// pitch as their row stride. Their other planes move without arithmetic in units of 2R rows of
+// one plane (one box of the same bytes as a q,k unit): one copy in, W out. The grid takes every
+// q,k unit first, then each other plane's units in turn.
+//
 // Warp roles per CTA: a loader (lane 0 issues the two tensor loads and leaves the unit's record),
 // a storer (one lane per (tensor, rank) store, once the consumers are done; the stage goes back to
 // the loader when the stores have read it), and consumer warps, half on q rows and half on k rows,
@@ -63,17 +69,26 @@ static_assert(3 * 8 * kFtStages <= kFtRecordsAt, "stage barriers must fit the he
 static_assert(kFtRecordsAt + 16 * kFtStages <= kFtTurnsAt, "unit records must fit the header");
 static_assert(kFtConsumerWarps % 2 == 0, "consumer warps split evenly between q and k");
 
+constexpr int kMaxPlain = kMaxPlanes - 2;  // planes of a packed input other than q and k
+
 struct FusedTensorArgs {
     CUtensorMap qmap[kMaxW];  // per source shard: (run / 8, rows, W, b), see encode_group_map
     CUtensorMap kmap[kMaxW];
+    CUtensorMap pmap[kMaxPlain][kMaxW];  // packed inputs: the other planes, boxes of 2R rows
     uint8_t* q_out[kMaxW];
     uint8_t* k_out[kMaxW];
+    uint8_t* plain_out[kMaxPlain][kMaxW];
     const float* rms_w;  // [2][d]
     int64_t seq_off[kMaxW];
     int64_t row_lo[kMaxW], rows[kMaxW];  // this launch's rows of shard q
-    int64_t blocks[kMaxW];               // row blocks per batch index of shard q
-    int64_t unit_begin[kMaxW + 1];       // prefix of unit counts over q
+    int64_t blocks[kMaxW];               // q,k units: blocks of R rows per batch index of shard q
+    int64_t unit_begin[kMaxW + 1];       // prefix of q,k unit counts over q
+    int64_t blocks2[kMaxW];              // other planes: blocks of 2R rows per batch index
+    int64_t unit_begin2[kMaxW + 1];      // prefix of one plane's unit counts over q
     int64_t S, R, total_units;
+    int64_t qk_units;     // units 0 .. qk_units - 1 are q,k units; then n_plain phases of
+    int64_t plain_units;  // plain_units each
+    int32_t n_plain;
     int32_t W, n;         // ranks; heads per rank (every rank the same)
     uint32_t run;         // n * d * elem_size: bytes of one rank's part of a row
     uint32_t box_bytes;   // R * W * run: one tensor's box
@@ -88,31 +103,44 @@ struct FusedTensorArgs {
 struct FtRecord {
     int64_t head_row0;  // the unit's first row on the head side: bb * S + seq_off(q) + row
     int32_t nrows;
-    int32_t pad;
+    int32_t kind;       // 0: q and k rows; 1 + p: other plane p's rows, moved plain
 };
 
 struct FtUnit {
-    int q;
+    int q, kind;
     int64_t bb, i0, nrows;  // i0: first row in this launch's rows of shard q
 };
 
 __device__ __forceinline__ FtUnit ft_decode(const FusedTensorArgs& a, int64_t u)
 {
+    FtUnit t;
+    t.kind = 0;
+    const int64_t* begin = a.unit_begin;
+    const int64_t* blocks_of = a.blocks;
+    int64_t R = a.R;
+    if (u >= a.qk_units) {  // another plane's unit: blocks of 2R rows
+        const int64_t v = u - a.qk_units;
+        const int64_t p = div_fast(v, a.plain_units);
+        t.kind = int(1 + p);
+        u = v - p * a.plain_units;
+        begin = a.unit_begin2;
+        blocks_of = a.blocks2;
+        R *= 2;
+    }
     int lo = 0, hi = a.W - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (a.unit_begin[mid] <= u)
+        if (begin[mid] <= u)
             lo = mid;
         else
             hi = mid - 1;
     }
-    FtUnit t;
     t.q = lo;
-    const int64_t local = u - a.unit_begin[lo];
-    const int64_t blocks = a.blocks[lo];
+    const int64_t local = u - begin[lo];
+    const int64_t blocks = blocks_of[lo];
     t.bb = div_fast(local, blocks);
-    t.i0 = (local - t.bb * blocks) * a.R;
-    t.nrows = min(a.R, a.rows[lo] - t.i0);
+    t.i0 = (local - t.bb * blocks) * R;
+    t.nrows = min(R, a.rows[lo] - t.i0);
     return t;
 }
 
@@ -187,12 +215,20 @@ __global__ void __launch_bounds__(kFtThreads, ULY_FT_CTAS_PER_SM)
             if (lane == 0) {
                 const FtUnit t = ft_decode(a, first + j * step);
                 uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
-                mbar_arrive_expect_tx(&full[s], 2 * a.box_bytes);  // rows past the chunk arrive filled
-                tensor_g2s_4d(dst, &a.qmap[t.q], 0, int(t.i0), 0, int(t.bb), &full[s]);
-                tensor_g2s_4d(dst + a.box_stride, &a.kmap[t.q], 0, int(t.i0), 0, int(t.bb), &full[s]);
+                // the whole boxes arrive: rows past the chunk are filled
+                mbar_arrive_expect_tx(&full[s], 2 * a.box_bytes);
+                if (t.kind == 0) {
+                    tensor_g2s_4d(dst, &a.qmap[t.q], 0, int(t.i0), 0, int(t.bb), &full[s]);
+                    tensor_g2s_4d(dst + a.box_stride, &a.kmap[t.q], 0, int(t.i0), 0, int(t.bb),
+                                  &full[s]);
+                } else {  // one box of 2R rows, the same bytes
+                    tensor_g2s_4d(dst, &a.pmap[t.kind - 1][t.q], 0, int(t.i0), 0, int(t.bb),
+                                  &full[s]);
+                }
                 FtRecord& rec = records[s];  // published by this lane's arrive
                 rec.head_row0 = t.bb * a.S + a.seq_off[t.q] + a.row_lo[t.q] + t.i0;
                 rec.nrows = int(t.nrows);
+                rec.kind = t.kind;
             }
             __syncwarp();
         }
@@ -208,7 +244,8 @@ __global__ void __launch_bounds__(kFtThreads, ULY_FT_CTAS_PER_SM)
         return;
     }
 
-    if (warp == 1) {  // storer: lane c < 2 W stores tensor c / W's rows for rank c % W
+    if (warp == 1) {  // storer: lane c < 2 W stores tensor c / W's rows for rank c % W (a q,k
+                      // unit), or lane r < W rank r's rows (another plane's unit)
         StageRing ring;
         for (int64_t j = 0; j < n; ++j, ring.next(K)) {
             const int s = ring.s;
@@ -216,12 +253,18 @@ __global__ void __launch_bounds__(kFtThreads, ULY_FT_CTAS_PER_SM)
                 if (lane == 0) atomicOr(&g_fused_tensor_status, kStatusWaitTimeout);
                 break;
             }
-            if (lane < 2 * a.W) {
-                const FtRecord rec = records[s];
+            const FtRecord rec = records[s];
+            const uint8_t* st = smem + L.stages + size_t(s) * a.stage_bytes;
+            if (rec.kind == 0 && lane < 2 * a.W) {
                 const int t = lane >= a.W, r = lane - t * a.W;
-                const uint8_t* src = smem + L.stages + size_t(s) * a.stage_bytes +
-                                     t * a.box_stride + size_t(r) * a.R * a.run;
+                const uint8_t* src = st + t * a.box_stride + size_t(r) * a.R * a.run;
                 uint8_t* dst = (t ? a.k_out[r] : a.q_out[r]) + rec.head_row0 * a.run;
+                bulk_s2g(dst, src, uint32_t(rec.nrows) * a.run);
+                bulk_commit();
+                bulk_wait_read<0>();
+            } else if (rec.kind > 0 && lane < a.W) {
+                const uint8_t* src = st + size_t(lane) * 2 * a.R * a.run;
+                uint8_t* dst = a.plain_out[rec.kind - 1][lane] + rec.head_row0 * a.run;
                 bulk_s2g(dst, src, uint32_t(rec.nrows) * a.run);
                 bulk_commit();
                 bulk_wait_read<0>();
@@ -268,7 +311,7 @@ __global__ void __launch_bounds__(kFtThreads, ULY_FT_CTAS_PER_SM)
         // rows i0 .. i0 + nrows - 1 sit at global positions p0 + i. The slot was last read for
         // unit k - K, which every consumer warp finished before the barrier of unit k - 1.
         const FtUnit t = ft_decode(a, first + k * step);
-        const int nrows = int(t.nrows);
+        const int nrows = t.kind == 0 ? int(t.nrows) : 0;  // another plane's unit: no table
         {
             float* table = reinterpret_cast<float*>(smem + L.tables + s * a.table_bytes);
             const float p0 = float(a.seq_off[t.q] + a.row_lo[t.q] + t.i0);
@@ -286,7 +329,7 @@ __global__ void __launch_bounds__(kFtThreads, ULY_FT_CTAS_PER_SM)
             if (lane == 0) atomicOr(&g_fused_tensor_status, kStatusWaitTimeout);
             failed = true;
         }
-        if (failed) {
+        if (failed || t.kind != 0) {  // nothing to compute
             __syncwarp();
             if (lane == 0) mbar_arrive(&computed[s]);
             continue;
@@ -425,9 +468,12 @@ cudaError_t fused_tensor_launch(const Plan& p, const FusedArgs& f, const ChunkRo
     const int64_t de = p.d * p.e;
     const int64_t run = p.n[0] * de;
     const int64_t row = W * run;  // N * d * e
+    const bool packed = f.interleaved != 0;
+    const int n_plain = packed ? f.planes - 2 : 0;
+    const int64_t pitch = packed ? f.tok_pitch : row;  // bytes from one token to the next
     a.R = ULY_FT_BOX_BYTES / row;
     if (a.R < ULY_FT_MIN_ROWS) a.R = ULY_FT_MIN_ROWS;
-    if (a.R > 256) a.R = 256;
+    if (a.R > 128) a.R = 128;  // a box holds at most 256 rows: 2R for the other planes
     if (a.R < 1) a.R = 1;
     auto up = [](int64_t x, int64_t m) { return (x + m - 1) / m * m; };
     for (;; --a.R) {  // the largest block of rows whose stages fit one CTA's shared memory
@@ -447,29 +493,46 @@ cudaError_t fused_tensor_launch(const Plan& p, const FusedArgs& f, const ChunkRo
     a.eps = f.eps;
     std::memcpy(a.turn_hi, f.turn_hi, sizeof a.turn_hi);
     std::memcpy(a.turn_lo, f.turn_lo, sizeof a.turn_lo);
-    int64_t total = 0;
+    int64_t total = 0, total2 = 0;
     for (int k = 0; k < kMaxW; ++k) {
         const bool live = k < W;
         a.q_out[k] = live ? f.q_out[k] : nullptr;
         a.k_out[k] = live ? f.k_out[k] : nullptr;
+        for (int pp = 0; pp < n_plain; ++pp)
+            a.plain_out[pp][k] = live ? f.plane_out[f.plain_plane[pp]][k] : nullptr;
         a.seq_off[k] = live ? p.seq_off[k] : 0;
         a.row_lo[k] = live ? rows.lo[k] : 0;
         a.rows[k] = live ? rows.cnt[k] : 0;
         a.blocks[k] = (a.rows[k] + a.R - 1) / a.R;
+        a.blocks2[k] = (a.rows[k] + 2 * a.R - 1) / (2 * a.R);
         a.unit_begin[k] = total;
+        a.unit_begin2[k] = total2;
         total += p.b * a.blocks[k];
+        total2 += p.b * a.blocks2[k];
     }
     a.unit_begin[kMaxW] = total;
-    a.total_units = total;
-    if (total == 0) return cudaSuccess;
+    a.unit_begin2[kMaxW] = total2;
+    a.qk_units = total;
+    a.plain_units = total2;
+    a.n_plain = n_plain;
+    a.total_units = total + n_plain * total2;
+    if (a.total_units == 0) return cudaSuccess;
     for (int q = 0; q < W; ++q) {
         if (a.rows[q] == 0) continue;
-        const int64_t off = a.row_lo[q] * row;
-        const int64_t bs = p.s[q] * row;
-        if (!encode_group_map(&a.qmap[q], f.q_in[q] + off, run, a.rows[q], W, p.b, row, bs, a.R) ||
-            !encode_group_map(&a.kmap[q], f.k_in[q] + off, run, a.rows[q], W, p.b, row, bs, a.R))
+        const int64_t off = a.row_lo[q] * pitch;
+        const int64_t bs = p.s[q] * pitch;
+        const uint8_t* qb = packed ? f.packed_in[q] + off + f.q_plane * row : f.q_in[q] + off;
+        const uint8_t* kb = packed ? f.packed_in[q] + off + f.k_plane * row : f.k_in[q] + off;
+        if (!encode_group_map(&a.qmap[q], qb, run, a.rows[q], W, p.b, pitch, bs, a.R) ||
+            !encode_group_map(&a.kmap[q], kb, run, a.rows[q], W, p.b, pitch, bs, a.R))
             return cudaErrorInvalidValue;
+        for (int pp = 0; pp < n_plain; ++pp) {
+            const uint8_t* pb = f.packed_in[q] + off + f.plain_plane[pp] * row;
+            if (!encode_group_map(&a.pmap[pp][q], pb, run, a.rows[q], W, p.b, pitch, bs, 2 * a.R))
+                return cudaErrorInvalidValue;
+        }
     }
+    total = a.total_units;
     int64_t grid = int64_t(sm_count) * ULY_FT_CTAS_PER_SM;
     if (max_grid > 0 && grid > max_grid) grid = max_grid;
     if (grid > total) grid = total;
