@@ -894,6 +894,14 @@ def run_configs(args):
             fn()
         return statistics.median(back_to_back_ms(torch, stream, fn, reps))
 
+    def engine_name(plan):  # the relayout kernel the automatic engine takes
+        return ("tensor" if B.ulysses_plan_auto_engine(plan) == B.ULY_ENGINE_TENSOR
+                else "row_tiles")
+
+    def fused_name(plan):  # the fused forward's kernel
+        return ("row_blocks" if B.ulysses_plan_fused_kernel(plan) == B.ULY_ENGINE_TENSOR
+                else "token_units")
+
     rows = [tiny_latency(torch, B, wl, stream)]
     for cfg in wl.UNEVEN:
         plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
@@ -906,7 +914,8 @@ def run_configs(args):
             ms = timed(lambda: B.ulysses_a2a_4d(plan, mode, ins, outs, stream))
             gbs = nbytes / (ms * 1e-3) / 1e9
             rows.append({"config": cfg.name, "kernel": "relayout", "W": cfg.W,
-                         "dtype": cfg.dtype, "mode": mode, "bytes": nbytes, "median_ms": round(ms, 4), "GB/s": round(gbs, 1),
+                         "dtype": cfg.dtype, "mode": mode, "engine": engine_name(plan),
+                         "bytes": nbytes, "median_ms": round(ms, 4), "GB/s": round(gbs, 1),
                          "frac_of_peak": round(gbs / peak, 4)})
         del seq, head, seq_out
     cfg = wl.LONG_QKV
@@ -954,8 +963,9 @@ def run_configs(args):
         ms = timed(lambda: B.ulysses_a2a_4d_qk_fused(plan, q, k, qo, ko, w, EPS, THETA, stream))
         gbs = 4 * side / (ms * 1e-3) / 1e9
         rows.append({"config": cfg.name, "kernel": "fused_qk", "W": cfg.W, "dtype": cfg.dtype,
-                     "rope_pairs": pairs, "bytes": 4 * side, "median_ms": round(ms, 4),
-                     "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)})
+                     "rope_pairs": pairs, "fused_kernel": fused_name(plan), "bytes": 4 * side,
+                     "median_ms": round(ms, 4), "GB/s": round(gbs, 1),
+                     "frac_of_peak": round(gbs / peak, 4)})
         dq = [torch.empty_like(t) for t in q]
         dk = [torch.empty_like(t) for t in k]
         dw = torch.empty((2, cfg.d), dtype=torch.float32, device="cuda")
@@ -984,7 +994,7 @@ def run_configs(args):
                                                   THETA, stream))
     gbs = 6 * side / (ms * 1e-3) / 1e9
     rows.append({"config": cfg.name, "kernel": "qkv_fused", "W": cfg.W, "dtype": cfg.dtype,
-                 "rope_pairs": "adjacent", "bytes": 6 * side, "median_ms": round(ms, 4),
+                 "rope_pairs": "adjacent", "fused_kernel": fused_name(plan), "bytes": 6 * side, "median_ms": round(ms, 4),
                  "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)})
     dqkv = [torch.empty_like(t) for t in qkv]
     dw = torch.empty((2, cfg.d), dtype=torch.float32, device="cuda")
