@@ -12,10 +12,11 @@ from ulysses_sequence_all_gb300 import binding as B
 pytestmark = pytest.mark.gpu
 
 G = (5, 2, [100, 110, 90, 105, 95], [9, 8, 8, 8, 7], 128)
+G_EQUAL = (5, 2, [100, 110, 90, 105, 95], [8] * 5, 128)  # row-block fused kernel, tensor relayout
 
 
-def _plan(cap):
-    plan = B.ulysses_plan(*G, "bfloat16")
+def _plan(cap, g=G):
+    plan = B.ulysses_plan(*g, "bfloat16")
     B.ulysses_plan_set_max_ctas(plan, cap)
     return plan
 
@@ -39,14 +40,15 @@ def test_relayout_capped_equals_uncapped(engine, cap):
     assert B.ulysses_device_status() == 0
 
 
+@pytest.mark.parametrize("g", [G, G_EQUAL], ids=["uneven_heads", "equal_heads"])
 @pytest.mark.parametrize("cap", [1, 9, 300])
-def test_fused_and_backward_capped(cap):
-    W, b, seq, heads, d = G
-    q, k, w = make_inputs(G, seed=4)
-    dq, dk = make_grads(G, seed=5)
+def test_fused_and_backward_capped(cap, g):
+    W, b, seq, heads, d = g
+    q, k, w = make_inputs(g, seed=4)
+    dq, dk = make_grads(g, seed=5)
     res = []
     for c in (0, cap):
-        plan = _plan(c)
+        plan = _plan(c, g)
         qo = [torch.empty((b, sum(seq), n, d), dtype=torch.bfloat16, device="cuda") for n in heads]
         ko = [torch.empty_like(x) for x in qo]
         B.ulysses_a2a_4d_qk_fused(plan, q, k, qo, ko, w, EPS, THETA)

@@ -29,7 +29,8 @@ def make_case(i):
     """Thread i's geometry and inputs (different splits per thread)."""
     W, b, d = 3, 1, 128
     seq = [200 + 17 * i, 150, 311 - 9 * i]
-    heads = [2 + (i % 2), 3, 1]
+    # odd threads: equal head groups (the tensor-map relayout and the row-block fused kernel)
+    heads = [2, 2, 2] if i % 2 else [2 + (i % 4 == 2), 3, 1]
     N, S = sum(heads), sum(seq)
     gen = torch.Generator(device="cpu")
     gen.manual_seed(500 + i)

@@ -67,8 +67,22 @@ static __device__ unsigned g_fused_bwd_status;
 #ifndef ULY_BWD_WAIT_HINT_NS  // suspend-time hint of the barrier waits (0: plain polling)
 #define ULY_BWD_WAIT_HINT_NS 10000
 #endif
+// Rotate-half pairs take 4 CTAs of 2 stages per SM (128 registers a thread, no spills): measured
+// at the Wan-720p shape 0.984 / 0.977 of the copy peak (bf16 / fp16) against 0.953-0.967 with the
+// adjacent pairs' 3 CTAs of 3 stages, which stay best for those (1.007 / 0.972 against 0.974 /
+// 0.966).
+#ifndef ULY_BWD_CTAS_PER_SM_HALF
+#define ULY_BWD_CTAS_PER_SM_HALF 4
+#endif
+#ifndef ULY_BWD_MAX_STAGES_HALF
+#define ULY_BWD_MAX_STAGES_HALF 2
+#endif
 constexpr int kBwdCtasPerSm = ULY_BWD_CTAS_PER_SM;
 constexpr int kBwdMaxStages = ULY_BWD_MAX_STAGES;
+constexpr int kBwdCtasPerSmHalf = ULY_BWD_CTAS_PER_SM_HALF;
+constexpr int kBwdMaxStagesHalf = ULY_BWD_MAX_STAGES_HALF;
+static_assert(kBwdMaxStagesHalf >= 2 && kBwdMaxStagesHalf <= kBwdMaxStages,
+              "the barrier area holds kBwdMaxStages stages");
 constexpr int kBwdNW = ULY_BWD_CONSUMER_WARPS;
 constexpr int kBwdIlp = ULY_BWD_ILP;  // head rows in flight per lane group
 #ifndef ULY_BWD_ILP_WIDE  // the same for the 8-pair row layout (rotate half), twice the values
@@ -170,7 +184,7 @@ __host__ __device__ inline BwdSmem bwd_smem_layout(int d, int tokens, int stages
 // adjacent pairs). The row layouts (G lanes per row, H packed slots per lane) are in
 // fused_row.cuh.
 template <int D, bool F16, bool HALF_PAIRS>
-__global__ void __launch_bounds__(kBwdThreads, kBwdCtasPerSm)
+__global__ void __launch_bounds__(kBwdThreads, HALF_PAIRS ? kBwdCtasPerSmHalf : kBwdCtasPerSm)
     fused_qk_bwd_kernel(const __grid_constant__ FusedBwdArgs a)
 {
     using IO = RowIO<F16, HALF_PAIRS, D, kBwdWide>;
@@ -518,12 +532,14 @@ void fused_bwd_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages,
     const int64_t tok_bytes = 2 * p.N * p.d * 2;  // one token's input and gradient rows
     int64_t T0 = ULY_BWD_STAGE_TARGET / tok_bytes;
     if (T0 < 1) T0 = 1;
-    for (int ctas = kBwdCtasPerSm; ctas >= 1; --ctas) {
+    const int ctas_max = p.rope_half ? kBwdCtasPerSmHalf : kBwdCtasPerSm;
+    const int stages_max = p.rope_half ? kBwdMaxStagesHalf : kBwdMaxStages;
+    for (int ctas = ctas_max; ctas >= 1; --ctas) {
         const int budget = kSmemPerSm / ctas - kSmemReservedPerCta;
         for (int64_t T = T0; T >= 1; T = T > 1 ? T / 2 : 0) {
             const int64_t sb = T * tok_bytes;
             if (sb >= (1 << 20)) continue;  // an mbarrier counts fewer than 2^20 bytes
-            for (int K = kBwdMaxStages; K >= 2; --K) {
+            for (int K = stages_max; K >= 2; --K) {
                 const BwdSmem m = bwd_smem_layout(int(p.d), int(T), K, uint32_t(sb));
                 if (m.total <= budget && m.total <= kSmemPerCtaMax) {
                     *tokens_per_unit = T;
