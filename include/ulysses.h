@@ -132,7 +132,8 @@ int ulysses_plan_set_chunk_bytes(ulysses_plan_t plan, int64_t max_chunk_bytes);
 int ulysses_plan_set_max_ctas(ulysses_plan_t plan, int64_t max_ctas);
 
 /* Kernel of the fused forward calls (ulysses_a2a_4d_qk_fused, its host-buffer form, and the
- * packed forms ulysses_a2a_4d_qkv_fused / ulysses_a2a_4d_packed_fused) made with this plan: ULY_ENGINE_TMA, units of whole tokens (one bulk
+ * packed forms ulysses_a2a_4d_qkv_fused / ulysses_a2a_4d_packed_fused) made with this plan, and
+ * of their backward (see ulysses_plan_fused_backward_kernel for its automatic choice): ULY_ENGINE_TMA, units of whole tokens (one bulk
  * copy in per tensor, one out per (token, tensor, destination rank)); ULY_ENGINE_TENSOR, units of
  * a block of whole rows (one tiled tensor-map copy in per tensor that lands the rows grouped by
  * destination rank, one bulk copy out per (tensor, rank)), for plans whose head groups all have
@@ -148,6 +149,15 @@ int ulysses_plan_set_fused_engine(ulysses_plan_t plan, int engine);
  * its fused-engine setting: ULY_ENGINE_TENSOR (row blocks through tensor maps) or ULY_ENGINE_TMA
  * (token units). No CUDA call. ULY_EINVAL for a null plan or engine pointer. */
 int ulysses_plan_fused_kernel(ulysses_plan_t plan, int* engine);
+
+/* The same for the backward of the fused call (ulysses_a2a_4d_qk_fused_backward and its packed
+ * and static forms): ULY_ENGINE_TENSOR, units of whole-row blocks whose forward input arrives
+ * through one tiled tensor-map copy grouped by head group and whose gradient rows arrive as one
+ * span per rank; or ULY_ENGINE_TMA, token units. The plan's fused-engine setting applies; under
+ * ULY_ENGINE_AUTO the backward takes row blocks where they fit (equal head groups, runs of at
+ * most 2048 bytes) and a row N * d * elem_size is at least 6,144 bytes, where they measured
+ * faster. No CUDA call. ULY_EINVAL for a null plan or engine pointer. */
+int ulysses_plan_fused_backward_kernel(ulysses_plan_t plan, int* engine);
 
 /* RoPE pair layout (ULY_ROPE_ADJACENT or ULY_ROPE_HALF) of the fused calls made with this plan:
  * the forward, the interleaved QKV form, the host-buffer form and the backward. Default

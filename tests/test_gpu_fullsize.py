@@ -244,10 +244,12 @@ def _wan_grads(cfg, dtype, seeds):
                                             dtype, seed=sd), "cuda") for sd in seeds]
 
 
-def test_backward_wan720p_full(oracle):
+@pytest.mark.parametrize("engine", [B.ULY_ENGINE_AUTO, B.ULY_ENGINE_TMA], ids=["auto", "tokens"])
+def test_backward_wan720p_full(oracle, engine):
     """Backward at the Wan shape on the step's q, k (seeds 3, 4), weights seed 2, output
     gradients N(0, 1) (seeds 52, 53): every element of dq and dk, and dw."""
     cfg, plan = _wan_plan()
+    B.ulysses_plan_set_fused_engine(plan, engine)
     q = wl.seq_side_inputs(cfg, "cuda", seed=3)
     k = wl.seq_side_inputs(cfg, "cuda", seed=4)
     w = wl.rms_weights(cfg.d, seed=2).cuda()
@@ -272,11 +274,13 @@ def test_backward_wan720p_full(oracle):
         _sensitivity(oracle, cfg, x, gy, wn[t], 0, 0, dw_bound(n_rows), f"dw {t}")
 
 
-def test_qkv_backward_wan720p_full(oracle):
+@pytest.mark.parametrize("engine", [B.ULY_ENGINE_AUTO, B.ULY_ENGINE_TMA], ids=["auto", "tokens"])
+def test_qkv_backward_wan720p_full(oracle, engine):
     """Backward of the interleaved call at the Wan shape: packed q, k, v of the step (seeds
     3, 4, 5), output gradients N(0, 1) (seeds 52, 53, 54): every element of the q and k planes of
     dqkv, the v plane byte for byte (mode 1 of its gradient), and dw."""
     cfg, plan = _wan_plan()
+    B.ulysses_plan_set_fused_engine(plan, engine)
     planes = [wl.seq_side_inputs(cfg, "cuda", seed=sd) for sd in (3, 4, 5)]
     qkv = [torch.stack(list(p), dim=2) for p in zip(*planes)]
     w = wl.rms_weights(cfg.d, seed=2).cuda()
@@ -373,10 +377,12 @@ def test_backward_long_sequence_full(oracle):
         _sensitivity(oracle, cfg, x, gy, wn[t], 0, 0, dw_bound(n_rows), f"dw {t}")
 
 
-def test_backward_wan720p_f16_half_full(oracle):
+@pytest.mark.parametrize("engine", [B.ULY_ENGINE_AUTO, B.ULY_ENGINE_TMA], ids=["auto", "tokens"])
+def test_backward_wan720p_f16_half_full(oracle, engine):
     """Backward of the fp16 rotate-half variant at the Wan shape (q, k seeds 3, 4; gradients
     N(0, 1) seeds 52, 53): every element of dq and dk, and dw."""
     cfg, plan = _wan_plan("float16", half=True)
+    B.ulysses_plan_set_fused_engine(plan, engine)
     cfg16 = wl.Workload("wan720p_fp16", cfg.W, 1, cfg.seq_splits, cfg.head_splits, cfg.d,
                         "float16", seed=1)
     q = wl.seq_side_inputs(cfg16, "cuda", seed=3)

@@ -66,9 +66,15 @@ def make_grads(g, seed, device="cuda"):
             [torch.randn((b, S, n, d), generator=gen).to(torch.bfloat16).to(device) for n in heads])
 
 
-def run_bwd(g, q, k, dq, dk, w, cap=None, workspace=None):
+# the backward's units follow the plan's fused-kernel setting: token units, or row blocks
+# grouped by head group (plans with equal head groups)
+ENGINES = {"tokens": B.ULY_ENGINE_TMA, "row_blocks": B.ULY_ENGINE_TENSOR}
+
+
+def run_bwd(g, q, k, dq, dk, w, cap=None, workspace=None, engine=B.ULY_ENGINE_AUTO):
     W, b, seq, heads, d = g
     plan = B.ulysses_plan(W, b, seq, heads, d, "bfloat16")
+    B.ulysses_plan_set_fused_engine(plan, engine)
     if cap is not None:
         B.ulysses_plan_set_chunk_bytes(plan, cap)
     shapes = [(b, s, sum(heads), d) for s in seq]
@@ -86,15 +92,16 @@ def run_bwd(g, q, k, dq, dk, w, cap=None, workspace=None):
     return dqo.tensors, dko.tensors, dwo.tensors[0]
 
 
+@pytest.mark.parametrize("engine", list(ENGINES))
 @pytest.mark.parametrize("g", SMALL, ids=[f"bwd{i}" for i in range(len(SMALL))])
-def test_backward_small(oracle, g):
+def test_backward_small(oracle, g, engine):
     """Every element of dq, dk and dw against the oracle, over several tiles and ragged tails
     (token blocks of up to 160 tokens at small N * d), empty shards and head groups, d 8..256,
     and positions up to 75,599."""
     W, b, seq, heads, d = g
     q, k, w = make_inputs(g, seed=sum(seq) + 3 * d)
     dq, dk = make_grads(g, seed=7 * sum(heads) + d)
-    dqo, dko, dwo = run_bwd(g, q, k, dq, dk, w)
+    dqo, dko, dwo = run_bwd(g, q, k, dq, dk, w, engine=ENGINES[engine])
     wn = w.cpu().numpy().astype(np.float64)
     n_rows = b * sum(seq) * sum(heads)
     for t, (x, gy, got) in enumerate(((q, dq, dqo), (k, dk, dko))):
@@ -105,13 +112,18 @@ def test_backward_small(oracle, g):
         check_dw(dwo[t].cpu().numpy(), ref_dw, n_rows, f"{g} dw {t}")
 
 
-def test_backward_chunked_matches_unchunked(oracle):
+@pytest.mark.parametrize("g", [(5, 2, [100, 110, 90, 105, 95], [9, 8, 8, 8, 7], 128),
+                               (5, 2, [100, 110, 90, 105, 95], [8] * 5, 128)],
+                         ids=["uneven_heads", "equal_heads"])
+def test_backward_chunked_matches_unchunked(oracle, g):
     """Chunking changes no dx byte; dw (summed in another order) stays within the bound."""
-    g = (5, 2, [100, 110, 90, 105, 95], [9, 8, 8, 8, 7], 128)
     q, k, w = make_inputs(g, seed=11)
     dq, dk = make_grads(g, seed=12)
     a = run_bwd(g, q, k, dq, dk, w)
     c = run_bwd(g, q, k, dq, dk, w, cap=1 << 20)
+    t = run_bwd(g, q, k, dq, dk, w, engine=B.ULY_ENGINE_TMA)  # token units: dx the same bytes
+    for x, y in zip(a[0] + a[1], t[0] + t[1]):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
     for x, y in zip(a[0] + a[1], c[0] + c[1]):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
     n_rows = 2 * sum(g[2]) * sum(g[3])

@@ -208,6 +208,27 @@ def test_fused_kernel_choice():
     assert lib.ulysses_plan_fused_kernel(None, ctypes.byref(engine)) == B.ULY_EINVAL
 
 
+def test_fused_backward_kernel_choice():
+    """The backward's kernel: row blocks for equal head groups with runs of at most 2,048 bytes
+    and rows of at least 6,144 bytes, else token units; the plan's setting overrides."""
+    def kernel(W, heads, d, dtype="bfloat16", engine=None):
+        plan = B.ulysses_plan(W, 1, [8] * W, heads, d, dtype)
+        if engine is not None:
+            B.ulysses_plan_set_fused_engine(plan, engine)
+        return B.ulysses_plan_fused_backward_kernel(plan)
+
+    T, K = B.ULY_ENGINE_TENSOR, B.ULY_ENGINE_TMA
+    assert kernel(8, [5] * 8, 128) == T                    # Wan-720p: rows of 10,240 bytes
+    assert kernel(8, [4] * 8, 256) == T                    # rows of 16,384 bytes
+    assert kernel(4, [14] * 4, 64) == T                    # rows of 7,168 bytes
+    assert kernel(4, [4] * 4, 128) == K                    # rows of 4,096 bytes
+    assert kernel(4, [4] * 4, 128, engine=T) == T          # forced: it fits
+    assert kernel(5, [9, 8, 8, 8, 7], 128, engine=T) == K  # unequal head groups
+    assert kernel(8, [5] * 8, 128, engine=K) == K
+    engine = ctypes.c_int()
+    assert B.library().ulysses_plan_fused_backward_kernel(None, ctypes.byref(engine)) == B.ULY_EINVAL
+
+
 def test_auto_engine_argument_errors():
     lib = B.library()
     engine = ctypes.c_int()

@@ -29,6 +29,7 @@ EXPORTS = ["ulysses_plan", "ulysses_plan_destroy", "ulysses_plan_set_chunk_bytes
            "ulysses_plan_set_max_ctas", "ulysses_plan_set_rope_pairs",
            "ulysses_plan_bytes", "ulysses_plan_num_chunks", "ulysses_plan_chunk_rows",
            "ulysses_plan_auto_engine", "ulysses_plan_set_fused_engine", "ulysses_plan_fused_kernel",
+           "ulysses_plan_fused_backward_kernel",
            "ulysses_plan_rank_segments",
            "ulysses_a2a_4d", "ulysses_a2a_4d_engine", "ulysses_a2a_4d_qk_fused",
            "ulysses_a2a_4d_qkv_fused", "ulysses_a2a_4d_packed_fused",
@@ -74,6 +75,7 @@ def _lib():
         lib.ulysses_plan_auto_engine.argtypes = [_p, ctypes.POINTER(ctypes.c_int)]
         lib.ulysses_plan_set_fused_engine.argtypes = [_p, ctypes.c_int]
         lib.ulysses_plan_fused_kernel.argtypes = [_p, ctypes.POINTER(ctypes.c_int)]
+        lib.ulysses_plan_fused_backward_kernel.argtypes = [_p, ctypes.POINTER(ctypes.c_int)]
         lib.ulysses_plan_chunk_rows.argtypes = [_p, ctypes.c_int, _i64, ctypes.POINTER(_i64),
                                                 ctypes.POINTER(_i64)]
         lib.ulysses_plan_rank_segments.argtypes = [_p, ctypes.c_int, ctypes.c_int, _p]
@@ -205,6 +207,15 @@ def ulysses_plan_fused_kernel(plan: Plan) -> int:
     (row blocks through tensor maps) or ULY_ENGINE_TMA (token units)."""
     e = ctypes.c_int()
     _check(_lib().ulysses_plan_fused_kernel(plan, ctypes.byref(e)), "ulysses_plan_fused_kernel")
+    return e.value
+
+
+def ulysses_plan_fused_backward_kernel(plan: Plan) -> int:
+    """The kernel the fused call's backward takes for this plan: ULY_ENGINE_TENSOR (row blocks)
+    or ULY_ENGINE_TMA (token units)."""
+    e = ctypes.c_int()
+    _check(_lib().ulysses_plan_fused_backward_kernel(plan, ctypes.byref(e)),
+           "ulysses_plan_fused_backward_kernel")
     return e.value
 
 

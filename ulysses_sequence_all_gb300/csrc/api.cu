@@ -12,6 +12,7 @@
 
 #include "../../include/ulysses.h"
 #include "plan.h"
+#include "tensor_map.h"
 
 namespace uly {
 int64_t relayout_unit_bytes(int engine);
@@ -37,7 +38,8 @@ bool fused_tensor_preferred(const Plan& p);
 cudaError_t fused_tensor_launch(const Plan& p, const FusedArgs& f, const ChunkRows& rows,
                                 cudaStream_t stream, int device, int sm_count, int64_t max_grid);
 cudaError_t fused_tensor_status(unsigned* status, bool clear);
-void fused_bwd_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages,
+bool fused_bwd_group_major_preferred(const Plan& p);
+void fused_bwd_geometry(const Plan& p, bool group_major, int64_t* tokens_per_unit, int* stages,
                         uint32_t* stage_bytes, int* ctas_per_sm);
 int64_t fused_bwd_grid(const FusedBwdArgs& a, int sm_count, int64_t max_grid);
 cudaError_t fused_bwd_launch(const FusedBwdArgs& a, float* dw, bool accumulate, cudaStream_t stream,
@@ -372,6 +374,14 @@ static bool fused_uses_tensor(const Plan& p)
     return p.fused_engine == ULY_ENGINE_TENSOR || fused_tensor_preferred(p);
 }
 
+// Whether the backward of the fused call takes row blocks grouped by head group: under the
+// plan's fused-kernel setting, where they fit, and under the automatic choice where measured faster.
+static bool fused_bwd_uses_group_major(const Plan& p)
+{
+    if (p.fused_engine == ULY_ENGINE_TMA || !fused_tensor_fits(p)) return false;
+    return p.fused_engine == ULY_ENGINE_TENSOR || fused_bwd_group_major_preferred(p);
+}
+
 // One launch of the fused kernel over the given rows of every sequence shard.
 int fused_rows(const Plan& p, FusedArgs* a, int64_t tokens_per_unit, const ChunkRows& rows,
                cudaStream_t stream, const DeviceInfo& dev)
@@ -419,7 +429,8 @@ int fused_bwd_setup(const Plan& p, const DeviceInfo& dev, int64_t* tokens_per_un
     if (!(p.d == 8 || p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128 || p.d == 256))
         return ULY_EINVAL;
     if (p.S >= (int64_t(1) << 24)) return ULY_EINVAL;  // positions must be exact in fp32
-    fused_bwd_geometry(p, tokens_per_unit, stages, stage_bytes, ctas_per_sm);
+    fused_bwd_geometry(p, fused_bwd_uses_group_major(p), tokens_per_unit, stages, stage_bytes,
+                       ctas_per_sm);
     if (*stages == 0) return ULY_EINVAL;  // one token's rows do not fit the stages
     *workspace_bytes = size_t(dev.sm_count) * size_t(*ctas_per_sm) * size_t(2 * p.d) * sizeof(float);
     return ULY_OK;
@@ -441,11 +452,25 @@ int fused_bwd_run(const Plan& p, FusedBwdArgs& a, const DeviceInfo& dev, int64_t
     a.stages = stages;
     a.stage_bytes = stage_bytes;
     a.ctas_per_sm = ctas_per_sm;
+    a.group_major = fused_bwd_uses_group_major(p) ? 1 : 0;  // the same choice as the geometry's
+    a.n_eq = int32_t(p.n[0]);
+    a.run = uint32_t(p.n[0] * p.d * p.e);
     rope_turns(p.d, double(rope_theta), a.turn_hi, a.turn_lo);
     for (int64_t c = 0; c < C; ++c) {
         ChunkRows rows;
         chunk_rows(p, C, c, &rows);
         build_fused_bwd_units(p, rows, T, &a);
+        if (a.group_major) {  // maps of this launch's rows of the forward inputs
+            for (int t = 0; t < 2; ++t) {
+                for (int q = 0; q < p.W; ++q) {
+                    if (rows.cnt[q] == 0) continue;
+                    if (!encode_group_map(&a.xmap[t][q], a.x_in[t][q] + rows.lo[q] * a.tok_stride,
+                                          a.run, rows.cnt[q], p.W, p.b, a.tok_stride,
+                                          p.s[q] * a.tok_stride, T))
+                        return cuda_fail(cudaErrorInvalidValue);
+                }
+            }
+        }
         cudaError_t e = fused_bwd_launch(a, dw, c > 0, stream, dev.device, dev.sm_count, p.max_ctas);
         if (e != cudaSuccess) return cuda_fail(e);
     }
@@ -828,6 +853,13 @@ int ulysses_plan_fused_kernel(ulysses_plan_t plan, int* engine)
 {
     if (!plan || !engine) return ULY_EINVAL;
     *engine = fused_uses_tensor(plan->p) ? ULY_ENGINE_TENSOR : ULY_ENGINE_TMA;
+    return ULY_OK;
+}
+
+int ulysses_plan_fused_backward_kernel(ulysses_plan_t plan, int* engine)
+{
+    if (!plan || !engine) return ULY_EINVAL;
+    *engine = fused_bwd_uses_group_major(plan->p) ? ULY_ENGINE_TENSOR : ULY_ENGINE_TMA;
     return ULY_OK;
 }
 

@@ -94,8 +94,30 @@ constexpr int kBwdHeader = 256;  // two barriers per stage, then one unit record
 constexpr int kBwdRecordsAt = 128;
 static_assert(2 * 8 * kBwdMaxStages <= kBwdRecordsAt, "stage barriers must fit the header");
 static_assert(kBwdRecordsAt + 16 * kBwdMaxStages <= kBwdHeader, "unit records must fit");
+// Row blocks (group-major units, plans with equal head groups): one CTA per SM with 10 consumer
+// warps, blocks of max(3, ULY_BWD_GM_BYTES / row) rows, 2 stages. Measured at the Wan-720p shape
+// 1.014-1.029 of the copy peak in all four element and pair layouts (token units 0.972-1.004);
+// 8, 9, 12 or 14 consumer warps, 3-row blocks in 3 stages or 2-row blocks measured 0.82-0.98.
+#ifndef ULY_BWD_GM_WARPS
+#define ULY_BWD_GM_WARPS 10
+#endif
+#ifndef ULY_BWD_GM_BYTES
+#define ULY_BWD_GM_BYTES 51200
+#endif
+#ifndef ULY_BWD_GM_MIN_ROWS
+#define ULY_BWD_GM_MIN_ROWS 3
+#endif
+#ifndef ULY_BWD_GM_STAGES
+#define ULY_BWD_GM_STAGES 2
+#endif
+constexpr int kBwdNWGm = ULY_BWD_GM_WARPS;
+static_assert(ULY_BWD_GM_STAGES >= 2 && ULY_BWD_GM_STAGES <= kBwdMaxStages, "stage barriers");
 constexpr int kBwdLoaderWarp = 0, kBwdFirstConsumer = 1;
-constexpr int kBwdThreads = 32 * (kBwdFirstConsumer + kBwdNW);
+__host__ __device__ constexpr int bwd_warps(bool gm) { return gm ? kBwdNWGm : kBwdNW; }
+__host__ __device__ constexpr int bwd_threads(bool gm)
+{
+    return 32 * (kBwdFirstConsumer + bwd_warps(gm));
+}
 constexpr int kBwdConsumerBarrier = 1;  // named barrier of the consumer warps (0: __syncthreads)
 
 struct BwdUnit {
@@ -166,7 +188,7 @@ struct BwdSmem {
 };
 
 __host__ __device__ inline BwdSmem bwd_smem_layout(int d, int tokens, int stages,
-                                                   uint32_t stage_bytes)
+                                                   uint32_t stage_bytes, int nw)
 {
     auto up = [](int x) { return (x + 127) & ~127; };
     BwdSmem m;
@@ -175,7 +197,7 @@ __host__ __device__ inline BwdSmem bwd_smem_layout(int d, int tokens, int stages
     m.table_bytes = up(tokens * (d / 2) * 8);
     m.weights = up(m.tables + stages * m.table_bytes);
     m.red = m.weights + 2 * d * 4;
-    m.stages = up(m.red + kBwdNW * 2 * d * 4);
+    m.stages = up(m.red + nw * 2 * d * 4);
     m.total = m.stages + stages * int(stage_bytes);
     return m;
 }
@@ -183,10 +205,12 @@ __host__ __device__ inline BwdSmem bwd_smem_layout(int d, int tokens, int stages
 // D: head dimension; F16: fp16 elements (else bf16); HALF_PAIRS: rotate-half RoPE pairs (else
 // adjacent pairs). The row layouts (G lanes per row, H packed slots per lane) are in
 // fused_row.cuh.
-template <int D, bool F16, bool HALF_PAIRS>
-__global__ void __launch_bounds__(kBwdThreads, HALF_PAIRS ? kBwdCtasPerSmHalf : kBwdCtasPerSm)
+template <int D, bool F16, bool HALF_PAIRS, bool GM>
+__global__ void __launch_bounds__(bwd_threads(GM),
+                                  GM ? 1 : HALF_PAIRS ? kBwdCtasPerSmHalf : kBwdCtasPerSm)
     fused_qk_bwd_kernel(const __grid_constant__ FusedBwdArgs a)
 {
+    constexpr int kNW = bwd_warps(GM);  // consumer warps
     using IO = RowIO<F16, HALF_PAIRS, D, kBwdWide>;
     using Words = typename IO::Words;
     constexpr int G = IO::G;
@@ -199,7 +223,7 @@ __global__ void __launch_bounds__(kBwdThreads, HALF_PAIRS ? kBwdCtasPerSmHalf : 
     extern __shared__ __align__(1024) uint8_t smem[];
     const int K = a.stages;
     const int N = int(a.N);
-    const BwdSmem L = bwd_smem_layout(D, a.tokens_per_unit, K, a.stage_bytes);
+    const BwdSmem L = bwd_smem_layout(D, a.tokens_per_unit, K, a.stage_bytes, kNW);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // data landed + table written
     uint64_t* empty = full + kBwdMaxStages;              // consumers done with the stage
     float2* turns = reinterpret_cast<float2*>(smem + L.turns);
@@ -212,12 +236,12 @@ __global__ void __launch_bounds__(kBwdThreads, HALF_PAIRS ? kBwdCtasPerSmHalf : 
     if (threadIdx.x == 0) {
         for (int s = 0; s < K; ++s) {
             mbar_init(&full[s], 1 + 32);  // the loader's expect_tx, then its lanes' table writes
-            mbar_init(&empty[s], kBwdNW);
+            mbar_init(&empty[s], kNW);
         }
         fence_barrier_init();
     }
     for (int j = threadIdx.x; j < HALF; j += blockDim.x) turns[j] = make_float2(a.turn_hi[j], a.turn_lo[j]);
-    for (int j = threadIdx.x; j < kBwdNW * 2 * D; j += blockDim.x) red[j] = 0.0f;
+    for (int j = threadIdx.x; j < kNW * 2 * D; j += blockDim.x) red[j] = 0.0f;
     for (int j = threadIdx.x; j < 2 * D; j += blockDim.x) wsm[j] = a.rms_w[j];
     __syncthreads();
     const int row_bytes = N * D * 2;                // one token, all heads, one tensor
@@ -246,7 +270,26 @@ __global__ void __launch_bounds__(kBwdThreads, HALF_PAIRS ? kBwdCtasPerSmHalf : 
             const uint32_t span = uint32_t(t.ntok) * uint32_t(row_bytes);
             uint8_t* dst = smem + L.stages + size_t(s) * a.stage_bytes;
             const int64_t tok0 = t.bb * a.s[t.q] + t.i0;
-            if (lane == 0) {
+            const int64_t row0 = t.bb * a.S + a.seq_off[t.q] + t.i0;  // first head-side row
+            if (GM && !is_v) {
+                // the input block, grouped by head group (R whole rows arrive: rows past the
+                // chunk are filled), then each rank's gradient rows as one span, in the same order
+                if (lane == 0) {
+                    const uint32_t box = uint32_t(a.tokens_per_unit) * uint32_t(row_bytes);
+                    mbar_arrive_expect_tx(&full[s], box + uint32_t(t.ntok) * a.run * uint32_t(a.W));
+                    tensor_g2s_4d(dst, &a.xmap[t.t][t.q], 0, int(t.i0 - a.row_lo[t.q]), 0,
+                                  int(t.bb), &full[s]);
+                    BwdRecord& rec = records[s];  // published by this lane's arrive below
+                    rec.seq_row0 = tok0;
+                    rec.t_q = t.t | (t.q << 3);
+                    rec.ntok = t.ntok;
+                }
+                __syncwarp();  // the unit's bytes are registered before any copy can complete
+                if (lane < a.W)
+                    bulk_g2s(dst + grad_at + size_t(lane) * a.tokens_per_unit * a.run,
+                             a.g_in[t.t][lane] + row0 * a.run, uint32_t(t.ntok) * a.run, &full[s]);
+            }
+            if (lane == 0 && !(GM && !is_v)) {
                 mbar_arrive_expect_tx(&full[s], is_v ? span : 2 * span);
                 if (!is_v && packed_rows)
                     bulk_g2s(dst, a.x_in[t.t][t.q] + tok0 * row_bytes, span, &full[s]);
@@ -256,14 +299,13 @@ __global__ void __launch_bounds__(kBwdThreads, HALF_PAIRS ? kBwdCtasPerSmHalf : 
                 rec.ntok = t.ntok;
             }
             __syncwarp();
-            if (!is_v && !packed_rows) {
+            if (!GM && !is_v && !packed_rows) {
                 for (int tok = lane; tok < t.ntok; tok += 32)
                     bulk_g2s(dst + tok * row_bytes, a.x_in[t.t][t.q] + (tok0 + tok) * a.tok_stride,
                              uint32_t(row_bytes), &full[s]);
             }
             uint8_t* gdst = is_v ? dst : dst + grad_at;
-            const int64_t row0 = t.bb * a.S + a.seq_off[t.q] + t.i0;  // first head-side row
-            const int copies = t.ntok * a.W;
+            const int copies = (GM && !is_v) ? 0 : t.ntok * a.W;  // token order: one per (token, rank)
             for (int c = lane; c < copies; c += 32) {
                 const int tok = c / a.W, r = c - tok * a.W;
                 const int64_t run = a.n[r] * (D * 2);  // bytes per token on rank r
@@ -317,9 +359,16 @@ __global__ void __launch_bounds__(kBwdThreads, HALF_PAIRS ? kBwdCtasPerSmHalf : 
     // this warp's share of the rows of a full token block (steps m_lo .. m_hi - 1 of PER_STEP
     // rows), and the (token, head) of its first row
     const int full_steps = (a.tokens_per_unit * N + PER_STEP - 1) / PER_STEP;
-    const int full_m_lo = cw * full_steps / kBwdNW, full_m_hi = (cw + 1) * full_steps / kBwdNW;
+    const int full_m_lo = cw * full_steps / kNW, full_m_hi = (cw + 1) * full_steps / kNW;
     const int full_base_tok = full_m_lo * PER_STEP / N;
     const int full_base_head = full_m_lo * PER_STEP - full_base_tok * N;
+    // group-major units: row (group g, row i, head h) at ((g R + i) n + h) in both halves of the
+    // stage, the same share of steps for every unit (short units skip rows past their end)
+    const int gm_n = GM ? a.n_eq : 1, gm_R = a.tokens_per_unit;
+    const int gm_run = GM ? int(a.run) : 0;
+    const int gm_pt0 = full_m_lo * PER_STEP / gm_n;  // pseudo-token g R + i of the first row
+    const int gm_h0 = full_m_lo * PER_STEP - gm_pt0 * gm_n;
+    const int gm_g0 = gm_pt0 / gm_R, gm_i0 = gm_pt0 - (gm_pt0 / gm_R) * gm_R;
     // sums over the lane groups of the warp, added to the warp's shared row, then cleared
     auto flush_dw = [&]() {
 #pragma unroll
@@ -389,14 +438,15 @@ __global__ void __launch_bounds__(kBwdThreads, HALF_PAIRS ? kBwdCtasPerSmHalf : 
         const int rows = ntok * N;
         int m_lo = full_m_lo, m_hi = full_m_hi;
         int base_tok = full_base_tok, base_head = full_base_head;
-        if (ntok != a.tokens_per_unit) {  // a short block: this warp's share of its rows
+        if (!GM && ntok != a.tokens_per_unit) {  // a short block: this warp's share of its rows
             const int steps = (rows + PER_STEP - 1) / PER_STEP;
-            m_lo = cw * steps / kBwdNW;
-            m_hi = (cw + 1) * steps / kBwdNW;
+            m_lo = cw * steps / kNW;
+            m_hi = (cw + 1) * steps / kNW;
             base_tok = m_lo * PER_STEP / N;
             base_head = m_lo * PER_STEP - base_tok * N;
         }
         int base = m_lo * PER_STEP;  // first row of the current step and its (token, head)
+        int bg = gm_g0, bi = gm_i0, bh = gm_h0;  // group-major: (group, row, head) of the step
         for (int m = m_lo; m < m_hi; ++m) {
             // The sums (mean square, <u * w, x>) need the whole row: u = R^T gy (fp32) and the
             // raw words of x are kept across the reduction, then dx and the dw terms are formed.
@@ -408,15 +458,31 @@ __global__ void __launch_bounds__(kBwdThreads, HALF_PAIRS ? kBwdCtasPerSmHalf : 
 #pragma unroll
             for (int u = 0; u < ILP; ++u) {
                 const int o = u * GPW + group;
-                ok[u] = base + o < rows;
-                int hh = base_head + o, tk = base_tok;
-                while (hh >= N) {
-                    hh -= N;
-                    ++tk;
+                int off;  // the row's offset in both halves of the stage
+                if constexpr (GM) {
+                    int hh = bh + o, ii = bi, gg = bg;
+                    while (hh >= gm_n) {
+                        hh -= gm_n;
+                        if (++ii == gm_R) {
+                            ii = 0;
+                            ++gg;
+                        }
+                    }
+                    ok[u] = gg < a.W && ii < ntok;
+                    tk_[u] = ii;
+                    hh_[u] = gg * gm_n + hh;  // head on the sequence side
+                    off = (gg * gm_R + ii) * gm_run + hh * (D * 2);
+                } else {
+                    ok[u] = base + o < rows;
+                    int hh = base_head + o, tk = base_tok;
+                    while (hh >= N) {
+                        hh -= N;
+                        ++tk;
+                    }
+                    tk_[u] = tk;
+                    hh_[u] = hh;
+                    off = (base + o) * (D * 2);  // row (tk, hh) of the unit in the stage
                 }
-                tk_[u] = tk;
-                hh_[u] = hh;
-                const int off = (base + o) * (D * 2);  // row (tk, hh) of the unit in the stage
                 Words g = {};
                 xr[u] = Words{};
                 if (ok[u]) {
@@ -430,7 +496,7 @@ __global__ void __launch_bounds__(kBwdThreads, HALF_PAIRS ? kBwdCtasPerSmHalf : 
                     IO::unpack(xr[u], h, xE, xO);
                     IO::unpack(g, h, gE, gO);
                     // (c_j, c_j+1, s_j, s_j+1) for j = P sub + 2 h
-                    const float4 cs = table[IO::table_entry(tk, h, sub)];
+                    const float4 cs = table[IO::table_entry(tk_[u], h, sub)];
                     const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
                     const float2 ns2 = make_float2(-cs.z, -cs.w);
                     // u = R^T gy: (c g_e + s g_o, c g_o - s g_e)
@@ -472,11 +538,22 @@ __global__ void __launch_bounds__(kBwdThreads, HALF_PAIRS ? kBwdCtasPerSmHalf : 
                 IO::store_global(out_base + int64_t(tk_[u]) * a.tok_stride + hh_[u] * (D * 2), sub,
                                  IO::pack(dxE, dxO));
             }
-            base += PER_STEP;
-            base_head += PER_STEP;
-            while (base_head >= N) {
-                base_head -= N;
-                ++base_tok;
+            if constexpr (GM) {
+                bh += PER_STEP;
+                while (bh >= gm_n) {
+                    bh -= gm_n;
+                    if (++bi == gm_R) {
+                        bi = 0;
+                        ++bg;
+                    }
+                }
+            } else {
+                base += PER_STEP;
+                base_head += PER_STEP;
+                while (base_head >= N) {
+                    base_head -= N;
+                    ++base_tok;
+                }
             }
         }
         // this warp has read all it needs of the stage: hand it back
@@ -486,12 +563,12 @@ __global__ void __launch_bounds__(kBwdThreads, HALF_PAIRS ? kBwdCtasPerSmHalf : 
     flush_dw();
     if (stored_v) bulk_wait<0>();
     // the CTA's dw sums, over its consumer warps in a fixed order, into its slot
-    asm volatile("bar.sync %0, %1;" ::"r"(kBwdConsumerBarrier), "r"(kBwdNW * 32) : "memory");
+    asm volatile("bar.sync %0, %1;" ::"r"(kBwdConsumerBarrier), "r"(kNW * 32) : "memory");
     const int ct = threadIdx.x - kBwdFirstConsumer * 32;
     float* slot_out = a.dw_part + size_t(blockIdx.x) * (2 * D);
-    for (int j = ct; j < 2 * D; j += kBwdNW * 32) {
+    for (int j = ct; j < 2 * D; j += kNW * 32) {
         float sum = 0.0f;
-        for (int w = 0; w < kBwdNW; ++w) sum += red[w * 2 * D + j];
+        for (int w = 0; w < kNW; ++w) sum += red[w * 2 * D + j];
         slot_out[j] = sum;
     }
 }
@@ -522,14 +599,41 @@ __global__ void __launch_bounds__(512) fused_bwd_reduce_kernel(const float* __re
 // Stage geometry for a plan: tokens per unit, stage count and CTAs per SM (0 stages: one token's
 // input and gradient rows do not fit even one CTA per SM). Narrower units, fewer stages, then
 // fewer CTAs per SM are tried in that order.
-void fused_bwd_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages,
+// Whether the backward takes row blocks under the automatic choice (the plan must fit them:
+// equal head groups, runs of at most 2,048 bytes). Measured across eight plans with equal head
+// groups (CUDA events, back to back): with rows of 7-16 KiB they ran at 1.006-1.034 of the copy
+// peak against the token units' 0.78-1.00; with 4 KiB rows (N d e = 4,096) at 0.81-0.88 against
+// 0.76-0.94, mostly below.
+bool fused_bwd_group_major_preferred(const Plan& p) { return p.N * p.d * p.e >= 6144; }
+
+void fused_bwd_geometry(const Plan& p, bool group_major, int64_t* tokens_per_unit, int* stages,
                         uint32_t* stage_bytes, int* ctas_per_sm)
 {
     *stages = 0;
     *tokens_per_unit = 1;
     *stage_bytes = 0;
     *ctas_per_sm = 1;
-    const int64_t tok_bytes = 2 * p.N * p.d * 2;  // one token's input and gradient rows
+    const int64_t row = p.N * p.d * 2;  // one token of one tensor
+    if (group_major) {  // one CTA per SM; the largest block (at least the target) that fits
+        int64_t R = ULY_BWD_GM_BYTES / row;
+        if (R < ULY_BWD_GM_MIN_ROWS) R = ULY_BWD_GM_MIN_ROWS;
+        if (R > 256) R = 256;
+        for (; R >= 1; --R) {
+            const int64_t half = (R * row + 127) / 128 * 128;  // input box, then gradient rows
+            if (2 * half >= (1 << 20)) continue;
+            const BwdSmem m = bwd_smem_layout(int(p.d), int(R), ULY_BWD_GM_STAGES,
+                                              uint32_t(2 * half), kBwdNWGm);
+            if (m.total <= kSmemPerCtaMax) {
+                *tokens_per_unit = R;
+                *stages = ULY_BWD_GM_STAGES;
+                *stage_bytes = uint32_t(2 * half);
+                *ctas_per_sm = 1;
+                return;
+            }
+        }
+        return;
+    }
+    const int64_t tok_bytes = 2 * row;  // one token's input and gradient rows
     int64_t T0 = ULY_BWD_STAGE_TARGET / tok_bytes;
     if (T0 < 1) T0 = 1;
     const int ctas_max = p.rope_half ? kBwdCtasPerSmHalf : kBwdCtasPerSm;
@@ -540,7 +644,7 @@ void fused_bwd_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages,
             const int64_t sb = T * tok_bytes;
             if (sb >= (1 << 20)) continue;  // an mbarrier counts fewer than 2^20 bytes
             for (int K = stages_max; K >= 2; --K) {
-                const BwdSmem m = bwd_smem_layout(int(p.d), int(T), K, uint32_t(sb));
+                const BwdSmem m = bwd_smem_layout(int(p.d), int(T), K, uint32_t(sb), kBwdNW);
                 if (m.total <= budget && m.total <= kSmemPerCtaMax) {
                     *tokens_per_unit = T;
                     *stages = K;
@@ -554,23 +658,32 @@ void fused_bwd_geometry(const Plan& p, int64_t* tokens_per_unit, int* stages,
 }
 
 // per device: the kernel variants whose shared-memory limit has been raised (any host thread)
-static std::atomic<unsigned> g_bwd_smem_set[64];
+static std::atomic<unsigned long long> g_bwd_smem_set[64];
 
-template <int D, bool F16, bool HALF>
+template <int D, bool F16, bool HALF, bool GM>
 static cudaError_t bwd_launch_d(const FusedBwdArgs& a, cudaStream_t stream, int device, int grid)
 {
     constexpr int dbit = D == 8 ? 0 : D == 16 ? 1 : D == 32 ? 2 : D == 64 ? 3 : D == 128 ? 4 : 5;
-    constexpr unsigned bit = 1u << (dbit * 4 + (F16 ? 2 : 0) + (HALF ? 1 : 0));
+    constexpr unsigned long long bit =
+        1ull << (dbit * 8 + (F16 ? 4 : 0) + (HALF ? 2 : 0) + (GM ? 1 : 0));
     if (device >= 0 && device < 64 && !(g_bwd_smem_set[device].load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(fused_qk_bwd_kernel<D, F16, HALF>,
+        cudaError_t e = cudaFuncSetAttribute(fused_qk_bwd_kernel<D, F16, HALF, GM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemPerCtaMax);
         if (e != cudaSuccess) return e;
         g_bwd_smem_set[device].fetch_or(bit);
     }
-    const BwdSmem m = bwd_smem_layout(a.d, a.tokens_per_unit, a.stages, a.stage_bytes);
-    fused_qk_bwd_kernel<D, F16, HALF><<<grid, kBwdThreads, m.total, stream>>>(a);
+    const BwdSmem m =
+        bwd_smem_layout(a.d, a.tokens_per_unit, a.stages, a.stage_bytes, bwd_warps(GM));
+    fused_qk_bwd_kernel<D, F16, HALF, GM><<<grid, bwd_threads(GM), m.total, stream>>>(a);
     return cudaGetLastError();
+}
+
+template <int D, bool F16, bool HALF>
+static cudaError_t bwd_launch_gm(const FusedBwdArgs& a, cudaStream_t stream, int device, int grid)
+{
+    return a.group_major ? bwd_launch_d<D, F16, HALF, true>(a, stream, device, grid)
+                         : bwd_launch_d<D, F16, HALF, false>(a, stream, device, grid);
 }
 
 template <int D>
@@ -578,10 +691,10 @@ static cudaError_t bwd_launch_variant(const FusedBwdArgs& a, cudaStream_t stream
                                       int grid)
 {
     if (a.elem_f16)
-        return a.rope_half ? bwd_launch_d<D, true, true>(a, stream, device, grid)
-                           : bwd_launch_d<D, true, false>(a, stream, device, grid);
-    return a.rope_half ? bwd_launch_d<D, false, true>(a, stream, device, grid)
-                       : bwd_launch_d<D, false, false>(a, stream, device, grid);
+        return a.rope_half ? bwd_launch_gm<D, true, true>(a, stream, device, grid)
+                           : bwd_launch_gm<D, true, false>(a, stream, device, grid);
+    return a.rope_half ? bwd_launch_gm<D, false, true>(a, stream, device, grid)
+                       : bwd_launch_gm<D, false, false>(a, stream, device, grid);
 }
 
 // CTAs of the main kernel for a launch of `a` (the number of partial-sum slots it fills); at

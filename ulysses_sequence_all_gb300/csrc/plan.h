@@ -1,6 +1,8 @@
 // plan.h -- host plan of the Ulysses 4D relayout and the by-value argument blocks its kernels
 // receive. Shared by plan.cpp (host only, no CUDA calls) and the .cu files.
 #pragma once
+#include <cuda.h>  // CUtensorMap
+
 #include <cstdint>
 
 namespace uly {
@@ -173,8 +175,15 @@ struct FusedBwdArgs {
     float eps;
     float turn_hi[kMaxFusedD / 2];
     float turn_lo[kMaxFusedD / 2];
+    // Row blocks (equal head groups): a unit's forward input arrives with one 4-D tensor-map copy
+    // that lands it grouped by head group, [group][row][run], and its gradient with one copy per
+    // rank in the same order (see encode_group_map).
+    int32_t group_major;
+    int32_t n_eq;     // heads per rank (all ranks equal) when group_major
+    uint32_t run;     // n_eq * d * elem_size
+    CUtensorMap xmap[2][kMaxW];  // q, k: per shard, this launch's rows
 };
-static_assert(sizeof(FusedBwdArgs) <= 4096, "kernel parameter block");
+static_assert(sizeof(FusedBwdArgs) <= 32764, "kernel parameter block");
 
 void build_fused_bwd_units(const Plan& p, const ChunkRows& rows, int64_t tokens_per_unit,
                            FusedBwdArgs* a);
