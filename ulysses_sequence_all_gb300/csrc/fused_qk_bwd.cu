@@ -32,6 +32,14 @@
 // order) fill its slot of a partial-sum array, which a second kernel adds up in a fixed order, so
 // dw does not depend on timing. A v unit of the interleaved call (gradient rows only, mode 1)
 // leaves by bulk stores from its stage.
+//
+// Row blocks (template flag GM; plans with equal head groups, runs of at most 2,048 bytes): a
+// unit is a block of R whole rows of one tensor. Its forward input arrives with ONE 4-D tensor-map
+// copy whose map walks (run, row, head group, batch), so it lands grouped by head group,
+// [group][row][run], and each rank's gradient rows arrive as one span into the same order: 1 + W
+// copies per R tokens instead of 1 + W per token. The consumers map a row (g, i, h) back to its
+// sequence-side place (token i, head g n + h) for the dx store. One CTA per SM with 10 consumer
+// warps and 2 stages of about 100 KiB.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
