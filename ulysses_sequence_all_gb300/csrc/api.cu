@@ -460,12 +460,15 @@ int fused_bwd_run(const Plan& p, FusedBwdArgs& a, const DeviceInfo& dev, int64_t
         ChunkRows rows;
         chunk_rows(p, C, c, &rows);
         build_fused_bwd_units(p, rows, T, &a);
-        if (a.group_major) {  // maps of this launch's rows of the forward inputs
-            for (int t = 0; t < 2; ++t) {
+        if (a.group_major) {  // maps of this launch's rows: the forward inputs, and the other
+                              // planes' gradient outputs of a packed call
+            for (int t = 0; t < a.tensors; ++t) {
                 for (int q = 0; q < p.W; ++q) {
                     if (rows.cnt[q] == 0) continue;
-                    if (!encode_group_map(&a.xmap[t][q], a.x_in[t][q] + rows.lo[q] * a.tok_stride,
-                                          a.run, rows.cnt[q], p.W, p.b, a.tok_stride,
+                    CUtensorMap* map = t < 2 ? &a.xmap[t][q] : &a.dmap[t - 2][q];
+                    const uint8_t* base = t < 2 ? a.x_in[t][q] : a.dx_out[t][q];
+                    if (!encode_group_map(map, base + rows.lo[q] * a.tok_stride, a.run,
+                                          rows.cnt[q], p.W, p.b, a.tok_stride,
                                           p.s[q] * a.tok_stride, T))
                         return cuda_fail(cudaErrorInvalidValue);
                 }

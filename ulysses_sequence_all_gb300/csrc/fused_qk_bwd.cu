@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(bwd_threads(GM),
                     bulk_g2s(dst + grad_at + size_t(lane) * a.tokens_per_unit * a.run,
                              a.g_in[t.t][lane] + row0 * a.run, uint32_t(t.ntok) * a.run, &full[s]);
             }
-            if (lane == 0 && !(GM && !is_v)) {
+            if (lane == 0 && !GM) {
                 mbar_arrive_expect_tx(&full[s], is_v ? span : 2 * span);
                 if (!is_v && packed_rows)
                     bulk_g2s(dst, a.x_in[t.t][t.q] + tok0 * row_bytes, span, &full[s]);
@@ -312,8 +312,21 @@ __global__ void __launch_bounds__(bwd_threads(GM),
                     bulk_g2s(dst + tok * row_bytes, a.x_in[t.t][t.q] + (tok0 + tok) * a.tok_stride,
                              uint32_t(row_bytes), &full[s]);
             }
+            if (GM && is_v) {  // each rank's rows as one span, grouped by head group as well
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[s], uint32_t(t.ntok) * a.run * uint32_t(a.W));
+                    BwdRecord& rec = records[s];  // published by this lane's arrive below
+                    rec.seq_row0 = tok0;
+                    rec.t_q = t.t | (t.q << 3);
+                    rec.ntok = t.ntok;
+                }
+                __syncwarp();  // the unit's bytes are registered before any copy can complete
+                if (lane < a.W)
+                    bulk_g2s(dst + size_t(lane) * a.tokens_per_unit * a.run,
+                             a.g_in[t.t][lane] + row0 * a.run, uint32_t(t.ntok) * a.run, &full[s]);
+            }
             uint8_t* gdst = is_v ? dst : dst + grad_at;
-            const int copies = (GM && !is_v) ? 0 : t.ntok * a.W;  // token order: one per (token, rank)
+            const int copies = GM ? 0 : t.ntok * a.W;  // token order: one per (token, rank)
             for (int c = lane; c < copies; c += 32) {
                 const int tok = c / a.W, r = c - tok * a.W;
                 const int64_t run = a.n[r] * (D * 2);  // bytes per token on rank r
@@ -419,7 +432,12 @@ __global__ void __launch_bounds__(bwd_threads(GM),
                         // by the first consumer warp
             if (cw == 0 && lane == 0) {
                 uint8_t* out = a.dx_out[tt][rec.t_q >> 3] + rec.seq_row0 * a.tok_stride;
-                if (packed_rows) {
+                if (GM) {  // grouped by head group: one tensor-map store back to token order
+                    const int q = rec.t_q >> 3;
+                    const int64_t bb = rec.seq_row0 / a.s[q];
+                    const int64_t i0 = rec.seq_row0 - bb * a.s[q] - a.row_lo[q];
+                    tensor_s2g_4d(&a.dmap[tt - 2][q], 0, int(i0), 0, int(bb), xs);
+                } else if (packed_rows) {
                     bulk_s2g(out, xs, uint32_t(ntok) * uint32_t(row_bytes));
                 } else {
                     for (int tok = 0; tok < ntok; ++tok)

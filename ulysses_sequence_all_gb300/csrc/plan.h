@@ -182,6 +182,7 @@ struct FusedBwdArgs {
     int32_t n_eq;     // heads per rank (all ranks equal) when group_major
     uint32_t run;     // n_eq * d * elem_size
     CUtensorMap xmap[2][kMaxW];  // q, k: per shard, this launch's rows
+    CUtensorMap dmap[kMaxPlanes - 2][kMaxW];  // packed calls: the other planes' gradient outputs
 };
 static_assert(sizeof(FusedBwdArgs) <= 32764, "kernel parameter block");
 

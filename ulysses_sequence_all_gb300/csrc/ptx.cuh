@@ -183,6 +183,17 @@ __device__ __forceinline__ void tensor_s2g_3d(const void* map, int c0, int c1, i
         : "memory");
 }
 
+// The same for a 4-D map: coordinates (c0, c1, c2, c3), c0 the innermost.
+__device__ __forceinline__ void tensor_s2g_4d(const void* map, int c0, int c1, int c2, int c3,
+                                              const void* src_smem)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+            map),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(src_smem))
+        : "memory");
+}
+
 // Bulk copy shared -> global, tracked by this thread's bulk async-groups.
 __device__ __forceinline__ void bulk_s2g(void* dst_gmem, const void* src_smem, uint32_t bytes)
 {
