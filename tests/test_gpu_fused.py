@@ -87,6 +87,7 @@ SMALL = [
     (4, 2, [3, 1, 0, 2], [1, 1, 1, 1], 16),
     (5, 2, [300, 310, 290, 305, 295], [8] * 5, 128),
     (8, 1, [1000, 999, 1001, 998, 1002, 997, 1003, 1000], [5] * 8, 128),
+    (4, 2, [20, 25, 0, 30], [3, 0, 5, 2], 128),  # unequal head groups with an empty one
 ]
 
 
