@@ -272,17 +272,7 @@ struct TensorShape {
     int stages, unit_bytes, lookahead;
 };
 // [mode]: measured at the Wan-720p shape (W = 8, runs of 1,280 bytes), CUDA events back to back.
-#ifndef ULY_TENSOR_FULL1_STAGES  // mode 1 of a full grid: stages, stage bytes, loads ahead
-#define ULY_TENSOR_FULL1_STAGES 9
-#endif
-#ifndef ULY_TENSOR_FULL1_UNIT
-#define ULY_TENSOR_FULL1_UNIT 24576
-#endif
-#ifndef ULY_TENSOR_FULL1_LOOK
-#define ULY_TENSOR_FULL1_LOOK 4
-#endif
-constexpr TensorShape kTensorFull[2] = {
-    {8, 24576, 7}, {ULY_TENSOR_FULL1_STAGES, ULY_TENSOR_FULL1_UNIT, ULY_TENSOR_FULL1_LOOK}};
+constexpr TensorShape kTensorFull[2] = {{8, 24576, 7}, {9, 24576, 4}};
 constexpr TensorShape kTensorCapped[2] = {{4, 53248, 3}, {4, 49152, 3}};
 
 constexpr int tensor_smem(TensorShape t) { return kTensorStageAlign + t.stages * t.unit_bytes; }
