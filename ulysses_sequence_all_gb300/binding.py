@@ -197,7 +197,7 @@ def ulysses_plan_set_max_ctas(plan: Plan, max_ctas: int):
 
 
 def ulysses_plan_set_fused_engine(plan: Plan, engine: int):
-    """Kernel of the fused forward calls (separate or packed inputs): ULY_ENGINE_AUTO,
+    """Kernel of the fused calls (forward, separate or packed, and their backward): ULY_ENGINE_AUTO,
     ULY_ENGINE_TMA (token units) or ULY_ENGINE_TENSOR (blocks of whole rows, grouped by head group
     through one tensor-map copy)."""
     _check(_lib().ulysses_plan_set_fused_engine(plan, engine), "ulysses_plan_set_fused_engine")
