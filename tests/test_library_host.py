@@ -261,6 +261,24 @@ def test_fused_argument_errors_before_cuda():
         assert ei.value.status == status
 
 
+def test_fused_sequence_limit_before_cuda():
+    """Positions travel as exact fp32 integers, so the fused calls take S < 2^24: a plan of
+    exactly 2^24 tokens is refused on the host (the relayout itself has no such limit)."""
+    plan = B.ulysses_plan(2, 1, [1 << 23, 1 << 23], [1, 1], 8, "bfloat16")
+    in_b = [B.ulysses_plan_bytes(plan, 0, k)[0] for k in range(2)]
+    out_b = [B.ulysses_plan_bytes(plan, 0, k)[1] for k in range(2)]
+    q, k = _fake_ptrs(1 << 40, in_b), _fake_ptrs(1 << 39, in_b)
+    qo, ko = _fake_ptrs(1 << 41, out_b), _fake_ptrs(1 << 42, out_b)
+    with pytest.raises(B.UlyssesError) as ei:
+        B.ulysses_a2a_4d_qk_fused(plan, q, k, qo, ko, 1 << 43, 1e-6, 1e4, stream=0)
+    assert ei.value.status == B.ULY_EINVAL
+    packed = _fake_ptrs(1 << 44, [2 * x for x in in_b])
+    with pytest.raises(B.UlyssesError) as ei:
+        B.ulysses_a2a_4d_packed_fused(plan, 2, 0, 1, 2 * 8 * 2 * 2, packed, [qo, ko], 1 << 43,
+                                      1e-6, 1e4, stream=0)
+    assert ei.value.status == B.ULY_EINVAL
+
+
 def test_packed_argument_errors_before_cuda():
     """The packed fused call refuses bad plane counts and roles, a short or unaligned token pitch,
     and overlapping outputs on the host."""
