@@ -670,7 +670,8 @@ def run_ours(args):
                                                       "mode0": wk.bytes_plain,
                                                       "mode1": wk.bytes_plain}[dominant]},
         "kernels": {k: {"kernel": {"fused_qk": fused_kernel}.get(k, relayout_kernel),
-                        "median_ms": round(med[k], 4), "GB/s": round(gbs[k], 1),
+                        "median_ms": round(med[k], 4), "min_ms": round(min(kt[k]), 4),
+                        "launches_timed": len(kt[k]), "GB/s": round(gbs[k], 1),
                         "frac_of_peak": round(gbs[k] / peak, 4),
                         "frac_of_d2d": round(gbs[k] / d2d, 4) if d2d else None} for k in med},
         "d2d_copy_GBps": round(d2d, 1) if d2d else None,
