@@ -138,8 +138,9 @@ int ulysses_plan_set_max_ctas(ulysses_plan_t plan, int64_t max_ctas);
  * a block of whole rows (one tiled tensor-map copy in per tensor that lands the rows grouped by
  * destination rank, one bulk copy out per (tensor, rank)), for plans whose head groups all have
  * the same run n * d * elem_size of at most 2048 bytes (other plans use the token units);
- * ULY_ENGINE_AUTO (the default) takes the tensor-map kernel where it fits and a row
- * (N * d * elem_size) is at most 10,240 bytes, where it measured faster, else the token units.
+ * ULY_ENGINE_AUTO (the default) takes the tensor-map kernel where it fits, d is a power of two
+ * and a row (N * d * elem_size) is at most 10,240 bytes, where it measured faster, else the
+ * token units.
  * All give the same bytes. The setting applies to the packed calls too (their q and k planes as
  * above, the other planes moved in blocks of 2R rows). ULY_EINVAL for another engine. Must not
  * race with launches using the plan. */
@@ -239,7 +240,8 @@ int ulysses_a2a_4d_engine(ulysses_plan_t plan, int mode, int engine, const void*
  *     or (y[j], y[j + d/2]) after ulysses_plan_set_rope_pairs(plan, ULY_ROPE_HALF))
  * computed in fp32 and rounded once to the element type (nearest even), then placed where mode 0
  * puts it.
- *   plan     must have dtype ULY_BF16 or ULY_F16 and d in {8, 16, 32, 64, 128, 256}; S < 2^24.
+ *   plan     must have dtype ULY_BF16 or ULY_F16, d a multiple of 8 from 8 to 256 (e.g. 64,
+ *            72, 80, 96, 128), S < 2^24.
  *   q_in, k_in     W device pointers, rank q's (b, s_q, N, d) elements of the plan's dtype.
  *   q_out, k_out   W device pointers, rank r's (b, S, n_r, d), same dtype.
  *   rms_w    device pointer to 2 * d fp32 values, q's weight then k's.

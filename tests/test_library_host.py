@@ -185,7 +185,8 @@ def test_fused_engine_setter():
 
 def test_fused_kernel_choice():
     """The fused forward's kernel, decided on the host: the row-block kernel for equal head groups
-    with runs of at most 2,048 bytes and rows of at most 10,240 bytes, else the token units."""
+    with runs of at most 2,048 bytes, rows of at most 10,240 bytes and a power-of-two d, else the
+    token units."""
     def kernel(W, heads, d, dtype="bfloat16", engine=None):
         plan = B.ulysses_plan(W, 1, [8] * W, heads, d, dtype)
         if engine is not None:
@@ -203,6 +204,10 @@ def test_fused_kernel_choice():
     assert kernel(2, [9, 9], 128) == K                     # runs of 2,304 bytes
     assert kernel(8, [5] * 8, 128, engine=K) == K
     assert kernel(2, [64, 64], 128, engine=T) == K         # runs of 16 KiB: token units
+    assert kernel(8, [5] * 8, 72) == K                     # d not a power of two: token units
+    assert kernel(8, [5] * 8, 72, engine=T) == T           # forced: it fits
+    assert kernel(5, [9, 8, 8, 8, 7], 72, engine=T) == K
+    assert kernel(8, [5] * 8, 96, engine=K) == K
     lib = B.library()
     engine = ctypes.c_int()
     assert lib.ulysses_plan_fused_kernel(None, ctypes.byref(engine)) == B.ULY_EINVAL
@@ -225,6 +230,9 @@ def test_fused_backward_kernel_choice():
     assert kernel(4, [4] * 4, 128, engine=T) == T          # forced: it fits
     assert kernel(5, [9, 8, 8, 8, 7], 128, engine=T) == K  # unequal head groups
     assert kernel(8, [5] * 8, 128, engine=K) == K
+    assert kernel(8, [8] * 8, 120) == T                    # d = 120: rows of 15,360 bytes
+    assert kernel(8, [5] * 8, 72) == K                     # rows of 5,760 bytes
+    assert kernel(8, [5] * 8, 72, engine=T) == T
     engine = ctypes.c_int()
     assert B.library().ulysses_plan_fused_backward_kernel(None, ctypes.byref(engine)) == B.ULY_EINVAL
 
@@ -240,7 +248,7 @@ def test_auto_engine_argument_errors():
 def test_fused_argument_errors_before_cuda():
     plan32 = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "float32")
     plan = B.ulysses_plan(2, 1, [4, 4], [2, 2], 64, "bfloat16")
-    plan_d = B.ulysses_plan(2, 1, [4, 4], [2, 2], 24, "bfloat16")  # 48-byte rows: not a power of 2
+    plan_d = B.ulysses_plan(2, 1, [4, 4], [2, 2], 264, "bfloat16")  # d above the fused calls' 256
     in_b = [B.ulysses_plan_bytes(plan, 0, k)[0] for k in range(2)]
     out_b = [B.ulysses_plan_bytes(plan, 0, k)[1] for k in range(2)]
     q, k = _fake_ptrs(1 << 40, in_b), _fake_ptrs(1 << 39, in_b)

@@ -256,6 +256,11 @@ struct PackedIn {
     void* const* outs;
 };
 
+// Head dimensions of the fused calls: every multiple of 8 from 8 to 256 (a head row of 2-byte
+// elements is then a whole number of 16-byte words). Powers of two run kernels compiled for
+// their d; the others the token-unit kernels' run-time row layout.
+bool fused_head_dim_ok(int64_t d) { return d >= 8 && d <= kMaxFusedD && d % 8 == 0; }
+
 // Checks of a fused call (no CUDA call) and its argument block, without the unit tables. Either
 // q_in, k_in, q_out and k_out are given (separate tensors) or a packed input (pk).
 int fused_prepare(const Plan& p, const void* const* q_in, const void* const* k_in,
@@ -263,8 +268,7 @@ int fused_prepare(const Plan& p, const void* const* q_in, const void* const* k_i
                   float eps, float rope_theta, FusedArgs* a, int64_t* tokens_per_unit)
 {
     if (p.dtype != ULY_BF16 && p.dtype != ULY_F16) return ULY_EINVAL;
-    if (!(p.d == 8 || p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128 || p.d == 256))
-        return ULY_EINVAL;
+    if (!fused_head_dim_ok(p.d)) return ULY_EINVAL;
     if (p.S >= (int64_t(1) << 24)) return ULY_EINVAL;  // positions must be exact in fp32
     if (!(eps >= 0.0f) || !(rope_theta > 0.0f)) return ULY_EINVAL;
     if (!rms_w) return ULY_EINVAL;
@@ -426,8 +430,7 @@ int fused_bwd_setup(const Plan& p, const DeviceInfo& dev, int64_t* tokens_per_un
                     uint32_t* stage_bytes, int* ctas_per_sm, size_t* workspace_bytes)
 {
     if (p.dtype != ULY_BF16 && p.dtype != ULY_F16) return ULY_EINVAL;
-    if (!(p.d == 8 || p.d == 16 || p.d == 32 || p.d == 64 || p.d == 128 || p.d == 256))
-        return ULY_EINVAL;
+    if (!fused_head_dim_ok(p.d)) return ULY_EINVAL;
     if (p.S >= (int64_t(1) << 24)) return ULY_EINVAL;  // positions must be exact in fp32
     fused_bwd_geometry(p, fused_bwd_uses_group_major(p), tokens_per_unit, stages, stage_bytes,
                        ctas_per_sm);

@@ -196,26 +196,31 @@ __host__ __device__ inline FusedSmem fused_smem_layout(int d, int tokens, int st
     return m;
 }
 
-// D: head dimension; F16: fp16 elements (else bf16); HALF_PAIRS: rotate-half RoPE pairs (else
-// adjacent pairs). The row layouts (G lanes per row, H packed slots per lane) are in
-// fused_row.cuh.
+// D: head dimension, a power of two, or below 8 for a.d with one of the run-time row layouts
+// (rt_layout_for: any multiple of 8 up to 256); F16: fp16 elements (else bf16); HALF_PAIRS:
+// rotate-half RoPE pairs (else adjacent pairs). The row layouts (G lanes per row, H packed slots
+// per lane) are in fused_row.cuh.
 template <int D, bool F16, bool HALF_PAIRS>
 __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     fused_qk_kernel(const __grid_constant__ FusedArgs a)
 {
     using IO = RowIO<F16, HALF_PAIRS, D, kFusedWide>;
-    constexpr int G = IO::G;
+    const int dd = rt_layout(D) ? a.d : D;            // head dimension
+    const RowDims dims = IO::dims(dd);
+    const int G = dims.g;                  // lanes per head row
     constexpr int H = IO::H;
-    constexpr int HALF = D / 2;
-    constexpr int GPW = 32 / G;         // head rows per warp per slot
+    const int HALF = dd / 2;
+    // lanes from a row's first to the next row's: G, or G rounded up to a power of two
+    const int GP = !rt_layout(D) ? G : rt_pow2(D) ? row_lane_stride(G) : G;
+    const int GPW = 32 / GP;  // head rows per warp per slot
     // rows in flight per lane group: a lane of an 8-pair layout holds twice the values
     constexpr int ILP = IO::P == 8 ? kIlpWide : kIlp;
-    constexpr int PER_STEP = GPW * ILP;
+    const int PER_STEP = GPW * ILP;
     constexpr int NW = ULY_FUSED_CONSUMER_WARPS;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int K = a.stages;
     const int N = int(a.N);
-    const FusedSmem L = fused_smem_layout(D, a.tokens_per_unit, K, a.stage_bytes);
+    const FusedSmem L = fused_smem_layout(dd, a.tokens_per_unit, K, a.stage_bytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);    // data landed + rope table written
     uint64_t* computed = full + kFusedMaxStages;           // consumers done with the stage
     uint64_t* empty = computed + kFusedMaxStages;          // stores have read the stage
@@ -235,7 +240,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     for (int j = threadIdx.x; j < HALF; j += blockDim.x) turns[j] = make_float2(a.turn_hi[j], a.turn_lo[j]);
     __syncthreads();
     if (n == 0) return;
-    const int row_bytes = N * D * 2;  // one token, all heads, one tensor
+    const int row_bytes = N * dd * 2;  // one token, all heads, one tensor
     const bool qkv = a.interleaved != 0;
     // Stage layouts. A q,k unit holds row (token t, plane c in {q, k}, head h) at
     // t * tok_stride + c * plane_stride(ntok) + h * 2d: separate inputs arrive as two spans (all q
@@ -310,7 +315,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
                 const int tok = e / HALF, jj = e % HALF;
                 const float2 tj = turns[jj];
                 const float2 cs = rope_cos_sin(p0 + float(tok), tj.x, tj.y);
-                const int at = IO::table_at(tok, jj);
+                const int at = IO::table_at(tok, jj, dims);
                 table[at] = cs.x;
                 table[at + 2] = cs.y;
             }
@@ -354,9 +359,9 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
             for (int idx = lane; idx < runs; idx += 32) {
                 const int rest = idx / W, r = idx - rest * W;
                 const int tok = rest / uplanes, plane = rest - tok * uplanes;
-                const int64_t run = a.n[r] * (D * 2);
+                const int64_t run = a.n[r] * (dd * 2);
                 if (run == 0) continue;
-                const uint8_t* src = st + tok * ustride + plane * pstride + a.head_off[r] * (D * 2);
+                const uint8_t* src = st + tok * ustride + plane * pstride + a.head_off[r] * (dd * 2);
                 uint8_t* out = v_unit ? plain_out[r] : plane == 0 ? a.q_out[r] : a.k_out[r];
                 bulk_s2g(out + (row0 + tok) * run, src, uint32_t(run));
             }
@@ -376,14 +381,16 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
     const int cw = warp - kFirstConsumerWarp;
     const int which = cw >= HALF_NW;          // 0: q, 1: k (uniform per warp)
     const int cwi = cw - which * HALF_NW;     // rank among the warps of this tensor
-    const int sub = lane % G;                 // which pairs of the row this lane holds
-    const int group = lane / G;               // which head row of the warp slot
+    const int group = lane / GP;       // which head row of the warp slot
+    const int sub = lane - group * GP;  // which pairs of the row this lane holds
+    const bool active = sub < G && group < GPW;  // lanes holding no row's pairs (run-time d)
     // This lane's weights as packed pairs: first / second elements of its pairs, plus the
     // negated second ones (the rotation subtracts them).
     float2 wE[H], wO[H], wOn[H];
-    IO::weights(a.rms_w + which * D, sub, wE, wO);
+    for (int h = 0; h < H; ++h) wE[h] = wO[h] = make_float2(0.f, 0.f);
+    if (active) IO::weights(a.rms_w + which * dd, sub, wE, wO, dims);
     for (int h = 0; h < H; ++h) wOn[h] = make_float2(-wO[h].x, -wO[h].y);
-    const float inv_d = 1.0f / float(D);
+    const float inv_d = 1.0f / float(dd);
     // this warp's share of the rows of a full token block (steps m_lo .. m_hi - 1 of PER_STEP
     // rows) and the (token, head) of its first row
     const int full_steps = (a.tokens_per_unit * N + PER_STEP - 1) / PER_STEP;
@@ -433,10 +440,10 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
                     hh -= N;
                     ++tk;
                 }
-                slot[u] = rows_base + tk * tok_stride + hh * (D * 2);
+                slot[u] = rows_base + tk * tok_stride + hh * (dd * 2);
                 tok[u] = tk;
                 typename IO::Words x = {};
-                if (ok[u]) x = IO::load(slot[u], sub);
+                if (ok[u] && active) x = IO::load(slot[u], sub, dims);
                 float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
@@ -446,21 +453,17 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
                 }
                 ss[u] = acc.x + acc.y;
             }
-#pragma unroll
-            for (int off = G / 2; off > 0; off >>= 1) {
-#pragma unroll
-                for (int u = 0; u < ILP; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], off);
-            }
+            row_sums<D, 1>(ss, ss, G, GP, sub, group);
 #pragma unroll
             for (int u = 0; u < ILP; ++u) {
-                if (!ok[u]) continue;
+                if (!ok[u] || !active) continue;
                 const float inv = rsqrtf(ss[u] * inv_d + a.eps);
                 const float2 inv2 = make_float2(inv, inv);
                 float2 oEs[H], oOs[H];
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
                     // (c_j, c_j+1, s_j, s_j+1) for j = P sub + 2 h (see the table layout)
-                    const float4 cs = table[IO::table_entry(tok[u], h, sub)];
+                    const float4 cs = table[IO::table_entry(tok[u], h, sub, dims)];
                     const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
                     const float2 A = __fmul2_rn(vE[u][h], wE[h]);   // weighted first elements
                     const float2 Bp = __fmul2_rn(vO[u][h], wO[h]);  // weighted second elements
@@ -469,7 +472,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
                     oEs[h] = __fmul2_rn(__ffma2_rn(Bn, s2, __fmul2_rn(A, c2)), inv2);
                     oOs[h] = __fmul2_rn(__ffma2_rn(A, s2, __fmul2_rn(Bp, c2)), inv2);
                 }
-                IO::store(slot[u], sub, IO::pack(oEs, oOs));  // in place
+                IO::store(slot[u], sub, IO::pack(oEs, oOs), dims);  // in place
             }
             base += PER_STEP;
             base_head += PER_STEP;
@@ -520,20 +523,17 @@ void fused_geometry(const Plan& p, int planes, int64_t* tokens_per_unit, int* st
     }
 }
 
-// per device: the kernel variants whose shared-memory limit has been raised (any host thread)
-static std::atomic<unsigned> g_fused_smem_set[64];
-
 template <int D, bool F16, bool HALF>
 static cudaError_t launch_d(const FusedArgs& a, cudaStream_t stream, int device, int grid)
 {
-    constexpr int dbit = D == 8 ? 0 : D == 16 ? 1 : D == 32 ? 2 : D == 64 ? 3 : D == 128 ? 4 : 5;
-    constexpr unsigned bit = 1u << (dbit * 4 + (F16 ? 2 : 0) + (HALF ? 1 : 0));
-    if (device >= 0 && device < 64 && !(g_fused_smem_set[device].load() & bit)) {
+    static std::atomic<unsigned long long> raised{0};  // devices with this variant's limit raised
+    const unsigned long long bit = device >= 0 && device < 64 ? 1ull << device : 0;
+    if (bit && !(raised.load() & bit)) {
         cudaError_t e = cudaFuncSetAttribute(fused_qk_kernel<D, F16, HALF>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemPerCtaMax);
         if (e != cudaSuccess) return e;
-        g_fused_smem_set[device].fetch_or(bit);
+        raised.fetch_or(bit);
     }
     const FusedSmem m = fused_smem_layout(a.d, a.tokens_per_unit, a.stages, a.stage_bytes);
     fused_qk_kernel<D, F16, HALF><<<grid, kFusedThreads, m.total, stream>>>(a);
@@ -564,7 +564,14 @@ cudaError_t fused_launch(const FusedArgs& a, cudaStream_t stream, int device, in
         case 64: return launch_variant<64>(a, stream, device, int(grid));
         case 128: return launch_variant<128>(a, stream, device, int(grid));
         case 256: return launch_variant<256>(a, stream, device, int(grid));
-        default: return cudaErrorInvalidValue;
+        default:  // any other multiple of 8 up to 256: a run-time row layout
+            if (a.d % 8 != 0 || a.d < 8 || a.d > kMaxFusedD) return cudaErrorInvalidValue;
+            switch (rt_layout_for(a.d)) {
+                case 0: return launch_variant<0>(a, stream, device, int(grid));
+                case kRtWide: return launch_variant<kRtWide>(a, stream, device, int(grid));
+                case kRtPow2: return launch_variant<kRtPow2>(a, stream, device, int(grid));
+                default: return launch_variant<kRtPow2 | kRtWide>(a, stream, device, int(grid));
+            }
     }
 }
 

@@ -210,9 +210,22 @@ __host__ __device__ inline BwdSmem bwd_smem_layout(int d, int tokens, int stages
     return m;
 }
 
-// D: head dimension; F16: fp16 elements (else bf16); HALF_PAIRS: rotate-half RoPE pairs (else
-// adjacent pairs). The row layouts (G lanes per row, H packed slots per lane) are in
-// fused_row.cuh.
+// Rows of dw sums per consumer warp in shared memory (each 2 x d floats, q then k): one per row
+// group of the warp where rows are packed back to back in the warp (a run-time layout whose
+// row_lane_stride is not a power of two; each lane then adds its sums to its group's row, no
+// shuffle), else one (the warp's groups summed with a butterfly first).
+__host__ __device__ inline int bwd_dw_rows_per_warp(int d)
+{
+    if ((d & (d - 1)) == 0) return 1;
+    const int g = d / (d % 16 == 0 ? 16 : 8);
+    const int gp = row_lane_stride(g);
+    return (gp & (gp - 1)) == 0 ? 1 : 32 / g;
+}
+
+// D: head dimension, a power of two, or below 8 for a.d with one of the run-time row layouts
+// (rt_layout_for: any multiple of 8 up to 256); F16: fp16 elements (else bf16); HALF_PAIRS:
+// rotate-half RoPE pairs (else adjacent pairs). The row layouts (G lanes per row, H packed slots
+// per lane) are in fused_row.cuh.
 template <int D, bool F16, bool HALF_PAIRS, bool GM>
 __global__ void __launch_bounds__(bwd_threads(GM),
                                   GM ? 1 : HALF_PAIRS ? kBwdCtasPerSmHalf : kBwdCtasPerSm)
@@ -221,17 +234,22 @@ __global__ void __launch_bounds__(bwd_threads(GM),
     constexpr int kNW = bwd_warps(GM);  // consumer warps
     using IO = RowIO<F16, HALF_PAIRS, D, kBwdWide>;
     using Words = typename IO::Words;
-    constexpr int G = IO::G;
+    const int dd = rt_layout(D) ? a.d : D;  // head dimension
+    const RowDims dims = IO::dims(dd);
+    const int G = dims.g;        // lanes per head row
     constexpr int H = IO::H;
-    constexpr int HALF = D / 2;
-    constexpr int GPW = 32 / G;  // head rows per warp per slot
+    const int HALF = dd / 2;
+    // lanes from a row's first to the next row's: G, or G rounded up to a power of two
+    const int GP = !rt_layout(D) ? G : rt_pow2(D) ? row_lane_stride(G) : G;
+    const int GPW = 32 / GP;  // head rows per warp per slot
     // rows in flight per lane group: a lane of an 8-pair layout holds twice the values
     constexpr int ILP = IO::P == 8 ? kBwdIlpWide : kBwdIlp;
-    constexpr int PER_STEP = GPW * ILP;
+    const int PER_STEP = GPW * ILP;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int K = a.stages;
     const int N = int(a.N);
-    const BwdSmem L = bwd_smem_layout(D, a.tokens_per_unit, K, a.stage_bytes, kNW);
+    const int RG = rt_layout(D) ? bwd_dw_rows_per_warp(dd) : 1;  // dw rows per consumer warp
+    const BwdSmem L = bwd_smem_layout(dd, a.tokens_per_unit, K, a.stage_bytes, kNW * RG);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // data landed + table written
     uint64_t* empty = full + kBwdMaxStages;              // consumers done with the stage
     float2* turns = reinterpret_cast<float2*>(smem + L.turns);
@@ -249,10 +267,10 @@ __global__ void __launch_bounds__(bwd_threads(GM),
         fence_barrier_init();
     }
     for (int j = threadIdx.x; j < HALF; j += blockDim.x) turns[j] = make_float2(a.turn_hi[j], a.turn_lo[j]);
-    for (int j = threadIdx.x; j < kNW * 2 * D; j += blockDim.x) red[j] = 0.0f;
-    for (int j = threadIdx.x; j < 2 * D; j += blockDim.x) wsm[j] = a.rms_w[j];
+    for (int j = threadIdx.x; j < kNW * RG * 2 * dd; j += blockDim.x) red[j] = 0.0f;
+    for (int j = threadIdx.x; j < 2 * dd; j += blockDim.x) wsm[j] = a.rms_w[j];
     __syncthreads();
-    const int row_bytes = N * D * 2;                // one token, all heads, one tensor
+    const int row_bytes = N * dd * 2;               // one token, all heads, one tensor
     const uint32_t grad_at = a.stage_bytes / 2;     // the gradient runs' offset in a stage
     const bool packed_rows = a.tok_stride == row_bytes;  // a block's rows are one span
 
@@ -329,9 +347,9 @@ __global__ void __launch_bounds__(bwd_threads(GM),
             const int copies = GM ? 0 : t.ntok * a.W;  // token order: one per (token, rank)
             for (int c = lane; c < copies; c += 32) {
                 const int tok = c / a.W, r = c - tok * a.W;
-                const int64_t run = a.n[r] * (D * 2);  // bytes per token on rank r
+                const int64_t run = a.n[r] * (dd * 2);  // bytes per token on rank r
                 if (run == 0) continue;
-                bulk_g2s(gdst + tok * row_bytes + int(a.head_off[r]) * (D * 2),
+                bulk_g2s(gdst + tok * row_bytes + int(a.head_off[r]) * (dd * 2),
                          a.g_in[t.t][r] + (row0 + tok) * run, uint32_t(run), &full[s]);
             }
             // While the copies fly, the lanes fill the stage's cos/sin table for the unit's
@@ -345,7 +363,7 @@ __global__ void __launch_bounds__(bwd_threads(GM),
                 const int tok = e / HALF, jj = e % HALF;
                 const float2 tj = turns[jj];
                 const float2 cs = rope_cos_sin(p0 + float(tok), tj.x, tj.y);
-                const int at = IO::table_at(tok, jj);
+                const int at = IO::table_at(tok, jj, dims);
                 table[at] = cs.x;
                 table[at + 2] = cs.y;
             }
@@ -367,9 +385,10 @@ __global__ void __launch_bounds__(bwd_threads(GM),
     // group of G lanes holds one head row (a lane's RoPE pairs as packed fp32 values: the first
     // and the second elements of its pairs), ILP rows in flight per group.
     const int cw = warp - kBwdFirstConsumer;
-    const int sub = lane % G;    // which pairs of the row this lane holds
-    const int group = lane / G;  // which head row of the warp slot
-    const float inv_d = 1.0f / float(D);
+    const int group = lane / GP;       // which head row of the warp slot
+    const int sub = lane - group * GP;  // which pairs of the row this lane holds
+    const bool active = sub < G && group < GPW;  // lanes holding no row's pairs (run-time d)
+    const float inv_d = 1.0f / float(dd);
     // dw partial sums of this lane's columns for tensor acc_t, flushed when the tensor changes
     // (with an even grid a CTA of the q, k call only ever sees one tensor) and at the end
     float2 aE[H], aO[H];
@@ -392,24 +411,29 @@ __global__ void __launch_bounds__(bwd_threads(GM),
     const int gm_g0 = gm_pt0 / gm_R, gm_i0 = gm_pt0 - (gm_pt0 / gm_R) * gm_R;
     // sums over the lane groups of the warp, added to the warp's shared row, then cleared
     auto flush_dw = [&]() {
+        if constexpr (rt_pow2(D)) {  // rows on power-of-two strides: sum the groups, then group 0
 #pragma unroll
-        for (int off = G; off < 32; off <<= 1) {
+            for (int off = 1; off < 32; off <<= 1) {
+                if (off < GP) continue;  // across the warp's row groups, not within a row
 #pragma unroll
-            for (int h = 0; h < H; ++h) {
-                aE[h].x += __shfl_xor_sync(0xffffffffu, aE[h].x, off);
-                aE[h].y += __shfl_xor_sync(0xffffffffu, aE[h].y, off);
-                aO[h].x += __shfl_xor_sync(0xffffffffu, aO[h].x, off);
-                aO[h].y += __shfl_xor_sync(0xffffffffu, aO[h].y, off);
+                for (int h = 0; h < H; ++h) {
+                    aE[h].x += __shfl_xor_sync(0xffffffffu, aE[h].x, off);
+                    aE[h].y += __shfl_xor_sync(0xffffffffu, aE[h].y, off);
+                    aO[h].x += __shfl_xor_sync(0xffffffffu, aO[h].x, off);
+                    aO[h].y += __shfl_xor_sync(0xffffffffu, aO[h].y, off);
+                }
             }
         }
-        if (group == 0 && acc_t >= 0) {
-            float* row = red + (cw * 2 + acc_t) * D;
+        // rows packed back to back: every group adds to its own row
+        const int rg = rt_pow2(D) ? 0 : group;
+        if ((rt_pow2(D) ? group == 0 : true) && active && acc_t >= 0) {
+            float* row = red + ((cw * RG + rg) * 2 + acc_t) * dd;
 #pragma unroll
             for (int h = 0; h < H; ++h) {
-                row[IO::col(sub, h, false, 0)] += aE[h].x;
-                row[IO::col(sub, h, true, 0)] += aO[h].x;
-                row[IO::col(sub, h, false, 1)] += aE[h].y;
-                row[IO::col(sub, h, true, 1)] += aO[h].y;
+                row[IO::col(sub, h, false, 0, dims)] += aE[h].x;
+                row[IO::col(sub, h, true, 0, dims)] += aO[h].x;
+                row[IO::col(sub, h, false, 1, dims)] += aE[h].y;
+                row[IO::col(sub, h, true, 1, dims)] += aO[h].y;
             }
         }
 #pragma unroll
@@ -453,7 +477,9 @@ __global__ void __launch_bounds__(bwd_threads(GM),
             continue;
         }
         float2 wE[H], wO[H];  // this lane's weights of the unit's tensor (first / second elements)
-        IO::weights(wsm + tt * D, sub, wE, wO);
+#pragma unroll
+        for (int h = 0; h < H; ++h) wE[h] = wO[h] = make_float2(0.f, 0.f);
+        if (active) IO::weights(wsm + tt * dd, sub, wE, wO, dims);
         const uint8_t* gs = xs + grad_at;
         uint8_t* out_base = a.dx_out[tt][rec.t_q >> 3] + rec.seq_row0 * a.tok_stride;
         const float4* table = reinterpret_cast<const float4*>(smem + L.tables + s * L.table_bytes);
@@ -497,7 +523,7 @@ __global__ void __launch_bounds__(bwd_threads(GM),
                     ok[u] = gg < a.W && ii < ntok;
                     tk_[u] = ii;
                     hh_[u] = gg * gm_n + hh;  // head on the sequence side
-                    off = (gg * gm_R + ii) * gm_run + hh * (D * 2);
+                    off = (gg * gm_R + ii) * gm_run + hh * (dd * 2);
                 } else {
                     ok[u] = base + o < rows;
                     int hh = base_head + o, tk = base_tok;
@@ -507,13 +533,13 @@ __global__ void __launch_bounds__(bwd_threads(GM),
                     }
                     tk_[u] = tk;
                     hh_[u] = hh;
-                    off = (base + o) * (D * 2);  // row (tk, hh) of the unit in the stage
+                    off = (base + o) * (dd * 2);  // row (tk, hh) of the unit in the stage
                 }
                 Words g = {};
                 xr[u] = Words{};
-                if (ok[u]) {
-                    xr[u] = IO::load(xs + off, sub);
-                    g = IO::load(gs + off, sub);
+                if (ok[u] && active) {
+                    xr[u] = IO::load(xs + off, sub, dims);
+                    g = IO::load(gs + off, sub, dims);
                 }
                 float2 acc_ss = make_float2(0.f, 0.f), acc_dp = make_float2(0.f, 0.f);
 #pragma unroll
@@ -522,7 +548,8 @@ __global__ void __launch_bounds__(bwd_threads(GM),
                     IO::unpack(xr[u], h, xE, xO);
                     IO::unpack(g, h, gE, gO);
                     // (c_j, c_j+1, s_j, s_j+1) for j = P sub + 2 h
-                    const float4 cs = table[IO::table_entry(tk_[u], h, sub)];
+                    const float4 cs = active ? table[IO::table_entry(tk_[u], h, sub, dims)]
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
                     const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
                     const float2 ns2 = make_float2(-cs.z, -cs.w);
                     // u = R^T gy: (c g_e + s g_o, c g_o - s g_e)
@@ -536,17 +563,10 @@ __global__ void __launch_bounds__(bwd_threads(GM),
                 ss[u] = acc_ss.x + acc_ss.y;
                 dp[u] = acc_dp.x + acc_dp.y;
             }
-#pragma unroll
-            for (int sh = G / 2; sh > 0; sh >>= 1) {
-#pragma unroll
-                for (int u = 0; u < ILP; ++u) {
-                    ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], sh);
-                    dp[u] += __shfl_xor_sync(0xffffffffu, dp[u], sh);
-                }
-            }
+            row_sums<D, 2>(ss, dp, G, GP, sub, group);
 #pragma unroll
             for (int u = 0; u < ILP; ++u) {
-                if (!ok[u]) continue;
+                if (!ok[u] || !active) continue;
                 const float rr = rsqrtf(ss[u] * inv_d + a.eps);
                 const float kk = rr * rr * rr * dp[u] * inv_d;
                 const float2 r2 = make_float2(rr, rr), nk2 = make_float2(-kk, -kk);
@@ -561,8 +581,8 @@ __global__ void __launch_bounds__(bwd_threads(GM),
                     aO[h] = __ffma2_rn(uO[u][h], __fmul2_rn(xO, r2), aO[h]);
                 }
                 // straight to the sequence side: row (token, head) of this unit's dx
-                IO::store_global(out_base + int64_t(tk_[u]) * a.tok_stride + hh_[u] * (D * 2), sub,
-                                 IO::pack(dxE, dxO));
+                IO::store_global(out_base + int64_t(tk_[u]) * a.tok_stride + hh_[u] * (dd * 2), sub,
+                                 IO::pack(dxE, dxO), dims);
             }
             if constexpr (GM) {
                 bh += PER_STEP;
@@ -591,10 +611,10 @@ __global__ void __launch_bounds__(bwd_threads(GM),
     // the CTA's dw sums, over its consumer warps in a fixed order, into its slot
     asm volatile("bar.sync %0, %1;" ::"r"(kBwdConsumerBarrier), "r"(kNW * 32) : "memory");
     const int ct = threadIdx.x - kBwdFirstConsumer * 32;
-    float* slot_out = a.dw_part + size_t(blockIdx.x) * (2 * D);
-    for (int j = ct; j < 2 * D; j += kNW * 32) {
+    float* slot_out = a.dw_part + size_t(blockIdx.x) * (2 * dd);
+    for (int j = ct; j < 2 * dd; j += kNW * 32) {
         float sum = 0.0f;
-        for (int w = 0; w < kNW; ++w) sum += red[w * 2 * D + j];
+        for (int w = 0; w < kNW * RG; ++w) sum += red[w * 2 * dd + j];
         slot_out[j] = sum;
     }
 }
@@ -648,7 +668,8 @@ void fused_bwd_geometry(const Plan& p, bool group_major, int64_t* tokens_per_uni
             const int64_t half = (R * row + 127) / 128 * 128;  // input box, then gradient rows
             if (2 * half >= (1 << 20)) continue;
             const BwdSmem m = bwd_smem_layout(int(p.d), int(R), ULY_BWD_GM_STAGES,
-                                              uint32_t(2 * half), kBwdNWGm);
+                                              uint32_t(2 * half),
+                                              kBwdNWGm * bwd_dw_rows_per_warp(int(p.d)));
             if (m.total <= kSmemPerCtaMax) {
                 *tokens_per_unit = R;
                 *stages = ULY_BWD_GM_STAGES;
@@ -670,7 +691,8 @@ void fused_bwd_geometry(const Plan& p, bool group_major, int64_t* tokens_per_uni
             const int64_t sb = T * tok_bytes;
             if (sb >= (1 << 20)) continue;  // an mbarrier counts fewer than 2^20 bytes
             for (int K = stages_max; K >= 2; --K) {
-                const BwdSmem m = bwd_smem_layout(int(p.d), int(T), K, uint32_t(sb), kBwdNW);
+                const BwdSmem m = bwd_smem_layout(int(p.d), int(T), K, uint32_t(sb),
+                                                  kBwdNW * bwd_dw_rows_per_warp(int(p.d)));
                 if (m.total <= budget && m.total <= kSmemPerCtaMax) {
                     *tokens_per_unit = T;
                     *stages = K;
@@ -683,24 +705,21 @@ void fused_bwd_geometry(const Plan& p, bool group_major, int64_t* tokens_per_uni
     }
 }
 
-// per device: the kernel variants whose shared-memory limit has been raised (any host thread)
-static std::atomic<unsigned long long> g_bwd_smem_set[64];
-
 template <int D, bool F16, bool HALF, bool GM>
 static cudaError_t bwd_launch_d(const FusedBwdArgs& a, cudaStream_t stream, int device, int grid)
 {
-    constexpr int dbit = D == 8 ? 0 : D == 16 ? 1 : D == 32 ? 2 : D == 64 ? 3 : D == 128 ? 4 : 5;
-    constexpr unsigned long long bit =
-        1ull << (dbit * 8 + (F16 ? 4 : 0) + (HALF ? 2 : 0) + (GM ? 1 : 0));
-    if (device >= 0 && device < 64 && !(g_bwd_smem_set[device].load() & bit)) {
+    static std::atomic<unsigned long long> raised{0};  // devices with this variant's limit raised
+    const unsigned long long bit = device >= 0 && device < 64 ? 1ull << device : 0;
+    if (bit && !(raised.load() & bit)) {
         cudaError_t e = cudaFuncSetAttribute(fused_qk_bwd_kernel<D, F16, HALF, GM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemPerCtaMax);
         if (e != cudaSuccess) return e;
-        g_bwd_smem_set[device].fetch_or(bit);
+        raised.fetch_or(bit);
     }
     const BwdSmem m =
-        bwd_smem_layout(a.d, a.tokens_per_unit, a.stages, a.stage_bytes, bwd_warps(GM));
+        bwd_smem_layout(a.d, a.tokens_per_unit, a.stages, a.stage_bytes,
+                        bwd_warps(GM) * bwd_dw_rows_per_warp(a.d));
     fused_qk_bwd_kernel<D, F16, HALF, GM><<<grid, bwd_threads(GM), m.total, stream>>>(a);
     return cudaGetLastError();
 }
@@ -747,7 +766,17 @@ cudaError_t fused_bwd_launch(const FusedBwdArgs& a, float* dw, bool accumulate, 
             case 64: e = bwd_launch_variant<64>(a, stream, device, int(grid)); break;
             case 128: e = bwd_launch_variant<128>(a, stream, device, int(grid)); break;
             case 256: e = bwd_launch_variant<256>(a, stream, device, int(grid)); break;
-            default: return cudaErrorInvalidValue;
+            default:  // any other multiple of 8 up to 256: a run-time row layout
+                if (a.d % 8 != 0 || a.d < 8 || a.d > kMaxFusedD) return cudaErrorInvalidValue;
+                switch (rt_layout_for(a.d)) {
+                    case 0: e = bwd_launch_variant<0>(a, stream, device, int(grid)); break;
+                    case kRtWide: e = bwd_launch_variant<kRtWide>(a, stream, device, int(grid)); break;
+                    case kRtPow2: e = bwd_launch_variant<kRtPow2>(a, stream, device, int(grid)); break;
+                    default:
+                        e = bwd_launch_variant<kRtPow2 | kRtWide>(a, stream, device, int(grid));
+                        break;
+                }
+                break;
         }
         if (e != cudaSuccess) return e;
     } else if (accumulate) {

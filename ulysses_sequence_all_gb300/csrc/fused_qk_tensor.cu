@@ -90,6 +90,7 @@ struct FusedTensorArgs {
     int64_t plain_units;  // plain_units each
     int32_t n_plain;
     int32_t W, n;         // ranks; heads per rank (every rank the same)
+    int32_t d;            // head dimension
     uint32_t run;         // n * d * elem_size: bytes of one rank's part of a row
     uint32_t box_bytes;   // R * W * run: one tensor's box
     uint32_t box_stride;  // bytes from a stage's q box to its k box (a multiple of 128)
@@ -165,21 +166,28 @@ __device__ __forceinline__ bool ft_wait(uint64_t* bar, uint32_t parity)
     return mbar_wait_bounded_hint<10000>(bar, parity);
 }
 
+// D: head dimension, a power of two, or below 8 for a.d with one of the run-time row layouts of
+// fused_row.cuh (rt_layout_for: any multiple of 8 up to 256); F16: fp16 elements (else bf16);
+// HALF_PAIRS: rotate-half RoPE pairs.
 template <int D, bool F16, bool HALF_PAIRS>
 __global__ void __launch_bounds__(kFtThreads, ULY_FT_CTAS_PER_SM)
     fused_qk_tensor_kernel(const __grid_constant__ FusedTensorArgs a)
 {
     using IO = RowIO<F16, HALF_PAIRS, D, true>;
-    constexpr int G = IO::G;
+    const int dd = rt_layout(D) ? a.d : D;  // head dimension
+    const RowDims dims = IO::dims(dd);
+    const int G = dims.g;        // lanes per head row
     constexpr int H = IO::H;
-    constexpr int HALF = D / 2;
-    constexpr int GPW = 32 / G;  // head rows per warp per slot
+    const int HALF = dd / 2;
+    // lanes from a row's first to the next row's: G, or G rounded up to a power of two
+    const int GP = !rt_layout(D) ? G : rt_pow2(D) ? row_lane_stride(G) : G;
+    const int GPW = 32 / GP;  // head rows per warp per slot
     constexpr int ILP = ULY_FT_ILP;
-    constexpr int PER_STEP = GPW * ILP;
+    const int PER_STEP = GPW * ILP;
     constexpr int K = kFtStages;
     constexpr int NW = kFtConsumerWarps;
     extern __shared__ __align__(1024) uint8_t smem[];
-    const FtSmem L = ft_smem_layout(D, a.table_bytes, a.stage_bytes);
+    const FtSmem L = ft_smem_layout(dd, a.table_bytes, a.stage_bytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // both boxes landed
     uint64_t* computed = full + K;                       // consumers done with the stage
     uint64_t* empty = computed + K;                      // the stores have read the stage
@@ -281,12 +289,14 @@ __global__ void __launch_bounds__(kFtThreads, ULY_FT_CTAS_PER_SM)
     const int cw = warp - 2;
     const int which = cw >= HALF_NW;       // 0: q, 1: k (uniform per warp)
     const int cwi = cw - which * HALF_NW;  // rank among the warps of this tensor
-    const int sub = lane % G;              // which pairs of the row this lane holds
-    const int group = lane / G;            // which head row of the warp slot
+    const int group = lane / GP;       // which head row of the warp slot
+    const int sub = lane - group * GP;  // which pairs of the row this lane holds
+    const bool active = sub < G && group < GPW;  // lanes holding no row's pairs (run-time d)
     float2 wE[H], wO[H], wOn[H];
-    IO::weights(a.rms_w + which * D, sub, wE, wO);
+    for (int h = 0; h < H; ++h) wE[h] = wO[h] = make_float2(0.f, 0.f);
+    if (active) IO::weights(a.rms_w + which * dd, sub, wE, wO, dims);
     for (int h = 0; h < H; ++h) wOn[h] = make_float2(-wO[h].x, -wO[h].y);
-    const float inv_d = 1.0f / float(D);
+    const float inv_d = 1.0f / float(dd);
     const int ctid = cw * 32 + lane;  // rank among the consumer threads
     const int nr = a.n, R = int(a.R), W = a.W;
     const int run = int(a.run);
@@ -319,7 +329,7 @@ __global__ void __launch_bounds__(kFtThreads, ULY_FT_CTAS_PER_SM)
                 const int tok = e / HALF, jj = e - tok * HALF;
                 const float2 tj = turns[jj];
                 const float2 cs = rope_cos_sin(p0 + float(tok), tj.x, tj.y);
-                const int at = IO::table_at(tok, jj);
+                const int at = IO::table_at(tok, jj, dims);
                 table[at] = cs.x;
                 table[at + 2] = cs.y;
             }
@@ -354,10 +364,10 @@ __global__ void __launch_bounds__(kFtThreads, ULY_FT_CTAS_PER_SM)
                     }
                 }
                 ok[u] = gg < W && ii < nrows;
-                slot[u] = rows_base + (gg * R + ii) * run + hh * (D * 2);
+                slot[u] = rows_base + (gg * R + ii) * run + hh * (dd * 2);
                 tok[u] = ii;
                 typename IO::Words x = {};
-                if (ok[u]) x = IO::load(slot[u], sub);
+                if (ok[u] && active) x = IO::load(slot[u], sub, dims);
                 float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
@@ -367,20 +377,16 @@ __global__ void __launch_bounds__(kFtThreads, ULY_FT_CTAS_PER_SM)
                 }
                 ss[u] = acc.x + acc.y;
             }
-#pragma unroll
-            for (int off = G / 2; off > 0; off >>= 1) {
-#pragma unroll
-                for (int u = 0; u < ILP; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], off);
-            }
+            row_sums<D, 1>(ss, ss, G, GP, sub, group);
 #pragma unroll
             for (int u = 0; u < ILP; ++u) {
-                if (!ok[u]) continue;
+                if (!ok[u] || !active) continue;
                 const float inv = rsqrtf(ss[u] * inv_d + a.eps);
                 const float2 inv2 = make_float2(inv, inv);
                 float2 oEs[H], oOs[H];
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
-                    const float4 cs = table[IO::table_entry(tok[u], h, sub)];
+                    const float4 cs = table[IO::table_entry(tok[u], h, sub, dims)];
                     const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
                     const float2 A = __fmul2_rn(vE[u][h], wE[h]);
                     const float2 Bp = __fmul2_rn(vO[u][h], wO[h]);
@@ -388,7 +394,7 @@ __global__ void __launch_bounds__(kFtThreads, ULY_FT_CTAS_PER_SM)
                     oEs[h] = __fmul2_rn(__ffma2_rn(Bn, s2, __fmul2_rn(A, c2)), inv2);
                     oOs[h] = __fmul2_rn(__ffma2_rn(A, s2, __fmul2_rn(Bp, c2)), inv2);
                 }
-                IO::store(slot[u], sub, IO::pack(oEs, oOs));  // in place
+                IO::store(slot[u], sub, IO::pack(oEs, oOs), dims);  // in place
             }
             bh += PER_STEP;
             while (bh >= nr) {
@@ -423,24 +429,25 @@ bool fused_tensor_fits(const Plan& p)
 // the token units' 0.83-0.98, and with longer rows (fewer than 3 rows per box) below them.
 bool fused_tensor_preferred(const Plan& p)
 {
+    // head dimensions that are not powers of two (the run-time row layouts): the token units
+    // measured as fast or faster (d = 72, 80, 96, 120 at 75,600 tokens: 0.67-0.72 against
+    // 0.48-0.72 of the copy peak)
+    if ((p.d & (p.d - 1)) != 0) return false;
     return fused_tensor_fits(p) && p.N * p.d * p.e <= 10240;
 }
-
-// per device: the kernel variants whose shared-memory limit has been raised (any host thread)
-static std::atomic<unsigned> g_ft_smem_set[64];
 
 template <int D, bool F16, bool HALF>
 static cudaError_t ft_launch_d(const FusedTensorArgs& a, int smem, cudaStream_t stream, int device,
                                int grid)
 {
-    constexpr int dbit = D == 8 ? 0 : D == 16 ? 1 : D == 32 ? 2 : D == 64 ? 3 : D == 128 ? 4 : 5;
-    constexpr unsigned bit = 1u << (dbit * 4 + (F16 ? 2 : 0) + (HALF ? 1 : 0));
-    if (device >= 0 && device < 64 && !(g_ft_smem_set[device].load() & bit)) {
+    static std::atomic<unsigned long long> raised{0};  // devices with this variant's limit raised
+    const unsigned long long bit = device >= 0 && device < 64 ? 1ull << device : 0;
+    if (bit && !(raised.load() & bit)) {
         cudaError_t e = cudaFuncSetAttribute(fused_qk_tensor_kernel<D, F16, HALF>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemPerCtaMax);
         if (e != cudaSuccess) return e;
-        g_ft_smem_set[device].fetch_or(bit);
+        raised.fetch_or(bit);
     }
     fused_qk_tensor_kernel<D, F16, HALF><<<grid, kFtThreads, smem, stream>>>(a);
     return cudaGetLastError();
@@ -487,6 +494,7 @@ cudaError_t fused_tensor_launch(const Plan& p, const FusedArgs& f, const ChunkRo
     const int smem = ft_smem_layout(int(p.d), a.table_bytes, a.stage_bytes).total;
     a.W = W;
     a.n = int32_t(p.n[0]);
+    a.d = int32_t(p.d);
     a.run = uint32_t(run);
     a.S = p.S;
     a.rms_w = f.rms_w;
@@ -544,7 +552,18 @@ cudaError_t fused_tensor_launch(const Plan& p, const FusedArgs& f, const ChunkRo
         case 64: return ft_launch_variant<64>(a, f16, half, smem, stream, device, int(grid));
         case 128: return ft_launch_variant<128>(a, f16, half, smem, stream, device, int(grid));
         case 256: return ft_launch_variant<256>(a, f16, half, smem, stream, device, int(grid));
-        default: return cudaErrorInvalidValue;
+        default:  // any other multiple of 8 up to 256: a run-time row layout
+            if (p.d % 8 != 0 || p.d < 8 || p.d > kMaxFusedD) return cudaErrorInvalidValue;
+            switch (rt_layout_for(int(p.d))) {
+                case 0: return ft_launch_variant<0>(a, f16, half, smem, stream, device, int(grid));
+                case kRtWide:
+                    return ft_launch_variant<kRtWide>(a, f16, half, smem, stream, device, int(grid));
+                case kRtPow2:
+                    return ft_launch_variant<kRtPow2>(a, f16, half, smem, stream, device, int(grid));
+                default:
+                    return ft_launch_variant<kRtPow2 | kRtWide>(a, f16, half, smem, stream, device,
+                                                                int(grid));
+            }
     }
 }
 
