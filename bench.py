@@ -950,6 +950,11 @@ def run_configs(args):
                     "adjacent"),
                    (wl.Workload("wan720p_fp16", 8, 1, (9450,) * 8, (5,) * 8, 128, "float16", seed=1),
                     "half")]
+    # head dimensions beside 128 at the Wan-720p length (W=8, 75,600 tokens): DiT-XL's 16 heads of
+    # 72, and 64, 80, 96, 120 (the non-powers of two take the run-time row layouts)
+    fused_cfgs += [(wl.Workload(f"s75600_N{8 * n}_d{d}", 8, 1, (9450,) * 8, (n,) * 8, d, "bfloat16",
+                                seed=1), "adjacent")
+                   for n, d in ((2, 72), (2, 64), (5, 80), (3, 96), (2, 120))]
     for cfg, pairs in fused_cfgs:
         plan = B.ulysses_plan(cfg.W, cfg.b, cfg.seq_splits, cfg.head_splits, cfg.d, cfg.dtype)
         if pairs == "half":
