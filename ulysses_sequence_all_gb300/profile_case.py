@@ -18,7 +18,11 @@ from . import workloads as wl
 
 # half the Wan sequence (37,800 tokens; 387 MB per tensor set) for captures with many passes
 WAN_HALF = wl.Workload("wan720p_half", 8, 1, (4725,) * 8, (5,) * 8, 128, "bfloat16", seed=1)
-WORKLOADS = {"wan": wl.WAN, "wan_half": WAN_HALF, "long": wl.LONG_QKV, "tiny": wl.TINY}
+# the Wan-720p length with 16 heads of 64 or of 72 (DiT-XL's heads; a run-time row layout)
+N16_D64 = wl.Workload("s75600_N16_d64", 8, 1, (9450,) * 8, (2,) * 8, 64, "bfloat16", seed=1)
+N16_D72 = wl.Workload("s75600_N16_d72", 8, 1, (9450,) * 8, (2,) * 8, 72, "bfloat16", seed=1)
+WORKLOADS = {"wan": wl.WAN, "wan_half": WAN_HALF, "long": wl.LONG_QKV, "tiny": wl.TINY,
+             "n16_d64": N16_D64, "n16_d72": N16_D72}
 ENGINES = {"auto": B.ULY_ENGINE_AUTO, "tma": B.ULY_ENGINE_TMA, "vec": B.ULY_ENGINE_VEC,
            "tensor": B.ULY_ENGINE_TENSOR}
 
