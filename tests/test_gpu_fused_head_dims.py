@@ -142,14 +142,16 @@ PACKED = [
 ]
 
 
+@pytest.mark.parametrize("engine", list(ENGINES))
 @pytest.mark.parametrize("case", PACKED, ids=[f"p{c[0][4]}" for c in PACKED])
-def test_packed_head_dims(oracle, case):
-    """The packed call: q and k planes against the oracle's packed form, the others byte-exact."""
+def test_packed_head_dims(oracle, case, engine):
+    """The packed call with each kernel: q and k planes against the oracle's packed form, the
+    others byte-exact."""
     g, planes, qp, kp, extra = case
     W, b, seq, heads, d = g
     xs, pitch = _packed_inputs(g, planes, extra, seed=sum(seq) + planes + d)
     w = wl.rms_weights(d, seed=planes + d).cuda()
-    outs = run_packed(g, planes, qp, kp, xs, pitch, w)
+    outs = run_packed(g, planes, qp, kp, xs, pitch, w, engine=ENGINES[engine])
     wn = w.cpu().numpy().astype(np.float64)
     qo, ko, plain = oracle.packed_fused([host_raw(x) for x in xs], seq, heads, d, planes, qp, kp,
                                         pitch, wn[0], wn[1], EPS, THETA)
@@ -161,10 +163,11 @@ def test_packed_head_dims(oracle, case):
                 assert np.array_equal(host_raw(outs[c][r]), plain[c][r]), f"{case} plane {c} rank {r}"
 
 
+@pytest.mark.parametrize("engine", list(ENGINES))
 @pytest.mark.parametrize("case", PACKED, ids=[f"pb{c[0][4]}" for c in PACKED])
-def test_packed_backward_head_dims(oracle, case):
-    """The packed backward: the q and k planes' dx within tolerance, the others byte-exact, a
-    token's extra columns untouched, and dw."""
+def test_packed_backward_head_dims(oracle, case, engine):
+    """The packed backward with each kernel: the q and k planes' dx within tolerance, the others
+    byte-exact, a token's extra columns untouched, and dw."""
     from gpu_util import FILL
     g, planes, qp, kp, extra = case
     W, b, seq, heads, d = g
@@ -176,6 +179,9 @@ def test_packed_backward_head_dims(oracle, case):
              for _ in range(planes)]
     w = wl.rms_weights(d, seed=planes + 3 + d).cuda()
     plan = B.ulysses_plan(*g, "bfloat16")
+    B.ulysses_plan_set_fused_engine(plan, ENGINES[engine])
+    want = ENGINES[engine] if _fits_row_blocks(g) else B.ULY_ENGINE_TMA
+    assert B.ulysses_plan_fused_backward_kernel(plan) == want
     dpk = GuardedOutputs([(b, s, pitch) for s in seq], torch.bfloat16)
     dwo = GuardedOutputs([(2, d)], torch.float32)
     ws = torch.empty(B.ulysses_qk_fused_backward_workspace(plan), dtype=torch.uint8, device="cuda")
