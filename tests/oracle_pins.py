@@ -236,7 +236,7 @@ def _freq(theta, j, d):
 
 def pin_rmsnorm_vs_torch(orc, quick=False):
     rng = np.random.default_rng(21)
-    for d in (2, 8, 64, 128):
+    for d in (2, 8, 24, 64, 72, 128):
         for eps in (1e-6, 1e-2, 0.0):
             x = rng.standard_normal(d) * rng.uniform(0.01, 10)
             w = 1.0 + 0.1 * rng.standard_normal(d)
@@ -248,7 +248,7 @@ def pin_rmsnorm_vs_torch(orc, quick=False):
 def pin_rope_vs_complex(orc, quick=False):
     """Adjacent pairs as complex numbers, multiplied by exp(i * p * theta^(-2j/d))."""
     rng = np.random.default_rng(22)
-    for d in (2, 8, 128):
+    for d in (2, 8, 24, 72, 128):
         for p in (0, 1, 7, 9450, 75599, 249999):
             y = rng.standard_normal(d)
             z = torch.view_as_complex(torch.from_numpy(y.copy()).view(d // 2, 2))
@@ -476,7 +476,7 @@ def _torch_row_forward(x, w, eps, p, theta):
 def pin_fused_bwd_vs_autograd(orc, quick=False):
     """The row backward equals torch.autograd's gradients of the library-built forward."""
     rng = np.random.default_rng(28)
-    for d in (2, 8, 128):
+    for d in (2, 8, 72, 128):
         for p in (0, 3, 9450, 75599):
             for eps in (1e-6, 0.3):
                 x = torch.tensor(rng.standard_normal(d), dtype=torch.float64, requires_grad=True)
@@ -581,7 +581,7 @@ def pin_f16_encode(orc, quick=False):
 def pin_rope_half_vs_complex(orc, quick=False):
     """Rotate-half pairs (y_j, y_(j+d/2)) as complex numbers times exp(i p theta^(-2j/d))."""
     rng = np.random.default_rng(41)
-    for d in (2, 8, 128):
+    for d in (2, 8, 24, 72, 128):
         for p in (0, 1, 9450, 75599):
             y = rng.standard_normal(d)
             h = d // 2
@@ -596,7 +596,7 @@ def pin_rope_half_is_permuted_adjacent(orc, quick=False):
     """Rotate-half equals adjacent pairs on the interleaved row: (P y)_(2j) = y_j,
     (P y)_(2j+1) = y_(j+d/2), rope_half(y) = P^-1 rope(P y)."""
     rng = np.random.default_rng(42)
-    for d in (4, 64, 256):
+    for d in (4, 24, 64, 72, 256):
         h = d // 2
         perm = np.empty(d, dtype=np.int64)
         perm[0::2] = np.arange(h)
@@ -625,7 +625,7 @@ def pin_fused_row_variants(orc, quick=False):
     the pinned complex formulation, rotate-half via the rotate_half formula; bf16 and fp16
     decoding via torch's own bf16 and numpy's float16."""
     rng = np.random.default_rng(43)
-    for d in (8, 128):
+    for d in (8, 72, 128):
         for f16 in (0, 1):
             for half in (0, 1):
                 for p in (0, 5, 75599):
@@ -652,7 +652,8 @@ def pin_fused_var_whole_call(orc, quick=False):
     A; every variant equals mode 0 of the raw elements (pinned above) followed by the variant row
     at the destination row's sequence index."""
     rng = np.random.default_rng(44)
-    for W, b, seq, heads, d in [(2, 1, [3, 2], [2, 1], 8), (3, 2, [2, 0, 3], [1, 2, 1], 16)]:
+    for W, b, seq, heads, d in [(2, 1, [3, 2], [2, 1], 8), (3, 2, [2, 0, 3], [1, 2, 1], 16),
+                                (2, 1, [2, 3], [1, 2], 24)]:
         N, S = sum(heads), sum(seq)
         raw = [rng.integers(0, 1 << 16, (b, s, N, d)).astype(np.uint16) for s in seq]
         # keep the elements finite and moderate for both decodings
@@ -679,7 +680,7 @@ def pin_fused_bwd_variants(orc, quick=False):
     """Row backward of a variant: adjacent pairs bit-identical to the pinned row backward;
     rotate-half against torch.autograd of the rotate_half formula (fp64), x.grad and w.grad."""
     rng = np.random.default_rng(45)
-    for d in (2, 8, 128):
+    for d in (2, 8, 72, 128):
         for p in (0, 3, 75599):
             x, g = rng.standard_normal(d), rng.standard_normal(d)
             w = 1.0 + 0.1 * rng.standard_normal(d)
