@@ -274,3 +274,50 @@ def test_dit_xl_shape_full(oracle):
         for qq in range(W):
             check_all(dxs[t][qq], ref_dx[qq], 2.0 ** -8, 1e-4, f"dx t{t} q{qq}")
         check_dw(dw[t].cpu().numpy(), ref_dw, b * S * sum(heads), f"dw t{t}")
+
+
+def test_head_dim_72_host_buffers_and_autograd():
+    """The host-buffer form and the differentiable form at d = 72 (fp16, rotate-half pairs): the
+    host-buffer call returns the device call's bytes, and the autograd gradients are the direct
+    backward call's, bit for bit."""
+    from ulysses_sequence_all_gb300 import autograd as A
+    g = (4, 2, [40, 37, 0, 45], [3, 3, 3, 3], 72)
+    W, b, seq, heads, d = g
+    S = sum(seq)
+    (q, k), w = _inputs(g, 1, seed=191)
+    plan = _plan(g, 1, 1)
+    qo = [torch.empty((b, S, n, d), dtype=torch.float16, device="cuda") for n in heads]
+    ko = [torch.empty_like(x) for x in qo]
+    B.ulysses_a2a_4d_qk_fused(plan, q, k, qo, ko, w, EPS, THETA)
+    torch.cuda.synchronize()
+    hq = [x.cpu().pin_memory() for x in q]
+    hk = [x.cpu().pin_memory() for x in k]
+    hqo = [torch.empty(x.shape, dtype=torch.float16).pin_memory() for x in qo]
+    hko = [torch.empty(x.shape, dtype=torch.float16).pin_memory() for x in ko]
+    dq_in = [torch.empty_like(x) for x in q]
+    dk_in = [torch.empty_like(x) for x in k]
+    dqo = [torch.empty_like(x) for x in qo]
+    dko = [torch.empty_like(x) for x in ko]
+    B.ulysses_a2a_4d_qk_fused_host(plan, hq, hk, hqo, hko, dq_in, dk_in, dqo, dko, w, EPS, THETA)
+    torch.cuda.synchronize()
+    for x, y in zip(hqo + hko, qo + ko):
+        assert torch.equal(x.view(torch.int16), y.cpu().view(torch.int16))
+
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(192)
+    gq = [torch.randn(x.shape, generator=gen).half().cuda() for x in qo]
+    gk = [torch.randn(x.shape, generator=gen).half().cuda() for x in ko]
+    qr = [x.clone().requires_grad_() for x in q]
+    kr = [x.clone().requires_grad_() for x in k]
+    wr = w.clone().requires_grad_()
+    ao, bo = A.qk_fused(plan, qr, kr, wr, EPS, THETA)
+    torch.autograd.backward(ao + bo, gq + gk)
+    dq = [torch.empty_like(x) for x in q]
+    dk = [torch.empty_like(x) for x in k]
+    dw = torch.empty_like(w)
+    ws = torch.empty(B.ulysses_qk_fused_backward_workspace(plan), dtype=torch.uint8, device="cuda")
+    B.ulysses_a2a_4d_qk_fused_backward(plan, dq, dk, q, k, gq, gk, w, dw, EPS, THETA, ws)
+    torch.cuda.synchronize()
+    for x, y in zip(ao + bo + [t.grad for t in qr + kr], qo + ko + dq + dk):
+        assert torch.equal(x.detach().view(torch.int16), y.view(torch.int16))
+    assert torch.equal(wr.grad.view(torch.int32), dw.view(torch.int32))
