@@ -258,7 +258,7 @@ struct PackedIn {
 
 // Head dimensions of the fused calls: every multiple of 8 from 8 to 256 (a head row of 2-byte
 // elements is then a whole number of 16-byte words). Powers of two run kernels compiled for
-// their d; the others the token-unit kernels' run-time row layout.
+// their d; the others the same kernels with d read at run time (fused_row.cuh).
 bool fused_head_dim_ok(int64_t d) { return d >= 8 && d <= kMaxFusedD && d % 8 == 0; }
 
 // Checks of a fused call (no CUDA call) and its argument block, without the unit tables. Either
