@@ -483,14 +483,46 @@ cudaError_t fused_tensor_launch(const Plan& p, const FusedArgs& f, const ChunkRo
     if (a.R > 128) a.R = 128;  // a box holds at most 256 rows: 2R for the other planes
     if (a.R < 1) a.R = 1;
     auto up = [](int64_t x, int64_t m) { return (x + m - 1) / m * m; };
-    for (;; --a.R) {  // the largest block of rows whose stages fit one CTA's shared memory
-        a.box_bytes = uint32_t(a.R * row);
-        a.box_stride = uint32_t(up(a.box_bytes, 128));
-        a.stage_bytes = 2 * a.box_stride;
-        a.table_bytes = uint32_t(up(a.R * (p.d / 2) * 8, 128));
-        if (ft_smem_layout(int(p.d), a.table_bytes, a.stage_bytes).total <= kSmemPerCtaMax) break;
+    auto fits = [&](int64_t R) {  // R rows' stages fit one CTA's shared memory
+        const uint32_t box = uint32_t(up(R * row, 128));
+        const uint32_t table = uint32_t(up(R * (p.d / 2) * 8, 128));
+        return ft_smem_layout(int(p.d), table, 2 * box).total <= kSmemPerCtaMax;
+    };
+    while (!fits(a.R)) {  // the largest block of rows whose stages fit
         if (a.R == 1) return cudaErrorInvalidValue;
+        --a.R;
     }
+    // A unit's W R n head rows of a tensor are shared out in steps of one row per lane group
+    // over the tensor's consumer warps, so a unit takes as long as its busiest warp. Where the
+    // block above leaves the warps unevenly loaded, take a larger one (up to twice as many rows,
+    // still fitting) that evens them out: e.g. 40 heads of 64 at W = 8, 160 rows per box, give 2
+    // or 3 steps per warp; 6 rows give 240, 4 steps for every warp.
+    {
+        const bool compiled = (p.d & (p.d - 1)) == 0;
+        const int P = compiled ? (p.d >= 16 ? 8 : 4) : (p.d % 16 == 0 ? 8 : 4);
+        const int g = int(p.d / (2 * P));
+        const int per_step = (32 / (compiled ? g : row_lane_stride(g))) * ULY_FT_ILP;
+        const int64_t half_nw = kFtConsumerWarps / 2;
+        auto balance = [&](int64_t R) {
+            const int64_t rows_ = W * R * p.n[0];
+            const int64_t steps = (rows_ + per_step - 1) / per_step;
+            const int64_t busiest = (steps + half_nw - 1) / half_nw;
+            return double(rows_) / double(half_nw * busiest * per_step);
+        };
+        int64_t best = a.R;
+        double best_b = balance(a.R);
+        for (int64_t R = a.R + 1; R <= 2 * a.R && R <= 128 && fits(R); ++R) {
+            if (balance(R) > best_b + 0.05) {
+                best = R;
+                best_b = balance(R);
+            }
+        }
+        a.R = best;
+    }
+    a.box_bytes = uint32_t(a.R * row);
+    a.box_stride = uint32_t(up(a.box_bytes, 128));
+    a.stage_bytes = 2 * a.box_stride;
+    a.table_bytes = uint32_t(up(a.R * (p.d / 2) * 8, 128));
     const int smem = ft_smem_layout(int(p.d), a.table_bytes, a.stage_bytes).total;
     a.W = W;
     a.n = int32_t(p.n[0]);
